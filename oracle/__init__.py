@@ -1,0 +1,160 @@
+"""ctypes wrapper around the fp64 C oracle (``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__``'s
+smoke check and by the CPU-baseline leg of ``bench.py``.  The library in
+``speculative_decoding_verification_71_gb300`` never imports this package,
+and this package never imports the library.
+
+``build()`` compiles ``oracle.c`` with gcc (-O2, no fast-math, OpenMP) into
+``liboracle.so`` beside it.  ``verify(...)`` takes numpy arrays or CPU torch
+tensors with the same layout as the library's entry point and returns the
+outputs plus the diagnostics the parity tests use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+STATUS_OK = 0
+STATUS_BAD_DRAFT_LEN = 2
+STATUS_BAD_TOKEN = 3
+STATUS_NONFINITE = 4
+FLAG_ZERO_RESIDUAL = 256
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH, extra=()) -> str:
+    """Compile the oracle (or, for mutation tests, another source file)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-Wall", *extra, src, "-o", out + ".tmp", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def _bind(lib):
+    c = ctypes
+    P = c.c_void_p
+    lib.oracle_verify.restype = c.c_int
+    lib.oracle_verify.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, P, P, c.c_double,
+                                  P, P, P, P, P, P, P, P, P, P, P, c.c_int]
+    lib.oracle_row_lse.restype = c.c_double
+    lib.oracle_row_lse.argtypes = [c.c_int, c.c_int, P, c.c_double]
+    lib.oracle_row_probs.restype = None
+    lib.oracle_row_probs.argtypes = [c.c_int, c.c_int, P, c.c_double, P]
+    lib.oracle_logit_value.restype = c.c_double
+    lib.oracle_logit_value.argtypes = [P, c.c_int, c.c_longlong]
+    lib.oracle_num_threads.restype = c.c_int
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library.  ``path`` loads another
+    build, e.g. a mutant compiled by the tests."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        build()
+        _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _as_np(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu()
+            if x.dtype == torch.bfloat16:
+                return x.contiguous().view(torch.int16).numpy().view(np.uint16), 1
+            return x.contiguous().numpy(), (0 if x.dtype == torch.float32 else None)
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, 0
+    if x.dtype == np.uint16:  # raw bf16 bits
+        return x, 1
+    return x, None
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def verify(target, draft, tokens, draft_len, uniforms, T, nthreads=0, lib=None):
+    """Run the oracle on one batch.
+
+    target [B,k+1,V] and draft [B,k,V]: float32 arrays, uint16 arrays of
+    bf16 bits, or CPU/GPU torch tensors (fp32 or bf16).  Returns a dict with
+    out_tokens, out_len, status and the fp64 diagnostics.
+    """
+    lib = lib or load()
+    t, dt = _as_np(target)
+    d, dd = _as_np(draft)
+    if dt is None or dt != dd:
+        raise TypeError("target and draft must both be float32 or both be bfloat16")
+    B, k1, V = t.shape
+    k = k1 - 1
+    if d.shape != (B, k, V) and not (k == 0 and d.size == 0):
+        raise ValueError(f"draft shape {d.shape} != {(B, k, V)}")
+    tok = np.ascontiguousarray(_as_np(tokens)[0], dtype=np.int32).reshape(B, max(k, 0))
+    kl = np.ascontiguousarray(_as_np(draft_len)[0], dtype=np.int32).reshape(B)
+    u = np.ascontiguousarray(_as_np(uniforms)[0], dtype=np.float32).reshape(B, k + 1)
+    if not (T >= 0.0) or not np.isfinite(T):
+        raise ValueError("temperature must be finite and >= 0")
+    out_tokens = np.empty((B, k + 1), np.int32)
+    out_len = np.empty(B, np.int32)
+    lse_t = np.empty((B, k + 1))
+    lse_d = np.empty((B, max(k, 1)))
+    p_x = np.empty((B, max(k, 1)))
+    q_x = np.empty((B, max(k, 1)))
+    alpha = np.empty((B, max(k, 1)))
+    mass = np.empty(B)
+    atie = np.empty(B)
+    stie = np.empty(B)
+    status = np.empty(B, np.int32)
+    d_arr = d if d.size else np.zeros(1, t.dtype)
+    lib.oracle_verify(B, k, V, dt, _ptr(t), _ptr(d_arr), _ptr(tok), _ptr(kl), _ptr(u), float(T),
+                      _ptr(out_tokens), _ptr(out_len), _ptr(lse_t), _ptr(lse_d), _ptr(p_x),
+                      _ptr(q_x), _ptr(alpha), _ptr(mass), _ptr(atie), _ptr(stie), _ptr(status),
+                      int(nthreads))
+    return {
+        "out_tokens": out_tokens, "out_len": out_len, "status": status,
+        "lse_t": lse_t, "lse_d": lse_d[:, :k], "p_x": p_x[:, :k], "q_x": q_x[:, :k],
+        "alpha": alpha[:, :k], "resid_mass": mass, "accept_tie": atie, "sample_tie": stie,
+    }
+
+
+def row_lse(row, T, lib=None):
+    lib = lib or load()
+    r, dt = _as_np(row)
+    return lib.oracle_row_lse(r.size, dt, _ptr(r), float(T))
+
+
+def row_probs(row, T, lib=None):
+    lib = lib or load()
+    r, dt = _as_np(row)
+    p = np.empty(r.size)
+    lib.oracle_row_probs(r.size, dt, _ptr(r), float(T), _ptr(p))
+    return p
+
+
+def logit_values(arr, lib=None):
+    lib = lib or load()
+    a, dt = _as_np(arr)
+    flat = a.reshape(-1)
+    return np.array([lib.oracle_logit_value(_ptr(flat), dt, i) for i in range(flat.size)])
+
+
+def num_threads(lib=None):
+    return (lib or load()).oracle_num_threads()

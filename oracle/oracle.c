@@ -1,0 +1,362 @@
+/*
+ * fp64 CPU oracle for lossless speculative-sampling verification.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the verification computes.  It is compiled and called
+ * only by the tests, by the smoke check and by the benchmark's CPU-baseline
+ * leg; the library under speculative_decoding_verification_71_gb300/ never
+ * links, loads or calls it, and the two share no source.
+ *
+ * What it computes (one sequence b at a time, all arithmetic in double):
+ *   The verifier accepts or rejects each drafted token from the verifier's
+ *   probability distribution, so that the rollout keeps the target policy's
+ *   distribution ("Accelerating RL Post-Training Rollouts via
+ *   System-Integrated Speculative Decoding", §2 core mechanism: rejection
+ *   sampling).  It checks the drafts together and rewrites from the first
+ *   wrong token ("Online Draft Co-Training for Speculative Decoding in
+ *   Large-Scale, Long-Context RL Post-Training", the stenographer/proof-reader
+ *   analogy).  The pages do not spell the rule out; the reading used is the
+ *   standard speculative-sampling rule:
+ *     p_i = softmax(z^t_i / T), q_i = softmax(z^d_i / T)
+ *     accept draft i iff u_i < min(1, p_i(x_i) / q_i(x_i)); stop at the first
+ *     rejection a;
+ *     if a < k_b sample y from max(0, p_a - q_a) (normalised), else sample the
+ *     bonus token y from p_{k_b};
+ *     sampling is inverse CDF in ascending token id with the one sampling
+ *     uniform s = u_{b,k}: y = min{x : s * S < C(x)}, C the running sum of
+ *     the weights, S their total.
+ *   q(x) = 0 for a drafted token gives r = +inf when p(x) > 0 and r = 0 when
+ *   p(x) = 0.  T == 0 is greedy: accept iff x_i is the first argmax of p_i;
+ *   the emitted token is the first argmax of the decided target row.
+ *
+ * Status per sequence: 0 ok, 2 draft length outside [0,k], 3 drafted token
+ * outside [0,V), 4 NaN or +inf in a needed row or a needed row that is all
+ * -inf.  A sequence with a nonzero status emits nothing (out_len 0, tokens
+ * -1).  Bit 8 is set (status stays "ok") when the residual mass was exactly
+ * zero and the sample was taken from p_a instead.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_BAD_DRAFT_LEN 2
+#define ORC_BAD_TOKEN 3
+#define ORC_NONFINITE 4
+#define ORC_FLAG_ZERO_RESIDUAL 256
+
+/* One logit as a double: fp32 widened, or bf16 bits placed in the top half
+ * of an fp32 word and widened.  Both conversions are exact. */
+static double logit_value(const void *base, int dtype, size_t idx)
+{
+    if (dtype == 0)
+        return (double)((const float *)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static void load_row(const void *base, int dtype, size_t row, int V, double *out)
+{
+    size_t off = row * (size_t)V;
+    for (int x = 0; x < V; ++x)
+        out[x] = logit_value(base, dtype, off + (size_t)x);
+}
+
+/* A row may hold -inf (masked tokens) but no NaN or +inf, and not only -inf. */
+static int row_is_valid(const double *z, int V)
+{
+    int finite_seen = 0;
+    for (int x = 0; x < V; ++x) {
+        if (isnan(z[x]) || z[x] == INFINITY)
+            return 0;
+        if (z[x] != -INFINITY)
+            finite_seen = 1;
+    }
+    return finite_seen;
+}
+
+/* Row maximum m and L = log sum_x exp((z_x - m)/T), so that
+ * log-sum-exp(z/T) = m/T + L and p(x) = exp((z_x - m)/T - L). */
+static void row_stats(const double *z, int V, double T, double *m_out, double *L_out)
+{
+    double m = -INFINITY;
+    for (int x = 0; x < V; ++x)
+        if (z[x] > m)
+            m = z[x];
+    double s = 0.0;
+    for (int x = 0; x < V; ++x)
+        s += exp((z[x] - m) / T);
+    *m_out = m;
+    *L_out = log(s);
+}
+
+static double prob_of(double zx, double m, double L, double T)
+{
+    return exp((zx - m) / T - L);
+}
+
+static int first_argmax(const double *z, int V)
+{
+    int best = 0;
+    for (int x = 1; x < V; ++x)
+        if (z[x] > z[best])
+            best = x;
+    return best;
+}
+
+/* Inverse CDF over weights w[0..V): the smallest x with s*S < C(x); if
+ * rounding leaves no such x, the last x with w(x) > 0.  Also returns the
+ * distance of s, in units of C/S, to the two boundaries of the chosen x. */
+static int inverse_cdf(const double *w, int V, double S, double s, double *tie)
+{
+    double t = s * S, c = 0.0, c_prev = 0.0;
+    int y = -1;
+    for (int x = 0; x < V; ++x) {
+        c_prev = c;
+        c += w[x];
+        if (t < c) {
+            y = x;
+            break;
+        }
+    }
+    if (y < 0) {
+        for (int x = V - 1; x >= 0; --x)
+            if (w[x] > 0.0) {
+                y = x;
+                break;
+            }
+        c = 0.0;
+        for (int x = 0; x <= y; ++x)
+            c += w[x];
+        c_prev = c - w[y];
+    }
+    double d0 = fabs(s - c_prev / S), d1 = fabs(s - c / S);
+    *tie = d0 < d1 ? d0 : d1;
+    return y;
+}
+
+/*
+ * oracle_verify: see the file comment.  Shapes as in the library:
+ *   target [B,k+1,V], draft [B,k,V] (dtype 0 = fp32, 1 = bf16 bits),
+ *   tokens [B,k], draft_len [B], uniforms [B,k+1] (float32),
+ *   out_tokens [B,k+1] (-1 padded), out_len [B].
+ * Optional diagnostics (any may be NULL):
+ *   lse_t [B,k+1], lse_d [B,k]   log-sum-exp of z/T per needed row (NaN if
+ *                                not needed or T == 0)
+ *   p_x, q_x [B,k]               p_i(x_i), q_i(x_i)
+ *   alpha [B,k]                  min(1, p_i(x_i)/q_i(x_i)) for every draft
+ *                                (greedy: 1 if accepted else 0)
+ *   resid_mass [B]               S of the sampled weights
+ *   accept_tie [B]               min |u_i - alpha_i| over the tests that
+ *                                decided a (1 if none)
+ *   sample_tie [B]               distance of s to the chosen x's CDF bounds
+ *   status [B]
+ * nthreads <= 0 uses the OpenMP default.  Returns the number of sequences
+ * with a nonzero status (flags excluded).
+ */
+int oracle_verify(int B, int k, int V, int dtype,
+                  const void *target, const void *draft,
+                  const int32_t *tokens, const int32_t *draft_len,
+                  const float *uniforms, double T,
+                  int32_t *out_tokens, int32_t *out_len,
+                  double *lse_t, double *lse_d, double *p_x, double *q_x,
+                  double *alpha, double *resid_mass, double *accept_tie,
+                  double *sample_tie, int32_t *status, int nthreads)
+{
+    int nerr = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(+ : nerr)
+#endif
+    for (int b = 0; b < B; ++b) {
+        double *zt = (double *)malloc(sizeof(double) * (size_t)V);
+        double *zd = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+        double *mt = (double *)malloc(sizeof(double) * (size_t)(k + 1) * 2);
+        double *Lt = mt + (k + 1);
+        double *md = (double *)malloc(sizeof(double) * (size_t)(k + 1) * 2);
+        double *Ld = md + (k + 1);
+        int *amax_t = (int *)malloc(sizeof(int) * (size_t)(k + 1));
+        int st = ORC_OK;
+
+        for (int j = 0; j <= k; ++j)
+            out_tokens[(size_t)b * (k + 1) + j] = -1;
+        out_len[b] = 0;
+        for (int j = 0; j <= k; ++j) {
+            if (lse_t) lse_t[(size_t)b * (k + 1) + j] = NAN;
+            if (j < k) {
+                if (lse_d) lse_d[(size_t)b * k + j] = NAN;
+                if (p_x) p_x[(size_t)b * k + j] = NAN;
+                if (q_x) q_x[(size_t)b * k + j] = NAN;
+                if (alpha) alpha[(size_t)b * k + j] = NAN;
+            }
+        }
+        if (resid_mass) resid_mass[b] = NAN;
+        if (accept_tie) accept_tie[b] = 1.0;
+        if (sample_tie) sample_tie[b] = 1.0;
+
+        int kb = draft_len[b];
+        if (kb < 0 || kb > k)
+            st = ORC_BAD_DRAFT_LEN;
+        for (int i = 0; st == ORC_OK && i < kb; ++i) {
+            int x = tokens[(size_t)b * k + i];
+            if (x < 0 || x >= V)
+                st = ORC_BAD_TOKEN;
+        }
+        /* Row statistics of every needed row. */
+        for (int i = 0; st == ORC_OK && i <= kb; ++i) {
+            load_row(target, dtype, (size_t)b * (k + 1) + i, V, zt);
+            if (!row_is_valid(zt, V)) {
+                st = ORC_NONFINITE;
+                break;
+            }
+            amax_t[i] = first_argmax(zt, V);
+            if (T > 0.0) {
+                row_stats(zt, V, T, &mt[i], &Lt[i]);
+                if (lse_t) lse_t[(size_t)b * (k + 1) + i] = mt[i] / T + Lt[i];
+            }
+            if (i < kb) {
+                load_row(draft, dtype, (size_t)b * k + i, V, zd);
+                if (!row_is_valid(zd, V)) {
+                    st = ORC_NONFINITE;
+                    break;
+                }
+                if (T > 0.0) {
+                    row_stats(zd, V, T, &md[i], &Ld[i]);
+                    if (lse_d) lse_d[(size_t)b * k + i] = md[i] / T + Ld[i];
+                }
+            }
+        }
+        if (st != ORC_OK) {
+            if (status) status[b] = st;
+            nerr += 1;
+            free(zt); free(zd); free(w); free(mt); free(md); free(amax_t);
+            continue;
+        }
+
+        const float *u = uniforms + (size_t)b * (k + 1);
+        int a = kb;
+        double atie = 1.0;
+        if (T > 0.0) {
+            /* Acceptance test of every draft (diagnostics), first rejection a. */
+            int decided = 0;
+            for (int i = 0; i < kb; ++i) {
+                int x = tokens[(size_t)b * k + i];
+                double zt_x = logit_value(target, dtype, ((size_t)b * (k + 1) + i) * (size_t)V + x);
+                double zd_x = logit_value(draft, dtype, ((size_t)b * k + i) * (size_t)V + x);
+                double p = prob_of(zt_x, mt[i], Lt[i], T);
+                double q = prob_of(zd_x, md[i], Ld[i], T);
+                double r = (q == 0.0) ? (p > 0.0 ? INFINITY : 0.0) : p / q;
+                double al = r < 1.0 ? r : 1.0;
+                if (p_x) p_x[(size_t)b * k + i] = p;
+                if (q_x) q_x[(size_t)b * k + i] = q;
+                if (alpha) alpha[(size_t)b * k + i] = al;
+                if (!decided) {
+                    double d = fabs((double)u[i] - al);
+                    if (d < atie) atie = d;
+                    if (!((double)u[i] < al)) {
+                        a = i;
+                        decided = 1;
+                    }
+                }
+            }
+            /* Weights of the final draw: residual at a, or bonus row k_b. */
+            double S = 0.0;
+            int flags = 0;
+            load_row(target, dtype, (size_t)b * (k + 1) + a, V, zt);
+            if (a < kb) {
+                load_row(draft, dtype, (size_t)b * k + a, V, zd);
+                for (int x = 0; x < V; ++x) {
+                    double d = prob_of(zt[x], mt[a], Lt[a], T) - prob_of(zd[x], md[a], Ld[a], T);
+                    w[x] = d > 0.0 ? d : 0.0;
+                }
+            } else {
+                for (int x = 0; x < V; ++x)
+                    w[x] = prob_of(zt[x], mt[a], Lt[a], T);
+            }
+            for (int x = 0; x < V; ++x)
+                S += w[x];
+            if (S == 0.0) {
+                flags |= ORC_FLAG_ZERO_RESIDUAL;
+                for (int x = 0; x < V; ++x)
+                    w[x] = prob_of(zt[x], mt[a], Lt[a], T);
+                S = 0.0;
+                for (int x = 0; x < V; ++x)
+                    S += w[x];
+            }
+            double stie = 1.0;
+            int y = inverse_cdf(w, V, S, (double)u[k], &stie);
+            if (resid_mass) resid_mass[b] = S;
+            if (sample_tie) sample_tie[b] = stie;
+            if (accept_tie) accept_tie[b] = atie;
+            for (int i = 0; i < a; ++i)
+                out_tokens[(size_t)b * (k + 1) + i] = tokens[(size_t)b * k + i];
+            out_tokens[(size_t)b * (k + 1) + a] = y;
+            out_len[b] = a + 1;
+            if (status) status[b] = flags;
+        } else {
+            /* Greedy: accept iff the draft is the first argmax of p_i. */
+            for (int i = 0; i < kb; ++i) {
+                int x = tokens[(size_t)b * k + i];
+                int ok = (x == amax_t[i]);
+                if (alpha) alpha[(size_t)b * k + i] = ok ? 1.0 : 0.0;
+                if (!ok && a == kb)
+                    a = i;
+            }
+            for (int i = 0; i < a; ++i)
+                out_tokens[(size_t)b * (k + 1) + i] = tokens[(size_t)b * k + i];
+            out_tokens[(size_t)b * (k + 1) + a] = amax_t[a];
+            out_len[b] = a + 1;
+            if (status) status[b] = ORC_OK;
+        }
+        free(zt); free(zd); free(w); free(mt); free(md); free(amax_t);
+    }
+    return nerr;
+}
+
+/* Row maximum and L (as in row_stats) of one row, for checking the
+ * log-sum-exp against a library routine.  Returns m/T + L. */
+double oracle_row_lse(int V, int dtype, const void *row, double T)
+{
+    double *z = (double *)calloc((size_t)V, sizeof(double));
+    load_row(row, dtype, 0, V, z);
+    double m, L;
+    row_stats(z, V, T, &m, &L);
+    free(z);
+    return m / T + L;
+}
+
+/* p(x) = softmax(z/T)(x) for every x of one row. */
+void oracle_row_probs(int V, int dtype, const void *row, double T, double *p)
+{
+    double *z = (double *)calloc((size_t)V, sizeof(double));
+    load_row(row, dtype, 0, V, z);
+    double m, L;
+    row_stats(z, V, T, &m, &L);
+    for (int x = 0; x < V; ++x)
+        p[x] = prob_of(z[x], m, L, T);
+    free(z);
+}
+
+/* Widening of one logit (exposed so that the exact bf16/fp32 conversion can
+ * be checked against the framework's own conversion). */
+double oracle_logit_value(const void *base, int dtype, long long idx)
+{
+    return logit_value(base, dtype, (size_t)idx);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
