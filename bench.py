@@ -1,0 +1,443 @@
+"""Benchmark: speculative-sampling verification on one GB300 (or N replicas).
+
+A step is one spec_verify call (the whole hot path: row maxima and
+log-sum-exp, acceptance test and first-rejection scan, residual/bonus draw,
+output compaction) over one batch of synthetic rollout-shaped logits.  The
+default workload is the ragged batch: B=256 sequences, per-sequence draft
+length k_b uniform in {0,1,2,3} (0 = speculation off), V=128256, bf16,
+T=1.  Inputs are resident in HBM before timing; four copies of the batch
+rotate so that no step finds its inputs in L2.
+
+metric: verified positions per second (sum over sequences of k_b + 1 target
+rows per call), with the achieved HBM bandwidth of the algorithmic bytes
+(every needed logit row read once, plus the small inputs and the outputs).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Multi-GPU (torchrun): every rank verifies its own batch (weak scaling, no
+data-path collective); the timed region is bracketed by barriers and the
+slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "spec_verify verified positions/s and HBM GB/s (fraction of ~8 TB/s), 1 GB300"
+UNIT = "positions/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_NAME = "verify_kernel"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="ragged")
+    ap.add_argument("--rotate", type=int, default=4, help="input copies rotated between steps")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cluster-size", type=int, default=0)
+    ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_71_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch of the verify kernel from the committed ncu
+    summary for this workload, if that summary was taken on the current
+    kernel source (its 'source_hash' line matches); else None."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sv_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle leg (also the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(w, seconds, seed_offset=0):
+    """Time the oracle, as it stands, on a bounded sample of the workload
+    (generated on the host) sized to take about `seconds`."""
+    import torch
+
+    import oracle
+    from workloads import make_inputs
+
+    lib = oracle.load()
+    threads = oracle.num_threads(lib)
+    probe = make_inputs(w, device="cpu", B=max(2, threads))
+    t0 = time.perf_counter()
+    r = oracle.verify(probe["target"], probe["draft"], probe["tokens"], probe["draft_len"],
+                      probe["uniforms"], probe["T"], lib=lib)
+    dt = time.perf_counter() - t0
+    per_seq = dt / probe["target"].shape[0] * threads
+    n = int(max(threads, min(w.B * 64, seconds * threads / max(per_seq, 1e-9))))
+    inp = make_inputs(w, device="cpu", B=n)
+    kb = inp["draft_len"].numpy()
+    t0 = time.perf_counter()
+    r = oracle.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"],
+                      inp["T"], lib=lib)
+    dt = time.perf_counter() - t0
+    positions = int(np.sum(kb + 1))
+    del torch
+    return {"positions": positions, "seconds": dt, "sequences": n, "threads": threads,
+            "mean_emitted": float(np.mean(r["out_len"]))}
+
+
+def reference_arm(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from workloads import algorithmic_bytes, make_inputs
+
+    lib = oracle.load()
+    threads = oracle.num_threads(lib)
+    # size each step so that the whole run stays within about two minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    probe = make_inputs(w, device="cpu", B=max(1, threads))
+    t0 = time.perf_counter()
+    oracle.verify(probe["target"], probe["draft"], probe["tokens"], probe["draft_len"],
+                  probe["uniforms"], probe["T"], lib=lib)
+    per_batch = time.perf_counter() - t0
+    n = max(1, int(threads * budget / max(per_batch, 1e-9)))
+    n = min(n, w.B)
+    inp = make_inputs(w, device="cpu", B=n)
+    kb = inp["draft_len"].numpy()
+    positions = int(np.sum(kb + 1))
+    nbytes = algorithmic_bytes(kb, w.k, w.V, w.elt)
+    for _ in range(args.warmup):
+        oracle.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"],
+                      inp["T"], lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"],
+                      inp["T"], lib=lib)
+    dt = time.perf_counter() - t0
+    value = positions * args.steps / dt
+    sample = f"{n} of {w.B} sequences of {w.describe()} per step (host-generated)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.describe(), "sample_sequences": n},
+        "gbs": nbytes * args.steps / dt / 1e9,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=None):
+    """Device-timed steps of one workload.  Returns a dict of measurements."""
+    import torch
+
+    from workloads import algorithmic_bytes, make_inputs
+
+    base = make_inputs(w, device=device)
+    sets = [base] + [{k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in base.items()}
+                     for _ in range(rotate - 1)]
+    kb = base["draft_len"].cpu().numpy()
+    positions = int(np.sum(kb + 1))
+    nbytes = algorithmic_bytes(kb, w.k, w.V, w.elt)
+    ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+    if args.cluster_size:
+        ver.set_cluster_size(args.cluster_size)
+    outs = [(torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device),
+             torch.empty(w.B, dtype=torch.int32, device=device)) for _ in range(rotate)]
+
+    def step(i):
+        s = sets[i % rotate]
+        o = outs[i % rotate]
+        ver.verify(s["target"], s["draft"], s["tokens"], s["draft_len"], s["uniforms"], s["T"],
+                   out_tokens=o[0], out_len=o[1], stream=stream)
+
+    with torch.cuda.stream(stream):
+        soak = 0
+        if sampler is not None:
+            sampler.start()
+            t_end = time.perf_counter() + 1.5      # let the clock sampler see a loaded GPU
+            while time.perf_counter() < t_end:
+                for _ in range(50):
+                    step(soak)
+                    soak += 1
+                stream.synchronize()
+        for i in range(warmup):
+            step(i)
+        ver.reset_stats(stream=stream)
+        stream.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(steps):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t_stop.record(stream)
+        stream.synchronize()
+    clocks = sampler.stop() if sampler is not None else None
+    total_ms = t_start.elapsed_time(t_stop)
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    st, stats = ver.stats(stream=stream)
+    if st != svp.SV_OK:
+        raise RuntimeError(f"device error {st} during the timed region: {stats}")
+    cfg = ver.config()
+    del sets, outs
+    return {"total_ms": total_ms, "kernel_ms_mean": float(np.mean(kern_ms)),
+            "kernel_ms_median": float(np.median(kern_ms)), "kernel_ms_best": float(np.min(kern_ms)),
+            "positions": positions, "bytes": nbytes, "stats": stats, "clocks": clocks,
+            "soak_steps": soak, "cfg": cfg, "ver": ver, "base_inputs": base}
+
+
+def e2e_measure(svp, w, args, device, stream, ver, base):
+    """End to end through the public binding with host buffers: per step the
+    pinned-host inputs are copied to the device, verified, and the outputs
+    copied back and read."""
+    import torch
+
+    host = {k: v.cpu().pin_memory() for k, v in base.items() if isinstance(v, torch.Tensor)}
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out_t = torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device)
+    out_l = torch.empty(w.B, dtype=torch.int32, device=device)
+    h_t = torch.empty(w.B, w.k + 1, dtype=torch.int32).pin_memory()
+    h_l = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = h_t.numel() * 4 + h_l.numel() * 4
+    positions = int(host["draft_len"].numpy().astype(np.int64).sum() + w.B)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for k in dev:
+                dev[k].copy_(host[k], non_blocking=True)
+            ver.verify(dev["target"], dev["draft"], dev["tokens"], dev["draft_len"], dev["uniforms"],
+                       base["T"], out_tokens=out_t, out_len=out_l, stream=stream)
+            h_t.copy_(out_t, non_blocking=True)
+            h_l.copy_(out_l, non_blocking=True)
+        stream.synchronize()
+        return int(h_l.numpy().sum())
+
+    for _ in range(3):
+        step()
+    n = max(1, args.e2e_steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    dt = time.perf_counter() - t0
+    return {"value": positions * n / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": dt / n * 1e3}
+
+
+def our_arm(args, w):
+    import torch
+
+    import speculative_decoding_verification_71_gb300 as svp
+    from speculative_decoding_verification_71_gb300 import build as svbuild
+
+    rank, world, local = dist_env()
+    svbuild.build()
+    svp.load_library()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+
+    stream = torch.cuda.Stream(device=device)
+    sampler = None if args.no_clocks else ClockSampler(local)
+    if pg:
+        pg.barrier()
+    m = time_workload(svp, w, args, device, stream, args.rotate, args.steps, args.warmup, sampler)
+    total_ms = m["total_ms"]
+    if pg:
+        t = torch.tensor([total_ms], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+        pg.barrier()
+    ms_per_step = total_ms / args.steps
+    value = world * m["positions"] * args.steps / (total_ms / 1e3)
+    gbs_step = m["bytes"] / (ms_per_step / 1e3) / 1e9
+    kern_gbs = m["bytes"] / (m["kernel_ms_mean"] / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    e2e = e2e_measure(svp, w, args, device, stream, m["ver"], m["base_inputs"])
+    if pg:
+        t = torch.tensor([e2e["ms_per_step"]], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e["value"] = world * m["positions"] / (float(t.item()) / 1e3)
+
+    aux = {}
+    for name in [a for a in args.aux.split(",") if a]:
+        from workloads import get_workload
+        aw = get_workload(name)
+        am = time_workload(svp, aw, args, device, stream, args.rotate, max(1, args.steps // 4), args.warmup)
+        aux[name] = {"workload": aw.describe(), "positions_per_s": am["positions"] / (am["total_ms"] / max(1, args.steps // 4) / 1e3),
+                     "ms_per_step": am["total_ms"] / max(1, args.steps // 4),
+                     "kernel_gbs": am["bytes"] / (am["kernel_ms_mean"] / 1e3) / 1e9,
+                     "frac_of_8tbs": am["bytes"] / (am["kernel_ms_mean"] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes": am["bytes"], "mean_emitted": am["stats"]["mean_emitted"]}
+        del am
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        r = oracle_sample_rate(w, args.cpu_seconds)
+        cpu = {"value": r["positions"] / r["seconds"], "unit": UNIT, "cores": r["threads"], "kind": "oracle",
+               "sample": f"{r['sequences']} sequences of {w.describe()} (host-generated), "
+                         f"{r['seconds']:.1f} s with {r['threads']} OpenMP threads"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.describe(), "global_batch": w.B * world, "vocab": w.V, "k_max": w.k,
+                   "verified_positions_per_step": m["positions"],
+                   "algorithmic_bytes_per_step": m["bytes"],
+                   "l2": f"{args.rotate} rotating copies of the inputs (each larger than the 129 MB L2)",
+                   "parallelism": f"replicas{world}", "cluster_size": m["cfg"]["cluster_size"],
+                   "threads": m["cfg"]["threads"], "smem_bytes": m["cfg"]["smem_bytes"]},
+        "gbs": gbs_step, "frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": kern_gbs / peak, "peak_source": peak_kind,
+                     "traffic": profiled_traffic(w.name), "kernel": KERNEL_NAME,
+                     "kernel_ms_mean": m["kernel_ms_mean"], "kernel_ms_median": m["kernel_ms_median"],
+                     "kernel_ms_best": m["kernel_ms_best"]},
+        "clocks": m["clocks"], "clock_soak_steps": m["soak_steps"],
+        "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+        "gpu_launches": args.steps,
+        "acceptance": {"mean_emitted": m["stats"]["mean_emitted"], "mean_accepted": m["stats"]["mean_accepted"],
+                       "accept_rate": m["stats"]["accept_rate"], "spec_off": m["stats"]["spec_off"]},
+        "cpu_baseline": cpu, "aux": aux or None,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from workloads import get_workload
+    w = get_workload(args.workload)
+    if args.impl == "reference":
+        reference_arm(args, w)
+    else:
+        our_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * specverify: lossless speculative-sampling verification on one GPU (sm_103a).
+ *
+ * The operation.  A drafter proposes k tokens per sequence; the target model
+ * scores them in one forward pass; the verifier accepts or rejects the drafts
+ * from the target's probability distribution so that the rollout keeps the
+ * target policy's output distribution exactly ("Accelerating RL Post-Training
+ * Rollouts via System-Integrated Speculative Decoding", §2 core mechanism:
+ * drafting, verification in one forward pass, rejection sampling).  The
+ * verifier checks all drafts together and rewrites from the first wrong token
+ * ("Online Draft Co-Training for Speculative Decoding in Large-Scale,
+ * Long-Context RL Post-Training", the stenographer/proof-reader analogy).
+ * The pages do not write the rule down; this library implements the standard
+ * speculative-sampling rule, which is the reading their exactness claim needs:
+ *
+ *   p_i = softmax(z^t_i / T),  q_i = softmax(z^d_i / T)
+ *   draft i is accepted iff u_i < min(1, p_i(x_i) / q_i(x_i));
+ *   the first rejection a ends the round;
+ *   if a < k_b the token at a is drawn from max(0, p_a - q_a) (normalised),
+ *   else a bonus token is drawn from p_{k_b};
+ *   draws are inverse CDF in ascending token id with the sequence's one
+ *   sampling uniform s_b = u_{b,k}: y = min{x : s_b * S < C(x)}.
+ *
+ * Per-sequence draft lengths k_b in [0, k] are allowed; k_b = 0 turns
+ * speculation off for that sequence, which then emits one token sampled from
+ * p_0 ("EfficientRollout: System-Aware Self-Speculative Decoding for RL
+ * Rollouts", abstract: system-aware SD toggle policy).  T == 0 is greedy:
+ * a draft is accepted iff it is the first argmax of p_i, and the emitted
+ * token is the first argmax of the decided target row.
+ *
+ * Memory.  Every tensor argument is caller-owned DEVICE memory, row-major and
+ * contiguous.  The context owns a fixed workspace allocated by sv_create;
+ * spec_verify itself allocates nothing.  One context serves one stream at a
+ * time and is not thread-safe.
+ *
+ * Errors.  Problems visible on the host (NULL pointers, sizes beyond the
+ * context's limits, a bad temperature) return an error code synchronously and
+ * launch nothing.  Problems found on the device (a draft length outside
+ * [0,k], a drafted token outside [0,V), NaN or +inf in a row that is read, a
+ * read row that is all -inf) mark only the affected sequence: it emits
+ * nothing (out_len 0, tokens -1), and the code's bit is set in a sticky
+ * device error word that spec_verify_stats returns.
+ *
+ * Determinism.  The library draws no random numbers: all randomness comes
+ * from `uniforms`.  Reductions run in a fixed order, so repeated calls on the
+ * same inputs give bitwise identical outputs.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *sv_stream_t;
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,   /* host-side argument check failed; nothing launched */
+    SV_ERR_BAD_DRAFT_LEN = 2, /* device: some draft_len[b] outside [0, k] */
+    SV_ERR_BAD_TOKEN = 3,     /* device: some drafted token outside [0, V) */
+    SV_ERR_NONFINITE = 4,     /* device: NaN/+inf in a read row, or a read row all -inf */
+    SV_ERR_TIMEOUT = 5,       /* device: a bounded wait for staged logits expired */
+    SV_ERR_CUDA = 6,          /* a CUDA runtime call failed (see sv_last_cuda_error) */
+    SV_ERR_UNSUPPORTED = 7    /* the device or configuration is not supported */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef struct sv_ctx sv_ctx;
+
+/* Running counters since the last reset (spec_verify_stats).  The pages track
+ * accepted length ("Accelerating RL Post-Training Rollouts ...", §4 draft
+ * initialisation; "ReSpec", GAP 2 / Fig. 4) without defining it, so both
+ * readings are reported: mean_accepted = sum a_b / sequences (accepted
+ * drafts) and mean_emitted = sum (a_b + 1) / sequences (tokens emitted per
+ * round, the usual "tau"). */
+typedef struct {
+    double mean_emitted;       /* sum(a_b + 1) / sequences */
+    double mean_accepted;      /* sum(a_b) / sequences */
+    double accept_rate;        /* drafts_accepted / drafts_proposed (0 if none) */
+    long long calls;           /* spec_verify calls counted */
+    long long sequences;       /* sequences verified without a device error */
+    long long drafts_proposed; /* sum k_b */
+    long long drafts_accepted; /* sum a_b */
+    long long emitted;         /* sum (a_b + 1) */
+    long long spec_off;        /* sequences with k_b == 0 */
+    long long zero_residual;   /* rejections whose residual mass was exactly 0 */
+    long long error_sequences; /* sequences that emitted nothing because of a device error */
+    unsigned int error_bits;   /* OR of (1 << code) over device errors seen */
+} sv_stats;
+
+/* Human-readable name of a status code (static string). */
+const char *sv_status_string(sv_status s);
+
+/* Message of the last CUDA error seen by this context ("" if none).
+ * ctx may be NULL for errors raised by sv_create. */
+const char *sv_last_cuda_error(const sv_ctx *ctx);
+
+/* Create a context for batches of up to max_B sequences, up to max_k drafts
+ * each, vocabulary V and logit dtype `dtype`, on the current CUDA device.
+ * Allocates the fixed device workspace (O(max_B * (max_k + 1)) words) and
+ * chooses the launch configuration.  *ctx receives the handle.
+ * Errors: SV_ERR_INVALID_ARG (sizes <= 0 or too large, NULL ctx),
+ * SV_ERR_UNSUPPORTED (no sm_100-family device), SV_ERR_CUDA. */
+sv_status sv_create(sv_ctx **ctx, int max_B, int max_k, int V, sv_dtype dtype);
+
+/* Release the context and its workspace.  NULL is accepted. */
+sv_status sv_destroy(sv_ctx *ctx);
+
+/*
+ * Verify one round of drafts for B sequences (asynchronous on `stream`).
+ *
+ *   target_logits  [B, k+1, V] dtype   target rows; row (b, i) scores position
+ *                                      i; row (b, k_b) is the bonus row.  Rows
+ *                                      i > k_b are never read.
+ *   draft_logits   [B, k, V]   dtype   drafter rows q; rows i >= k_b are never
+ *                                      read.  May be NULL when k == 0 or T == 0.
+ *   draft_tokens   [B, k]      int32   x_{b,i}; entries i >= k_b are ignored.
+ *   draft_len      [B]         int32   k_b in [0, k].
+ *   uniforms       [B, k+1]    float   in [0,1): columns 0..k-1 are the accept
+ *                                      tests, column k the sampling uniform.
+ *   temperature    T >= 0, finite; T == 0 is greedy (uniforms unused).
+ *   out_tokens     [B, k+1]    int32   written: accepted drafts, then the
+ *                                      sampled token, then -1 padding.
+ *   out_len        [B]         int32   written: a_b + 1 (0 on a device error).
+ *
+ * Requires 1 <= B <= max_B, 0 <= k <= max_k.  Rows are read with 16-byte
+ * bulk copies when V * sizeof(dtype) is a multiple of 16 and the logit
+ * pointers are 16-byte aligned, and with plain loads otherwise.
+ * Returns SV_OK once the work is enqueued; device-side problems are reported
+ * by spec_verify_stats.
+ */
+sv_status spec_verify(sv_ctx *ctx, int B, int k,
+                      const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, const int32_t *draft_len,
+                      const float *uniforms, float temperature,
+                      int32_t *out_tokens, int32_t *out_len,
+                      sv_stream_t stream);
+
+/*
+ * Compact the outputs of a verification into one packed token list
+ * (asynchronous on `stream`): offsets[b] = sum_{b' < b} out_len[b'],
+ * offsets[B] = total, packed[offsets[b] + j] = out_tokens[b, j] for
+ * j < out_len[b].  All pointers are device memory; packed must hold
+ * B * (k+1) entries (the worst case).  Requires 1 <= B <= max_B.
+ */
+sv_status spec_verify_compact(sv_ctx *ctx, int B, int k,
+                              const int32_t *out_tokens, const int32_t *out_len,
+                              int32_t *packed, int32_t *offsets,
+                              sv_stream_t stream);
+
+/*
+ * Per-row diagnostics of the LAST spec_verify call on this context, for
+ * parity checks (asynchronous on `stream`; device pointers; any may be NULL):
+ *   lse_t      [B, k+1] double  log-sum-exp of z^t_i / T for rows i <= k_b
+ *   lse_d      [B, k]   double  log-sum-exp of z^d_i / T for rows i < k_b
+ *   accept_prob[B, k]   double  min(1, p_i(x_i)/q_i(x_i)) for i < k_b
+ *   mass       [B, k+1] double  total weight S of the draw computed at
+ *                               position i (NaN where no draw was computed)
+ * Entries that do not apply (padding rows, T == 0, sequences with a device
+ * error) are NaN.  B and k must match the last call.
+ */
+sv_status spec_verify_debug(sv_ctx *ctx, int B, int k, double *lse_t, double *lse_d,
+                            double *accept_prob, double *mass, sv_stream_t stream);
+
+/* Synchronise `stream`, then read the running counters and the sticky device
+ * error word into *out.  Returns SV_OK, or the lowest-numbered device error
+ * code seen since the last reset, or SV_ERR_CUDA. */
+sv_status spec_verify_stats(sv_ctx *ctx, sv_stream_t stream, sv_stats *out);
+
+/* Clear the counters and the device error word (asynchronous on `stream`). */
+sv_status spec_verify_reset_stats(sv_ctx *ctx, sv_stream_t stream);
+
+/* Tuning and introspection.  sv_set_cluster_size picks how many CTAs (1, 2,
+ * 4, 8 or 16) share one target/draft row pair; 0 restores the automatic
+ * choice.  sv_get_config reports the current launch shape. */
+sv_status sv_set_cluster_size(sv_ctx *ctx, int cluster_size);
+sv_status sv_get_config(const sv_ctx *ctx, int *cluster_size, int *threads,
+                        int *smem_bytes, int *max_active_clusters);
+
+/* Test hook: the limit, in nanoseconds, of each bounded wait for staged logits
+ * (default 1 s; 0 makes every wait that is not already complete expire and
+ * report SV_ERR_TIMEOUT; the data is then still drained before the CTA
+ * moves on).  Negative restores the default. */
+sv_status sv_set_wait_limit_ns(sv_ctx *ctx, long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

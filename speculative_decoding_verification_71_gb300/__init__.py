@@ -1,0 +1,273 @@
+"""Lossless speculative-sampling verification on GB300 (sm_103a).
+
+A thin ctypes binding over ``libspecverify.so`` (C ABI in
+``include/specverify.h``).  Every step of the verification runs in the
+library's CUDA kernels; this module only marshals arguments: it checks
+shapes and dtypes, passes device pointers and the current CUDA stream, and
+allocates output tensors when the caller does not supply them.  There is no
+CPU fallback: if the library is missing or cannot be loaded, the first call
+raises.
+
+The low-level functions carry the C names (``sv_create``, ``spec_verify``,
+``spec_verify_compact``, ``spec_verify_debug``, ``spec_verify_stats``,
+``spec_verify_reset_stats``, ``sv_destroy`` ...).  ``SpecVerifier`` wraps a
+context for convenient use from PyTorch.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "SpecVerifier", "SpecVerifyError", "Stats", "load_library", "library_path",
+    "SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_BAD_DRAFT_LEN", "SV_ERR_BAD_TOKEN",
+    "SV_ERR_NONFINITE", "SV_ERR_TIMEOUT", "SV_ERR_CUDA", "SV_ERR_UNSUPPORTED",
+    "SV_F32", "SV_BF16", "EXPORTED_SYMBOLS",
+]
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_BAD_DRAFT_LEN, SV_ERR_BAD_TOKEN = 0, 1, 2, 3
+SV_ERR_NONFINITE, SV_ERR_TIMEOUT, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 4, 5, 6, 7
+SV_F32, SV_BF16 = 0, 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+_lib = None
+
+EXPORTED_SYMBOLS = (
+    "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
+    "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
+    "sv_set_cluster_size", "sv_get_config", "sv_set_wait_limit_ns",
+)
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [
+        ("mean_emitted", ctypes.c_double), ("mean_accepted", ctypes.c_double),
+        ("accept_rate", ctypes.c_double), ("calls", ctypes.c_longlong),
+        ("sequences", ctypes.c_longlong), ("drafts_proposed", ctypes.c_longlong),
+        ("drafts_accepted", ctypes.c_longlong), ("emitted", ctypes.c_longlong),
+        ("spec_off", ctypes.c_longlong), ("zero_residual", ctypes.c_longlong),
+        ("error_sequences", ctypes.c_longlong), ("error_bits", ctypes.c_uint),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status, where, detail=""):
+        self.status = status
+        name = _status_name(status)
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load the C-ABI library (once).  Raises if it is absent: build it with
+    ``speculative_decoding_verification_71_gb300.build.build()``."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libspecverify.so not found at {p}; build it first (build.build())")
+    lib = ctypes.CDLL(p)
+    c, P = ctypes, ctypes.c_void_p
+    lib.sv_status_string.restype = c.c_char_p
+    lib.sv_status_string.argtypes = [c.c_int]
+    lib.sv_last_cuda_error.restype = c.c_char_p
+    lib.sv_last_cuda_error.argtypes = [P]
+    lib.sv_create.restype = c.c_int
+    lib.sv_create.argtypes = [c.POINTER(P), c.c_int, c.c_int, c.c_int, c.c_int]
+    lib.sv_destroy.restype = c.c_int
+    lib.sv_destroy.argtypes = [P]
+    lib.spec_verify.restype = c.c_int
+    lib.spec_verify.argtypes = [P, c.c_int, c.c_int, P, P, P, P, P, c.c_float, P, P, P]
+    lib.spec_verify_compact.restype = c.c_int
+    lib.spec_verify_compact.argtypes = [P, c.c_int, c.c_int, P, P, P, P, P]
+    lib.spec_verify_debug.restype = c.c_int
+    lib.spec_verify_debug.argtypes = [P, c.c_int, c.c_int, P, P, P, P, P]
+    lib.spec_verify_stats.restype = c.c_int
+    lib.spec_verify_stats.argtypes = [P, P, c.POINTER(Stats)]
+    lib.spec_verify_reset_stats.restype = c.c_int
+    lib.spec_verify_reset_stats.argtypes = [P, P]
+    lib.sv_set_cluster_size.restype = c.c_int
+    lib.sv_set_cluster_size.argtypes = [P, c.c_int]
+    lib.sv_get_config.restype = c.c_int
+    lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 4
+    lib.sv_set_wait_limit_ns.restype = c.c_int
+    lib.sv_set_wait_limit_ns.argtypes = [P, c.c_longlong]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _status_name(status):
+    names = ["SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_BAD_DRAFT_LEN", "SV_ERR_BAD_TOKEN",
+             "SV_ERR_NONFINITE", "SV_ERR_TIMEOUT", "SV_ERR_CUDA", "SV_ERR_UNSUPPORTED"]
+    return names[status] if 0 <= status < len(names) else f"status {status}"
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream_handle(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_dev(name, t, dtype, shape, device):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class SpecVerifier:
+    """A verification context: fixed workspace for up to ``max_B`` sequences
+    of up to ``max_k`` drafts over vocabulary ``V`` in ``dtype``
+    (torch.float32 or torch.bfloat16), on the current CUDA device."""
+
+    def __init__(self, max_B: int, max_k: int, V: int, dtype=torch.bfloat16, device=None):
+        self.lib = load_library()
+        if dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("dtype must be torch.float32 or torch.bfloat16")
+        self.max_B, self.max_k, self.V, self.dtype = max_B, max_k, V, dtype
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   torch.device(device).index or 0)
+        self._ctx = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            st = self.lib.sv_create(ctypes.byref(self._ctx), max_B, max_k, V,
+                                    SV_F32 if dtype == torch.float32 else SV_BF16)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "sv_create", self.lib.sv_last_cuda_error(None).decode())
+
+    # -- lifetime -------------------------------------------------------
+    def close(self):
+        if self._ctx:
+            self.lib.sv_destroy(self._ctx)
+            self._ctx = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @property
+    def handle(self):
+        return self._ctx
+
+    def _raise(self, st, where):
+        raise SpecVerifyError(st, where, self.lib.sv_last_cuda_error(self._ctx).decode())
+
+    # -- the verification ------------------------------------------------
+    def verify(self, target, draft, tokens, draft_len, uniforms, temperature,
+               out_tokens=None, out_len=None, stream=None):
+        """Enqueue one verification on ``stream`` (default: current stream).
+
+        target [B,k+1,V], draft [B,k,V] (dtype of the context), tokens [B,k]
+        int32, draft_len [B] int32, uniforms [B,k+1] float32.  Returns
+        (out_tokens [B,k+1] int32, out_len [B] int32), allocated if not given.
+        """
+        B, k1, V = target.shape
+        k = k1 - 1
+        dev = target.device
+        _check_dev("target", target, self.dtype, (B, k + 1, self.V), dev)
+        if draft is not None:
+            _check_dev("draft", draft, self.dtype, (B, k, self.V), dev)
+        if tokens is not None:
+            _check_dev("tokens", tokens, torch.int32, (B, k), dev)
+        _check_dev("draft_len", draft_len, torch.int32, (B,), dev)
+        if uniforms is not None:
+            _check_dev("uniforms", uniforms, torch.float32, (B, k + 1), dev)
+        if out_tokens is None:
+            out_tokens = torch.empty(B, k + 1, dtype=torch.int32, device=dev)
+        if out_len is None:
+            out_len = torch.empty(B, dtype=torch.int32, device=dev)
+        _check_dev("out_tokens", out_tokens, torch.int32, (B, k + 1), dev)
+        _check_dev("out_len", out_len, torch.int32, (B,), dev)
+        st = self.lib.spec_verify(self._ctx, B, k, _ptr(target), _ptr(draft), _ptr(tokens),
+                                  _ptr(draft_len), _ptr(uniforms), float(temperature),
+                                  _ptr(out_tokens), _ptr(out_len), _stream_handle(stream))
+        if st != SV_OK:
+            self._raise(st, "spec_verify")
+        return out_tokens, out_len
+
+    def compact(self, out_tokens, out_len, packed=None, offsets=None, stream=None):
+        """Packed token list and exclusive-scan offsets of a verification's outputs."""
+        B, k1 = out_tokens.shape
+        dev = out_tokens.device
+        if packed is None:
+            packed = torch.empty(B * k1, dtype=torch.int32, device=dev)
+        if offsets is None:
+            offsets = torch.empty(B + 1, dtype=torch.int32, device=dev)
+        st = self.lib.spec_verify_compact(self._ctx, B, k1 - 1, _ptr(out_tokens), _ptr(out_len),
+                                          _ptr(packed), _ptr(offsets), _stream_handle(stream))
+        if st != SV_OK:
+            self._raise(st, "spec_verify_compact")
+        return packed, offsets
+
+    def debug(self, B, k, stream=None):
+        """Per-row diagnostics of the last call (float64 device tensors)."""
+        dev = self.device
+        lse_t = torch.empty(B, k + 1, dtype=torch.float64, device=dev)
+        lse_d = torch.empty(B, max(k, 1), dtype=torch.float64, device=dev)
+        alpha = torch.empty(B, max(k, 1), dtype=torch.float64, device=dev)
+        mass = torch.empty(B, k + 1, dtype=torch.float64, device=dev)
+        st = self.lib.spec_verify_debug(self._ctx, B, k, _ptr(lse_t), _ptr(lse_d), _ptr(alpha),
+                                        _ptr(mass), _stream_handle(stream))
+        if st != SV_OK:
+            self._raise(st, "spec_verify_debug")
+        return {"lse_t": lse_t, "lse_d": lse_d[:, :k], "alpha": alpha[:, :k], "mass": mass}
+
+    def stats(self, stream=None):
+        """Synchronise and read the counters.  Returns (status, dict)."""
+        s = Stats()
+        st = self.lib.spec_verify_stats(self._ctx, _stream_handle(stream), ctypes.byref(s))
+        if st == SV_ERR_CUDA:
+            self._raise(st, "spec_verify_stats")
+        return st, s.as_dict()
+
+    def reset_stats(self, stream=None):
+        st = self.lib.spec_verify_reset_stats(self._ctx, _stream_handle(stream))
+        if st != SV_OK:
+            self._raise(st, "spec_verify_reset_stats")
+
+    def set_cluster_size(self, cs: int):
+        st = self.lib.sv_set_cluster_size(self._ctx, int(cs))
+        if st != SV_OK:
+            self._raise(st, "sv_set_cluster_size")
+
+    def set_wait_limit_ns(self, ns: int):
+        st = self.lib.sv_set_wait_limit_ns(self._ctx, int(ns))
+        if st != SV_OK:
+            self._raise(st, "sv_set_wait_limit_ns")
+
+    def config(self):
+        vals = [ctypes.c_int() for _ in range(4)]
+        st = self.lib.sv_get_config(self._ctx, *[ctypes.byref(v) for v in vals])
+        if st != SV_OK:
+            self._raise(st, "sv_get_config")
+        return dict(zip(("cluster_size", "threads", "smem_bytes", "max_active_clusters"),
+                        (v.value for v in vals)))

@@ -1,0 +1,329 @@
+// C ABI of the verification library (declared in include/specverify.h).
+//
+// Host side only: argument checks, the context and its workspace, the
+// launch configuration.  Every step of the verification itself runs in the
+// kernels of sv_kernels.cu.
+
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/specverify.h"
+#include "sv_internal.h"
+
+struct sv_ctx {
+  int max_B = 0, max_k = 0, V = 0;
+  sv_dtype dtype = SV_BF16;
+  int elt = 2;
+  int device = 0;
+  int cluster = 1;
+  int slice = 0;
+  int smem_bytes = 0;
+  int max_active_clusters = 0;
+  long long wait_limit_ns = sv::kDrainLimitNs;
+  void* ws_mem = nullptr;
+  sv::Workspace ws{};
+  long long calls = 0;
+  int last_B = 0, last_k = 0, last_greedy = 0;
+  float last_inv_T = 1.f;
+  char cuda_msg[256] = {0};
+};
+
+namespace {
+
+thread_local char g_create_msg[256] = {0};
+
+sv_status cuda_fail(sv_ctx* ctx, cudaError_t e, const char* where) {
+  char* dst = ctx ? ctx->cuda_msg : g_create_msg;
+  std::snprintf(dst, 256, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  return SV_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int slice_for(int V, int cluster) {
+  const int per = (V + cluster - 1) / cluster;
+  return ((per + 7) / 8) * 8;
+}
+
+// Configure for a cluster size; fails if the shape cannot be launched.
+sv_status configure(sv_ctx* ctx, int cluster) {
+  const int slice = slice_for(ctx->V, cluster);
+  const int smem = sv::verify_smem_bytes(slice, ctx->elt, true);
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, ctx->device);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDeviceProperties");
+  if (smem > static_cast<int>(prop.sharedMemPerBlockOptin)) return SV_ERR_UNSUPPORTED;
+  e = sv::prepare_verify_kernel(smem, cluster);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute");
+  int active = 0;
+  e = sv::query_max_active_clusters(cluster, smem, &active);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SV_ERR_UNSUPPORTED;
+  }
+  if (active <= 0) return SV_ERR_UNSUPPORTED;
+  ctx->cluster = cluster;
+  ctx->slice = slice;
+  ctx->smem_bytes = smem;
+  ctx->max_active_clusters = active;
+  return SV_OK;
+}
+
+// Automatic choice: the smallest cluster whose per-CTA slice pair fits in
+// about 48 KB of shared memory, so that several CTAs share each SM and one
+// CTA's staging overlaps another's arithmetic.
+sv_status configure_auto(sv_ctx* ctx) {
+  const int sizes[5] = {1, 2, 4, 8, 16};
+  for (int i = 0; i < 5; ++i) {
+    const int cs = sizes[i];
+    const int smem = sv::verify_smem_bytes(slice_for(ctx->V, cs), ctx->elt, true);
+    if (smem > 48 * 1024 && cs < 16) continue;
+    if (configure(ctx, cs) == SV_OK) return SV_OK;
+  }
+  for (int i = 4; i >= 0; --i)
+    if (configure(ctx, sizes[i]) == SV_OK) return SV_OK;
+  return SV_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "SV_OK";
+    case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG";
+    case SV_ERR_BAD_DRAFT_LEN: return "SV_ERR_BAD_DRAFT_LEN";
+    case SV_ERR_BAD_TOKEN: return "SV_ERR_BAD_TOKEN";
+    case SV_ERR_NONFINITE: return "SV_ERR_NONFINITE";
+    case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA";
+    case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED";
+  }
+  return "SV_ERR_UNKNOWN";
+}
+
+const char* sv_last_cuda_error(const sv_ctx* ctx) { return ctx ? ctx->cuda_msg : g_create_msg; }
+
+sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
+  if (!out) return SV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (max_B <= 0 || max_k < 0 || V <= 0) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  // per-call index arithmetic is 32-bit in cluster ids and 64-bit in bytes
+  if (static_cast<long long>(max_B) * (max_k + 1) > (1LL << 26)) return SV_ERR_INVALID_ARG;
+  if (max_k > 4096) return SV_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDeviceProperties");
+  if (!(prop.major == 10 && prop.minor == 3)) {
+    std::snprintf(g_create_msg, sizeof g_create_msg,
+                  "built for sm_103a; device is sm_%d%d", prop.major, prop.minor);
+    return SV_ERR_UNSUPPORTED;
+  }
+
+  sv_ctx* ctx = new (std::nothrow) sv_ctx();
+  if (!ctx) return SV_ERR_CUDA;
+  ctx->max_B = max_B;
+  ctx->max_k = max_k;
+  ctx->V = V;
+  ctx->dtype = dtype;
+  ctx->elt = dtype == SV_F32 ? 4 : 2;
+  ctx->device = dev;
+
+  // one allocation, 256-byte aligned sub-arrays
+  const size_t nB = static_cast<size_t>(max_B);
+  const size_t nT = nB * (max_k + 1);
+  const size_t nD = nB * (max_k > 0 ? max_k : 1);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
+  const size_t o_done = take(nB * 4), o_rej = take(nB * 4), o_err = take(nB * 4);
+  const size_t o_y = take(nT * 4), o_mt = take(nT * 4), o_Lt = take(nT * 4);
+  const size_t o_md = take(nD * 4), o_Ld = take(nD * 4), o_al = take(nD * 4), o_mass = take(nT * 4);
+  const size_t o_stats = take(sv::kStatCount * 8), o_word = take(4);
+  e = cudaMalloc(&ctx->ws_mem, off);
+  if (e != cudaSuccess) {
+    sv_status s = cuda_fail(nullptr, e, "cudaMalloc(workspace)");
+    delete ctx;
+    return s;
+  }
+  char* base = static_cast<char*>(ctx->ws_mem);
+  sv::Workspace& ws = ctx->ws;
+  ws.done = reinterpret_cast<int*>(base + o_done);
+  ws.rej_min = reinterpret_cast<int*>(base + o_rej);
+  ws.seq_err = reinterpret_cast<int*>(base + o_err);
+  ws.y_slot = reinterpret_cast<int*>(base + o_y);
+  ws.m_t = reinterpret_cast<float*>(base + o_mt);
+  ws.L_t = reinterpret_cast<float*>(base + o_Lt);
+  ws.m_d = reinterpret_cast<float*>(base + o_md);
+  ws.L_d = reinterpret_cast<float*>(base + o_Ld);
+  ws.alpha = reinterpret_cast<float*>(base + o_al);
+  ws.mass = reinterpret_cast<float*>(base + o_mass);
+  ws.stats = reinterpret_cast<unsigned long long*>(base + o_stats);
+  ws.err_word = reinterpret_cast<unsigned int*>(base + o_word);
+
+  e = cudaMemset(ctx->ws_mem, 0, off);
+  if (e == cudaSuccess) e = sv::launch_init_workspace(ws, max_B, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    sv_status s = cuda_fail(nullptr, e, "workspace init");
+    cudaFree(ctx->ws_mem);
+    delete ctx;
+    return s;
+  }
+  sv_status s = configure_auto(ctx);
+  if (s != SV_OK) {
+    std::snprintf(g_create_msg, sizeof g_create_msg, "no launchable cluster shape for V=%d", V);
+    cudaFree(ctx->ws_mem);
+    delete ctx;
+    return s;
+  }
+  *out = ctx;
+  return SV_OK;
+}
+
+sv_status sv_destroy(sv_ctx* ctx) {
+  if (!ctx) return SV_OK;
+  cudaError_t e = cudaFree(ctx->ws_mem);
+  delete ctx;
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, const int32_t* draft_len, const float* uniforms,
+                      float temperature, int32_t* out_tokens, int32_t* out_len, sv_stream_t stream) {
+  if (!ctx) return SV_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->max_B || k < 0 || k > ctx->max_k) return SV_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+  const bool greedy = temperature == 0.f;
+  const double c2 = greedy ? 0.0 : 1.4426950408889634 / static_cast<double>(temperature);
+  if (!greedy && !(c2 < 1e30)) return SV_ERR_INVALID_ARG;
+  if (!target_logits || !draft_len || !out_tokens || !out_len) return SV_ERR_INVALID_ARG;
+  if (k > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;
+  if (k > 0 && !greedy && !draft_logits) return SV_ERR_INVALID_ARG;
+  if (!greedy && !uniforms) return SV_ERR_INVALID_ARG;
+
+  sv::VerifyParams p{};
+  p.target = target_logits;
+  p.draft = draft_logits;
+  p.tokens = draft_tokens;
+  p.draft_len = draft_len;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.out_len = out_len;
+  p.B = B;
+  p.k = k;
+  p.V = ctx->V;
+  p.elt = ctx->elt;
+  p.greedy = greedy ? 1 : 0;
+  p.c2 = static_cast<float>(c2);
+  p.slice = ctx->slice;
+  p.bulk = ((static_cast<long long>(ctx->V) * ctx->elt) % 16 == 0) && aligned16(target_logits) &&
+           (draft_logits == nullptr || aligned16(draft_logits));
+  p.wait_limit_ns = ctx->wait_limit_ns;
+  p.ws = ctx->ws;
+  cudaError_t e = sv::launch_verify(p, ctx->cluster, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "launch verify");
+  ctx->calls += 1;
+  ctx->last_B = B;
+  ctx->last_k = k;
+  ctx->last_greedy = greedy ? 1 : 0;
+  ctx->last_inv_T = greedy ? 0.f : 1.f / temperature;
+  return SV_OK;
+}
+
+sv_status spec_verify_compact(sv_ctx* ctx, int B, int k, const int32_t* out_tokens, const int32_t* out_len,
+                              int32_t* packed, int32_t* offsets, sv_stream_t stream) {
+  if (!ctx || B < 1 || B > ctx->max_B || k < 0 || k > ctx->max_k) return SV_ERR_INVALID_ARG;
+  if (!out_tokens || !out_len || !packed || !offsets) return SV_ERR_INVALID_ARG;
+  cudaError_t e = sv::launch_compact(B, k, out_tokens, out_len, packed, offsets,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : cuda_fail(ctx, e, "launch compact");
+}
+
+sv_status spec_verify_debug(sv_ctx* ctx, int B, int k, double* lse_t, double* lse_d, double* accept_prob,
+                            double* mass, sv_stream_t stream) {
+  if (!ctx || ctx->calls == 0) return SV_ERR_INVALID_ARG;
+  if (B != ctx->last_B || k != ctx->last_k) return SV_ERR_INVALID_ARG;
+  cudaError_t e = sv::launch_debug(ctx->ws, B, k, nullptr, ctx->last_greedy, ctx->last_inv_T, lse_t, lse_d,
+                                   accept_prob, mass, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SV_OK : cuda_fail(ctx, e, "launch debug");
+}
+
+sv_status spec_verify_stats(sv_ctx* ctx, sv_stream_t stream, sv_stats* out) {
+  if (!ctx || !out) return SV_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned long long st[sv::kStatCount];
+  unsigned int word = 0;
+  cudaError_t e = cudaMemcpyAsync(st, ctx->ws.stats, sizeof st, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&word, ctx->ws.err_word, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "spec_verify_stats");
+  std::memset(out, 0, sizeof *out);
+  out->calls = ctx->calls;
+  out->sequences = static_cast<long long>(st[sv::kStatSequences]);
+  out->drafts_proposed = static_cast<long long>(st[sv::kStatProposed]);
+  out->drafts_accepted = static_cast<long long>(st[sv::kStatAccepted]);
+  out->emitted = static_cast<long long>(st[sv::kStatEmitted]);
+  out->spec_off = static_cast<long long>(st[sv::kStatSpecOff]);
+  out->zero_residual = static_cast<long long>(st[sv::kStatZeroResidual]);
+  out->error_sequences = static_cast<long long>(st[sv::kStatErrorSeqs]);
+  out->error_bits = word;
+  if (out->sequences > 0) {
+    out->mean_emitted = static_cast<double>(out->emitted) / static_cast<double>(out->sequences);
+    out->mean_accepted = static_cast<double>(out->drafts_accepted) / static_cast<double>(out->sequences);
+  }
+  if (out->drafts_proposed > 0)
+    out->accept_rate = static_cast<double>(out->drafts_accepted) / static_cast<double>(out->drafts_proposed);
+  for (int code = SV_ERR_BAD_DRAFT_LEN; code <= SV_ERR_TIMEOUT; ++code)
+    if (word & (1u << code)) return static_cast<sv_status>(code);
+  return SV_OK;
+}
+
+sv_status spec_verify_reset_stats(sv_ctx* ctx, sv_stream_t stream) {
+  if (!ctx) return SV_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ctx->ws.stats, 0, sizeof(unsigned long long) * sv::kStatCount, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->ws.err_word, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "spec_verify_reset_stats");
+  ctx->calls = 0;
+  return SV_OK;
+}
+
+sv_status sv_set_cluster_size(sv_ctx* ctx, int cluster_size) {
+  if (!ctx) return SV_ERR_INVALID_ARG;
+  if (cluster_size == 0) return configure_auto(ctx);
+  if (cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8 && cluster_size != 16)
+    return SV_ERR_INVALID_ARG;
+  const int prev = ctx->cluster;
+  sv_status s = configure(ctx, cluster_size);
+  if (s != SV_OK) configure(ctx, prev);
+  return s;
+}
+
+sv_status sv_get_config(const sv_ctx* ctx, int* cluster_size, int* threads, int* smem_bytes,
+                        int* max_active_clusters) {
+  if (!ctx) return SV_ERR_INVALID_ARG;
+  if (cluster_size) *cluster_size = ctx->cluster;
+  if (threads) *threads = sv::kThreads;
+  if (smem_bytes) *smem_bytes = ctx->smem_bytes;
+  if (max_active_clusters) *max_active_clusters = ctx->max_active_clusters;
+  return SV_OK;
+}
+
+sv_status sv_set_wait_limit_ns(sv_ctx* ctx, long long ns) {
+  if (!ctx) return SV_ERR_INVALID_ARG;
+  ctx->wait_limit_ns = ns < 0 ? sv::kDrainLimitNs : ns;
+  return SV_OK;
+}
+
+}  // extern "C"

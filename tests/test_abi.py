@@ -1,0 +1,76 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; host-side argument checks reject bad calls without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_71_gb300 as svp
+from speculative_decoding_verification_71_gb300 import build as svbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    svbuild.build()
+    return svp.load_library()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b((?:sv|spec_verify)\w*)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(svp.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_BAD_DRAFT_LEN",
+                                 "SV_ERR_BAD_TOKEN", "SV_ERR_NONFINITE", "SV_ERR_TIMEOUT",
+                                 "SV_ERR_CUDA", "SV_ERR_UNSUPPORTED"]):
+        assert lib.sv_status_string(code).decode() == name
+
+
+def test_null_context_is_rejected_on_the_host(lib):
+    P = None
+    assert lib.spec_verify(P, 1, 1, P, P, P, P, P, 1.0, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_compact(P, 1, 1, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_debug(P, 1, 1, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_stats(P, P, None) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_reset_stats(P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_set_cluster_size(P, 4) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_set_wait_limit_ns(P, 0) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_get_config(P, None, None, None, None) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_destroy(P) == svp.SV_OK
+
+
+def test_create_rejects_bad_sizes_before_any_cuda_call(lib):
+    h = ctypes.c_void_p()
+    for args in [(0, 3, 100, 1), (4, -1, 100, 1), (4, 3, 0, 1), (4, 3, 100, 7), (1 << 25, 7, 100, 1)]:
+        assert lib.sv_create(ctypes.byref(h), *args) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_create(None, 4, 3, 100, 1) == svp.SV_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not found"):
+        svp.load_library(str(tmp_path / "missing.so"))
+
+
+def test_product_does_not_use_the_oracle():
+    """The library and its binding never import, load or name the oracle."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_71_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cuh", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"import\s+oracle|from\s+oracle|liboracle|oracle\.c", text), f

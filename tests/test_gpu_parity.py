@@ -1,0 +1,310 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import softmax
+from scipy import stats as sstats
+
+import oracle
+import speculative_decoding_verification_71_gb300 as svp
+from speculative_decoding_verification_71_gb300 import build as svbuild
+from tests import enum_cases
+from tests.parity import (NEAR_TIE, RTOL, check_invariants, compare, compare_diagnostics,
+                          run_gpu, run_oracle)
+from workloads import get_workload, gumbel_argmax_tokens, make_inputs, philox_uniforms
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    svbuild.build()
+    svp.load_library()
+
+
+def verifier_for(inp, **kw):
+    w = inp["meta"]["workload"]
+    return svp.SpecVerifier(inp["meta"]["B"], w.k, w.V, w.torch_dtype, **kw)
+
+
+def small(name, **over):
+    w = dataclasses.replace(get_workload(name), **over)
+    return make_inputs(w, device=DEV)
+
+
+def assert_parity(inp, ver=None, check_diag=True, max_tie_frac=0.2):
+    ver = ver or verifier_for(inp)
+    toks, lens = run_gpu(ver, inp)
+    ref = run_oracle(inp)
+    kb = inp["draft_len"].cpu().numpy()
+    res = compare(toks, lens, ref, kb)
+    assert res["mismatch"] == 0, res["bad"][:10]
+    assert res["accept_ties"] + res["sample_ties"] <= max_tie_frac * res["sequences"] + 2, res
+    if check_diag and inp["T"] > 0:
+        worst = compare_diagnostics(ver.debug(lens.shape[0], inp["meta"]["k"]), ref, kb, lens)
+        assert worst["lse"] < RTOL and worst["alpha"] < RTOL and worst["mass"] < RTOL, worst
+    return toks, lens, ref, res
+
+
+# --- the tiny workload and small cases spanning several CTAs -----------------
+
+def test_tiny_workload():
+    assert_parity(make_inputs(get_workload("tiny"), device=DEV))
+
+
+SMALL_CASES = [
+    # name, overrides
+    ("ragged", dict(B=48, k=4, V=20000)),                          # bulk copies, several CTAs
+    ("ragged", dict(B=40, k=3, V=5003, T=0.8)),                    # unaligned rows: plain loads
+    ("tiny", dict(B=32, k=2, V=4099, T=1.3, ragged=True)),         # fp32 unaligned
+    ("tiny", dict(B=64, k=3, V=1024)),                             # fp32, one CTA per item
+    ("long_draft", dict(B=24, k=7, V=12288)),                      # heavy tails, T = 0.6
+    ("grpo", dict(B=32, k=3, V=8192)),                             # near-full acceptance
+    ("qwen_b32", dict(B=16, k=0, V=3000)),                         # speculation off everywhere
+    ("qwen_b32", dict(B=8, k=3, V=151936)),                        # full vocabulary rows
+]
+
+
+@pytest.mark.parametrize("name,over", SMALL_CASES, ids=[f"{n}-{o}" for n, o in SMALL_CASES])
+def test_small_cases(name, over):
+    assert_parity(small(name, **over))
+
+
+@pytest.mark.parametrize("cs", [1, 2, 4, 8, 16])
+def test_every_cluster_size_gives_the_same_result(cs):
+    inp = small("ragged", B=32, k=3, V=24576)
+    ver = verifier_for(inp)
+    ver.set_cluster_size(cs)
+    assert ver.config()["cluster_size"] == cs
+    toks, lens, _, _ = assert_parity(inp, ver)
+    ver.set_cluster_size(16 if cs != 16 else 1)
+    toks2, lens2 = run_gpu(ver, inp)
+    np.testing.assert_array_equal(lens, lens2)
+    np.testing.assert_array_equal(toks, toks2)
+
+
+# --- exhaustive enumeration batch ----------------------------------------------
+
+@pytest.mark.parametrize("kb,T,seed", [(2, 1.0, 0), (1, 0.7, 1), (0, 1.6, 2)])
+def test_enumeration_batch_decisions(kb, T, seed):
+    batch, P = enum_cases.build(V=4, k=2, kb=kb, T=T, seed=seed)
+    far = batch["margin"] >= NEAR_TIE
+    inp = {k: torch.from_numpy(batch[k]).to(DEV) for k in ("target", "draft", "tokens", "draft_len", "uniforms")}
+    inp["T"] = T
+    ver = svp.SpecVerifier(len(batch["weight"]), 2, 4, torch.float32)
+    toks, lens = run_gpu(ver, inp)
+    ref = oracle.verify(batch["target"], batch["draft"], batch["tokens"], batch["draft_len"],
+                        batch["uniforms"], T)
+    np.testing.assert_array_equal(lens[far], ref["out_len"][far])
+    np.testing.assert_array_equal(toks[far], ref["out_tokens"][far])
+    # the GPU's own outputs give the target's joint distribution
+    if far.all():
+        got = enum_cases.joint_from_outputs(toks, lens, batch["weight"], P, 4, 2)
+        assert np.max(np.abs(got - enum_cases.target_joint(P, 4, 2))) < 1e-12
+
+
+# --- special cases ----------------------------------------------------------------
+
+def test_identical_draft_accepts_all():
+    inp = small("ragged", B=64, k=5, V=10000)
+    inp["draft"] = inp["target"][:, :5].clone()
+    kb = inp["draft_len"]
+    pad = torch.arange(5, device=DEV).view(1, 5) >= kb.view(-1, 1)
+    inp["draft"][pad] = float("nan")
+    ver = verifier_for(inp)
+    toks, lens = run_gpu(ver, inp)
+    np.testing.assert_array_equal(lens, kb.cpu().numpy() + 1)
+    dbg = ver.debug(64, 5)
+    a = dbg["alpha"].cpu().numpy()
+    kbn = kb.cpu().numpy()
+    for b in range(64):
+        assert (a[b, :kbn[b]] == 1.0).all()
+
+
+@pytest.mark.parametrize("T", [1e-3, 0.0])
+def test_low_temperature_is_argmax(T):
+    rng = np.random.default_rng(21)
+    B, k, V = 128, 3, 256
+    # distinct multiples of 0.25 in [-32, 32): exact in bf16, gaps of 0.25
+    t = np.stack([(rng.permutation(V) - 128) * 0.25 for _ in range(B * (k + 1))]).astype(np.float32)
+    t = t.reshape(B, k + 1, V)
+    d = np.stack([(rng.permutation(V) - 128) * 0.25 for _ in range(B * k)]).astype(np.float32).reshape(B, k, V)
+    agree = rng.random((B, k)) < 0.5
+    d[agree] = t[:, :k][agree]
+    tok = d.argmax(axis=2).astype(np.int32)
+    kl = np.full(B, k, np.int32)
+    u = philox_uniforms(B * (k + 1), seed=6).reshape(B, k + 1)
+    tb = torch.from_numpy(t).to(torch.bfloat16)
+    db = torch.from_numpy(d).to(torch.bfloat16)
+    inp = {"target": tb.to(DEV), "draft": db.to(DEV), "tokens": torch.from_numpy(tok).to(DEV),
+           "draft_len": torch.from_numpy(kl).to(DEV), "uniforms": torch.from_numpy(u).to(DEV), "T": T}
+    ver = svp.SpecVerifier(B, k, V, torch.bfloat16)
+    toks, lens = run_gpu(ver, inp)
+    ref = oracle.verify(tb, db, tok, kl, u, T)
+    np.testing.assert_array_equal(lens, ref["out_len"])
+    np.testing.assert_array_equal(toks, ref["out_tokens"])
+    amax = tb.float().numpy().argmax(axis=2)
+    for b in range(B):
+        a = lens[b] - 1
+        assert toks[b, a] == amax[b, a]
+
+
+def test_greedy_ties_and_null_draft():
+    V, k = 64, 1
+    t = torch.zeros(1, 2, V)
+    t[0, 0, [2, 5]] = 3.0
+    t[0, 1, [1, 6]] = 4.0
+    inp = {"target": t.to(DEV), "draft": None, "tokens": torch.tensor([[2]], dtype=torch.int32, device=DEV),
+           "draft_len": torch.tensor([1], dtype=torch.int32, device=DEV), "uniforms": None, "T": 0.0}
+    ver = svp.SpecVerifier(1, k, V, torch.float32)
+    toks, lens = run_gpu(ver, inp)
+    assert lens[0] == 2 and list(toks[0]) == [2, 1]
+
+
+def test_device_errors_mark_only_their_sequence():
+    inp = small("tiny", B=8, k=2, V=2048)
+    kb = torch.tensor([2, 3, 2, 2, 1, 0, 2, -1], dtype=torch.int32, device=DEV)
+    inp["draft_len"] = kb
+    inp["tokens"][2, 1] = 2048            # bad token
+    inp["target"][3, 1, 5] = float("nan")  # NaN in a read row
+    inp["target"][4, 2] = float("nan")     # padding only (k_b = 1): fine
+    inp["draft"][4, 1] = float("nan")
+    inp["target"][5, 1:] = float("inf")    # padding of a k_b = 0 sequence: fine
+    inp["target"][6, 0] = float("-inf")    # a read row that is all -inf
+    ver = verifier_for(inp)
+    ver.reset_stats()
+    toks, lens = run_gpu(ver, inp)
+    st, s = ver.stats()
+    assert st == svp.SV_ERR_BAD_DRAFT_LEN
+    assert s["error_bits"] == (1 << 2) | (1 << 3) | (1 << 4)
+    for b in (1, 2, 3, 6, 7):
+        assert lens[b] == 0 and (toks[b] == -1).all(), b
+    ref = run_oracle(inp)
+    res = compare(toks, lens, ref, kb.cpu().numpy())
+    assert res["mismatch"] == 0, res["bad"]
+    assert s["error_sequences"] == 5 and s["sequences"] == 3
+    # nothing carries over into the next call
+    good = small("tiny", B=8, k=2, V=2048)
+    ver.reset_stats()
+    assert_parity(good, ver)
+    st, s = ver.stats()
+    assert st == svp.SV_OK and s["error_bits"] == 0 and s["sequences"] == 8
+
+
+def test_masked_vocabulary_is_allowed():
+    inp = small("ragged", B=16, k=3, V=8192)
+    inp["target"][:, :, :100] = float("-inf")
+    inp["draft"][:, :, 50:150] = float("-inf")
+    kb = inp["draft_len"].long()
+    inp["target"][torch.arange(4, device=DEV).view(1, 4) > kb.view(-1, 1)] = float("nan")
+    inp["draft"][torch.arange(3, device=DEV).view(1, 3) >= kb.view(-1, 1)] = float("nan")
+    assert_parity(inp)
+
+
+def test_repeated_calls_are_bitwise_identical():
+    inp = small("ragged", B=64, k=3, V=32768)
+    ver = verifier_for(inp)
+    t0, l0 = run_gpu(ver, inp)
+    for _ in range(9):
+        t1, l1 = run_gpu(ver, inp)
+        np.testing.assert_array_equal(t0, t1)
+        np.testing.assert_array_equal(l0, l1)
+
+
+def test_compaction_and_stats():
+    inp = small("ragged", B=300, k=3, V=4096)
+    ver = verifier_for(inp)
+    ver.reset_stats()
+    ot, ol = ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"], inp["T"])
+    packed, offsets = ver.compact(ot, ol)
+    torch.cuda.synchronize()
+    otn, oln = ot.cpu().numpy(), ol.cpu().numpy()
+    offs = offsets.cpu().numpy()
+    np.testing.assert_array_equal(offs, np.concatenate([[0], np.cumsum(oln)]))
+    pk = packed.cpu().numpy()
+    for b in range(300):
+        np.testing.assert_array_equal(pk[offs[b]:offs[b + 1]], otn[b, :oln[b]])
+    st, s = ver.stats()
+    kb = inp["draft_len"].cpu().numpy()
+    assert st == svp.SV_OK
+    assert s["sequences"] == 300 and s["emitted"] == oln.sum()
+    assert s["drafts_proposed"] == kb.sum() and s["drafts_accepted"] == (oln - 1).sum()
+    assert s["spec_off"] == (kb == 0).sum()
+    assert abs(s["mean_emitted"] - oln.mean()) < 1e-12
+
+
+def test_wait_timeout_is_reported_not_hung():
+    inp = small("ragged", B=16, k=3, V=65536)
+    ver = verifier_for(inp)
+    ver.reset_stats()
+    ver.set_wait_limit_ns(0)
+    toks, lens = run_gpu(ver, inp)
+    st, s = ver.stats()
+    assert s["error_bits"] & (1 << svp.SV_ERR_TIMEOUT)
+    assert st == svp.SV_ERR_TIMEOUT
+    timed_out = lens == 0
+    assert timed_out.any()
+    assert (toks[timed_out] == -1).all()
+    # restoring the limit restores parity
+    ver.set_wait_limit_ns(-1)
+    ver.reset_stats()
+    assert_parity(inp, ver)
+
+
+# --- full-size workloads: invariants everywhere, oracle on sampled sequences ----
+
+@pytest.mark.parametrize("name", ["qwen_b32", "ragged", "ragged_dense", "long_draft", "grpo"])
+def test_full_size_workload(name):
+    w = get_workload(name)
+    inp = make_inputs(w, device=DEV)
+    ver = verifier_for(inp)
+    ver.reset_stats()
+    toks, lens = run_gpu(ver, inp)
+    kb = inp["draft_len"].cpu().numpy()
+    check_invariants(toks, lens, kb, inp["tokens"].cpu().numpy(), w.V)
+    st, s = ver.stats()
+    assert st == svp.SV_OK and s["sequences"] == w.B and s["emitted"] == lens.sum()
+    rng = np.random.default_rng(0)
+    n = min(w.B, 32)
+    idx = np.sort(rng.choice(w.B, n, replace=False))
+    idx_t = torch.from_numpy(idx).to(DEV)
+    ref = run_oracle(inp, idx_t)
+    res = compare(toks[idx], lens[idx], ref, kb[idx])
+    assert res["mismatch"] == 0, res["bad"]
+    dbg = ver.debug(w.B, w.k)
+    sub = {k: v[idx_t] for k, v in dbg.items()}
+    worst = compare_diagnostics(sub, ref, kb[idx], lens[idx])
+    assert worst["lse"] < RTOL and worst["alpha"] < RTOL and worst["mass"] < RTOL, worst
+
+
+# --- statistical closed forms on the GPU (>= 1e6 draws) ------------------------------
+
+def test_acceptance_rate_and_token_law_on_gpu():
+    rng = np.random.default_rng(13)
+    B, k, V, T = 262_144, 3, 16, 1.0
+    base_t = rng.normal(0, 1.0, (k + 1, V)).astype(np.float32)
+    base_d = (base_t[:k] + rng.normal(0, 0.8, (k, V))).astype(np.float32)
+    t = torch.from_numpy(base_t).to(DEV).expand(B, k + 1, V).contiguous()
+    d = torch.from_numpy(base_d).to(DEV).expand(B, k, V).contiguous()
+    g = torch.Generator(device=DEV).manual_seed(3)
+    tok = gumbel_argmax_tokens(d.view(B * k, V), T, g, chunk=1 << 16).view(B, k)
+    u = torch.from_numpy(philox_uniforms(B * (k + 1), seed=12).reshape(B, k + 1)).to(DEV)
+    kl = torch.full((B,), k, dtype=torch.int32, device=DEV)
+    ver = svp.SpecVerifier(B, k, V, torch.float32)
+    toks, lens = run_gpu(ver, {"target": t, "draft": d, "tokens": tok, "draft_len": kl, "uniforms": u, "T": T})
+    p = softmax(base_t.astype(np.float64) / T, axis=1)
+    q = softmax(base_d.astype(np.float64) / T, axis=1)
+    alpha = np.minimum(p[:k], q).sum(axis=1)
+    a = lens - 1
+    acc0 = (a >= 1).mean()
+    assert abs(acc0 - alpha[0]) < 5 * np.sqrt(alpha[0] * (1 - alpha[0]) / B)
+    ea = sum(np.prod(alpha[:j]) for j in range(1, k + 1))
+    assert abs(a.mean() - ea) < 5 * a.std() / np.sqrt(B)
+    for pos in (0, 1, 2):
+        sel = lens > pos
+        counts = np.bincount(toks[sel, pos], minlength=V)
+        _, pval = sstats.chisquare(counts, p[pos] * sel.sum())
+        assert pval > 1e-4, (pos, pval)
