@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cluster-size", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=2)
     ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
     return ap.parse_args()
 
@@ -252,7 +253,7 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
     nbytes = algorithmic_bytes(kb, w.k, w.V, w.elt)
     ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
     if args.cluster_size:
-        ver.set_cluster_size(args.cluster_size)
+        ver.set_pipeline(args.cluster_size, args.stages)
     outs = [(torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device),
              torch.empty(w.B, dtype=torch.int32, device=device)) for _ in range(rotate)]
 
@@ -410,6 +411,7 @@ def our_arm(args, w):
                    "algorithmic_bytes_per_step": m["bytes"],
                    "l2": f"{args.rotate} rotating copies of the inputs (each larger than the 129 MB L2)",
                    "parallelism": f"replicas{world}", "cluster_size": m["cfg"]["cluster_size"],
+                   "stages": m["cfg"]["stages"], "clusters": m["cfg"]["max_active_clusters"],
                    "threads": m["cfg"]["threads"], "smem_bytes": m["cfg"]["smem_bytes"]},
         "gbs": gbs_step, "frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",

@@ -175,17 +175,23 @@ sv_status spec_verify_stats(sv_ctx *ctx, sv_stream_t stream, sv_stats *out);
 /* Clear the counters and the device error word (asynchronous on `stream`). */
 sv_status spec_verify_reset_stats(sv_ctx *ctx, sv_stream_t stream);
 
-/* Tuning and introspection.  sv_set_cluster_size picks how many CTAs (1, 2,
- * 4, 8 or 16) share one target/draft row pair; 0 restores the automatic
- * choice.  sv_get_config reports the current launch shape. */
-sv_status sv_set_cluster_size(sv_ctx *ctx, int cluster_size);
-sv_status sv_get_config(const sv_ctx *ctx, int *cluster_size, int *threads,
+/* Tuning and introspection.  sv_set_pipeline picks how many CTAs (1, 2, 4,
+ * 8 or 16) split one row's vocabulary (the cluster size) and how many
+ * shared-memory staging buffers (2..4) each CTA keeps, so that the rows of the
+ * next items are being copied while the current one is computed; (0, 0)
+ * restores the automatic choice.  Returns SV_ERR_UNSUPPORTED, keeping the
+ * previous shape, when the shape cannot be launched.  sv_get_config reports
+ * the current shape and how many clusters the persistent grid runs (any
+ * output pointer may be NULL). */
+sv_status sv_set_pipeline(sv_ctx *ctx, int cluster_size, int stages);
+sv_status sv_get_config(const sv_ctx *ctx, int *cluster_size, int *stages, int *threads,
                         int *smem_bytes, int *max_active_clusters);
 
 /* Test hook: the limit, in nanoseconds, of each bounded wait for staged logits
- * (default 1 s; 0 makes every wait that is not already complete expire and
- * report SV_ERR_TIMEOUT; the data is then still drained before the CTA
- * moves on).  Negative restores the default. */
+ * (default 1 s).  0 makes every wait report expiry, so every sequence that
+ * reads a row ends with SV_ERR_TIMEOUT; the copies are still drained (with a
+ * 1 s bound) before the shared memory is reused.  Negative restores the
+ * default. */
 sv_status sv_set_wait_limit_ns(sv_ctx *ctx, long long ns);
 
 #ifdef __cplusplus

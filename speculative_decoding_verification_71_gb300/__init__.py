@@ -38,7 +38,7 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
-    "sv_set_cluster_size", "sv_get_config", "sv_set_wait_limit_ns",
+    "sv_set_pipeline", "sv_get_config", "sv_set_wait_limit_ns",
 )
 
 
@@ -96,10 +96,10 @@ def load_library(path: str | None = None):
     lib.spec_verify_stats.argtypes = [P, P, c.POINTER(Stats)]
     lib.spec_verify_reset_stats.restype = c.c_int
     lib.spec_verify_reset_stats.argtypes = [P, P]
-    lib.sv_set_cluster_size.restype = c.c_int
-    lib.sv_set_cluster_size.argtypes = [P, c.c_int]
+    lib.sv_set_pipeline.restype = c.c_int
+    lib.sv_set_pipeline.argtypes = [P, c.c_int, c.c_int]
     lib.sv_get_config.restype = c.c_int
-    lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 4
+    lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 5
     lib.sv_set_wait_limit_ns.restype = c.c_int
     lib.sv_set_wait_limit_ns.argtypes = [P, c.c_longlong]
     if path is None:
@@ -254,10 +254,11 @@ class SpecVerifier:
         if st != SV_OK:
             self._raise(st, "spec_verify_reset_stats")
 
-    def set_cluster_size(self, cs: int):
-        st = self.lib.sv_set_cluster_size(self._ctx, int(cs))
+    def set_pipeline(self, cluster_size: int, stages: int = 2):
+        """Cluster size (CTAs per row) and staging buffers per CTA; (0, 0) = automatic."""
+        st = self.lib.sv_set_pipeline(self._ctx, int(cluster_size), int(stages))
         if st != SV_OK:
-            self._raise(st, "sv_set_cluster_size")
+            self._raise(st, "sv_set_pipeline")
 
     def set_wait_limit_ns(self, ns: int):
         st = self.lib.sv_set_wait_limit_ns(self._ctx, int(ns))
@@ -265,9 +266,9 @@ class SpecVerifier:
             self._raise(st, "sv_set_wait_limit_ns")
 
     def config(self):
-        vals = [ctypes.c_int() for _ in range(4)]
+        vals = [ctypes.c_int() for _ in range(5)]
         st = self.lib.sv_get_config(self._ctx, *[ctypes.byref(v) for v in vals])
         if st != SV_OK:
             self._raise(st, "sv_get_config")
-        return dict(zip(("cluster_size", "threads", "smem_bytes", "max_active_clusters"),
+        return dict(zip(("cluster_size", "stages", "threads", "smem_bytes", "max_active_clusters"),
                         (v.value for v in vals)))

@@ -21,6 +21,7 @@ struct sv_ctx {
   int elt = 2;
   int device = 0;
   int cluster = 1;
+  int stages = 2;
   int slice = 0;
   int smem_bytes = 0;
   int max_active_clusters = 0;
@@ -50,10 +51,11 @@ int slice_for(int V, int cluster) {
   return ((per + 7) / 8) * 8;
 }
 
-// Configure for a cluster size; fails if the shape cannot be launched.
-sv_status configure(sv_ctx* ctx, int cluster) {
+// Configure for a cluster size and a number of staging buffers; fails if
+// the shape cannot be launched.
+sv_status configure(sv_ctx* ctx, int cluster, int stages) {
   const int slice = slice_for(ctx->V, cluster);
-  const int smem = sv::verify_smem_bytes(slice, ctx->elt, true);
+  const int smem = sv::verify_smem_bytes(slice, ctx->elt, stages);
   cudaDeviceProp prop;
   cudaError_t e = cudaGetDeviceProperties(&prop, ctx->device);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDeviceProperties");
@@ -68,25 +70,26 @@ sv_status configure(sv_ctx* ctx, int cluster) {
   }
   if (active <= 0) return SV_ERR_UNSUPPORTED;
   ctx->cluster = cluster;
+  ctx->stages = stages;
   ctx->slice = slice;
   ctx->smem_bytes = smem;
   ctx->max_active_clusters = active;
   return SV_OK;
 }
 
-// Automatic choice: the smallest cluster whose per-CTA slice pair fits in
-// about 48 KB of shared memory, so that several CTAs share each SM and one
-// CTA's staging overlaps another's arithmetic.
+// Automatic choice: two staging buffers, and the smallest cluster whose
+// per-CTA buffers fit in about 80 KB of shared memory, so that two or more
+// CTAs share each SM.
 sv_status configure_auto(sv_ctx* ctx) {
   const int sizes[5] = {1, 2, 4, 8, 16};
   for (int i = 0; i < 5; ++i) {
     const int cs = sizes[i];
-    const int smem = sv::verify_smem_bytes(slice_for(ctx->V, cs), ctx->elt, true);
-    if (smem > 48 * 1024 && cs < 16) continue;
-    if (configure(ctx, cs) == SV_OK) return SV_OK;
+    const int smem = sv::verify_smem_bytes(slice_for(ctx->V, cs), ctx->elt, 2);
+    if (smem > 80 * 1024 && cs < 16) continue;
+    if (configure(ctx, cs, 2) == SV_OK) return SV_OK;
   }
   for (int i = 4; i >= 0; --i)
-    if (configure(ctx, sizes[i]) == SV_OK) return SV_OK;
+    if (configure(ctx, sizes[i], 2) == SV_OK) return SV_OK;
   return SV_ERR_UNSUPPORTED;
 }
 
@@ -148,6 +151,7 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
   auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
   const size_t o_done = take(nB * 4), o_rej = take(nB * 4), o_err = take(nB * 4);
   const size_t o_y = take(nT * 4), o_mt = take(nT * 4), o_Lt = take(nT * 4);
+  const size_t o_items = take(nT * 8), o_nitems = take(4), o_ticket = take(4);
   const size_t o_md = take(nD * 4), o_Ld = take(nD * 4), o_al = take(nD * 4), o_mass = take(nT * 4);
   const size_t o_stats = take(sv::kStatCount * 8), o_word = take(4);
   e = cudaMalloc(&ctx->ws_mem, off);
@@ -162,6 +166,9 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
   ws.rej_min = reinterpret_cast<int*>(base + o_rej);
   ws.seq_err = reinterpret_cast<int*>(base + o_err);
   ws.y_slot = reinterpret_cast<int*>(base + o_y);
+  ws.items = reinterpret_cast<int2*>(base + o_items);
+  ws.n_items = reinterpret_cast<int*>(base + o_nitems);
+  ws.ticket = reinterpret_cast<int*>(base + o_ticket);
   ws.m_t = reinterpret_cast<float*>(base + o_mt);
   ws.L_t = reinterpret_cast<float*>(base + o_Lt);
   ws.m_d = reinterpret_cast<float*>(base + o_md);
@@ -227,11 +234,16 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   p.greedy = greedy ? 1 : 0;
   p.c2 = static_cast<float>(c2);
   p.slice = ctx->slice;
+  p.stages = ctx->stages;
   p.bulk = ((static_cast<long long>(ctx->V) * ctx->elt) % 16 == 0) && aligned16(target_logits) &&
            (draft_logits == nullptr || aligned16(draft_logits));
   p.wait_limit_ns = ctx->wait_limit_ns;
   p.ws = ctx->ws;
-  cudaError_t e = sv::launch_verify(p, ctx->cluster, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
+  // persistent grid: as many clusters as fit at once, but never more than items
+  const long long items_max = static_cast<long long>(B) * (k + 1);
+  const int clusters = static_cast<int>(items_max < ctx->max_active_clusters ? items_max : ctx->max_active_clusters);
+  cudaError_t e = sv::launch_verify(p, ctx->cluster, clusters, ctx->smem_bytes,
+                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch verify");
   ctx->calls += 1;
   ctx->last_B = B;
@@ -254,7 +266,7 @@ sv_status spec_verify_debug(sv_ctx* ctx, int B, int k, double* lse_t, double* ls
                             double* mass, sv_stream_t stream) {
   if (!ctx || ctx->calls == 0) return SV_ERR_INVALID_ARG;
   if (B != ctx->last_B || k != ctx->last_k) return SV_ERR_INVALID_ARG;
-  cudaError_t e = sv::launch_debug(ctx->ws, B, k, nullptr, ctx->last_greedy, ctx->last_inv_T, lse_t, lse_d,
+  cudaError_t e = sv::launch_debug(ctx->ws, B, k, ctx->last_greedy, ctx->last_inv_T, lse_t, lse_d,
                                    accept_prob, mass, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SV_OK : cuda_fail(ctx, e, "launch debug");
 }
@@ -299,21 +311,23 @@ sv_status spec_verify_reset_stats(sv_ctx* ctx, sv_stream_t stream) {
   return SV_OK;
 }
 
-sv_status sv_set_cluster_size(sv_ctx* ctx, int cluster_size) {
+sv_status sv_set_pipeline(sv_ctx* ctx, int cluster_size, int stages) {
   if (!ctx) return SV_ERR_INVALID_ARG;
-  if (cluster_size == 0) return configure_auto(ctx);
+  if (cluster_size == 0 && stages == 0) return configure_auto(ctx);
   if (cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8 && cluster_size != 16)
     return SV_ERR_INVALID_ARG;
-  const int prev = ctx->cluster;
-  sv_status s = configure(ctx, cluster_size);
-  if (s != SV_OK) configure(ctx, prev);
+  if (stages < 2 || stages > sv::kMaxStages) return SV_ERR_INVALID_ARG;
+  const int prev_c = ctx->cluster, prev_s = ctx->stages;
+  sv_status s = configure(ctx, cluster_size, stages);
+  if (s != SV_OK) configure(ctx, prev_c, prev_s);
   return s;
 }
 
-sv_status sv_get_config(const sv_ctx* ctx, int* cluster_size, int* threads, int* smem_bytes,
+sv_status sv_get_config(const sv_ctx* ctx, int* cluster_size, int* stages, int* threads, int* smem_bytes,
                         int* max_active_clusters) {
   if (!ctx) return SV_ERR_INVALID_ARG;
   if (cluster_size) *cluster_size = ctx->cluster;
+  if (stages) *stages = ctx->stages;
   if (threads) *threads = sv::kThreads;
   if (smem_bytes) *smem_bytes = ctx->smem_bytes;
   if (max_active_clusters) *max_active_clusters = ctx->max_active_clusters;
