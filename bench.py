@@ -55,8 +55,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--cluster-size", type=int, default=0)
-    ap.add_argument("--stages", type=int, default=2)
+    ap.add_argument("--stages", type=int, default=0, help="staging slots per CTA (0 = automatic)")
+    ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
     return ap.parse_args()
 
@@ -252,8 +252,8 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
     positions = int(np.sum(kb + 1))
     nbytes = algorithmic_bytes(kb, w.k, w.V, w.elt)
     ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
-    if args.cluster_size:
-        ver.set_pipeline(args.cluster_size, args.stages)
+    if args.stages or args.ctas_per_sm:
+        ver.set_pipeline(args.stages or 3, args.ctas_per_sm)
     outs = [(torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device),
              torch.empty(w.B, dtype=torch.int32, device=device)) for _ in range(rotate)]
 
@@ -410,8 +410,8 @@ def our_arm(args, w):
                    "verified_positions_per_step": m["positions"],
                    "algorithmic_bytes_per_step": m["bytes"],
                    "l2": f"{args.rotate} rotating copies of the inputs (each larger than the 129 MB L2)",
-                   "parallelism": f"replicas{world}", "cluster_size": m["cfg"]["cluster_size"],
-                   "stages": m["cfg"]["stages"], "clusters": m["cfg"]["max_active_clusters"],
+                   "parallelism": f"replicas{world}", "stages": m["cfg"]["stages"],
+                   "ctas_per_sm": m["cfg"]["ctas_per_sm"], "grid_ctas": m["cfg"]["grid_ctas"],
                    "threads": m["cfg"]["threads"], "smem_bytes": m["cfg"]["smem_bytes"]},
         "gbs": gbs_step, "frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",

@@ -104,6 +104,7 @@ const char *sv_last_cuda_error(const sv_ctx *ctx);
  * each, vocabulary V and logit dtype `dtype`, on the current CUDA device.
  * Allocates the fixed device workspace (O(max_B * (max_k + 1)) words) and
  * chooses the launch configuration.  *ctx receives the handle.
+ * Limits: max_k <= 31; V * sizeof(dtype) <= 1 MiB.
  * Errors: SV_ERR_INVALID_ARG (sizes <= 0 or too large, NULL ctx),
  * SV_ERR_UNSUPPORTED (no sm_100-family device), SV_ERR_CUDA. */
 sv_status sv_create(sv_ctx **ctx, int max_B, int max_k, int V, sv_dtype dtype);
@@ -175,17 +176,16 @@ sv_status spec_verify_stats(sv_ctx *ctx, sv_stream_t stream, sv_stats *out);
 /* Clear the counters and the device error word (asynchronous on `stream`). */
 sv_status spec_verify_reset_stats(sv_ctx *ctx, sv_stream_t stream);
 
-/* Tuning and introspection.  sv_set_pipeline picks how many CTAs (1, 2, 4,
- * 8 or 16) split one row's vocabulary (the cluster size) and how many
- * shared-memory staging buffers (2..4) each CTA keeps, so that the rows of the
- * next items are being copied while the current one is computed; (0, 0)
- * restores the automatic choice.  Returns SV_ERR_UNSUPPORTED, keeping the
- * previous shape, when the shape cannot be launched.  sv_get_config reports
- * the current shape and how many clusters the persistent grid runs (any
- * output pointer may be NULL). */
-sv_status sv_set_pipeline(sv_ctx *ctx, int cluster_size, int stages);
-sv_status sv_get_config(const sv_ctx *ctx, int *cluster_size, int *stages, int *threads,
-                        int *smem_bytes, int *max_active_clusters);
+/* Tuning and introspection.  Each CTA streams whole sequences through a ring
+ * of 16 KB shared-memory slots; sv_set_pipeline picks the number of slots
+ * (2..16) and how many CTAs share an SM (0: as many as fit); (0, 0) restores
+ * the automatic choice.  Returns SV_ERR_UNSUPPORTED, keeping the previous
+ * shape, when the shape cannot be launched.  sv_get_config reports the current
+ * shape and the size of the persistent grid (any output pointer may be
+ * NULL). */
+sv_status sv_set_pipeline(sv_ctx *ctx, int stages, int ctas_per_sm);
+sv_status sv_get_config(const sv_ctx *ctx, int *stages, int *ctas_per_sm, int *threads,
+                        int *smem_bytes, int *grid_ctas);
 
 /* Test hook: the limit, in nanoseconds, of each bounded wait for staged logits
  * (default 1 s).  0 makes every wait report expiry, so every sequence that

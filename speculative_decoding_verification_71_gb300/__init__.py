@@ -254,9 +254,10 @@ class SpecVerifier:
         if st != SV_OK:
             self._raise(st, "spec_verify_reset_stats")
 
-    def set_pipeline(self, cluster_size: int, stages: int = 2):
-        """Cluster size (CTAs per row) and staging buffers per CTA; (0, 0) = automatic."""
-        st = self.lib.sv_set_pipeline(self._ctx, int(cluster_size), int(stages))
+    def set_pipeline(self, stages: int, ctas_per_sm: int = 0):
+        """Staging slots (16 KB each) per CTA and CTAs per SM (0 = as many as
+        fit); (0, 0) = automatic."""
+        st = self.lib.sv_set_pipeline(self._ctx, int(stages), int(ctas_per_sm))
         if st != SV_OK:
             self._raise(st, "sv_set_pipeline")
 
@@ -270,5 +271,5 @@ class SpecVerifier:
         st = self.lib.sv_get_config(self._ctx, *[ctypes.byref(v) for v in vals])
         if st != SV_OK:
             self._raise(st, "sv_get_config")
-        return dict(zip(("cluster_size", "stages", "threads", "smem_bytes", "max_active_clusters"),
+        return dict(zip(("stages", "ctas_per_sm", "threads", "smem_bytes", "grid_ctas"),
                         (v.value for v in vals)))

@@ -20,11 +20,10 @@ struct sv_ctx {
   sv_dtype dtype = SV_BF16;
   int elt = 2;
   int device = 0;
-  int cluster = 1;
-  int stages = 2;
-  int slice = 0;
+  int stages = 6;
+  int ctas_per_sm = 0;
+  int num_sms = 0;
   int smem_bytes = 0;
-  int max_active_clusters = 0;
   long long wait_limit_ns = sv::kDrainLimitNs;
   void* ws_mem = nullptr;
   sv::Workspace ws{};
@@ -46,51 +45,32 @@ sv_status cuda_fail(sv_ctx* ctx, cudaError_t e, const char* where) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int slice_for(int V, int cluster) {
-  const int per = (V + cluster - 1) / cluster;
-  return ((per + 7) / 8) * 8;
-}
-
-// Configure for a cluster size and a number of staging buffers; fails if
-// the shape cannot be launched.
-sv_status configure(sv_ctx* ctx, int cluster, int stages) {
-  const int slice = slice_for(ctx->V, cluster);
-  const int smem = sv::verify_smem_bytes(slice, ctx->elt, stages);
+// Configure the staging ring (slots of 16 KB per CTA) and how many CTAs
+// share an SM (0: as many as fit); fails if the shape cannot be launched.
+sv_status configure(sv_ctx* ctx, int stages, int ctas_per_sm) {
+  const int smem = sv::verify_smem_bytes(stages);
   cudaDeviceProp prop;
   cudaError_t e = cudaGetDeviceProperties(&prop, ctx->device);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDeviceProperties");
   if (smem > static_cast<int>(prop.sharedMemPerBlockOptin)) return SV_ERR_UNSUPPORTED;
-  e = sv::prepare_verify_kernel(smem, cluster);
+  e = sv::prepare_verify_kernel(smem);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute");
-  int active = 0;
-  e = sv::query_max_active_clusters(cluster, smem, &active);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return SV_ERR_UNSUPPORTED;
-  }
-  if (active <= 0) return SV_ERR_UNSUPPORTED;
-  ctx->cluster = cluster;
+  int fit = 0;
+  e = sv::query_ctas_per_sm(smem, &fit);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (fit <= 0) return SV_ERR_UNSUPPORTED;
+  if (ctas_per_sm > fit) return SV_ERR_UNSUPPORTED;
   ctx->stages = stages;
-  ctx->slice = slice;
+  ctx->ctas_per_sm = ctas_per_sm > 0 ? ctas_per_sm : fit;
+  ctx->num_sms = prop.multiProcessorCount;
   ctx->smem_bytes = smem;
-  ctx->max_active_clusters = active;
   return SV_OK;
 }
 
-// Automatic choice: two staging buffers, and the smallest cluster whose
-// per-CTA buffers fit in about 80 KB of shared memory, so that two or more
-// CTAs share each SM.
+// Automatic choice: three 64 KB slots per CTA, one CTA per SM.
 sv_status configure_auto(sv_ctx* ctx) {
-  const int sizes[5] = {1, 2, 4, 8, 16};
-  for (int i = 0; i < 5; ++i) {
-    const int cs = sizes[i];
-    const int smem = sv::verify_smem_bytes(slice_for(ctx->V, cs), ctx->elt, 2);
-    if (smem > 80 * 1024 && cs < 16) continue;
-    if (configure(ctx, cs, 2) == SV_OK) return SV_OK;
-  }
-  for (int i = 4; i >= 0; --i)
-    if (configure(ctx, sizes[i], 2) == SV_OK) return SV_OK;
-  return SV_ERR_UNSUPPORTED;
+  if (configure(ctx, 3, 0) == SV_OK) return SV_OK;
+  return configure(ctx, 2, 0);
 }
 
 }  // namespace
@@ -120,7 +100,9 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
   // per-call index arithmetic is 32-bit in cluster ids and 64-bit in bytes
   if (static_cast<long long>(max_B) * (max_k + 1) > (1LL << 26)) return SV_ERR_INVALID_ARG;
-  if (max_k > 4096) return SV_ERR_INVALID_ARG;
+  if (max_k > 31) return SV_ERR_INVALID_ARG;              // one warp lane per position
+  const long long row_bytes = static_cast<long long>(V) * (dtype == SV_F32 ? 4 : 2);
+  if (row_bytes > static_cast<long long>(sv::kMaxChunks) * sv::kChunkBytes) return SV_ERR_INVALID_ARG;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -149,9 +131,8 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
   const size_t nD = nB * (max_k > 0 ? max_k : 1);
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
-  const size_t o_done = take(nB * 4), o_rej = take(nB * 4), o_err = take(nB * 4);
-  const size_t o_y = take(nT * 4), o_mt = take(nT * 4), o_Lt = take(nT * 4);
-  const size_t o_items = take(nT * 8), o_nitems = take(4), o_ticket = take(4);
+  const size_t o_seqs = take(nB * 8), o_nseqs = take(4), o_ticket = take(4);
+  const size_t o_mt = take(nT * 4), o_Lt = take(nT * 4);
   const size_t o_md = take(nD * 4), o_Ld = take(nD * 4), o_al = take(nD * 4), o_mass = take(nT * 4);
   const size_t o_stats = take(sv::kStatCount * 8), o_word = take(4);
   e = cudaMalloc(&ctx->ws_mem, off);
@@ -162,12 +143,8 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
   }
   char* base = static_cast<char*>(ctx->ws_mem);
   sv::Workspace& ws = ctx->ws;
-  ws.done = reinterpret_cast<int*>(base + o_done);
-  ws.rej_min = reinterpret_cast<int*>(base + o_rej);
-  ws.seq_err = reinterpret_cast<int*>(base + o_err);
-  ws.y_slot = reinterpret_cast<int*>(base + o_y);
-  ws.items = reinterpret_cast<int2*>(base + o_items);
-  ws.n_items = reinterpret_cast<int*>(base + o_nitems);
+  ws.seqs = reinterpret_cast<int2*>(base + o_seqs);
+  ws.n_seqs = reinterpret_cast<int*>(base + o_nseqs);
   ws.ticket = reinterpret_cast<int*>(base + o_ticket);
   ws.m_t = reinterpret_cast<float*>(base + o_mt);
   ws.L_t = reinterpret_cast<float*>(base + o_Lt);
@@ -179,7 +156,7 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
   ws.err_word = reinterpret_cast<unsigned int*>(base + o_word);
 
   e = cudaMemset(ctx->ws_mem, 0, off);
-  if (e == cudaSuccess) e = sv::launch_init_workspace(ws, max_B, nullptr);
+  if (e == cudaSuccess) e = sv::launch_init_workspace(ws, nullptr);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     sv_status s = cuda_fail(nullptr, e, "workspace init");
@@ -189,7 +166,7 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
   }
   sv_status s = configure_auto(ctx);
   if (s != SV_OK) {
-    std::snprintf(g_create_msg, sizeof g_create_msg, "no launchable cluster shape for V=%d", V);
+    std::snprintf(g_create_msg, sizeof g_create_msg, "no launchable shape for V=%d", V);
     cudaFree(ctx->ws_mem);
     delete ctx;
     return s;
@@ -233,17 +210,15 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   p.elt = ctx->elt;
   p.greedy = greedy ? 1 : 0;
   p.c2 = static_cast<float>(c2);
-  p.slice = ctx->slice;
   p.stages = ctx->stages;
   p.bulk = ((static_cast<long long>(ctx->V) * ctx->elt) % 16 == 0) && aligned16(target_logits) &&
            (draft_logits == nullptr || aligned16(draft_logits));
   p.wait_limit_ns = ctx->wait_limit_ns;
   p.ws = ctx->ws;
-  // persistent grid: as many clusters as fit at once, but never more than items
-  const long long items_max = static_cast<long long>(B) * (k + 1);
-  const int clusters = static_cast<int>(items_max < ctx->max_active_clusters ? items_max : ctx->max_active_clusters);
-  cudaError_t e = sv::launch_verify(p, ctx->cluster, clusters, ctx->smem_bytes,
-                                    reinterpret_cast<cudaStream_t>(stream));
+  // persistent grid: every CTA that fits at once, but never more than sequences
+  const int fit = ctx->num_sms * ctx->ctas_per_sm;
+  const int ctas = B < fit ? B : fit;
+  cudaError_t e = sv::launch_verify(p, ctas, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch verify");
   ctx->calls += 1;
   ctx->last_B = B;
@@ -311,26 +286,24 @@ sv_status spec_verify_reset_stats(sv_ctx* ctx, sv_stream_t stream) {
   return SV_OK;
 }
 
-sv_status sv_set_pipeline(sv_ctx* ctx, int cluster_size, int stages) {
+sv_status sv_set_pipeline(sv_ctx* ctx, int stages, int ctas_per_sm) {
   if (!ctx) return SV_ERR_INVALID_ARG;
-  if (cluster_size == 0 && stages == 0) return configure_auto(ctx);
-  if (cluster_size != 1 && cluster_size != 2 && cluster_size != 4 && cluster_size != 8 && cluster_size != 16)
-    return SV_ERR_INVALID_ARG;
-  if (stages < 2 || stages > sv::kMaxStages) return SV_ERR_INVALID_ARG;
-  const int prev_c = ctx->cluster, prev_s = ctx->stages;
-  sv_status s = configure(ctx, cluster_size, stages);
-  if (s != SV_OK) configure(ctx, prev_c, prev_s);
+  if (stages == 0 && ctas_per_sm == 0) return configure_auto(ctx);
+  if (stages < 2 || stages > sv::kMaxStages || ctas_per_sm < 0) return SV_ERR_INVALID_ARG;
+  const int prev_s = ctx->stages, prev_c = ctx->ctas_per_sm;
+  sv_status s = configure(ctx, stages, ctas_per_sm);
+  if (s != SV_OK) configure(ctx, prev_s, prev_c);
   return s;
 }
 
-sv_status sv_get_config(const sv_ctx* ctx, int* cluster_size, int* stages, int* threads, int* smem_bytes,
-                        int* max_active_clusters) {
+sv_status sv_get_config(const sv_ctx* ctx, int* stages, int* ctas_per_sm, int* threads, int* smem_bytes,
+                        int* grid_ctas) {
   if (!ctx) return SV_ERR_INVALID_ARG;
-  if (cluster_size) *cluster_size = ctx->cluster;
   if (stages) *stages = ctx->stages;
+  if (ctas_per_sm) *ctas_per_sm = ctx->ctas_per_sm;
   if (threads) *threads = sv::kThreads;
   if (smem_bytes) *smem_bytes = ctx->smem_bytes;
-  if (max_active_clusters) *max_active_clusters = ctx->max_active_clusters;
+  if (grid_ctas) *grid_ctas = ctx->num_sms * ctx->ctas_per_sm;
   return SV_OK;
 }
 

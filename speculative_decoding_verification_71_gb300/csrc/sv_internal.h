@@ -6,12 +6,14 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;           // threads per CTA of the verify kernel
-constexpr int kMaxCluster = 16;         // largest cluster (non-portable size)
-constexpr int kMaxStages = 4;           // staging buffers per CTA
-constexpr int kNoReject = 0x7fffffff;   // "no rejection seen" in rej_min
-constexpr int kCtrlBytes = 2048;        // control block at the start of shared memory
-constexpr long long kDrainLimitNs = 1000000000LL;  // second wait: always 1 s
+constexpr int kConsumerWarps = 16;                      // warps that compute
+constexpr int kThreads = (kConsumerWarps + 1) * 32;     // + one producer warp
+constexpr int kVecsPerLane = 8;                         // 16-byte vectors per lane and chunk
+constexpr int kVecsPerWarp = kVecsPerLane * 32;         // 256 x 16 B per warp and chunk
+constexpr int kChunkBytes = kVecsPerWarp * 16 * kConsumerWarps;  // one staging slot: 64 KB
+constexpr int kMaxChunks = 16;                          // rows up to 1 MiB
+constexpr int kMaxStages = 16;                          // staging slots per CTA
+constexpr long long kDrainLimitNs = 1000000000LL;       // second wait: always 1 s
 
 // Counters kept on the device (unsigned long long each).
 enum StatSlot {
@@ -25,15 +27,10 @@ enum StatSlot {
   kStatCount
 };
 
-// Workspace owned by the context.  The plan kernel that starts every call
-// resets the per-sequence words and the ticket counter.
+// Workspace owned by the context.
 struct Workspace {
-  int* done;        // [max_B]   items of the sequence finished so far
-  int* rej_min;     // [max_B]   smallest rejecting draft index, kNoReject if none
-  int* seq_err;     // [max_B]   OR of (1 << code) for the sequence
-  int* y_slot;      // [max_B * (max_k + 1)]  token drawn at each position
-  int2* items;      // [max_B * (max_k + 1)]  work list: {b, (pos << 1) | is_pair}
-  int* n_items;     // [1]       entries in the work list
+  int2* seqs;       // [max_B]   work list {b, k_b}, longest first
+  int* n_seqs;      // [1]       entries in the work list
   int* ticket;      // [1]       next work-list entry to hand out
   float* m_t;       // [max_B * (max_k + 1)]  target row maximum (debug)
   float* L_t;       // [max_B * (max_k + 1)]  log2 sum 2^(z c - fl(m c)) (debug)
@@ -57,28 +54,23 @@ struct VerifyParams {
   int elt;              // bytes per logit: 4 (fp32) or 2 (bf16)
   int greedy;           // T == 0
   float c2;             // log2(e) / T
-  int slice;            // logits per CTA (multiple of 8)
-  int stages;           // staging buffers per CTA (2..kMaxStages)
+  int stages;           // staging slots per CTA (2..kMaxStages)
   int bulk;             // 1: rows staged with cp.async.bulk; 0: plain loads
   long long wait_limit_ns;
   Workspace ws;
 };
 
 // Launchers (sv_kernels.cu).
-cudaError_t launch_verify(const VerifyParams& p, int cluster, int clusters, int smem_bytes, cudaStream_t s);
-cudaError_t prepare_verify_kernel(int smem_bytes, int cluster);
-cudaError_t query_max_active_clusters(int cluster, int smem_bytes, int* out);
+cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s);
+cudaError_t prepare_verify_kernel(int smem_bytes);
+cudaError_t query_ctas_per_sm(int smem_bytes, int* out);
 cudaError_t launch_compact(int B, int k, const int* out_tokens, const int* out_len,
                            int* packed, int* offsets, cudaStream_t s);
 cudaError_t launch_debug(const Workspace& ws, int B, int k, int greedy, float inv_T, double* lse_t,
                          double* lse_d, double* accept_prob, double* mass, cudaStream_t s);
-cudaError_t launch_init_workspace(const Workspace& ws, int max_B, cudaStream_t s);
+cudaError_t launch_init_workspace(const Workspace& ws, cudaStream_t s);
 
-// Shared-memory bytes the verify kernel needs for `stages` buffers of a
-// target/draft slice pair of `slice` logits each.
-inline int row_bytes_padded(int slice, int elt) { return ((slice * elt + 127) / 128) * 128; }
-inline int verify_smem_bytes(int slice, int elt, int stages) {
-  return kCtrlBytes + stages * 2 * row_bytes_padded(slice, elt);
-}
+// Shared-memory bytes of the verify kernel with `stages` staging slots.
+int verify_smem_bytes(int stages);
 
 }  // namespace sv

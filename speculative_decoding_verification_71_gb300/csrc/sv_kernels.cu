@@ -1,34 +1,33 @@
 // Speculative-sampling verification kernels for sm_103a.
 //
-// Work unit ("item"): a (target row i, draft row i) pair of sequence b with
-// i < k_b, or the bonus target row k_b of sequence b.
+// verify_kernel is persistent and warp-specialised.  Each CTA verifies whole
+// sequences, one after another, taking them from a work list ordered longest
+// first (plan_kernel) with an atomic ticket:
 //
-// plan_kernel (one CTA) lists the items position-major (every sequence's
-// position 0, then position 1, ..., then all bonus rows), resets the
-// per-sequence words and the ticket counter, and handles sequences whose
-// draft length is invalid.
+//   producer warp   streams the sequence's rows in position order (target 0,
+//                   draft 0, target 1, draft 1, ..., target k_b) through a
+//                   ring of 16 KB shared-memory slots with cp.async.bulk, and
+//                   runs ahead into the next sequence while the consumers
+//                   are busy, so HBM reads never wait on arithmetic;
+//   8 consumer warps  fold every 16 KB chunk into per-warp running maxima and
+//                   sums of 2^(z c - fl(m c)), c = log2(e)/T (one ex2 per
+//                   logit), pick up the drafted token's logit, and at each
+//                   row end combine the warps into the row's log-sum-exp.
 //
-// verify_kernel is persistent: each thread-block CLUSTER pulls items with an
-// atomic ticket and its CTAs split the vocabulary.  Every CTA keeps `stages`
-// shared-memory buffers; while it computes on one item, cp.async.bulk is
-// already staging the rows of the next ones, so each needed logit crosses
-// HBM exactly once and the copy engine never idles.  Per item:
-//
-//   local    slice maximum m_r and sum s_r = sum 2^(z c - fl(m_r c)),
-//            c = log2(e)/T, plus the drafted token's logits
-//   barrier  cluster combine through distributed shared memory:
-//            M = max m_r, S = sum s_r 2^(fl(m_r c) - fl(M c))
-//   test     alpha = min(1, p(x)/q(x)); accept iff u < alpha
-//   draw     (rejected pair: w = max(0, p - q); bonus row: w = p)
-//            per-warp totals -> barrier -> cluster scan in rank order ->
-//            the CTA holding s*S walks its warp's chunk to the token
-//
-// Items of one sequence run in different clusters; the last one to finish
-// (threadfence + atomic counter, no waiting) writes the sequence's outputs.
-// A rejecting pair does atomicMin on its sequence's first-rejection word and
-// skips its draw when an earlier position already rejected; the bonus row
-// skips its draw when any rejection is known.  Position-major order makes
-// earlier positions finish first, so most useless draws are skipped.
+// Because one CTA sees the positions of a sequence in order, the first
+// rejection is known exactly:
+//   * after draft row i: alpha_i = min(1, p_i(x_i) / q_i(x_i)); accept iff
+//     u_i < alpha_i (every position's alpha is kept for diagnostics);
+//   * at the first rejection a: the pair (target a, draft a), read moments
+//     ago and still in L2, is read again to get exact per-segment masses of
+//     max(0, p - q); a warp scan finds the segment holding s*S and one warp
+//     walks that segment to the drawn token;
+//   * if every draft is accepted, the bonus row needs no second read at
+//     all: its per-segment sums were kept while streaming, so only the one
+//     segment holding s*S is read again.
+// Every needed logit crosses HBM once; the only extra reads are the rejected
+// pair (from L2) and one segment.  The CTA writes the sequence's outputs
+// itself: no atomics on the data path and no waiting on other CTAs.
 //
 // The rule implemented (accept with min(1, p/q), stop at the first
 // rejection, resample from max(0, p - q) or draw the bonus token from the
@@ -54,58 +53,16 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t remote_addr(const void* local, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(local)), "r"(rank));
-  return out;
-}
-
-__device__ __forceinline__ float ld_remote_f32(const void* local, uint32_t rank) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote_addr(local, rank)) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ double ld_remote_f64(const void* local, uint32_t rank) {
-  double v;
-  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(remote_addr(local, rank)) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int ld_remote_s32(const void* local, uint32_t rank) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote_addr(local, rank)) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_remote_s32(void* local, uint32_t rank, int v) {
-  asm volatile("st.shared::cluster.s32 [%0], %1;" :: "r"(remote_addr(local, rank)), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_fence_init() {
+__device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -124,8 +81,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Global -> shared bulk copy completing on `bar` (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// The same with an L2 eviction-priority policy (for rows never read again).
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+               :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -134,13 +104,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Programmatic dependent launch: wait until the preceding grid's writes are
-// visible / let the dependent grid start launching.
+// Programmatic dependent launch: wait for the preceding grid's results / let
+// the dependent grid start its prologue.
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Barrier of the consumer warps only (the producer never joins it).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" :: "n"(kConsumerWarps * 32) : "memory");
 }
 
 // 2^x on the special-function unit (PTX ex2.approx; -inf -> +0, NaN -> NaN).
@@ -150,9 +125,41 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic: two lanes, one
+// instruction, each lane rounded exactly as the scalar operation).
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pack2(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(f2 r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 exp2_2(f2 t) {
+  float a, b;
+  unpack2(t, a, b);
+  return pack2(fast_exp2(a), fast_exp2(b));
+}
+
 // Bounded wait on an mbarrier phase.  Returns false if `limit_ns` passed
 // before the phase completed.  A limit <= 0 is the error-path test hook: it
-// always reports expiry (the caller then drains the copies with a 1 s wait).
+// always reports expiry (the caller then drains with a 1 s wait).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long limit_ns) {
   if (limit_ns <= 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
@@ -170,8 +177,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 template <int ELT> struct Vec;
 template <> struct Vec<2> {
   static constexpr int N = 8;
-  __device__ __forceinline__ static void load(const unsigned char* p, float (&v)[8]) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
+  __device__ __forceinline__ static void unpack(const uint4 w, float (&v)[8]) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -179,25 +185,64 @@ template <> struct Vec<2> {
       v[2 * j + 1] = __uint_as_float(ws[j] & 0xffff0000u);
     }
   }
-  __device__ __forceinline__ static float scalar(const unsigned char* base, int idx) {
-    const uint16_t h = reinterpret_cast<const uint16_t*>(base)[idx];
+  __device__ __forceinline__ static float scalar(const void* base, long long idx) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(base) + idx);
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
   }
   __device__ __forceinline__ static void store_scalar(unsigned char* base, int idx, float v) {
     reinterpret_cast<uint16_t*>(base)[idx] = static_cast<uint16_t>(__float_as_uint(v) >> 16);
   }
+  __device__ __forceinline__ static uint4 neg_inf() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
+  // the four fp32 pairs of a vector (element order within a pair: low, high)
+  __device__ __forceinline__ static void pairs(const uint4 w, f2 (&z)[4]) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] = pack2(__uint_as_float(ws[i] << 16), __uint_as_float(ws[i] & 0xffff0000u));
+  }
+  // packed maximum of two bf16 pairs (NaN loses to a number, as with fmaxf)
+  __device__ __forceinline__ static uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+  }
+  template <int N>
+  __device__ __forceinline__ static float vmax(const uint4 (&r)[N]) {
+    uint32_t m[4] = {r[0].x, r[0].y, r[0].z, r[0].w};
+#pragma unroll
+    for (int j = 1; j < N; ++j) {
+      m[0] = max2(m[0], r[j].x); m[1] = max2(m[1], r[j].y);
+      m[2] = max2(m[2], r[j].z); m[3] = max2(m[3], r[j].w);
+    }
+    const uint32_t w = max2(max2(m[0], m[1]), max2(m[2], m[3]));
+    return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
 };
 template <> struct Vec<4> {
   static constexpr int N = 4;
-  __device__ __forceinline__ static void load(const unsigned char* p, float (&v)[4]) {
-    const float4 w = *reinterpret_cast<const float4*>(p);
-    v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+  __device__ __forceinline__ static void unpack(const uint4 w, float (&v)[4]) {
+    v[0] = __uint_as_float(w.x); v[1] = __uint_as_float(w.y);
+    v[2] = __uint_as_float(w.z); v[3] = __uint_as_float(w.w);
   }
-  __device__ __forceinline__ static float scalar(const unsigned char* base, int idx) {
-    return reinterpret_cast<const float*>(base)[idx];
+  __device__ __forceinline__ static float scalar(const void* base, long long idx) {
+    return __ldg(reinterpret_cast<const float*>(base) + idx);
   }
   __device__ __forceinline__ static void store_scalar(unsigned char* base, int idx, float v) {
     reinterpret_cast<float*>(base)[idx] = v;
+  }
+  __device__ __forceinline__ static uint4 neg_inf() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
+  __device__ __forceinline__ static void pairs(const uint4 w, f2 (&z)[2]) {
+    z[0] = pack2(__uint_as_float(w.x), __uint_as_float(w.y));
+    z[1] = pack2(__uint_as_float(w.z), __uint_as_float(w.w));
+  }
+  template <int N>
+  __device__ __forceinline__ static float vmax(const uint4 (&r)[N]) {
+    float m[4] = {__uint_as_float(r[0].x), __uint_as_float(r[0].y), __uint_as_float(r[0].z), __uint_as_float(r[0].w)};
+#pragma unroll
+    for (int j = 1; j < N; ++j) {
+      m[0] = fmaxf(m[0], __uint_as_float(r[j].x)); m[1] = fmaxf(m[1], __uint_as_float(r[j].y));
+      m[2] = fmaxf(m[2], __uint_as_float(r[j].z)); m[3] = fmaxf(m[3], __uint_as_float(r[j].w));
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
   }
 };
 
@@ -225,88 +270,88 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
   }
 }
+__device__ __forceinline__ double warp_incl_scan(double v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double up = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += up;
+  }
+  return v;
+}
+__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float up = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += up;
+  }
+  return v;
+}
 
 // ---------------------------------------------------------------------------
-// Shared control block (first kCtrlBytes of dynamic shared memory).
+// Shared control block
 // ---------------------------------------------------------------------------
 
-// Values a CTA publishes to its cluster for one item.  Two copies alternate
-// between consecutive items, so a CTA can publish item j+1 while another CTA
-// is still reading item j.
-struct Pub {
-  float m_t, s_t, m_d, s_d;   // slice maximum and sum relative to fl(m c)
-  float zt_x, zd_x;           // logits at the drafted token (owner CTA only)
-  int arg_t;                  // greedy: first index of the slice maximum
-  int flags;                  // bit0 wait timed out, bit1 non-finite seen (greedy)
-  double W;                   // this CTA's total draw weight
-  int skip;                   // this CTA skipped the draw
-  int pad_;
+// What a staging slot holds.
+//   kind 0 / 1: chunk `chunk` of the target / draft row at position pos;
+//   kind 2:     chunk `chunk` of the re-read of the pair at pos for its draw:
+//               the first half of the slot holds target logits, the second
+//               half the draft logits of the same vocabulary range (x holds
+//               the draw mode: 1 residual max(0, p - q), 2 p alone);
+//   kind -1:    no more work.
+struct Desc {
+  int b, kb, pos, kind;
+  int chunk, nchunks, x, rec;  // x: drafted token at pos (rows of pairs, else -1); rec: sequence record
+  float u, s;                  // accept uniform at pos, sampling uniform of b
 };
+
+// One sequence in flight.  Its stream and its draw can finish in either
+// order; the outputs are written when both are done.
+struct SeqRec {
+  int b, kb, a, err, y, zero_resid;
+  int pending;                 // events left before the outputs can be written
+  float Kt, Lt, Kd, Ld;        // normalisers of the pair being drawn from
+  float s;                     // sampling uniform
+};
+
+constexpr int kRecs = 8;       // sequence records (ring)
+constexpr int kReqs = 8;       // re-read requests (ring)
+constexpr int kHalfBytes = kChunkBytes / 2;                   // one row's part of a draw chunk
+constexpr int kDrawVecsPerWarp = kHalfBytes / 16 / kConsumerWarps;   // 128
+constexpr int kDrawVecsPerLane = kDrawVecsPerWarp / 32;              // 4
+constexpr int kMaxDrawSegs = 2 * kMaxChunks * kConsumerWarps;
+
+enum : int { kErrBadToken = 1 << 3, kErrNonfinite = 1 << 4, kErrTimeout = 1 << 5 };
 
 struct Ctrl {
-  uint64_t bar[kMaxStages];   // staging barrier per buffer
-  int inbox[kMaxStages];      // tickets written by the cluster leader
-  int2 desc[kMaxStages];      // item staged in each buffer ({-1, 0} = none)
-  Pub pub[2];
-  float red_f[64];
-  int red_i[64];
-  double warp_W[32];
-  // cluster-wide values of the current item (same in every CTA)
-  float g_Kt, g_Kd, g_Lt, g_Ld, g_zt_x, g_zd_x, g_Mt, g_Md;
-  int g_arg_t, g_flags, g_accept, g_compute, g_skip, g_rstar, g_found_warp, g_y;
-  double g_S, g_target;
+  uint64_t full[kMaxStages];   // slot filled (producer -> consumers)
+  uint64_t empty[kMaxStages];  // slot released (one arrival per consumer warp)
+  Desc desc[kMaxStages];
+  // per-warp row state published at a row end
+  float wK[kConsumerWarps], wS[kConsumerWarps], wM[kConsumerWarps];
+  int wArg[kConsumerWarps], wBad[kConsumerWarps];
+  // the current pair: [0] target row, [1] draft row
+  float zx[2];
+  float rowK[2], rowL[2];
+  SeqRec rec[kRecs];
+  // re-read requests: consumer thread 0 pushes, the producer pops
+  int req_b[kReqs], req_pos[kReqs], req_rec[kReqs], req_mode[kReqs];
+  volatile int req_head, req_tail;
+  volatile int seqs_finished;  // sequences whose outputs are written
+  // broadcasts from consumer thread 0 / warp 0 to the consumer warps
+  int flag_bonus, flag_finish;
+  // the draw being located
+  int seg;
+  double seg_t, S;
+  float segK[kMaxChunks * kConsumerWarps];   // bonus row: per-segment fl(m c)
+  float segS[kMaxChunks * kConsumerWarps];   // bonus row: per-segment sum
+  double bmass[kMaxChunks * kConsumerWarps]; // bonus draw: weight per stream segment
+  double rmass[kMaxDrawSegs];                // re-read draws: weight per draw segment
 };
-static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block too large");
+
+constexpr int kCtrlBytes = ((static_cast<int>(sizeof(Ctrl)) + 1023) / 1024) * 1024;
 
 // ---------------------------------------------------------------------------
-// Sequence bookkeeping
-// ---------------------------------------------------------------------------
-
-// Sequence epilogue, run by the item that finishes last.
-__device__ void finalize_sequence(const VerifyParams& P, int b, int kb) {
-  const Workspace& ws = P.ws;
-  const int err = __ldcg(ws.seq_err + b);
-  const int rmin = __ldcg(ws.rej_min + b);
-  int* ot = P.out_tokens + static_cast<size_t>(b) * (P.k + 1);
-  if (err) {
-    for (int j = 0; j <= P.k; ++j) ot[j] = -1;
-    P.out_len[b] = 0;
-    atomicAdd(ws.stats + kStatErrorSeqs, 1ull);
-    return;
-  }
-  const int a = rmin < kb ? rmin : kb;
-  const int y = __ldcg(ws.y_slot + static_cast<size_t>(b) * (P.k + 1) + a);
-  const int* xt = P.tokens + static_cast<size_t>(b) * P.k;
-  for (int j = 0; j < a; ++j) ot[j] = xt[j];
-  ot[a] = y;
-  for (int j = a + 1; j <= P.k; ++j) ot[j] = -1;
-  P.out_len[b] = a + 1;
-  atomicAdd(ws.stats + kStatSequences, 1ull);
-  atomicAdd(ws.stats + kStatProposed, static_cast<unsigned long long>(kb));
-  atomicAdd(ws.stats + kStatAccepted, static_cast<unsigned long long>(a));
-  atomicAdd(ws.stats + kStatEmitted, static_cast<unsigned long long>(a + 1));
-  if (kb == 0) atomicAdd(ws.stats + kStatSpecOff, 1ull);
-}
-
-// Report one finished item; the last of the sequence's k_b + 1 items
-// finalises it.  `y` < -1 means "no token recorded".
-__device__ void report_item(const VerifyParams& P, int b, int kb, int pos, int y) {
-  if (y >= -1) P.ws.y_slot[static_cast<size_t>(b) * (P.k + 1) + pos] = y;
-  __threadfence();
-  const int prev = atomicAdd(P.ws.done + b, 1);
-  if (prev == kb) {
-    __threadfence();
-    finalize_sequence(P, b, kb);
-  }
-}
-
-__device__ void mark_error(const VerifyParams& P, int b, int code) {
-  atomicOr(P.ws.seq_err + b, 1 << code);
-  atomicOr(P.ws.err_word, 1u << code);
-}
-
-// ---------------------------------------------------------------------------
-// plan_kernel: the work list and per-call resets (one CTA).
+// plan_kernel: the work list (valid sequences, longest first) and resets.
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
 
@@ -317,11 +362,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = P.B, k = P.k;
   const Workspace& ws = P.ws;
-  // per-sequence resets, diagnostics cleared to NaN, invalid draft lengths
   for (int b = tid; b < B; b += kPlanThreads) {
-    ws.done[b] = 0;
-    ws.rej_min[b] = kNoReject;
-    ws.seq_err[b] = 0;
     const int kb = P.draft_len[b];
     if (kb < 0 || kb > k) {
       int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
@@ -339,15 +380,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
   }
   if (tid == 0) { base = 0; *ws.ticket = 0; }
   __syncthreads();
-  // position-major list: level L < k holds pairs (b, L) with k_b > L;
-  // level k holds the bonus row (b, k_b) of every valid sequence
-  for (int L = 0; L <= k; ++L) {
+  // counting sort by k_b, largest first, stable in b
+  for (int L = k; L >= 0; --L) {
     for (int b0 = 0; b0 < B; b0 += kPlanThreads) {
       const int b = b0 + tid;
-      int kb = -1;
-      if (b < B) kb = P.draft_len[b];
-      const bool valid = kb >= 0 && kb <= k;
-      const bool take = valid && (L < k ? kb > L : true);
+      const int kb = b < B ? P.draft_len[b] : -1;
+      const bool take = (kb == L);
       const unsigned m = __ballot_sync(0xffffffffu, take);
       if (lane == 0) warp_cnt[warp] = __popc(m);
       __syncthreads();
@@ -362,17 +400,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
         warp_cnt[lane] = incl - c;
       }
       __syncthreads();
-      if (take) {
-        const int idx = base + warp_cnt[warp] + __popc(m & ((1u << lane) - 1u));
-        const int pos = L < k ? L : kb;
-        ws.items[idx] = make_int2(b, (pos << 1) | (L < k ? 1 : 0));
-      }
+      if (take) ws.seqs[base + warp_cnt[warp] + __popc(m & ((1u << lane) - 1u))] = make_int2(b, kb);
       __syncthreads();
       if (tid == kPlanThreads - 1) base += warp_cnt[31] + __popc(m);
       __syncthreads();
     }
   }
-  if (tid == 0) *ws.n_items = base;
+  if (tid == 0) *ws.n_seqs = base;
 }
 
 // ---------------------------------------------------------------------------
@@ -380,486 +414,713 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
 // ---------------------------------------------------------------------------
 
 template <int ELT>
-__global__ void __launch_bounds__(kThreads)
-verify_kernel(const VerifyParams P) {
+struct Verifier {
   using V = Vec<ELT>;
-  constexpr int NV = V::N;          // logits per 16-byte vector
-  constexpr int NW = kThreads / 32;
-  extern __shared__ __align__(128) unsigned char smem[];
-  Ctrl& C = *reinterpret_cast<Ctrl*>(smem);
+  static constexpr int NV = V::N;                          // logits per vector
+  static constexpr int kSegElems = kVecsPerWarp * NV;      // logits per stream segment (chunk, warp)
 
-  const uint32_t CS = cluster_size();
-  const uint32_t rank = cluster_rank();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k = P.k;
-  const int S = P.stages;
-  const float c2 = P.c2;
+  const VerifyParams& P;
+  Ctrl& C;
+  unsigned char* ring;
+  const int lane, warp;
+  const long long row_bytes;    // V * ELT
+  const int nchunks;            // stream chunks per row
+  const int ndraw;              // draw chunks per row
+  const int nvec_row;           // 16-byte vectors per row (last one padded)
 
-  // this CTA's slice of every row, and this warp's part of it
-  const int lo = static_cast<int>(rank) * P.slice;
-  const int hi = min(P.V, lo + P.slice);
-  const int n = max(0, hi - lo);
-  const int nvec = (n + NV - 1) / NV;
-  const int vpw = (nvec + NW - 1) / NW;
-  const int v0 = warp * vpw;
-  const int v1 = min(nvec, v0 + vpw);
-  const int row_pad = ((P.slice * ELT + 127) / 128) * 128;
-  auto bufT = [&](int s) { return smem + kCtrlBytes + s * 2 * row_pad; };
-  auto bufD = [&](int s) { return smem + kCtrlBytes + s * 2 * row_pad + row_pad; };
+  __device__ Verifier(const VerifyParams& p, Ctrl& c, unsigned char* r, int ln, int wp)
+      : P(p), C(c), ring(r), lane(ln), warp(wp),
+        row_bytes(static_cast<long long>(p.V) * ELT),
+        nchunks(static_cast<int>((static_cast<long long>(p.V) * ELT + kChunkBytes - 1) / kChunkBytes)),
+        ndraw(static_cast<int>((static_cast<long long>(p.V) * ELT + kHalfBytes - 1) / kHalfBytes)),
+        nvec_row(static_cast<int>((static_cast<long long>(p.V) * ELT + 15) / 16)) {}
 
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&C.bar[s], 1);
-    mbar_fence_init();
+  __device__ const unsigned char* row_ptr(int b, int pos, int kind) const {
+    if (kind == 0)
+      return static_cast<const unsigned char*>(P.target) +
+             (static_cast<size_t>(b) * (P.k + 1) + pos) * static_cast<size_t>(row_bytes);
+    return static_cast<const unsigned char*>(P.draft) +
+           (static_cast<size_t>(b) * P.k + pos) * static_cast<size_t>(row_bytes);
   }
-  grid_dependency_wait();           // the work list of plan_kernel is ready
-  const int n_items = __ldcg(P.ws.n_items);
-  const bool leader = (rank == 0 && tid == 0);
 
-  // stage item `t` (a ticket) into buffer s; records the descriptor
-  auto stage = [&](int s, int t) {
-    int2 d = make_int2(-1, 0);
-    if (t < n_items) d = __ldcg(P.ws.items + t);
-    C.desc[s] = d;
-    if (d.x < 0 || !P.bulk || n == 0) return;
-    const int b = d.x, pos = d.y >> 1;
-    const bool pair = (d.y & 1) && !P.greedy;
-    const uint32_t bytes = static_cast<uint32_t>(n) * ELT;
-    const unsigned char* gT = static_cast<const unsigned char*>(P.target) +
-        ((static_cast<size_t>(b) * (k + 1) + pos) * P.V + lo) * ELT;
-    mbar_expect_tx(&C.bar[s], pair ? 2 * bytes : bytes);
-    constexpr uint32_t kChunk = 32768;
-    for (uint32_t o = 0; o < bytes; o += kChunk)
-      bulk_load(bufT(s) + o, gT + o, min(kChunk, bytes - o), &C.bar[s]);
-    if (pair) {
-      const unsigned char* gD = static_cast<const unsigned char*>(P.draft) +
-          ((static_cast<size_t>(b) * k + pos) * P.V + lo) * ELT;
-      for (uint32_t o = 0; o < bytes; o += kChunk)
-        bulk_load(bufD(s) + o, gD + o, min(kChunk, bytes - o), &C.bar[s]);
+  // Vector v of a row read straight from global memory, -inf beyond V.
+  __device__ uint4 load_global_raw(const unsigned char* row, int v) const {
+    if (v >= nvec_row) return V::neg_inf();
+    if (P.bulk) return __ldg(reinterpret_cast<const uint4*>(row) + v);
+    unsigned char buf[16];
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int x = v * NV + e;
+      V::store_scalar(buf, e, x < P.V ? V::scalar(row, x) : -INFINITY);
     }
-  };
-  // plain-load staging (rows not 16-byte aligned): every thread helps; the
-  // tail of the last vector is padded with -inf
-  auto stage_plain = [&](int s) {
-    const int2 d = C.desc[s];
-    if (d.x < 0 || P.bulk) return;
-    const int b = d.x, pos = d.y >> 1;
-    const bool pair = (d.y & 1) && !P.greedy;
-    const unsigned char* gT = static_cast<const unsigned char*>(P.target) +
-        ((static_cast<size_t>(b) * (k + 1) + pos) * P.V + lo) * ELT;
-    const unsigned char* gD = pair ? static_cast<const unsigned char*>(P.draft) +
-        ((static_cast<size_t>(b) * k + pos) * P.V + lo) * ELT : nullptr;
-    for (int e = tid; e < nvec * NV; e += kThreads) {
-      V::store_scalar(bufT(s), e, e < n ? V::scalar(gT, e) : -INFINITY);
-      if (pair) V::store_scalar(bufD(s), e, e < n ? V::scalar(gD, e) : -INFINITY);
-    }
-  };
-
-  // prologue: the leader takes S tickets and hands them to every CTA
-  if (leader) {
-    const int t0 = atomicAdd(P.ws.ticket, S);
-    for (uint32_t r = 0; r < CS; ++r)
-      for (int s = 0; s < S; ++s) st_remote_s32(&C.inbox[s], r, t0 + s);
+    return *reinterpret_cast<const uint4*>(buf);
   }
-  cluster_barrier();
-  if (tid == 0)
-    for (int s = 0; s < S; ++s) stage(s, C.inbox[s]);
-  __syncthreads();
-  for (int s = 0; s < S; ++s) stage_plain(s);
-  __syncthreads();
 
-  for (int j = 0;; ++j) {
-    const int s = j % S;
-    const int2 d = C.desc[s];
-    if (d.x < 0) break;             // same ticket stream in every CTA: uniform
-    const int pb = j & 1;
-    const int b = d.x, pos = d.y >> 1;
-    const bool pair = (d.y & 1) != 0;
-    const int kb = __ldg(P.draft_len + b);
-    const bool use_draft = pair && !P.greedy;
-    const int x = pair ? __ldg(P.tokens + static_cast<size_t>(b) * k + pos) : -1;
-    const bool bad_token = pair && (x < 0 || x >= P.V);
-    const unsigned char* T_ = bufT(s);
-    const unsigned char* D_ = bufD(s);
+  // ======================= producer ==========================================
 
-    // ---- wait for the staged slice ----------------------------------------
-    int my_flags = 0;
-    if (P.bulk && n > 0) {
-      const uint32_t parity = static_cast<uint32_t>(j / S) & 1u;
-      if (!mbar_wait_bounded(&C.bar[s], parity, P.wait_limit_ns)) {
-        my_flags |= 1;
-        mbar_wait_bounded(&C.bar[s], parity, kDrainLimitNs);
+  // Wait for slot q%S to be free (lane 0 waits, the warp follows).
+  __device__ bool acquire_slot(int q) {
+    const int S = P.stages;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(&C.empty[q % S], ((q / S) & 1) ^ 1, kDrainLimitNs) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+    __syncwarp();
+    return ok != 0;
+  }
+
+  // Copy `bytes` of a row starting at byte `off` into dst (bulk or plain).
+  __device__ void fill(unsigned char* dst, const unsigned char* src, long long off, int bytes,
+                       uint64_t* bar, bool hint, uint64_t policy) {
+    if (P.bulk) {
+      if (lane == 0) {
+        if (hint) bulk_load_hint(dst, src + off, static_cast<uint32_t>(bytes), bar, policy);
+        else bulk_load(dst, src + off, static_cast<uint32_t>(bytes), bar);
+      }
+    } else {
+      // plain loads (rows not 16-byte aligned); pad the last vector with -inf
+      const int e0 = static_cast<int>(off / ELT);
+      const int n = (bytes + ELT - 1) / ELT;
+      const int npad = ((n + NV - 1) / NV) * NV;
+      for (int e = lane; e < npad; e += 32) {
+        const int xg = e0 + e;
+        V::store_scalar(dst, e, xg < P.V ? V::scalar(src, xg) : -INFINITY);
       }
     }
-    my_flags = __syncthreads_or(my_flags);
+  }
 
-    // ---- local pass: slice maximum and sum (or argmax when greedy) --------
-    float mt = -INFINITY, md = -INFINITY, st = 0.f, sd = 0.f;
-    int arg = 0x7fffffff;
-    int bad = 0;
-    if (!bad_token) {
+  // Issue the draw chunks of every queued re-read request.
+  __device__ bool service_requests(int& q) {
+    const int S = P.stages;
+    while (true) {
+      int head = 0, tail = 0;
+      if (lane == 0) { head = C.req_head; tail = C.req_tail; }
+      head = __shfl_sync(0xffffffffu, head, 0);
+      tail = __shfl_sync(0xffffffffu, tail, 0);
+      if (head == tail) return true;
+      const int r = head % kReqs;
+      const int b = C.req_b[r], pos = C.req_pos[r], rec = C.req_rec[r], mode = C.req_mode[r];
+      __syncwarp();
+      if (lane == 0) { __threadfence_block(); C.req_head = head + 1; }
+      const unsigned char* srcT = row_ptr(b, pos, 0);
+      const unsigned char* srcD = row_ptr(b, pos, 1);
+      for (int c = 0; c < ndraw; ++c) {
+        if (!acquire_slot(q)) return false;
+        const int slot = q % S;
+        const long long off = static_cast<long long>(c) * kHalfBytes;
+        const long long rem = row_bytes - off;
+        const int bytes = static_cast<int>(rem < kHalfBytes ? rem : kHalfBytes);
+        unsigned char* dst = ring + static_cast<size_t>(slot) * kChunkBytes;
+        if (lane == 0) {
+          Desc& d = C.desc[slot];
+          d.b = b; d.kb = 0; d.pos = pos; d.kind = 2;
+          d.chunk = c; d.nchunks = ndraw; d.x = mode; d.rec = rec;
+          d.u = 0.f; d.s = 0.f;
+          if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(mode == 1 ? 2 * bytes : bytes));
+        }
+        fill(dst, srcT, off, bytes, &C.full[slot], false, 0);
+        if (mode == 1) fill(dst + kHalfBytes, srcD, off, bytes, &C.full[slot], false, 0);
+        if (!P.bulk) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&C.full[slot]);
+        }
+        ++q;
+      }
+    }
+  }
+
+  __device__ void produce() {
+    const int S = P.stages;
+    const int k = P.k;
+    const int n_seqs = __ldcg(P.ws.n_seqs);
+    const uint64_t evict_first = evict_first_policy();
+    int q = 0, streamed = 0;
+    int t = 0;
+    if (lane == 0) t = atomicAdd(P.ws.ticket, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    bool ok = true;
+    while (ok && t < n_seqs) {
+      const int2 sq = __ldcg(P.ws.seqs + t);
+      const int b = sq.x, kb = sq.y;
+      const int rec = streamed % kRecs;
+      int t_next = 0;
+      if (lane == 0) t_next = atomicAdd(P.ws.ticket, 1);
+      // the sequence's drafted tokens and uniforms, one per lane
+      const int xj = lane < kb ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
+      const float uj = (!P.greedy && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
+      const float s_samp = __shfl_sync(0xffffffffu, uj, k);
+      const int nrows = P.greedy ? kb + 1 : 2 * kb + 1;
+      for (int r = 0; r < nrows && ok; ++r) {
+        int pos, kind;
+        if (P.greedy) { pos = r; kind = 0; }
+        else if (r < 2 * kb) { pos = r >> 1; kind = r & 1; }
+        else { pos = kb; kind = 0; }
+        const int x = __shfl_sync(0xffffffffu, xj, pos < kb ? pos : 0);
+        const float u = __shfl_sync(0xffffffffu, uj, pos < kb ? pos : 0);
+        const unsigned char* src = row_ptr(b, pos, kind);
+        for (int c = 0; c < nchunks && ok; ++c) {
+          if (!(ok = acquire_slot(q))) break;
+          const int slot = q % S;
+          const long long off = static_cast<long long>(c) * kChunkBytes;
+          const long long rem = row_bytes - off;
+          const int bytes = static_cast<int>(rem < kChunkBytes ? rem : kChunkBytes);
+          if (lane == 0) {
+            Desc& d = C.desc[slot];
+            d.b = b; d.kb = kb; d.pos = pos; d.kind = kind;
+            d.chunk = c; d.nchunks = nchunks;
+            d.x = pos < kb ? x : -1; d.rec = rec;
+            d.u = u; d.s = s_samp;
+            if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(bytes));
+          }
+          // the bonus row is never read in full again: first out of L2
+          fill(ring + static_cast<size_t>(slot) * kChunkBytes, src, off, bytes, &C.full[slot],
+               pos == kb, evict_first);
+          if (!P.bulk) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&C.full[slot]);
+          }
+          ++q;
+          ok = service_requests(q);
+        }
+      }
+      ++streamed;
+      t = __shfl_sync(0xffffffffu, t_next, 0);
+    }
+    // no more sequences: keep serving re-reads until every streamed sequence
+    // is finished, then signal the end (bounded: 1 s without progress)
+    unsigned long long t0 = global_ns();
+    int last_done = -1;
+    while (ok) {
+      ok = service_requests(q);
+      int done = 0;
+      if (lane == 0) done = C.seqs_finished;
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (done >= streamed) break;
+      if (done != last_done) { last_done = done; t0 = global_ns(); }
+      if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
+        if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+        break;
+      }
+      __nanosleep(200);
+    }
+    if (acquire_slot(q)) {
+      if (lane == 0) {
+        C.desc[q % S].kind = -1;
+        mbar_arrive(&C.full[q % S]);
+      }
+    }
+  }
+
+  // ======================= consumers =========================================
+
+  __device__ void consume() {
+    const int S = P.stages;
+    const float c2 = P.c2;
+    // warp-uniform running state of the current row
+    float rK = -INFINITY, rS = 0.f, rM = -INFINITY;
+    int rArg = 0x7fffffff, rBad = 0;
+    int q = 0;
+    while (true) {
+      const int slot = q % S;
+      const uint32_t par = static_cast<uint32_t>(q / S) & 1u;
+      int timed_out = 0;
+      if (!mbar_wait_bounded(&C.full[slot], par, P.wait_limit_ns)) {
+        timed_out = 1;
+        if (!mbar_wait_bounded(&C.full[slot], par, kDrainLimitNs)) {
+          if (warp == 0 && lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+          return;   // the producer is gone; nothing is left in flight for this slot
+        }
+      }
+      const Desc d = C.desc[slot];
+      if (d.kind < 0) return;
+      if (d.kind == 2) {
+        draw_chunk(d, slot, timed_out);
+        ++q;
+        continue;
+      }
+
+      // this lane's vectors of the chunk (raw 16-byte words)
+      const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
+      const long long off = static_cast<long long>(d.chunk) * kChunkBytes;
+      const long long rem = row_bytes - off;
+      const int nvec = static_cast<int>(((rem < kChunkBytes ? rem : kChunkBytes) + 15) / 16);
+      uint4 raw[kVecsPerLane];
+#pragma unroll
+      for (int j = 0; j < kVecsPerLane; ++j) {
+        const int v = warp * kVecsPerWarp + j * 32 + lane;
+        raw[j] = v < nvec ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&C.empty[slot]);   // the slot is free again
+
+      const int seg = d.chunk * kConsumerWarps + warp;
+      const int seg_base = seg * kSegElems;
+      if (d.chunk == 0) { rK = -INFINITY; rS = 0.f; rM = -INFINITY; rArg = 0x7fffffff; rBad = 0; }
+      if (timed_out) rBad |= 2;
+      // the drafted token's logit
+      if (d.x >= 0 && d.x < P.V && !P.greedy) {
+        const int rel = d.x - seg_base;
+        if (rel >= 0 && rel < kSegElems && ((rel / NV) & 31) == lane) {
+          const int vv = rel / NV;
+          const int j = vv >> 5, e = rel - vv * NV;
+#pragma unroll
+          for (int jj = 0; jj < kVecsPerLane; ++jj) {
+            if (jj == j) {
+              float z[NV];
+              V::unpack(raw[jj], z);
+#pragma unroll
+              for (int ee = 0; ee < NV; ++ee)
+                if (ee == e) C.zx[d.kind] = z[ee];
+            }
+          }
+        }
+      }
       if (P.greedy) {
-        for (int v = v0 + lane; v < v1; v += 32) {
+        float lm = -INFINITY;
+        int li = 0x7fffffff, bad = 0;
+#pragma unroll
+        for (int j = 0; j < kVecsPerLane; ++j) {
           float z[NV];
-          V::load(T_ + v * 16, z);
+          V::unpack(raw[j], z);
 #pragma unroll
           for (int e = 0; e < NV; ++e) {
             bad |= (z[e] != z[e]) || (z[e] == INFINITY);
-            if (z[e] > mt) { mt = z[e]; arg = lo + v * NV + e; }
+            if (z[e] > lm) { lm = z[e]; li = seg_base + (j * 32 + lane) * NV + e; }
           }
         }
-        warp_argmax(mt, arg);
+        warp_argmax(lm, li);
         bad = warp_or(bad);
+        if (lm > rM) { rM = lm; rArg = li; }
+        rBad |= bad;
       } else {
-        for (int v = v0 + lane; v < v1; v += 32) {
-          float z[NV];
-          V::load(T_ + v * 16, z);
+        const float wm = warp_max(V::vmax(raw));
+        float Ks = -INFINITY, ss = 0.f;
+        if (wm > -INFINITY) {
+          Ks = __fmul_rn(wm, c2);      // fl(m c), used identically wherever rescaled
+          const f2 cc = pack2(c2, c2), nk = pack2(-Ks, -Ks);
+          f2 acc[NV / 2];
 #pragma unroll
-          for (int e = 0; e < NV; ++e) mt = fmaxf(mt, z[e]);
-          if (use_draft) {
-            V::load(D_ + v * 16, z);
+          for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
 #pragma unroll
-            for (int e = 0; e < NV; ++e) md = fmaxf(md, z[e]);
+          for (int j = 0; j < kVecsPerLane; ++j) {
+            f2 z[NV / 2];
+            V::pairs(raw[j], z);
+#pragma unroll
+            for (int i = 0; i < NV / 2; ++i) acc[i] = add2(acc[i], exp2_2(fma2(z[i], cc, nk)));
           }
-        }
-        mt = warp_max(mt);
-        md = warp_max(md);
-      }
-      if (lane == 0) { C.red_f[warp] = mt; C.red_f[NW + warp] = md; C.red_i[warp] = arg; C.red_i[NW + warp] = bad; }
-      __syncthreads();
-      if (P.greedy) {
-        if (warp == 0) {
-          float m = lane < NW ? C.red_f[lane] : -INFINITY;
-          int a = lane < NW ? C.red_i[lane] : 0x7fffffff;
-          warp_argmax(m, a);
-          mt = m;
-          arg = a;
-          bad = warp_or(lane < NW ? C.red_i[NW + lane] : 0);
-        }
-      } else {
-        mt = C.red_f[0];
-        md = C.red_f[NW];
-        for (int w = 1; w < NW; ++w) { mt = fmaxf(mt, C.red_f[w]); md = fmaxf(md, C.red_f[NW + w]); }
-        // K = fl(m c), rounded once and used identically wherever this slice's
-        // sum is rescaled (no contraction into an FMA)
-        const float Kt = __fmul_rn(mt, c2), Kd = __fmul_rn(md, c2);
-        for (int v = v0 + lane; v < v1; v += 32) {
-          float z[NV];
-          V::load(T_ + v * 16, z);
+          float a0, a1, sum = 0.f;
 #pragma unroll
-          for (int e = 0; e < NV; ++e) st += fast_exp2(fmaf(z[e], c2, -Kt));
-          if (use_draft) {
-            V::load(D_ + v * 16, z);
+          for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); sum += a0 + a1; }
+          ss = warp_sum(sum);   // NaN logits make this NaN: caught at the row end
+          if (Ks > rK) { rS = rS * fast_exp2(__fsub_rn(rK, Ks)) + ss; rK = Ks; }
+          else         { rS += ss * fast_exp2(__fsub_rn(Ks, rK)); }
+        } else {
+          // no finite logit in the segment: only NaN can still hide here
+          int nan_seen = 0;
 #pragma unroll
-            for (int e = 0; e < NV; ++e) sd += fast_exp2(fmaf(z[e], c2, -Kd));
+          for (int j = 0; j < kVecsPerLane; ++j) {
+            float z[NV];
+            V::unpack(raw[j], z);
+#pragma unroll
+            for (int e = 0; e < NV; ++e) nan_seen |= (z[e] != z[e]);
           }
+          rBad |= warp_or(nan_seen);
         }
-        st = warp_sum(st);
-        sd = warp_sum(sd);
-        __syncthreads();            // red_f is reused below
-        if (lane == 0) { C.red_f[warp] = st; C.red_f[NW + warp] = sd; }
-        __syncthreads();
-        if (tid == 0) {
-          st = 0.f; sd = 0.f;
-          for (int w = 0; w < NW; ++w) { st += C.red_f[w]; sd += C.red_f[NW + w]; }
-          if (mt == -INFINITY) st = 0.f;      // empty or fully masked slice
-          if (md == -INFINITY) sd = 0.f;
+        rM = fmaxf(rM, wm);
+        if (d.kind == 0 && d.pos == d.kb && lane == 0 && seg < kMaxChunks * kConsumerWarps) {
+          C.segK[seg] = Ks;
+          C.segS[seg] = ss;
         }
       }
-    }
 
-    // ---- publish, take the next ticket, cluster barrier A -------------------
-    if (tid == 0) {
-      Pub& pp = C.pub[pb];
-      pp.m_t = mt; pp.s_t = st; pp.m_d = md; pp.s_d = sd; pp.arg_t = arg;
-      pp.flags = my_flags | (bad ? 2 : 0);
-      pp.zt_x = NAN; pp.zd_x = NAN;
-      if (pair && !bad_token && x >= lo && x < hi) {
-        pp.zt_x = V::scalar(T_, x - lo);
-        if (use_draft) pp.zd_x = V::scalar(D_, x - lo);
-      }
+      if (d.chunk == d.nchunks - 1) row_end(d, rK, rS, rM, rArg, rBad);
+      ++q;
     }
-    if (leader) {
-      const int t = atomicAdd(P.ws.ticket, 1);
-      for (uint32_t r = 0; r < CS; ++r) st_remote_s32(&C.inbox[s], r, t);
-    }
-    cluster_barrier();  // A
+  }
 
-    // ---- cluster combine (warp 0, one lane per CTA) -------------------------
-    int next_t = 0;
+  // Row end: combine the warps, then the decisions that need the row.
+  __device__ void row_end(const Desc& d, float rK, float rS, float rM, int rArg, int rBad) {
+    const int ctid = warp * 32 + lane;
+    const float c2 = P.c2;
+    if (lane == 0) {
+      C.wK[warp] = rK; C.wS[warp] = rS; C.wM[warp] = rM; C.wArg[warp] = rArg; C.wBad[warp] = rBad;
+    }
+    consumer_sync();
+    // warp 0 combines the warps' states, one lane per warp
+    float M = -INFINITY, K = -INFINITY, Ssum = 0.f;
+    int arg = 0x7fffffff, bad = 0;
     if (warp == 0) {
-      const bool in = lane < static_cast<int>(CS);
-      const uint32_t r = in ? static_cast<uint32_t>(lane) : 0u;
-      float rmt = in ? ld_remote_f32(&C.pub[pb].m_t, r) : -INFINITY;
-      const float rst = in ? ld_remote_f32(&C.pub[pb].s_t, r) : 0.f;
-      const float rmd = in ? ld_remote_f32(&C.pub[pb].m_d, r) : -INFINITY;
-      const float rsd = in ? ld_remote_f32(&C.pub[pb].s_d, r) : 0.f;
-      int rarg = in ? ld_remote_s32(&C.pub[pb].arg_t, r) : 0x7fffffff;
-      const int rfl = in ? ld_remote_s32(&C.pub[pb].flags, r) : 0;
-      int fl = warp_or(rfl);
-      if (P.greedy) {
-        warp_argmax(rmt, rarg);
-        if (!(rmt > -INFINITY) && !bad_token) fl |= 2;
-        if (lane == 0) { C.g_Mt = rmt; C.g_arg_t = rarg; C.g_flags = fl; }
-      } else {
-        const float Mt = warp_max(rmt);
-        const float Md = warp_max(rmd);
-        const float Kt = __fmul_rn(Mt, c2), Kd = __fmul_rn(Md, c2);
-        // s_r was summed relative to fl(m_r c): rescale by 2^(fl(m_r c) - fl(M c))
-        const float tt = (rmt == -INFINITY) ? 0.f : rst * fast_exp2(__fsub_rn(__fmul_rn(rmt, c2), Kt));
-        const float td = (rmd == -INFINITY) ? 0.f : rsd * fast_exp2(__fsub_rn(__fmul_rn(rmd, c2), Kd));
-        const float St = warp_sum(tt), Sd = warp_sum(td);
-        if (lane == 0) {
-          C.g_Mt = Mt; C.g_Md = Md;
-          C.g_Kt = Kt; C.g_Kd = Kd;
-          C.g_Lt = log2f(St);
-          C.g_Ld = use_draft ? log2f(Sd) : 0.f;
-          bool nonfinite = !(isfinite(Mt) && isfinite(St) && St > 0.f);
-          if (use_draft) nonfinite |= !(isfinite(Md) && isfinite(Sd) && Sd > 0.f);
-          if (nonfinite && !bad_token) fl |= 2;
-          C.g_flags = fl;
-        }
-      }
-      if (pair && !bad_token && lane == 0) {
-        const uint32_t owner = static_cast<uint32_t>(x / P.slice);
-        C.g_zt_x = ld_remote_f32(&C.pub[pb].zt_x, owner);
-        C.g_zd_x = use_draft ? ld_remote_f32(&C.pub[pb].zd_x, owner) : 0.f;
-      }
-      if (lane == 0) next_t = C.inbox[s];
+      const bool in = lane < kConsumerWarps;
+      M = in ? C.wM[lane] : -INFINITY;
+      arg = in ? C.wArg[lane] : 0x7fffffff;
+      warp_argmax(M, arg);
+      const float wk = in ? C.wK[lane] : -INFINITY;
+      K = warp_max(wk);
+      bad = warp_or(in ? C.wBad[lane] : 0);
+      if (!P.greedy) Ssum = warp_sum(wk > -INFINITY ? C.wS[lane] * fast_exp2(__fsub_rn(wk, K)) : 0.f);
     }
-    __syncthreads();
-
-    const size_t slot_t = static_cast<size_t>(b) * (k + 1) + pos;
-    const size_t slot_d = static_cast<size_t>(b) * k + pos;
-    const int flags = C.g_flags;
-
-    if (bad_token || flags) {
-      // ---- errors: the sequence emits nothing ---------------------------
-      if (leader) {
-        if (bad_token) mark_error(P, b, 3 /* SV_ERR_BAD_TOKEN */);
-        if (flags & 1) mark_error(P, b, 5 /* SV_ERR_TIMEOUT */);
-        if (flags & 2) mark_error(P, b, 4 /* SV_ERR_NONFINITE */);
-        report_item(P, b, kb, pos, -2);
+    int bonus_draw = 0;
+    if (ctid == 0) {
+      SeqRec& R = C.rec[d.rec];
+      const int kind = d.kind;
+      const size_t b = static_cast<size_t>(d.b);
+      if (d.pos == 0 && kind == 0) {
+        // first row of the sequence: open its record (free unless the ring of
+        // records has wrapped onto a sequence still waiting for its draw)
+        if (R.pending != 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+        R.b = d.b; R.kb = d.kb; R.a = -1; R.err = 0; R.y = -1; R.zero_resid = 0;
+        R.pending = 1; R.s = d.s;
       }
-    } else if (P.greedy) {
-      // ---- T == 0: accept iff x is the first argmax ---------------------
-      if (leader) {
-        P.ws.m_t[slot_t] = C.g_Mt;
-        if (pair) {
-          const bool acc = (x == C.g_arg_t);
-          P.ws.alpha[slot_d] = acc ? 1.f : 0.f;
-          if (!acc) atomicMin(P.ws.rej_min + b, pos);
+      if (bad & 2) R.err |= kErrTimeout;
+      if (d.pos < d.kb && (d.x < 0 || d.x >= P.V)) R.err |= kErrBadToken;
+      if (P.greedy) {
+        if ((bad & 1) || !(M > -INFINITY)) R.err |= kErrNonfinite;
+        P.ws.m_t[b * (P.k + 1) + d.pos] = M;
+        if (d.pos < d.kb) {
+          const bool acc = (d.x == arg);
+          P.ws.alpha[b * P.k + d.pos] = acc ? 1.f : 0.f;
+          if (!acc && R.a < 0) { R.a = d.pos; R.y = arg; }
+        } else if (R.a < 0) {
+          R.y = arg;
         }
-        report_item(P, b, kb, pos, C.g_arg_t);
-      }
-    } else {
-      // ---- acceptance test (identical in every CTA) ---------------------
-      const float Kt = C.g_Kt, Kd = C.g_Kd, Lt = C.g_Lt, Ld = C.g_Ld;
-      if (tid == 0) {
-        int accept = 0;
-        float alpha = NAN;
-        if (pair) {
-          const float zt = C.g_zt_x, zd = C.g_zd_x;
+      } else {
+        const float L = log2f(Ssum);
+        C.rowK[kind] = K;
+        C.rowL[kind] = L;
+        if ((bad & 1) || !(isfinite(M) && isfinite(Ssum) && Ssum > 0.f)) R.err |= kErrNonfinite;
+        if (kind == 0) {
+          P.ws.m_t[b * (P.k + 1) + d.pos] = M;
+          P.ws.L_t[b * (P.k + 1) + d.pos] = L;
+        } else {
+          P.ws.m_d[b * P.k + d.pos] = M;
+          P.ws.L_d[b * P.k + d.pos] = L;
+        }
+        if (kind == 1 && !R.err) {
+          // the pair is complete: acceptance test of draft d.pos
+          const float zt = C.zx[0], zd = C.zx[1];
+          float alpha;
           if (zt == -INFINITY) alpha = 0.f;               // p(x) = 0
           else if (zd == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
           else {
-            const float log2r = (fmaf(zt, c2, -Kt) - Lt) - (fmaf(zd, c2, -Kd) - Ld);
+            const float log2r = (fmaf(zt, c2, -C.rowK[0]) - C.rowL[0]) - (fmaf(zd, c2, -C.rowK[1]) - C.rowL[1]);
             alpha = log2r >= 0.f ? 1.f : exp2f(log2r);
           }
-          const float u = __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + pos);
-          accept = (u < alpha) ? 1 : 0;
-        }
-        C.g_accept = accept;
-        if (rank == 0) {
-          // debug: log-sum-exp(z/T) = m/T + L ln 2 (to within the rounding of fl(m c))
-          P.ws.m_t[slot_t] = C.g_Mt;
-          P.ws.L_t[slot_t] = Lt;
-          if (pair) {
-            P.ws.m_d[slot_d] = C.g_Md;
-            P.ws.L_d[slot_d] = Ld;
-            P.ws.alpha[slot_d] = alpha;
+          P.ws.alpha[b * P.k + d.pos] = alpha;
+          if (!(d.u < alpha) && R.a < 0) {
+            // first rejection: the producer re-reads this pair for the draw
+            R.a = d.pos;
+            R.Kt = C.rowK[0]; R.Lt = C.rowL[0]; R.Kd = C.rowK[1]; R.Ld = C.rowL[1];
+            R.pending += 1;
+            push_request(d.b, d.pos, d.rec, 1);
           }
+        } else if (kind == 0 && d.pos == d.kb && R.a < 0 && !R.err) {
+          bonus_draw = 1;   // every draft accepted: the bonus draw
+          R.Kt = K; R.Lt = L;
         }
-        int compute = 0;
-        if (pair && !accept) compute = atomicMin(P.ws.rej_min + b, pos) >= pos;
-        else if (!pair) compute = __ldcg(P.ws.rej_min + b) == kNoReject;
-        C.g_compute = compute;
       }
-      __syncthreads();
+      C.flag_bonus = bonus_draw;   // broadcast through the barrier below
+    }
+    consumer_sync();
+    if (C.flag_bonus) this->bonus_draw(d);
+    if (d.pos == d.kb && d.kind == 0) {
+      // the sequence's stream is done
+      if (ctid == 0) C.flag_finish = (--C.rec[d.rec].pending == 0) ? 1 : 0;
+      consumer_sync();
+      if (C.flag_finish) finish_sequence(d.rec);
+    }
+  }
 
-      if (pair && C.g_accept) {
-        if (leader) report_item(P, b, kb, pos, -2);
-      } else {
-        // ---- the draw ----------------------------------------------------
-        const float s_u = __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + k);
-        bool resid = pair;
-        auto vec_weights = [&](int v, float (&w)[NV]) {
-          float zt[NV], zd[NV];
-          V::load(T_ + v * 16, zt);
-          if (resid) V::load(D_ + v * 16, zd);
+  __device__ void push_request(int b, int pos, int rec, int mode) {
+    // single producer (this thread) / single consumer (the producer warp) ring
+    unsigned long long t0 = 0;
+    while (C.req_tail - C.req_head >= kReqs) {
+      if (!t0) t0 = global_ns();
+      if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
+        atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+        C.rec[rec].err |= kErrTimeout;
+        return;
+      }
+    }
+    const int tail = C.req_tail;
+    const int r = tail % kReqs;
+    C.req_b[r] = b; C.req_pos[r] = pos; C.req_rec[r] = rec; C.req_mode[r] = mode;
+    __threadfence_block();
+    C.req_tail = tail + 1;
+  }
+
+  // Warp 0: the segment holding s * S among `nseg` masses (index order).
+  // Writes C.S, C.seg, C.seg_t.
+  __device__ void locate(const double* mass, int nseg, float s) {
+    const int per = (nseg + 31) / 32;
+    const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
+    double gs = 0.0;
+    for (int i = g0; i < g1; ++i) gs += mass[i];
+    const double incl = warp_incl_scan(gs, lane);
+    const double excl = incl - gs;
+    const double Stot = __shfl_sync(0xffffffffu, incl, 31);
+    const double tgt = static_cast<double>(s) * Stot;
+    const unsigned hit = __ballot_sync(0xffffffffu, gs > 0.0 && tgt < incl);
+    const unsigned posg = __ballot_sync(0xffffffffu, gs > 0.0);
+    const int owner = hit ? (__ffs(hit) - 1) : (posg ? 31 - __clz(posg) : -1);
+    int seg = -1;
+    double seg_t = 0.0;
+    if (owner >= 0 && lane == owner) {
+      double run = excl, last_run = excl;
+      int last = -1;
+      for (int i = g0; i < g1; ++i) {
+        const double m = mass[i];
+        if (m > 0.0) { last = i; last_run = run; }
+        if (seg < 0 && m > 0.0 && tgt < run + m) { seg = i; seg_t = tgt - run; }
+        run += m;
+      }
+      if (seg < 0) { seg = last; seg_t = tgt - last_run; }
+    }
+    if (owner >= 0) {
+      seg = __shfl_sync(0xffffffffu, seg, owner);
+      seg_t = __shfl_sync(0xffffffffu, seg_t, owner);
+    }
+    if (lane == 0) { C.S = Stot; C.seg = seg; C.seg_t = seg_t; }
+  }
+
+  // Warp 0: walk `nsteps` x 32 vectors starting at vector v0 of the row(s),
+  // a warp inclusive scan per step, to the token where the running weight
+  // passes t.  resid: weights max(0, p - q); else p.
+  template <int NSTEPS, bool RESID>
+  __device__ int walk(int v0, double t, const unsigned char* rowT, const unsigned char* rowD,
+                      float Kt, float Lt, float Kd, float Ld) const {
+    // all loads first (raw), then the scan
+    uint4 rt[NSTEPS], rd[RESID ? NSTEPS : 1];
+#pragma unroll
+    for (int j = 0; j < NSTEPS; ++j) {
+      rt[j] = load_global_raw(rowT, v0 + j * 32 + lane);
+      if (RESID) rd[RESID ? j : 0] = load_global_raw(rowD, v0 + j * 32 + lane);
+    }
+    double base = 0.0;
+    int found = -1, last_positive = -1;
+#pragma unroll
+    for (int j = 0; j < NSTEPS; ++j) {
+      float w[NV], zt[NV], zd[NV];
+      V::unpack(rt[j], zt);
+      if (RESID) V::unpack(rd[RESID ? j : 0], zd);
+      float ls = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const float p = fast_exp2(fmaf(zt[e], P.c2, -Kt) - Lt);
+        w[e] = RESID ? fmaxf(p - fast_exp2(fmaf(zd[e], P.c2, -Kd) - Ld), 0.f) : p;
+        ls += w[e];
+      }
+      const float incl = warp_incl_scan(ls, lane);
+      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.f;
+      const float step_total = __shfl_sync(0xffffffffu, incl, 31);
+      const int x0 = (v0 + j * 32 + lane) * NV;
+      const bool mine = found < 0 && ls > 0.f && t < base + static_cast<double>(incl) &&
+                        !(t < base + static_cast<double>(excl));
+      const unsigned hit = __ballot_sync(0xffffffffu, mine);
+      int lp = -1;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) if (w[e] > 0.f) lp = x0 + e;
+      const unsigned anyp = __ballot_sync(0xffffffffu, lp >= 0);
+      if (found < 0 && anyp) last_positive = __shfl_sync(0xffffffffu, lp, 31 - __clz(anyp));
+      if (hit) {
+        const int hl = __ffs(hit) - 1;
+        int pick = -1;
+        if (lane == hl) {
+          double c = base + static_cast<double>(excl);
+          int lastp = -1;
 #pragma unroll
           for (int e = 0; e < NV; ++e) {
-            const float p = fast_exp2(fmaf(zt[e], c2, -Kt) - Lt);
-            w[e] = resid ? fmaxf(p - fast_exp2(fmaf(zd[e], c2, -Kd) - Ld), 0.f) : p;
+            if (w[e] > 0.f) lastp = x0 + e;
+            c += static_cast<double>(w[e]);
+            if (pick < 0 && w[e] > 0.f && t < c) pick = x0 + e;
           }
-        };
-        int zero_resid = 0, y = -2, reporter = 0;
-        for (int attempt = 0; attempt < 2; ++attempt) {
-          double wW = 0.0;
-          if (C.g_compute) {
-            float acc = 0.f;
-            for (int v = v0 + lane; v < v1; v += 32) {
-              float w[NV];
-              vec_weights(v, w);
-              float ls = 0.f;
-#pragma unroll
-              for (int e = 0; e < NV; ++e) ls += w[e];
-              acc += ls;
-            }
-            wW = static_cast<double>(warp_sum(acc));
-          }
-          if (lane == 0) C.warp_W[warp] = wW;
-          __syncthreads();
-          if (tid == 0) {
-            double t = 0.0;
-            for (int w = 0; w < NW; ++w) t += C.warp_W[w];
-            C.pub[pb].W = t;
-            C.pub[pb].skip = C.g_compute ? 0 : 1;
-          }
-          cluster_barrier();  // B
-          if (warp == 0) {
-            const bool in = lane < static_cast<int>(CS);
-            const double Wr = in ? ld_remote_f64(&C.pub[pb].W, static_cast<uint32_t>(lane)) : 0.0;
-            const int sk = in ? ld_remote_s32(&C.pub[pb].skip, static_cast<uint32_t>(lane)) : 0;
-            double incl = Wr;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const double up = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += up;
-            }
-            double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (lane == 0) excl = 0.0;
-            const double Stot = __shfl_sync(0xffffffffu, incl, 31);
-            const double tgt = static_cast<double>(s_u) * Stot;
-            const unsigned hit = __ballot_sync(0xffffffffu, in && tgt < incl);
-            const unsigned pos_w = __ballot_sync(0xffffffffu, in && Wr > 0.0);
-            const int rstar = hit ? (__ffs(hit) - 1) : (pos_w ? 31 - __clz(pos_w) : -1);
-            const double before = __shfl_sync(0xffffffffu, excl, rstar < 0 ? 0 : rstar);
-            const int skip = warp_or(sk);
-            if (lane == 0) {
-              C.g_skip = skip;
-              C.g_rstar = rstar;
-              C.g_S = Stot;
-              C.g_target = tgt - before;
-            }
-          }
-          __syncthreads();
-          if (C.g_skip) break;           // an earlier position rejected: never used
-          if (!(C.g_S > 0.0)) {
-            if (resid) {
-              // exact arithmetic rules this out (a rejection implies p > q
-              // somewhere); draw from p_a instead and count it
-              zero_resid = 1;
-              resid = false;
-              cluster_barrier();         // pub W read everywhere before it is rewritten
-              continue;
-            }
-            break;
-          }
-          reporter = C.g_rstar;
-          if (static_cast<int>(rank) == C.g_rstar) {
-            if (tid == 0) {
-              const double t = C.g_target;
-              double run = 0.0, last_run = 0.0;
-              int wstar = -1, wlast = 0;
-              for (int w = 0; w < NW; ++w) {
-                const double Ww = C.warp_W[w];
-                if (Ww > 0.0) { wlast = w; last_run = run; }
-                if (wstar < 0 && t < run + Ww) { wstar = w; C.g_target = t - run; }
-                run += Ww;
-              }
-              if (wstar < 0) { wstar = wlast; C.g_target = t - last_run; }
-              C.g_found_warp = wstar;
-              C.g_y = -1;
-            }
-            __syncthreads();
-            if (warp == C.g_found_warp) {
-              // walk the chunk 32 vectors at a time with a warp inclusive scan
-              const double t = C.g_target;
-              double base = 0.0;
-              int found = -1, last_positive = -1;
-              for (int vb = v0; vb < v1 && found < 0; vb += 32) {
-                const int v = vb + lane;
-                float w[NV];
-                float ls = 0.f;
-                if (v < v1) {
-                  vec_weights(v, w);
-#pragma unroll
-                  for (int e = 0; e < NV; ++e) ls += w[e];
-                } else {
-#pragma unroll
-                  for (int e = 0; e < NV; ++e) w[e] = 0.f;
-                }
-                float incl = ls;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                  const float up = __shfl_up_sync(0xffffffffu, incl, o);
-                  if (lane >= o) incl += up;
-                }
-                float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-                if (lane == 0) excl = 0.f;
-                const float step_total = __shfl_sync(0xffffffffu, incl, 31);
-                const bool mine = ls > 0.f && t < base + static_cast<double>(incl) &&
-                                  !(t < base + static_cast<double>(excl));
-                const unsigned hit = __ballot_sync(0xffffffffu, mine);
-                int lp = -1;
-#pragma unroll
-                for (int e = 0; e < NV; ++e) if (w[e] > 0.f) lp = lo + v * NV + e;
-                const unsigned anyp = __ballot_sync(0xffffffffu, lp >= 0);
-                if (anyp) last_positive = __shfl_sync(0xffffffffu, lp, 31 - __clz(anyp));
-                if (hit) {
-                  const int hl = __ffs(hit) - 1;
-                  int pick = -1;
-                  if (lane == hl) {
-                    double c = base + static_cast<double>(excl);
-                    int lastp = -1;
-#pragma unroll
-                    for (int e = 0; e < NV; ++e) {
-                      if (w[e] > 0.f) lastp = lo + v * NV + e;
-                      c += static_cast<double>(w[e]);
-                      if (pick < 0 && w[e] > 0.f && t < c) pick = lo + v * NV + e;
-                    }
-                    if (pick < 0) pick = lastp;
-                  }
-                  found = __shfl_sync(0xffffffffu, pick, hl);
-                }
-                base += static_cast<double>(step_total);
-              }
-              if (found < 0) found = last_positive;
-              if (lane == 0) C.g_y = found;
-            }
-            __syncthreads();
-            y = C.g_y;
-          }
-          break;
+          if (pick < 0) pick = lastp;
         }
-        if (static_cast<int>(rank) == reporter && tid == 0) {
-          P.ws.mass[slot_t] = C.g_skip ? NAN : static_cast<float>(C.g_S);
-          if (zero_resid && !C.g_skip) atomicAdd(P.ws.stats + kStatZeroResidual, 1ull);
-          report_item(P, b, kb, pos, y);
+        found = __shfl_sync(0xffffffffu, pick, hl);
+      }
+      base += static_cast<double>(step_total);
+    }
+    return found >= 0 ? found : last_positive;
+  }
+
+  // The bonus draw of the sequence whose last row just ended (blocking; the
+  // producer keeps the ring full meanwhile): masses from the sums kept while
+  // streaming, then one stream segment of the bonus row is read again.
+  __device__ void bonus_draw(const Desc& d) {
+    const int ctid = warp * 32 + lane;
+    SeqRec& R = C.rec[d.rec];
+    const float Kt = R.Kt, Lt = R.Lt;
+    const int nseg = nchunks * kConsumerWarps;
+    for (int sg = ctid; sg < nseg; sg += kConsumerWarps * 32) {
+      const float ks = C.segK[sg];
+      C.bmass[sg] = ks == -INFINITY ? 0.0
+                    : static_cast<double>(C.segS[sg]) * static_cast<double>(fast_exp2(__fsub_rn(ks, Kt) - Lt));
+    }
+    consumer_sync();
+    if (warp == 0) {
+      locate(C.bmass, nseg, R.s);
+      __syncwarp();
+      const int seg = C.seg;
+      int y = -1;
+      if (seg >= 0)
+        y = walk<kVecsPerLane, false>(seg * kVecsPerWarp, C.seg_t, row_ptr(d.b, d.kb, 0), nullptr, Kt, Lt, 0.f, 0.f);
+      if (lane == 0) {
+        R.y = y;
+        P.ws.mass[static_cast<size_t>(d.b) * (P.k + 1) + d.kb] = static_cast<float>(C.S);
+      }
+    }
+    consumer_sync();
+  }
+
+  // One chunk of a pair's re-read: per-segment weights of the draw; the last
+  // chunk locates the token.
+  __device__ void draw_chunk(const Desc& d, int slot, int timed_out) {
+    SeqRec& R = C.rec[d.rec];
+    const bool resid = (d.x == 1);
+    const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
+    const long long off = static_cast<long long>(d.chunk) * kHalfBytes;
+    const long long rem = row_bytes - off;
+    const int nvec = static_cast<int>(((rem < kHalfBytes ? rem : kHalfBytes) + 15) / 16);
+    uint4 rt[kDrawVecsPerLane], rd[kDrawVecsPerLane];
+#pragma unroll
+    for (int j = 0; j < kDrawVecsPerLane; ++j) {
+      const int v = warp * kDrawVecsPerWarp + j * 32 + lane;
+      const bool in = v < nvec;
+      rt[j] = in ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
+      rd[j] = (in && resid) ? *reinterpret_cast<const uint4*>(data + kHalfBytes + static_cast<size_t>(v) * 16)
+                            : V::neg_inf();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&C.empty[slot]);
+    if (timed_out && lane == 0) atomicOr(&R.err, kErrTimeout);
+    const float c2 = P.c2;
+    const float Kt = R.Kt, Lt = R.Lt, Kd = R.Kd, Ld = R.Ld;
+    const f2 cc = pack2(c2, c2), nkt = pack2(-Kt, -Kt), nlt = pack2(-Lt, -Lt);
+    const f2 nkd = pack2(-Kd, -Kd), nld = pack2(-Ld, -Ld);
+    f2 acc[NV / 2];
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
+#pragma unroll
+    for (int j = 0; j < kDrawVecsPerLane; ++j) {
+      f2 zt[NV / 2], zd[NV / 2];
+      V::pairs(rt[j], zt);
+      V::pairs(rd[j], zd);
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        // the same roundings as the scalar fmaf(z, c, -K) - L of the walk
+        const f2 p = exp2_2(add2(fma2(zt[i], cc, nkt), nlt));
+        if (resid) {
+          float d0, d1;
+          unpack2(sub2(p, exp2_2(add2(fma2(zd[i], cc, nkd), nld))), d0, d1);
+          acc[i] = add2(acc[i], pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+        } else {
+          acc[i] = add2(acc[i], p);
         }
       }
     }
+    float a0, a1, sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); sum += a0 + a1; }
+    const float ws = warp_sum(sum);
+    const int sg = d.chunk * kConsumerWarps + warp;
+    if (lane == 0) C.rmass[sg] = static_cast<double>(ws);
+    if (d.chunk != d.nchunks - 1) return;
 
-    // ---- buffer s is free: stage the item S positions ahead ---------------
-    __syncthreads();
-    if (tid == 0) stage(s, next_t);
-    if (!P.bulk) {
-      __syncthreads();
-      stage_plain(s);
+    // last chunk: the total, the segment, the token
+    consumer_sync();
+    const int nseg = d.nchunks * kConsumerWarps;
+    if (warp == 0) {
+      locate(C.rmass, nseg, R.s);
+      __syncwarp();
+      if (C.S > 0.0 || !resid) {
+        const int seg = C.seg;
+        int y = -1;
+        if (seg >= 0) {
+          if (resid)
+            y = walk<kDrawVecsPerLane, true>(seg * kDrawVecsPerWarp, C.seg_t, row_ptr(d.b, d.pos, 0),
+                                             row_ptr(d.b, d.pos, 1), Kt, Lt, Kd, Ld);
+          else
+            y = walk<kDrawVecsPerLane, false>(seg * kDrawVecsPerWarp, C.seg_t, row_ptr(d.b, d.pos, 0),
+                                              nullptr, Kt, Lt, Kd, Ld);
+        }
+        if (lane == 0) {
+          R.y = y;
+          P.ws.mass[static_cast<size_t>(d.b) * (P.k + 1) + d.pos] = static_cast<float>(C.S);
+          C.flag_finish = (--R.pending == 0) ? 1 : 0;
+        }
+      } else if (lane == 0) {
+        // exact arithmetic rules a zero residual out (a rejection implies
+        // p > q somewhere); draw from p_a instead and count it
+        R.zero_resid = 1;
+        push_request(d.b, d.pos, d.rec, 2);
+        C.flag_finish = 0;
+      }
     }
-    __syncthreads();
+    consumer_sync();
+    if (C.flag_finish) finish_sequence(d.rec);
   }
-  cluster_barrier();  // no CTA leaves while others may still read its shared memory
+
+  // Outputs of a sequence whose stream and draw are both done.
+  __device__ void finish_sequence(int rec) {
+    if (warp == 0) {
+      const SeqRec& R = C.rec[rec];
+      const int k = P.k;
+      const size_t b = static_cast<size_t>(R.b);
+      int* ot = P.out_tokens + b * (k + 1);
+      const int err = R.err;
+      const int a = R.a < 0 ? R.kb : R.a;
+      const int y = R.y;
+      const bool ok = !err && y >= 0;
+      for (int j = lane; j <= k; j += 32) {
+        int v = -1;
+        if (ok) v = j < a ? __ldg(P.tokens + b * k + j) : (j == a ? y : -1);
+        ot[j] = v;
+      }
+      if (lane == 0) {
+        P.out_len[b] = ok ? a + 1 : 0;
+        if (ok) {
+          atomicAdd(P.ws.stats + kStatSequences, 1ull);
+          atomicAdd(P.ws.stats + kStatProposed, static_cast<unsigned long long>(R.kb));
+          atomicAdd(P.ws.stats + kStatAccepted, static_cast<unsigned long long>(a));
+          atomicAdd(P.ws.stats + kStatEmitted, static_cast<unsigned long long>(a + 1));
+          if (R.kb == 0) atomicAdd(P.ws.stats + kStatSpecOff, 1ull);
+          if (R.zero_resid) atomicAdd(P.ws.stats + kStatZeroResidual, 1ull);
+        } else {
+          atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
+          unsigned bits = static_cast<unsigned>(err & (kErrBadToken | kErrNonfinite | kErrTimeout));
+          if (!bits) bits = kErrNonfinite;   // no token could be drawn
+          atomicOr(P.ws.err_word, bits);
+        }
+        __threadfence_block();
+        C.seqs_finished = C.seqs_finished + 1;
+      }
+    }
+  }
+};
+
+template <int ELT>
+__global__ void __launch_bounds__(kThreads, 1)
+verify_kernel(const VerifyParams P) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  Ctrl& C = *reinterpret_cast<Ctrl*>(smem);
+  unsigned char* ring = smem + kCtrlBytes;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < P.stages; ++s) {
+      mbar_init(&C.full[s], 1);
+      mbar_init(&C.empty[s], kConsumerWarps);
+    }
+    C.req_head = 0;
+    C.req_tail = 0;
+    C.seqs_finished = 0;
+    for (int r = 0; r < kRecs; ++r) C.rec[r].pending = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_dependency_wait();           // the work list of plan_kernel is ready
+  Verifier<ELT> v(P, C, ring, lane, warp);
+  if (warp == kConsumerWarps) v.produce();
+  else v.consume();
 }
 
 // ---------------------------------------------------------------------------
@@ -929,15 +1190,10 @@ __global__ void debug_kernel(Workspace ws, int B, int k, int greedy, float inv_T
   }
 }
 
-__global__ void init_workspace_kernel(Workspace ws, int max_B) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < max_B) {
-    ws.done[i] = 0;
-    ws.rej_min[i] = kNoReject;
-    ws.seq_err[i] = 0;
-  }
+__global__ void init_workspace_kernel(Workspace ws) {
+  const int i = threadIdx.x;
   if (i < kStatCount) ws.stats[i] = 0ull;
-  if (i == 0) { *ws.err_word = 0u; *ws.n_items = 0; *ws.ticket = 0; }
+  if (i == 0) { *ws.err_word = 0u; *ws.n_seqs = 0; *ws.ticket = 0; }
 }
 
 }  // namespace
@@ -946,50 +1202,37 @@ __global__ void init_workspace_kernel(Workspace ws, int max_B) {
 // Launchers
 // ---------------------------------------------------------------------------
 
-cudaError_t prepare_verify_kernel(int smem_bytes, int cluster) {
+int verify_smem_bytes(int stages) { return kCtrlBytes + stages * kChunkBytes; }
+
+cudaError_t prepare_verify_kernel(int smem_bytes) {
   const void* fns[2] = {reinterpret_cast<const void*>(&verify_kernel<2>),
                         reinterpret_cast<const void*>(&verify_kernel<4>)};
   for (const void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    if (cluster > 8) {
-      e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
   }
   return cudaSuccess;
 }
 
-static cudaLaunchConfig_t verify_config(int nclusters, int cluster, int smem_bytes, cudaStream_t s,
-                                        cudaLaunchAttribute* attr, bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(nclusters) * static_cast<unsigned>(cluster), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
-  cfg.stream = s;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
-  return cfg;
+cudaError_t query_ctas_per_sm(int smem_bytes, int* out) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, verify_kernel<2>, kThreads,
+                                                       static_cast<size_t>(smem_bytes));
 }
 
-cudaError_t query_max_active_clusters(int cluster, int smem_bytes, int* out) {
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = verify_config(1, cluster, smem_bytes, nullptr, attr, false);
-  return cudaOccupancyMaxActiveClusters(out, reinterpret_cast<const void*>(&verify_kernel<2>), &cfg);
-}
-
-cudaError_t launch_verify(const VerifyParams& p, int cluster, int clusters, int smem_bytes, cudaStream_t s) {
+cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s) {
   plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = verify_config(clusters, cluster, smem_bytes, s, attr, true);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (p.elt == 2) return cudaLaunchKernelEx(&cfg, verify_kernel<2>, p);
   return cudaLaunchKernelEx(&cfg, verify_kernel<4>, p);
 }
@@ -1007,9 +1250,8 @@ cudaError_t launch_debug(const Workspace& ws, int B, int k, int greedy, float in
   return cudaGetLastError();
 }
 
-cudaError_t launch_init_workspace(const Workspace& ws, int max_B, cudaStream_t s) {
-  const int n = max_B > kStatCount ? max_B : kStatCount;
-  init_workspace_kernel<<<(n + 255) / 256, 256, 0, s>>>(ws, max_B);
+cudaError_t launch_init_workspace(const Workspace& ws, cudaStream_t s) {
+  init_workspace_kernel<<<1, 32, 0, s>>>(ws);
   return cudaGetLastError();
 }
 

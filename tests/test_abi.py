@@ -56,8 +56,9 @@ def test_null_context_is_rejected_on_the_host(lib):
 
 def test_create_rejects_bad_sizes_before_any_cuda_call(lib):
     h = ctypes.c_void_p()
-    for args in [(0, 3, 100, 1), (4, -1, 100, 1), (4, 3, 0, 1), (4, 3, 100, 7), (1 << 25, 7, 100, 1)]:
-        assert lib.sv_create(ctypes.byref(h), *args) == svp.SV_ERR_INVALID_ARG
+    for args in [(0, 3, 100, 1), (4, -1, 100, 1), (4, 3, 0, 1), (4, 3, 100, 7), (1 << 25, 7, 100, 1),
+                 (4, 32, 100, 1), (4, 3, 1 << 20, 0)]:
+        assert lib.sv_create(ctypes.byref(h), *args) == svp.SV_ERR_INVALID_ARG, args
     assert lib.sv_create(None, 4, 3, 100, 1) == svp.SV_ERR_INVALID_ARG
 
 
