@@ -7,7 +7,7 @@
 namespace sv {
 
 constexpr int kConsumerWarps = 16;                      // warps that compute
-constexpr int kThreads = (kConsumerWarps + 1) * 32;     // + one producer warp
+constexpr int kThreads = (kConsumerWarps + 2) * 32;     // + a producer and a control warp
 constexpr int kVecsPerLane = 8;                         // 16-byte vectors per lane and chunk
 constexpr int kVecsPerWarp = kVecsPerLane * 32;         // 256 x 16 B per warp and chunk
 constexpr int kChunkBytes = kVecsPerWarp * 16 * kConsumerWarps;  // one staging slot: 64 KB

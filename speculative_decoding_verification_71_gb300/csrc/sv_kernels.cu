@@ -113,11 +113,6 @@ __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Barrier of the consumer warps only (the producer never joins it).
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" :: "n"(kConsumerWarps * 32) : "memory");
-}
-
 // 2^x on the special-function unit (PTX ex2.approx; -inf -> +0, NaN -> NaN).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -287,6 +282,16 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
   return v;
 }
 
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+  return done != 0;
+}
+
 // ---------------------------------------------------------------------------
 // Shared control block
 // ---------------------------------------------------------------------------
@@ -295,27 +300,45 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 //   kind 0 / 1: chunk `chunk` of the target / draft row at position pos;
 //   kind 2:     chunk `chunk` of the re-read of the pair at pos for its draw:
 //               the first half of the slot holds target logits, the second
-//               half the draft logits of the same vocabulary range (x holds
-//               the draw mode: 1 residual max(0, p - q), 2 p alone);
+//               half the draft logits of the same vocabulary range; x holds
+//               the draw mode (1: residual max(0, p - q), 2: p alone) and
+//               K0, L0, K1, L1 the pair's normalisers;
 //   kind -1:    no more work.
 struct Desc {
   int b, kb, pos, kind;
   int chunk, nchunks, x, rec;  // x: drafted token at pos (rows of pairs, else -1); rec: sequence record
   float u, s;                  // accept uniform at pos, sampling uniform of b
+  float K0, L0, K1, L1;
 };
 
-// One sequence in flight.  Its stream and its draw can finish in either
-// order; the outputs are written when both are done.
+// A finished row, published by the consumer warps for the control warp.
+struct RowBuf {
+  Desc d;
+  float wK[kConsumerWarps], wS[kConsumerWarps], wM[kConsumerWarps];
+  int wArg[kConsumerWarps], wBad[kConsumerWarps];
+  float zx;                                  // logit of the drafted token
+  float segK[kMaxChunks * kConsumerWarps];   // bonus rows: per-segment fl(m c)
+  float segS[kMaxChunks * kConsumerWarps];   // bonus rows: per-segment sum
+};
+
+// One sequence in flight (control warp only).  Its stream and its draw can
+// finish in either order; the outputs are written when both are done.
 struct SeqRec {
   int b, kb, a, err, y, zero_resid;
   int pending;                 // events left before the outputs can be written
-  float Kt, Lt, Kd, Ld;        // normalisers of the pair being drawn from
   float s;                     // sampling uniform
+};
+
+// A re-read request as the control warp remembers it.
+struct DrawReq {
+  int b, pos, rec, mode;
+  float Kt, Lt, Kd, Ld;
 };
 
 constexpr int kRecs = 8;       // sequence records (ring)
 constexpr int kReqs = 8;       // re-read requests (ring)
-constexpr int kHalfBytes = kChunkBytes / 2;                   // one row's part of a draw chunk
+constexpr int kRowBufs = 4;    // row buffers (ring)
+constexpr int kHalfBytes = kChunkBytes / 2;                          // one row's part of a draw chunk
 constexpr int kDrawVecsPerWarp = kHalfBytes / 16 / kConsumerWarps;   // 128
 constexpr int kDrawVecsPerLane = kDrawVecsPerWarp / 32;              // 4
 constexpr int kMaxDrawSegs = 2 * kMaxChunks * kConsumerWarps;
@@ -323,29 +346,26 @@ constexpr int kMaxDrawSegs = 2 * kMaxChunks * kConsumerWarps;
 enum : int { kErrBadToken = 1 << 3, kErrNonfinite = 1 << 4, kErrTimeout = 1 << 5 };
 
 struct Ctrl {
-  uint64_t full[kMaxStages];   // slot filled (producer -> consumers)
-  uint64_t empty[kMaxStages];  // slot released (one arrival per consumer warp)
+  uint64_t full[kMaxStages];        // slot filled (producer -> consumers)
+  uint64_t empty[kMaxStages];       // slot released (one arrival per consumer warp)
+  uint64_t row_ready[kRowBufs];     // row published (one arrival per consumer warp)
+  uint64_t row_free[kRowBufs];      // row consumed by the control warp
+  uint64_t draw_ready[2];           // draw masses complete (one arrival per consumer warp)
+  uint64_t draw_free[2];            // draw masses consumed by the control warp
   Desc desc[kMaxStages];
-  // per-warp row state published at a row end
-  float wK[kConsumerWarps], wS[kConsumerWarps], wM[kConsumerWarps];
-  int wArg[kConsumerWarps], wBad[kConsumerWarps];
-  // the current pair: [0] target row, [1] draft row
-  float zx[2];
-  float rowK[2], rowL[2];
-  SeqRec rec[kRecs];
-  // re-read requests: consumer thread 0 pushes, the producer pops
-  int req_b[kReqs], req_pos[kReqs], req_rec[kReqs], req_mode[kReqs];
+  RowBuf rows[kRowBufs];
+  double rmass[2][kMaxDrawSegs];    // per-segment weights of a re-read draw
+  int draw_err[2];
+  // re-read requests: the control warp pushes, the producer pops
+  DrawReq req[kReqs];
   volatile int req_head, req_tail;
-  volatile int seqs_finished;  // sequences whose outputs are written
-  // broadcasts from consumer thread 0 / warp 0 to the consumer warps
-  int flag_bonus, flag_finish;
-  // the draw being located
-  int seg;
-  double seg_t, S;
-  float segK[kMaxChunks * kConsumerWarps];   // bonus row: per-segment fl(m c)
-  float segS[kMaxChunks * kConsumerWarps];   // bonus row: per-segment sum
-  double bmass[kMaxChunks * kConsumerWarps]; // bonus draw: weight per stream segment
-  double rmass[kMaxDrawSegs];                // re-read draws: weight per draw segment
+  volatile int seqs_finished;       // sequences whose outputs are written
+  // control warp state
+  SeqRec rec[kRecs];
+  DrawReq ctl_req[kReqs];           // every pushed request, by push order, until its draw is done
+  int pushed;                       // requests pushed so far
+  float pairK, pairL, pairZx;       // target row of the current pair
+  double bmass[kMaxChunks * kConsumerWarps];
 };
 
 constexpr int kCtrlBytes = ((static_cast<int>(sizeof(Ctrl)) + 1023) / 1024) * 1024;
@@ -456,18 +476,18 @@ struct Verifier {
     return *reinterpret_cast<const uint4*>(buf);
   }
 
-  // ======================= producer ==========================================
-
-  // Wait for slot q%S to be free (lane 0 waits, the warp follows).
-  __device__ bool acquire_slot(int q) {
-    const int S = P.stages;
+  // Bounded wait by lane 0 for the whole warp; false (and the error word
+  // set) if nothing happened for 1 s.
+  __device__ bool warp_wait(uint64_t* bar, uint32_t parity) const {
     int ok = 1;
-    if (lane == 0) ok = mbar_wait_bounded(&C.empty[q % S], ((q / S) & 1) ^ 1, kDrainLimitNs) ? 1 : 0;
+    if (lane == 0) ok = mbar_wait_bounded(bar, parity, kDrainLimitNs) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok && lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
     __syncwarp();
     return ok != 0;
   }
+
+  // ======================= producer ==========================================
 
   // Copy `bytes` of a row starting at byte `off` into dst (bulk or plain).
   __device__ void fill(unsigned char* dst, const unsigned char* src, long long off, int bytes,
@@ -489,6 +509,11 @@ struct Verifier {
     }
   }
 
+  __device__ bool acquire_slot(int q) {
+    const int S = P.stages;
+    return warp_wait(&C.empty[q % S], ((q / S) & 1) ^ 1);
+  }
+
   // Issue the draw chunks of every queued re-read request.
   __device__ bool service_requests(int& q) {
     const int S = P.stages;
@@ -498,12 +523,11 @@ struct Verifier {
       head = __shfl_sync(0xffffffffu, head, 0);
       tail = __shfl_sync(0xffffffffu, tail, 0);
       if (head == tail) return true;
-      const int r = head % kReqs;
-      const int b = C.req_b[r], pos = C.req_pos[r], rec = C.req_rec[r], mode = C.req_mode[r];
+      const DrawReq r = C.req[head % kReqs];
       __syncwarp();
       if (lane == 0) { __threadfence_block(); C.req_head = head + 1; }
-      const unsigned char* srcT = row_ptr(b, pos, 0);
-      const unsigned char* srcD = row_ptr(b, pos, 1);
+      const unsigned char* srcT = row_ptr(r.b, r.pos, 0);
+      const unsigned char* srcD = row_ptr(r.b, r.pos, 1);
       for (int c = 0; c < ndraw; ++c) {
         if (!acquire_slot(q)) return false;
         const int slot = q % S;
@@ -513,13 +537,14 @@ struct Verifier {
         unsigned char* dst = ring + static_cast<size_t>(slot) * kChunkBytes;
         if (lane == 0) {
           Desc& d = C.desc[slot];
-          d.b = b; d.kb = 0; d.pos = pos; d.kind = 2;
-          d.chunk = c; d.nchunks = ndraw; d.x = mode; d.rec = rec;
+          d.b = r.b; d.kb = 0; d.pos = r.pos; d.kind = 2;
+          d.chunk = c; d.nchunks = ndraw; d.x = r.mode; d.rec = r.rec;
           d.u = 0.f; d.s = 0.f;
-          if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(mode == 1 ? 2 * bytes : bytes));
+          d.K0 = r.Kt; d.L0 = r.Lt; d.K1 = r.Kd; d.L1 = r.Ld;
+          if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(r.mode == 1 ? 2 * bytes : bytes));
         }
         fill(dst, srcT, off, bytes, &C.full[slot], false, 0);
-        if (mode == 1) fill(dst + kHalfBytes, srcD, off, bytes, &C.full[slot], false, 0);
+        if (r.mode == 1) fill(dst + kHalfBytes, srcD, off, bytes, &C.full[slot], false, 0);
         if (!P.bulk) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&C.full[slot]);
@@ -535,19 +560,37 @@ struct Verifier {
     const int n_seqs = __ldcg(P.ws.n_seqs);
     const uint64_t evict_first = evict_first_policy();
     int q = 0, streamed = 0;
+    // the next sequence's work-list entry, tokens and uniforms are fetched one
+    // sequence ahead so that a sequence start never waits on global memory
     int t = 0;
     if (lane == 0) t = atomicAdd(P.ws.ticket, 1);
     t = __shfl_sync(0xffffffffu, t, 0);
+    int2 sq = make_int2(-1, 0);
+    int xj = -1;
+    float uj = 0.f;
+    auto fetch = [&](int tt, int2& s_, int& x_, float& u_) {
+      s_ = make_int2(-1, 0);
+      x_ = -1;
+      u_ = 0.f;
+      if (tt < n_seqs) {
+        s_ = __ldcg(P.ws.seqs + tt);
+        x_ = lane < s_.y ? __ldg(P.tokens + static_cast<size_t>(s_.x) * k + lane) : -1;
+        u_ = (!P.greedy && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(s_.x) * (k + 1) + lane) : 0.f;
+      }
+    };
+    fetch(t, sq, xj, uj);
     bool ok = true;
     while (ok && t < n_seqs) {
-      const int2 sq = __ldcg(P.ws.seqs + t);
       const int b = sq.x, kb = sq.y;
       const int rec = streamed % kRecs;
+      // the next ticket is taken when this sequence's last row starts: late
+      // enough that sequences keep going to whichever CTA frees up first
+      // (longest first), early enough to hide the fetch behind that row
       int t_next = 0;
-      if (lane == 0) t_next = atomicAdd(P.ws.ticket, 1);
-      // the sequence's drafted tokens and uniforms, one per lane
-      const int xj = lane < kb ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
-      const float uj = (!P.greedy && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
+      int2 sq_next = make_int2(-1, 0);
+      int xj_next = -1;
+      float uj_next = 0.f;
+      bool fetched = false;
       const float s_samp = __shfl_sync(0xffffffffu, uj, k);
       const int nrows = P.greedy ? kb + 1 : 2 * kb + 1;
       for (int r = 0; r < nrows && ok; ++r) {
@@ -580,11 +623,25 @@ struct Verifier {
             if (lane == 0) mbar_arrive(&C.full[slot]);
           }
           ++q;
+          if (!fetched && r == nrows - 1) {
+            if (lane == 0) t_next = atomicAdd(P.ws.ticket, 1);
+            t_next = __shfl_sync(0xffffffffu, t_next, 0);
+            fetch(t_next, sq_next, xj_next, uj_next);
+            fetched = true;
+          }
           ok = service_requests(q);
         }
       }
+      if (!fetched) {
+        if (lane == 0) t_next = atomicAdd(P.ws.ticket, 1);
+        t_next = __shfl_sync(0xffffffffu, t_next, 0);
+        fetch(t_next, sq_next, xj_next, uj_next);
+      }
       ++streamed;
-      t = __shfl_sync(0xffffffffu, t_next, 0);
+      t = t_next;
+      sq = sq_next;
+      xj = xj_next;
+      uj = uj_next;
     }
     // no more sequences: keep serving re-reads until every streamed sequence
     // is finished, then signal the end (bounded: 1 s without progress)
@@ -601,7 +658,7 @@ struct Verifier {
         if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
         break;
       }
-      __nanosleep(200);
+      __nanosleep(256);
     }
     if (acquire_slot(q)) {
       if (lane == 0) {
@@ -612,14 +669,16 @@ struct Verifier {
   }
 
   // ======================= consumers =========================================
+  // They never wait on each other: a finished row is published into a ring
+  // of row buffers, a re-read's weights into a pair of mass arrays, and the
+  // control warp takes it from there.
 
   __device__ void consume() {
     const int S = P.stages;
     const float c2 = P.c2;
-    // warp-uniform running state of the current row
-    float rK = -INFINITY, rS = 0.f, rM = -INFINITY;
+    float rK = -INFINITY, rS = 0.f, rM = -INFINITY;   // running state of the current row
     int rArg = 0x7fffffff, rBad = 0;
-    int q = 0;
+    int q = 0, rr = 0, dr = 0;                        // slots, rows, re-reads seen
     while (true) {
       const int slot = q % S;
       const uint32_t par = static_cast<uint32_t>(q / S) & 1u;
@@ -627,19 +686,88 @@ struct Verifier {
       if (!mbar_wait_bounded(&C.full[slot], par, P.wait_limit_ns)) {
         timed_out = 1;
         if (!mbar_wait_bounded(&C.full[slot], par, kDrainLimitNs)) {
-          if (warp == 0 && lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-          return;   // the producer is gone; nothing is left in flight for this slot
+          if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+          return;   // the producer is gone
         }
       }
       const Desc d = C.desc[slot];
-      if (d.kind < 0) return;
+      if (d.kind < 0) {
+        // tell the control warp that the work is over
+        const int buf = rr % kRowBufs;
+        if (!warp_wait(&C.row_free[buf], ((rr / kRowBufs) & 1) ^ 1)) return;
+        if (warp == 0 && lane == 0) C.rows[buf].d.kind = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.row_ready[buf]);
+        return;
+      }
+
       if (d.kind == 2) {
-        draw_chunk(d, slot, timed_out);
+        // ---- a chunk of a pair's re-read: per-segment draw weights --------
+        const int dp = dr & 1;
+        if (d.chunk == 0 && !warp_wait(&C.draw_free[dp], ((dr >> 1) & 1) ^ 1)) return;
+        const bool resid = (d.x == 1);
+        const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
+        const long long off = static_cast<long long>(d.chunk) * kHalfBytes;
+        const long long rem = row_bytes - off;
+        const int nvec = static_cast<int>(((rem < kHalfBytes ? rem : kHalfBytes) + 15) / 16);
+        uint4 rt[kDrawVecsPerLane], rd[kDrawVecsPerLane];
+#pragma unroll
+        for (int j = 0; j < kDrawVecsPerLane; ++j) {
+          const int v = warp * kDrawVecsPerWarp + j * 32 + lane;
+          const bool in = v < nvec;
+          rt[j] = in ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
+          rd[j] = (in && resid) ? *reinterpret_cast<const uint4*>(data + kHalfBytes + static_cast<size_t>(v) * 16)
+                                : V::neg_inf();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.empty[slot]);
+        const f2 cc = pack2(c2, c2), nkt = pack2(-d.K0, -d.K0), nlt = pack2(-d.L0, -d.L0);
+        const f2 nkd = pack2(-d.K1, -d.K1), nld = pack2(-d.L1, -d.L1);
+        f2 acc[NV / 2];
+#pragma unroll
+        for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
+#pragma unroll
+        for (int j = 0; j < kDrawVecsPerLane; ++j) {
+          f2 zt[NV / 2], zd[NV / 2];
+          V::pairs(rt[j], zt);
+          V::pairs(rd[j], zd);
+#pragma unroll
+          for (int i = 0; i < NV / 2; ++i) {
+            // the same roundings as the scalar fmaf(z, c, -K) - L of the walk
+            const f2 p = exp2_2(add2(fma2(zt[i], cc, nkt), nlt));
+            if (resid) {
+              float d0, d1;
+              unpack2(sub2(p, exp2_2(add2(fma2(zd[i], cc, nkd), nld))), d0, d1);
+              acc[i] = add2(acc[i], pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+            } else {
+              acc[i] = add2(acc[i], p);
+            }
+          }
+        }
+        float a0, a1, sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); sum += a0 + a1; }
+        const float ws = warp_sum(sum);
+        if (lane == 0) {
+          C.rmass[dp][d.chunk * kConsumerWarps + warp] = static_cast<double>(ws);
+          if (timed_out) atomicOr(&C.draw_err[dp], 1);
+        }
+        if (d.chunk == d.nchunks - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&C.draw_ready[dp]);
+          ++dr;
+        }
         ++q;
         continue;
       }
 
-      // this lane's vectors of the chunk (raw 16-byte words)
+      // ---- a chunk of a streamed row ----------------------------------------
+      const int buf = rr % kRowBufs;
+      RowBuf& RB = C.rows[buf];
+      if (d.chunk == 0) {
+        if (!warp_wait(&C.row_free[buf], ((rr / kRowBufs) & 1) ^ 1)) return;
+        rK = -INFINITY; rS = 0.f; rM = -INFINITY; rArg = 0x7fffffff; rBad = 0;
+      }
       const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
       const long long off = static_cast<long long>(d.chunk) * kChunkBytes;
       const long long rem = row_bytes - off;
@@ -655,7 +783,6 @@ struct Verifier {
 
       const int seg = d.chunk * kConsumerWarps + warp;
       const int seg_base = seg * kSegElems;
-      if (d.chunk == 0) { rK = -INFINITY; rS = 0.f; rM = -INFINITY; rArg = 0x7fffffff; rBad = 0; }
       if (timed_out) rBad |= 2;
       // the drafted token's logit
       if (d.x >= 0 && d.x < P.V && !P.greedy) {
@@ -670,7 +797,7 @@ struct Verifier {
               V::unpack(raw[jj], z);
 #pragma unroll
               for (int ee = 0; ee < NV; ++ee)
-                if (ee == e) C.zx[d.kind] = z[ee];
+                if (ee == e) RB.zx = z[ee];
             }
           }
         }
@@ -728,142 +855,61 @@ struct Verifier {
         }
         rM = fmaxf(rM, wm);
         if (d.kind == 0 && d.pos == d.kb && lane == 0 && seg < kMaxChunks * kConsumerWarps) {
-          C.segK[seg] = Ks;
-          C.segS[seg] = ss;
+          RB.segK[seg] = Ks;
+          RB.segS[seg] = ss;
         }
       }
 
-      if (d.chunk == d.nchunks - 1) row_end(d, rK, rS, rM, rArg, rBad);
+      if (d.chunk == d.nchunks - 1) {
+        // publish the row: this warp's state, the descriptor (warp 0)
+        if (lane == 0) {
+          RB.wK[warp] = rK; RB.wS[warp] = rS; RB.wM[warp] = rM; RB.wArg[warp] = rArg; RB.wBad[warp] = rBad;
+          if (warp == 0) RB.d = d;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.row_ready[buf]);
+        ++rr;
+      }
       ++q;
     }
   }
 
-  // Row end: combine the warps, then the decisions that need the row.
-  __device__ void row_end(const Desc& d, float rK, float rS, float rM, int rArg, int rBad) {
-    const int ctid = warp * 32 + lane;
-    const float c2 = P.c2;
-    if (lane == 0) {
-      C.wK[warp] = rK; C.wS[warp] = rS; C.wM[warp] = rM; C.wArg[warp] = rArg; C.wBad[warp] = rBad;
-    }
-    consumer_sync();
-    // warp 0 combines the warps' states, one lane per warp
-    float M = -INFINITY, K = -INFINITY, Ssum = 0.f;
-    int arg = 0x7fffffff, bad = 0;
-    if (warp == 0) {
-      const bool in = lane < kConsumerWarps;
-      M = in ? C.wM[lane] : -INFINITY;
-      arg = in ? C.wArg[lane] : 0x7fffffff;
-      warp_argmax(M, arg);
-      const float wk = in ? C.wK[lane] : -INFINITY;
-      K = warp_max(wk);
-      bad = warp_or(in ? C.wBad[lane] : 0);
-      if (!P.greedy) Ssum = warp_sum(wk > -INFINITY ? C.wS[lane] * fast_exp2(__fsub_rn(wk, K)) : 0.f);
-    }
-    int bonus_draw = 0;
-    if (ctid == 0) {
-      SeqRec& R = C.rec[d.rec];
-      const int kind = d.kind;
-      const size_t b = static_cast<size_t>(d.b);
-      if (d.pos == 0 && kind == 0) {
-        // first row of the sequence: open its record (free unless the ring of
-        // records has wrapped onto a sequence still waiting for its draw)
-        if (R.pending != 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-        R.b = d.b; R.kb = d.kb; R.a = -1; R.err = 0; R.y = -1; R.zero_resid = 0;
-        R.pending = 1; R.s = d.s;
-      }
-      if (bad & 2) R.err |= kErrTimeout;
-      if (d.pos < d.kb && (d.x < 0 || d.x >= P.V)) R.err |= kErrBadToken;
-      if (P.greedy) {
-        if ((bad & 1) || !(M > -INFINITY)) R.err |= kErrNonfinite;
-        P.ws.m_t[b * (P.k + 1) + d.pos] = M;
-        if (d.pos < d.kb) {
-          const bool acc = (d.x == arg);
-          P.ws.alpha[b * P.k + d.pos] = acc ? 1.f : 0.f;
-          if (!acc && R.a < 0) { R.a = d.pos; R.y = arg; }
-        } else if (R.a < 0) {
-          R.y = arg;
-        }
-      } else {
-        const float L = log2f(Ssum);
-        C.rowK[kind] = K;
-        C.rowL[kind] = L;
-        if ((bad & 1) || !(isfinite(M) && isfinite(Ssum) && Ssum > 0.f)) R.err |= kErrNonfinite;
-        if (kind == 0) {
-          P.ws.m_t[b * (P.k + 1) + d.pos] = M;
-          P.ws.L_t[b * (P.k + 1) + d.pos] = L;
-        } else {
-          P.ws.m_d[b * P.k + d.pos] = M;
-          P.ws.L_d[b * P.k + d.pos] = L;
-        }
-        if (kind == 1 && !R.err) {
-          // the pair is complete: acceptance test of draft d.pos
-          const float zt = C.zx[0], zd = C.zx[1];
-          float alpha;
-          if (zt == -INFINITY) alpha = 0.f;               // p(x) = 0
-          else if (zd == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
-          else {
-            const float log2r = (fmaf(zt, c2, -C.rowK[0]) - C.rowL[0]) - (fmaf(zd, c2, -C.rowK[1]) - C.rowL[1]);
-            alpha = log2r >= 0.f ? 1.f : exp2f(log2r);
-          }
-          P.ws.alpha[b * P.k + d.pos] = alpha;
-          if (!(d.u < alpha) && R.a < 0) {
-            // first rejection: the producer re-reads this pair for the draw
-            R.a = d.pos;
-            R.Kt = C.rowK[0]; R.Lt = C.rowL[0]; R.Kd = C.rowK[1]; R.Ld = C.rowL[1];
-            R.pending += 1;
-            push_request(d.b, d.pos, d.rec, 1);
-          }
-        } else if (kind == 0 && d.pos == d.kb && R.a < 0 && !R.err) {
-          bonus_draw = 1;   // every draft accepted: the bonus draw
-          R.Kt = K; R.Lt = L;
-        }
-      }
-      C.flag_bonus = bonus_draw;   // broadcast through the barrier below
-    }
-    consumer_sync();
-    if (C.flag_bonus) this->bonus_draw(d);
-    if (d.pos == d.kb && d.kind == 0) {
-      // the sequence's stream is done
-      if (ctid == 0) C.flag_finish = (--C.rec[d.rec].pending == 0) ? 1 : 0;
-      consumer_sync();
-      if (C.flag_finish) finish_sequence(d.rec);
-    }
-  }
+  // ======================= control warp ======================================
 
-  __device__ void push_request(int b, int pos, int rec, int mode) {
-    // single producer (this thread) / single consumer (the producer warp) ring
+  __device__ void push_request(const DrawReq& r) {
+    // the control warp (lane 0) produces, the producer warp consumes
     unsigned long long t0 = 0;
     while (C.req_tail - C.req_head >= kReqs) {
       if (!t0) t0 = global_ns();
       if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
         atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-        C.rec[rec].err |= kErrTimeout;
+        C.rec[r.rec].err |= kErrTimeout;
         return;
       }
     }
     const int tail = C.req_tail;
-    const int r = tail % kReqs;
-    C.req_b[r] = b; C.req_pos[r] = pos; C.req_rec[r] = rec; C.req_mode[r] = mode;
+    C.req[tail % kReqs] = r;
+    C.ctl_req[C.pushed % kReqs] = r;
+    C.pushed = C.pushed + 1;
     __threadfence_block();
     C.req_tail = tail + 1;
   }
 
-  // Warp 0: the segment holding s * S among `nseg` masses (index order).
-  // Writes C.S, C.seg, C.seg_t.
-  __device__ void locate(const double* mass, int nseg, float s) {
+  // The segment holding s * S among `nseg` masses (index order).
+  __device__ void locate(const double* mass, int nseg, float s, double& Stot, int& seg, double& seg_t) const {
     const int per = (nseg + 31) / 32;
     const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
     double gs = 0.0;
     for (int i = g0; i < g1; ++i) gs += mass[i];
     const double incl = warp_incl_scan(gs, lane);
     const double excl = incl - gs;
-    const double Stot = __shfl_sync(0xffffffffu, incl, 31);
+    Stot = __shfl_sync(0xffffffffu, incl, 31);
     const double tgt = static_cast<double>(s) * Stot;
     const unsigned hit = __ballot_sync(0xffffffffu, gs > 0.0 && tgt < incl);
     const unsigned posg = __ballot_sync(0xffffffffu, gs > 0.0);
     const int owner = hit ? (__ffs(hit) - 1) : (posg ? 31 - __clz(posg) : -1);
-    int seg = -1;
-    double seg_t = 0.0;
+    seg = -1;
+    seg_t = 0.0;
     if (owner >= 0 && lane == owner) {
       double run = excl, last_run = excl;
       int last = -1;
@@ -879,16 +925,14 @@ struct Verifier {
       seg = __shfl_sync(0xffffffffu, seg, owner);
       seg_t = __shfl_sync(0xffffffffu, seg_t, owner);
     }
-    if (lane == 0) { C.S = Stot; C.seg = seg; C.seg_t = seg_t; }
   }
 
-  // Warp 0: walk `nsteps` x 32 vectors starting at vector v0 of the row(s),
-  // a warp inclusive scan per step, to the token where the running weight
-  // passes t.  resid: weights max(0, p - q); else p.
+  // Walk NSTEPS x 32 vectors starting at vector v0, a warp inclusive scan
+  // per step, to the token where the running weight passes t.
+  // RESID: weights max(0, p - q); else p.
   template <int NSTEPS, bool RESID>
   __device__ int walk(int v0, double t, const unsigned char* rowT, const unsigned char* rowD,
                       float Kt, float Lt, float Kd, float Ld) const {
-    // all loads first (raw), then the scan
     uint4 rt[NSTEPS], rd[RESID ? NSTEPS : 1];
 #pragma unroll
     for (int j = 0; j < NSTEPS; ++j) {
@@ -943,156 +987,235 @@ struct Verifier {
     return found >= 0 ? found : last_positive;
   }
 
-  // The bonus draw of the sequence whose last row just ended (blocking; the
-  // producer keeps the ring full meanwhile): masses from the sums kept while
-  // streaming, then one stream segment of the bonus row is read again.
-  __device__ void bonus_draw(const Desc& d) {
-    const int ctid = warp * 32 + lane;
-    SeqRec& R = C.rec[d.rec];
-    const float Kt = R.Kt, Lt = R.Lt;
-    const int nseg = nchunks * kConsumerWarps;
-    for (int sg = ctid; sg < nseg; sg += kConsumerWarps * 32) {
-      const float ks = C.segK[sg];
-      C.bmass[sg] = ks == -INFINITY ? 0.0
-                    : static_cast<double>(C.segS[sg]) * static_cast<double>(fast_exp2(__fsub_rn(ks, Kt) - Lt));
-    }
-    consumer_sync();
-    if (warp == 0) {
-      locate(C.bmass, nseg, R.s);
-      __syncwarp();
-      const int seg = C.seg;
-      int y = -1;
-      if (seg >= 0)
-        y = walk<kVecsPerLane, false>(seg * kVecsPerWarp, C.seg_t, row_ptr(d.b, d.kb, 0), nullptr, Kt, Lt, 0.f, 0.f);
-      if (lane == 0) {
-        R.y = y;
-        P.ws.mass[static_cast<size_t>(d.b) * (P.k + 1) + d.kb] = static_cast<float>(C.S);
-      }
-    }
-    consumer_sync();
-  }
-
-  // One chunk of a pair's re-read: per-segment weights of the draw; the last
-  // chunk locates the token.
-  __device__ void draw_chunk(const Desc& d, int slot, int timed_out) {
-    SeqRec& R = C.rec[d.rec];
-    const bool resid = (d.x == 1);
-    const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
-    const long long off = static_cast<long long>(d.chunk) * kHalfBytes;
-    const long long rem = row_bytes - off;
-    const int nvec = static_cast<int>(((rem < kHalfBytes ? rem : kHalfBytes) + 15) / 16);
-    uint4 rt[kDrawVecsPerLane], rd[kDrawVecsPerLane];
-#pragma unroll
-    for (int j = 0; j < kDrawVecsPerLane; ++j) {
-      const int v = warp * kDrawVecsPerWarp + j * 32 + lane;
-      const bool in = v < nvec;
-      rt[j] = in ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
-      rd[j] = (in && resid) ? *reinterpret_cast<const uint4*>(data + kHalfBytes + static_cast<size_t>(v) * 16)
-                            : V::neg_inf();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&C.empty[slot]);
-    if (timed_out && lane == 0) atomicOr(&R.err, kErrTimeout);
-    const float c2 = P.c2;
-    const float Kt = R.Kt, Lt = R.Lt, Kd = R.Kd, Ld = R.Ld;
-    const f2 cc = pack2(c2, c2), nkt = pack2(-Kt, -Kt), nlt = pack2(-Lt, -Lt);
-    const f2 nkd = pack2(-Kd, -Kd), nld = pack2(-Ld, -Ld);
-    f2 acc[NV / 2];
-#pragma unroll
-    for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
-#pragma unroll
-    for (int j = 0; j < kDrawVecsPerLane; ++j) {
-      f2 zt[NV / 2], zd[NV / 2];
-      V::pairs(rt[j], zt);
-      V::pairs(rd[j], zd);
-#pragma unroll
-      for (int i = 0; i < NV / 2; ++i) {
-        // the same roundings as the scalar fmaf(z, c, -K) - L of the walk
-        const f2 p = exp2_2(add2(fma2(zt[i], cc, nkt), nlt));
-        if (resid) {
-          float d0, d1;
-          unpack2(sub2(p, exp2_2(add2(fma2(zd[i], cc, nkd), nld))), d0, d1);
-          acc[i] = add2(acc[i], pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
-        } else {
-          acc[i] = add2(acc[i], p);
-        }
-      }
-    }
-    float a0, a1, sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); sum += a0 + a1; }
-    const float ws = warp_sum(sum);
-    const int sg = d.chunk * kConsumerWarps + warp;
-    if (lane == 0) C.rmass[sg] = static_cast<double>(ws);
-    if (d.chunk != d.nchunks - 1) return;
-
-    // last chunk: the total, the segment, the token
-    consumer_sync();
-    const int nseg = d.nchunks * kConsumerWarps;
-    if (warp == 0) {
-      locate(C.rmass, nseg, R.s);
-      __syncwarp();
-      if (C.S > 0.0 || !resid) {
-        const int seg = C.seg;
-        int y = -1;
-        if (seg >= 0) {
-          if (resid)
-            y = walk<kDrawVecsPerLane, true>(seg * kDrawVecsPerWarp, C.seg_t, row_ptr(d.b, d.pos, 0),
-                                             row_ptr(d.b, d.pos, 1), Kt, Lt, Kd, Ld);
-          else
-            y = walk<kDrawVecsPerLane, false>(seg * kDrawVecsPerWarp, C.seg_t, row_ptr(d.b, d.pos, 0),
-                                              nullptr, Kt, Lt, Kd, Ld);
-        }
-        if (lane == 0) {
-          R.y = y;
-          P.ws.mass[static_cast<size_t>(d.b) * (P.k + 1) + d.pos] = static_cast<float>(C.S);
-          C.flag_finish = (--R.pending == 0) ? 1 : 0;
-        }
-      } else if (lane == 0) {
-        // exact arithmetic rules a zero residual out (a rejection implies
-        // p > q somewhere); draw from p_a instead and count it
-        R.zero_resid = 1;
-        push_request(d.b, d.pos, d.rec, 2);
-        C.flag_finish = 0;
-      }
-    }
-    consumer_sync();
-    if (C.flag_finish) finish_sequence(d.rec);
-  }
-
   // Outputs of a sequence whose stream and draw are both done.
   __device__ void finish_sequence(int rec) {
-    if (warp == 0) {
-      const SeqRec& R = C.rec[rec];
-      const int k = P.k;
-      const size_t b = static_cast<size_t>(R.b);
-      int* ot = P.out_tokens + b * (k + 1);
-      const int err = R.err;
-      const int a = R.a < 0 ? R.kb : R.a;
-      const int y = R.y;
-      const bool ok = !err && y >= 0;
-      for (int j = lane; j <= k; j += 32) {
-        int v = -1;
-        if (ok) v = j < a ? __ldg(P.tokens + b * k + j) : (j == a ? y : -1);
-        ot[j] = v;
+    const SeqRec& R = C.rec[rec];
+    const int k = P.k;
+    const size_t b = static_cast<size_t>(R.b);
+    int* ot = P.out_tokens + b * (k + 1);
+    const int err = R.err;
+    const int a = R.a < 0 ? R.kb : R.a;
+    const int y = R.y;
+    const bool ok = !err && y >= 0;
+    for (int j = lane; j <= k; j += 32) {
+      int v = -1;
+      if (ok) v = j < a ? __ldg(P.tokens + b * k + j) : (j == a ? y : -1);
+      ot[j] = v;
+    }
+    if (lane == 0) {
+      P.out_len[b] = ok ? a + 1 : 0;
+      if (ok) {
+        atomicAdd(P.ws.stats + kStatSequences, 1ull);
+        atomicAdd(P.ws.stats + kStatProposed, static_cast<unsigned long long>(R.kb));
+        atomicAdd(P.ws.stats + kStatAccepted, static_cast<unsigned long long>(a));
+        atomicAdd(P.ws.stats + kStatEmitted, static_cast<unsigned long long>(a + 1));
+        if (R.kb == 0) atomicAdd(P.ws.stats + kStatSpecOff, 1ull);
+        if (R.zero_resid) atomicAdd(P.ws.stats + kStatZeroResidual, 1ull);
+      } else {
+        atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
+        unsigned bits = static_cast<unsigned>(err & (kErrBadToken | kErrNonfinite | kErrTimeout));
+        if (!bits) bits = kErrNonfinite;   // no token could be drawn
+        atomicOr(P.ws.err_word, bits);
+      }
+      __threadfence_block();
+      C.seqs_finished = C.seqs_finished + 1;
+    }
+    __syncwarp();
+  }
+
+  // A finished row: combine the warps, decide, draw the bonus token.
+  // Returns false at the end of the work.
+  __device__ bool control_row(int buf) {
+    const float c2 = P.c2;
+    RowBuf& RB = C.rows[buf];
+    const Desc d = RB.d;
+    if (d.kind < 0) return false;
+    // combine the consumer warps, one lane per warp
+    const bool in = lane < kConsumerWarps;
+    float M = in ? RB.wM[lane] : -INFINITY;
+    int arg = in ? RB.wArg[lane] : 0x7fffffff;
+    warp_argmax(M, arg);
+    const float wk = in ? RB.wK[lane] : -INFINITY;
+    const float K = warp_max(wk);
+    const int bad = warp_or(in ? RB.wBad[lane] : 0);
+    const float Ssum = warp_sum((in && wk > -INFINITY) ? RB.wS[lane] * fast_exp2(__fsub_rn(wk, K)) : 0.f);
+    const float L = log2f(Ssum);
+    SeqRec& R = C.rec[d.rec];
+    const size_t b = static_cast<size_t>(d.b);
+    int bonus = 0;
+    if (lane == 0) {
+      if (d.pos == 0 && d.kind == 0) {
+        // first row of the sequence: open its record (free unless the ring of
+        // records has wrapped onto a sequence still waiting for its draw)
+        if (R.pending != 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+        R.b = d.b; R.kb = d.kb; R.a = -1; R.err = 0; R.y = -1; R.zero_resid = 0;
+        R.pending = 1; R.s = d.s;
+      }
+      if (bad & 2) R.err |= kErrTimeout;
+      if (d.pos < d.kb && (d.x < 0 || d.x >= P.V)) R.err |= kErrBadToken;
+      if (P.greedy) {
+        if ((bad & 1) || !(M > -INFINITY)) R.err |= kErrNonfinite;
+        P.ws.m_t[b * (P.k + 1) + d.pos] = M;
+        if (d.pos < d.kb) {
+          const bool acc = (d.x == arg);
+          P.ws.alpha[b * P.k + d.pos] = acc ? 1.f : 0.f;
+          if (!acc && R.a < 0) { R.a = d.pos; R.y = arg; }
+        } else if (R.a < 0) {
+          R.y = arg;
+        }
+      } else {
+        if ((bad & 1) || !(isfinite(M) && isfinite(Ssum) && Ssum > 0.f)) R.err |= kErrNonfinite;
+        if (d.kind == 0) {
+          P.ws.m_t[b * (P.k + 1) + d.pos] = M;
+          P.ws.L_t[b * (P.k + 1) + d.pos] = L;
+          C.pairK = K; C.pairL = L; C.pairZx = RB.zx;
+        } else {
+          P.ws.m_d[b * P.k + d.pos] = M;
+          P.ws.L_d[b * P.k + d.pos] = L;
+        }
+        if (d.kind == 1 && !R.err) {
+          // the pair is complete: acceptance test of draft d.pos
+          const float zt = C.pairZx, zd = RB.zx;
+          float alpha;
+          if (zt == -INFINITY) alpha = 0.f;               // p(x) = 0
+          else if (zd == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
+          else {
+            const float log2r = (fmaf(zt, c2, -C.pairK) - C.pairL) - (fmaf(zd, c2, -K) - L);
+            alpha = log2r >= 0.f ? 1.f : exp2f(log2r);
+          }
+          P.ws.alpha[b * P.k + d.pos] = alpha;
+          if (!(d.u < alpha) && R.a < 0) {
+            // first rejection: the producer re-reads this pair for the draw
+            R.a = d.pos;
+            R.pending += 1;
+            DrawReq rq;
+            rq.b = d.b; rq.pos = d.pos; rq.rec = d.rec; rq.mode = 1;
+            rq.Kt = C.pairK; rq.Lt = C.pairL; rq.Kd = K; rq.Ld = L;
+            push_request(rq);
+          }
+        } else if (d.kind == 0 && d.pos == d.kb && R.a < 0 && !R.err) {
+          bonus = 1;   // every draft accepted: the bonus draw
+        }
+      }
+    }
+    bonus = __shfl_sync(0xffffffffu, bonus, 0);
+    __syncwarp();
+    if (bonus) {
+      // masses of the stream segments from the sums kept while streaming,
+      // then one segment of the bonus row is read again
+      const int nseg = nchunks * kConsumerWarps;
+      for (int sg = lane; sg < nseg; sg += 32) {
+        const float ks = RB.segK[sg];
+        C.bmass[sg] = ks == -INFINITY ? 0.0
+                      : static_cast<double>(RB.segS[sg]) * static_cast<double>(fast_exp2(__fsub_rn(ks, K) - L));
+      }
+      __syncwarp();
+      double S;
+      int seg;
+      double seg_t;
+      locate(C.bmass, nseg, R.s, S, seg, seg_t);
+      int y = -1;
+      if (seg >= 0)
+        y = walk<kVecsPerLane, false>(seg * kVecsPerWarp, seg_t, row_ptr(d.b, d.kb, 0), nullptr, K, L, 0.f, 0.f);
+      if (lane == 0) {
+        R.y = y;
+        P.ws.mass[b * (P.k + 1) + d.kb] = static_cast<float>(S);
+      }
+      __syncwarp();
+    }
+    if (d.pos == d.kb && d.kind == 0) {
+      // the sequence's stream is done
+      int fin = 0;
+      if (lane == 0) fin = (--R.pending == 0) ? 1 : 0;
+      fin = __shfl_sync(0xffffffffu, fin, 0);
+      if (fin) finish_sequence(d.rec);
+    }
+    return true;
+  }
+
+  // A re-read draw whose segment weights are complete.
+  __device__ void control_draw(int di) {
+    const int dp = di & 1;
+    const DrawReq r = C.ctl_req[di % kReqs];
+    SeqRec& R = C.rec[r.rec];
+    const int nseg = ndraw * kConsumerWarps;
+    const bool resid = (r.mode == 1);
+    double S;
+    int seg;
+    double seg_t;
+    locate(C.rmass[dp], nseg, R.s, S, seg, seg_t);
+    int fin = 0;
+    if (lane == 0 && C.draw_err[dp]) { R.err |= kErrTimeout; C.draw_err[dp] = 0; }
+    if (S > 0.0 || !resid) {
+      int y = -1;
+      if (seg >= 0) {
+        if (resid)
+          y = walk<kDrawVecsPerLane, true>(seg * kDrawVecsPerWarp, seg_t, row_ptr(r.b, r.pos, 0),
+                                           row_ptr(r.b, r.pos, 1), r.Kt, r.Lt, r.Kd, r.Ld);
+        else
+          y = walk<kDrawVecsPerLane, false>(seg * kDrawVecsPerWarp, seg_t, row_ptr(r.b, r.pos, 0),
+                                            nullptr, r.Kt, r.Lt, r.Kd, r.Ld);
       }
       if (lane == 0) {
-        P.out_len[b] = ok ? a + 1 : 0;
-        if (ok) {
-          atomicAdd(P.ws.stats + kStatSequences, 1ull);
-          atomicAdd(P.ws.stats + kStatProposed, static_cast<unsigned long long>(R.kb));
-          atomicAdd(P.ws.stats + kStatAccepted, static_cast<unsigned long long>(a));
-          atomicAdd(P.ws.stats + kStatEmitted, static_cast<unsigned long long>(a + 1));
-          if (R.kb == 0) atomicAdd(P.ws.stats + kStatSpecOff, 1ull);
-          if (R.zero_resid) atomicAdd(P.ws.stats + kStatZeroResidual, 1ull);
-        } else {
-          atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
-          unsigned bits = static_cast<unsigned>(err & (kErrBadToken | kErrNonfinite | kErrTimeout));
-          if (!bits) bits = kErrNonfinite;   // no token could be drawn
-          atomicOr(P.ws.err_word, bits);
+        R.y = y;
+        P.ws.mass[static_cast<size_t>(r.b) * (P.k + 1) + r.pos] = static_cast<float>(S);
+        fin = (--R.pending == 0) ? 1 : 0;
+      }
+    } else if (lane == 0) {
+      // exact arithmetic rules a zero residual out (a rejection implies
+      // p > q somewhere); draw from p_a instead and count it
+      R.zero_resid = 1;
+      DrawReq rq = r;
+      rq.mode = 2;
+      push_request(rq);
+    }
+    fin = __shfl_sync(0xffffffffu, fin, 0);
+    __syncwarp();
+    if (fin) finish_sequence(r.rec);
+  }
+
+  __device__ void control() {
+    int ri = 0, di = 0;
+    unsigned long long idle_since = 0;
+    while (true) {
+      bool progressed = false;
+      const int buf = ri % kRowBufs;
+      int ready = 0;
+      if (lane == 0) ready = mbar_test_wait(&C.row_ready[buf], static_cast<uint32_t>(ri / kRowBufs) & 1u) ? 1 : 0;
+      ready = __shfl_sync(0xffffffffu, ready, 0);
+      if (ready) {
+        const bool more = control_row(buf);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&C.row_free[buf]);
+        ++ri;
+        if (!more) return;
+        progressed = true;
+      }
+      int pushed = 0;
+      if (lane == 0) pushed = C.pushed;
+      pushed = __shfl_sync(0xffffffffu, pushed, 0);
+      if (di < pushed) {
+        const int dp = di & 1;
+        int dready = 0;
+        if (lane == 0) dready = mbar_test_wait(&C.draw_ready[dp], static_cast<uint32_t>(di >> 1) & 1u) ? 1 : 0;
+        dready = __shfl_sync(0xffffffffu, dready, 0);
+        if (dready) {
+          control_draw(di);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&C.draw_free[dp]);
+          ++di;
+          progressed = true;
         }
-        __threadfence_block();
-        C.seqs_finished = C.seqs_finished + 1;
+      }
+      if (progressed) {
+        idle_since = 0;
+      } else {
+        if (!idle_since) idle_since = global_ns();
+        if (static_cast<long long>(global_ns() - idle_since) > 4 * kDrainLimitNs) {
+          if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+          return;
+        }
+        __nanosleep(64);
       }
     }
   }
@@ -1110,8 +1233,18 @@ verify_kernel(const VerifyParams P) {
       mbar_init(&C.full[s], 1);
       mbar_init(&C.empty[s], kConsumerWarps);
     }
+    for (int r = 0; r < kRowBufs; ++r) {
+      mbar_init(&C.row_ready[r], kConsumerWarps);
+      mbar_init(&C.row_free[r], 1);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&C.draw_ready[r], kConsumerWarps);
+      mbar_init(&C.draw_free[r], 1);
+      C.draw_err[r] = 0;
+    }
     C.req_head = 0;
     C.req_tail = 0;
+    C.pushed = 0;
     C.seqs_finished = 0;
     for (int r = 0; r < kRecs; ++r) C.rec[r].pending = 0;
     fence_mbar_init();
@@ -1119,8 +1252,9 @@ verify_kernel(const VerifyParams P) {
   __syncthreads();
   grid_dependency_wait();           // the work list of plan_kernel is ready
   Verifier<ELT> v(P, C, ring, lane, warp);
-  if (warp == kConsumerWarps) v.produce();
-  else v.consume();
+  if (warp < kConsumerWarps) v.consume();
+  else if (warp == kConsumerWarps) v.produce();
+  else v.control();
 }
 
 // ---------------------------------------------------------------------------
