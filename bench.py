@@ -385,10 +385,11 @@ def our_arm(args, w):
         pg.barrier()
     m = time_workload(svp, w, args, device, stream, args.rotate, args.steps, args.warmup, sampler)
     total_ms = m["total_ms"]
+    stats = m["stats"]
     if pg:
-        t = torch.tensor([total_ms], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+        from speculative_decoding_verification_71_gb300.replicas import max_over_ranks, reduce_counts
+        total_ms = max_over_ranks(total_ms)
+        stats = reduce_counts(stats)
         pg.barrier()
     ms_per_step = total_ms / args.steps
     value = world * m["positions"] * args.steps / (total_ms / 1e3)
@@ -401,9 +402,8 @@ def our_arm(args, w):
 
     e2e = e2e_measure(svp, w, args, device, stream, m["ver"], m["base_inputs"])
     if pg:
-        t = torch.tensor([e2e["ms_per_step"]], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e["value"] = world * m["positions"] / (float(t.item()) / 1e3)
+        from speculative_decoding_verification_71_gb300.replicas import max_over_ranks
+        e2e["value"] = world * m["positions"] / (max_over_ranks(e2e["ms_per_step"]) / 1e3)
 
     aux = {}
     for name in [a for a in args.aux.split(",") if a]:
@@ -449,8 +449,8 @@ def our_arm(args, w):
         "clocks": m["clocks"], "clock_soak_steps": m["soak_steps"],
         "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
         "gpu_launches": 2 * args.steps,   # per call: the work-list kernel and the verify kernel
-        "acceptance": {"mean_emitted": m["stats"]["mean_emitted"], "mean_accepted": m["stats"]["mean_accepted"],
-                       "accept_rate": m["stats"]["accept_rate"], "spec_off": m["stats"]["spec_off"]},
+        "acceptance": {"mean_emitted": stats["mean_emitted"], "mean_accepted": stats["mean_accepted"],
+                       "accept_rate": stats["accept_rate"], "spec_off": stats["spec_off"]},
         "cpu_baseline": cpu, "aux": aux or None,
     }
     print(json.dumps(line), flush=True)
