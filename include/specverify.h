@@ -194,6 +194,37 @@ sv_status sv_get_config(const sv_ctx *ctx, int *stages, int *ctas_per_sm, int *t
  * default. */
 sv_status sv_set_wait_limit_ns(sv_ctx *ctx, long long ns);
 
+/*
+ * spec_verify without a context, for callers that may not allocate device
+ * memory (the pages describe no such entry point; it is a property of this
+ * library).  Code running under an allocator it does not own, code that must
+ * not synchronise the device, or code with a memory budget fixed in advance
+ * cannot call sv_create, which allocates its workspace with cudaMalloc.  This
+ * entry point keeps that workspace in one fixed array of about 420 KB in the
+ * library's own device memory (every GPU that loads the library holds a copy
+ * until the process exits) and calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Arguments are those of spec_verify, with the vocabulary V and the logit
+ * dtype passed directly; inputs and outputs are caller-owned device buffers
+ * as there.  Limits: 1 <= B <= 4096, 0 <= k <= 31, B * (k+1) <= 16384,
+ * V * sizeof(dtype) <= 1 MiB; larger requests return SV_ERR_INVALID_ARG and
+ * launch nothing.  Device-side errors show in the outputs only (out_len 0,
+ * tokens -1 for the affected sequences); there are no counters.
+ *
+ * The first call on a device sets that device up (the array's device address
+ * and the launch shape); make that first call before any stream capture.
+ * Every call on a device shares the array: calls that may overlap on the GPU
+ * (on different streams without ordering between them) race on it and give
+ * wrong results; order them on one stream.
+ */
+sv_status spec_verify_noalloc(int B, int k, int V, sv_dtype dtype,
+                              const void *target_logits, const void *draft_logits,
+                              const int32_t *draft_tokens, const int32_t *draft_len,
+                              const float *uniforms, float temperature,
+                              int32_t *out_tokens, int32_t *out_len,
+                              sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

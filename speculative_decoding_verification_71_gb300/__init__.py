@@ -38,7 +38,7 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
-    "sv_set_pipeline", "sv_get_config", "sv_set_wait_limit_ns",
+    "sv_set_pipeline", "sv_get_config", "sv_set_wait_limit_ns", "spec_verify_noalloc",
 )
 
 
@@ -102,6 +102,8 @@ def load_library(path: str | None = None):
     lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 5
     lib.sv_set_wait_limit_ns.restype = c.c_int
     lib.sv_set_wait_limit_ns.argtypes = [P, c.c_longlong]
+    lib.spec_verify_noalloc.restype = c.c_int
+    lib.spec_verify_noalloc.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, P, P, c.c_float, P, P, P]
     if path is None:
         _lib = lib
     return lib
@@ -273,3 +275,36 @@ class SpecVerifier:
             self._raise(st, "sv_get_config")
         return dict(zip(("stages", "ctas_per_sm", "threads", "smem_bytes", "grid_ctas"),
                         (v.value for v in vals)))
+
+
+def spec_verify_noalloc(target, draft, tokens, draft_len, uniforms, temperature, out_tokens, out_len,
+                        stream=None):
+    """Verification without a context, for callers that may not allocate
+    device memory: the library keeps the workspace in a fixed array of its
+    own (limits: B <= 4096, k <= 31, B * (k+1) <= 16384).  The output buffers
+    must be supplied.  Calls that may overlap on the GPU share that array and
+    must be ordered on one stream.  Raises SpecVerifyError on a bad argument.
+    """
+    lib = load_library()
+    B, k1, V = target.shape
+    k = k1 - 1
+    dev = target.device
+    dtype = target.dtype
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    _check_dev("target", target, dtype, (B, k + 1, V), dev)
+    if draft is not None:
+        _check_dev("draft", draft, dtype, (B, k, V), dev)
+    if tokens is not None:
+        _check_dev("tokens", tokens, torch.int32, (B, k), dev)
+    _check_dev("draft_len", draft_len, torch.int32, (B,), dev)
+    if uniforms is not None:
+        _check_dev("uniforms", uniforms, torch.float32, (B, k + 1), dev)
+    _check_dev("out_tokens", out_tokens, torch.int32, (B, k + 1), dev)
+    _check_dev("out_len", out_len, torch.int32, (B,), dev)
+    st = lib.spec_verify_noalloc(B, k, V, SV_F32 if dtype == torch.float32 else SV_BF16, _ptr(target),
+                                 _ptr(draft), _ptr(tokens), _ptr(draft_len), _ptr(uniforms),
+                                 float(temperature), _ptr(out_tokens), _ptr(out_len), _stream_handle(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_noalloc")
+    return out_tokens, out_len
