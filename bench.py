@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--stages", type=int, default=0, help="staging slots per CTA (0 = automatic)")
     ap.add_argument("--ctas-per-sm", type=int, default=0)
+    ap.add_argument("--cluster", type=int, default=0, help="CTAs per sequence (1, 2, 4, 8; 0 = automatic)")
     ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
     return ap.parse_args()
 
@@ -254,6 +255,7 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
     ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
     if args.stages or args.ctas_per_sm:
         ver.set_pipeline(args.stages or 3, args.ctas_per_sm)
+    ver.set_cluster(args.cluster)
     outs = [(torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device),
              torch.empty(w.B, dtype=torch.int32, device=device)) for _ in range(rotate)]
 
@@ -317,6 +319,7 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
     if st != svp.SV_OK:
         raise RuntimeError(f"device error {st} during the timed region: {stats}")
     cfg = ver.config()
+    cfg["cluster"], cfg["grid_ctas"] = ver.launch_shape(w.B)
     del sets, outs
     return {"total_ms": total_ms, "kernel_ms_mean": float(np.mean(kern_ms)),
             "kernel_ms_median": float(np.median(kern_ms)), "kernel_ms_best": float(np.min(kern_ms)),
@@ -414,7 +417,8 @@ def our_arm(args, w):
                      "ms_per_step": am["total_ms"] / max(1, args.steps // 4),
                      "kernel_gbs": am["bytes"] / (am["kernel_ms_mean"] / 1e3) / 1e9,
                      "frac_of_8tbs": am["bytes"] / (am["kernel_ms_mean"] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-                     "algorithmic_bytes": am["bytes"], "mean_emitted": am["stats"]["mean_emitted"]}
+                     "algorithmic_bytes": am["bytes"], "mean_emitted": am["stats"]["mean_emitted"],
+                     "cluster": am["cfg"]["cluster"], "grid_ctas": am["cfg"]["grid_ctas"]}
         del am
 
     if rank != 0:
@@ -439,6 +443,7 @@ def our_arm(args, w):
                    "l2": f"{args.rotate} rotating copies of the inputs (each larger than the 129 MB L2)",
                    "parallelism": f"replicas{world}", "launch": m["launch"], "stages": m["cfg"]["stages"],
                    "ctas_per_sm": m["cfg"]["ctas_per_sm"], "grid_ctas": m["cfg"]["grid_ctas"],
+                   "cluster": m["cfg"]["cluster"],
                    "threads": m["cfg"]["threads"], "smem_bytes": m["cfg"]["smem_bytes"]},
         "gbs": gbs_step, "frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",

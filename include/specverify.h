@@ -176,16 +176,25 @@ sv_status spec_verify_stats(sv_ctx *ctx, sv_stream_t stream, sv_stats *out);
 /* Clear the counters and the device error word (asynchronous on `stream`). */
 sv_status spec_verify_reset_stats(sv_ctx *ctx, sv_stream_t stream);
 
-/* Tuning and introspection.  Each CTA streams whole sequences through a ring
- * of 16 KB shared-memory slots; sv_set_pipeline picks the number of slots
- * (2..16) and how many CTAs share an SM (0: as many as fit); (0, 0) restores
- * the automatic choice.  Returns SV_ERR_UNSUPPORTED, keeping the previous
- * shape, when the shape cannot be launched.  sv_get_config reports the current
- * shape and the size of the persistent grid (any output pointer may be
- * NULL). */
+/* Tuning and introspection.  A cluster of 1, 2, 4 or 8 CTAs verifies one
+ * sequence at a time: each CTA takes an equal slice of every row's vocabulary
+ * and streams it through a ring of 64 KB shared-memory slots, and the CTAs
+ * combine their slices through distributed shared memory.
+ * sv_set_pipeline picks the number of slots (2..16) and how many CTAs share
+ * an SM (0: as many as fit); (0, 0) restores the automatic choice.
+ * sv_set_cluster fixes the cluster size (1, 2, 4 or 8), or 0 (the default)
+ * to choose it on every call from the batch size and the row length.  Both
+ * return SV_ERR_INVALID_ARG for values outside these ranges and
+ * SV_ERR_UNSUPPORTED, keeping the previous setting, when the shape cannot be
+ * launched on this device.  sv_get_config reports the current shape and
+ * cluster setting, and the most CTAs the persistent grid can have;
+ * sv_launch_shape the cluster size and grid a call with batch B would use.
+ * Any output pointer may be NULL. */
 sv_status sv_set_pipeline(sv_ctx *ctx, int stages, int ctas_per_sm);
+sv_status sv_set_cluster(sv_ctx *ctx, int cluster);
 sv_status sv_get_config(const sv_ctx *ctx, int *stages, int *ctas_per_sm, int *threads,
-                        int *smem_bytes, int *grid_ctas);
+                        int *smem_bytes, int *grid_ctas, int *cluster);
+sv_status sv_launch_shape(const sv_ctx *ctx, int B, int *cluster, int *grid_ctas);
 
 /* Test hook: the limit, in nanoseconds, of each bounded wait for staged logits
  * (default 1 s).  0 makes every wait report expiry, so every sequence that

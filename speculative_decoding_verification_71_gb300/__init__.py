@@ -38,7 +38,8 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
-    "sv_set_pipeline", "sv_get_config", "sv_set_wait_limit_ns", "spec_verify_noalloc",
+    "sv_set_pipeline", "sv_set_cluster", "sv_get_config", "sv_launch_shape", "sv_set_wait_limit_ns",
+    "spec_verify_noalloc",
 )
 
 
@@ -98,8 +99,12 @@ def load_library(path: str | None = None):
     lib.spec_verify_reset_stats.argtypes = [P, P]
     lib.sv_set_pipeline.restype = c.c_int
     lib.sv_set_pipeline.argtypes = [P, c.c_int, c.c_int]
+    lib.sv_set_cluster.restype = c.c_int
+    lib.sv_set_cluster.argtypes = [P, c.c_int]
     lib.sv_get_config.restype = c.c_int
-    lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 5
+    lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 6
+    lib.sv_launch_shape.restype = c.c_int
+    lib.sv_launch_shape.argtypes = [P, c.c_int, c.POINTER(c.c_int), c.POINTER(c.c_int)]
     lib.sv_set_wait_limit_ns.restype = c.c_int
     lib.sv_set_wait_limit_ns.argtypes = [P, c.c_longlong]
     lib.spec_verify_noalloc.restype = c.c_int
@@ -257,7 +262,7 @@ class SpecVerifier:
             self._raise(st, "spec_verify_reset_stats")
 
     def set_pipeline(self, stages: int, ctas_per_sm: int = 0):
-        """Staging slots (16 KB each) per CTA and CTAs per SM (0 = as many as
+        """Staging slots (64 KB each) per CTA and CTAs per SM (0 = as many as
         fit); (0, 0) = automatic."""
         st = self.lib.sv_set_pipeline(self._ctx, int(stages), int(ctas_per_sm))
         if st != SV_OK:
@@ -268,13 +273,28 @@ class SpecVerifier:
         if st != SV_OK:
             self._raise(st, "sv_set_wait_limit_ns")
 
+    def set_cluster(self, cluster: int):
+        """CTAs that share each sequence, one vocabulary slice each (1, 2, 4
+        or 8); 0 = chosen per call from the batch size."""
+        st = self.lib.sv_set_cluster(self._ctx, int(cluster))
+        if st != SV_OK:
+            self._raise(st, "sv_set_cluster")
+
     def config(self):
-        vals = [ctypes.c_int() for _ in range(5)]
+        vals = [ctypes.c_int() for _ in range(6)]
         st = self.lib.sv_get_config(self._ctx, *[ctypes.byref(v) for v in vals])
         if st != SV_OK:
             self._raise(st, "sv_get_config")
-        return dict(zip(("stages", "ctas_per_sm", "threads", "smem_bytes", "grid_ctas"),
+        return dict(zip(("stages", "ctas_per_sm", "threads", "smem_bytes", "grid_ctas", "cluster"),
                         (v.value for v in vals)))
+
+    def launch_shape(self, B: int):
+        """(cluster size, CTAs in the grid) of a call with batch B."""
+        cs, ctas = ctypes.c_int(), ctypes.c_int()
+        st = self.lib.sv_launch_shape(self._ctx, int(B), ctypes.byref(cs), ctypes.byref(ctas))
+        if st != SV_OK:
+            self._raise(st, "sv_launch_shape")
+        return cs.value, ctas.value
 
 
 def spec_verify_noalloc(target, draft, tokens, draft_len, uniforms, temperature, out_tokens, out_len,

@@ -20,8 +20,10 @@ struct sv_ctx {
   sv_dtype dtype = SV_BF16;
   int elt = 2;
   int device = 0;
-  int stages = 6;
+  int stages = 3;
   int ctas_per_sm = 0;
+  int cluster = 0;             // 0: chosen per call
+  int max_clusters[4] = {0};   // clusters of 1, 2, 4, 8 CTAs that fit at once
   int num_sms = 0;
   int smem_bytes = 0;
   long long wait_limit_ns = sv::kDrainLimitNs;
@@ -45,7 +47,7 @@ sv_status cuda_fail(sv_ctx* ctx, cudaError_t e, const char* where) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Configure the staging ring (slots of 16 KB per CTA) and how many CTAs
+// Configure the staging ring (slots of 64 KB per CTA) and how many CTAs
 // share an SM (0: as many as fit); fails if the shape cannot be launched.
 sv_status configure(sv_ctx* ctx, int stages, int ctas_per_sm) {
   const int smem = sv::verify_smem_bytes(stages);
@@ -60,10 +62,26 @@ sv_status configure(sv_ctx* ctx, int stages, int ctas_per_sm) {
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   if (fit <= 0) return SV_ERR_UNSUPPORTED;
   if (ctas_per_sm > fit) return SV_ERR_UNSUPPORTED;
+  const int per_sm = ctas_per_sm > 0 ? ctas_per_sm : fit;
+  int clusters[4] = {0, 0, 0, 0};
+  for (int i = 0; i < 4; ++i) {
+    const int c = 1 << i;
+    e = sv::query_max_clusters(c, smem, &clusters[i]);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();   // a size the device cannot place is simply not offered
+      clusters[i] = 0;
+    }
+    const int cap = prop.multiProcessorCount * per_sm / c;
+    if (clusters[i] > cap) clusters[i] = cap;
+  }
+  if (clusters[0] <= 0) return SV_ERR_UNSUPPORTED;
+  if (ctx->cluster > 0 && clusters[__builtin_ctz(static_cast<unsigned>(ctx->cluster))] <= 0)
+    return SV_ERR_UNSUPPORTED;
   ctx->stages = stages;
-  ctx->ctas_per_sm = ctas_per_sm > 0 ? ctas_per_sm : fit;
+  ctx->ctas_per_sm = per_sm;
   ctx->num_sms = prop.multiProcessorCount;
   ctx->smem_bytes = smem;
+  for (int i = 0; i < 4; ++i) ctx->max_clusters[i] = clusters[i];
   return SV_OK;
 }
 
@@ -71,6 +89,17 @@ sv_status configure(sv_ctx* ctx, int stages, int ctas_per_sm) {
 sv_status configure_auto(sv_ctx* ctx) {
   if (configure(ctx, 3, 0) == SV_OK) return SV_OK;
   return configure(ctx, 2, 0);
+}
+
+// Cluster size and grid of a call with batch B.
+void launch_shape(const sv_ctx* ctx, int B, int* cluster, int* ctas) {
+  int cs = ctx->cluster;
+  if (cs == 0)
+    cs = sv::auto_cluster(B, static_cast<long long>(ctx->V) * ctx->elt, ctx->num_sms, ctx->max_clusters);
+  const int fit = ctx->max_clusters[__builtin_ctz(static_cast<unsigned>(cs))];
+  const int clusters = B < fit ? B : fit;
+  *cluster = cs;
+  *ctas = clusters * cs;
 }
 
 }  // namespace
@@ -215,9 +244,9 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
            (draft_logits == nullptr || aligned16(draft_logits));
   p.wait_limit_ns = ctx->wait_limit_ns;
   p.ws = ctx->ws;
-  // persistent grid: every CTA that fits at once, but never more than sequences
-  const int fit = ctx->num_sms * ctx->ctas_per_sm;
-  const int ctas = B < fit ? B : fit;
+  // persistent grid: every cluster that fits at once, but never more than sequences
+  int ctas = 0;
+  launch_shape(ctx, B, &p.cluster, &ctas);
   cudaError_t e = sv::launch_verify(p, ctas, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch verify");
   ctx->calls += 1;
@@ -296,14 +325,33 @@ sv_status sv_set_pipeline(sv_ctx* ctx, int stages, int ctas_per_sm) {
   return s;
 }
 
+sv_status sv_set_cluster(sv_ctx* ctx, int cluster) {
+  if (!ctx) return SV_ERR_INVALID_ARG;
+  if (cluster != 0 && cluster != 1 && cluster != 2 && cluster != 4 && cluster != 8) return SV_ERR_INVALID_ARG;
+  if (cluster > 0 && ctx->max_clusters[__builtin_ctz(static_cast<unsigned>(cluster))] <= 0)
+    return SV_ERR_UNSUPPORTED;
+  ctx->cluster = cluster;
+  return SV_OK;
+}
+
 sv_status sv_get_config(const sv_ctx* ctx, int* stages, int* ctas_per_sm, int* threads, int* smem_bytes,
-                        int* grid_ctas) {
+                        int* grid_ctas, int* cluster) {
   if (!ctx) return SV_ERR_INVALID_ARG;
   if (stages) *stages = ctx->stages;
   if (ctas_per_sm) *ctas_per_sm = ctx->ctas_per_sm;
   if (threads) *threads = sv::kThreads;
   if (smem_bytes) *smem_bytes = ctx->smem_bytes;
   if (grid_ctas) *grid_ctas = ctx->num_sms * ctx->ctas_per_sm;
+  if (cluster) *cluster = ctx->cluster;
+  return SV_OK;
+}
+
+sv_status sv_launch_shape(const sv_ctx* ctx, int B, int* cluster, int* grid_ctas) {
+  if (!ctx || B < 1 || B > ctx->max_B) return SV_ERR_INVALID_ARG;
+  int cs = 0, ctas = 0;
+  launch_shape(ctx, B, &cs, &ctas);
+  if (cluster) *cluster = cs;
+  if (grid_ctas) *grid_ctas = ctas;
   return SV_OK;
 }
 

@@ -7,13 +7,14 @@
 namespace sv {
 
 constexpr int kConsumerWarps = 16;                      // warps that compute
-constexpr int kThreads = (kConsumerWarps + 2) * 32;     // + a producer and a control warp
+constexpr int kThreads = (kConsumerWarps + 3) * 32;     // + producer, control and walker warps
 constexpr int kVecsPerLane = 8;                         // 16-byte vectors per lane and chunk
 constexpr int kVecsPerWarp = kVecsPerLane * 32;         // 256 x 16 B per warp and chunk
 constexpr int kChunkBytes = kVecsPerWarp * 16 * kConsumerWarps;  // one staging slot: 64 KB
 constexpr int kMaxChunks = 16;                          // rows up to 1 MiB
 constexpr int kMaxStages = 16;                          // staging slots per CTA
 constexpr long long kDrainLimitNs = 1000000000LL;       // second wait: always 1 s
+constexpr int kMaxCluster = 8;                          // CTAs sharing one sequence (portable limit)
 
 // Counters kept on the device (unsigned long long each).
 enum StatSlot {
@@ -56,6 +57,7 @@ struct VerifyParams {
   float c2;             // log2(e) / T
   int stages;           // staging slots per CTA (2..kMaxStages)
   int bulk;             // 1: rows staged with cp.async.bulk; 0: plain loads
+  int cluster;          // CTAs per cluster: each takes one slice of every row (1, 2, 4 or 8)
   long long wait_limit_ns;
   Workspace ws;
 };
@@ -64,6 +66,7 @@ struct VerifyParams {
 cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s);
 cudaError_t prepare_verify_kernel(int smem_bytes);
 cudaError_t query_ctas_per_sm(int smem_bytes, int* out);
+cudaError_t query_max_clusters(int cluster, int smem_bytes, int* out);
 cudaError_t launch_compact(int B, int k, const int* out_tokens, const int* out_len,
                            int* packed, int* offsets, cudaStream_t s);
 cudaError_t launch_debug(const Workspace& ws, int B, int k, int greedy, float inv_T, double* lse_t,
@@ -72,5 +75,22 @@ cudaError_t launch_init_workspace(const Workspace& ws, cudaStream_t s);
 
 // Shared-memory bytes of the verify kernel with `stages` staging slots.
 int verify_smem_bytes(int stages);
+
+// Cluster size chosen when the caller leaves it open.  A sequence is the
+// unit of work of a cluster, so with few sequences per cluster the last ones
+// to finish leave most SMs idle; splitting every row over more CTAs makes the
+// units smaller.  Slices stay at 32 KB or more, and a size is only taken if
+// its clusters still cover nearly every SM (max_clusters[i]: clusters of
+// 2^i CTAs that fit at once).
+inline int auto_cluster(int B, long long row_bytes, int num_sms, const int (&max_clusters)[4]) {
+  int best = 1;
+  for (int i = 1, c = 2; c <= kMaxCluster; ++i, c *= 2) {
+    if (static_cast<long long>(B) * c > 4LL * num_sms) break;
+    if (row_bytes / c < 32 * 1024) break;
+    if (max_clusters[i] * c * 10 < num_sms * 9) continue;
+    best = c;
+  }
+  return best;
+}
 
 }  // namespace sv

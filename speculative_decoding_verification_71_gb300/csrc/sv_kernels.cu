@@ -1,33 +1,39 @@
 // Speculative-sampling verification kernels for sm_103a.
 //
-// verify_kernel is persistent and warp-specialised.  Each CTA verifies whole
-// sequences, one after another, taking them from a work list ordered longest
-// first (plan_kernel) with an atomic ticket:
+// verify_kernel is persistent and warp-specialised.  A cluster of cs CTAs
+// (1, 2, 4 or 8) verifies whole sequences, one after another, taken from a
+// work list ordered longest first (plan_kernel) with an atomic ticket.  Each
+// CTA of the cluster owns one slice of the vocabulary (a 1/cs share of every
+// row, in 128-byte-aligned pieces) and runs four roles:
 //
-//   producer warp   streams the sequence's rows in position order (target 0,
-//                   draft 0, target 1, draft 1, ..., target k_b) through a
-//                   ring of 16 KB shared-memory slots with cp.async.bulk, and
-//                   runs ahead into the next sequence while the consumers
-//                   are busy, so HBM reads never wait on arithmetic;
-//   8 consumer warps  fold every 16 KB chunk into per-warp running maxima and
-//                   sums of 2^(z c - fl(m c)), c = log2(e)/T (one ex2 per
-//                   logit), pick up the drafted token's logit, and at each
-//                   row end combine the warps into the row's log-sum-exp.
+//   producer warp    streams its slice of the sequence's rows in position
+//                    order (target 0, draft 0, target 1, ..., target k_b)
+//                    through a ring of 64 KB shared-memory slots with
+//                    cp.async.bulk, and runs ahead into the next sequence;
+//   16 consumer warps  fold every chunk into per-warp running maxima and sums
+//                    of 2^(z c - fl(m c)), c = log2(e)/T (one ex2 per logit),
+//                    and pick up the drafted token's logit;
+//   control warp     combines the warps into the slice's part of the row,
+//                    sends it to every CTA of the cluster (st.async into their
+//                    shared memory, counted on their mbarriers), combines the
+//                    parts into the row's log-sum-exp and decides: after draft
+//                    row i, alpha_i = min(1, p_i(x_i) / q_i(x_i)) and accept iff
+//                    u_i < alpha_i, up to the first rejection;
+//   walker warp      walks the one segment that holds the drawn token and
+//                    writes the sequence's outputs.
 //
-// Because one CTA sees the positions of a sequence in order, the first
-// rejection is known exactly:
-//   * after draft row i: alpha_i = min(1, p_i(x_i) / q_i(x_i)); accept iff
-//     u_i < alpha_i (every position's alpha is kept for diagnostics);
-//   * at the first rejection a: the pair (target a, draft a), read moments
-//     ago and still in L2, is read again to get exact per-segment masses of
-//     max(0, p - q); a warp scan finds the segment holding s*S and one warp
-//     walks that segment to the drawn token;
-//   * if every draft is accepted, the bonus row needs no second read at
-//     all: its per-segment sums were kept while streaming, so only the one
-//     segment holding s*S is read again.
-// Every needed logit crosses HBM once; the only extra reads are the rejected
-// pair (from L2) and one segment.  The CTA writes the sequence's outputs
-// itself: no atomics on the data path and no waiting on other CTAs.
+// Because every CTA of a cluster sees the positions of a sequence in order,
+// the first rejection is known exactly, identically everywhere:
+//   * at the first rejection a, the pair (target a, draft a) is read again
+//     (each CTA its slice) for exact per-segment masses of max(0, p - q) and
+//     of p; the slice, then the segment, holding s*S is found and the walker
+//     of the CTA that owns it finds the token;
+//   * if every draft is accepted, the bonus row needs no second pass: its
+//     per-segment sums were kept while streaming, so only the one segment
+//     holding s*S is read again.
+// Every CTA of a cluster inserts the re-reads at the same place in its
+// stream, so the CTAs see one common order of events and each waits only for
+// events that come earlier in it; every wait is bounded.
 //
 // The rule implemented (accept with min(1, p/q), stop at the first
 // rejection, resample from max(0, p - q) or draw the bonus token from the
@@ -293,20 +299,90 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
+// Clusters: distributed shared memory between the CTAs of one cluster
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+__device__ __forceinline__ int cluster_ctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+// Address of shared variable `p` in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t peer(const volatile void* p, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r) : "r"(smem_addr(const_cast<const void*>(p))), "r"(rank));
+  return r;
+}
+// Asynchronous stores into the shared memory of a CTA of the cluster; each
+// counts its bytes on an mbarrier of that CTA (complete_tx), so a receiver
+// that saw the phase complete sees the data, with no fence on either side.
+__device__ __forceinline__ void st_async(uint32_t addr, uint4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void st_async(uint32_t addr, int v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               :: "r"(addr), "r"(v), "r"(bar) : "memory");
+}
+// A plain arrival on an mbarrier of a CTA of the cluster.  No data rides on
+// it: it only says that a buffer of the arriving CTA's has been read (the
+// values read are already in registers) and may be written again.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" :: "r"(addr) : "memory");
+}
+// Every thread of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Order-preserving int view of a non-NaN float (for redux.sync max), and back.
+__device__ __forceinline__ int ordered_key(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7fffffff;
+}
+__device__ __forceinline__ float from_ordered_key(int k) {
+  return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
+}
+
+// Wait for a phase in hardware for at most about `ns` nanoseconds (the warp
+// is not scheduled meanwhile); returns whether the phase completed.
+__device__ __forceinline__ bool mbar_park(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(done) : "r"(smem_addr(bar)), "r"(parity), "r"(ns) : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
 // Shared control block
 // ---------------------------------------------------------------------------
 
 // What a staging slot holds.
-//   kind 0 / 1: chunk `chunk` of the target / draft row at position pos;
-//   kind 2:     chunk `chunk` of the re-read of the pair at pos for its draw:
-//               the first half of the slot holds target logits, the second
-//               half the draft logits of the same vocabulary range; x holds
-//               the draw mode (1: residual max(0, p - q), 2: p alone) and
-//               K0, L0, K1, L1 the pair's normalisers;
-//   kind -1:    no more work.
+//   kind 0 / 1: chunk `chunk` of this CTA's slice of the target / draft row
+//               at position pos of sequence b;
+//   kind 2:     chunk `chunk` of the re-read of this CTA's slice of the
+//               rejected pair at pos: the first half of the slot holds target
+//               logits, the second half the draft logits of the same range;
+//               K0, L0, K1, L1 are the pair's normalisers;
+//   kind -1:    no more work; x = draws inserted in all.
 struct Desc {
   int b, kb, pos, kind;
-  int chunk, nchunks, x, rec;  // x: drafted token at pos (rows of pairs, else -1); rec: sequence record
+  int chunk, nchunks, x, rec;  // x: drafted token at pos (rows of pairs, else -1); rec: record slot
+  int seq, pad;                // seq: sequences streamed before this one
   float u, s;                  // accept uniform at pos, sampling uniform of b
   float K0, L0, K1, L1;
 };
@@ -316,32 +392,58 @@ struct RowBuf {
   Desc d;
   float wK[kConsumerWarps], wS[kConsumerWarps], wM[kConsumerWarps];
   int wArg[kConsumerWarps], wBad[kConsumerWarps];
-  float zx;                                  // logit of the drafted token
+  float zx;                                  // logit of the drafted token (if in this slice)
   float segK[kMaxChunks * kConsumerWarps];   // bonus rows: per-segment fl(m c)
   float segS[kMaxChunks * kConsumerWarps];   // bonus rows: per-segment sum
 };
 
-// One sequence in flight (control warp only).  Its stream and its draw can
-// finish in either order; the outputs are written when both are done.
+// One CTA's reduction of its slice of a row, sent to every CTA of the cluster.
+struct alignas(16) RowPart {
+  float M, K, S, zx;           // max logit, fl(M c), sum 2^(z c - K), drafted logit
+  int arg, bad, has_zx, pad;   // argmax, error bits, zx present
+};
+
+// One CTA's masses of its slice of a re-read pair.
+struct alignas(16) DrawPart {
+  double r, p;                 // sum max(0, p - q), sum p
+  int err, pad[3];
+};
+
+// One sequence in flight, kept identically by every CTA of the cluster.
 struct SeqRec {
   int b, kb, a, err, y, zero_resid;
-  int pending;                 // events left before the outputs can be written
+  int open;                    // from the first row until the outputs are settled
+  int draw;                    // a residual draw follows (final once resolved)
+  volatile int resolved;       // seq + 1 once `draw` and the normalisers are final
   float s;                     // sampling uniform
+  float Kt, Lt, Kd, Ld;        // normalisers of the rejected pair
+  int tok[32];                 // drafted tokens, taken from the rows as they pass
 };
 
-// A re-read request as the control warp remembers it.
-struct DrawReq {
-  int b, pos, rec, mode;
-  float Kt, Lt, Kd, Ld;
+// An inverse-CDF walk over one segment, handed from the control warp to the
+// walker warp (which reads the logits and writes the sequence's outputs).
+struct WalkReq {
+  int rec, mode;               // mode 0: p over a stream segment; 1: max(0, p - q) / 2: p over a draw segment
+  int v0, b, pos;              // first vector of the segment (-1: nothing to walk), row
+  int pad;
+  double t;                    // target weight left at the segment's start
+  float K0, L0, K1, L1;        // normalisers of the target (0) and draft (1) rows
 };
 
-constexpr int kRecs = 8;       // sequence records (ring)
-constexpr int kReqs = 8;       // re-read requests (ring)
-constexpr int kRowBufs = 4;    // row buffers (ring)
+constexpr int kRecs = 32;          // sequence records (ring)
+constexpr int kWalkReqs = 16;      // walk requests (ring)
+constexpr int kRowBufs = 4;        // row buffers (ring)
+constexpr int kXRing = 4;          // exchange slots of rows and of draws
+constexpr int kDrawLagChunks = 6;  // a draw is inserted about this many chunks after its sequence ends ...
+constexpr int kMaxPending = 24;    // ... or when this many sequences wait for theirs
 constexpr int kHalfBytes = kChunkBytes / 2;                          // one row's part of a draw chunk
 constexpr int kDrawVecsPerWarp = kHalfBytes / 16 / kConsumerWarps;   // 128
 constexpr int kDrawVecsPerLane = kDrawVecsPerWarp / 32;              // 4
 constexpr int kMaxDrawSegs = 2 * kMaxChunks * kConsumerWarps;
+constexpr int kSliceAlign = 64;    // slice boundaries in logits (128 B of bf16)
+
+static_assert(sizeof(RowPart) == 32 && sizeof(DrawPart) == 32, "parts travel as two 16-byte stores");
+static_assert(kMaxPending + 4 <= kRecs, "records must outlive the pending window");
 
 enum : int { kErrBadToken = 1 << 3, kErrNonfinite = 1 << 4, kErrTimeout = 1 << 5 };
 
@@ -352,23 +454,32 @@ struct Ctrl {
   uint64_t row_free[kRowBufs];      // row consumed by the control warp
   uint64_t draw_ready[2];           // draw masses complete (one arrival per consumer warp)
   uint64_t draw_free[2];            // draw masses consumed by the control warp
+  uint64_t xrow_ready[kXRing];      // every CTA's part of a row has arrived here
+  uint64_t xrow_free[kXRing];       // every CTA has read this CTA's part of a row
+  uint64_t xdraw_ready[kXRing];     // the same for draws
+  uint64_t xdraw_free[kXRing];
+  uint64_t tk_full[2];              // a ticket was delivered (by the first CTA)
+  uint64_t tk_empty[2];             // first CTA: every CTA has read the ticket
+  RowPart xrow[kXRing][kMaxCluster];
+  DrawPart xdraw[kXRing][kMaxCluster];
   Desc desc[kMaxStages];
   RowBuf rows[kRowBufs];
-  double rmass[2][kMaxDrawSegs];    // per-segment weights of a re-read draw
+  float rmass[2][kMaxDrawSegs];     // per-segment sum max(0, p - q) of a re-read
+  float pmass[2][kMaxDrawSegs];     // per-segment sum p of a re-read
+  int draw_rec[2];
   int draw_err[2];
-  // re-read requests: the control warp pushes, the producer pops
-  DrawReq req[kReqs];
-  volatile int req_head, req_tail;
-  volatile int seqs_finished;       // sequences whose outputs are written
-  // control warp state
+  volatile int tk[2];
+  int pend_end[kRecs];              // producer: rows streamed when a sequence ended
   SeqRec rec[kRecs];
-  DrawReq ctl_req[kReqs];           // every pushed request, by push order, until its draw is done
-  int pushed;                       // requests pushed so far
-  float pairK, pairL, pairZx;       // target row of the current pair
   double bmass[kMaxChunks * kConsumerWarps];
+  WalkReq wreq[kWalkReqs];          // control warp -> walker warp
+  volatile int wreq_head, wreq_tail;
+  volatile int ctl_done;            // the control warp has left
+  float pairK, pairL, pairZx;       // target row of the current pair
 };
 
 constexpr int kCtrlBytes = ((static_cast<int>(sizeof(Ctrl)) + 1023) / 1024) * 1024;
+static_assert(kCtrlBytes + 3 * kChunkBytes <= 227 * 1024, "three staging slots must fit in one CTA");
 
 // ---------------------------------------------------------------------------
 // plan_kernel: the work list (valid sequences, longest first) and resets.
@@ -443,17 +554,31 @@ struct Verifier {
   Ctrl& C;
   unsigned char* ring;
   const int lane, warp;
+  const int cs, rank;           // CTAs in the cluster, this CTA's rank
   const long long row_bytes;    // V * ELT
-  const int nchunks;            // stream chunks per row
-  const int ndraw;              // draw chunks per row
-  const int nvec_row;           // 16-byte vectors per row (last one padded)
+  int slice_lo, slice_n;        // this CTA's logits [slice_lo, slice_lo + slice_n) of every row
+  int slice_bytes;
+  int nchunks;                  // stream chunks per slice (at least one)
+  int ndraw;                    // draw chunks per slice (at least one)
+  int v_lo, v_hi;               // 16-byte vectors of the row covering the slice
+  int lag_rows;                 // rows between a sequence's end and its re-read (same in every CTA)
 
-  __device__ Verifier(const VerifyParams& p, Ctrl& c, unsigned char* r, int ln, int wp)
-      : P(p), C(c), ring(r), lane(ln), warp(wp),
-        row_bytes(static_cast<long long>(p.V) * ELT),
-        nchunks(static_cast<int>((static_cast<long long>(p.V) * ELT + kChunkBytes - 1) / kChunkBytes)),
-        ndraw(static_cast<int>((static_cast<long long>(p.V) * ELT + kHalfBytes - 1) / kHalfBytes)),
-        nvec_row(static_cast<int>((static_cast<long long>(p.V) * ELT + 15) / 16)) {}
+  __device__ Verifier(const VerifyParams& p, Ctrl& c, unsigned char* r, int ln, int wp, int ncta, int rk)
+      : P(p), C(c), ring(r), lane(ln), warp(wp), cs(ncta), rank(rk),
+        row_bytes(static_cast<long long>(p.V) * ELT) {
+    const int per = ((p.V + cs - 1) / cs + kSliceAlign - 1) / kSliceAlign * kSliceAlign;
+    slice_lo = min(p.V, rank * per);
+    const int hi = min(p.V, slice_lo + per);
+    slice_n = hi - slice_lo;
+    slice_bytes = slice_n * ELT;
+    nchunks = max(1, (slice_bytes + kChunkBytes - 1) / kChunkBytes);
+    ndraw = max(1, (slice_bytes + kHalfBytes - 1) / kHalfBytes);
+    v_lo = slice_lo / NV;                       // slice_lo is a multiple of kSliceAlign
+    v_hi = (hi * ELT + 15) / 16;
+    // counted in chunks of the first (largest) slice so that every CTA agrees
+    const int chunks0 = max(1, (min(p.V, per) * ELT + kChunkBytes - 1) / kChunkBytes);
+    lag_rows = max(1, (kDrawLagChunks + chunks0 - 1) / chunks0);
+  }
 
   __device__ const unsigned char* row_ptr(int b, int pos, int kind) const {
     if (kind == 0)
@@ -463,9 +588,9 @@ struct Verifier {
            (static_cast<size_t>(b) * P.k + pos) * static_cast<size_t>(row_bytes);
   }
 
-  // Vector v of a row read straight from global memory, -inf beyond V.
+  // Vector v of a row read straight from global memory, -inf outside the slice.
   __device__ uint4 load_global_raw(const unsigned char* row, int v) const {
-    if (v >= nvec_row) return V::neg_inf();
+    if (v < v_lo || v >= v_hi) return V::neg_inf();
     if (P.bulk) return __ldg(reinterpret_cast<const uint4*>(row) + v);
     unsigned char buf[16];
 #pragma unroll
@@ -487,25 +612,36 @@ struct Verifier {
     return ok != 0;
   }
 
+  // One look at a phase (lane 0 looks, every lane learns the answer and, if
+  // it completed, takes its own acquire).
+  __device__ bool probe(uint64_t* bar, uint32_t parity) const {
+    int r = 0;
+    if (lane == 0) r = mbar_test_wait(bar, parity) ? 1 : 0;
+    r = __shfl_sync(0xffffffffu, r, 0);
+    if (r) mbar_test_wait(bar, parity);
+    return r != 0;
+  }
+
   // ======================= producer ==========================================
+  // Every CTA of a cluster streams its slice of the same rows and inserts the
+  // same re-reads at the same places, so the CTAs see one common order of
+  // events and each waits only for events that come earlier in it.
 
   // Copy `bytes` of a row starting at byte `off` into dst (bulk or plain).
   __device__ void fill(unsigned char* dst, const unsigned char* src, long long off, int bytes,
                        uint64_t* bar, bool hint, uint64_t policy) {
     if (P.bulk) {
-      if (lane == 0) {
+      if (lane == 0 && bytes > 0) {
         if (hint) bulk_load_hint(dst, src + off, static_cast<uint32_t>(bytes), bar, policy);
         else bulk_load(dst, src + off, static_cast<uint32_t>(bytes), bar);
       }
     } else {
       // plain loads (rows not 16-byte aligned); pad the last vector with -inf
       const int e0 = static_cast<int>(off / ELT);
-      const int n = (bytes + ELT - 1) / ELT;
+      const int n = bytes / ELT;
       const int npad = ((n + NV - 1) / NV) * NV;
-      for (int e = lane; e < npad; e += 32) {
-        const int xg = e0 + e;
-        V::store_scalar(dst, e, xg < P.V ? V::scalar(src, xg) : -INFINITY);
-      }
+      for (int e = lane; e < npad; e += 32)
+        V::store_scalar(dst, e, e < n ? V::scalar(src, e0 + e) : -INFINITY);
     }
   }
 
@@ -514,44 +650,91 @@ struct Verifier {
     return warp_wait(&C.empty[q % S], ((q / S) & 1) ^ 1);
   }
 
-  // Issue the draw chunks of every queued re-read request.
-  __device__ bool service_requests(int& q) {
-    const int S = P.stages;
-    while (true) {
-      int head = 0, tail = 0;
-      if (lane == 0) { head = C.req_head; tail = C.req_tail; }
-      head = __shfl_sync(0xffffffffu, head, 0);
-      tail = __shfl_sync(0xffffffffu, tail, 0);
-      if (head == tail) return true;
-      const DrawReq r = C.req[head % kReqs];
-      __syncwarp();
-      if (lane == 0) { __threadfence_block(); C.req_head = head + 1; }
-      const unsigned char* srcT = row_ptr(r.b, r.pos, 0);
-      const unsigned char* srcD = row_ptr(r.b, r.pos, 1);
-      for (int c = 0; c < ndraw; ++c) {
-        if (!acquire_slot(q)) return false;
-        const int slot = q % S;
-        const long long off = static_cast<long long>(c) * kHalfBytes;
-        const long long rem = row_bytes - off;
-        const int bytes = static_cast<int>(rem < kHalfBytes ? rem : kHalfBytes);
-        unsigned char* dst = ring + static_cast<size_t>(slot) * kChunkBytes;
-        if (lane == 0) {
-          Desc& d = C.desc[slot];
-          d.b = r.b; d.kb = 0; d.pos = r.pos; d.kind = 2;
-          d.chunk = c; d.nchunks = ndraw; d.x = r.mode; d.rec = r.rec;
-          d.u = 0.f; d.s = 0.f;
-          d.K0 = r.Kt; d.L0 = r.Lt; d.K1 = r.Kd; d.L1 = r.Ld;
-          if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(r.mode == 1 ? 2 * bytes : bytes));
-        }
-        fill(dst, srcT, off, bytes, &C.full[slot], false, 0);
-        if (r.mode == 1) fill(dst + kHalfBytes, srcD, off, bytes, &C.full[slot], false, 0);
-        if (!P.bulk) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&C.full[slot]);
-        }
-        ++q;
-      }
+  // The next work-list entry: the first CTA of the cluster takes it and
+  // hands it to every CTA (itself included).
+  __device__ int take_ticket(int& tki, bool& ok) {
+    const int slot = tki & 1;
+    const uint32_t ph = static_cast<uint32_t>(tki >> 1) & 1u;
+    ++tki;
+    if (rank == 0) {
+      if (!(ok = warp_wait(&C.tk_empty[slot], ph ^ 1u))) return 0x7fffffff;
+      int t = 0;
+      if (lane == 0) t = atomicAdd(P.ws.ticket, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (lane < cs) st_async(peer(&C.tk[slot], lane), t, peer(&C.tk_full[slot], lane));
     }
+    if (!(ok = warp_wait(&C.tk_full[slot], ph))) return 0x7fffffff;
+    int t = 0;
+    if (lane == 0) {
+      t = C.tk[slot];
+      mbar_expect_tx(&C.tk_full[slot], 4u);              // armed for the slot's next ticket
+      mbar_arrive_peer(peer(&C.tk_empty[slot], 0));
+    }
+    return __shfl_sync(0xffffffffu, t, 0);
+  }
+
+  // Issue the re-reads of the waiting sequences whose turn has come: lag_rows
+  // rows after the sequence ended (long enough for the control warp to have
+  // decided, normally), when kMaxPending sequences wait, or (all) at the end.
+  __device__ bool insert_due(int& q, int& pend, int streamed, int rows, int& draws, bool all) {
+    const int S = P.stages;
+    while (pend < streamed) {
+      const int rc = pend % kRecs;
+      if (!all && rows - C.pend_end[rc] < lag_rows && streamed - pend < kMaxPending) return true;
+      int res = 0, drw = 0, b = 0, pos = 0;
+      float Kt = 0.f, Lt = 0.f, Kd = 0.f, Ld = 0.f;
+      if (lane == 0) {
+        const unsigned long long t0 = global_ns();
+        while (true) {
+          if (C.rec[rc].resolved == pend + 1) { res = 1; break; }
+          if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) break;
+          __nanosleep(64);
+        }
+        if (res) {
+          __threadfence_block();
+          const SeqRec& R = C.rec[rc];
+          drw = R.draw; b = R.b; pos = R.a;
+          Kt = R.Kt; Lt = R.Lt; Kd = R.Kd; Ld = R.Ld;
+        } else {
+          atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+        }
+      }
+      res = __shfl_sync(0xffffffffu, res, 0);
+      if (!res) return false;
+      drw = __shfl_sync(0xffffffffu, drw, 0);
+      if (drw) {
+        b = __shfl_sync(0xffffffffu, b, 0);
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        const unsigned char* srcT = row_ptr(b, pos, 0);
+        const unsigned char* srcD = row_ptr(b, pos, 1);
+        for (int c = 0; c < ndraw; ++c) {
+          if (!acquire_slot(q)) return false;
+          const int slot = q % S;
+          const int rem = slice_bytes - c * kHalfBytes;
+          const int bytes = rem < kHalfBytes ? max(rem, 0) : kHalfBytes;
+          const long long off = static_cast<long long>(slice_lo) * ELT + static_cast<long long>(c) * kHalfBytes;
+          unsigned char* dst = ring + static_cast<size_t>(slot) * kChunkBytes;
+          if (lane == 0) {
+            Desc& d = C.desc[slot];
+            d.b = b; d.kb = 0; d.pos = pos; d.kind = 2;
+            d.chunk = c; d.nchunks = ndraw; d.x = -1; d.rec = rc; d.seq = pend;
+            d.u = 0.f; d.s = 0.f;
+            d.K0 = Kt; d.L0 = Lt; d.K1 = Kd; d.L1 = Ld;
+            if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(2 * bytes));
+          }
+          fill(dst, srcT, off, bytes, &C.full[slot], false, 0);
+          fill(dst + kHalfBytes, srcD, off, bytes, &C.full[slot], false, 0);
+          if (!P.bulk) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&C.full[slot]);
+          }
+          ++q;
+        }
+        ++draws;
+      }
+      ++pend;
+    }
+    return true;
   }
 
   __device__ void produce() {
@@ -559,15 +742,10 @@ struct Verifier {
     const int k = P.k;
     const int n_seqs = __ldcg(P.ws.n_seqs);
     const uint64_t evict_first = evict_first_policy();
-    int q = 0, streamed = 0;
+    int q = 0, tki = 0, streamed = 0, rows = 0, draws = 0, pend = 0;
+    bool ok = true;
     // the next sequence's work-list entry, tokens and uniforms are fetched one
     // sequence ahead so that a sequence start never waits on global memory
-    int t = 0;
-    if (lane == 0) t = atomicAdd(P.ws.ticket, 1);
-    t = __shfl_sync(0xffffffffu, t, 0);
-    int2 sq = make_int2(-1, 0);
-    int xj = -1;
-    float uj = 0.f;
     auto fetch = [&](int tt, int2& s_, int& x_, float& u_) {
       s_ = make_int2(-1, 0);
       x_ = -1;
@@ -578,15 +756,18 @@ struct Verifier {
         u_ = (!P.greedy && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(s_.x) * (k + 1) + lane) : 0.f;
       }
     };
+    int t = take_ticket(tki, ok);
+    int2 sq;
+    int xj;
+    float uj;
     fetch(t, sq, xj, uj);
-    bool ok = true;
     while (ok && t < n_seqs) {
       const int b = sq.x, kb = sq.y;
-      const int rec = streamed % kRecs;
+      const int rc = streamed % kRecs;
       // the next ticket is taken when this sequence's last row starts: late
-      // enough that sequences keep going to whichever CTA frees up first
+      // enough that sequences keep going to whichever cluster frees up first
       // (longest first), early enough to hide the fetch behind that row
-      int t_next = 0;
+      int t_next = 0x7fffffff;
       int2 sq_next = make_int2(-1, 0);
       int xj_next = -1;
       float uj_next = 0.f;
@@ -594,6 +775,7 @@ struct Verifier {
       const float s_samp = __shfl_sync(0xffffffffu, uj, k);
       const int nrows = P.greedy ? kb + 1 : 2 * kb + 1;
       for (int r = 0; r < nrows && ok; ++r) {
+        if (!(ok = insert_due(q, pend, streamed, rows, draws, false))) break;
         int pos, kind;
         if (P.greedy) { pos = r; kind = 0; }
         else if (r < 2 * kb) { pos = r >> 1; kind = r & 1; }
@@ -604,14 +786,14 @@ struct Verifier {
         for (int c = 0; c < nchunks && ok; ++c) {
           if (!(ok = acquire_slot(q))) break;
           const int slot = q % S;
-          const long long off = static_cast<long long>(c) * kChunkBytes;
-          const long long rem = row_bytes - off;
-          const int bytes = static_cast<int>(rem < kChunkBytes ? rem : kChunkBytes);
+          const int rem = slice_bytes - c * kChunkBytes;
+          const int bytes = rem < kChunkBytes ? max(rem, 0) : kChunkBytes;
+          const long long off = static_cast<long long>(slice_lo) * ELT + static_cast<long long>(c) * kChunkBytes;
           if (lane == 0) {
             Desc& d = C.desc[slot];
             d.b = b; d.kb = kb; d.pos = pos; d.kind = kind;
             d.chunk = c; d.nchunks = nchunks;
-            d.x = pos < kb ? x : -1; d.rec = rec;
+            d.x = pos < kb ? x : -1; d.rec = rc; d.seq = streamed;
             d.u = u; d.s = s_samp;
             if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(bytes));
           }
@@ -624,45 +806,32 @@ struct Verifier {
           }
           ++q;
           if (!fetched && r == nrows - 1) {
-            if (lane == 0) t_next = atomicAdd(P.ws.ticket, 1);
-            t_next = __shfl_sync(0xffffffffu, t_next, 0);
+            t_next = take_ticket(tki, ok);
             fetch(t_next, sq_next, xj_next, uj_next);
             fetched = true;
           }
-          ok = service_requests(q);
         }
+        ++rows;
       }
+      if (!ok) break;
       if (!fetched) {
-        if (lane == 0) t_next = atomicAdd(P.ws.ticket, 1);
-        t_next = __shfl_sync(0xffffffffu, t_next, 0);
+        t_next = take_ticket(tki, ok);
         fetch(t_next, sq_next, xj_next, uj_next);
       }
+      if (lane == 0) C.pend_end[rc] = rows;
+      __syncwarp();
       ++streamed;
       t = t_next;
       sq = sq_next;
       xj = xj_next;
       uj = uj_next;
     }
-    // no more sequences: keep serving re-reads until every streamed sequence
-    // is finished, then signal the end (bounded: 1 s without progress)
-    unsigned long long t0 = global_ns();
-    int last_done = -1;
-    while (ok) {
-      ok = service_requests(q);
-      int done = 0;
-      if (lane == 0) done = C.seqs_finished;
-      done = __shfl_sync(0xffffffffu, done, 0);
-      if (done >= streamed) break;
-      if (done != last_done) { last_done = done; t0 = global_ns(); }
-      if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
-        if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-        break;
-      }
-      __nanosleep(256);
-    }
+    if (ok) insert_due(q, pend, streamed, rows, draws, true);
+    // the end of the work (also after an error, so that every warp stops)
     if (acquire_slot(q)) {
       if (lane == 0) {
         C.desc[q % S].kind = -1;
+        C.desc[q % S].x = draws;
         mbar_arrive(&C.full[q % S]);
       }
     }
@@ -695,7 +864,7 @@ struct Verifier {
         // tell the control warp that the work is over
         const int buf = rr % kRowBufs;
         if (!warp_wait(&C.row_free[buf], ((rr / kRowBufs) & 1) ^ 1)) return;
-        if (warp == 0 && lane == 0) C.rows[buf].d.kind = -1;
+        if (warp == 0 && lane == 0) C.rows[buf].d = d;
         __syncwarp();
         if (lane == 0) mbar_arrive(&C.row_ready[buf]);
         return;
@@ -705,27 +874,25 @@ struct Verifier {
         // ---- a chunk of a pair's re-read: per-segment draw weights --------
         const int dp = dr & 1;
         if (d.chunk == 0 && !warp_wait(&C.draw_free[dp], ((dr >> 1) & 1) ^ 1)) return;
-        const bool resid = (d.x == 1);
         const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
-        const long long off = static_cast<long long>(d.chunk) * kHalfBytes;
-        const long long rem = row_bytes - off;
-        const int nvec = static_cast<int>(((rem < kHalfBytes ? rem : kHalfBytes) + 15) / 16);
+        const int rem = slice_bytes - d.chunk * kHalfBytes;
+        const int nvec = (min(max(rem, 0), kHalfBytes) + 15) / 16;
         uint4 rt[kDrawVecsPerLane], rd[kDrawVecsPerLane];
 #pragma unroll
         for (int j = 0; j < kDrawVecsPerLane; ++j) {
           const int v = warp * kDrawVecsPerWarp + j * 32 + lane;
           const bool in = v < nvec;
           rt[j] = in ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
-          rd[j] = (in && resid) ? *reinterpret_cast<const uint4*>(data + kHalfBytes + static_cast<size_t>(v) * 16)
-                                : V::neg_inf();
+          rd[j] = in ? *reinterpret_cast<const uint4*>(data + kHalfBytes + static_cast<size_t>(v) * 16)
+                     : V::neg_inf();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&C.empty[slot]);
         const f2 cc = pack2(c2, c2), nkt = pack2(-d.K0, -d.K0), nlt = pack2(-d.L0, -d.L0);
         const f2 nkd = pack2(-d.K1, -d.K1), nld = pack2(-d.L1, -d.L1);
-        f2 acc[NV / 2];
+        f2 accr[NV / 2], accp[NV / 2];
 #pragma unroll
-        for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
+        for (int i = 0; i < NV / 2; ++i) { accr[i] = 0ull; accp[i] = 0ull; }
 #pragma unroll
         for (int j = 0; j < kDrawVecsPerLane; ++j) {
           f2 zt[NV / 2], zd[NV / 2];
@@ -735,22 +902,24 @@ struct Verifier {
           for (int i = 0; i < NV / 2; ++i) {
             // the same roundings as the scalar fmaf(z, c, -K) - L of the walk
             const f2 p = exp2_2(add2(fma2(zt[i], cc, nkt), nlt));
-            if (resid) {
-              float d0, d1;
-              unpack2(sub2(p, exp2_2(add2(fma2(zd[i], cc, nkd), nld))), d0, d1);
-              acc[i] = add2(acc[i], pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
-            } else {
-              acc[i] = add2(acc[i], p);
-            }
+            float d0, d1;
+            unpack2(sub2(p, exp2_2(add2(fma2(zd[i], cc, nkd), nld))), d0, d1);
+            accr[i] = add2(accr[i], pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+            accp[i] = add2(accp[i], p);
           }
         }
-        float a0, a1, sum = 0.f;
+        float a0, a1, sr = 0.f, sp = 0.f;
 #pragma unroll
-        for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); sum += a0 + a1; }
-        const float ws = warp_sum(sum);
+        for (int i = 0; i < NV / 2; ++i) {
+          unpack2(accr[i], a0, a1); sr += a0 + a1;
+          unpack2(accp[i], a0, a1); sp += a0 + a1;
+        }
+        const float wr = warp_sum(sr), wp = warp_sum(sp);
         if (lane == 0) {
-          C.rmass[dp][d.chunk * kConsumerWarps + warp] = static_cast<double>(ws);
+          C.rmass[dp][d.chunk * kConsumerWarps + warp] = wr;
+          C.pmass[dp][d.chunk * kConsumerWarps + warp] = wp;
           if (timed_out) atomicOr(&C.draw_err[dp], 1);
+          if (warp == 0 && d.chunk == d.nchunks - 1) C.draw_rec[dp] = d.rec;
         }
         if (d.chunk == d.nchunks - 1) {
           __syncwarp();
@@ -769,9 +938,8 @@ struct Verifier {
         rK = -INFINITY; rS = 0.f; rM = -INFINITY; rArg = 0x7fffffff; rBad = 0;
       }
       const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
-      const long long off = static_cast<long long>(d.chunk) * kChunkBytes;
-      const long long rem = row_bytes - off;
-      const int nvec = static_cast<int>(((rem < kChunkBytes ? rem : kChunkBytes) + 15) / 16);
+      const int rem = slice_bytes - d.chunk * kChunkBytes;
+      const int nvec = (min(max(rem, 0), kChunkBytes) + 15) / 16;
       uint4 raw[kVecsPerLane];
 #pragma unroll
       for (int j = 0; j < kVecsPerLane; ++j) {
@@ -782,7 +950,7 @@ struct Verifier {
       if (lane == 0) mbar_arrive(&C.empty[slot]);   // the slot is free again
 
       const int seg = d.chunk * kConsumerWarps + warp;
-      const int seg_base = seg * kSegElems;
+      const int seg_base = slice_lo + seg * kSegElems;
       if (timed_out) rBad |= 2;
       // the drafted token's logit
       if (d.x >= 0 && d.x < P.V && !P.greedy) {
@@ -876,35 +1044,17 @@ struct Verifier {
 
   // ======================= control warp ======================================
 
-  __device__ void push_request(const DrawReq& r) {
-    // the control warp (lane 0) produces, the producer warp consumes
-    unsigned long long t0 = 0;
-    while (C.req_tail - C.req_head >= kReqs) {
-      if (!t0) t0 = global_ns();
-      if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
-        atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-        C.rec[r.rec].err |= kErrTimeout;
-        return;
-      }
-    }
-    const int tail = C.req_tail;
-    C.req[tail % kReqs] = r;
-    C.ctl_req[C.pushed % kReqs] = r;
-    C.pushed = C.pushed + 1;
-    __threadfence_block();
-    C.req_tail = tail + 1;
-  }
-
-  // The segment holding s * S among `nseg` masses (index order).
-  __device__ void locate(const double* mass, int nseg, float s, double& Stot, int& seg, double& seg_t) const {
+  // The segment holding the target weight `tgt` among `nseg` masses (index
+  // order); seg_t is what is left of tgt at the segment's start.  Past the
+  // end (rounding) it is the last segment with positive mass.
+  template <typename T>
+  __device__ void locate(const T* mass, int nseg, double tgt, int& seg, double& seg_t) const {
     const int per = (nseg + 31) / 32;
     const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
     double gs = 0.0;
-    for (int i = g0; i < g1; ++i) gs += mass[i];
+    for (int i = g0; i < g1; ++i) gs += static_cast<double>(mass[i]);
     const double incl = warp_incl_scan(gs, lane);
     const double excl = incl - gs;
-    Stot = __shfl_sync(0xffffffffu, incl, 31);
-    const double tgt = static_cast<double>(s) * Stot;
     const unsigned hit = __ballot_sync(0xffffffffu, gs > 0.0 && tgt < incl);
     const unsigned posg = __ballot_sync(0xffffffffu, gs > 0.0);
     const int owner = hit ? (__ffs(hit) - 1) : (posg ? 31 - __clz(posg) : -1);
@@ -914,7 +1064,7 @@ struct Verifier {
       double run = excl, last_run = excl;
       int last = -1;
       for (int i = g0; i < g1; ++i) {
-        const double m = mass[i];
+        const double m = static_cast<double>(mass[i]);
         if (m > 0.0) { last = i; last_run = run; }
         if (seg < 0 && m > 0.0 && tgt < run + m) { seg = i; seg_t = tgt - run; }
         run += m;
@@ -925,6 +1075,21 @@ struct Verifier {
       seg = __shfl_sync(0xffffffffu, seg, owner);
       seg_t = __shfl_sync(0xffffffffu, seg_t, owner);
     }
+  }
+
+  // Which CTA's slice holds the target: each lane < cs holds slice weight w
+  // (the same values, in the same lanes, in every CTA, so every CTA agrees).
+  // Returns the rank (-1 if no slice has weight) and, in that lane's terms,
+  // what is left of the target at the slice's start.
+  __device__ int slice_owner(double w, double s, double& tot, double& t_loc) const {
+    const double incl = warp_incl_scan(w, lane);
+    tot = __shfl_sync(0xffffffffu, incl, 31);
+    const double tgt = s * tot;
+    const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0 && tgt < incl);
+    const unsigned any = __ballot_sync(0xffffffffu, w > 0.0);
+    const int owner = hit ? (__ffs(hit) - 1) : (any ? 31 - __clz(any) : -1);
+    t_loc = __shfl_sync(0xffffffffu, tgt - (incl - w), owner >= 0 ? owner : 0);
+    return owner;
   }
 
   // Walk NSTEPS x 32 vectors starting at vector v0, a warp inclusive scan
@@ -987,7 +1152,7 @@ struct Verifier {
     return found >= 0 ? found : last_positive;
   }
 
-  // Outputs of a sequence whose stream and draw are both done.
+  // Outputs of a settled sequence (written by one CTA of the cluster).
   __device__ void finish_sequence(int rec) {
     const SeqRec& R = C.rec[rec];
     const int k = P.k;
@@ -999,7 +1164,7 @@ struct Verifier {
     const bool ok = !err && y >= 0;
     for (int j = lane; j <= k; j += 32) {
       int v = -1;
-      if (ok) v = j < a ? __ldg(P.tokens + b * k + j) : (j == a ? y : -1);
+      if (ok) v = j < a ? R.tok[j] : (j == a ? y : -1);
       ot[j] = v;
     }
     if (lane == 0) {
@@ -1017,48 +1182,165 @@ struct Verifier {
         if (!bits) bits = kErrNonfinite;   // no token could be drawn
         atomicOr(P.ws.err_word, bits);
       }
-      __threadfence_block();
-      C.seqs_finished = C.seqs_finished + 1;
     }
     __syncwarp();
   }
 
-  // A finished row: combine the warps, decide, draw the bonus token.
-  // Returns false at the end of the work.
-  __device__ bool control_row(int buf) {
-    const float c2 = P.c2;
-    RowBuf& RB = C.rows[buf];
-    const Desc d = RB.d;
-    if (d.kind < 0) return false;
-    // combine the consumer warps, one lane per warp
+  // Hand a walk to the walker warp (lane 0 of the control warp).  Waits,
+  // bounded, while the ring is full: the walker always makes progress.
+  __device__ void push_walk(const WalkReq& r) {
+    if (lane == 0) {
+      const unsigned long long t0 = global_ns();
+      while (C.wreq_tail - C.wreq_head >= kWalkReqs) {
+        if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
+          atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+          break;
+        }
+        __nanosleep(64);
+      }
+      const int tail = C.wreq_tail;
+      C.wreq[tail % kWalkReqs] = r;
+      __threadfence_block();
+      C.wreq_tail = tail + 1;
+    }
+    __syncwarp();
+  }
+
+  // ======================= walker warp =======================================
+  // The only warp of the CTA that waits on logits read from global memory
+  // outside the staging ring: the walk inside the drawn segment, then the
+  // sequence's outputs.  Nothing waits for it but the reuse of a record.
+
+  __device__ void walker() {
+    int head = 0;
+    unsigned long long idle_since = 0;
+    while (true) {
+      int tail = 0, done = 0;
+      if (lane == 0) { done = C.ctl_done; tail = C.wreq_tail; }
+      tail = __shfl_sync(0xffffffffu, tail, 0);
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (head == tail) {
+        if (done) {
+          // the control warp has left: take what it pushed before leaving
+          if (lane == 0) tail = C.wreq_tail;
+          tail = __shfl_sync(0xffffffffu, tail, 0);
+          if (head == tail) return;
+        } else {
+          if (!idle_since) idle_since = global_ns();
+          if (static_cast<long long>(global_ns() - idle_since) > 8 * kDrainLimitNs) {
+            if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+            return;
+          }
+          __nanosleep(128);
+          continue;
+        }
+      }
+      idle_since = 0;
+      __threadfence_block();
+      const WalkReq r = C.wreq[head % kWalkReqs];
+      int y = -1;
+      if (r.v0 >= 0) {
+        if (r.mode == 0)
+          y = walk<kVecsPerLane, false>(r.v0, r.t, row_ptr(r.b, r.pos, 0), nullptr, r.K0, r.L0, 0.f, 0.f);
+        else if (r.mode == 1)
+          y = walk<kDrawVecsPerLane, true>(r.v0, r.t, row_ptr(r.b, r.pos, 0), row_ptr(r.b, r.pos, 1),
+                                           r.K0, r.L0, r.K1, r.L1);
+        else
+          y = walk<kDrawVecsPerLane, false>(r.v0, r.t, row_ptr(r.b, r.pos, 0), nullptr, r.K0, r.L0, 0.f, 0.f);
+      }
+      if (lane == 0) C.rec[r.rec].y = y;
+      __syncwarp();
+      finish_sequence(r.rec);
+      if (lane == 0) {
+        C.rec[r.rec].open = 0;
+        C.wreq_head = head + 1;
+      }
+      __syncwarp();
+      ++head;
+    }
+  }
+
+  // This CTA's part of a finished row: its consumer warps combined.  Each
+  // warp's K is fl(M_w c) of its own maximum, so the part's K is fl(M c).
+  __device__ void local_part(const RowBuf& RB, RowPart& out) const {
     const bool in = lane < kConsumerWarps;
-    float M = in ? RB.wM[lane] : -INFINITY;
-    int arg = in ? RB.wArg[lane] : 0x7fffffff;
-    warp_argmax(M, arg);
+    const float m = in ? RB.wM[lane] : -INFINITY;
+    const float M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(m)));
+    out.M = M;
+    out.arg = P.greedy ? __reduce_min_sync(0xffffffffu, (in && m == M) ? RB.wArg[lane] : 0x7fffffff) : 0;
+    out.bad = static_cast<int>(__reduce_or_sync(0xffffffffu, in ? static_cast<unsigned>(RB.wBad[lane]) : 0u));
+    const float K = M > -INFINITY ? __fmul_rn(M, P.c2) : -INFINITY;
+    out.K = K;
     const float wk = in ? RB.wK[lane] : -INFINITY;
-    const float K = warp_max(wk);
-    const int bad = warp_or(in ? RB.wBad[lane] : 0);
-    const float Ssum = warp_sum((in && wk > -INFINITY) ? RB.wS[lane] * fast_exp2(__fsub_rn(wk, K)) : 0.f);
+    float v = (!P.greedy && wk > -INFINITY) ? RB.wS[lane] * fast_exp2(__fsub_rn(wk, K)) : 0.f;
+#pragma unroll
+    for (int o = kConsumerWarps / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    out.S = v;
+    const int x = RB.d.x;
+    out.has_zx = (!P.greedy && x >= slice_lo && x < slice_lo + slice_n) ? 1 : 0;
+    out.zx = out.has_zx ? RB.zx : 0.f;
+    out.pad = 0;
+  }
+
+  __device__ void send_row_part(int xs, const RowPart& pt) const {
+    if (lane < cs) {
+      const uint32_t dst = peer(&C.xrow[xs][rank], lane);
+      const uint32_t bar = peer(&C.xrow_ready[xs], lane);
+      st_async(dst, make_uint4(__float_as_uint(pt.M), __float_as_uint(pt.K), __float_as_uint(pt.S),
+                               __float_as_uint(pt.zx)), bar);
+      st_async(dst + 16, make_uint4(static_cast<unsigned>(pt.arg), static_cast<unsigned>(pt.bad),
+                                    static_cast<unsigned>(pt.has_zx), 0u), bar);
+    }
+    __syncwarp();
+  }
+
+  // Every CTA's part of the row has arrived: combine, decide, and settle
+  // the sequence if this was its last row and no re-read follows.
+  __device__ void finish_row(int buf, int xs) {
+    const float c2 = P.c2;
+    const RowBuf& RB = C.rows[buf];
+    const Desc d = RB.d;
+    const bool in = lane < cs;
+    RowPart pt{};
+    if (in) pt = C.xrow[xs][lane];
+    const float pm = in ? pt.M : -INFINITY;
+    const float M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(pm)));
+    const int arg = P.greedy ? __reduce_min_sync(0xffffffffu, (in && pm == M) ? pt.arg : 0x7fffffff) : 0;
+    const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, in ? static_cast<unsigned>(pt.bad) : 0u));
+    const float pk = in ? pt.K : -INFINITY;
+    const float K = M > -INFINITY ? __fmul_rn(M, c2) : -INFINITY;   // = the largest part K
+    float sv = (!P.greedy && pk > -INFINITY) ? pt.S * fast_exp2(__fsub_rn(pk, K)) : 0.f;
+    for (int o = cs >> 1; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+    const float Ssum = __shfl_sync(0xffffffffu, sv, 0);
+    const unsigned hz = __ballot_sync(0xffffffffu, in && pt.has_zx);
+    const float zx = __shfl_sync(0xffffffffu, in ? pt.zx : 0.f, hz ? __ffs(hz) - 1 : 0);
+    // every part is in registers: arm the slot for its next row and let the
+    // senders reuse it
+    if (cs > 1) {
+      if (lane == 0) mbar_expect_tx(&C.xrow_ready[xs], static_cast<uint32_t>(cs * sizeof(RowPart)));
+      if (in) mbar_arrive_peer(peer(&C.xrow_free[xs], lane));
+    }
     const float L = log2f(Ssum);
     SeqRec& R = C.rec[d.rec];
     const size_t b = static_cast<size_t>(d.b);
-    int bonus = 0;
+    const bool diag = (rank == 0);
+    const bool last = (d.kind == 0 && d.pos == d.kb);
+    int bonus = 0, settle = 0;
     if (lane == 0) {
       if (d.pos == 0 && d.kind == 0) {
-        // first row of the sequence: open its record (free unless the ring of
-        // records has wrapped onto a sequence still waiting for its draw)
-        if (R.pending != 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+        // first row of the sequence: open its record
         R.b = d.b; R.kb = d.kb; R.a = -1; R.err = 0; R.y = -1; R.zero_resid = 0;
-        R.pending = 1; R.s = d.s;
+        R.open = 1; R.draw = 0; R.s = d.s;
       }
       if (bad & 2) R.err |= kErrTimeout;
+      if (d.pos < d.kb) R.tok[d.pos] = d.x;
       if (d.pos < d.kb && (d.x < 0 || d.x >= P.V)) R.err |= kErrBadToken;
       if (P.greedy) {
         if ((bad & 1) || !(M > -INFINITY)) R.err |= kErrNonfinite;
-        P.ws.m_t[b * (P.k + 1) + d.pos] = M;
+        if (diag) P.ws.m_t[b * (P.k + 1) + d.pos] = M;
         if (d.pos < d.kb) {
           const bool acc = (d.x == arg);
-          P.ws.alpha[b * P.k + d.pos] = acc ? 1.f : 0.f;
+          if (diag) P.ws.alpha[b * P.k + d.pos] = acc ? 1.f : 0.f;
           if (!acc && R.a < 0) { R.a = d.pos; R.y = arg; }
         } else if (R.a < 0) {
           R.y = arg;
@@ -1066,16 +1348,18 @@ struct Verifier {
       } else {
         if ((bad & 1) || !(isfinite(M) && isfinite(Ssum) && Ssum > 0.f)) R.err |= kErrNonfinite;
         if (d.kind == 0) {
-          P.ws.m_t[b * (P.k + 1) + d.pos] = M;
-          P.ws.L_t[b * (P.k + 1) + d.pos] = L;
-          C.pairK = K; C.pairL = L; C.pairZx = RB.zx;
-        } else {
+          if (diag) {
+            P.ws.m_t[b * (P.k + 1) + d.pos] = M;
+            P.ws.L_t[b * (P.k + 1) + d.pos] = L;
+          }
+          C.pairK = K; C.pairL = L; C.pairZx = zx;
+        } else if (diag) {
           P.ws.m_d[b * P.k + d.pos] = M;
           P.ws.L_d[b * P.k + d.pos] = L;
         }
         if (d.kind == 1 && !R.err) {
           // the pair is complete: acceptance test of draft d.pos
-          const float zt = C.pairZx, zd = RB.zx;
+          const float zt = C.pairZx, zd = zx;
           float alpha;
           if (zt == -INFINITY) alpha = 0.f;               // p(x) = 0
           else if (zd == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
@@ -1083,130 +1367,215 @@ struct Verifier {
             const float log2r = (fmaf(zt, c2, -C.pairK) - C.pairL) - (fmaf(zd, c2, -K) - L);
             alpha = log2r >= 0.f ? 1.f : exp2f(log2r);
           }
-          P.ws.alpha[b * P.k + d.pos] = alpha;
+          if (diag) P.ws.alpha[b * P.k + d.pos] = alpha;
           if (!(d.u < alpha) && R.a < 0) {
-            // first rejection: the producer re-reads this pair for the draw
+            // first rejection: the pair is read again for the residual draw
             R.a = d.pos;
-            R.pending += 1;
-            DrawReq rq;
-            rq.b = d.b; rq.pos = d.pos; rq.rec = d.rec; rq.mode = 1;
-            rq.Kt = C.pairK; rq.Lt = C.pairL; rq.Kd = K; rq.Ld = L;
-            push_request(rq);
+            R.Kt = C.pairK; R.Lt = C.pairL; R.Kd = K; R.Ld = L;
           }
-        } else if (d.kind == 0 && d.pos == d.kb && R.a < 0 && !R.err) {
+        } else if (last && R.a < 0 && !R.err) {
           bonus = 1;   // every draft accepted: the bonus draw
         }
       }
+      if (last) {
+        // the outcome is known: tell the producer whether a re-read follows
+        R.draw = (!P.greedy && R.a >= 0 && !R.err) ? 1 : 0;
+        __threadfence_block();
+        R.resolved = d.seq + 1;
+        settle = R.draw ? 0 : 1;
+      }
     }
     bonus = __shfl_sync(0xffffffffu, bonus, 0);
+    settle = __shfl_sync(0xffffffffu, settle, 0);
     __syncwarp();
+    int fin_rank = 0;
     if (bonus) {
-      // masses of the stream segments from the sums kept while streaming,
-      // then one segment of the bonus row is read again
-      const int nseg = nchunks * kConsumerWarps;
-      for (int sg = lane; sg < nseg; sg += 32) {
-        const float ks = RB.segK[sg];
-        C.bmass[sg] = ks == -INFINITY ? 0.0
-                      : static_cast<double>(RB.segS[sg]) * static_cast<double>(fast_exp2(__fsub_rn(ks, K) - L));
-      }
-      __syncwarp();
-      double S;
-      int seg;
-      double seg_t;
-      locate(C.bmass, nseg, R.s, S, seg, seg_t);
-      int y = -1;
-      if (seg >= 0)
-        y = walk<kVecsPerLane, false>(seg * kVecsPerWarp, seg_t, row_ptr(d.b, d.kb, 0), nullptr, K, L, 0.f, 0.f);
-      if (lane == 0) {
-        R.y = y;
-        P.ws.mass[b * (P.k + 1) + d.kb] = static_cast<float>(S);
+      // the slice holding s * S from every CTA's (K, S); inside it, the
+      // segment from the sums kept while streaming, then one segment of the
+      // bonus row is read again
+      const double w = (in && pk > -INFINITY)
+                           ? static_cast<double>(pt.S) * static_cast<double>(fast_exp2(__fsub_rn(pk, K) - L))
+                           : 0.0;
+      double tot, t_loc;
+      const int owner = slice_owner(w, static_cast<double>(d.s), tot, t_loc);
+      fin_rank = owner >= 0 ? owner : 0;
+      if (owner == rank) {
+        const int nseg = nchunks * kConsumerWarps;
+        for (int sg = lane; sg < nseg; sg += 32) {
+          const float ks = RB.segK[sg];
+          C.bmass[sg] = ks == -INFINITY ? 0.0
+                        : static_cast<double>(RB.segS[sg]) * static_cast<double>(fast_exp2(__fsub_rn(ks, K) - L));
+        }
+        __syncwarp();
+        int seg;
+        double seg_t;
+        locate(C.bmass, nseg, t_loc, seg, seg_t);
+        if (lane == 0) P.ws.mass[b * (P.k + 1) + d.kb] = static_cast<float>(tot);
+        WalkReq wr;
+        wr.rec = d.rec; wr.mode = 0; wr.v0 = seg >= 0 ? v_lo + seg * kVecsPerWarp : -1;
+        wr.b = d.b; wr.pos = d.kb; wr.pad = 0; wr.t = seg_t;
+        wr.K0 = K; wr.L0 = L; wr.K1 = 0.f; wr.L1 = 0.f;
+        push_walk(wr);       // the walker writes the outputs and frees the record
+        settle = 0;
       }
       __syncwarp();
     }
-    if (d.pos == d.kb && d.kind == 0) {
-      // the sequence's stream is done
-      int fin = 0;
-      if (lane == 0) fin = (--R.pending == 0) ? 1 : 0;
-      fin = __shfl_sync(0xffffffffu, fin, 0);
-      if (fin) finish_sequence(d.rec);
+    if (settle) {
+      if (rank == fin_rank) finish_sequence(d.rec);
+      if (lane == 0) R.open = 0;
+      __syncwarp();
     }
-    return true;
   }
 
-  // A re-read draw whose segment weights are complete.
-  __device__ void control_draw(int di) {
-    const int dp = di & 1;
-    const DrawReq r = C.ctl_req[di % kReqs];
-    SeqRec& R = C.rec[r.rec];
-    const int nseg = ndraw * kConsumerWarps;
-    const bool resid = (r.mode == 1);
-    double S;
-    int seg;
-    double seg_t;
-    locate(C.rmass[dp], nseg, R.s, S, seg, seg_t);
-    int fin = 0;
-    if (lane == 0 && C.draw_err[dp]) { R.err |= kErrTimeout; C.draw_err[dp] = 0; }
-    if (S > 0.0 || !resid) {
-      int y = -1;
-      if (seg >= 0) {
-        if (resid)
-          y = walk<kDrawVecsPerLane, true>(seg * kDrawVecsPerWarp, seg_t, row_ptr(r.b, r.pos, 0),
-                                           row_ptr(r.b, r.pos, 1), r.Kt, r.Lt, r.Kd, r.Ld);
-        else
-          y = walk<kDrawVecsPerLane, false>(seg * kDrawVecsPerWarp, seg_t, row_ptr(r.b, r.pos, 0),
-                                            nullptr, r.Kt, r.Lt, r.Kd, r.Ld);
-      }
-      if (lane == 0) {
-        R.y = y;
-        P.ws.mass[static_cast<size_t>(r.b) * (P.k + 1) + r.pos] = static_cast<float>(S);
-        fin = (--R.pending == 0) ? 1 : 0;
-      }
-    } else if (lane == 0) {
-      // exact arithmetic rules a zero residual out (a rejection implies
-      // p > q somewhere); draw from p_a instead and count it
-      R.zero_resid = 1;
-      DrawReq rq = r;
-      rq.mode = 2;
-      push_request(rq);
+  // Every CTA's masses of a re-read have arrived: the slice, then the
+  // segment, then the token; the CTA whose slice holds it settles the sequence.
+  __device__ void finish_draw(int dp, int xs) {
+    int rc = 0;
+    if (lane == 0) rc = C.draw_rec[dp];
+    rc = __shfl_sync(0xffffffffu, rc, 0);
+    SeqRec& R = C.rec[rc];
+    const bool in = lane < cs;
+    double r = 0.0, p = 0.0;
+    int err = 0;
+    if (in) {
+      const DrawPart& dpt = C.xdraw[xs][lane];
+      r = dpt.r; p = dpt.p; err = dpt.err;
     }
-    fin = __shfl_sync(0xffffffffu, fin, 0);
+    err = warp_or(err);
+    const double rtot = warp_sum(r);
+    if (lane == 0) mbar_expect_tx(&C.xdraw_ready[xs], static_cast<uint32_t>(cs * sizeof(DrawPart)));
+    if (in) mbar_arrive_peer(peer(&C.xdraw_free[xs], lane));
+    // exact arithmetic rules a zero residual out (a rejection implies p > q
+    // somewhere); if rounding leaves none, the draw is from p_a (counted)
+    const bool resid = rtot > 0.0;
+    double tot, t_loc;
+    const int owner = slice_owner(resid ? r : p, static_cast<double>(R.s), tot, t_loc);
+    const int fin_rank = owner >= 0 ? owner : 0;
+    if (lane == 0) {
+      if (err) R.err |= kErrTimeout;
+      R.zero_resid = resid ? 0 : 1;
+    }
     __syncwarp();
-    if (fin) finish_sequence(r.rec);
+    if (owner == rank) {
+      const int nseg = ndraw * kConsumerWarps;
+      int seg;
+      double seg_t;
+      locate(resid ? C.rmass[dp] : C.pmass[dp], nseg, t_loc, seg, seg_t);
+      if (lane == 0) P.ws.mass[static_cast<size_t>(R.b) * (P.k + 1) + R.a] = static_cast<float>(tot);
+      WalkReq wr;
+      wr.rec = rc; wr.mode = resid ? 1 : 2; wr.v0 = seg >= 0 ? v_lo + seg * kDrawVecsPerWarp : -1;
+      wr.b = R.b; wr.pos = R.a; wr.pad = 0; wr.t = seg_t;
+      wr.K0 = R.Kt; wr.L0 = R.Lt; wr.K1 = R.Kd; wr.L1 = R.Ld;
+      push_walk(wr);       // the walker writes the outputs and frees the record
+    } else {
+      if (rank == fin_rank) finish_sequence(rc);
+      if (lane == 0) R.open = 0;
+      __syncwarp();
+    }
   }
 
   __device__ void control() {
-    int ri = 0, di = 0;
+    control_loop();
+    __syncwarp();
+    if (lane == 0) { __threadfence_block(); C.ctl_done = 1; }
+  }
+
+  __device__ void control_loop() {
+    // rows: parts are sent as soon as a row is local, up to kXRing ahead of
+    // the oldest row whose exchange is not complete; rows finish in order
+    int rs = 0, rf = 0, end_row = -1;
+    int di = 0, dphase = 0;       // draws: 0 wait local, 1 send, 2 wait every part
+    double dR = 0.0, dP = 0.0;
+    int dErr = 0;
+    int end_draws = -1;           // re-reads in all, known at the end of the work
     unsigned long long idle_since = 0;
     while (true) {
       bool progressed = false;
-      const int buf = ri % kRowBufs;
-      int ready = 0;
-      if (lane == 0) ready = mbar_test_wait(&C.row_ready[buf], static_cast<uint32_t>(ri / kRowBufs) & 1u) ? 1 : 0;
-      ready = __shfl_sync(0xffffffffu, ready, 0);
-      if (ready) {
-        const bool more = control_row(buf);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&C.row_free[buf]);
-        ++ri;
-        if (!more) return;
+      while (end_row < 0 && rs - rf < kXRing) {
+        const int buf = rs % kRowBufs;
+        const int xs = rs % kXRing;
+        if (!probe(&C.row_ready[buf], static_cast<uint32_t>(rs / kRowBufs) & 1u)) break;
+        if (C.rows[buf].d.kind < 0) {
+          end_row = rs;
+          progressed = true;
+          break;
+        }
+        if (cs > 1 && !probe(&C.xrow_free[xs], (static_cast<uint32_t>(rs / kXRing) & 1u) ^ 1u)) break;
+        RowPart mine;
+        local_part(C.rows[buf], mine);
+        if (cs > 1) {
+          send_row_part(xs, mine);
+        } else {
+          // a cluster of one: the part is the row
+          if (lane == 0) C.xrow[xs][0] = mine;
+          __syncwarp();
+        }
+        ++rs;
         progressed = true;
       }
-      int pushed = 0;
-      if (lane == 0) pushed = C.pushed;
-      pushed = __shfl_sync(0xffffffffu, pushed, 0);
-      if (di < pushed) {
+      if (rf < rs) {
+        const int buf = rf % kRowBufs;
+        const int xs = rf % kXRing;
+        if (cs == 1 || probe(&C.xrow_ready[xs], static_cast<uint32_t>(rf / kXRing) & 1u)) {
+          // a sequence's first row waits until its record is free again
+          int free_rec = 1;
+          if (lane == 0) {
+            const Desc& d = C.rows[buf].d;
+            if (d.pos == 0 && d.kind == 0 && C.rec[d.rec].open) free_rec = 0;
+          }
+          free_rec = __shfl_sync(0xffffffffu, free_rec, 0);
+          if (free_rec) {
+            finish_row(buf, xs);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&C.row_free[buf]);
+            ++rf;
+            progressed = true;
+          }
+        }
+      }
+      if (end_row >= 0 && rf == end_row && end_draws < 0) end_draws = C.rows[end_row % kRowBufs].d.x;
+      {
         const int dp = di & 1;
-        int dready = 0;
-        if (lane == 0) dready = mbar_test_wait(&C.draw_ready[dp], static_cast<uint32_t>(di >> 1) & 1u) ? 1 : 0;
-        dready = __shfl_sync(0xffffffffu, dready, 0);
-        if (dready) {
-          control_draw(di);
+        const int xs = di % kXRing;
+        if (dphase == 0 && (end_draws < 0 || di < end_draws) &&
+            probe(&C.draw_ready[dp], static_cast<uint32_t>(di >> 1) & 1u)) {
+          const int nseg = ndraw * kConsumerWarps;
+          double r = 0.0, p = 0.0;
+          for (int sg = lane; sg < nseg; sg += 32) {
+            r += static_cast<double>(C.rmass[dp][sg]);
+            p += static_cast<double>(C.pmass[dp][sg]);
+          }
+          dR = warp_sum(r);
+          dP = warp_sum(p);
+          if (lane == 0) { dErr = C.draw_err[dp]; C.draw_err[dp] = 0; }
+          dErr = __shfl_sync(0xffffffffu, dErr, 0);
+          dphase = 1;
+          progressed = true;
+        }
+        if (dphase == 1 && probe(&C.xdraw_free[xs], (static_cast<uint32_t>(di / kXRing) & 1u) ^ 1u)) {
+          if (lane < cs) {
+            const uint32_t dst = peer(&C.xdraw[xs][rank], lane);
+            const uint32_t bar = peer(&C.xdraw_ready[xs], lane);
+            const unsigned long long rb = static_cast<unsigned long long>(__double_as_longlong(dR));
+            const unsigned long long pb = static_cast<unsigned long long>(__double_as_longlong(dP));
+            st_async(dst, make_uint4(static_cast<unsigned>(rb), static_cast<unsigned>(rb >> 32),
+                                     static_cast<unsigned>(pb), static_cast<unsigned>(pb >> 32)), bar);
+            st_async(dst + 16, make_uint4(static_cast<unsigned>(dErr), 0u, 0u, 0u), bar);
+          }
+          __syncwarp();
+          dphase = 2;
+          progressed = true;
+        }
+        if (dphase == 2 && probe(&C.xdraw_ready[xs], static_cast<uint32_t>(di / kXRing) & 1u)) {
+          finish_draw(dp, xs);
           __syncwarp();
           if (lane == 0) mbar_arrive(&C.draw_free[dp]);
           ++di;
+          dphase = 0;
           progressed = true;
         }
       }
+      if (end_draws >= 0 && di >= end_draws) return;
       if (progressed) {
         idle_since = 0;
       } else {
@@ -1215,7 +1584,10 @@ struct Verifier {
           if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
           return;
         }
-        __nanosleep(64);
+        // wait in hardware, briefly, for what the rows need next
+        if (end_row >= 0) __nanosleep(64);
+        else if (rf < rs && cs > 1) mbar_park(&C.xrow_ready[rf % kXRing], static_cast<uint32_t>(rf / kXRing) & 1u, 300u);
+        else mbar_park(&C.row_ready[rs % kRowBufs], static_cast<uint32_t>(rs / kRowBufs) & 1u, 300u);
       }
     }
   }
@@ -1228,6 +1600,7 @@ verify_kernel(const VerifyParams P) {
   Ctrl& C = *reinterpret_cast<Ctrl*>(smem);
   unsigned char* ring = smem + kCtrlBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cs = cluster_ctas();
   if (tid == 0) {
     for (int s = 0; s < P.stages; ++s) {
       mbar_init(&C.full[s], 1);
@@ -1240,21 +1613,39 @@ verify_kernel(const VerifyParams P) {
     for (int r = 0; r < 2; ++r) {
       mbar_init(&C.draw_ready[r], kConsumerWarps);
       mbar_init(&C.draw_free[r], 1);
+      mbar_init(&C.tk_full[r], 1);
+      mbar_init(&C.tk_empty[r], cs);
       C.draw_err[r] = 0;
     }
-    C.req_head = 0;
-    C.req_tail = 0;
-    C.pushed = 0;
-    C.seqs_finished = 0;
-    for (int r = 0; r < kRecs; ++r) C.rec[r].pending = 0;
+    // the data barriers complete on one local arrival (made when a slot is
+    // armed) plus the bytes of the asynchronous stores of every sender
+    for (int x = 0; x < kXRing; ++x) {
+      mbar_init(&C.xrow_ready[x], 1);
+      mbar_init(&C.xrow_free[x], cs);
+      mbar_init(&C.xdraw_ready[x], 1);
+      mbar_init(&C.xdraw_free[x], cs);
+    }
+    for (int r = 0; r < kRecs; ++r) { C.rec[r].open = 0; C.rec[r].resolved = 0; }
+    C.wreq_head = 0;
+    C.wreq_tail = 0;
+    C.ctl_done = 0;
     fence_mbar_init();
+    for (int r = 0; r < 2; ++r) mbar_expect_tx(&C.tk_full[r], 4u);
+    for (int x = 0; x < kXRing; ++x) {
+      mbar_expect_tx(&C.xrow_ready[x], static_cast<uint32_t>(cs * sizeof(RowPart)));
+      mbar_expect_tx(&C.xdraw_ready[x], static_cast<uint32_t>(cs * sizeof(DrawPart)));
+    }
   }
-  __syncthreads();
+  cluster_sync();                   // every CTA's barriers exist before anyone arrives on them
   grid_dependency_wait();           // the work list of plan_kernel is ready
-  Verifier<ELT> v(P, C, ring, lane, warp);
-  if (warp < kConsumerWarps) v.consume();
-  else if (warp == kConsumerWarps) v.produce();
-  else v.control();
+  {
+    Verifier<ELT> v(P, C, ring, lane, warp, cs, cluster_rank());
+    if (warp < kConsumerWarps) v.consume();
+    else if (warp == kConsumerWarps) v.produce();
+    else if (warp == kConsumerWarps + 1) v.control();
+    else v.walker();
+  }
+  cluster_sync();                   // nobody leaves while a peer may still reach its shared memory
 }
 
 // ---------------------------------------------------------------------------
@@ -1353,20 +1744,41 @@ cudaError_t query_ctas_per_sm(int smem_bytes, int* out) {
                                                        static_cast<size_t>(smem_bytes));
 }
 
-cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+namespace {
+void verify_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int cluster, int ctas,
+                   int smem_bytes, cudaStream_t s) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = s;
   cfg.attrs = attr;
+  cfg.numAttrs = 2;
+}
+}  // namespace
+
+cudaError_t query_max_clusters(int cluster, int smem_bytes, int* out) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  verify_config(cfg, attr, cluster, cluster, smem_bytes, nullptr);
   cfg.numAttrs = 1;
+  cfg.attrs = attr + 1;   // the cluster shape alone
+  return cudaOccupancyMaxActiveClusters(out, reinterpret_cast<const void*>(&verify_kernel<2>), &cfg);
+}
+
+cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  verify_config(cfg, attr, p.cluster, ctas, smem_bytes, s);
   if (p.elt == 2) return cudaLaunchKernelEx(&cfg, verify_kernel<2>, p);
   return cudaLaunchKernelEx(&cfg, verify_kernel<4>, p);
 }

@@ -50,15 +50,16 @@ struct DeviceSetup {
   bool ready = false;
   unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch
   int num_sms = 0;
-  int ctas = 0;                       // CTAs of the persistent grid
   int smem = 0;
+  int max_clusters[4] = {0, 0, 0, 0}; // clusters of 1, 2, 4, 8 CTAs that fit at once
 };
 
 std::mutex g_setup_mutex;
 DeviceSetup g_setup[kMaxDevices];
 
 // Once per device, with that device current: the array's device address and
-// the launch shape (three 64 KB staging slots, as many CTAs as fit).
+// the launch shape (three 64 KB staging slots, one CTA per SM, the cluster
+// size chosen per call as for a context).
 sv_status setup_device(int dev, DeviceSetup** out) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   DeviceSetup& s = g_setup[dev];
@@ -73,9 +74,19 @@ sv_status setup_device(int dev, DeviceSetup** out) {
     if (sv::prepare_verify_kernel(smem) != cudaSuccess) return SV_ERR_CUDA;
     int fit = 0;
     if (sv::query_ctas_per_sm(smem, &fit) != cudaSuccess || fit <= 0) return SV_ERR_UNSUPPORTED;
+    for (int i = 0; i < 4; ++i) {
+      const int c = 1 << i;
+      int n = 0;
+      if (sv::query_max_clusters(c, smem, &n) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+      const int cap = prop.multiProcessorCount * fit / c;
+      s.max_clusters[i] = n < cap ? n : cap;
+    }
+    if (s.max_clusters[0] <= 0) return SV_ERR_UNSUPPORTED;
     s.scratch = static_cast<unsigned char*>(ptr);
     s.num_sms = prop.multiProcessorCount;
-    s.ctas = prop.multiProcessorCount * fit;
     s.smem = smem;
     s.ready = true;
   }
@@ -154,6 +165,8 @@ extern "C" sv_status spec_verify_noalloc(int B, int k, int V, sv_dtype dtype,
   p.bulk = ((static_cast<long long>(V) * elt) % 16 == 0) && aligned;
   p.wait_limit_ns = sv::kDrainLimitNs;
   p.ws = ws;
-  const int ctas = B < setup->ctas ? B : setup->ctas;
+  p.cluster = sv::auto_cluster(B, static_cast<long long>(V) * elt, setup->num_sms, setup->max_clusters);
+  const int fit = setup->max_clusters[__builtin_ctz(static_cast<unsigned>(p.cluster))];
+  const int ctas = (B < fit ? B : fit) * p.cluster;
   return sv::launch_verify(p, ctas, setup->smem, s) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

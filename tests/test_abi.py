@@ -50,7 +50,9 @@ def test_null_context_is_rejected_on_the_host(lib):
     assert lib.spec_verify_reset_stats(P, P) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_set_pipeline(P, 4, 2) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_set_wait_limit_ns(P, 0) == svp.SV_ERR_INVALID_ARG
-    assert lib.sv_get_config(P, None, None, None, None, None) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_get_config(P, None, None, None, None, None, None) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_set_cluster(P, 2) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_launch_shape(P, 4, None, None) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_destroy(P) == svp.SV_OK
 
 

@@ -87,6 +87,44 @@ def test_every_pipeline_shape_gives_the_same_result(stages, ctas):
     np.testing.assert_array_equal(toks, toks2)
 
 
+# --- every cluster size: slices of 1/2, 1/4, 1/8 of each row per CTA -----------
+
+CLUSTER_CASES = [
+    ("ragged", dict(B=40, k=3, V=24576)),                          # bulk copies, one chunk per slice
+    ("tiny", dict(B=24, k=2, V=4099, T=1.3, ragged=True)),         # fp32 unaligned: plain loads per slice
+    ("tiny", dict(B=16, k=3, V=100)),                              # short rows: most slices empty
+    ("long_draft", dict(B=24, k=7, V=12288)),                      # low acceptance: many re-reads
+    ("qwen_b32", dict(B=8, k=3, V=151936)),                        # several chunks per slice
+    ("ragged", dict(B=32, k=3, V=24576, T=0.0)),                   # greedy
+]
+
+
+@pytest.mark.parametrize("cs", [1, 2, 4, 8])
+@pytest.mark.parametrize("name,over", CLUSTER_CASES, ids=[f"{n}-{o}" for n, o in CLUSTER_CASES])
+def test_every_cluster_size_matches_the_oracle(cs, name, over):
+    inp = small(name, **over)
+    ver = verifier_for(inp)
+    ver.set_cluster(cs)
+    assert ver.config()["cluster"] == cs
+    shape = ver.launch_shape(inp["meta"]["B"])
+    assert shape[0] == cs and shape[1] % cs == 0 and shape[1] <= cs * inp["meta"]["B"]
+    ver.reset_stats()
+    toks, lens, _, _ = assert_parity(inp, ver)
+    st, s = ver.stats()
+    assert st == svp.SV_OK and s["sequences"] == inp["meta"]["B"] and s["emitted"] == lens.sum()
+
+
+def test_cluster_setting_is_checked():
+    inp = small("ragged", B=8, k=3, V=4096)
+    ver = verifier_for(inp)
+    for bad in (3, 16, -1):
+        with pytest.raises(svp.SpecVerifyError):
+            ver.set_cluster(bad)
+    ver.set_cluster(0)
+    cs, ctas = ver.launch_shape(8)
+    assert cs in (1, 2, 4, 8) and ctas % cs == 0
+
+
 # --- exhaustive enumeration batch ----------------------------------------------
 
 @pytest.mark.parametrize("kb,T,seed", [(2, 1.0, 0), (1, 0.7, 1), (0, 1.6, 2)])
