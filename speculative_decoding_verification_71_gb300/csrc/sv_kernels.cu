@@ -247,11 +247,6 @@ template <> struct Vec<4> {
   }
 };
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -970,6 +965,10 @@ struct Verifier {
           }
         }
       }
+      // Each lane keeps its own running state over the row (rM, rArg / rK,
+      // rS relative to its own maximum); the warp combines once, at the row
+      // end, and per chunk only for the bonus row, whose per-segment sums the
+      // draw needs.
       if (P.greedy) {
         float lm = -INFINITY;
         int li = 0x7fffffff, bad = 0;
@@ -983,16 +982,14 @@ struct Verifier {
             if (z[e] > lm) { lm = z[e]; li = seg_base + (j * 32 + lane) * NV + e; }
           }
         }
-        warp_argmax(lm, li);
-        bad = warp_or(bad);
-        if (lm > rM) { rM = lm; rArg = li; }
+        if (lm > rM) { rM = lm; rArg = li; }   // chunks come in index order: ties keep the first
         rBad |= bad;
       } else {
-        const float wm = warp_max(V::vmax(raw));
-        float Ks = -INFINITY, ss = 0.f;
-        if (wm > -INFINITY) {
-          Ks = __fmul_rn(wm, c2);      // fl(m c), used identically wherever rescaled
-          const f2 cc = pack2(c2, c2), nk = pack2(-Ks, -Ks);
+        const float lm = V::vmax(raw);
+        float ks = -INFINITY, ls = 0.f;
+        if (lm > -INFINITY) {
+          ks = __fmul_rn(lm, c2);      // fl(m c), used identically wherever rescaled
+          const f2 cc = pack2(c2, c2), nk = pack2(-ks, -ks);
           f2 acc[NV / 2];
 #pragma unroll
           for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
@@ -1003,14 +1000,14 @@ struct Verifier {
 #pragma unroll
             for (int i = 0; i < NV / 2; ++i) acc[i] = add2(acc[i], exp2_2(fma2(z[i], cc, nk)));
           }
-          float a0, a1, sum = 0.f;
+          float a0, a1;
 #pragma unroll
-          for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); sum += a0 + a1; }
-          ss = warp_sum(sum);   // NaN logits make this NaN: caught at the row end
-          if (Ks > rK) { rS = rS * fast_exp2(__fsub_rn(rK, Ks)) + ss; rK = Ks; }
-          else         { rS += ss * fast_exp2(__fsub_rn(Ks, rK)); }
+          for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); ls += a0 + a1; }
+          // NaN logits make ls NaN: caught at the row end
+          if (ks > rK) { rS = rS * fast_exp2(__fsub_rn(rK, ks)) + ls; rK = ks; }
+          else         { rS += ls * fast_exp2(__fsub_rn(ks, rK)); }
         } else {
-          // no finite logit in the segment: only NaN can still hide here
+          // no finite logit in this lane's part: only NaN can still hide here
           int nan_seen = 0;
 #pragma unroll
           for (int j = 0; j < kVecsPerLane; ++j) {
@@ -1019,19 +1016,37 @@ struct Verifier {
 #pragma unroll
             for (int e = 0; e < NV; ++e) nan_seen |= (z[e] != z[e]);
           }
-          rBad |= warp_or(nan_seen);
+          rBad |= nan_seen;
         }
-        rM = fmaxf(rM, wm);
-        if (d.kind == 0 && d.pos == d.kb && lane == 0 && seg < kMaxChunks * kConsumerWarps) {
-          RB.segK[seg] = Ks;
-          RB.segS[seg] = ss;
+        rM = fmaxf(rM, lm);
+        if (d.kind == 0 && d.pos == d.kb && seg < kMaxChunks * kConsumerWarps) {
+          // bonus row: the segment's (fl(m c), sum) for the draw
+          const float wm = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(lm)));
+          const float Ks = wm > -INFINITY ? __fmul_rn(wm, c2) : -INFINITY;
+          const float ss = warp_sum(ks > -INFINITY ? ls * fast_exp2(__fsub_rn(ks, Ks)) : 0.f);
+          if (lane == 0) {
+            RB.segK[seg] = Ks;
+            RB.segS[seg] = ss;
+          }
         }
       }
 
       if (d.chunk == d.nchunks - 1) {
         // publish the row: this warp's state, the descriptor (warp 0)
+        float wM, wK = -INFINITY, wS = 0.f;
+        int wArg = 0x7fffffff;
+        if (P.greedy) {
+          wM = rM;
+          wArg = rArg;
+          warp_argmax(wM, wArg);
+        } else {
+          wM = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(rM)));
+          wK = wM > -INFINITY ? __fmul_rn(wM, c2) : -INFINITY;   // = the largest lane rK
+          wS = warp_sum(rK > -INFINITY ? rS * fast_exp2(__fsub_rn(rK, wK)) : 0.f);
+        }
+        const int wBad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(rBad)));
         if (lane == 0) {
-          RB.wK[warp] = rK; RB.wS[warp] = rS; RB.wM[warp] = rM; RB.wArg[warp] = rArg; RB.wBad[warp] = rBad;
+          RB.wK[warp] = wK; RB.wS[warp] = wS; RB.wM[warp] = wM; RB.wArg[warp] = wArg; RB.wBad[warp] = wBad;
           if (warp == 0) RB.d = d;
         }
         __syncwarp();
