@@ -98,6 +98,12 @@ __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint3
                :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy) : "memory");
 }
 
+__device__ __forceinline__ uint64_t evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
 // verify_kernel
 // ---------------------------------------------------------------------------
 
-template <int ELT>
+template <int ELT, bool GREEDY>
 struct Verifier {
   using V = Vec<ELT>;
   static constexpr int NV = V::N;                          // logits per vector
@@ -737,6 +743,7 @@ struct Verifier {
     const int k = P.k;
     const int n_seqs = __ldcg(P.ws.n_seqs);
     const uint64_t evict_first = evict_first_policy();
+    const uint64_t evict_last = evict_last_policy();
     int q = 0, tki = 0, streamed = 0, rows = 0, draws = 0, pend = 0;
     bool ok = true;
     // the next sequence's work-list entry, tokens and uniforms are fetched one
@@ -748,7 +755,7 @@ struct Verifier {
       if (tt < n_seqs) {
         s_ = __ldcg(P.ws.seqs + tt);
         x_ = lane < s_.y ? __ldg(P.tokens + static_cast<size_t>(s_.x) * k + lane) : -1;
-        u_ = (!P.greedy && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(s_.x) * (k + 1) + lane) : 0.f;
+        u_ = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(s_.x) * (k + 1) + lane) : 0.f;
       }
     };
     int t = take_ticket(tki, ok);
@@ -768,11 +775,11 @@ struct Verifier {
       float uj_next = 0.f;
       bool fetched = false;
       const float s_samp = __shfl_sync(0xffffffffu, uj, k);
-      const int nrows = P.greedy ? kb + 1 : 2 * kb + 1;
+      const int nrows = GREEDY ? kb + 1 : 2 * kb + 1;
       for (int r = 0; r < nrows && ok; ++r) {
         if (!(ok = insert_due(q, pend, streamed, rows, draws, false))) break;
         int pos, kind;
-        if (P.greedy) { pos = r; kind = 0; }
+        if (GREEDY) { pos = r; kind = 0; }
         else if (r < 2 * kb) { pos = r >> 1; kind = r & 1; }
         else { pos = kb; kind = 0; }
         const int x = __shfl_sync(0xffffffffu, xj, pos < kb ? pos : 0);
@@ -792,9 +799,10 @@ struct Verifier {
             d.u = u; d.s = s_samp;
             if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(bytes));
           }
-          // the bonus row is never read in full again: first out of L2
+          // the bonus row is never read in full again: first out of L2; a
+          // pair may be read again for its draw shortly after: last out
           fill(ring + static_cast<size_t>(slot) * kChunkBytes, src, off, bytes, &C.full[slot],
-               pos == kb, evict_first);
+               true, pos == kb ? evict_first : evict_last);
           if (!P.bulk) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&C.full[slot]);
@@ -948,7 +956,7 @@ struct Verifier {
       const int seg_base = slice_lo + seg * kSegElems;
       if (timed_out) rBad |= 2;
       // the drafted token's logit
-      if (d.x >= 0 && d.x < P.V && !P.greedy) {
+      if (d.x >= 0 && d.x < P.V && !GREEDY) {
         const int rel = d.x - seg_base;
         if (rel >= 0 && rel < kSegElems && ((rel / NV) & 31) == lane) {
           const int vv = rel / NV;
@@ -969,7 +977,7 @@ struct Verifier {
       // rS relative to its own maximum); the warp combines once, at the row
       // end, and per chunk only for the bonus row, whose per-segment sums the
       // draw needs.
-      if (P.greedy) {
+      if (GREEDY) {
         float lm = -INFINITY;
         int li = 0x7fffffff, bad = 0;
 #pragma unroll
@@ -1035,7 +1043,7 @@ struct Verifier {
         // publish the row: this warp's state, the descriptor (warp 0)
         float wM, wK = -INFINITY, wS = 0.f;
         int wArg = 0x7fffffff;
-        if (P.greedy) {
+        if (GREEDY) {
           wM = rM;
           wArg = rArg;
           warp_argmax(wM, wArg);
@@ -1282,17 +1290,17 @@ struct Verifier {
     const float m = in ? RB.wM[lane] : -INFINITY;
     const float M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(m)));
     out.M = M;
-    out.arg = P.greedy ? __reduce_min_sync(0xffffffffu, (in && m == M) ? RB.wArg[lane] : 0x7fffffff) : 0;
+    out.arg = GREEDY ? __reduce_min_sync(0xffffffffu, (in && m == M) ? RB.wArg[lane] : 0x7fffffff) : 0;
     out.bad = static_cast<int>(__reduce_or_sync(0xffffffffu, in ? static_cast<unsigned>(RB.wBad[lane]) : 0u));
     const float K = M > -INFINITY ? __fmul_rn(M, P.c2) : -INFINITY;
     out.K = K;
     const float wk = in ? RB.wK[lane] : -INFINITY;
-    float v = (!P.greedy && wk > -INFINITY) ? RB.wS[lane] * fast_exp2(__fsub_rn(wk, K)) : 0.f;
+    float v = (!GREEDY && wk > -INFINITY) ? RB.wS[lane] * fast_exp2(__fsub_rn(wk, K)) : 0.f;
 #pragma unroll
     for (int o = kConsumerWarps / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     out.S = v;
     const int x = RB.d.x;
-    out.has_zx = (!P.greedy && x >= slice_lo && x < slice_lo + slice_n) ? 1 : 0;
+    out.has_zx = (!GREEDY && x >= slice_lo && x < slice_lo + slice_n) ? 1 : 0;
     out.zx = out.has_zx ? RB.zx : 0.f;
     out.pad = 0;
   }
@@ -1320,11 +1328,11 @@ struct Verifier {
     if (in) pt = C.xrow[xs][lane];
     const float pm = in ? pt.M : -INFINITY;
     const float M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(pm)));
-    const int arg = P.greedy ? __reduce_min_sync(0xffffffffu, (in && pm == M) ? pt.arg : 0x7fffffff) : 0;
+    const int arg = GREEDY ? __reduce_min_sync(0xffffffffu, (in && pm == M) ? pt.arg : 0x7fffffff) : 0;
     const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, in ? static_cast<unsigned>(pt.bad) : 0u));
     const float pk = in ? pt.K : -INFINITY;
     const float K = M > -INFINITY ? __fmul_rn(M, c2) : -INFINITY;   // = the largest part K
-    float sv = (!P.greedy && pk > -INFINITY) ? pt.S * fast_exp2(__fsub_rn(pk, K)) : 0.f;
+    float sv = (!GREEDY && pk > -INFINITY) ? pt.S * fast_exp2(__fsub_rn(pk, K)) : 0.f;
     for (int o = cs >> 1; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
     const float Ssum = __shfl_sync(0xffffffffu, sv, 0);
     const unsigned hz = __ballot_sync(0xffffffffu, in && pt.has_zx);
@@ -1350,7 +1358,7 @@ struct Verifier {
       if (bad & 2) R.err |= kErrTimeout;
       if (d.pos < d.kb) R.tok[d.pos] = d.x;
       if (d.pos < d.kb && (d.x < 0 || d.x >= P.V)) R.err |= kErrBadToken;
-      if (P.greedy) {
+      if (GREEDY) {
         if ((bad & 1) || !(M > -INFINITY)) R.err |= kErrNonfinite;
         if (diag) P.ws.m_t[b * (P.k + 1) + d.pos] = M;
         if (d.pos < d.kb) {
@@ -1394,7 +1402,7 @@ struct Verifier {
       }
       if (last) {
         // the outcome is known: tell the producer whether a re-read follows
-        R.draw = (!P.greedy && R.a >= 0 && !R.err) ? 1 : 0;
+        R.draw = (!GREEDY && R.a >= 0 && !R.err) ? 1 : 0;
         __threadfence_block();
         R.resolved = d.seq + 1;
         settle = R.draw ? 0 : 1;
@@ -1608,7 +1616,7 @@ struct Verifier {
   }
 };
 
-template <int ELT>
+template <int ELT, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_kernel(const VerifyParams P) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -1654,7 +1662,7 @@ verify_kernel(const VerifyParams P) {
   cluster_sync();                   // every CTA's barriers exist before anyone arrives on them
   grid_dependency_wait();           // the work list of plan_kernel is ready
   {
-    Verifier<ELT> v(P, C, ring, lane, warp, cs, cluster_rank());
+    Verifier<ELT, GREEDY> v(P, C, ring, lane, warp, cs, cluster_rank());
     if (warp < kConsumerWarps) v.consume();
     else if (warp == kConsumerWarps) v.produce();
     else if (warp == kConsumerWarps + 1) v.control();
@@ -1745,8 +1753,10 @@ __global__ void init_workspace_kernel(Workspace ws) {
 int verify_smem_bytes(int stages) { return kCtrlBytes + stages * kChunkBytes; }
 
 cudaError_t prepare_verify_kernel(int smem_bytes) {
-  const void* fns[2] = {reinterpret_cast<const void*>(&verify_kernel<2>),
-                        reinterpret_cast<const void*>(&verify_kernel<4>)};
+  const void* fns[4] = {reinterpret_cast<const void*>(&verify_kernel<2, false>),
+                        reinterpret_cast<const void*>(&verify_kernel<4, false>),
+                        reinterpret_cast<const void*>(&verify_kernel<2, true>),
+                        reinterpret_cast<const void*>(&verify_kernel<4, true>)};
   for (const void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
@@ -1755,7 +1765,7 @@ cudaError_t prepare_verify_kernel(int smem_bytes) {
 }
 
 cudaError_t query_ctas_per_sm(int smem_bytes, int* out) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, verify_kernel<2>, kThreads,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, verify_kernel<2, false>, kThreads,
                                                        static_cast<size_t>(smem_bytes));
 }
 
@@ -1784,7 +1794,7 @@ cudaError_t query_max_clusters(int cluster, int smem_bytes, int* out) {
   verify_config(cfg, attr, cluster, cluster, smem_bytes, nullptr);
   cfg.numAttrs = 1;
   cfg.attrs = attr + 1;   // the cluster shape alone
-  return cudaOccupancyMaxActiveClusters(out, reinterpret_cast<const void*>(&verify_kernel<2>), &cfg);
+  return cudaOccupancyMaxActiveClusters(out, reinterpret_cast<const void*>(&verify_kernel<2, false>), &cfg);
 }
 
 cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s) {
@@ -1794,8 +1804,12 @@ cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaS
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
   verify_config(cfg, attr, p.cluster, ctas, smem_bytes, s);
-  if (p.elt == 2) return cudaLaunchKernelEx(&cfg, verify_kernel<2>, p);
-  return cudaLaunchKernelEx(&cfg, verify_kernel<4>, p);
+  if (p.greedy) {
+    if (p.elt == 2) return cudaLaunchKernelEx(&cfg, verify_kernel<2, true>, p);
+    return cudaLaunchKernelEx(&cfg, verify_kernel<4, true>, p);
+  }
+  if (p.elt == 2) return cudaLaunchKernelEx(&cfg, verify_kernel<2, false>, p);
+  return cudaLaunchKernelEx(&cfg, verify_kernel<4, false>, p);
 }
 
 cudaError_t launch_compact(int B, int k, const int* out_tokens, const int* out_len,
