@@ -487,6 +487,8 @@ static_assert(kCtrlBytes + 3 * kChunkBytes <= 227 * 1024, "three staging slots m
 // ---------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
 
+constexpr int kPlanCached = 8;   // k_b values a thread keeps in registers (B <= 8192)
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P) {
   grid_dependents_launch();   // the verify grid may start its prologue now
   __shared__ int warp_cnt[32];
@@ -494,8 +496,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = P.B, k = P.k;
   const Workspace& ws = P.ws;
+  // one read of the lengths; invalid ones are answered here
+  int kbc[kPlanCached];
+#pragma unroll
+  for (int c = 0; c < kPlanCached; ++c) {
+    const int b = c * kPlanThreads + tid;
+    kbc[c] = b < B ? __ldg(P.draft_len + b) : -1;
+  }
   for (int b = tid; b < B; b += kPlanThreads) {
-    const int kb = P.draft_len[b];
+    const int kb = b < kPlanCached * kPlanThreads ? kbc[b / kPlanThreads] : P.draft_len[b];
     if (kb < 0 || kb > k) {
       int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
       for (int j = 0; j <= k; ++j) ot[j] = -1;
@@ -514,22 +523,31 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
   __syncthreads();
   // counting sort by k_b, largest first, stable in b
   for (int L = k; L >= 0; --L) {
-    for (int b0 = 0; b0 < B; b0 += kPlanThreads) {
+    for (int b0 = 0, c = 0; b0 < B; b0 += kPlanThreads, ++c) {
       const int b = b0 + tid;
-      const int kb = b < B ? P.draft_len[b] : -1;
+      int kb = -1;
+      if (b < B) {
+        if (c < kPlanCached) {
+#pragma unroll
+          for (int cc = 0; cc < kPlanCached; ++cc)
+            if (cc == c) kb = kbc[cc];
+        } else {
+          kb = P.draft_len[b];
+        }
+      }
       const bool take = (kb == L);
       const unsigned m = __ballot_sync(0xffffffffu, take);
       if (lane == 0) warp_cnt[warp] = __popc(m);
       __syncthreads();
       if (warp == 0) {
-        const int c = warp_cnt[lane];
-        int incl = c;
+        const int cnt = warp_cnt[lane];
+        int incl = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int up = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += up;
         }
-        warp_cnt[lane] = incl - c;
+        warp_cnt[lane] = incl - cnt;
       }
       __syncthreads();
       if (take) ws.seqs[base + warp_cnt[warp] + __popc(m & ((1u << lane) - 1u))] = make_int2(b, kb);
