@@ -54,6 +54,8 @@ def _bind(lib):
     lib.oracle_logit_value.restype = c.c_double
     lib.oracle_logit_value.argtypes = [P, c.c_int, c.c_longlong]
     lib.oracle_num_threads.restype = c.c_int
+    lib.oracle_kd.restype = c.c_int
+    lib.oracle_kd.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, c.c_double, P, P, P, P, c.c_int]
     return lib
 
 
@@ -158,3 +160,29 @@ def logit_values(arr, lib=None):
 
 def num_threads(lib=None):
     return (lib or load()).oracle_num_threads()
+
+
+def kd(target, draft, weights, T=1.0, grad=True, nthreads=0, lib=None):
+    """Reward-weighted distillation loss of the draft (see ``oracle_kd`` in
+    oracle.c).  target, draft: [n_seq, t_len, V] fp32 or bf16; weights:
+    [n_seq] (w(r) per rollout).  Returns row_kl [n_seq, t_len], loss [n_seq],
+    grad [n_seq, t_len, V] (float64, or None) and status [n_seq, t_len]."""
+    lib = lib or load()
+    t, dt = _as_np(target)
+    d, dd = _as_np(draft)
+    if dt is None or dd != dt:
+        raise TypeError("target and draft must both be float32 or both bfloat16")
+    n_seq, t_len, V = t.shape
+    t = np.ascontiguousarray(t)
+    d = np.ascontiguousarray(d)
+    w = np.ascontiguousarray(np.asarray(weights, dtype=np.float64).reshape(n_seq))
+    row_kl = np.empty((n_seq, t_len), np.float64)
+    loss = np.empty(n_seq, np.float64)
+    g = np.empty((n_seq, t_len, V), np.float64) if grad else None
+    status = np.empty((n_seq, t_len), np.int32)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+    rc = lib.oracle_kd(n_seq, t_len, V, dt, ptr(t), ptr(d), ptr(w), float(T), ptr(row_kl), ptr(loss),
+                       ptr(g), ptr(status), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_kd failed ({rc})")
+    return {"row_kl": row_kl, "loss": loss, "grad": g, "status": status}

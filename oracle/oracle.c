@@ -360,3 +360,87 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/*
+ * Reward-weighted distillation loss of the draft model ("ReSpec: Towards
+ * Optimizing Speculative Decoding in Reinforcement Learning Systems", Online
+ * Learner, reward-weighted KD): each rollout b of t_len positions adds
+ *   L_b = w_b * sum_t KL(pt_{b,t} || q_{b,t}),
+ *   pt = softmax(z^t / T) (the updated target), q = softmax(z^d / T) (draft),
+ *   KL(p || q) = sum_x p(x) (log p(x) - log q(x)),
+ * where a term with p(x) = 0 is 0 and p(x) > 0 with q(x) = 0 makes KL = +inf.
+ * The gradient with respect to the draft logits is
+ *   dL_b / dz^d_{b,t}(x) = w_b (q(x) - pt(x)) / T.
+ * w_b = w(r_b) is an input per rollout: the page weights the KL by a function
+ * of the reward without fixing it.
+ *
+ * Per row, all in double: the row maximum and L of row_stats, then every
+ * log-probability from them.  A row pair with NaN or +inf, or a row that is
+ * all -inf, has status 4: its KL and gradient are NaN and so is its loss.
+ * The loss sums the rows of a rollout in position order.
+ * row_kl [n_seq * t_len], loss [n_seq], grad [n_seq * t_len * V] (may be
+ * NULL), status [n_seq * t_len] (may be NULL).
+ */
+int oracle_kd(int n_seq, int t_len, int V, int dtype, const void *target, const void *draft,
+              const double *weights, double T, double *row_kl, double *loss, double *grad,
+              int *status, int nthreads)
+{
+    if (n_seq <= 0 || t_len <= 0 || V <= 0 || !(T > 0.0))
+        return -1;
+    const long long rows = (long long)n_seq * t_len;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#endif
+    int bad_alloc = 0;
+#pragma omp parallel reduction(| : bad_alloc)
+    {
+        double *zt = (double *)malloc(sizeof(double) * (size_t)V);
+        double *zd = (double *)malloc(sizeof(double) * (size_t)V);
+        if (!zt || !zd) {
+            bad_alloc = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long long r = 0; r < rows; ++r) {
+                const double w = weights[r / t_len];
+                load_row(target, dtype, (size_t)r, V, zt);
+                load_row(draft, dtype, (size_t)r, V, zd);
+                int st = (row_is_valid(zt, V) && row_is_valid(zd, V)) ? ORC_OK : ORC_NONFINITE;
+                if (status)
+                    status[r] = st;
+                if (st != ORC_OK) {
+                    row_kl[r] = NAN;
+                    if (grad)
+                        for (int x = 0; x < V; ++x)
+                            grad[(size_t)r * V + x] = NAN;
+                    continue;
+                }
+                double mt, Lt, md, Ld;
+                row_stats(zt, V, T, &mt, &Lt);
+                row_stats(zd, V, T, &md, &Ld);
+                double kl = 0.0;
+                for (int x = 0; x < V; ++x) {
+                    const double lp = (zt[x] - mt) / T - Lt;      /* log p(x) */
+                    const double lq = (zd[x] - md) / T - Ld;      /* log q(x) */
+                    const double p = exp(lp), q = exp(lq);
+                    if (p > 0.0)
+                        kl += p * (lp - lq);                     /* +inf when q(x) = 0 */
+                    if (grad)
+                        grad[(size_t)r * V + x] = w * (q - p) / T;
+                }
+                row_kl[r] = kl;
+            }
+        }
+        free(zt);
+        free(zd);
+    }
+    if (bad_alloc)
+        return -2;
+    for (int b = 0; b < n_seq; ++b) {
+        double s = 0.0;
+        for (int t = 0; t < t_len; ++t)
+            s += row_kl[(size_t)b * t_len + t];
+        loss[b] = weights[b] * s;
+    }
+    return 0;
+}
