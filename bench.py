@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--cluster", type=int, default=0, help="CTAs per sequence (1, 2, 4, 8; 0 = automatic)")
     ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
+    ap.add_argument("--kd-steps", type=int, default=100, help="timed calls of the distillation loss (0 = skip)")
+    ap.add_argument("--kd-only", action="store_true", help="time only the distillation loss and print its line")
+    ap.add_argument("--kd-rollouts", type=int, default=64, help="rollouts of the distillation batch")
     return ap.parse_args()
 
 
@@ -327,6 +330,55 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
             "soak_steps": soak, "cfg": cfg, "ver": ver, "base_inputs": base, "launch": launch}
 
 
+def time_kd(svp, device, stream, steps, warmup, n_seq=64, t_len=64, V=151936):
+    """Device-timed calls of the reward-weighted distillation loss on a batch
+    of rollouts (bf16, Qwen vocabulary): with the gradient and loss alone.
+    Two input copies rotate (each larger than L2); outputs are preallocated
+    and the calls go straight through the C ABI."""
+    import torch
+
+    lib = svp.load_library()
+    g = torch.Generator(device=device).manual_seed(11)
+    sets = []
+    for _ in range(2):
+        t = torch.randn(n_seq, t_len, V, generator=g, device=device) * 3.0
+        d = (t + torch.randn(n_seq, t_len, V, generator=g, device=device) * 0.7).to(torch.bfloat16)
+        sets.append((t.to(torch.bfloat16), d, torch.rand(n_seq, generator=g, device=device)))
+        del t
+    row_kl = torch.empty(n_seq, t_len, dtype=torch.float32, device=device)
+    loss = torch.empty(n_seq, dtype=torch.float32, device=device)
+    grad = torch.empty(n_seq, t_len, V, dtype=torch.bfloat16, device=device)
+    h = svp._stream_handle(stream)
+    rows = n_seq * t_len
+    out = {"workload": f"kd: {n_seq} rollouts x {t_len} positions, V={V} bf16, T=1",
+           "kernel": "kd_kernel", "rows_per_call": rows}
+    cs, nb, ctas = svp.kd_launch_shape(V, torch.bfloat16, True)
+    out["launch"] = {"cluster": cs, "row_buffers": nb, "grid_ctas": ctas}
+    for name, gp in (("with_grad", grad.data_ptr()), ("loss_only", None)):
+        def call(i):
+            t, d, w = sets[i % 2]
+            st = lib.spec_kd_loss(n_seq, t_len, V, svp.SV_BF16, t.data_ptr(), d.data_ptr(), w.data_ptr(), 1.0,
+                                  row_kl.data_ptr(), loss.data_ptr(), gp, h)
+            if st != svp.SV_OK:
+                raise RuntimeError(f"spec_kd_loss failed: {st}")
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                call(i)
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                call(i)
+            e1.record(stream)
+            stream.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        nbytes = 2 * rows * V * 2 + (rows * V * 2 if gp else 0) + rows * 4 + n_seq * 8
+        out[name] = {"ms_per_call": ms, "rows_per_s": rows / (ms / 1e3), "algorithmic_bytes": nbytes,
+                     "gbs": nbytes / (ms / 1e3) / 1e9, "frac_of_measured_peak": nbytes / (ms / 1e3) / 1e9 / measured_peak()[0]}
+    del sets, grad
+    return out
+
+
 def e2e_measure(svp, w, args, device, stream, ver, base):
     """End to end through the public binding with host buffers: per step the
     pinned-host inputs are copied to the device, verified, and the outputs
@@ -420,6 +472,8 @@ def our_arm(args, w):
                      "algorithmic_bytes": am["bytes"], "mean_emitted": am["stats"]["mean_emitted"],
                      "cluster": am["cfg"]["cluster"], "grid_ctas": am["cfg"]["grid_ctas"]}
         del am
+    if args.kd_steps > 0 and world == 1:
+        aux["kd_loss"] = time_kd(svp, device, stream, args.kd_steps, max(3, args.warmup // 10), n_seq=args.kd_rollouts)
 
     if rank != 0:
         if pg:
@@ -463,11 +517,29 @@ def our_arm(args, w):
         pg.destroy_process_group()
 
 
+def kd_only(args):
+    """The distillation loss alone (for profiling it): one JSON line."""
+    import torch
+
+    import speculative_decoding_verification_71_gb300 as svp
+    from speculative_decoding_verification_71_gb300 import build as svbuild
+
+    svbuild.build()
+    svp.load_library()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream()
+    out = time_kd(svp, device, stream, max(1, args.kd_steps), max(1, args.warmup), n_seq=args.kd_rollouts)
+    print(json.dumps({"kd_loss": out}), flush=True)
+
+
 def main():
     args = parse()
     from workloads import get_workload
     w = get_workload(args.workload)
-    if args.impl == "reference":
+    if args.kd_only:
+        kd_only(args)
+    elif args.impl == "reference":
         reference_arm(args, w)
     else:
         our_arm(args, w)

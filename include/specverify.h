@@ -196,6 +196,41 @@ sv_status sv_get_config(const sv_ctx *ctx, int *stages, int *ctas_per_sm, int *t
                         int *smem_bytes, int *grid_ctas, int *cluster);
 sv_status sv_launch_shape(const sv_ctx *ctx, int B, int *cluster, int *grid_ctas);
 
+/* Reward-weighted distillation loss of the draft model and its gradient in
+ * the draft logits ("ReSpec: Towards Optimizing Speculative Decoding in
+ * Reinforcement Learning Systems", Online Learner, reward-weighted KD):
+ *   L_b = w_b * sum_t KL(p_{b,t} || q_{b,t}),
+ *   p = softmax(z^t / T) (the updated target), q = softmax(z^d / T) (draft),
+ *   grad_{b,t}(x) = dL_b / dz^d_{b,t}(x) = w_b (q(x) - p(x)) / T.
+ * The page weights the KL by a function of the rollout's reward without
+ * fixing it: w_b = w(r_b) is computed by the caller.
+ *   target_logits, draft_logits  [n_seq, t_len, V] dtype, device, contiguous
+ *   weights                      [n_seq] fp32 device
+ *   temperature                  > 0 (else SV_ERR_INVALID_ARG)
+ *   row_kl                       [n_seq, t_len] fp32 device, out
+ *   loss                         [n_seq] fp32 device, out
+ *   grad                         [n_seq, t_len, V] dtype device, out (bf16:
+ *                                rounded to nearest even), or NULL for the
+ *                                loss alone (one read of the logits)
+ * A row pair holding NaN or +inf, or a row that is all -inf, gives a NaN
+ * KL, NaN gradient and NaN loss for its rollout; a masked draft logit (-inf)
+ * where the target has mass gives KL = +inf.  Asynchronous on `stream`; no
+ * context and no allocation per call (the first call on a device allocates
+ * one word).  Deterministic: every sum is taken in a fixed order.  Rows whose
+ * V * sizeof(dtype) is a multiple of 16 with 16-byte aligned bases are staged
+ * with bulk copies, others with plain loads.  Vocabularies up to 8 * 27 KB
+ * of logits per row use two row buffers per CTA, larger ones one;
+ * SV_ERR_UNSUPPORTED if a row does not fit a cluster of 8 CTAs. */
+sv_status spec_kd_loss(int n_seq, int t_len, int V, sv_dtype dtype, const void *target_logits,
+                       const void *draft_logits, const float *weights, float temperature,
+                       float *row_kl, float *loss, void *grad, sv_stream_t stream);
+
+/* The launch shape spec_kd_loss uses for rows of V logits of `dtype` (with or
+ * without the gradient): CTAs per cluster, row buffers per CTA, and the most
+ * CTAs of the persistent grid.  Any output pointer may be NULL. */
+sv_status spec_kd_launch_shape(int V, sv_dtype dtype, int with_grad, int *cluster, int *buffers,
+                               int *grid_ctas);
+
 /* Test hook: the limit, in nanoseconds, of each bounded wait for staged logits
  * (default 1 s).  0 makes every wait report expiry, so every sequence that
  * reads a row ends with SV_ERR_TIMEOUT; the copies are still drained (with a

@@ -39,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
     "sv_set_pipeline", "sv_set_cluster", "sv_get_config", "sv_launch_shape", "sv_set_wait_limit_ns",
-    "spec_verify_noalloc",
+    "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
 )
 
 
@@ -103,6 +103,11 @@ def load_library(path: str | None = None):
     lib.sv_set_cluster.argtypes = [P, c.c_int]
     lib.sv_get_config.restype = c.c_int
     lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 6
+    lib.spec_kd_loss.restype = c.c_int
+    lib.spec_kd_loss.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, c.c_float, P, P, P, P]
+    lib.spec_kd_launch_shape.restype = c.c_int
+    lib.spec_kd_launch_shape.argtypes = [c.c_int, c.c_int, c.c_int, c.POINTER(c.c_int), c.POINTER(c.c_int),
+                                         c.POINTER(c.c_int)]
     lib.sv_launch_shape.restype = c.c_int
     lib.sv_launch_shape.argtypes = [P, c.c_int, c.POINTER(c.c_int), c.POINTER(c.c_int)]
     lib.sv_set_wait_limit_ns.restype = c.c_int
@@ -328,3 +333,43 @@ def spec_verify_noalloc(target, draft, tokens, draft_len, uniforms, temperature,
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_noalloc")
     return out_tokens, out_len
+
+
+def kd_loss(target, draft, weights, temperature=1.0, grad=True, stream=None):
+    """Reward-weighted distillation loss of the draft and its gradient in the
+    draft logits (see ``spec_kd_loss`` in include/specverify.h).  target,
+    draft: [n_seq, t_len, V] float32 or bfloat16 on the GPU; weights: [n_seq]
+    float32 (w(r) per rollout).  Returns (row_kl [n_seq, t_len] float32,
+    loss [n_seq] float32, grad [n_seq, t_len, V] in the logits' dtype or
+    None)."""
+    lib = load_library()
+    n_seq, t_len, V = target.shape
+    dtype = target.dtype
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    dev = target.device
+    _check_dev("target", target, dtype, (n_seq, t_len, V), dev)
+    _check_dev("draft", draft, dtype, (n_seq, t_len, V), dev)
+    _check_dev("weights", weights, torch.float32, (n_seq,), dev)
+    row_kl = torch.empty((n_seq, t_len), dtype=torch.float32, device=dev)
+    loss = torch.empty((n_seq,), dtype=torch.float32, device=dev)
+    g = torch.empty((n_seq, t_len, V), dtype=dtype, device=dev) if grad else None
+    st = lib.spec_kd_loss(n_seq, t_len, V, SV_BF16 if dtype == torch.bfloat16 else SV_F32,
+                          target.data_ptr(), draft.data_ptr(), weights.data_ptr(), float(temperature),
+                          row_kl.data_ptr(), loss.data_ptr(), g.data_ptr() if g is not None else None,
+                          _stream_handle(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_kd_loss")
+    return row_kl, loss, g
+
+
+def kd_launch_shape(V, dtype=torch.bfloat16, grad=True):
+    """(CTAs per cluster, row buffers per CTA, grid CTAs) of ``kd_loss`` for
+    rows of V logits."""
+    lib = load_library()
+    cs, nb, ctas = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    st = lib.spec_kd_launch_shape(int(V), SV_BF16 if dtype == torch.bfloat16 else SV_F32, int(bool(grad)),
+                                  ctypes.byref(cs), ctypes.byref(nb), ctypes.byref(ctas))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_kd_launch_shape")
+    return cs.value, nb.value, ctas.value

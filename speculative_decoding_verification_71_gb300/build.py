@@ -1,6 +1,6 @@
 """Build ``libspecverify.so`` in-tree with nvcc for sm_103a.
 
-The two translation units are compiled in parallel and linked with the
+The translation units are compiled in parallel and linked with the
 static CUDA runtime, so the library needs nothing on the loader path.
 """
 from __future__ import annotations
@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libspecverify.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu"]
+SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_kd.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "-I", INCLUDE]
 
@@ -28,7 +28,8 @@ def _nvcc():
 
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "sv_internal.h"), os.path.join(INCLUDE, "specverify.h"), __file__]
+    files += [os.path.join(CSRC, "sv_internal.h"), os.path.join(CSRC, "sv_device.cuh"),
+              os.path.join(INCLUDE, "specverify.h"), __file__]
     return files
 
 

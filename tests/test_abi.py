@@ -21,7 +21,7 @@ def lib():
 
 def declared_functions():
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    return sorted(set(re.findall(r"\b((?:sv|spec_verify)\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:sv|spec_verify|spec_kd)\w*)\s*\(", text)))
 
 
 def test_header_declares_the_binding_symbols():
@@ -53,6 +53,12 @@ def test_null_context_is_rejected_on_the_host(lib):
     assert lib.sv_get_config(P, None, None, None, None, None, None) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_set_cluster(P, 2) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_launch_shape(P, 4, None, None) == svp.SV_ERR_INVALID_ARG
+    # the distillation loss checks its sizes, temperature and pointers on the host
+    assert lib.spec_kd_loss(0, 1, 10, 1, P, P, P, 1.0, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_kd_loss(1, 1, 10, 1, P, P, P, 1.0, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_kd_loss(1, 1, 10, 5, P, P, P, 1.0, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    one = ctypes.c_void_p(16)
+    assert lib.spec_kd_loss(1, 1, 10, 1, one, one, one, 0.0, one, one, None, P) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_destroy(P) == svp.SV_OK
 
 
