@@ -61,6 +61,10 @@ def parse():
     ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
     ap.add_argument("--kd-steps", type=int, default=100, help="timed calls of the distillation loss (0 = skip)")
     ap.add_argument("--kd-only", action="store_true", help="time only the distillation loss and print its line")
+    ap.add_argument("--early-exit-workload", default="long_draft",
+                    help="workload timed with and without early exit in the aux block ('' = skip)")
+    ap.add_argument("--early-exit-sigmas", default="1.5,4.0",
+                    help="drafter noise levels of that workload (a noisier drafter is rejected earlier)")
     ap.add_argument("--kd-rollouts", type=int, default=64, help="rollouts of the distillation batch")
     return ap.parse_args()
 
@@ -243,7 +247,7 @@ def reference_arm(args, w):
 # our arm
 # ---------------------------------------------------------------------------
 
-def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=None):
+def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=None, early_exit=False):
     """Device-timed steps of one workload.  Returns a dict of measurements."""
     import torch
 
@@ -259,6 +263,7 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
     if args.stages or args.ctas_per_sm:
         ver.set_pipeline(args.stages or 3, args.ctas_per_sm)
     ver.set_cluster(args.cluster)
+    ver.set_early_exit(early_exit)
     outs = [(torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device),
              torch.empty(w.B, dtype=torch.int32, device=device)) for _ in range(rotate)]
 
@@ -472,6 +477,23 @@ def our_arm(args, w):
                      "algorithmic_bytes": am["bytes"], "mean_emitted": am["stats"]["mean_emitted"],
                      "cluster": am["cfg"]["cluster"], "grid_ctas": am["cfg"]["grid_ctas"]}
         del am
+    if args.early_exit_workload and world == 1:
+        # rows after a decided rejection are not read: reported apart from the
+        # read-once metric (same outputs, fewer bytes)
+        from workloads import get_workload
+        runs = []
+        for sigma in [float(x) for x in args.early_exit_sigmas.split(",") if x]:
+            ew = get_workload(args.early_exit_workload, draft_sigma=sigma)
+            n = max(1, args.steps // 4)
+            on = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=True)
+            off = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=False)
+            runs.append({"workload": ew.describe() + f" draft noise {sigma}", "ms_per_step_on": on["total_ms"] / n,
+                         "ms_per_step_off": off["total_ms"] / n,
+                         "positions_per_s_on": on["positions"] / (on["total_ms"] / n / 1e3),
+                         "speedup": off["total_ms"] / on["total_ms"], "mean_emitted": on["stats"]["mean_emitted"],
+                         "cluster": on["cfg"]["cluster"]})
+            del on, off
+        aux["early_exit"] = runs
     if args.kd_steps > 0 and world == 1:
         aux["kd_loss"] = time_kd(svp, device, stream, args.kd_steps, max(3, args.warmup // 10), n_seq=args.kd_rollouts)
 

@@ -196,6 +196,17 @@ sv_status sv_get_config(const sv_ctx *ctx, int *stages, int *ctas_per_sm, int *t
                         int *smem_bytes, int *grid_ctas, int *cluster);
 sv_status sv_launch_shape(const sv_ctx *ctx, int B, int *cluster, int *grid_ctas);
 
+/* Early exit (off by default): rows of a sequence after its first rejection
+ * are not read once the rejection is decided.  The outputs are the same; the
+ * diagnostics of the rows not read stay NaN.  With one CTA per sequence the
+ * rest of a sequence is dropped as soon as its rejection is known; in a
+ * cluster the decision on pair i spares the rows from pair i + E on, E fixed
+ * by the row length (about 32 64 KB chunks of every CTA's slice), so that
+ * every CTA skips the same rows.  Reading stops before the bonus row too.  The bytes read then fall
+ * below "every needed row once": report such runs apart from that metric.
+ * on: 0 or 1 (else SV_ERR_INVALID_ARG). */
+sv_status sv_set_early_exit(sv_ctx *ctx, int on);
+
 /* Reward-weighted distillation loss of the draft model and its gradient in
  * the draft logits ("ReSpec: Towards Optimizing Speculative Decoding in
  * Reinforcement Learning Systems", Online Learner, reward-weighted KD):

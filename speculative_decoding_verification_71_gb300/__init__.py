@@ -38,7 +38,8 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
-    "sv_set_pipeline", "sv_set_cluster", "sv_get_config", "sv_launch_shape", "sv_set_wait_limit_ns",
+    "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_get_config", "sv_launch_shape",
+    "sv_set_wait_limit_ns",
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
 )
 
@@ -99,6 +100,8 @@ def load_library(path: str | None = None):
     lib.spec_verify_reset_stats.argtypes = [P, P]
     lib.sv_set_pipeline.restype = c.c_int
     lib.sv_set_pipeline.argtypes = [P, c.c_int, c.c_int]
+    lib.sv_set_early_exit.restype = c.c_int
+    lib.sv_set_early_exit.argtypes = [P, c.c_int]
     lib.sv_set_cluster.restype = c.c_int
     lib.sv_set_cluster.argtypes = [P, c.c_int]
     lib.sv_get_config.restype = c.c_int
@@ -284,6 +287,14 @@ class SpecVerifier:
         st = self.lib.sv_set_cluster(self._ctx, int(cluster))
         if st != SV_OK:
             self._raise(st, "sv_set_cluster")
+
+    def set_early_exit(self, on: bool):
+        """Skip the rows of a sequence after its first rejection once it is
+        decided (same outputs; fewer bytes read; diagnostics of skipped rows
+        stay NaN)."""
+        st = self.lib.sv_set_early_exit(self._ctx, 1 if on else 0)
+        if st != SV_OK:
+            self._raise(st, "sv_set_early_exit")
 
     def config(self):
         vals = [ctypes.c_int() for _ in range(6)]

@@ -23,6 +23,7 @@ struct sv_ctx {
   int stages = 3;
   int ctas_per_sm = 0;
   int cluster = 0;             // 0: chosen per call
+  int early_exit = 0;          // 1: rows after a decided rejection are not read
   int max_clusters[4] = {0};   // clusters of 1, 2, 4, 8 CTAs that fit at once
   int num_sms = 0;
   int smem_bytes = 0;
@@ -244,6 +245,7 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
            (draft_logits == nullptr || aligned16(draft_logits));
   p.wait_limit_ns = ctx->wait_limit_ns;
   p.ws = ctx->ws;
+  p.early_exit = ctx->early_exit;
   // persistent grid: every cluster that fits at once, but never more than sequences
   int ctas = 0;
   launch_shape(ctx, B, &p.cluster, &ctas);
@@ -323,6 +325,12 @@ sv_status sv_set_pipeline(sv_ctx* ctx, int stages, int ctas_per_sm) {
   sv_status s = configure(ctx, stages, ctas_per_sm);
   if (s != SV_OK) configure(ctx, prev_s, prev_c);
   return s;
+}
+
+sv_status sv_set_early_exit(sv_ctx* ctx, int on) {
+  if (!ctx || (on != 0 && on != 1)) return SV_ERR_INVALID_ARG;
+  ctx->early_exit = on;
+  return SV_OK;
 }
 
 sv_status sv_set_cluster(sv_ctx* ctx, int cluster) {

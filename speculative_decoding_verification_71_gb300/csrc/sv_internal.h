@@ -58,6 +58,7 @@ struct VerifyParams {
   int stages;           // staging slots per CTA (2..kMaxStages)
   int bulk;             // 1: rows staged with cp.async.bulk; 0: plain loads
   int cluster;          // CTAs per cluster: each takes one slice of every row (1, 2, 4 or 8)
+  int early_exit;       // 1: rows after a decided rejection are not read
   long long wait_limit_ns;
   Workspace ws;
 };

@@ -63,6 +63,7 @@ namespace {
 //               rejected pair at pos: the first half of the slot holds target
 //               logits, the second half the draft logits of the same range;
 //               K0, L0, K1, L1 are the pair's normalisers;
+//   kind 3:     end of a sequence cut short (early exit): no data;
 //   kind -1:    no more work; x = draws inserted in all.
 struct Desc {
   int b, kb, pos, kind;
@@ -100,6 +101,9 @@ struct SeqRec {
   int open;                    // from the first row until the outputs are settled
   int draw;                    // a residual draw follows (final once resolved)
   volatile int resolved;       // seq + 1 once `draw` and the normalisers are final
+  volatile int seq_tag;        // seq of the sequence the record holds (set when opened)
+  volatile int decided;        // pairs decided so far (early exit)
+  volatile int stop;           // a rejection or an error: later rows are not needed
   float s;                     // sampling uniform
   float Kt, Lt, Kd, Ld;        // normalisers of the rejected pair
   int tok[32];                 // drafted tokens, taken from the rows as they pass
@@ -120,6 +124,7 @@ constexpr int kWalkReqs = 16;      // walk requests (ring)
 constexpr int kRowBufs = 4;        // row buffers (ring)
 constexpr int kXRing = 4;          // exchange slots of rows and of draws
 constexpr int kDrawLagChunks = 6;  // a draw is inserted about this many chunks after its sequence ends ...
+constexpr int kExitLagChunks = 32; // early exit in a cluster: a decision spares the rows this many chunks later
 constexpr int kMaxPending = 24;    // ... or when this many sequences wait for theirs
 constexpr int kHalfBytes = kChunkBytes / 2;                          // one row's part of a draw chunk
 constexpr int kDrawVecsPerWarp = kHalfBytes / 16 / kConsumerWarps;   // 128
@@ -265,6 +270,7 @@ struct Verifier {
   int ndraw;                    // draw chunks per slice (at least one)
   int v_lo, v_hi;               // 16-byte vectors of the row covering the slice
   int lag_rows;                 // rows between a sequence's end and its re-read (same in every CTA)
+  int exit_lag;                 // early exit: pairs between a decision and the rows it can spare
 
   __device__ Verifier(const VerifyParams& p, Ctrl& c, unsigned char* r, int ln, int wp, int ncta, int rk)
       : P(p), C(c), ring(r), lane(ln), warp(wp), cs(ncta), rank(rk),
@@ -281,6 +287,8 @@ struct Verifier {
     // counted in chunks of the first (largest) slice so that every CTA agrees
     const int chunks0 = max(1, (min(p.V, per) * ELT + kChunkBytes - 1) / kChunkBytes);
     lag_rows = max(1, (kDrawLagChunks + chunks0 - 1) / chunks0);
+    const int pair_chunks = (GREEDY ? 1 : 2) * chunks0;
+    exit_lag = max(1, (kExitLagChunks + pair_chunks - 1) / pair_chunks);
   }
 
   __device__ const unsigned char* row_ptr(int b, int pos, int kind) const {
@@ -484,6 +492,69 @@ struct Verifier {
         if (GREEDY) { pos = r; kind = 0; }
         else if (r < 2 * kb) { pos = r >> 1; kind = r & 1; }
         else { pos = kb; kind = 0; }
+        if (P.early_exit && cs == 1 && r > 0) {
+          // early exit, one CTA per sequence: no peer to stay in step with, so
+          // the rest of the sequence is dropped as soon as a rejection (or an
+          // error) is known, without waiting for it
+          int stop = 0;
+          if (lane == 0) {
+            const SeqRec& R = C.rec[rc];
+            stop = (R.seq_tag == streamed && R.stop) ? 1 : 0;
+          }
+          if (__shfl_sync(0xffffffffu, stop, 0)) {
+            if (!(ok = acquire_slot(q))) break;
+            const int slot = q % S;
+            if (lane == 0) {
+              Desc& d = C.desc[slot];
+              d.b = b; d.kb = kb; d.pos = pos; d.kind = 3;
+              d.chunk = 0; d.nchunks = 1; d.x = -1; d.rec = rc; d.seq = streamed;
+              d.u = 0.f; d.s = s_samp;
+              mbar_arrive(&C.full[slot]);
+            }
+            ++q;
+            ++rows;
+            break;
+          }
+        }
+        if (P.early_exit && cs > 1 && kind == 0 && pos >= exit_lag) {
+          // early exit in a cluster, decided the same way in every CTA: wait
+          // for the control warp's decision on pair pos - exit_lag; after a
+          // rejection (or an error) the rest of the sequence is not read
+          int stop = 0, seen = 0;
+          if (lane == 0) {
+            const unsigned long long t0 = global_ns();
+            while (true) {
+              const SeqRec& R = C.rec[rc];
+              if (R.seq_tag == streamed && R.decided > pos - exit_lag) {
+                __threadfence_block();
+                stop = R.stop;
+                seen = 1;
+                break;
+              }
+              if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) break;
+              __nanosleep(64);
+            }
+            if (!seen) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+          }
+          seen = __shfl_sync(0xffffffffu, seen, 0);
+          stop = __shfl_sync(0xffffffffu, stop, 0);
+          if (!(ok = seen != 0)) break;
+          if (stop) {
+            // the end marker: no data, it closes the sequence downstream
+            if (!(ok = acquire_slot(q))) break;
+            const int slot = q % S;
+            if (lane == 0) {
+              Desc& d = C.desc[slot];
+              d.b = b; d.kb = kb; d.pos = pos; d.kind = 3;
+              d.chunk = 0; d.nchunks = 1; d.x = -1; d.rec = rc; d.seq = streamed;
+              d.u = 0.f; d.s = s_samp;
+              mbar_arrive(&C.full[slot]);
+            }
+            ++q;
+            ++rows;
+            break;
+          }
+        }
         const int x = __shfl_sync(0xffffffffu, xj, pos < kb ? pos : 0);
         const float u = __shfl_sync(0xffffffffu, uj, pos < kb ? pos : 0);
         const unsigned char* src = row_ptr(b, pos, kind);
@@ -643,7 +714,7 @@ struct Verifier {
         rK = -INFINITY; rS = 0.f; rM = -INFINITY; rArg = 0x7fffffff; rBad = 0;
       }
       const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
-      const int rem = slice_bytes - d.chunk * kChunkBytes;
+      const int rem = d.kind == 3 ? 0 : slice_bytes - d.chunk * kChunkBytes;   // an end marker is empty
       const int nvec = (min(max(rem, 0), kChunkBytes) + 15) / 16;
       uint4 raw[kVecsPerLane];
 #pragma unroll
@@ -1049,13 +1120,17 @@ struct Verifier {
     SeqRec& R = C.rec[d.rec];
     const size_t b = static_cast<size_t>(d.b);
     const bool diag = (rank == 0);
-    const bool last = (d.kind == 0 && d.pos == d.kb);
+    const bool marker = (d.kind == 3);      // the sequence was cut short after a rejection
+    const bool last = (d.kind == 0 && d.pos == d.kb) || marker;
     int bonus = 0, settle = 0;
-    if (lane == 0) {
+    if (lane == 0 && !marker) {
       if (d.pos == 0 && d.kind == 0) {
         // first row of the sequence: open its record
         R.b = d.b; R.kb = d.kb; R.a = -1; R.err = 0; R.y = -1; R.zero_resid = 0;
         R.open = 1; R.draw = 0; R.s = d.s;
+        R.decided = 0; R.stop = 0;
+        __threadfence_block();
+        R.seq_tag = d.seq;
       }
       if (bad & 2) R.err |= kErrTimeout;
       if (d.pos < d.kb) R.tok[d.pos] = d.x;
@@ -1102,6 +1177,14 @@ struct Verifier {
           bonus = 1;   // every draft accepted: the bonus draw
         }
       }
+      if ((GREEDY && d.pos < d.kb) || (!GREEDY && d.kind == 1)) {
+        // pair d.pos is decided: the producer may stop streaming this sequence
+        R.stop = (R.a >= 0 || R.err) ? 1 : 0;
+        __threadfence_block();
+        R.decided = d.pos + 1;
+      }
+    }
+    if (lane == 0) {
       if (last) {
         // the outcome is known: tell the producer whether a re-read follows
         R.draw = (!GREEDY && R.a >= 0 && !R.err) ? 1 : 0;
@@ -1350,7 +1433,10 @@ verify_kernel(const VerifyParams P) {
       mbar_init(&C.xdraw_ready[x], 1);
       mbar_init(&C.xdraw_free[x], cs);
     }
-    for (int r = 0; r < kRecs; ++r) { C.rec[r].open = 0; C.rec[r].resolved = 0; }
+    for (int r = 0; r < kRecs; ++r) {
+      C.rec[r].open = 0; C.rec[r].resolved = 0;
+      C.rec[r].seq_tag = -1; C.rec[r].decided = 0; C.rec[r].stop = 0;
+    }
     C.wreq_head = 0;
     C.wreq_tail = 0;
     C.ctl_done = 0;

@@ -89,8 +89,10 @@ def compare(gpu_tokens, gpu_len, ref, draft_len):
 MASS_ABS = 1e-6
 
 
-def compare_diagnostics(dbg, ref, draft_len, out_len):
-    """Largest error / tolerance of LSE, alpha and the drawn mass."""
+def compare_diagnostics(dbg, ref, draft_len, out_len, skipped_ok=False):
+    """Largest error / tolerance of LSE, alpha and the drawn mass.  With
+    ``skipped_ok`` (early exit) rows after a rejection may hold NaN: they were
+    not read."""
     kb = np.asarray(draft_len)
     B, k1 = ref["lse_t"].shape
     k = k1 - 1
@@ -102,11 +104,17 @@ def compare_diagnostics(dbg, ref, draft_len, out_len):
     for b in range(B):
         if int(ref["status"][b]) & 0xFF:
             continue
+        a_ref = int(ref["out_len"][b]) - 1
+        skip = lambda i, v: skipped_ok and i > a_ref and np.isnan(v)
         for i in range(kb[b] + 1):
             r = ref["lse_t"][b, i]
+            if skip(i, lse_t[b, i]):
+                continue
             worst["lse"] = max(worst["lse"], abs(lse_t[b, i] - r) / (RTOL * max(1.0, abs(r))))
         for i in range(kb[b]):
             r = ref["lse_d"][b, i]
+            if skip(i, lse_d[b, i]):
+                continue
             worst["lse"] = max(worst["lse"], abs(lse_d[b, i] - r) / (RTOL * max(1.0, abs(r))))
             ra = ref["alpha"][b, i]
             if ra >= 1e-30:

@@ -125,6 +125,45 @@ def test_cluster_setting_is_checked():
     assert cs in (1, 2, 4, 8) and ctas % cs == 0
 
 
+# --- early exit: the rows after a decided rejection are not read ----------------
+
+EXIT_CASES = [
+    ("long_draft", dict(B=48, k=7, V=12288), 1),     # low acceptance: early rejections
+    ("long_draft", dict(B=24, k=24, V=24576), 2),   # clusters wait exit_lag = 16 pairs
+    ("ragged", dict(B=40, k=3, V=20000), 4),
+    ("ragged", dict(B=32, k=5, V=8192, T=0.0), 1),  # greedy
+]
+
+
+@pytest.mark.parametrize("name,over,cs", EXIT_CASES, ids=[f"{n}-{o}-cs{c}" for n, o, c in EXIT_CASES])
+def test_early_exit_keeps_the_outputs(name, over, cs):
+    inp = small(name, **over)
+    B, k = inp["meta"]["B"], inp["meta"]["k"]
+    ver = verifier_for(inp)
+    ver.set_cluster(cs)
+    t0, l0 = run_gpu(ver, inp)
+    ver.set_early_exit(True)
+    t1, l1 = run_gpu(ver, inp)
+    np.testing.assert_array_equal(l0, l1)
+    np.testing.assert_array_equal(t0, t1)
+    ref = run_oracle(inp)
+    kb = inp["draft_len"].cpu().numpy()
+    res = compare(t1, l1, ref, kb)
+    assert res["mismatch"] == 0, res["bad"][:10]
+    if inp["T"] > 0:
+        dbg = ver.debug(B, k)
+        worst = compare_diagnostics(dbg, ref, kb, l1, skipped_ok=True)
+        assert max(worst.values()) < 1.0, worst
+        # rows far enough after an early rejection were not read
+        lse_t = dbg["lse_t"].cpu().numpy()
+        skipped = sum(int(np.isnan(lse_t[b, l1[b] + 2:kb[b] + 1]).sum()) for b in range(B))
+        if name == "long_draft":
+            assert skipped > 0
+        # and every row up to the rejection was
+        for b in range(B):
+            assert np.isfinite(lse_t[b, :l1[b]]).all()
+
+
 # --- exhaustive enumeration batch ----------------------------------------------
 
 @pytest.mark.parametrize("kb,T,seed", [(2, 1.0, 0), (1, 0.7, 1), (0, 1.6, 2)])
