@@ -5,7 +5,8 @@ smoke check and by the CPU-baseline leg of ``bench.py``.  The library in
 ``speculative_decoding_verification_71_gb300`` never imports this package,
 and this package never imports the library.
 
-``build()`` compiles ``oracle.c`` with gcc (-O2, no fast-math, OpenMP) into
+``build()`` compiles ``oracle.c`` with gcc (-O2, no fast-math, no contraction of
+a multiply and an add into one rounding, OpenMP) into
 ``liboracle.so`` beside it.  ``verify(...)`` takes numpy arrays or CPU torch
 tensors with the same layout as the library's entry point and returns the
 outputs plus the diagnostics the parity tests use.
@@ -34,7 +35,7 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH, extra=()) 
     """Compile the oracle (or, for mutation tests, another source file)."""
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
         return out
-    cmd = ["gcc", "-O2", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c11",
            "-Wall", *extra, src, "-o", out + ".tmp", "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(out + ".tmp", out)
@@ -56,6 +57,17 @@ def _bind(lib):
     lib.oracle_num_threads.restype = c.c_int
     lib.oracle_kd.restype = c.c_int
     lib.oracle_kd.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, c.c_double, P, P, P, P, c.c_int]
+    D, I = c.c_double, c.c_int
+    lib.oracle_ctrl_observe.restype = I
+    lib.oracle_ctrl_observe.argtypes = [I, P, P, I, P, P, P, I, D, P]
+    lib.oracle_ctrl_alpha.restype = D
+    lib.oracle_ctrl_alpha.argtypes = [D, D, D, D]
+    lib.oracle_ctrl_expected_tokens.restype = D
+    lib.oracle_ctrl_expected_tokens.argtypes = [D, I]
+    lib.oracle_ctrl_round_time.restype = D
+    lib.oracle_ctrl_round_time.argtypes = [I, P, P, I, I, I]
+    lib.oracle_ctrl_choose.restype = I
+    lib.oracle_ctrl_choose.argtypes = [I, P, P, I, P, I, D, D, I, I, P, P, P, P, P, P, P]
     return lib
 
 
@@ -186,3 +198,74 @@ def kd(target, draft, weights, T=1.0, grad=True, nthreads=0, lib=None):
     if rc != 0:
         raise ValueError(f"oracle_kd failed ({rc})")
     return {"row_kl": row_kl, "loss": loss, "grad": g, "status": status}
+
+
+CTRL_USED, CTRL_SKIPPED, CTRL_BAD_LEN, CTRL_BAD_ID = 0, 1, 2, 5
+
+
+class Controller:
+    """The draft-length controller of ``oracle_ctrl_*`` in oracle.c: decayed
+    acceptance counts per sequence slot and the round-time table.  Mirrors
+    the library's controller call for call (observe, choose, alpha)."""
+
+    def __init__(self, n_slots, max_k, batch_sizes, table, decay=0.9, prior_alpha=0.5,
+                 prior_weight=2.0, mode=0, lib=None):
+        self.lib = lib or load()
+        self.n_slots, self.max_k = int(n_slots), int(max_k)
+        self.A = np.zeros(self.n_slots)
+        self.N = np.zeros(self.n_slots)
+        self.set_cost(batch_sizes, table)
+        self.decay, self.prior_alpha, self.prior_weight, self.mode = float(decay), float(prior_alpha), \
+            float(prior_weight), int(mode)
+
+    def set_cost(self, batch_sizes, table):
+        self.batch_sizes = np.ascontiguousarray(batch_sizes, dtype=np.int32).reshape(-1)
+        self.table = np.ascontiguousarray(table, dtype=np.float64).reshape(self.batch_sizes.size, self.max_k + 1)
+
+    def reset(self, seq_ids=None):
+        if seq_ids is None:
+            self.A[:] = 0.0
+            self.N[:] = 0.0
+        else:
+            self.A[np.asarray(seq_ids)] = 0.0
+            self.N[np.asarray(seq_ids)] = 0.0
+
+    def observe(self, seq_ids, draft_len, out_len):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        k = np.ascontiguousarray(draft_len, dtype=np.int32)
+        n = np.ascontiguousarray(out_len, dtype=np.int32)
+        st = np.empty(ids.size, np.int32)
+        self.lib.oracle_ctrl_observe(self.n_slots, _ptr(self.A), _ptr(self.N), ids.size, _ptr(ids), _ptr(k),
+                                     _ptr(n), self.max_k, self.decay, _ptr(st))
+        return st
+
+    def alpha(self, seq_ids):
+        return np.array([self.lib.oracle_ctrl_alpha(self.A[i], self.N[i], self.prior_alpha, self.prior_weight)
+                         for i in np.asarray(seq_ids)])
+
+    def round_time(self, B, n):
+        return self.lib.oracle_ctrl_round_time(self.batch_sizes.size, _ptr(self.batch_sizes), _ptr(self.table),
+                                               self.max_k, int(B), int(n))
+
+    def choose(self, seq_ids):
+        """Returns next_len [B], choice, rates [max_k+1] (batch mode), margin
+        ([1] batch mode, [B] per sequence) and the row status."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        B = ids.size
+        nxt = np.empty(B, np.int32)
+        choice = np.zeros(1, np.int32)
+        rates = np.zeros(self.max_k + 1)
+        margin = np.zeros(max(B, 1))
+        st = np.empty(B, np.int32)
+        rc = self.lib.oracle_ctrl_choose(self.n_slots, _ptr(self.A), _ptr(self.N), B, _ptr(ids), self.max_k,
+                                         self.prior_alpha, self.prior_weight, self.mode, self.batch_sizes.size,
+                                         _ptr(self.batch_sizes), _ptr(self.table), _ptr(nxt), _ptr(choice),
+                                         _ptr(rates), _ptr(margin), _ptr(st))
+        if rc != 0:
+            raise ValueError(f"oracle_ctrl_choose failed ({rc})")
+        return {"next_len": nxt, "choice": int(choice[0]), "rates": rates,
+                "margin": margin[:1] if self.mode == 0 else margin[:B], "status": st}
+
+
+def expected_tokens(alpha, n, lib=None):
+    return (lib or load()).oracle_ctrl_expected_tokens(float(alpha), int(n))

@@ -444,3 +444,185 @@ int oracle_kd(int n_seq, int t_len, int V, int dtype, const void *target, const 
     }
     return 0;
 }
+
+/*
+ * Acceptance-aware draft-length controller with the speculation toggle
+ * ("EfficientRollout: System-Aware Self-Speculative Decoding for RL
+ * Rollouts", abstract: a system-aware SD toggle with acceptance-aware
+ * draft-length adaptation; "ReSpec: Towards Optimizing Speculative Decoding
+ * in Reinforcement Learning Systems", Adaptive Server: a performance model
+ * profiled offline per batch size picks the SD configuration for the
+ * effective batch size, and the scheduler runs non-speculatively when the
+ * batch is large).  The pages fix no formulas; the readings used:
+ *
+ *   observe: a round of sequence b with draft length k_b > 0 and emitted
+ *     length out_len = a + 1 tested a + r drafts, r = 1 if a < k_b (the
+ *     first rejection) else 0; drafts after a rejection are never tested.
+ *     Decayed counts: A_b <- decay * A_b + a, N_b <- decay * N_b + (a + r).
+ *   estimate: alpha_b = (A_b + alpha0 * w0) / (N_b + w0) (w0 prior
+ *     pseudo-tests at rate alpha0); alpha0 when N_b + w0 = 0.  With decay 1
+ *     and w0 = 0 this is the maximum-likelihood rate of the truncated
+ *     geometric law of a.
+ *   expected tokens of a round with draft length n at per-draft acceptance
+ *     alpha: E_n(alpha) = sum_{j=0..n} alpha^j (the corrected or bonus token
+ *     plus each accepted prefix).
+ *   round time T(B, n): a table at profiled batch sizes B_0 < ... < B_m-1,
+ *     linear in B between two of them, the end row outside.
+ *   choose (mode 0, batch): n* = argmax_n sum_b E_n(alpha_b) / T(B, n) over
+ *     n = 0..max_k, the smallest n on ties; every row gets n*; n* = 0 is
+ *     speculation off.  (mode 1, per sequence): n_b = argmax_n
+ *     E_n(alpha_b) / T(B, n).
+ *
+ * Row status: 0 used, 1 skipped (out_len 0: the verifier rejected the
+ * sequence; or k_b = 0: nothing tested), 2 bad length (k_b outside
+ * [0, max_k] or out_len outside [0, k_b + 1]), 5 bad id (outside
+ * [0, n_slots) or repeated within the call).  Rows with status 2 or 5 leave
+ * the state unchanged.
+ */
+#define ORC_CTRL_USED 0
+#define ORC_CTRL_SKIPPED 1
+#define ORC_CTRL_BAD_LEN 2
+#define ORC_CTRL_BAD_ID 5
+
+int oracle_ctrl_observe(int n_slots, double *A, double *N, int B, const int *seq_ids,
+                        const int *draft_len, const int *out_len, int max_k, double decay,
+                        int *row_status)
+{
+    for (int b = 0; b < B; ++b) {
+        const int id = seq_ids[b];
+        int repeated = 0;
+        for (int c = 0; c < B; ++c)
+            if (c != b && seq_ids[c] == id)
+                repeated = 1;
+        if (id < 0 || id >= n_slots || repeated) {
+            row_status[b] = ORC_CTRL_BAD_ID;
+            continue;
+        }
+        const int k = draft_len[b], len = out_len[b];
+        if (k < 0 || k > max_k || len < 0 || len > k + 1) {
+            row_status[b] = ORC_CTRL_BAD_LEN;
+            continue;
+        }
+        if (len == 0 || k == 0) {
+            row_status[b] = ORC_CTRL_SKIPPED;
+            continue;
+        }
+        const int a = len - 1;
+        const int r = (a < k) ? 1 : 0;
+        A[id] = decay * A[id] + (double)a;
+        N[id] = decay * N[id] + (double)(a + r);
+        row_status[b] = ORC_CTRL_USED;
+    }
+    return 0;
+}
+
+double oracle_ctrl_alpha(double A, double N, double alpha0, double w0)
+{
+    const double den = N + w0;
+    if (den == 0.0)
+        return alpha0;
+    return (A + alpha0 * w0) / den;
+}
+
+double oracle_ctrl_expected_tokens(double alpha, int n)
+{
+    double e = 0.0;
+    for (int j = 0; j <= n; ++j)
+        e += pow(alpha, (double)j);
+    return e;
+}
+
+double oracle_ctrl_round_time(int n_points, const int *batch_sizes, const double *table,
+                              int max_k, int B, int n)
+{
+    const int K1 = max_k + 1;
+    if (B <= batch_sizes[0])
+        return table[n];
+    if (B >= batch_sizes[n_points - 1])
+        return table[(size_t)(n_points - 1) * K1 + n];
+    int j = 0;
+    while (!(batch_sizes[j] <= B && B < batch_sizes[j + 1]))
+        ++j;
+    const double t0 = table[(size_t)j * K1 + n], t1 = table[(size_t)(j + 1) * K1 + n];
+    const double f = (double)(B - batch_sizes[j]) / (double)(batch_sizes[j + 1] - batch_sizes[j]);
+    return t0 + (t1 - t0) * f;
+}
+
+/* rates [max_k + 1] (may be NULL) receives, in batch mode, sum_b E_n / T(B, n);
+ * margin (may be NULL) the relative gap between the best and the second-best
+ * rate of the batch (mode 0) or of each row (mode 1, [B]).  Rows with a bad
+ * id get 0 and status 5. */
+int oracle_ctrl_choose(int n_slots, const double *A, const double *N, int B, const int *seq_ids,
+                       int max_k, double alpha0, double w0, int mode, int n_points,
+                       const int *batch_sizes, const double *table, int *next_len, int *choice,
+                       double *rates, double *margin, int *row_status)
+{
+    const int K1 = max_k + 1;
+    double T[32], R[32];
+    if (K1 > 32)
+        return -1;
+    for (int n = 0; n < K1; ++n) {
+        T[n] = oracle_ctrl_round_time(n_points, batch_sizes, table, max_k, B, n);
+        R[n] = 0.0;
+    }
+    int best_all = 0;
+    for (int b = 0; b < B; ++b) {
+        const int id = seq_ids[b];
+        if (id < 0 || id >= n_slots) {
+            row_status[b] = ORC_CTRL_BAD_ID;
+            next_len[b] = 0;
+            if (mode == 1 && margin)
+                margin[b] = INFINITY;
+            continue;
+        }
+        row_status[b] = ORC_CTRL_USED;
+        const double alpha = oracle_ctrl_alpha(A[id], N[id], alpha0, w0);
+        if (mode == 0) {
+            for (int n = 0; n < K1; ++n)
+                R[n] += oracle_ctrl_expected_tokens(alpha, n);
+            continue;
+        }
+        int best = 0;
+        double top = -1.0, second = -1.0;
+        for (int n = 0; n < K1; ++n) {
+            const double rate = oracle_ctrl_expected_tokens(alpha, n) / T[n];
+            if (rate > top) {
+                second = top;
+                top = rate;
+                best = n;
+            } else if (rate > second) {
+                second = rate;
+            }
+        }
+        next_len[b] = best;
+        if (best > best_all)
+            best_all = best;
+        if (margin)
+            margin[b] = (K1 > 1) ? (top - second) / top : INFINITY;
+    }
+    if (mode == 0) {
+        int best = 0;
+        double top = -1.0, second = -1.0;
+        for (int n = 0; n < K1; ++n) {
+            R[n] = R[n] / T[n];
+            if (R[n] > top) {
+                second = top;
+                top = R[n];
+                best = n;
+            } else if (R[n] > second) {
+                second = R[n];
+            }
+            if (rates)
+                rates[n] = R[n];
+        }
+        for (int b = 0; b < B; ++b)
+            if (row_status[b] == ORC_CTRL_USED)
+                next_len[b] = best;
+        best_all = best;
+        if (margin)
+            margin[0] = (K1 > 1 && top > 0.0) ? (top - second) / top : INFINITY;
+    }
+    if (choice)
+        *choice = best_all;
+    return 0;
+}
