@@ -280,6 +280,102 @@ sv_status spec_verify_noalloc(int B, int k, int V, sv_dtype dtype,
                               int32_t *out_tokens, int32_t *out_len,
                               sv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Draft-length controller and speculation toggle.
+ *
+ * "EfficientRollout: System-Aware Self-Speculative Decoding for RL Rollouts"
+ * (abstract): speculation is switched on only in the regimes where it pays
+ * for the system, and the draft length follows the drafter's acceptance.
+ * "ReSpec: Towards Optimizing Speculative Decoding in Reinforcement Learning
+ * Systems" (Adaptive Server): a performance model profiled offline gives, per
+ * batch size, the speed of each SD configuration; at run time the effective
+ * batch size picks the configuration, and large batches decode without
+ * speculation.  The pages give no formulas; the rule used here:
+ *
+ *   observe: a verified round of sequence b (draft length k_b > 0, emitted
+ *     length a + 1) tested a + r drafts, r = 1 if a < k_b; the per-slot
+ *     counts decay: A <- decay A + a, N <- decay N + (a + r);
+ *   alpha_b = (A + prior_alpha * prior_weight) / (N + prior_weight), or
+ *     prior_alpha while N + prior_weight = 0;
+ *   expected tokens of a round of n drafts: E_n(alpha) = sum_{j=0..n} alpha^j;
+ *   round time T(B, n): the caller's profiled table, linear in B between two
+ *     profiled batch sizes, the nearest end row outside them;
+ *   SV_CTRL_BATCH: n* = argmax_n sum_b E_n(alpha_b) / T(B, n) over
+ *     n = 0..max_k (smallest n on ties) for every row; n* = 0 switches
+ *     speculation off for the round;
+ *   SV_CTRL_PER_SEQUENCE: n_b = argmax_n E_n(alpha_b) / T(B, n).
+ * B is the number of rows of the choose call: the active batch size.
+ *
+ * State: fp64 A and N per sequence slot, on the device, owned by the
+ * controller.  A decode loop runs spec_verify -> spec_ctrl_observe (its
+ * draft_len and out_len) -> spec_ctrl_choose (next round's draft lengths,
+ * which spec_verify accepts as they are) with no host round trip; every call
+ * is stream-ordered, allocates nothing and can be captured in a CUDA graph.
+ * One controller per stream; not thread-safe.
+ *
+ * Arrays marked "device" are caller-owned memory of the controller's device
+ * (checked for NULL only, as for spec_verify).
+ *
+ * Errors: host-checkable errors return SV_ERR_INVALID_ARG and launch
+ * nothing.  Errors found on the device set a sticky word read by
+ * spec_ctrl_status: a slot id outside [0, n_slots) or named twice in one
+ * observe call (SV_ERR_INVALID_ARG; the row is skipped, and choose gives it
+ * draft length 0), a draft length outside [0, max_k] or an emitted length
+ * outside [0, k_b + 1] (SV_ERR_BAD_DRAFT_LEN; skipped).  A row with emitted
+ * length 0 (a sequence the verifier rejected) or draft length 0 carries no
+ * acceptance information and is skipped without an error.
+ * ------------------------------------------------------------------------ */
+
+#define SV_CTRL_MAX_POINTS 12    /* profiled batch sizes in the round-time table */
+
+typedef enum { SV_CTRL_BATCH = 0, SV_CTRL_PER_SEQUENCE = 1 } sv_ctrl_mode;
+
+typedef struct sv_ctrl sv_ctrl;
+
+/* n_slots sequence slots (1..2^24), draft lengths 0..max_k (max_k <= 31).
+ * Allocates the state (zero: every slot at the prior) on the current device.
+ * Defaults: decay 0.9, prior_alpha 0.5, prior_weight 2, SV_CTRL_BATCH; no
+ * round-time table (spec_ctrl_choose fails until one is set). */
+sv_status spec_ctrl_create(sv_ctrl **ctrl, int n_slots, int max_k);
+sv_status spec_ctrl_destroy(sv_ctrl *ctrl);
+
+/* The profiled round-time table (host memory, copied): batch_sizes
+ * [n_points] strictly increasing and >= 1, round_time [n_points][max_k + 1]
+ * row-major, finite and > 0, any time unit (n = 0 is a round without
+ * speculation: one target step).  1 <= n_points <= SV_CTRL_MAX_POINTS.
+ * Takes effect for the choose calls issued after it. */
+sv_status spec_ctrl_set_cost(sv_ctrl *ctrl, int n_points, const int *batch_sizes, const double *round_time);
+
+/* decay in (0, 1], prior_alpha in [0, 1], prior_weight >= 0 and finite. */
+sv_status spec_ctrl_set_params(sv_ctrl *ctrl, double decay, double prior_alpha, double prior_weight,
+                               sv_ctrl_mode mode);
+
+/* Put slots back at the prior: seq_ids == NULL resets every slot and clears
+ * the error word; otherwise the n slots of seq_ids (device [n]) are reset. */
+sv_status spec_ctrl_reset(sv_ctrl *ctrl, int n, const int32_t *seq_ids, sv_stream_t stream);
+
+/* Add one verified round of B rows (device arrays [B]: slot ids, the draft
+ * lengths the round was verified with and spec_verify's out_len).
+ * 0 <= B <= n_slots. */
+sv_status spec_ctrl_observe(sv_ctrl *ctrl, int B, const int32_t *seq_ids, const int32_t *draft_len,
+                            const int32_t *out_len, sv_stream_t stream);
+
+/* Draft lengths of the next round for its B active rows: next_draft_len
+ * (device [B]) receives n* (batch mode) or n_b (per-sequence mode); choice
+ * (device, one int32, may be NULL) receives n* or the largest n_b, so
+ * choice == 0 means the round runs without speculation. */
+sv_status spec_ctrl_choose(sv_ctrl *ctrl, int B, const int32_t *seq_ids, int32_t *next_draft_len,
+                           int32_t *choice, sv_stream_t stream);
+
+/* The acceptance estimate alpha_b of B slots (device [B] fp64; NaN for a bad
+ * id). */
+sv_status spec_ctrl_alpha(sv_ctrl *ctrl, int B, const int32_t *seq_ids, double *alpha, sv_stream_t stream);
+
+/* Synchronises the stream and returns the sticky device error: SV_OK,
+ * SV_ERR_INVALID_ARG or SV_ERR_BAD_DRAFT_LEN (SV_ERR_CUDA if the copy
+ * failed). */
+sv_status spec_ctrl_status(sv_ctrl *ctrl, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

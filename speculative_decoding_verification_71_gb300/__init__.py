@@ -24,12 +24,14 @@ __all__ = [
     "SpecVerifier", "SpecVerifyError", "Stats", "load_library", "library_path",
     "SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_BAD_DRAFT_LEN", "SV_ERR_BAD_TOKEN",
     "SV_ERR_NONFINITE", "SV_ERR_TIMEOUT", "SV_ERR_CUDA", "SV_ERR_UNSUPPORTED",
-    "SV_F32", "SV_BF16", "EXPORTED_SYMBOLS",
+    "SV_F32", "SV_BF16", "EXPORTED_SYMBOLS", "DraftController", "SV_CTRL_BATCH", "SV_CTRL_PER_SEQUENCE",
 ]
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_BAD_DRAFT_LEN, SV_ERR_BAD_TOKEN = 0, 1, 2, 3
 SV_ERR_NONFINITE, SV_ERR_TIMEOUT, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 4, 5, 6, 7
 SV_F32, SV_BF16 = 0, 1
+SV_CTRL_BATCH, SV_CTRL_PER_SEQUENCE = 0, 1
+SV_CTRL_MAX_POINTS = 12
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libspecverify.so")
@@ -41,6 +43,8 @@ EXPORTED_SYMBOLS = (
     "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_get_config", "sv_launch_shape",
     "sv_set_wait_limit_ns",
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
+    "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_set_cost", "spec_ctrl_set_params", "spec_ctrl_reset",
+    "spec_ctrl_observe", "spec_ctrl_choose", "spec_ctrl_alpha", "spec_ctrl_status",
 )
 
 
@@ -115,6 +119,24 @@ def load_library(path: str | None = None):
     lib.sv_launch_shape.argtypes = [P, c.c_int, c.POINTER(c.c_int), c.POINTER(c.c_int)]
     lib.sv_set_wait_limit_ns.restype = c.c_int
     lib.sv_set_wait_limit_ns.argtypes = [P, c.c_longlong]
+    lib.spec_ctrl_create.restype = c.c_int
+    lib.spec_ctrl_create.argtypes = [c.POINTER(P), c.c_int, c.c_int]
+    lib.spec_ctrl_destroy.restype = c.c_int
+    lib.spec_ctrl_destroy.argtypes = [P]
+    lib.spec_ctrl_set_cost.restype = c.c_int
+    lib.spec_ctrl_set_cost.argtypes = [P, c.c_int, P, P]
+    lib.spec_ctrl_set_params.restype = c.c_int
+    lib.spec_ctrl_set_params.argtypes = [P, c.c_double, c.c_double, c.c_double, c.c_int]
+    lib.spec_ctrl_reset.restype = c.c_int
+    lib.spec_ctrl_reset.argtypes = [P, c.c_int, P, P]
+    lib.spec_ctrl_observe.restype = c.c_int
+    lib.spec_ctrl_observe.argtypes = [P, c.c_int, P, P, P, P]
+    lib.spec_ctrl_choose.restype = c.c_int
+    lib.spec_ctrl_choose.argtypes = [P, c.c_int, P, P, P, P]
+    lib.spec_ctrl_alpha.restype = c.c_int
+    lib.spec_ctrl_alpha.argtypes = [P, c.c_int, P, P, P]
+    lib.spec_ctrl_status.restype = c.c_int
+    lib.spec_ctrl_status.argtypes = [P, P]
     lib.spec_verify_noalloc.restype = c.c_int
     lib.spec_verify_noalloc.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, P, P, c.c_float, P, P, P]
     if path is None:
@@ -384,3 +406,88 @@ def kd_launch_shape(V, dtype=torch.bfloat16, grad=True):
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_kd_launch_shape")
     return cs.value, nb.value, ctas.value
+
+
+class DraftController:
+    """Draft-length controller and speculation toggle (``spec_ctrl_*`` in
+    include/specverify.h): per-slot acceptance state on the device, a
+    profiled round-time table, and the choice of the next round's draft
+    lengths.  ``n_slots`` sequence slots, draft lengths 0..``max_k``."""
+
+    def __init__(self, n_slots: int, max_k: int, device=None):
+        self.lib = load_library()
+        self.n_slots, self.max_k = int(n_slots), int(max_k)
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   torch.device(device).index or 0)
+        self._c = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            st = self.lib.spec_ctrl_create(ctypes.byref(self._c), self.n_slots, self.max_k)
+        if st != SV_OK:
+            raise SpecVerifyError(st, "spec_ctrl_create")
+
+    def close(self):
+        if self._c:
+            self.lib.spec_ctrl_destroy(self._c)
+            self._c = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _ok(self, st, where):
+        if st != SV_OK:
+            raise SpecVerifyError(st, where)
+
+    def set_cost(self, batch_sizes, round_time):
+        """batch_sizes [P] increasing; round_time [P, max_k + 1] (host)."""
+        import numpy as np
+        bs = np.ascontiguousarray(batch_sizes, dtype=np.int32).reshape(-1)
+        t = np.ascontiguousarray(round_time, dtype=np.float64).reshape(bs.size, self.max_k + 1)
+        self._ok(self.lib.spec_ctrl_set_cost(self._c, bs.size, bs.ctypes.data_as(ctypes.c_void_p),
+                                             t.ctypes.data_as(ctypes.c_void_p)), "spec_ctrl_set_cost")
+
+    def set_params(self, decay=0.9, prior_alpha=0.5, prior_weight=2.0, mode=SV_CTRL_BATCH):
+        self._ok(self.lib.spec_ctrl_set_params(self._c, float(decay), float(prior_alpha), float(prior_weight),
+                                               int(mode)), "spec_ctrl_set_params")
+
+    def _ids(self, seq_ids):
+        _check_dev("seq_ids", seq_ids, torch.int32, (seq_ids.numel(),), self.device)
+        return seq_ids.numel()
+
+    def reset(self, seq_ids=None, stream=None):
+        n = 0 if seq_ids is None else self._ids(seq_ids)
+        self._ok(self.lib.spec_ctrl_reset(self._c, n, _ptr(seq_ids), _stream_handle(stream)), "spec_ctrl_reset")
+
+    def observe(self, seq_ids, draft_len, out_len, stream=None):
+        B = self._ids(seq_ids)
+        _check_dev("draft_len", draft_len, torch.int32, (B,), self.device)
+        _check_dev("out_len", out_len, torch.int32, (B,), self.device)
+        self._ok(self.lib.spec_ctrl_observe(self._c, B, _ptr(seq_ids), _ptr(draft_len), _ptr(out_len),
+                                            _stream_handle(stream)), "spec_ctrl_observe")
+
+    def choose(self, seq_ids, next_draft_len=None, choice=None, stream=None):
+        """Returns (next_draft_len [B] int32, choice [1] int32) on the device."""
+        B = self._ids(seq_ids)
+        if next_draft_len is None:
+            next_draft_len = torch.empty(B, dtype=torch.int32, device=self.device)
+        if choice is None:
+            choice = torch.empty(1, dtype=torch.int32, device=self.device)
+        _check_dev("next_draft_len", next_draft_len, torch.int32, (B,), self.device)
+        _check_dev("choice", choice, torch.int32, (1,), self.device)
+        self._ok(self.lib.spec_ctrl_choose(self._c, B, _ptr(seq_ids), _ptr(next_draft_len), _ptr(choice),
+                                           _stream_handle(stream)), "spec_ctrl_choose")
+        return next_draft_len, choice
+
+    def alpha(self, seq_ids, stream=None):
+        B = self._ids(seq_ids)
+        out = torch.empty(B, dtype=torch.float64, device=self.device)
+        self._ok(self.lib.spec_ctrl_alpha(self._c, B, _ptr(seq_ids), _ptr(out), _stream_handle(stream)),
+                 "spec_ctrl_alpha")
+        return out
+
+    def status(self, stream=None):
+        """The sticky device error (SV_OK, SV_ERR_INVALID_ARG or
+        SV_ERR_BAD_DRAFT_LEN); synchronises the stream."""
+        return self.lib.spec_ctrl_status(self._c, _stream_handle(stream))

@@ -21,7 +21,7 @@ def lib():
 
 def declared_functions():
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
-    return sorted(set(re.findall(r"\b((?:sv|spec_verify|spec_kd)\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:sv|spec_verify|spec_kd|spec_ctrl)\w*)\s*\(", text)))
 
 
 def test_header_declares_the_binding_symbols():
@@ -84,3 +84,21 @@ def test_product_does_not_use_the_oracle():
             if f.endswith((".py", ".cu", ".h", ".cuh", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"import\s+oracle|from\s+oracle|liboracle|oracle\.c", text), f
+
+
+def test_controller_host_checks(lib):
+    P = None
+    out = ctypes.c_void_p()
+    assert lib.spec_ctrl_create(None, 4, 3) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_create(ctypes.byref(out), 0, 3) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_create(ctypes.byref(out), 4, 32) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_create(ctypes.byref(out), 4, -1) == svp.SV_ERR_INVALID_ARG
+    assert not out.value
+    assert lib.spec_ctrl_destroy(P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_set_cost(P, 1, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_set_params(P, 0.9, 0.5, 2.0, 0) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_reset(P, 0, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_observe(P, 1, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_choose(P, 1, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_alpha(P, 1, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_ctrl_status(P, P) == svp.SV_ERR_INVALID_ARG
