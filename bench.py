@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--early-exit-sigmas", default="1.5,4.0",
                     help="drafter noise levels of that workload (a noisier drafter is rejected earlier)")
     ap.add_argument("--kd-rollouts", type=int, default=64, help="rollouts of the distillation batch")
+    ap.add_argument("--ctrl-steps", type=int, default=200,
+                    help="timed rounds of the draft-length controller (0 = skip)")
     return ap.parse_args()
 
 
@@ -335,6 +337,84 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
             "soak_steps": soak, "cfg": cfg, "ver": ver, "base_inputs": base, "launch": launch}
 
 
+def _graph_ms(torch, stream, fn, steps):
+    """ms per call of fn, replayed `steps` times from one CUDA graph."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(steps):
+                fn()
+        g.replay()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        stream.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def time_controller(svp, w, device, stream, steps):
+    """The draft-length controller: one round (observe + choose) alone at a
+    GRPO-sized batch, and its cost on top of the verification step of
+    workload `w` (verify alone vs verify + observe + choose in one graph;
+    the chosen lengths are not fed back, so both time the same verify)."""
+    import torch
+
+    from workloads import make_inputs
+
+    out = {}
+    rng = np.random.default_rng(0)
+    B, K = 1024, 7
+    bs = np.array([1, 64, 256, 1024], np.int32)
+    table = 1.0 + np.array([0.02, 0.1, 0.3, 0.9])[:, None] * np.arange(K + 1)[None]
+    ids = torch.arange(B, dtype=torch.int32, device=device)
+    kb = torch.from_numpy(rng.integers(0, K + 1, B).astype(np.int32)).to(device)
+    ol = torch.minimum(kb + 1, torch.from_numpy(rng.integers(1, K + 2, B).astype(np.int32)).to(device))
+    nxt = torch.empty(B, dtype=torch.int32, device=device)
+    ch = torch.empty(1, dtype=torch.int32, device=device)
+    for mode, name in ((svp.SV_CTRL_BATCH, "batch"), (svp.SV_CTRL_PER_SEQUENCE, "per_sequence")):
+        c = svp.DraftController(B, K)
+        c.set_cost(bs, table)
+        c.set_params(0.9, 0.5, 2.0, mode)
+
+        def rnd():
+            c.observe(ids, kb, ol, stream=stream)
+            c.choose(ids, nxt, ch, stream=stream)
+        out[f"round_us_{name}"] = _graph_ms(torch, stream, rnd, steps) * 1e3
+        assert c.status(stream=stream) == svp.SV_OK
+    out["round_batch"] = f"B={B} slots, max_k={K}, {bs.size}-point round-time table"
+
+    inp = make_inputs(w, device=device)
+    ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+    ot = torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device)
+    on = torch.empty(w.B, dtype=torch.int32, device=device)
+    vids = torch.arange(w.B, dtype=torch.int32, device=device)
+    vnext = torch.empty(w.B, dtype=torch.int32, device=device)
+    c = svp.DraftController(w.B, w.k)
+    c.set_cost(bs, 1.0 + np.array([0.02, 0.1, 0.3, 0.9])[:, None] * np.arange(w.k + 1)[None])
+
+    def verify():
+        ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"], inp["T"],
+                   out_tokens=ot, out_len=on, stream=stream)
+
+    def verify_ctrl():
+        verify()
+        c.observe(vids, inp["draft_len"], on, stream=stream)
+        c.choose(vids, vnext, ch, stream=stream)
+    n = max(20, steps // 4)
+    v_ms = _graph_ms(torch, stream, verify, n)
+    vc_ms = _graph_ms(torch, stream, verify_ctrl, n)
+    assert c.status(stream=stream) == svp.SV_OK
+    out.update({"workload": w.describe(), "verify_ms": v_ms, "verify_observe_choose_ms": vc_ms,
+                "controller_overhead_us": (vc_ms - v_ms) * 1e3,
+                "note": "L2 not flushed between rounds (the same inputs each round)"})
+    return out
+
+
 def time_kd(svp, device, stream, steps, warmup, n_seq=64, t_len=64, V=151936):
     """Device-timed calls of the reward-weighted distillation loss on a batch
     of rollouts (bf16, Qwen vocabulary): with the gradient and loss alone.
@@ -494,6 +574,8 @@ def our_arm(args, w):
                          "cluster": on["cfg"]["cluster"]})
             del on, off
         aux["early_exit"] = runs
+    if args.ctrl_steps > 0 and world == 1:
+        aux["draft_controller"] = time_controller(svp, w, device, stream, args.ctrl_steps)
     if args.kd_steps > 0 and world == 1:
         aux["kd_loss"] = time_kd(svp, device, stream, args.kd_steps, max(3, args.warmup // 10), n_seq=args.kd_rollouts)
 

@@ -23,15 +23,18 @@
 // The state (A, N per sequence slot) stays on the device, so a decode loop
 // runs verify -> observe -> choose -> draft without a host round trip and
 // can be captured in one CUDA graph.  The work is B rows of at most 32
-// candidates: one CTA per call, fp64 throughout, each multiply and add
-// rounded on its own (no fused multiply-add), in the order stated above.
+// candidates, in fp64 with each multiply and add rounded on its own (no
+// fused multiply-add), in the order stated above; a per-sequence rate is
+// e_n * (1 / T(B, n)), which may differ from the quotient in the last bit.
 
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <utility>
 
 #include "../../include/specverify.h"
 
@@ -40,8 +43,12 @@ namespace {
 constexpr int kCtrlMaxK = 31;
 constexpr int kCtrlMaxPoints = SV_CTRL_MAX_POINTS;
 constexpr int kObserveThreads = 1024;
-constexpr int kChooseThreads = 256;
+#ifndef SV_CTRL_CHOOSE_THREADS
+#define SV_CTRL_CHOOSE_THREADS 128
+#endif
+constexpr int kChooseThreads = SV_CTRL_CHOOSE_THREADS;
 constexpr int kChooseWarps = kChooseThreads / 32;
+constexpr int kChooseMaxCtas = 1024;
 
 // The round-time table travels by value in the launch parameters (3 KB).
 struct CostTable {
@@ -70,6 +77,9 @@ struct ChooseParams {
   int32_t* next_len;
   int32_t* choice;
   double* alpha_out;          // spec_ctrl_alpha only
+  double* cta_sums;           // [kChooseMaxCtas][kCtrlMaxK + 1]
+  int* cta_max;               // [kChooseMaxCtas]
+  unsigned int* ticket;       // zero between calls
   int B, n_slots, max_k, mode;
   double alpha0, w0;
   CostTable cost;
@@ -94,12 +104,20 @@ __device__ double round_time(const CostTable& c, int B, int n) {
 
 __device__ __forceinline__ bool bad_id(int id, int n_slots) { return id < 0 || id >= n_slots; }
 
+// Programmatic dependent launch: a controller kernel may start while the
+// kernel before it on the stream finishes; it waits here, before its first
+// read of anything that kernel wrote, and lets the next kernel start early.
+__device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void release_successor() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_bits(unsigned int* err, unsigned int bits) {
   bits = __reduce_or_sync(0xffffffffu, bits);
   if ((threadIdx.x & 31) == 0 && bits) atomicOr(err, bits);
 }
 
 __global__ void __launch_bounds__(kObserveThreads) ctrl_observe_kernel(const ObserveParams P) {
+  wait_for_predecessor();
+  release_successor();
   // a slot named twice in one call is an error: count the claims first
   for (int b = threadIdx.x; b < P.B; b += blockDim.x) {
     const int id = P.seq_ids[b];
@@ -132,22 +150,35 @@ __global__ void __launch_bounds__(kObserveThreads) ctrl_observe_kernel(const Obs
   raise_bits(P.err, bits);
 }
 
+// One thread per row, rows spread over up to kChooseMaxCtas CTAs: fp64 runs at
+// a small fraction of the fp32 rate, so the rows must use many SMs.  Batch
+// mode sums E_n per CTA (fixed order), the last CTA to finish adds the CTA
+// sums in CTA order, takes the first maximum of sum / T(B, n) and writes
+// every row's length.
 __global__ void __launch_bounds__(kChooseThreads) ctrl_choose_kernel(const ChooseParams P) {
-  __shared__ double T[kCtrlMaxK + 1];
+  __shared__ double T[kCtrlMaxK + 1], invT[kCtrlMaxK + 1];
+  __shared__ double tile[kCtrlMaxK + 1][kChooseThreads];   // batch mode: E_n of each thread's rows
   __shared__ double part[kChooseWarps][kCtrlMaxK + 1];
   __shared__ int wmax[kChooseWarps];
   __shared__ int best_s;
+  __shared__ bool last_cta;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = P.max_k;
-  if (tid <= K) T[tid] = round_time(P.cost, P.B, tid);
+  if (tid <= K) {
+    T[tid] = round_time(P.cost, P.B, tid);
+    invT[tid] = __ddiv_rn(1.0, T[tid]);
+  }
+  wait_for_predecessor();
+  release_successor();
   __syncthreads();
 
+  const bool batch = (P.mode == SV_CTRL_BATCH) && !P.alpha_out;
   double acc[kCtrlMaxK + 1];
 #pragma unroll
   for (int n = 0; n <= kCtrlMaxK; ++n) acc[n] = 0.0;
   unsigned int bits = 0;
   int top_n = 0;
-  for (int b = tid; b < P.B; b += kChooseThreads) {
+  for (int b = blockIdx.x * kChooseThreads + tid; b < P.B; b += gridDim.x * kChooseThreads) {
     const int id = P.seq_ids[b];
     if (bad_id(id, P.n_slots)) {
       bits |= 1u << SV_ERR_INVALID_ARG;
@@ -168,10 +199,10 @@ __global__ void __launch_bounds__(kChooseThreads) ctrl_choose_kernel(const Choos
       if (n <= K) {
         e = __dadd_rn(e, pw);
         pw = __dmul_rn(pw, alpha);
-        if (P.mode == SV_CTRL_BATCH) {
+        if (batch) {
           acc[n] = __dadd_rn(acc[n], e);
         } else {
-          const double rate = __ddiv_rn(e, T[n]);
+          const double rate = __dmul_rn(e, invT[n]);
           if (rate > best_rate) {
             best_rate = rate;
             best = n;
@@ -179,7 +210,7 @@ __global__ void __launch_bounds__(kChooseThreads) ctrl_choose_kernel(const Choos
         }
       }
     }
-    if (P.mode != SV_CTRL_BATCH) {
+    if (!batch) {
       P.next_len[b] = best;
       top_n = max(top_n, best);
     }
@@ -187,49 +218,91 @@ __global__ void __launch_bounds__(kChooseThreads) ctrl_choose_kernel(const Choos
   raise_bits(P.err, bits);
   if (P.alpha_out) return;
 
-  if (P.mode != SV_CTRL_BATCH) {
+  // this CTA's part: the sums of E_n (batch) or the largest n_b.  Batch
+  // sums go through shared memory so that each warp reduces only its own
+  // share of the n (fp64 adds are the scarce resource here): warp w takes
+  // n = w, w + W, ..., each lane first adds its column of the tile, then the
+  // warp adds the 32 lane sums
+  if (batch) {
+#pragma unroll
+    for (int n = 0; n <= kCtrlMaxK; ++n)
+      if (n <= K) tile[n][tid] = acc[n];
+  } else {
     top_n = __reduce_max_sync(0xffffffffu, top_n);
     if (lane == 0) wmax[warp] = top_n;
-    __syncthreads();
-    if (tid == 0 && P.choice) {
+  }
+  __syncthreads();
+  if (batch) {
+    for (int n = warp; n <= K; n += kChooseWarps) {
+      double v = tile[n][lane];
+#pragma unroll
+      for (int i = 1; i < kChooseThreads / 32; ++i) v = __dadd_rn(v, tile[n][lane + 32 * i]);
+      for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_down_sync(0xffffffffu, v, o));
+      if (lane == 0) P.cta_sums[blockIdx.x * (kCtrlMaxK + 1) + n] = v;
+    }
+  }
+  if (!batch && tid == 0) {
+    int m = 0;
+    for (int w = 0; w < kChooseWarps; ++w) m = max(m, wmax[w]);
+    P.cta_max[blockIdx.x] = m;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last_cta = (atomicAdd(P.ticket, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!last_cta) return;
+  __threadfence();
+
+  if (!batch) {
+    if (tid == 0) {
       int m = 0;
-      for (int w = 0; w < kChooseWarps; ++w) m = max(m, wmax[w]);
-      *P.choice = m;
+      for (int c = 0; c < static_cast<int>(gridDim.x); ++c) m = max(m, __ldcg(&P.cta_max[c]));
+      if (P.choice) *P.choice = m;
+      *P.ticket = 0;
     }
     return;
   }
-  // batch mode: sum E_n over the rows (fixed order for a given B), divide by
-  // T(B, n), take the first maximum
-#pragma unroll
-  for (int n = 0; n <= kCtrlMaxK; ++n) {
-    double v = acc[n];
-    for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_down_sync(0xffffffffu, v, o));
-    if (lane == 0) part[warp][n] = v;
+  if (tid <= K) {
+    double v = 0.0;
+#pragma unroll 8
+    for (int c = 0; c < static_cast<int>(gridDim.x); ++c) v = __dadd_rn(v, __ldcg(&P.cta_sums[c * (kCtrlMaxK + 1) + tid]));
+    part[0][tid] = __ddiv_rn(v, T[tid]);
   }
   __syncthreads();
   if (tid == 0) {
     double top = -1.0;
     int best = 0;
     for (int n = 0; n <= K; ++n) {
-      double s = 0.0;
-      for (int w = 0; w < kChooseWarps; ++w) s = __dadd_rn(s, part[w][n]);
-      const double rate = __ddiv_rn(s, T[n]);
-      if (rate > top) {
-        top = rate;
+      if (part[0][n] > top) {
+        top = part[0][n];
         best = n;
       }
     }
     best_s = best;
     if (P.choice) *P.choice = best;
+    *P.ticket = 0;
   }
   __syncthreads();
   const int best = best_s;
-  for (int b = tid; b < P.B; b += kChooseThreads)
+  const bool vec = ((reinterpret_cast<uintptr_t>(P.seq_ids) | reinterpret_cast<uintptr_t>(P.next_len)) & 15u) == 0;
+  const int B4 = vec ? (P.B & ~3) : 0;
+  for (int b = 4 * tid; b < B4; b += 4 * kChooseThreads) {
+    const int4 id = *reinterpret_cast<const int4*>(P.seq_ids + b);
+    int4 o;
+    o.x = bad_id(id.x, P.n_slots) ? 0 : best;
+    o.y = bad_id(id.y, P.n_slots) ? 0 : best;
+    o.z = bad_id(id.z, P.n_slots) ? 0 : best;
+    o.w = bad_id(id.w, P.n_slots) ? 0 : best;
+    *reinterpret_cast<int4*>(P.next_len + b) = o;
+  }
+  for (int b = B4 + tid; b < P.B; b += kChooseThreads)
     if (!bad_id(P.seq_ids[b], P.n_slots)) P.next_len[b] = best;
 }
 
 __global__ void ctrl_forget_kernel(double* A, double* N, const int32_t* ids, int n, int n_slots,
                                    unsigned int* err) {
+  wait_for_predecessor();
+  release_successor();
   unsigned int bits = 0;
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < n) {
@@ -252,6 +325,9 @@ struct sv_ctrl {
   double* N = nullptr;
   int* claim = nullptr;
   unsigned int* err = nullptr;
+  double* cta_sums = nullptr;
+  int* cta_max = nullptr;
+  unsigned int* ticket = nullptr;
   double decay = 0.9, alpha0 = 0.5, w0 = 2.0;
   int mode = SV_CTRL_BATCH;
   bool has_cost = false;
@@ -265,10 +341,27 @@ void release(sv_ctrl* c) {
   cudaFree(c->N);
   cudaFree(c->claim);
   cudaFree(c->err);
+  cudaFree(c->cta_sums);
+  cudaFree(c->cta_max);
+  cudaFree(c->ticket);
   delete c;
 }
 
-sv_status launched() { return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
+// Launch with programmatic stream serialisation (see wait_for_predecessor).
+template <typename... KArgs, typename... Args>
+sv_status launch_pdl(void (*kernel)(KArgs...), int ctas, int threads, cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -286,7 +379,11 @@ sv_status spec_ctrl_create(sv_ctrl** out, int n_slots, int max_k) {
   if (cudaMalloc(&c->A, n * sizeof(double)) != cudaSuccess || cudaMalloc(&c->N, n * sizeof(double)) != cudaSuccess ||
       cudaMalloc(&c->claim, n * sizeof(int)) != cudaSuccess || cudaMalloc(&c->err, sizeof(unsigned int)) != cudaSuccess ||
       cudaMemset(c->A, 0, n * sizeof(double)) != cudaSuccess || cudaMemset(c->N, 0, n * sizeof(double)) != cudaSuccess ||
-      cudaMemset(c->claim, 0, n * sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, sizeof(unsigned int)) != cudaSuccess) {
+      cudaMemset(c->claim, 0, n * sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, sizeof(unsigned int)) != cudaSuccess ||
+      cudaMalloc(&c->cta_sums, sizeof(double) * kChooseMaxCtas * (kCtrlMaxK + 1)) != cudaSuccess ||
+      cudaMalloc(&c->cta_max, sizeof(int) * kChooseMaxCtas) != cudaSuccess ||
+      cudaMalloc(&c->ticket, sizeof(unsigned int)) != cudaSuccess ||
+      cudaMemset(c->ticket, 0, sizeof(unsigned int)) != cudaSuccess) {
     cudaGetLastError();
     release(c);
     return SV_ERR_CUDA;
@@ -347,8 +444,7 @@ sv_status spec_ctrl_reset(sv_ctrl* c, int n, const int32_t* seq_ids, sv_stream_t
   }
   if (n < 0 || n > c->n_slots) return SV_ERR_INVALID_ARG;
   if (n == 0) return SV_OK;
-  ctrl_forget_kernel<<<(n + 255) / 256, 256, 0, s>>>(c->A, c->N, seq_ids, n, c->n_slots, c->err);
-  return launched();
+  return launch_pdl(ctrl_forget_kernel, (n + 255) / 256, 256, s, c->A, c->N, seq_ids, n, c->n_slots, c->err);
 }
 
 sv_status spec_ctrl_observe(sv_ctrl* c, int B, const int32_t* seq_ids, const int32_t* draft_len,
@@ -357,8 +453,7 @@ sv_status spec_ctrl_observe(sv_ctrl* c, int B, const int32_t* seq_ids, const int
   if (B == 0) return SV_OK;
   if (!seq_ids || !draft_len || !out_len) return SV_ERR_INVALID_ARG;
   ObserveParams p{c->A, c->N, c->claim, c->err, seq_ids, draft_len, out_len, B, c->n_slots, c->max_k, c->decay};
-  ctrl_observe_kernel<<<1, kObserveThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  return launched();
+  return launch_pdl(ctrl_observe_kernel, 1, kObserveThreads, reinterpret_cast<cudaStream_t>(stream), p);
 }
 
 static sv_status launch_choose(sv_ctrl* c, int B, const int32_t* seq_ids, int32_t* next_len, int32_t* choice,
@@ -378,8 +473,12 @@ static sv_status launch_choose(sv_ctrl* c, int B, const int32_t* seq_ids, int32_
   p.alpha0 = c->alpha0;
   p.w0 = c->w0;
   p.cost = c->cost;
-  ctrl_choose_kernel<<<1, kChooseThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  return launched();
+  p.cta_sums = c->cta_sums;
+  p.cta_max = c->cta_max;
+  p.ticket = c->ticket;
+  const int ctas = B < 1 ? 1 : (B + kChooseThreads - 1) / kChooseThreads;
+  return launch_pdl(ctrl_choose_kernel, ctas < kChooseMaxCtas ? ctas : kChooseMaxCtas, kChooseThreads,
+                    reinterpret_cast<cudaStream_t>(stream), p);
 }
 
 sv_status spec_ctrl_choose(sv_ctrl* c, int B, const int32_t* seq_ids, int32_t* next_draft_len, int32_t* choice,
