@@ -92,13 +92,17 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+VERIFY_KERNEL_SOURCES = ("sv_device.cuh", "sv_internal.h", "sv_kernels.cu")
+
+
 def kernel_source_hash():
+    """sha256 (first 16 hex digits) of the files the verify kernel is
+    compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_71_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in VERIFY_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
