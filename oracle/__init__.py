@@ -68,6 +68,8 @@ def _bind(lib):
     lib.oracle_ctrl_round_time.argtypes = [I, P, P, I, I, I]
     lib.oracle_ctrl_choose.restype = I
     lib.oracle_ctrl_choose.argtypes = [I, P, P, I, P, I, D, D, I, I, P, P, P, P, P, P, P]
+    lib.oracle_tree_verify.restype = I
+    lib.oracle_tree_verify.argtypes = [I, I, I, I, P, P, P, P, P, P, D, P, P, P, P, P, P, P, P, P, I]
     return lib
 
 
@@ -269,3 +271,36 @@ class Controller:
 
 def expected_tokens(alpha, n, lib=None):
     return (lib or load()).oracle_ctrl_expected_tokens(float(alpha), int(n))
+
+
+def tree_verify(target, draft, parents, tokens, n_nodes, uniforms, T, final_w=False, nthreads=0, lib=None):
+    """Tree verification (see ``oracle_tree_verify`` in oracle.c).
+
+    target, draft [B,M,V] (fp32 / bf16 as for ``verify``), parents, tokens
+    [B,M] int32, n_nodes [B], uniforms [B,M] float32 (column 0 samples).
+    Returns out_tokens, out_nodes [B,M], out_len [B], status and the fp64
+    diagnostics (alpha [B,M], resid_mass, accept_tie, sample_tie; final_w
+    [B,V] if asked for)."""
+    lib = lib or load()
+    t, dt = _as_np(target)
+    d, dd = _as_np(draft)
+    if dt is None or dt != dd:
+        raise TypeError("target and draft must both be float32 or both be bfloat16")
+    B, M, V = t.shape
+    t, d = np.ascontiguousarray(t), np.ascontiguousarray(d)
+    par = np.ascontiguousarray(_as_np(parents)[0], dtype=np.int32).reshape(B, M)
+    tok = np.ascontiguousarray(_as_np(tokens)[0], dtype=np.int32).reshape(B, M)
+    nn = np.ascontiguousarray(_as_np(n_nodes)[0], dtype=np.int32).reshape(B)
+    u = np.ascontiguousarray(_as_np(uniforms)[0], dtype=np.float32).reshape(B, M)
+    out_tokens = np.empty((B, M), np.int32)
+    out_nodes = np.empty((B, M), np.int32)
+    out_len = np.empty(B, np.int32)
+    alpha = np.empty((B, M))
+    fw = np.empty((B, V)) if final_w else None
+    mass, atie, stie = np.empty(B), np.empty(B), np.empty(B)
+    status = np.empty(B, np.int32)
+    lib.oracle_tree_verify(B, M, V, dt, _ptr(t), _ptr(d), _ptr(par), _ptr(tok), _ptr(nn), _ptr(u), float(T),
+                           _ptr(out_tokens), _ptr(out_nodes), _ptr(out_len), _ptr(alpha), _ptr(fw), _ptr(mass),
+                           _ptr(atie), _ptr(stie), _ptr(status), int(nthreads))
+    return {"out_tokens": out_tokens, "out_nodes": out_nodes, "out_len": out_len, "status": status,
+            "alpha": alpha, "final_w": fw, "resid_mass": mass, "accept_tie": atie, "sample_tie": stie}

@@ -626,3 +626,203 @@ int oracle_ctrl_choose(int n_slots, const double *A, const double *N, int B, con
         *choice = best_all;
     return 0;
 }
+
+/*
+ * Tree verification ("ReSpec: Towards Optimizing Speculative Decoding in
+ * Reinforcement Learning Systems", GAP 1: an SD configuration has a number of
+ * rounds, a branching factor t and a draft length per round; the page gives
+ * no verification rule for branching drafts).  Reading used: recursive
+ * rejection sampling over a draft tree whose children at each node are
+ * independent draws from the drafter's distribution q at that node, the
+ * multi-candidate form of the rule of oracle_verify:
+ *
+ *   start at the root with r = p (the target distribution at the node);
+ *   test the node's children in index order: child c with token x is
+ *     accepted iff u_c < min(1, r(x) / q(x)) (r(x) > 0 = q(x) accepts);
+ *     after a rejection w = max(0, r - q), S = sum_x w (index order), and
+ *     r = w / S for the next child (S = 0: w = r, flagged);
+ *   an accepted child emits its token and the walk continues at it;
+ *   if every child was rejected, y is drawn from the last w, S; a node with
+ *     no children draws the bonus token y from w = p, S = sum p;
+ *   the draw is the inverse CDF of oracle_verify with the one sampling
+ *     uniform s = u[b, 0].
+ * A chain (one child per node) is exactly oracle_verify.  T == 0: the first
+ * child whose token is the first argmax of the node's target row is accepted;
+ * if none, or at a leaf, y is that argmax.
+ *
+ * Shapes: target, draft [B, M, V] (row j: after the path to node j; draft
+ * row j is read only if node j has children), parents, tokens [B, M]
+ * (node 0 is the root; 0 <= parents[j] < j for 1 <= j < n_nodes[b]),
+ * n_nodes [B] in [1, M], uniforms [B, M] (column 0 samples, column j >= 1 is
+ * child j's test).  Outputs: out_tokens [B, M] and out_nodes [B, M] (-1
+ * padded; out_nodes holds the accepted nodes), out_len [B].  Optional (may
+ * be NULL): alpha [B, M] (min(1, r(x)/q(x)) of each tested child, NaN if not
+ * tested; greedy 1 or 0), final_w [B, V] (w / S of the draw), resid_mass [B]
+ * (S of the draw), accept_tie [B] (min |u - alpha| over the tests made, 1 if
+ * none), sample_tie [B], status [B] (2 bad structure, 3 bad token, 4 a row
+ * the walk reads is not finite or all -inf; flag 256: a zero residual).
+ * Only the rows the walk reads are checked.
+ */
+int oracle_tree_verify(int B, int M, int V, int dtype, const void *target, const void *draft,
+                       const int32_t *parents, const int32_t *tokens, const int32_t *n_nodes,
+                       const float *uniforms, double T, int32_t *out_tokens, int32_t *out_nodes,
+                       int32_t *out_len, double *alpha, double *final_w, double *resid_mass,
+                       double *accept_tie, double *sample_tie, int32_t *status, int nthreads)
+{
+    int nerr = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(+ : nerr)
+#endif
+    for (int b = 0; b < B; ++b) {
+        double *zt = (double *)malloc(sizeof(double) * (size_t)V);
+        double *zd = (double *)malloc(sizeof(double) * (size_t)V);
+        double *r = (double *)malloc(sizeof(double) * (size_t)V);
+        double *q = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+        const int32_t *par = parents + (size_t)b * M;
+        const int32_t *tok = tokens + (size_t)b * M;
+        const float *u = uniforms + (size_t)b * M;
+        int32_t *ot = out_tokens + (size_t)b * M;
+        int32_t *on = out_nodes + (size_t)b * M;
+        for (int j = 0; j < M; ++j) {
+            ot[j] = -1;
+            on[j] = -1;
+            if (alpha)
+                alpha[(size_t)b * M + j] = NAN;
+        }
+        out_len[b] = 0;
+        if (final_w)
+            for (int x = 0; x < V; ++x)
+                final_w[(size_t)b * V + x] = NAN;
+        if (resid_mass) resid_mass[b] = NAN;
+        if (accept_tie) accept_tie[b] = 1.0;
+        if (sample_tie) sample_tie[b] = 1.0;
+
+        int st = ORC_OK, flags = 0;
+        const int n = n_nodes[b];
+        if (n < 1 || n > M)
+            st = ORC_BAD_DRAFT_LEN;
+        for (int j = 1; st == ORC_OK && j < n; ++j)
+            if (par[j] < 0 || par[j] >= j)
+                st = ORC_BAD_DRAFT_LEN;
+        for (int j = 1; st == ORC_OK && j < n; ++j)
+            if (tok[j] < 0 || tok[j] >= V)
+                st = ORC_BAD_TOKEN;
+
+        int len = 0, cur = 0, y = -1;
+        double atie = 1.0, stie = 1.0, S = 0.0;
+        while (st == ORC_OK) {
+            load_row(target, dtype, (size_t)b * M + cur, V, zt);
+            if (!row_is_valid(zt, V)) {
+                st = ORC_NONFINITE;
+                break;
+            }
+            int has_children = 0;
+            for (int c = cur + 1; c < n; ++c)
+                if (par[c] == cur)
+                    has_children = 1;
+            if (has_children) {
+                load_row(draft, dtype, (size_t)b * M + cur, V, zd);
+                if (!row_is_valid(zd, V)) {
+                    st = ORC_NONFINITE;
+                    break;
+                }
+            }
+            if (T == 0.0) {
+                const int am = first_argmax(zt, V);
+                int next = -1;
+                for (int c = cur + 1; c < n && next < 0; ++c)
+                    if (par[c] == cur) {
+                        const int ok = (tok[c] == am);
+                        if (alpha) alpha[(size_t)b * M + c] = ok ? 1.0 : 0.0;
+                        if (ok) next = c;
+                    }
+                if (next < 0) {
+                    y = am;
+                    break;
+                }
+                on[len] = next;
+                ot[len++] = tok[next];
+                cur = next;
+                continue;
+            }
+            double mt, Lt;
+            row_stats(zt, V, T, &mt, &Lt);
+            for (int x = 0; x < V; ++x)
+                r[x] = prob_of(zt[x], mt, Lt, T);
+            if (!has_children) {
+                /* bonus token from p */
+                S = 0.0;
+                for (int x = 0; x < V; ++x) {
+                    w[x] = r[x];
+                    S += w[x];
+                }
+                break;
+            }
+            double md, Ld;
+            row_stats(zd, V, T, &md, &Ld);
+            for (int x = 0; x < V; ++x)
+                q[x] = prob_of(zd[x], md, Ld, T);
+            int next = -1;
+            for (int c = cur + 1; c < n; ++c) {
+                if (par[c] != cur)
+                    continue;
+                const int x = tok[c];
+                const double ratio = (q[x] == 0.0) ? (r[x] > 0.0 ? INFINITY : 0.0) : r[x] / q[x];
+                const double al = ratio < 1.0 ? ratio : 1.0;
+                if (alpha) alpha[(size_t)b * M + c] = al;
+                const double d = fabs((double)u[c] - al);
+                if (d < atie) atie = d;
+                if ((double)u[c] < al) {
+                    next = c;
+                    break;
+                }
+                S = 0.0;
+                for (int xx = 0; xx < V; ++xx) {
+                    const double v = r[xx] - q[xx];
+                    w[xx] = v > 0.0 ? v : 0.0;
+                    S += w[xx];
+                }
+                if (S == 0.0) {
+                    flags |= ORC_FLAG_ZERO_RESIDUAL;
+                    S = 0.0;
+                    for (int xx = 0; xx < V; ++xx) {
+                        w[xx] = r[xx];
+                        S += w[xx];
+                    }
+                }
+                for (int xx = 0; xx < V; ++xx)
+                    r[xx] = w[xx] / S;
+            }
+            if (next < 0)
+                break;                  /* every child rejected: draw from w, S */
+            on[len] = next;
+            ot[len++] = tok[next];
+            cur = next;
+        }
+        if (st == ORC_OK && T > 0.0) {
+            y = inverse_cdf(w, V, S, (double)u[0], &stie);
+            if (final_w)
+                for (int x = 0; x < V; ++x)
+                    final_w[(size_t)b * V + x] = w[x] / S;
+            if (resid_mass) resid_mass[b] = S;
+        }
+        if (st == ORC_OK) {
+            ot[len++] = y;
+            out_len[b] = len;
+            if (accept_tie) accept_tie[b] = atie;
+            if (sample_tie) sample_tie[b] = stie;
+        } else {
+            for (int j = 0; j < M; ++j) {
+                ot[j] = -1;
+                on[j] = -1;
+            }
+            nerr += 1;
+        }
+        if (status) status[b] = st != ORC_OK ? st : flags;
+        free(zt); free(zd); free(r); free(q); free(w);
+    }
+    return nerr;
+}
