@@ -281,6 +281,58 @@ sv_status spec_verify_noalloc(int B, int k, int V, sv_dtype dtype,
                               sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Tree verification.
+ *
+ * "ReSpec: Towards Optimizing Speculative Decoding in Reinforcement Learning
+ * Systems" (GAP 1) describes an SD configuration by its rounds, a branching
+ * factor and a draft length per round, without a rule for verifying
+ * branching drafts.  The rule implemented (recursive rejection sampling, the
+ * multi-candidate form of spec_verify's rule, exact when the children of a
+ * node are independent draws from the drafter's q at that node):
+ *   at node j (starting at the root, node 0) let r = p_j = softmax(z^t_j / T);
+ *   test the children c of j in index order: accept c (token x) iff
+ *     u[b, c] < min(1, r(x) / q_j(x)) (r(x) > 0 = q_j(x) accepts);
+ *     after a rejection r <- max(0, r - q_j) / S with S its mass (if S = 0, r
+ *     is kept);
+ *   an accepted child emits its token and the walk moves to it;
+ *   if every child of j is rejected, y is drawn from the last residual; at a
+ *     node without children y is the bonus token drawn from p_j;
+ *   the draw is the inverse CDF in ascending token id with s = u[b, 0].
+ * A chain (one child per node) is exactly spec_verify.  temperature == 0:
+ * accept the first child whose token is the first argmax of z^t_j; y is that
+ * argmax where none is.
+ *
+ * Layout (device memory, caller-owned; M = max_nodes <= SV_TREE_MAX_NODES):
+ *   target_logits [B, M, V]: row j = target logits after the path to node j;
+ *   draft_logits  [B, M, V]: row j = the drafter's logits from which node j's
+ *                 children were drawn (read only for nodes with children);
+ *   parents [B, M] (0 <= parents[b, j] < j for 1 <= j < n_nodes[b]; entry 0
+ *   unused), tokens [B, M] (entry 0 unused), n_nodes [B] in [1, M],
+ *   uniforms [B, M] in [0, 1) (column 0 samples, column j tests child j);
+ *   out_tokens, out_nodes [B, M] (-1 padded): the accepted tokens and their
+ *   nodes, then y (out_nodes has no entry for y); out_len [B] = accepted + 1;
+ *   status [B] (may be NULL): SV_OK, SV_ERR_BAD_DRAFT_LEN (n_nodes or a
+ *   parent out of range), SV_ERR_BAD_TOKEN, SV_ERR_NONFINITE (NaN or +inf in
+ *   a row the walk reads, or such a row all -inf); a sequence with an error
+ *   emits nothing (out_len 0, tokens -1);
+ *   alpha [B, M] (may be NULL): min(1, r(x)/q(x)) of each tested child, NaN
+ *   for the others (greedy: 1 or 0).
+ * Only the rows on the walk are read.  No context and no workspace: the call
+ * allocates nothing and can be captured in a CUDA graph.  Host-checkable
+ * errors (sizes, dtype, temperature < 0 or not finite, NULL pointers) return
+ * SV_ERR_INVALID_ARG and launch nothing.  V <= 524288.
+ * ------------------------------------------------------------------------ */
+
+#define SV_TREE_MAX_NODES 64
+
+sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtype,
+                           const void *target_logits, const void *draft_logits,
+                           const int32_t *parents, const int32_t *tokens, const int32_t *n_nodes,
+                           const float *uniforms, float temperature,
+                           int32_t *out_tokens, int32_t *out_nodes, int32_t *out_len,
+                           int32_t *status, float *alpha, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Draft-length controller and speculation toggle.
  *
  * "EfficientRollout: System-Aware Self-Speculative Decoding for RL Rollouts"

@@ -24,7 +24,7 @@ __all__ = [
     "SpecVerifier", "SpecVerifyError", "Stats", "load_library", "library_path",
     "SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_BAD_DRAFT_LEN", "SV_ERR_BAD_TOKEN",
     "SV_ERR_NONFINITE", "SV_ERR_TIMEOUT", "SV_ERR_CUDA", "SV_ERR_UNSUPPORTED",
-    "SV_F32", "SV_BF16", "EXPORTED_SYMBOLS", "DraftController", "SV_CTRL_BATCH", "SV_CTRL_PER_SEQUENCE",
+    "SV_F32", "SV_BF16", "EXPORTED_SYMBOLS", "DraftController", "verify_tree", "SV_CTRL_BATCH", "SV_CTRL_PER_SEQUENCE",
 ]
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_BAD_DRAFT_LEN, SV_ERR_BAD_TOKEN = 0, 1, 2, 3
@@ -45,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
     "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_set_cost", "spec_ctrl_set_params", "spec_ctrl_reset",
     "spec_ctrl_observe", "spec_ctrl_choose", "spec_ctrl_alpha", "spec_ctrl_status",
+    "spec_verify_tree",
 )
 
 
@@ -137,6 +138,9 @@ def load_library(path: str | None = None):
     lib.spec_ctrl_alpha.argtypes = [P, c.c_int, P, P, P]
     lib.spec_ctrl_status.restype = c.c_int
     lib.spec_ctrl_status.argtypes = [P, P]
+    lib.spec_verify_tree.restype = c.c_int
+    lib.spec_verify_tree.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, P, P, P, c.c_float,
+                                     P, P, P, P, P, P]
     lib.spec_verify_noalloc.restype = c.c_int
     lib.spec_verify_noalloc.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, P, P, c.c_float, P, P, P]
     if path is None:
@@ -491,3 +495,43 @@ class DraftController:
         """The sticky device error (SV_OK, SV_ERR_INVALID_ARG or
         SV_ERR_BAD_DRAFT_LEN); synchronises the stream."""
         return self.lib.spec_ctrl_status(self._c, _stream_handle(stream))
+
+
+SV_TREE_MAX_NODES = 64
+
+
+def verify_tree(target, draft, parents, tokens, n_nodes, uniforms, temperature, out_tokens=None, out_nodes=None,
+                out_len=None, status=None, alpha=None, stream=None):
+    """Tree verification (``spec_verify_tree`` in include/specverify.h).
+
+    target, draft [B, M, V] (float32 or bfloat16), parents, tokens [B, M]
+    int32, n_nodes [B] int32, uniforms [B, M] float32 (column 0 samples).
+    Returns (out_tokens [B, M], out_nodes [B, M], out_len [B], status [B])
+    int32 and, if given, fills alpha [B, M] float32."""
+    lib = load_library()
+    B, M, V = target.shape
+    dtype = target.dtype
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("logits must be float32 or bfloat16")
+    dev = target.device
+    _check_dev("target", target, dtype, (B, M, V), dev)
+    _check_dev("draft", draft, dtype, (B, M, V), dev)
+    _check_dev("parents", parents, torch.int32, (B, M), dev)
+    _check_dev("tokens", tokens, torch.int32, (B, M), dev)
+    _check_dev("n_nodes", n_nodes, torch.int32, (B,), dev)
+    _check_dev("uniforms", uniforms, torch.float32, (B, M), dev)
+    mk = lambda t, shape: t if t is not None else torch.empty(shape, dtype=torch.int32, device=dev)
+    out_tokens, out_nodes = mk(out_tokens, (B, M)), mk(out_nodes, (B, M))
+    out_len, status = mk(out_len, (B,)), mk(status, (B,))
+    for name, t, shape in (("out_tokens", out_tokens, (B, M)), ("out_nodes", out_nodes, (B, M)),
+                           ("out_len", out_len, (B,)), ("status", status, (B,))):
+        _check_dev(name, t, torch.int32, shape, dev)
+    if alpha is not None:
+        _check_dev("alpha", alpha, torch.float32, (B, M), dev)
+    st = lib.spec_verify_tree(B, M, V, SV_BF16 if dtype == torch.bfloat16 else SV_F32, _ptr(target), _ptr(draft),
+                              _ptr(parents), _ptr(tokens), _ptr(n_nodes), _ptr(uniforms), float(temperature),
+                              _ptr(out_tokens), _ptr(out_nodes), _ptr(out_len), _ptr(status), _ptr(alpha),
+                              _stream_handle(stream))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_tree")
+    return out_tokens, out_nodes, out_len, status

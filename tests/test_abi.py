@@ -102,3 +102,15 @@ def test_controller_host_checks(lib):
     assert lib.spec_ctrl_choose(P, 1, P, P, P, P) == svp.SV_ERR_INVALID_ARG
     assert lib.spec_ctrl_alpha(P, 1, P, P, P) == svp.SV_ERR_INVALID_ARG
     assert lib.spec_ctrl_status(P, P) == svp.SV_ERR_INVALID_ARG
+
+
+def test_tree_host_checks(lib):
+    P = None
+    # sizes, dtype, temperature and pointers are checked before any launch
+    assert lib.spec_verify_tree(1, 0, 10, 1, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_tree(1, 65, 10, 1, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_tree(1, 4, 0, 1, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_tree(1, 4, 10, 7, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_tree(1, 4, 10, 1, P, P, P, P, P, P, -1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_tree(1, 4, 10, 1, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
+    assert lib.spec_verify_tree(0, 4, 10, 1, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_OK

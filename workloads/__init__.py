@@ -41,6 +41,8 @@ from .philox import philox_uniforms, philox4x32_10  # noqa: F401
 __all__ = [
     "Workload", "WORKLOADS", "get_workload", "make_inputs", "make_tables",
     "philox_uniforms", "philox4x32_10", "gumbel_argmax_tokens", "algorithmic_bytes",
+    "TreeWorkload", "TREE_WORKLOADS", "get_tree_workload", "tree_parents", "tree_algorithmic_bytes",
+    "make_tree_inputs",
 ]
 
 
@@ -230,3 +232,136 @@ def make_tables(rng: np.random.Generator, V: int, depth: int, scale: float = 1.5
                 nxt.append(p)
         frontier = nxt
     return tab
+
+
+# --- draft trees ----------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class TreeWorkload:
+    """A batch of draft trees.  ``branching`` gives the children of every
+    node per level (a full tree in breadth-first order: node 0 is the root,
+    parents precede children); ``ragged`` keeps a random prefix of 1..M nodes
+    per sequence (a prefix of a breadth-first order is itself a tree)."""
+    name: str
+    B: int
+    branching: tuple
+    V: int
+    dtype: str
+    T: float
+    kind: str
+    draft_sigma: float
+    ragged: bool = False
+    seed: int = 0
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def elt(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    @property
+    def M(self) -> int:
+        return len(tree_parents(self.branching))
+
+    def describe(self) -> str:
+        shape = "x".join(str(t) for t in self.branching)
+        nodes = f"1..{self.M} nodes" if self.ragged else f"{self.M} nodes"
+        return f"{self.name}: B={self.B} branching {shape} ({nodes}) V={self.V} {self.dtype} T={self.T}"
+
+
+TREE_WORKLOADS = {
+    # ReSpec-style configuration: branching 2 over 3 levels (15 nodes), Qwen
+    # vocabulary, the same logit recipe as qwen_b32
+    "tree": TreeWorkload("tree", 64, (2, 2, 2), 151936, "bf16", 1.0, "peaked", 1.0, seed=6),
+    # wider first level, ragged node counts, Llama-3 vocabulary
+    "tree_wide": TreeWorkload("tree_wide", 128, (4, 2), 128256, "bf16", 1.0, "peaked", 0.7, ragged=True, seed=7),
+}
+
+
+def get_tree_workload(name: str, **overrides) -> TreeWorkload:
+    w = TREE_WORKLOADS[name]
+    return dataclasses.replace(w, **overrides) if overrides else w
+
+
+def tree_parents(branching) -> list:
+    """Parents of a full tree with ``branching[l]`` children per node of
+    level l, in breadth-first order (parents[0] = -1)."""
+    parents, level = [-1], [0]
+    for t in branching:
+        nxt = []
+        for p in level:
+            for _ in range(t):
+                parents.append(p)
+                nxt.append(len(parents) - 1)
+        level = nxt
+    return parents
+
+
+def tree_algorithmic_bytes(visited_t: int, visited_d: int, B: int, M: int, V: int, elt: int) -> int:
+    """Bytes a tree verification must move once: the target rows of the
+    visited nodes and the draft rows of the visited nodes with children, the
+    small inputs (parents, tokens, n_nodes, uniforms) and the outputs."""
+    small = B * M * 4 * 3 + B * 4
+    outs = B * M * 4 * 2 + B * 4 * 2
+    return (visited_t + visited_d) * V * elt + small + outs
+
+
+def make_tree_inputs(w: TreeWorkload, device="cpu", seed=None, B=None, uniform_seed=0):
+    """Inputs of tree workload ``w``: target, draft [B, M, V], parents,
+    tokens [B, M] int32, n_nodes [B] int32, uniforms [B, M] float32
+    (Philox, counter b*M + j; column 0 samples).  Each child's token is a
+    draw from softmax(z^d/T) of its parent's draft row (T = 1 for greedy
+    workloads).  Draft rows of nodes without children and every row past a
+    sequence's last node are NaN: they must never be read."""
+    B = w.B if B is None else B
+    V = w.V
+    par = tree_parents(w.branching)
+    M = len(par)
+    g = _gen(device, w.seed if seed is None else seed)
+    rows = B * M
+    if w.kind == "peaked":
+        zt = _peaked_rows(rows, V, g, device)
+    elif w.kind == "normal":
+        zt = torch.randn(rows, V, generator=g, device=device) * 2.0
+    else:
+        raise ValueError(w.kind)
+    target = zt.to(w.torch_dtype).view(B, M, V)
+    del zt
+    draft = torch.empty(B, M, V, dtype=w.torch_dtype, device=device)
+    for b in range(0, B, 32):
+        e = min(B, b + 32)
+        noise = torch.randn(e - b, M, V, generator=g, device=device) * w.draft_sigma
+        draft[b:e] = (target[b:e].float() + noise).to(w.torch_dtype)
+    if w.ragged:
+        n_nodes = torch.randint(1, M + 1, (B,), generator=g, device=device, dtype=torch.int64).to(torch.int32)
+    else:
+        n_nodes = torch.full((B,), M, dtype=torch.int32, device=device)
+    parents = torch.tensor(par, dtype=torch.int32, device=device).view(1, M).repeat(B, 1)
+    # child j's token: one draw from its parent's draft distribution
+    pidx = torch.tensor([max(p, 0) for p in par], dtype=torch.long, device=device)
+    tokens = torch.zeros(B, M, dtype=torch.int32, device=device)
+    for b in range(0, B, 32):
+        e = min(B, b + 32)
+        src = draft[b:e, pidx].reshape((e - b) * M, V)
+        tokens[b:e] = gumbel_argmax_tokens(src, w.T if w.T > 0 else 1.0, g).view(e - b, M)
+    tokens[:, 0] = 0
+    # poison what must not be read
+    node = torch.arange(M, device=device).view(1, M)
+    has_kids = torch.zeros(M, dtype=torch.bool, device=device)
+    for j in range(1, M):
+        has_kids[par[j]] = True
+    beyond = node >= n_nodes.view(B, 1).long()
+    kid_in = torch.zeros(B, M, dtype=torch.bool, device=device)
+    for j in range(1, M):
+        kid_in[:, par[j]] |= j < n_nodes.long()
+    target[beyond] = float("nan")
+    draft[beyond | ~kid_in] = float("nan")
+    u = philox_uniforms(B * M, seed=uniform_seed).reshape(B, M)
+    return {
+        "target": target.contiguous(), "draft": draft.contiguous(), "parents": parents.contiguous(),
+        "tokens": tokens.contiguous(), "n_nodes": n_nodes.contiguous(),
+        "uniforms": torch.from_numpy(u).to(device).contiguous(), "T": w.T,
+        "meta": {"workload": w, "B": B, "M": M, "V": V},
+    }
