@@ -61,11 +61,15 @@ def parse():
     ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
     ap.add_argument("--kd-steps", type=int, default=100, help="timed calls of the distillation loss (0 = skip)")
     ap.add_argument("--kd-only", action="store_true", help="time only the distillation loss and print its line")
+    ap.add_argument("--tree-only", action="store_true", help="time only tree verification and print its line")
     ap.add_argument("--early-exit-workload", default="long_draft",
                     help="workload timed with and without early exit in the aux block ('' = skip)")
     ap.add_argument("--early-exit-sigmas", default="1.5,4.0",
                     help="drafter noise levels of that workload (a noisier drafter is rejected earlier)")
     ap.add_argument("--kd-rollouts", type=int, default=64, help="rollouts of the distillation batch")
+    ap.add_argument("--tree-steps", type=int, default=100,
+                    help="timed calls of tree verification per tree workload (0 = skip)")
+    ap.add_argument("--tree-workloads", default="tree,tree_wide", help="tree workloads timed in the aux block")
     ap.add_argument("--ctrl-steps", type=int, default=200,
                     help="timed rounds of the draft-length controller (0 = skip)")
     return ap.parse_args()
@@ -361,6 +365,55 @@ def _graph_ms(torch, stream, fn, steps):
     return a.elapsed_time(b) / steps
 
 
+def time_tree(svp, name, device, stream, steps, rotate=4):
+    """Tree verification on `rotate` seeded input sets (each larger than L2,
+    replayed in turn from one CUDA graph).  Algorithmic bytes: the target
+    rows of the visited nodes and the draft rows of the visited nodes with
+    children, counted from each set's outputs."""
+    import torch
+
+    from workloads import get_tree_workload, make_tree_inputs, tree_algorithmic_bytes
+
+    w = get_tree_workload(name)
+    sets = [make_tree_inputs(w, device=device, seed=w.seed + 100 * i, uniform_seed=i) for i in range(rotate)]
+    B, M, V = sets[0]["target"].shape
+    outs = [tuple(torch.empty(shape, dtype=torch.int32, device=device) for shape in ((B, M), (B, M), (B,), (B,)))
+            for _ in range(rotate)]
+    it = [0]
+
+    def call():
+        i = it[0] % rotate
+        it[0] += 1
+        s_ = sets[i]
+        svp.verify_tree(s_["target"], s_["draft"], s_["parents"], s_["tokens"], s_["n_nodes"], s_["uniforms"],
+                        s_["T"], *outs[i], stream=stream)
+    n = max(rotate, (steps // rotate) * rotate)
+    ms = _graph_ms(torch, stream, call, n)
+    nbytes, nodes, emitted = [], [], []
+    for s_, o in zip(sets, outs):
+        par = s_["parents"].cpu().numpy()
+        nn = s_["n_nodes"].cpu().numpy()
+        on = o[1].cpu().numpy()
+        ol = o[2].cpu().numpy()
+        st = o[3].cpu().numpy()
+        assert (st == 0).all(), st
+        vt = vd = 0
+        for b in range(B):
+            visited = [0] + [int(x) for x in on[b, :ol[b] - 1]]
+            vt += len(visited)
+            kids = set(int(p) for p in par[b, 1:nn[b]])
+            vd += sum(1 for v in visited if v in kids)
+        nbytes.append(tree_algorithmic_bytes(vt, vd, B, M, V, w.elt))
+        nodes.append(int(nn.sum()))
+        emitted.append(float(ol.mean()))
+    mb = float(np.mean(nbytes))
+    peak, kind = measured_peak()
+    return {"workload": w.describe(), "kernel": "tree_kernel", "ms_per_call": ms,
+            "nodes_per_s": float(np.mean(nodes)) / (ms / 1e3), "mean_emitted": float(np.mean(emitted)),
+            "algorithmic_bytes": mb, "gbs": mb / (ms / 1e3) / 1e9, "frac_of_peak": mb / (ms / 1e3) / 1e9 / peak,
+            "peak_source": kind, "l2": f"{rotate} rotating input sets, each larger than L2"}
+
+
 def time_controller(svp, w, device, stream, steps):
     """The draft-length controller: one round (observe + choose) alone at a
     GRPO-sized batch, and its cost on top of the verification step of
@@ -578,6 +631,9 @@ def our_arm(args, w):
                          "cluster": on["cfg"]["cluster"]})
             del on, off
         aux["early_exit"] = runs
+    if args.tree_steps > 0 and world == 1:
+        aux["tree_verify"] = [time_tree(svp, t, device, stream, args.tree_steps)
+                              for t in args.tree_workloads.split(",") if t]
     if args.ctrl_steps > 0 and world == 1:
         aux["draft_controller"] = time_controller(svp, w, device, stream, args.ctrl_steps)
     if args.kd_steps > 0 and world == 1:
@@ -641,12 +697,30 @@ def kd_only(args):
     print(json.dumps({"kd_loss": out}), flush=True)
 
 
+def tree_only(args):
+    """Tree verification alone (for profiling it): one JSON line."""
+    import torch
+
+    import speculative_decoding_verification_71_gb300 as svp
+    from speculative_decoding_verification_71_gb300 import build as svbuild
+
+    svbuild.build()
+    svp.load_library()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream()
+    out = [time_tree(svp, t, device, stream, max(4, args.tree_steps)) for t in args.tree_workloads.split(",") if t]
+    print(json.dumps({"tree_verify": out}), flush=True)
+
+
 def main():
     args = parse()
     from workloads import get_workload
     w = get_workload(args.workload)
     if args.kd_only:
         kd_only(args)
+    elif args.tree_only:
+        tree_only(args)
     elif args.impl == "reference":
         reference_arm(args, w)
     else:

@@ -16,7 +16,8 @@
 //   s = u[b, 0]; T == 0 accepts the first child equal to the first argmax of
 //   the node's target row and emits that argmax.
 //
-// One CTA walks one sequence.  Each visited node costs one pass over its
+// One CTA walks one sequence (its warps stream the rows through a cp.async
+// ring in shared memory, see Chunks).  Each visited node costs one pass over its
 // target row (and draft row, if it has children) for the row maximum and
 // log-sum of 2^(z c), one more pass over both rows per rejected child (the
 // residual mass, with the sums of 256-logit chunks kept for the draw), and
@@ -82,6 +83,78 @@ struct Rows {
   }
 };
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+// Calls f(c, e0, zt[8], zd[8]) for each chunk c of this warp (c = warp,
+// warp + W, ...), zt / zd being the lane's eight logits of the target and
+// (if `both`) draft rows from e0.  Each lane streams its own 16 (bf16) or 32
+// (fp32) bytes per row and chunk through a ring of D slots in shared memory
+// with cp.async, D chunks ahead of its use: every lane reads back only what
+// it copied itself, so no barrier is needed, and a slot is refilled only
+// after its logits were consumed.  Lanes past V or on rows that are not
+// 16-byte aligned read their logits with plain loads instead.
+template <int ELT>
+struct Chunks {
+  static constexpr int D = ELT == 2 ? 8 : 4;      // chunks in flight per warp
+  static constexpr int LB = 8 * ELT;               // bytes per lane, row and chunk
+  static constexpr int kRingBytes = kTreeWarps * D * 2 * 32 * LB;
+  __device__ __forceinline__ static unsigned char* slot(unsigned char* ring, int warp, int s, int row, int lane) {
+    return ring + ((((warp * D + s) * 2 + row) * 32 + lane) * LB);
+  }
+  template <typename F>
+  __device__ __forceinline__ static void each(unsigned char* ring, const unsigned char* rt, const unsigned char* rd,
+                                              bool both, int nch, int V, int vec, F&& f) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int mine = warp < nch ? (nch - warp + kTreeWarps - 1) / kTreeWarps : 0;
+    auto issue = [&](int i) {
+      const int c = warp + i * kTreeWarps;
+      const int e0 = c * kChunkElems + lane * 8;
+      if (i < mine && vec && e0 + 8 <= V) {
+        const int sl = i % D;
+#pragma unroll
+        for (int w = 0; w < LB / 16; ++w) {
+          cp_async16(slot(ring, warp, sl, 0, lane) + 16 * w, rt + static_cast<size_t>(e0) * ELT + 16 * w);
+          if (both) cp_async16(slot(ring, warp, sl, 1, lane) + 16 * w, rd + static_cast<size_t>(e0) * ELT + 16 * w);
+        }
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < D; ++i) issue(i);
+    for (int i = 0; i < mine; ++i) {
+      cp_async_wait<D - 1>();                      // chunk i has landed
+      const int c = warp + i * kTreeWarps;
+      const int e0 = c * kChunkElems + lane * 8;
+      float zt[8], zd[8];
+      if (vec && e0 + 8 <= V) {
+        const int sl = i % D;
+        unpack(slot(ring, warp, sl, 0, lane), zt);
+        if (both) unpack(slot(ring, warp, sl, 1, lane), zd);
+      } else {
+        Rows<ELT>::load8(rt, e0, V, 0, zt);
+        if (both) Rows<ELT>::load8(rd, e0, V, 0, zd);
+      }
+      f(c, e0, zt, zd);
+      issue(i + D);
+    }
+    cp_async_wait<0>();
+  }
+  __device__ __forceinline__ static void unpack(const unsigned char* p, float (&v)[8]) {
+    if (ELT == 2) {
+      Vec<2>::unpack(*reinterpret_cast<const uint4*>(p), v);
+    } else {
+      const uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
+      v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+      v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+    }
+  }
+};
+
 // Per-CTA scratch for the walk.
 struct TreeShared {
   int par[kTreeMaxNodes], tok[kTreeMaxNodes];
@@ -89,13 +162,11 @@ struct TreeShared {
   int kids[kTreeMaxNodes];
   int nkids, n, cur, len, st, next, y;
   float csum[kTreeMaxChunks];        // chunk sums of the last weight pass
-  double S[kTreeMaxNodes + 1];       // S[i]: mass after the i-th rejection at this node
-  float invS[kTreeMaxNodes + 1];
-  int fb[kTreeMaxNodes + 1];         // 1: that rejection kept r (zero residual)
+  double cc, PP;                     // residual after the rejections so far: max(0, p - cc q) / PP
+  float wA, wB;                      // weights of the last pass: max(0, A 2^(z^t c - K^t) - B 2^(z^d c - K^d))
   float wm[kTreeWarps], ws[kTreeWarps], wmd[kTreeWarps], wsd[kTreeWarps];
   int wbad[kTreeWarps], widx[kTreeWarps];
   float Kt, St, Kd, Sd;              // row statistics of the current node
-  float invSt, invSd;
   double total;                      // mass of the last weight pass
 };
 
@@ -103,10 +174,8 @@ struct TreeShared {
 __device__ __forceinline__ void online8(const float (&z)[8], float c2, float& m, float& K, float& s, int& bad) {
   float vm = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    bad |= (z[j] != z[j]) || (z[j] == INFINITY);
-    vm = fmaxf(vm, z[j]);
-  }
+  for (int j = 0; j < 8; ++j) vm = fmax_nan(vm, z[j]);     // NaN survives the maximum
+  bad |= (vm != vm) || (vm == INFINITY);
   if (vm > m) {
     const float Kn = vm * c2;
     s = (m == -INFINITY) ? 0.f : s * fast_exp2(K - Kn);
@@ -147,18 +216,19 @@ __device__ void combine_stats(TreeShared& sh, float m, float K, float s, float& 
   }
 }
 
-// The weight of one logit pair in the current weight pass.
-//   mode 0: bonus weight 2^(z^t c - K^t) (unnormalised p);
-//   mode 1: max(0, r_i - q) after i = nrej rejections (fb: r kept);
-//   mode 2: r_i itself (the zero-residual fallback).
-__device__ __forceinline__ float weight_of(const TreeShared& sh, int mode, int nrej, float zt, float zd, float c2) {
-  const float pe = fast_exp2(fmaf(zt, c2, -sh.Kt));
-  if (mode == 0) return pe;
-  const float p = pe * sh.invSt;
-  const float q = fast_exp2(fmaf(zd, c2, -sh.Kd)) * sh.invSd;
-  float r = p;
-  for (int h = 1; h <= nrej; ++h) r = (sh.fb[h] ? r : fmaxf(r - q, 0.f)) * sh.invS[h];
-  return mode == 2 ? r : fmaxf(r - q, 0.f);
+// Residual after h rejections at a node, in closed form: with r_1 = p and
+// r_{h+1} = max(0, r_h - q) / S_h (or r_h / S_h when S_h was zero and r was
+// kept), r_{h+1} = max(0, p - c_h q) / P_h where c_0 = 0, P_0 = 1,
+// c_h = c_{h-1} + P_{h-1} (c unchanged when r was kept), P_h = P_{h-1} S_h.
+// A weight pass therefore needs, per logit pair, only
+//   w = max(0, A e^t - B e^d),  e = 2^(z c - K) (unnormalised p and q),
+// with A, B fixed for the pass: the bonus weights are A = 1, B = 0; the
+// residual after one more rejection A = 1 / (S^t P), B = (c + P) / (S^d P);
+// r itself (zero-residual fallback) A = 1 / (S^t P), B = c / (S^d P).
+__device__ __forceinline__ float pair_weight(float zt, float zd, float c2, float Kt, float Kd, float A, float B) {
+  const float et = fast_exp2(fmaf(zt, c2, -Kt));
+  const float ed = fast_exp2(fmaf(zd, c2, -Kd));
+  return fmaxf(fmaf(A, et, -B * ed), 0.f);
 }
 
 // Fixed-order fp64 total of the chunk sums: lane l adds chunks
@@ -176,23 +246,32 @@ __device__ __forceinline__ double chunk_total(const TreeShared& sh, int nch, int
 
 // One pass of weights over the current node's rows: chunk sums into
 // sh.csum, the fixed-order fp64 total into sh.total.
+//   mode 0: bonus weights (A = 1, B = 0; the draft row is not read);
+//   mode 1: the residual after one more rejection;
+//   mode 2: the current residual r itself (zero-residual fallback).
 template <int ELT>
-__device__ void weight_pass(TreeShared& sh, const TreeParams& P, const unsigned char* rt, const unsigned char* rd,
-                            int mode, int nrej, int nch) {
+__device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParams& P, const unsigned char* rt,
+                            const unsigned char* rd, int mode, int nch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int V = P.V;
-  for (int c = warp; c < nch; c += kTreeWarps) {
-    const int e0 = c * kChunkElems + lane * 8;
-    float zt[8], zd[8];
-    Rows<ELT>::load8(rt, e0, V, P.vec, zt);
-    if (mode != 0) Rows<ELT>::load8(rd, e0, V, P.vec, zd);
+  if (threadIdx.x == 0) {
+    if (mode == 0) {
+      sh.wA = 1.f;
+      sh.wB = 0.f;
+    } else {
+      const double den = 1.0 / sh.PP;
+      sh.wA = static_cast<float>(den / static_cast<double>(sh.St));
+      sh.wB = static_cast<float>((mode == 1 ? sh.cc + sh.PP : sh.cc) * den / static_cast<double>(sh.Sd));
+    }
+  }
+  __syncthreads();
+  const float c2 = P.c2, Kt = sh.Kt, Kd = sh.Kd, A = sh.wA, B = sh.wB;
+  Chunks<ELT>::each(ring, rt, rd, mode != 0, nch, P.V, P.vec, [&](int c, int, const float (&zt)[8], const float (&zd)[8]) {
     float part = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (e0 + j < V) part += weight_of(sh, mode, nrej, zt[j], mode != 0 ? zd[j] : 0.f, P.c2);
+    for (int j = 0; j < 8; ++j) part += pair_weight(zt[j], mode != 0 ? zd[j] : -INFINITY, c2, Kt, Kd, A, B);
     part = warp_sum(part);
     if (lane == 0) sh.csum[c] = part;
-  }
+  });
   __syncthreads();
   if (warp == 0) {
     double excl;
@@ -209,7 +288,7 @@ __device__ void weight_pass(TreeShared& sh, const TreeParams& P, const unsigned 
 // the chunk (or of the row) takes the last logit with weight there.
 template <int ELT>
 __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt, const unsigned char* rd, int mode,
-                    int nrej, int nch) {
+                    int nch) {
   const int lane = threadIdx.x & 31;
   const int V = P.V;
   double excl;
@@ -257,7 +336,7 @@ __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt
   int lastw = -1;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    w[j] = (e0 + j < V) ? weight_of(sh, mode, nrej, zt[j], mode != 0 ? zd[j] : 0.f, P.c2) : 0.f;
+    w[j] = pair_weight(zt[j], mode != 0 ? zd[j] : -INFINITY, P.c2, sh.Kt, sh.Kd, sh.wA, sh.wB);
     wpart += w[j];
     if (w[j] > 0.f) lastw = e0 + j;
   }
@@ -291,8 +370,9 @@ __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt
 }
 
 template <int ELT, bool GREEDY>
-__global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams P) {
+__global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams P) {
   __shared__ TreeShared sh;
+  extern __shared__ __align__(16) unsigned char ring[];   // Chunks<ELT>::kRingBytes
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int M = P.M, V = P.V;
@@ -344,10 +424,7 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
       // first argmax of the target row; both rows checked
       float best = -INFINITY, dmax = -INFINITY;
       int bi = 0x7fffffff, bad = 0;
-      for (int c = warp; c < nch; c += kTreeWarps) {
-        const int e0 = c * kChunkElems + lane * 8;
-        float z[8];
-        Rows<ELT>::load8(rt, e0, V, P.vec, z);
+      Chunks<ELT>::each(ring, rt, rd, nk > 0, nch, V, P.vec, [&](int, int e0, const float (&z)[8], const float (&zd)[8]) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           bad |= (z[j] != z[j]) || (z[j] == INFINITY);
@@ -357,14 +434,13 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
           }
         }
         if (nk > 0) {
-          Rows<ELT>::load8(rd, e0, V, P.vec, z);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            bad |= (z[j] != z[j]) || (z[j] == INFINITY);
-            dmax = fmaxf(dmax, z[j]);
+            bad |= (zd[j] != zd[j]) || (zd[j] == INFINITY);
+            dmax = fmaxf(dmax, zd[j]);
           }
         }
-      }
+      });
       warp_argmax(best, bi);
       bad = warp_or(bad);
 #pragma unroll
@@ -417,16 +493,10 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
     {
       float mt = -INFINITY, Kt = 0.f, st = 0.f, md = -INFINITY, Kd = 0.f, sd = 0.f;
       int bad = 0;
-      for (int c = warp; c < nch; c += kTreeWarps) {
-        const int e0 = c * kChunkElems + lane * 8;
-        float z[8];
-        Rows<ELT>::load8(rt, e0, V, P.vec, z);
+      Chunks<ELT>::each(ring, rt, rd, nk > 0, nch, V, P.vec, [&](int, int, const float (&z)[8], const float (&zd)[8]) {
         online8(z, c2, mt, Kt, st, bad);
-        if (nk > 0) {
-          Rows<ELT>::load8(rd, e0, V, P.vec, z);
-          online8(z, c2, md, Kd, sd, bad);
-        }
-      }
+        if (nk > 0) online8(zd, c2, md, Kd, sd, bad);
+      });
       bad = warp_or(bad);
       if (lane == 0) sh.wbad[warp] = bad;
       combine_stats(sh, mt, Kt, st, sh.Kt, sh.St, sh.wm, sh.ws, c2);
@@ -436,8 +506,8 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
         int anybad = 0;
         for (int w = 0; w < kTreeWarps; ++w) anybad |= sh.wbad[w];
         if (anybad || !(sh.St > 0.f) || (nk > 0 && !(sh.Sd > 0.f))) sh.st = SV_ERR_NONFINITE;
-        sh.invSt = 1.f / sh.St;
-        sh.invSd = nk > 0 ? 1.f / sh.Sd : 0.f;
+        sh.cc = 0.0;
+        sh.PP = 1.0;
       }
       __syncthreads();
       if (sh.st != 0) break;
@@ -452,8 +522,7 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
         const float zt = Vec<ELT>::scalar(rt, x), zd = Vec<ELT>::scalar(rd, x);
         const double p = static_cast<double>(fast_exp2(fmaf(zt, c2, -sh.Kt))) / static_cast<double>(sh.St);
         const double q = static_cast<double>(fast_exp2(fmaf(zd, c2, -sh.Kd))) / static_cast<double>(sh.Sd);
-        double r = p;
-        for (int h = 1; h <= nrej; ++h) r = (sh.fb[h] ? r : fmax(r - q, 0.0)) / sh.S[h];
+        const double r = fmax(p - sh.cc * q, 0.0) / sh.PP;
         const double al = (q == 0.0) ? (r > 0.0 ? 1.0 : 0.0) : fmin(1.0, r / q);
         if (P.alpha) P.alpha[rb + c] = static_cast<float>(al);
         sh.next = (static_cast<double>(sh.u[c]) < al) ? c : -1;
@@ -465,15 +534,16 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
       }
       // rejected: the residual after this rejection, its mass and chunk sums
       last_mode = 1;
-      weight_pass<ELT>(sh, P, rt, rd, 1, nrej, nch);
+      weight_pass<ELT>(sh, ring, P, rt, rd, 1, nch);
       if (!(sh.total > 0.0)) {
         last_mode = 2;                       // zero residual: keep r
-        weight_pass<ELT>(sh, P, rt, rd, 2, nrej, nch);
+        weight_pass<ELT>(sh, ring, P, rt, rd, 2, nch);
       }
       if (tid == 0) {
-        sh.S[nrej + 1] = sh.total;
-        sh.invS[nrej + 1] = static_cast<float>(1.0 / sh.total);
-        sh.fb[nrej + 1] = (last_mode == 2);
+        // S = sh.total is the mass of max(0, r - q) (or of r); the new
+        // residual is that weight over S
+        if (last_mode == 1) sh.cc += sh.PP;
+        sh.PP *= sh.total;
       }
       __syncthreads();
       nrej += 1;
@@ -492,10 +562,9 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
     // --- the draw: the bonus weights at a node without children, else the
     // last residual (whose chunk sums the last pass left in sh.csum)
     const int wmode = nk == 0 ? 0 : last_mode;
-    const int wrej = nk == 0 ? 0 : nrej - 1;
-    if (nk == 0) weight_pass<ELT>(sh, P, rt, rd, 0, 0, nch);
+    if (nk == 0) weight_pass<ELT>(sh, ring, P, rt, rd, 0, nch);
     if (warp == 0) {
-      const int y = draw<ELT>(sh, P, rt, rd, wmode, wrej, nch);
+      const int y = draw<ELT>(sh, P, rt, rd, wmode, nch);
       if (lane == 0) {
         sh.y = y;
         sh.st = -1;
@@ -564,12 +633,20 @@ extern "C" sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtyp
   p.c2 = static_cast<float>(c2);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid(static_cast<unsigned>(B)), block(sv::kTreeThreads);
-  if (elt == 2) {
-    if (greedy) sv::tree_kernel<2, true><<<grid, block, 0, s>>>(p);
-    else sv::tree_kernel<2, false><<<grid, block, 0, s>>>(p);
-  } else {
-    if (greedy) sv::tree_kernel<4, true><<<grid, block, 0, s>>>(p);
-    else sv::tree_kernel<4, false><<<grid, block, 0, s>>>(p);
+  void (*kern)(const sv::TreeParams) = elt == 2 ? (greedy ? sv::tree_kernel<2, true> : sv::tree_kernel<2, false>)
+                                                : (greedy ? sv::tree_kernel<4, true> : sv::tree_kernel<4, false>);
+  const int ring = elt == 2 ? sv::Chunks<2>::kRingBytes : sv::Chunks<4>::kRingBytes;
+  // the ring needs more than the default 48 KB of dynamic shared memory
+  // (set once per device and kernel)
+  static bool ready[64][4] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
+  const int which = (elt == 2 ? 0 : 2) + (greedy ? 1 : 0);
+  if (!ready[dev][which]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ring) != cudaSuccess)
+      return SV_ERR_CUDA;
+    ready[dev][which] = true;
   }
+  kern<<<grid, block, ring, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
