@@ -16,8 +16,12 @@
 //   s = u[b, 0]; T == 0 accepts the first child equal to the first argmax of
 //   the node's target row and emits that argmax.
 //
-// One CTA walks one sequence (its warps stream the rows through a cp.async
-// ring in shared memory, see Chunks).  Each visited node costs one pass over its
+// A cluster of cs CTAs walks one sequence: each CTA streams a contiguous
+// slice of every row (through a cp.async ring in shared memory, see Chunks),
+// and the slices' sums are exchanged through distributed shared memory and
+// combined in rank order, so every CTA takes the same decisions.  cs is the
+// largest of 8, 4, 2, 1 that keeps one CTA per SM for the whole batch.  Each
+// visited node costs one pass over its
 // target row (and draft row, if it has children) for the row maximum and
 // log-sum of 2^(z c), one more pass over both rows per rejected child (the
 // residual mass, with the sums of 256-logit chunks kept for the draw), and
@@ -28,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 
 #include "../../include/specverify.h"
@@ -41,6 +46,7 @@ constexpr int kTreeWarps = kTreeThreads / 32;
 constexpr int kChunkElems = 256;                 // logits per warp step: 8 per lane
 constexpr int kTreeMaxChunks = 2048;             // V <= 524288
 constexpr int kTreeMaxNodes = SV_TREE_MAX_NODES;
+constexpr int kTreeMaxCluster = 8;
 
 struct TreeParams {
   const unsigned char* target;   // [B, M, V]
@@ -57,6 +63,7 @@ struct TreeParams {
   int B, M, V;
   int vec;                       // rows 16-byte aligned: vector loads
   float c2;                      // log2(e) / T
+  int cs;                        // CTAs per sequence (the cluster): each streams a slice of every row
 };
 
 template <int ELT>
@@ -90,8 +97,8 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
-// Calls f(c, e0, zt[8], zd[8]) for each chunk c of this warp (c = warp,
-// warp + W, ...), zt / zd being the lane's eight logits of the target and
+// Calls f(c, e0, zt[8], zd[8]) for each chunk c in [c_lo, c_hi) of this
+// warp (c = c_lo + warp, c_lo + warp + W, ...), zt / zd being the lane's eight logits of the target and
 // (if `both`) draft rows from e0.  Each lane streams its own 16 (bf16) or 32
 // (fp32) bytes per row and chunk through a ring of D slots in shared memory
 // with cp.async, D chunks ahead of its use: every lane reads back only what
@@ -108,11 +115,11 @@ struct Chunks {
   }
   template <typename F>
   __device__ __forceinline__ static void each(unsigned char* ring, const unsigned char* rt, const unsigned char* rd,
-                                              bool both, int nch, int V, int vec, F&& f) {
+                                              bool both, int c_lo, int c_hi, int V, int vec, F&& f) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int mine = warp < nch ? (nch - warp + kTreeWarps - 1) / kTreeWarps : 0;
+    const int mine = c_lo + warp < c_hi ? (c_hi - c_lo - warp + kTreeWarps - 1) / kTreeWarps : 0;
     auto issue = [&](int i) {
-      const int c = warp + i * kTreeWarps;
+      const int c = c_lo + warp + i * kTreeWarps;
       const int e0 = c * kChunkElems + lane * 8;
       if (i < mine && vec && e0 + 8 <= V) {
         const int sl = i % D;
@@ -128,7 +135,7 @@ struct Chunks {
     for (int i = 0; i < D; ++i) issue(i);
     for (int i = 0; i < mine; ++i) {
       cp_async_wait<D - 1>();                      // chunk i has landed
-      const int c = warp + i * kTreeWarps;
+      const int c = c_lo + warp + i * kTreeWarps;
       const int e0 = c * kChunkElems + lane * 8;
       float zt[8], zd[8];
       if (vec && e0 + 8 <= V) {
@@ -155,20 +162,71 @@ struct Chunks {
   }
 };
 
+// What a CTA contributes to one exchange of its cluster.
+struct XSlot {
+  float Kt, St, Kd, Sd;     // row statistics of its slice (greedy: Kt = best logit, St = draft maximum)
+  int bad, idx, y, pad;     // a bad logit seen; greedy argmax; the drawn token
+  double total;             // its slice's weight
+};
+
 // Per-CTA scratch for the walk.
 struct TreeShared {
   int par[kTreeMaxNodes], tok[kTreeMaxNodes];
   float u[kTreeMaxNodes];
   int kids[kTreeMaxNodes];
-  int nkids, n, cur, len, st, next, y;
-  float csum[kTreeMaxChunks];        // chunk sums of the last weight pass
+  int nkids, n, cur, len, st, next, y, owner;
+  float csum[kTreeMaxChunks];        // chunk sums of the last weight pass (this CTA's chunks)
   double cc, PP;                     // residual after the rejections so far: max(0, p - cc q) / PP
   float wA, wB;                      // weights of the last pass: max(0, A 2^(z^t c - K^t) - B 2^(z^d c - K^d))
   float wm[kTreeWarps], ws[kTreeWarps], wmd[kTreeWarps], wsd[kTreeWarps];
   int wbad[kTreeWarps], widx[kTreeWarps];
-  float Kt, St, Kd, Sd;              // row statistics of the current node
-  double total;                      // mass of the last weight pass
+  float Kt, St, Kd, Sd;              // row statistics of the current node (whole row)
+  float myKt, mySt, myKd, mySd;      // the same for this CTA's slice
+  double total;                      // weight of the last pass (whole row)
+  double mytotal;                    // ... of this CTA's slice
+  double base[kTreeMaxCluster];      // weight of the slices before each CTA's
+  double slice[kTreeMaxCluster];     // weight of each CTA's slice
+  XSlot xs[2];                       // exchange slots (double-buffered)
 };
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_peer_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ double ld_peer_f64(uint32_t a) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// One exchange: thread 0 has filled sh.xs[xp]; after the cluster barrier
+// every CTA's slot is visible, and thread 0 reads them in rank order.  The
+// slots are double-buffered: a CTA writes a slot again only after the next
+// barrier, which every peer reaches only after reading it.
+__device__ __forceinline__ void exchange(int& xp) {
+  cluster_sync();
+  xp ^= 1;
+}
+__device__ __forceinline__ XSlot peer_slot(const TreeShared& sh, int xp_read, int rank) {
+  XSlot x;
+  const uint32_t a = peer(&sh.xs[xp_read], rank);
+  x.Kt = ld_peer_f32(a + offsetof(XSlot, Kt));
+  x.St = ld_peer_f32(a + offsetof(XSlot, St));
+  x.Kd = ld_peer_f32(a + offsetof(XSlot, Kd));
+  x.Sd = ld_peer_f32(a + offsetof(XSlot, Sd));
+  x.bad = ld_peer_s32(a + offsetof(XSlot, bad));
+  x.idx = ld_peer_s32(a + offsetof(XSlot, idx));
+  x.y = ld_peer_s32(a + offsetof(XSlot, y));
+  x.pad = 0;
+  x.total = ld_peer_f64(a + offsetof(XSlot, total));
+  return x;
+}
 
 // Running (max, sum 2^(z c - fl(max c))) of one lane, updated by 8 logits.
 __device__ __forceinline__ void online8(const float (&z)[8], float c2, float& m, float& K, float& s, int& bad) {
@@ -188,10 +246,25 @@ __device__ __forceinline__ void online8(const float (&z)[8], float c2, float& m,
   }
 }
 
-// CTA-wide combination of the lanes' (m, K, s): returns through the shared
-// struct (Kout = fl(M c), Sout = sum 2^(z c - Kout)), in warp order.
-__device__ void combine_stats(TreeShared& sh, float m, float K, float s, float& Kout, float& Sout, float* wm,
-                              float* ws, float c2) {
+// Merge of (K, S) pairs, S = sum 2^(z c - K), K = fl(max z * c): the larger
+// K wins and the other sum is rescaled.  (-inf, 0) is the empty pair.
+__device__ __forceinline__ void merge_ks(float& K, float& S, float K2, float S2) {
+  if (!(S2 > 0.f)) return;
+  if (!(S > 0.f)) {
+    K = K2;
+    S = S2;
+    return;
+  }
+  if (K2 > K) {
+    S = S * fast_exp2(K - K2) + S2;
+    K = K2;
+  } else {
+    S += S2 * fast_exp2(K2 - K);
+  }
+}
+
+// CTA-wide (K, S) of the lanes' running pairs, in warp order (thread 0).
+__device__ void combine_stats(float m, float K, float s, float& Kout, float& Sout, float* wm, float* ws, float c2) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float M = m;
 #pragma unroll
@@ -211,7 +284,7 @@ __device__ void combine_stats(TreeShared& sh, float m, float K, float s, float& 
     float S = 0.f;
     for (int w = 0; w < kTreeWarps; ++w)
       if (wm[w] != -INFINITY) S += ws[w] * fast_exp2(wm[w] * c2 - Kall);
-    Kout = Kall;
+    Kout = (Mall == -INFINITY) ? -INFINITY : Kall;
     Sout = (Mall == -INFINITY) ? 0.f : S;
   }
 }
@@ -230,13 +303,17 @@ __device__ __forceinline__ float pair_weight(float zt, float zd, float c2, float
   const float ed = fast_exp2(fmaf(zd, c2, -Kd));
   return fmaxf(fmaf(A, et, -B * ed), 0.f);
 }
+// The bonus weight: no draft row (K^d may be -inf at a node without children).
+__device__ __forceinline__ float bonus_weight(float zt, float c2, float Kt) { return fast_exp2(fmaf(zt, c2, -Kt)); }
 
-// Fixed-order fp64 total of the chunk sums: lane l adds chunks
-// [l*per, (l+1)*per) in order, then the lanes are scanned.
-__device__ __forceinline__ double chunk_total(const TreeShared& sh, int nch, int lane, double& excl, int& lo, int& hi) {
-  const int per = (nch + 31) / 32;
-  lo = min(lane * per, nch);
-  hi = min(lo + per, nch);
+// Fixed-order fp64 total of the chunk sums of [c_lo, c_hi): lane l adds a
+// contiguous run of chunks in order, then the lanes are scanned.
+__device__ __forceinline__ double chunk_total(const TreeShared& sh, int c_lo, int c_hi, int lane, double& excl,
+                                             int& lo, int& hi) {
+  const int n = c_hi - c_lo;
+  const int per = (n + 31) / 32;
+  lo = c_lo + min(lane * per, n);
+  hi = min(lo + per, c_hi);
   double part = 0.0;
   for (int c = lo; c < hi; ++c) part += static_cast<double>(sh.csum[c]);
   const double incl = warp_incl_scan(part, lane);
@@ -244,14 +321,15 @@ __device__ __forceinline__ double chunk_total(const TreeShared& sh, int nch, int
   return __shfl_sync(0xffffffffu, incl, 31);
 }
 
-// One pass of weights over the current node's rows: chunk sums into
-// sh.csum, the fixed-order fp64 total into sh.total.
+// One pass of weights over this CTA's slice of the current node's rows:
+// chunk sums into sh.csum, then the slices' weights exchanged in the
+// cluster (sh.slice, sh.base, sh.total, identical in every CTA).
 //   mode 0: bonus weights (A = 1, B = 0; the draft row is not read);
 //   mode 1: the residual after one more rejection;
 //   mode 2: the current residual r itself (zero-residual fallback).
 template <int ELT>
 __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParams& P, const unsigned char* rt,
-                            const unsigned char* rd, int mode, int nch) {
+                            const unsigned char* rd, int mode, int c_lo, int c_hi, int& xp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     if (mode == 0) {
@@ -265,10 +343,16 @@ __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParam
   }
   __syncthreads();
   const float c2 = P.c2, Kt = sh.Kt, Kd = sh.Kd, A = sh.wA, B = sh.wB;
-  Chunks<ELT>::each(ring, rt, rd, mode != 0, nch, P.V, P.vec, [&](int c, int, const float (&zt)[8], const float (&zd)[8]) {
+  Chunks<ELT>::each(ring, rt, rd, mode != 0, c_lo, c_hi, P.V, P.vec,
+                    [&](int c, int, const float (&zt)[8], const float (&zd)[8]) {
     float part = 0.f;
+    if (mode == 0) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) part += pair_weight(zt[j], mode != 0 ? zd[j] : -INFINITY, c2, Kt, Kd, A, B);
+      for (int j = 0; j < 8; ++j) part += bonus_weight(zt[j], c2, Kt);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) part += pair_weight(zt[j], zd[j], c2, Kt, Kd, A, B);
+    }
     part = warp_sum(part);
     if (lane == 0) sh.csum[c] = part;
   });
@@ -276,30 +360,46 @@ __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParam
   if (warp == 0) {
     double excl;
     int lo, hi;
-    const double tot = chunk_total(sh, nch, lane, excl, lo, hi);
-    if (lane == 0) sh.total = tot;
+    const double tot = chunk_total(sh, c_lo, c_hi, lane, excl, lo, hi);
+    if (lane == 0) {
+      sh.mytotal = tot;
+      sh.xs[xp].total = tot;
+    }
+  }
+  __syncthreads();
+  const int xr = xp;
+  exchange(xp);
+  if (threadIdx.x == 0) {
+    double acc = 0.0;
+    for (int r = 0; r < P.cs; ++r) {
+      const double t = peer_slot(sh, xr, r).total;
+      sh.base[r] = acc;
+      sh.slice[r] = t;
+      acc += t;
+    }
+    sh.total = acc;
   }
   __syncthreads();
 }
 
-// Inverse CDF over the weights of the last pass with the sampling uniform
-// (warp 0): the chunk from the chunk sums, then the logit from the chunk's
-// recomputed weights.  Rounding that leaves the point past the weights of
-// the chunk (or of the row) takes the last logit with weight there.
+// Inverse CDF with the sampling uniform over the weights of the last pass,
+// for the CTA whose slice holds the point (warp 0): the chunk from the chunk
+// sums, then the logit from the chunk's recomputed weights.  `last`: the
+// point lies past every weight (rounding); take the last logit with weight.
 template <int ELT>
 __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt, const unsigned char* rd, int mode,
-                    int nch) {
+                    int c_lo, int c_hi, double t, double slice_base, bool last) {
   const int lane = threadIdx.x & 31;
   const int V = P.V;
   double excl;
   int lo, hi;
-  const double tot = chunk_total(sh, nch, lane, excl, lo, hi);
+  chunk_total(sh, c_lo, c_hi, lane, excl, lo, hi);
+  excl += slice_base;
   double part = 0.0;
   for (int c = lo; c < hi; ++c) part += static_cast<double>(sh.csum[c]);
-  const double t = static_cast<double>(sh.u[0]) * tot;
   int chunk = -1;
   double base = 0.0;
-  const unsigned in = __ballot_sync(0xffffffffu, part > 0.0 && excl <= t && t < excl + part);
+  const unsigned in = last ? 0u : __ballot_sync(0xffffffffu, part > 0.0 && excl <= t && t < excl + part);
   if (in) {
     const int l = __ffs(in) - 1;
     if (lane == l) {
@@ -318,14 +418,14 @@ __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt
     base = __shfl_sync(0xffffffffu, base, l);
   }
   if (chunk < 0) {
-    // past the total: the last chunk with weight
-    int last = -1;
+    // past the weights: the last chunk with weight
+    int lastc = -1;
     for (int c = lo; c < hi; ++c)
-      if (sh.csum[c] > 0.f) last = c;
+      if (sh.csum[c] > 0.f) lastc = c;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-    chunk = last;
-    base = -1.0;   // take the chunk's last logit with weight
+    for (int o = 16; o > 0; o >>= 1) lastc = max(lastc, __shfl_xor_sync(0xffffffffu, lastc, o));
+    chunk = lastc;
+    base = -1.0;
   }
   if (chunk < 0) return -1;
   const int e0 = chunk * kChunkElems + lane * 8;
@@ -336,7 +436,7 @@ __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt
   int lastw = -1;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    w[j] = pair_weight(zt[j], mode != 0 ? zd[j] : -INFINITY, P.c2, sh.Kt, sh.Kd, sh.wA, sh.wB);
+    w[j] = mode == 0 ? bonus_weight(zt[j], P.c2, sh.Kt) : pair_weight(zt[j], zd[j], P.c2, sh.Kt, sh.Kd, sh.wA, sh.wB);
     wpart += w[j];
     if (w[j] > 0.f) lastw = e0 + j;
   }
@@ -373,21 +473,29 @@ template <int ELT, bool GREEDY>
 __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams P) {
   __shared__ TreeShared sh;
   extern __shared__ __align__(16) unsigned char ring[];   // Chunks<ELT>::kRingBytes
-  const int b = blockIdx.x;
+  const int cs = P.cs;
+  const int rank = cluster_rank();
+  const int b = blockIdx.x / cs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int M = P.M, V = P.V;
   const int nch = (V + kChunkElems - 1) / kChunkElems;
+  const int c_lo = static_cast<int>((static_cast<long long>(rank) * nch) / cs);
+  const int c_hi = static_cast<int>((static_cast<long long>(rank + 1) * nch) / cs);
   const size_t row_bytes = static_cast<size_t>(V) * ELT;
   const float c2 = P.c2;
   const size_t rb = static_cast<size_t>(b) * M;
+  const bool lead = rank == 0;        // the CTA that writes the outputs
+  int xp = 0;
 
   for (int j = tid; j < M; j += kTreeThreads) {
     sh.par[j] = P.parents[rb + j];
     sh.tok[j] = P.tokens[rb + j];
     sh.u[j] = P.uniforms[rb + j];
-    P.out_tokens[rb + j] = -1;
-    P.out_nodes[rb + j] = -1;
-    if (P.alpha) P.alpha[rb + j] = NAN;
+    if (lead) {
+      P.out_tokens[rb + j] = -1;
+      P.out_nodes[rb + j] = -1;
+      if (P.alpha) P.alpha[rb + j] = NAN;
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -406,7 +514,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
   }
   __syncthreads();
 
-  // sh.st: 0 walking, > 0 an error, -1 done
+  // sh.st: 0 walking, > 0 an error, -1 done.  Every decision below is taken
+  // from values that are the same in every CTA of the cluster (the inputs,
+  // or exchanged and combined in rank order), so the CTAs walk in lockstep
+  // and meet at every cluster barrier.
   while (sh.st == 0) {
     const int cur = sh.cur;
     if (tid == 0) {
@@ -424,7 +535,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       // first argmax of the target row; both rows checked
       float best = -INFINITY, dmax = -INFINITY;
       int bi = 0x7fffffff, bad = 0;
-      Chunks<ELT>::each(ring, rt, rd, nk > 0, nch, V, P.vec, [&](int, int e0, const float (&z)[8], const float (&zd)[8]) {
+      Chunks<ELT>::each(ring, rt, rd, nk > 0, c_lo, c_hi, V, P.vec,
+                        [&](int, int e0, const float (&z)[8], const float (&zd)[8]) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           bad |= (z[j] != z[j]) || (z[j] == INFINITY);
@@ -463,6 +575,26 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
             bx = sh.widx[w];
           }
         }
+        sh.xs[xp].Kt = bv;
+        sh.xs[xp].idx = bx;
+        sh.xs[xp].St = dm;
+        sh.xs[xp].bad = anybad;
+      }
+      __syncthreads();
+      const int xr = xp;
+      exchange(xp);
+      if (tid == 0) {
+        float bv = -INFINITY, dm = -INFINITY;
+        int bx = 0x7fffffff, anybad = 0;
+        for (int r = 0; r < cs; ++r) {          // slices in index order: ties go to the lower rank
+          const XSlot x = peer_slot(sh, xr, r);
+          anybad |= x.bad;
+          dm = fmaxf(dm, x.St);
+          if (x.Kt > bv) {
+            bv = x.Kt;
+            bx = x.idx;
+          }
+        }
         if (anybad || bv == -INFINITY || (nk > 0 && dm == -INFINITY)) {
           sh.st = SV_ERR_NONFINITE;
         } else {
@@ -470,12 +602,14 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
           for (int i = 0; i < nk && next < 0; ++i) {
             const int c = sh.kids[i];
             const int ok = (sh.tok[c] == bx);
-            if (P.alpha) P.alpha[rb + c] = ok ? 1.f : 0.f;
+            if (P.alpha && lead) P.alpha[rb + c] = ok ? 1.f : 0.f;
             if (ok) next = c;
           }
           if (next >= 0) {
-            P.out_nodes[rb + sh.len] = next;
-            P.out_tokens[rb + sh.len] = sh.tok[next];
+            if (lead) {
+              P.out_nodes[rb + sh.len] = next;
+              P.out_tokens[rb + sh.len] = sh.tok[next];
+            }
             sh.len += 1;
             sh.cur = next;
           } else {
@@ -488,24 +622,48 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       continue;
     }
 
-    // --- row statistics: one pass over the target row and, for a node with
-    // children, its draft row
+    // --- row statistics: one pass over this CTA's slice of the target row
+    // and, for a node with children, of the draft row; then the slices'
+    // pairs are merged in rank order
     {
       float mt = -INFINITY, Kt = 0.f, st = 0.f, md = -INFINITY, Kd = 0.f, sd = 0.f;
       int bad = 0;
-      Chunks<ELT>::each(ring, rt, rd, nk > 0, nch, V, P.vec, [&](int, int, const float (&z)[8], const float (&zd)[8]) {
+      Chunks<ELT>::each(ring, rt, rd, nk > 0, c_lo, c_hi, V, P.vec,
+                        [&](int, int, const float (&z)[8], const float (&zd)[8]) {
         online8(z, c2, mt, Kt, st, bad);
         if (nk > 0) online8(zd, c2, md, Kd, sd, bad);
       });
       bad = warp_or(bad);
       if (lane == 0) sh.wbad[warp] = bad;
-      combine_stats(sh, mt, Kt, st, sh.Kt, sh.St, sh.wm, sh.ws, c2);
-      if (nk > 0) combine_stats(sh, md, Kd, sd, sh.Kd, sh.Sd, sh.wmd, sh.wsd, c2);
+      combine_stats(mt, Kt, st, sh.myKt, sh.mySt, sh.wm, sh.ws, c2);
+      if (nk > 0) combine_stats(md, Kd, sd, sh.myKd, sh.mySd, sh.wmd, sh.wsd, c2);
       __syncthreads();
       if (tid == 0) {
         int anybad = 0;
         for (int w = 0; w < kTreeWarps; ++w) anybad |= sh.wbad[w];
-        if (anybad || !(sh.St > 0.f) || (nk > 0 && !(sh.Sd > 0.f))) sh.st = SV_ERR_NONFINITE;
+        sh.xs[xp].Kt = sh.myKt;
+        sh.xs[xp].St = sh.mySt;
+        sh.xs[xp].Kd = nk > 0 ? sh.myKd : -INFINITY;
+        sh.xs[xp].Sd = nk > 0 ? sh.mySd : 0.f;
+        sh.xs[xp].bad = anybad;
+      }
+      __syncthreads();
+      const int xr = xp;
+      exchange(xp);
+      if (tid == 0) {
+        float K1 = -INFINITY, S1 = 0.f, K2 = -INFINITY, S2 = 0.f;
+        int anybad = 0;
+        for (int r = 0; r < cs; ++r) {
+          const XSlot x = peer_slot(sh, xr, r);
+          anybad |= x.bad;
+          merge_ks(K1, S1, x.Kt, x.St);
+          merge_ks(K2, S2, x.Kd, x.Sd);
+        }
+        sh.Kt = K1;
+        sh.St = S1;
+        sh.Kd = K2;
+        sh.Sd = S2;
+        if (anybad || !(S1 > 0.f) || (nk > 0 && !(S2 > 0.f))) sh.st = SV_ERR_NONFINITE;
         sh.cc = 0.0;
         sh.PP = 1.0;
       }
@@ -514,7 +672,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     }
 
     // --- the children, in index order
-    int nrej = 0, accepted = -1, last_mode = 1;
+    int accepted = -1, last_mode = 1;
     for (int i = 0; i < nk; ++i) {
       if (tid == 0) {
         const int c = sh.kids[i];
@@ -524,7 +682,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         const double q = static_cast<double>(fast_exp2(fmaf(zd, c2, -sh.Kd))) / static_cast<double>(sh.Sd);
         const double r = fmax(p - sh.cc * q, 0.0) / sh.PP;
         const double al = (q == 0.0) ? (r > 0.0 ? 1.0 : 0.0) : fmin(1.0, r / q);
-        if (P.alpha) P.alpha[rb + c] = static_cast<float>(al);
+        if (P.alpha && lead) P.alpha[rb + c] = static_cast<float>(al);
         sh.next = (static_cast<double>(sh.u[c]) < al) ? c : -1;
       }
       __syncthreads();
@@ -534,10 +692,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       }
       // rejected: the residual after this rejection, its mass and chunk sums
       last_mode = 1;
-      weight_pass<ELT>(sh, ring, P, rt, rd, 1, nch);
+      weight_pass<ELT>(sh, ring, P, rt, rd, 1, c_lo, c_hi, xp);
       if (!(sh.total > 0.0)) {
         last_mode = 2;                       // zero residual: keep r
-        weight_pass<ELT>(sh, ring, P, rt, rd, 2, nch);
+        weight_pass<ELT>(sh, ring, P, rt, rd, 2, c_lo, c_hi, xp);
       }
       if (tid == 0) {
         // S = sh.total is the mass of max(0, r - q) (or of r); the new
@@ -546,12 +704,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         sh.PP *= sh.total;
       }
       __syncthreads();
-      nrej += 1;
     }
     if (accepted >= 0) {
       if (tid == 0) {
-        P.out_nodes[rb + sh.len] = accepted;
-        P.out_tokens[rb + sh.len] = sh.tok[accepted];
+        if (lead) {
+          P.out_nodes[rb + sh.len] = accepted;
+          P.out_tokens[rb + sh.len] = sh.tok[accepted];
+        }
         sh.len += 1;
         sh.cur = accepted;
       }
@@ -560,20 +719,39 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     }
 
     // --- the draw: the bonus weights at a node without children, else the
-    // last residual (whose chunk sums the last pass left in sh.csum)
+    // last residual (whose chunk sums the last pass left in sh.csum).  The
+    // CTA whose slice holds s * S draws; the token is then exchanged.
     const int wmode = nk == 0 ? 0 : last_mode;
-    if (nk == 0) weight_pass<ELT>(sh, ring, P, rt, rd, 0, nch);
-    if (warp == 0) {
-      const int y = draw<ELT>(sh, P, rt, rd, wmode, nch);
-      if (lane == 0) {
-        sh.y = y;
-        sh.st = -1;
+    if (nk == 0) weight_pass<ELT>(sh, ring, P, rt, rd, 0, c_lo, c_hi, xp);
+    if (tid == 0) {
+      const double t = static_cast<double>(sh.u[0]) * sh.total;
+      int owner = -1, lastw = -1;
+      for (int r = 0; r < cs; ++r) {
+        if (sh.slice[r] > 0.0) {
+          lastw = r;
+          if (owner < 0 && sh.base[r] <= t && t < sh.base[r] + sh.slice[r]) owner = r;
+        }
       }
+      sh.owner = owner >= 0 ? owner : lastw;
+      sh.next = owner >= 0 ? 0 : 1;     // 1: past every weight
+    }
+    __syncthreads();
+    int y = -1;
+    if (rank == sh.owner && warp == 0)
+      y = draw<ELT>(sh, P, rt, rd, wmode, c_lo, c_hi, static_cast<double>(sh.u[0]) * sh.total, sh.base[rank],
+                    sh.next == 1);
+    if (tid == 0) sh.xs[xp].y = y;
+    __syncthreads();
+    const int xr = xp;
+    exchange(xp);
+    if (tid == 0) {
+      sh.y = sh.owner >= 0 ? peer_slot(sh, xr, sh.owner).y : -1;
+      sh.st = -1;
     }
     __syncthreads();
   }
 
-  if (tid == 0) {
+  if (tid == 0 && lead) {
     const int st = sh.st < 0 ? 0 : sh.st;
     if (st == 0) {
       P.out_tokens[rb + sh.len] = sh.y;
@@ -584,12 +762,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     if (P.status) P.status[b] = st;
   }
   __syncthreads();
-  if (sh.st > 0) {
+  if (sh.st > 0 && lead) {
     for (int j = tid; j < M; j += kTreeThreads) {
       P.out_tokens[rb + j] = -1;
       P.out_nodes[rb + j] = -1;
     }
   }
+  cluster_sync();                     // no CTA leaves while a peer may still read its slots
 }
 
 }  // namespace
@@ -632,21 +811,71 @@ extern "C" sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtyp
           (reinterpret_cast<uintptr_t>(draft_logits) & 15u) == 0;
   p.c2 = static_cast<float>(c2);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid(static_cast<unsigned>(B)), block(sv::kTreeThreads);
   void (*kern)(const sv::TreeParams) = elt == 2 ? (greedy ? sv::tree_kernel<2, true> : sv::tree_kernel<2, false>)
                                                 : (greedy ? sv::tree_kernel<4, true> : sv::tree_kernel<4, false>);
   const int ring = elt == 2 ? sv::Chunks<2>::kRingBytes : sv::Chunks<4>::kRingBytes;
-  // the ring needs more than the default 48 KB of dynamic shared memory
-  // (set once per device and kernel)
-  static bool ready[64][4] = {};
+  // Once per device and kernel: the ring needs more than the default 48 KB
+  // of dynamic shared memory, and the cluster sizes that can be resident
+  // with it (clusters of 1, 2, 4, 8 CTAs) are recorded.
+  struct DevInfo {
+    bool ready[4];
+    int sms;
+    int fits[4][4];   // [kernel][log2 cluster]: clusters that fit at once
+  };
+  static DevInfo info[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
   const int which = (elt == 2 ? 0 : 2) + (greedy ? 1 : 0);
-  if (!ready[dev][which]) {
+  DevInfo& di = info[dev];
+  if (!di.ready[which]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ring) != cudaSuccess)
       return SV_ERR_CUDA;
-    ready[dev][which] = true;
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SV_ERR_CUDA;
+    for (int l = 0; l < 4; ++l) {
+      cudaLaunchConfig_t q{};
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 1u << l;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.gridDim = dim3(1u << l, 1, 1);
+      q.blockDim = dim3(sv::kTreeThreads, 1, 1);
+      q.dynamicSmemBytes = static_cast<size_t>(ring);
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &q) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      di.fits[which][l] = n;
+    }
+    di.ready[which] = true;
   }
-  kern<<<grid, block, ring, s>>>(p);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  // CTAs per sequence: the largest cluster (up to 8) that keeps one CTA per
+  // SM for the whole batch; a sequence's walk is serial, so idle SMs are
+  // better spent on slices of its rows
+  int cs = 1;
+  for (int l = 3; l >= 1; --l) {
+    const int c = 1 << l;
+    if (static_cast<long long>(B) * c <= di.sms && di.fits[which][l] > 0) {
+      cs = c;
+      break;
+    }
+  }
+  if (di.fits[which][0] <= 0) return SV_ERR_UNSUPPORTED;
+  p.cs = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(cs), 1, 1);
+  cfg.blockDim = dim3(sv::kTreeThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(ring);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
