@@ -317,10 +317,16 @@ sv_status spec_verify_noalloc(int B, int k, int V, sv_dtype dtype,
  *   emits nothing (out_len 0, tokens -1);
  *   alpha [B, M] (may be NULL): min(1, r(x)/q(x)) of each tested child, NaN
  *   for the others (greedy: 1 or 0).
- * Only the rows on the walk are read.  No context and no workspace: the call
- * allocates nothing and can be captured in a CUDA graph.  Host-checkable
- * errors (sizes, dtype, temperature < 0 or not finite, NULL pointers) return
- * SV_ERR_INVALID_ARG and launch nothing.  V <= 524288.
+ * Only the rows on the walk are read.  A cluster of up to 8 CTAs walks each
+ * sequence (each streams a slice of every row); the size is chosen from B
+ * and the SM count, and the result is deterministic for a given B.  No
+ * context and no workspace: the call allocates nothing and can be captured
+ * in a CUDA graph.  The first call on a device (per dtype, and for sampling
+ * and greedy separately) sets the kernel's shared-memory limit and queries
+ * the cluster sizes that fit: make it before any stream capture.  Not
+ * thread-safe on that first call.  Host-checkable errors (sizes, dtype,
+ * temperature < 0 or not finite, NULL pointers) return SV_ERR_INVALID_ARG
+ * and launch nothing.  V <= 524288.
  * ------------------------------------------------------------------------ */
 
 #define SV_TREE_MAX_NODES 64
