@@ -162,11 +162,12 @@ struct Chunks {
   }
 };
 
-// What a CTA contributes to one exchange of its cluster.
-struct XSlot {
+// What a CTA contributes to one exchange of its cluster (three 16-byte
+// words, read by a peer with three vector loads).
+struct __align__(16) XSlot {
   float Kt, St, Kd, Sd;     // row statistics of its slice (greedy: Kt = best logit, St = draft maximum)
   int bad, idx, y, pad;     // a bad logit seen; greedy argmax; the drawn token
-  double total;             // its slice's weight
+  double total, pad2;       // its slice's weight
 };
 
 // Per-CTA scratch for the walk.
@@ -176,7 +177,8 @@ struct TreeShared {
   int kids[kTreeMaxNodes];
   int nkids, n, cur, len, st, next, y, owner;
   float csum[kTreeMaxChunks];        // chunk sums of the last weight pass (this CTA's chunks)
-  double cc, PP;                     // residual after the rejections so far: max(0, p - cc q) / PP
+  double cc, PP, invPP;              // residual after the rejections so far: max(0, p - cc q) / PP
+  double invSt, invSd;               // 1 / S^t, 1 / S^d of the current node
   float wA, wB;                      // weights of the last pass: max(0, A 2^(z^t c - K^t) - B 2^(z^d c - K^d))
   float wm[kTreeWarps], ws[kTreeWarps], wmd[kTreeWarps], wsd[kTreeWarps];
   int wbad[kTreeWarps], widx[kTreeWarps];
@@ -187,45 +189,34 @@ struct TreeShared {
   double base[kTreeMaxCluster];      // weight of the slices before each CTA's
   double slice[kTreeMaxCluster];     // weight of each CTA's slice
   XSlot xs[2];                       // exchange slots (double-buffered)
+  XSlot got[kTreeMaxCluster];        // the slots of the last exchange, rank order
 };
 
-__device__ __forceinline__ float ld_peer_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_peer_s32(uint32_t a) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ double ld_peer_f64(uint32_t a) {
-  double v;
-  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
+__device__ __forceinline__ uint4 ld_peer_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
   return v;
 }
 
-// One exchange: thread 0 has filled sh.xs[xp]; after the cluster barrier
-// every CTA's slot is visible, and thread 0 reads them in rank order.  The
-// slots are double-buffered: a CTA writes a slot again only after the next
-// barrier, which every peer reaches only after reading it.
-__device__ __forceinline__ void exchange(int& xp) {
+// One exchange: thread 0 has filled sh.xs[xp].  After the cluster barrier
+// every CTA's slot is visible; thread r < cs copies rank r's slot into
+// sh.got[r] (three 16-byte loads), so that thread 0 then merges them in rank
+// order from local shared memory.  The slots are double-buffered: a CTA
+// writes a slot again only after the next barrier, which every peer reaches
+// only after reading it.
+__device__ __forceinline__ void exchange(TreeShared& sh, int& xp, int cs) {
   cluster_sync();
+  const int t = threadIdx.x;
+  if (t < cs) {
+    const uint32_t a = peer(&sh.xs[xp], t);
+    uint4* dst = reinterpret_cast<uint4*>(&sh.got[t]);
+    dst[0] = ld_peer_v4(a);
+    dst[1] = ld_peer_v4(a + 16);
+    dst[2] = ld_peer_v4(a + 32);
+  }
+  __syncthreads();
   xp ^= 1;
-}
-__device__ __forceinline__ XSlot peer_slot(const TreeShared& sh, int xp_read, int rank) {
-  XSlot x;
-  const uint32_t a = peer(&sh.xs[xp_read], rank);
-  x.Kt = ld_peer_f32(a + offsetof(XSlot, Kt));
-  x.St = ld_peer_f32(a + offsetof(XSlot, St));
-  x.Kd = ld_peer_f32(a + offsetof(XSlot, Kd));
-  x.Sd = ld_peer_f32(a + offsetof(XSlot, Sd));
-  x.bad = ld_peer_s32(a + offsetof(XSlot, bad));
-  x.idx = ld_peer_s32(a + offsetof(XSlot, idx));
-  x.y = ld_peer_s32(a + offsetof(XSlot, y));
-  x.pad = 0;
-  x.total = ld_peer_f64(a + offsetof(XSlot, total));
-  return x;
 }
 
 // Running (max, sum 2^(z c - fl(max c))) of one lane, updated by 8 logits.
@@ -336,9 +327,8 @@ __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParam
       sh.wA = 1.f;
       sh.wB = 0.f;
     } else {
-      const double den = 1.0 / sh.PP;
-      sh.wA = static_cast<float>(den / static_cast<double>(sh.St));
-      sh.wB = static_cast<float>((mode == 1 ? sh.cc + sh.PP : sh.cc) * den / static_cast<double>(sh.Sd));
+      sh.wA = static_cast<float>(sh.invPP * sh.invSt);
+      sh.wB = static_cast<float>((mode == 1 ? sh.cc + sh.PP : sh.cc) * sh.invPP * sh.invSd);
     }
   }
   __syncthreads();
@@ -367,12 +357,11 @@ __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParam
     }
   }
   __syncthreads();
-  const int xr = xp;
-  exchange(xp);
+  exchange(sh, xp, P.cs);
   if (threadIdx.x == 0) {
     double acc = 0.0;
     for (int r = 0; r < P.cs; ++r) {
-      const double t = peer_slot(sh, xr, r).total;
+      const double t = sh.got[r].total;
       sh.base[r] = acc;
       sh.slice[r] = t;
       acc += t;
@@ -581,13 +570,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         sh.xs[xp].bad = anybad;
       }
       __syncthreads();
-      const int xr = xp;
-      exchange(xp);
+      exchange(sh, xp, cs);
       if (tid == 0) {
         float bv = -INFINITY, dm = -INFINITY;
         int bx = 0x7fffffff, anybad = 0;
         for (int r = 0; r < cs; ++r) {          // slices in index order: ties go to the lower rank
-          const XSlot x = peer_slot(sh, xr, r);
+          const XSlot& x = sh.got[r];
           anybad |= x.bad;
           dm = fmaxf(dm, x.St);
           if (x.Kt > bv) {
@@ -648,13 +636,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         sh.xs[xp].bad = anybad;
       }
       __syncthreads();
-      const int xr = xp;
-      exchange(xp);
+      exchange(sh, xp, cs);
       if (tid == 0) {
         float K1 = -INFINITY, S1 = 0.f, K2 = -INFINITY, S2 = 0.f;
         int anybad = 0;
         for (int r = 0; r < cs; ++r) {
-          const XSlot x = peer_slot(sh, xr, r);
+          const XSlot& x = sh.got[r];
           anybad |= x.bad;
           merge_ks(K1, S1, x.Kt, x.St);
           merge_ks(K2, S2, x.Kd, x.Sd);
@@ -664,8 +651,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         sh.Kd = K2;
         sh.Sd = S2;
         if (anybad || !(S1 > 0.f) || (nk > 0 && !(S2 > 0.f))) sh.st = SV_ERR_NONFINITE;
+        sh.invSt = 1.0 / static_cast<double>(S1);
+        sh.invSd = nk > 0 ? 1.0 / static_cast<double>(S2) : 0.0;
         sh.cc = 0.0;
         sh.PP = 1.0;
+        sh.invPP = 1.0;
       }
       __syncthreads();
       if (sh.st != 0) break;
@@ -678,12 +668,14 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         const int c = sh.kids[i];
         const long long x = sh.tok[c];
         const float zt = Vec<ELT>::scalar(rt, x), zd = Vec<ELT>::scalar(rd, x);
-        const double p = static_cast<double>(fast_exp2(fmaf(zt, c2, -sh.Kt))) / static_cast<double>(sh.St);
-        const double q = static_cast<double>(fast_exp2(fmaf(zd, c2, -sh.Kd))) / static_cast<double>(sh.Sd);
-        const double r = fmax(p - sh.cc * q, 0.0) / sh.PP;
-        const double al = (q == 0.0) ? (r > 0.0 ? 1.0 : 0.0) : fmin(1.0, r / q);
-        if (P.alpha && lead) P.alpha[rb + c] = static_cast<float>(al);
-        sh.next = (static_cast<double>(sh.u[c]) < al) ? c : -1;
+        const double p = static_cast<double>(fast_exp2(fmaf(zt, c2, -sh.Kt))) * sh.invSt;
+        const double q = static_cast<double>(fast_exp2(fmaf(zd, c2, -sh.Kd))) * sh.invSd;
+        const double r = fmax(p - sh.cc * q, 0.0) * sh.invPP;
+        // u < min(1, r / q) with u in [0, 1): u q < r (q = 0: accept iff r > 0)
+        const double u = static_cast<double>(sh.u[c]);
+        const bool acc = (q == 0.0) ? (r > 0.0) : (u * q < r);
+        if (P.alpha && lead) P.alpha[rb + c] = static_cast<float>((q == 0.0) ? (r > 0.0 ? 1.0 : 0.0) : fmin(1.0, r / q));
+        sh.next = acc ? c : -1;
       }
       __syncthreads();
       if (sh.next >= 0) {
@@ -702,6 +694,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         // residual is that weight over S
         if (last_mode == 1) sh.cc += sh.PP;
         sh.PP *= sh.total;
+        sh.invPP = 1.0 / sh.PP;
       }
       __syncthreads();
     }
@@ -742,10 +735,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
                     sh.next == 1);
     if (tid == 0) sh.xs[xp].y = y;
     __syncthreads();
-    const int xr = xp;
-    exchange(xp);
+    exchange(sh, xp, cs);
     if (tid == 0) {
-      sh.y = sh.owner >= 0 ? peer_slot(sh, xr, sh.owner).y : -1;
+      sh.y = sh.owner >= 0 ? sh.got[sh.owner].y : -1;
       sh.st = -1;
     }
     __syncthreads();
