@@ -168,6 +168,9 @@ def _check_dev(name, t, dtype, shape, device):
         return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        # the kernels read device memory: a host pointer must never reach them
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
     if t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
     if t.dtype != dtype:

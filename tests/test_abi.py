@@ -114,3 +114,17 @@ def test_tree_host_checks(lib):
     assert lib.spec_verify_tree(1, 4, 10, 1, P, P, P, P, P, P, -1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
     assert lib.spec_verify_tree(1, 4, 10, 1, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_ERR_INVALID_ARG
     assert lib.spec_verify_tree(0, 4, 10, 1, P, P, P, P, P, P, 1.0, P, P, P, P, P, P) == svp.SV_OK
+
+
+def test_host_tensors_are_rejected_before_any_call(lib):
+    # CPU tensors must never reach a kernel as device pointers
+    import torch
+    t = torch.zeros(2, 3, 8, dtype=torch.float32)
+    i = torch.zeros(2, 3, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        svp.verify_tree(t, t, i, i, torch.ones(2, dtype=torch.int32), torch.zeros(2, 3), 1.0)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        svp.kd_loss(t, t, torch.ones(2), 1.0)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        svp.spec_verify_noalloc(t, t[:, :2], i[:, :2], torch.ones(2, dtype=torch.int32), torch.zeros(2, 3), 1.0,
+                                i, torch.zeros(2, dtype=torch.int32))
