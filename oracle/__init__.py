@@ -47,7 +47,7 @@ def _bind(lib):
     P = c.c_void_p
     lib.oracle_verify.restype = c.c_int
     lib.oracle_verify.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, P, P, P, P, P, c.c_double,
-                                  P, P, P, P, P, P, P, P, P, P, P, c.c_int]
+                                  P, P, P, P, P, P, P, P, P, P, c.c_double, P, P, P, c.c_int]
     lib.oracle_row_lse.restype = c.c_double
     lib.oracle_row_lse.argtypes = [c.c_int, c.c_int, P, c.c_double]
     lib.oracle_row_probs.restype = None
@@ -69,7 +69,7 @@ def _bind(lib):
     lib.oracle_ctrl_choose.restype = I
     lib.oracle_ctrl_choose.argtypes = [I, P, P, I, P, I, D, D, I, I, P, P, P, P, P, P, P]
     lib.oracle_tree_verify.restype = I
-    lib.oracle_tree_verify.argtypes = [I, I, I, I, P, P, P, P, P, P, D, P, P, P, P, P, P, P, P, P, I]
+    lib.oracle_tree_verify.argtypes = [I, I, I, I, P, P, P, P, P, P, D, P, P, P, P, P, P, P, P, D, P, P, P, I]
     return lib
 
 
@@ -107,12 +107,17 @@ def _ptr(a):
     return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
 
 
-def verify(target, draft, tokens, draft_len, uniforms, T, nthreads=0, lib=None):
+TIE_BAND = 1e-5
+
+
+def verify(target, draft, tokens, draft_len, uniforms, T, nthreads=0, lib=None, tie_band=TIE_BAND):
     """Run the oracle on one batch.
 
     target [B,k+1,V] and draft [B,k,V]: float32 arrays, uint16 arrays of
     bf16 bits, or CPU/GPU torch tensors (fp32 or bf16).  Returns a dict with
-    out_tokens, out_len, status and the fp64 diagnostics.
+    out_tokens, out_len, status and the fp64 diagnostics; sample_lo and
+    sample_hi bound the tokens a draw could give with its uniform moved by at
+    most ``tie_band`` (in units of the normalised CDF).
     """
     lib = lib or load()
     t, dt = _as_np(target)
@@ -138,16 +143,19 @@ def verify(target, draft, tokens, draft_len, uniforms, T, nthreads=0, lib=None):
     mass = np.empty(B)
     atie = np.empty(B)
     stie = np.empty(B)
+    slo = np.empty(B, np.int32)
+    shi = np.empty(B, np.int32)
     status = np.empty(B, np.int32)
     d_arr = d if d.size else np.zeros(1, t.dtype)
     lib.oracle_verify(B, k, V, dt, _ptr(t), _ptr(d_arr), _ptr(tok), _ptr(kl), _ptr(u), float(T),
                       _ptr(out_tokens), _ptr(out_len), _ptr(lse_t), _ptr(lse_d), _ptr(p_x),
-                      _ptr(q_x), _ptr(alpha), _ptr(mass), _ptr(atie), _ptr(stie), _ptr(status),
-                      int(nthreads))
+                      _ptr(q_x), _ptr(alpha), _ptr(mass), _ptr(atie), _ptr(stie), float(tie_band),
+                      _ptr(slo), _ptr(shi), _ptr(status), int(nthreads))
     return {
         "out_tokens": out_tokens, "out_len": out_len, "status": status,
         "lse_t": lse_t, "lse_d": lse_d[:, :k], "p_x": p_x[:, :k], "q_x": q_x[:, :k],
         "alpha": alpha[:, :k], "resid_mass": mass, "accept_tie": atie, "sample_tie": stie,
+        "sample_lo": slo, "sample_hi": shi, "tie_band": float(tie_band),
     }
 
 
@@ -273,7 +281,8 @@ def expected_tokens(alpha, n, lib=None):
     return (lib or load()).oracle_ctrl_expected_tokens(float(alpha), int(n))
 
 
-def tree_verify(target, draft, parents, tokens, n_nodes, uniforms, T, final_w=False, nthreads=0, lib=None):
+def tree_verify(target, draft, parents, tokens, n_nodes, uniforms, T, final_w=False, nthreads=0, lib=None,
+                tie_band=TIE_BAND):
     """Tree verification (see ``oracle_tree_verify`` in oracle.c).
 
     target, draft [B,M,V] (fp32 / bf16 as for ``verify``), parents, tokens
@@ -298,9 +307,12 @@ def tree_verify(target, draft, parents, tokens, n_nodes, uniforms, T, final_w=Fa
     alpha = np.empty((B, M))
     fw = np.empty((B, V)) if final_w else None
     mass, atie, stie = np.empty(B), np.empty(B), np.empty(B)
+    slo, shi = np.empty(B, np.int32), np.empty(B, np.int32)
     status = np.empty(B, np.int32)
     lib.oracle_tree_verify(B, M, V, dt, _ptr(t), _ptr(d), _ptr(par), _ptr(tok), _ptr(nn), _ptr(u), float(T),
                            _ptr(out_tokens), _ptr(out_nodes), _ptr(out_len), _ptr(alpha), _ptr(fw), _ptr(mass),
-                           _ptr(atie), _ptr(stie), _ptr(status), int(nthreads))
+                           _ptr(atie), _ptr(stie), float(tie_band), _ptr(slo), _ptr(shi), _ptr(status),
+                           int(nthreads))
     return {"out_tokens": out_tokens, "out_nodes": out_nodes, "out_len": out_len, "status": status,
-            "alpha": alpha, "final_w": fw, "resid_mass": mass, "accept_tie": atie, "sample_tie": stie}
+            "alpha": alpha, "final_w": fw, "resid_mass": mass, "accept_tie": atie, "sample_tie": stie,
+            "sample_lo": slo, "sample_hi": shi, "tie_band": float(tie_band)}

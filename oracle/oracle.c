@@ -141,6 +141,27 @@ static int inverse_cdf(const double *w, int V, double S, double s, double *tie)
     return y;
 }
 
+/* The tokens a draw could give if the uniform moved by at most `band` (in
+ * units of C/S): the smallest and the largest x with w(x) > 0 whose CDF
+ * interval [C(x-1), C(x)] comes within band * S of s * S.  When s lies that
+ * close to a boundary of the drawn token, any token in [lo, hi] is a valid
+ * outcome of a computation whose CDF is off by less than band. */
+static void cdf_window(const double *w, int V, double S, double s, double band, int *lo, int *hi)
+{
+    double t_lo = (s - band) * S, t_hi = (s + band) * S, c_prev = 0.0, c = 0.0;
+    *lo = -1;
+    *hi = -1;
+    for (int x = 0; x < V; ++x) {
+        c_prev = c;
+        c += w[x];
+        if (w[x] > 0.0 && c >= t_lo && c_prev <= t_hi) {
+            if (*lo < 0)
+                *lo = x;
+            *hi = x;
+        }
+    }
+}
+
 /*
  * oracle_verify: see the file comment.  Shapes as in the library:
  *   target [B,k+1,V], draft [B,k,V] (dtype 0 = fp32, 1 = bf16 bits),
@@ -156,6 +177,9 @@ static int inverse_cdf(const double *w, int V, double S, double s, double *tie)
  *   accept_tie [B]               min |u_i - alpha_i| over the tests that
  *                                decided a (1 if none)
  *   sample_tie [B]               distance of s to the chosen x's CDF bounds
+ *   sample_lo, sample_hi [B]     the window of valid draws for a uniform off
+ *                                by at most tie_band (see cdf_window); greedy:
+ *                                both are the emitted token
  *   status [B]
  * nthreads <= 0 uses the OpenMP default.  Returns the number of sequences
  * with a nonzero status (flags excluded).
@@ -167,7 +191,8 @@ int oracle_verify(int B, int k, int V, int dtype,
                   int32_t *out_tokens, int32_t *out_len,
                   double *lse_t, double *lse_d, double *p_x, double *q_x,
                   double *alpha, double *resid_mass, double *accept_tie,
-                  double *sample_tie, int32_t *status, int nthreads)
+                  double *sample_tie, double tie_band, int32_t *sample_lo,
+                  int32_t *sample_hi, int32_t *status, int nthreads)
 {
     int nerr = 0;
 #ifdef _OPENMP
@@ -201,6 +226,8 @@ int oracle_verify(int B, int k, int V, int dtype,
         if (resid_mass) resid_mass[b] = NAN;
         if (accept_tie) accept_tie[b] = 1.0;
         if (sample_tie) sample_tie[b] = 1.0;
+        if (sample_lo) sample_lo[b] = -1;
+        if (sample_hi) sample_hi[b] = -1;
 
         int kb = draft_len[b];
         if (kb < 0 || kb > k)
@@ -293,8 +320,12 @@ int oracle_verify(int B, int k, int V, int dtype,
             }
             double stie = 1.0;
             int y = inverse_cdf(w, V, S, (double)u[k], &stie);
+            int wlo, whi;
+            cdf_window(w, V, S, (double)u[k], tie_band, &wlo, &whi);
             if (resid_mass) resid_mass[b] = S;
             if (sample_tie) sample_tie[b] = stie;
+            if (sample_lo) sample_lo[b] = wlo;
+            if (sample_hi) sample_hi[b] = whi;
             if (accept_tie) accept_tie[b] = atie;
             for (int i = 0; i < a; ++i)
                 out_tokens[(size_t)b * (k + 1) + i] = tokens[(size_t)b * k + i];
@@ -314,6 +345,8 @@ int oracle_verify(int B, int k, int V, int dtype,
                 out_tokens[(size_t)b * (k + 1) + i] = tokens[(size_t)b * k + i];
             out_tokens[(size_t)b * (k + 1) + a] = amax_t[a];
             out_len[b] = a + 1;
+            if (sample_lo) sample_lo[b] = amax_t[a];
+            if (sample_hi) sample_hi[b] = amax_t[a];
             if (status) status[b] = ORC_OK;
         }
         free(zt); free(zd); free(w); free(mt); free(md); free(amax_t);
@@ -659,7 +692,9 @@ int oracle_ctrl_choose(int n_slots, const double *A, const double *N, int B, con
  * be NULL): alpha [B, M] (min(1, r(x)/q(x)) of each tested child, NaN if not
  * tested; greedy 1 or 0), final_w [B, V] (w / S of the draw), resid_mass [B]
  * (S of the draw), accept_tie [B] (min |u - alpha| over the tests made, 1 if
- * none), sample_tie [B], status [B] (2 bad structure, 3 bad token, 4 a row
+ * none), sample_tie [B], sample_lo / sample_hi [B] (the window of valid
+ * draws for a uniform off by at most tie_band, as in oracle_verify), status
+ * [B] (2 bad structure, 3 bad token, 4 a row
  * the walk reads is not finite or all -inf; flag 256: a zero residual).
  * Only the rows the walk reads are checked.
  */
@@ -667,7 +702,8 @@ int oracle_tree_verify(int B, int M, int V, int dtype, const void *target, const
                        const int32_t *parents, const int32_t *tokens, const int32_t *n_nodes,
                        const float *uniforms, double T, int32_t *out_tokens, int32_t *out_nodes,
                        int32_t *out_len, double *alpha, double *final_w, double *resid_mass,
-                       double *accept_tie, double *sample_tie, int32_t *status, int nthreads)
+                       double *accept_tie, double *sample_tie, double tie_band, int32_t *sample_lo,
+                       int32_t *sample_hi, int32_t *status, int nthreads)
 {
     int nerr = 0;
 #ifdef _OPENMP
@@ -699,6 +735,8 @@ int oracle_tree_verify(int B, int M, int V, int dtype, const void *target, const
         if (resid_mass) resid_mass[b] = NAN;
         if (accept_tie) accept_tie[b] = 1.0;
         if (sample_tie) sample_tie[b] = 1.0;
+        if (sample_lo) sample_lo[b] = -1;
+        if (sample_hi) sample_hi[b] = -1;
 
         int st = ORC_OK, flags = 0;
         const int n = n_nodes[b];
@@ -802,8 +840,10 @@ int oracle_tree_verify(int B, int M, int V, int dtype, const void *target, const
             ot[len++] = tok[next];
             cur = next;
         }
+        int wlo = y, whi = y;
         if (st == ORC_OK && T > 0.0) {
             y = inverse_cdf(w, V, S, (double)u[0], &stie);
+            cdf_window(w, V, S, (double)u[0], tie_band, &wlo, &whi);
             if (final_w)
                 for (int x = 0; x < V; ++x)
                     final_w[(size_t)b * V + x] = w[x] / S;
@@ -814,6 +854,8 @@ int oracle_tree_verify(int B, int M, int V, int dtype, const void *target, const
             out_len[b] = len;
             if (accept_tie) accept_tie[b] = atie;
             if (sample_tie) sample_tie[b] = stie;
+            if (sample_lo) sample_lo[b] = T > 0.0 ? wlo : y;
+            if (sample_hi) sample_hi[b] = T > 0.0 ? whi : y;
         } else {
             for (int j = 0; j < M; ++j) {
                 ot[j] = -1;

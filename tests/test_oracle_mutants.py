@@ -31,6 +31,20 @@ MUTANTS = {
     "non_strict_accept": ("if (!((double)u[i] < al))", "if (!((double)u[i] <= al))"),
     "non_strict_cdf": ("if (t < c) {", "if (t <= c) {"),
     "no_residual_clamp": ("w[x] = d > 0.0 ? d : 0.0;", "w[x] = d;"),
+    # the near-tie diagnostics the parity tests rely on
+    "sample_tie_in_cdf_units": ("double d0 = fabs(s - c_prev / S), d1 = fabs(s - c / S);",
+                                "double d0 = fabs(t - c_prev), d1 = fabs(t - c);"),
+    "sample_tie_one_boundary": ("*tie = d0 < d1 ? d0 : d1;", "*tie = d1;"),
+    "accept_tie_over_every_test": (
+        "                if (!decided) {\n                    double d = fabs((double)u[i] - al);\n"
+        "                    if (d < atie) atie = d;",
+        "                double d = fabs((double)u[i] - al);\n                if (d < atie) atie = d;\n"
+        "                if (!decided) {"),
+    "resid_mass_reports_the_point": ("            if (resid_mass) resid_mass[b] = S;\n            if (sample_tie)",
+                                     "            if (resid_mass) resid_mass[b] = S * (double)u[k];\n"
+                                     "            if (sample_tie)"),
+    "window_band_in_cdf_units": ("double t_lo = (s - band) * S, t_hi = (s + band) * S",
+                                 "double t_lo = s * S - band, t_hi = s * S + band"),
 }
 
 
@@ -47,6 +61,13 @@ def _pins_pass(lib):
             return False
         got = enum_cases.joint_from_outputs(res["out_tokens"], res["out_len"], batch["weight"], P, V, k)
         if np.max(np.abs(got - enum_cases.target_joint(P, V, k))) > 1e-12:
+            return False
+    # the near-tie diagnostics against numpy, narrow and wide band
+    from tests.test_oracle_diagnostics import check_linear
+    for seed, band in ((3, 1e-5), (4, 0.02)):
+        try:
+            check_linear(lib, seed=seed, dtype="f32", T=1.0, band=band)
+        except AssertionError:
             return False
     rng = np.random.default_rng(5)
     z = rng.normal(0, 3, 300).astype(np.float32)

@@ -177,6 +177,34 @@ def pin_structure_and_rows_are_checked(lib):
     assert r["status"][5] == 0 and r["out_len"][5] == 3
 
 
+def pin_near_tie_diagnostics_of_a_rejected_fan(lib):
+    """Root with three leaf children, each drafted where q exceeds p most and
+    tested at u ~ 1 (all rejected): alpha, accept_tie, the final residual
+    mass, sample_tie and the draw window against numpy's recursion."""
+    from tests import diag_reference as ref_np
+    rng = np.random.default_rng(44)
+    V, M = 300, 4
+    for _ in range(6):
+        t = rng.normal(0, 2.0, (1, M, V)).astype(np.float32)
+        d = (t + rng.normal(0, 2.0, (1, M, V))).astype(np.float32)
+        fav = np.argsort(d[0, 0].astype(np.float64) - t[0, 0])[::-1][:3]
+        par = np.array([[-1, 0, 0, 0]], np.int32)
+        tok = np.array([[0] + list(fav)], np.int32)
+        u = np.array([[rng.random(), 0.999999, 0.999999, 0.999999]], np.float32)
+        for band in (1e-5, 0.03):
+            r = oracle.tree_verify(t, d, par, tok, np.array([M], np.int32), u, 1.0, lib=lib, tie_band=band)
+            j, atie, alphas, draw = ref_np.root_fan(t[0, 0], d[0, 0], tok[0, 1:], u[0, 1:], float(u[0, 0]), 1.0,
+                                                    band)
+            assert abs(r["accept_tie"][0] - atie) < 1e-12
+            if j >= 0:
+                continue
+            y, S, stie, lo, hi = draw
+            assert r["out_tokens"][0, 0] == y
+            assert abs(r["resid_mass"][0] - S) <= 1e-12 * S
+            assert abs(r["sample_tie"][0] - stie) < 1e-12
+            assert (r["sample_lo"][0], r["sample_hi"][0]) == (lo, hi)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 
@@ -197,6 +225,12 @@ TREE_MUTANTS = {
     "masked_draft_rejected": ("(q[x] == 0.0) ? (r[x] > 0.0 ? INFINITY : 0.0)", "(q[x] == 0.0) ? 0.0"),
     "accepted_parent_token_emitted": ("                on[len] = next;\n                ot[len++] = tok[next];",
                                       "                on[len] = next;\n                ot[len++] = tok[cur];"),
+    "accept_tie_of_rejections_only": ("                if (d < atie) atie = d;\n                if ((double)u[c] < al) {",
+                                      "                if (d < atie && !((double)u[c] < al)) atie = d;\n"
+                                      "                if ((double)u[c] < al) {"),
+    "resid_mass_of_the_normalised_residual": (
+        "                    final_w[(size_t)b * V + x] = w[x] / S;\n            if (resid_mass) resid_mass[b] = S;",
+        "                    final_w[(size_t)b * V + x] = w[x] / S;\n            if (resid_mass) resid_mass[b] = 1.0;"),
     "bonus_from_the_draft": ("                    w[x] = r[x];\n                    S += w[x];",
                              "                    w[x] = prob_of(zd[x], 0.0, 0.0, 1.0);\n                    S += w[x];"),
 }
