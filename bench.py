@@ -52,13 +52,15 @@ def parse():
     ap.add_argument("--workload", default="ragged")
     ap.add_argument("--rotate", type=int, default=4, help="input copies rotated between steps")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="CPU time of the all-threads oracle passes over the benchmark batch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--stages", type=int, default=0, help="staging slots per CTA (0 = automatic)")
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--cluster", type=int, default=0, help="CTAs per sequence (1, 2, 4, 8; 0 = automatic)")
-    ap.add_argument("--aux", default="ragged_dense", help="comma list of extra workloads to time ('' = none)")
+    ap.add_argument("--aux", default="ragged_dense,tiny,qwen_b32,long_draft,grpo",
+                    help="comma list of extra workloads to time ('' = none)")
     ap.add_argument("--kd-steps", type=int, default=100, help="timed calls of the distillation loss (0 = skip)")
     ap.add_argument("--kd-only", action="store_true", help="time only the distillation loss and print its line")
     ap.add_argument("--tree-only", action="store_true", help="time only tree verification and print its line")
@@ -180,33 +182,39 @@ class ClockSampler:
 # the CPU oracle leg (also the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_rate(w, seconds, seed_offset=0):
-    """Time the oracle, as it stands, on a bounded sample of the workload
-    (generated on the host) sized to take about `seconds`."""
-    import torch
-
+def oracle_on_batch(inp, seconds, gpu_out=None):
+    """The CPU-baseline leg: the oracle, as it stands, timed on the host cores
+    on the benchmark's own batch (copied to the host), at one thread (one
+    pass) and at every thread (passes repeated until about `seconds`).  With
+    the GPU's outputs for that batch, the oracle's outputs of the timed pass
+    also give the batch's parity counts (near-ties at 1e-5 and 1e-7)."""
     import oracle
-    from workloads import make_inputs
 
     lib = oracle.load()
     threads = oracle.num_threads(lib)
-    probe = make_inputs(w, device="cpu", B=max(2, threads))
-    t0 = time.perf_counter()
-    r = oracle.verify(probe["target"], probe["draft"], probe["tokens"], probe["draft_len"],
-                      probe["uniforms"], probe["T"], lib=lib)
-    dt = time.perf_counter() - t0
-    per_seq = dt / probe["target"].shape[0] * threads
-    n = int(max(threads, min(w.B * 64, seconds * threads / max(per_seq, 1e-9))))
-    inp = make_inputs(w, device="cpu", B=n)
-    kb = inp["draft_len"].numpy()
-    t0 = time.perf_counter()
-    r = oracle.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"],
-                      inp["T"], lib=lib)
-    dt = time.perf_counter() - t0
+    host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in inp.items()}
+    args = (host["target"], host["draft"], host["tokens"], host["draft_len"], host["uniforms"], host["T"])
+    kb = host["draft_len"].numpy()
     positions = int(np.sum(kb + 1))
-    del torch
-    return {"positions": positions, "seconds": dt, "sequences": n, "threads": threads,
-            "mean_emitted": float(np.mean(r["out_len"]))}
+    t0 = time.perf_counter()
+    oracle.verify(*args, lib=lib, nthreads=1)
+    t1 = time.perf_counter() - t0
+    passes, dt, ref = 0, 0.0, None
+    while dt < seconds or passes < 2:
+        t0 = time.perf_counter()
+        ref = oracle.verify(*args, lib=lib, nthreads=threads)
+        dt += time.perf_counter() - t0
+        passes += 1
+    out = {"positions": positions, "seconds": dt, "passes": passes, "threads": threads,
+           "value_all": positions * passes / dt, "value_1": positions / t1, "seconds_1": t1,
+           "sequences": len(kb)}
+    if gpu_out is not None:
+        from tests.parity import compare
+        toks, lens = gpu_out
+        res = compare(toks, lens, ref, kb)
+        out["parity"] = {k: v for k, v in res.items() if k != "bad"}
+        out["parity"].update({"near_tie_band": 1e-5, "tight_band": 1e-7})
+    return out
 
 
 def reference_arm(args, w):
@@ -606,11 +614,15 @@ def our_arm(args, w):
     for name in [a for a in args.aux.split(",") if a]:
         from workloads import get_workload
         aw = get_workload(name)
-        am = time_workload(svp, aw, args, device, stream, args.rotate, max(1, args.steps // 4), args.warmup)
-        aux[name] = {"workload": aw.describe(), "positions_per_s": am["positions"] / (am["total_ms"] / max(1, args.steps // 4) / 1e3),
-                     "ms_per_step": am["total_ms"] / max(1, args.steps // 4),
-                     "kernel_gbs": am["bytes"] / (am["kernel_ms_mean"] / 1e3) / 1e9,
-                     "frac_of_8tbs": am["bytes"] / (am["kernel_ms_mean"] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+        n_aux = max(1, args.steps // 4)
+        am = time_workload(svp, aw, args, device, stream, args.rotate, n_aux, args.warmup)
+        ms = am["total_ms"] / n_aux
+        gbs = am["bytes"] / (ms / 1e3) / 1e9
+        aux[name] = {"workload": aw.describe(), "positions_per_s": am["positions"] / (ms / 1e3),
+                     "us_per_call": ms * 1e3, "ms_per_step": ms,
+                     "timing": f"{n_aux} calls replayed from one CUDA graph ({am['launch']}), "
+                               f"{args.rotate} rotating input copies",
+                     "gbs": gbs, "frac_of_measured_peak": gbs / peak, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
                      "algorithmic_bytes": am["bytes"], "mean_emitted": am["stats"]["mean_emitted"],
                      "cluster": am["cfg"]["cluster"], "grid_ctas": am["cfg"]["grid_ctas"]}
         del am
@@ -645,11 +657,19 @@ def our_arm(args, w):
         return
 
     cpu = None
+    parity = None
     if not args.no_cpu_baseline:
-        r = oracle_sample_rate(w, args.cpu_seconds)
-        cpu = {"value": r["positions"] / r["seconds"], "unit": UNIT, "cores": r["threads"], "kind": "oracle",
-               "sample": f"{r['sequences']} sequences of {w.describe()} (host-generated), "
-                         f"{r['seconds']:.1f} s with {r['threads']} OpenMP threads"}
+        ver, base = m["ver"], m["base_inputs"]
+        toks, lens = ver.verify(base["target"], base["draft"], base["tokens"], base["draft_len"], base["uniforms"],
+                                base["T"], stream=stream)
+        stream.synchronize()
+        r = oracle_on_batch(base, args.cpu_seconds, (toks.cpu().numpy(), lens.cpu().numpy()))
+        cpu = {"value": r["value_all"], "unit": UNIT, "cores": r["threads"], "kind": "oracle",
+               "value_1_thread": r["value_1"],
+               "sample": f"the benchmark batch itself ({r['sequences']} sequences of {w.describe()}, copied to "
+                         f"the host): {r['passes']} passes in {r['seconds']:.1f} s on {r['threads']} OpenMP "
+                         f"threads; one pass in {r['seconds_1']:.1f} s on 1 thread"}
+        parity = r.get("parity")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -667,6 +687,9 @@ def our_arm(args, w):
         "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
                      "frac": kern_gbs / peak, "peak_source": peak_kind,
                      "traffic": profiled_traffic(w.name), "kernel": KERNEL_NAME,
+                     "traffic_source": f"dram__bytes_read.sum + dram__bytes_write.sum per launch from the "
+                                       f"committed ncu summary profiles/{KERNEL_NAME}_{w.name}.md, used only "
+                                       f"when its source hash matches this kernel (else null)",
                      "launch_ms": launch_ms, "eager_launch_ms_mean": m["kernel_ms_mean"],
                      "eager_launch_ms_median": m["kernel_ms_median"], "eager_launch_ms_best": m["kernel_ms_best"]},
         "clocks": m["clocks"], "clock_soak_steps": m["soak_steps"],
@@ -674,7 +697,7 @@ def our_arm(args, w):
         "gpu_launches": 2 * args.steps,   # per call: the work-list kernel and the verify kernel
         "acceptance": {"mean_emitted": stats["mean_emitted"], "mean_accepted": stats["mean_accepted"],
                        "accept_rate": stats["accept_rate"], "spec_off": stats["spec_off"]},
-        "cpu_baseline": cpu, "aux": aux or None,
+        "cpu_baseline": cpu, "parity": parity, "aux": aux or None,
     }
     print(json.dumps(line), flush=True)
     if pg:

@@ -37,6 +37,7 @@
 #include <utility>
 
 #include "../../include/specverify.h"
+#include "sv_internal.h"
 
 namespace {
 
@@ -349,7 +350,9 @@ void release(sv_ctrl* c) {
 
 // Launch with programmatic stream serialisation (see wait_for_predecessor).
 template <typename... KArgs, typename... Args>
-sv_status launch_pdl(void (*kernel)(KArgs...), int ctas, int threads, cudaStream_t s, Args&&... args) {
+sv_status launch_pdl(const char* name, void (*kernel)(KArgs...), int ctas, int threads, cudaStream_t s,
+                     Args&&... args) {
+  sv::NvtxRange range(name);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -444,7 +447,7 @@ sv_status spec_ctrl_reset(sv_ctrl* c, int n, const int32_t* seq_ids, sv_stream_t
   }
   if (n < 0 || n > c->n_slots) return SV_ERR_INVALID_ARG;
   if (n == 0) return SV_OK;
-  return launch_pdl(ctrl_forget_kernel, (n + 255) / 256, 256, s, c->A, c->N, seq_ids, n, c->n_slots, c->err);
+  return launch_pdl("spec_ctrl_reset", ctrl_forget_kernel, (n + 255) / 256, 256, s, c->A, c->N, seq_ids, n, c->n_slots, c->err);
 }
 
 sv_status spec_ctrl_observe(sv_ctrl* c, int B, const int32_t* seq_ids, const int32_t* draft_len,
@@ -453,7 +456,7 @@ sv_status spec_ctrl_observe(sv_ctrl* c, int B, const int32_t* seq_ids, const int
   if (B == 0) return SV_OK;
   if (!seq_ids || !draft_len || !out_len) return SV_ERR_INVALID_ARG;
   ObserveParams p{c->A, c->N, c->claim, c->err, seq_ids, draft_len, out_len, B, c->n_slots, c->max_k, c->decay};
-  return launch_pdl(ctrl_observe_kernel, 1, kObserveThreads, reinterpret_cast<cudaStream_t>(stream), p);
+  return launch_pdl("spec_ctrl_observe", ctrl_observe_kernel, 1, kObserveThreads, reinterpret_cast<cudaStream_t>(stream), p);
 }
 
 static sv_status launch_choose(sv_ctrl* c, int B, const int32_t* seq_ids, int32_t* next_len, int32_t* choice,
@@ -477,7 +480,7 @@ static sv_status launch_choose(sv_ctrl* c, int B, const int32_t* seq_ids, int32_
   p.cta_max = c->cta_max;
   p.ticket = c->ticket;
   const int ctas = B < 1 ? 1 : (B + kChooseThreads - 1) / kChooseThreads;
-  return launch_pdl(ctrl_choose_kernel, ctas < kChooseMaxCtas ? ctas : kChooseMaxCtas, kChooseThreads,
+  return launch_pdl("spec_ctrl_choose", ctrl_choose_kernel, ctas < kChooseMaxCtas ? ctas : kChooseMaxCtas, kChooseThreads,
                     reinterpret_cast<cudaStream_t>(stream), p);
 }
 

@@ -122,10 +122,68 @@ __device__ __forceinline__ f2 sub2(f2 a, f2 b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ f2 exp2_2(f2 t) {
   float a, b;
   unpack2(t, a, b);
   return pack2(fast_exp2(a), fast_exp2(b));
+}
+
+// 1 - 2^d, accurate relative to the result as d -> 0 (where 1 - ex2(d)
+// would cancel).  For d > -1/4, i.e. |y| < ln(2)/4 with y = d ln 2, the
+// Taylor series of -expm1(y) = -(y + y^2/2! + ... + y^6/6!) in Horner form
+// (truncation below 6e-9 relative); below, 1 - 2^d >= 0.16 and the
+// subtraction loses nothing.  d >= 0 gives a result <= 0 (or NaN for
+// d = +inf), which callers clamp away.  The scalar and the packed form round
+// identically, lane by lane.
+constexpr float kLn2f = 0.693147180559945309f;
+constexpr float kSmallDelta = -0.25f;
+__device__ __forceinline__ float one_minus_exp2(float d) {
+  const float y = __fmul_rn(d, kLn2f);
+  float s = __fmaf_rn(y, 1.f / 720.f, 1.f / 120.f);
+  s = __fmaf_rn(y, s, 1.f / 24.f);
+  s = __fmaf_rn(y, s, 1.f / 6.f);
+  s = __fmaf_rn(y, s, 0.5f);
+  s = __fmaf_rn(y, s, 1.f);
+  const float small = -__fmul_rn(y, s);
+  const float big = __fsub_rn(1.f, fast_exp2(d));
+  return d > kSmallDelta ? small : big;
+}
+__device__ __forceinline__ f2 one_minus_exp2_2(f2 d) {
+  // the series lane by lane: scalar multiply-adds take their constants as
+  // immediates, where the packed form would hold seven constant pairs in
+  // registers
+  float d0, d1;
+  unpack2(d, d0, d1);
+  return pack2(one_minus_exp2(d0), one_minus_exp2(d1));
+}
+
+// Residual weight max(0, p - q) of one logit pair without cancellation:
+// with log2 p = z_t c - K_t - L_t and log2 q = z_d c - K_d - L_d,
+//   p - q = p (1 - 2^delta),  delta = log2 q - log2 p = (z_d - z_t) c + G,
+// G = (K_t + L_t) - (K_d + L_d) the log2 ratio of the two normalisers, held
+// as an unevaluated sum Gh + Gl of two floats.  The fused multiply-add
+// rounds (z_d - z_t) c + Gh once, at the magnitude of delta itself, so delta
+// (and the weight, relative to itself) stays accurate where p ~ q.  Returns
+// the weight and sets p.
+__device__ __forceinline__ float resid_weight(float zt, float zd, float c, float Kt, float Lt, float Gh, float Gl,
+                                              float& p) {
+  p = fast_exp2(__fsub_rn(__fmaf_rn(zt, c, -Kt), Lt));
+  const float delta = __fadd_rn(__fmaf_rn(__fsub_rn(zd, zt), c, Gh), Gl);
+  return fmaxf(__fmul_rn(p, one_minus_exp2(delta)), 0.f);
+}
+// The same for two pairs at once (bit-identical to the scalar form).
+__device__ __forceinline__ void resid_weight2(f2 zt, f2 zd, f2 cc, f2 nkt, f2 nlt, f2 gh, f2 gl, f2& p, float& w0,
+                                              float& w1) {
+  p = exp2_2(add2(fma2(zt, cc, nkt), nlt));
+  const f2 delta = add2(fma2(sub2(zd, zt), cc, gh), gl);
+  unpack2(mul2(p, one_minus_exp2_2(delta)), w0, w1);
+  w0 = fmaxf(w0, 0.f);
+  w1 = fmaxf(w1, 0.f);
 }
 
 // Bounded wait on an mbarrier phase.  Returns false if `limit_ns` passed

@@ -3,8 +3,19 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 namespace sv {
+
+// A named NVTX range over the host code that enqueues a kernel (header-only
+// NVTX v3: a no-op unless a profiler is attached), so that a timeline or an
+// ncu --nvtx filter can tell the library's launches apart.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kConsumerWarps = 16;                      // warps that compute
 constexpr int kThreads = (kConsumerWarps + 3) * 32;     // + producer, control and walker warps

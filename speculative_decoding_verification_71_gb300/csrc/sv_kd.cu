@@ -534,6 +534,7 @@ extern "C" sv_status spec_kd_loss(int n_seq, int t_len, int V, sv_dtype dtype, c
   auto aligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
   p.bulk = (row_bytes % 16 == 0) && aligned(target_logits) && aligned(draft_logits) &&
            (grad == nullptr || aligned(grad));
+  sv::NvtxRange range("spec_kd_loss");
   cudaError_t e;
   if (elt == 2)
     e = with_grad ? cudaLaunchKernelEx(&cfg, kd_kernel<2, true>, p, D->failed)

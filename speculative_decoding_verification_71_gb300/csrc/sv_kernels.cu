@@ -62,7 +62,8 @@ namespace {
 //   kind 2:     chunk `chunk` of the re-read of this CTA's slice of the
 //               rejected pair at pos: the first half of the slot holds target
 //               logits, the second half the draft logits of the same range;
-//               K0, L0, K1, L1 are the pair's normalisers;
+//               K0, L0 are the target row's normaliser, G0 + G1 the log2
+//               ratio of the target's to the draft's normaliser;
 //   kind 3:     end of a sequence cut short (early exit): no data;
 //   kind -1:    no more work; x = draws inserted in all.
 struct Desc {
@@ -70,7 +71,7 @@ struct Desc {
   int chunk, nchunks, x, rec;  // x: drafted token at pos (rows of pairs, else -1); rec: record slot
   int seq, pad;                // seq: sequences streamed before this one
   float u, s;                  // accept uniform at pos, sampling uniform of b
-  float K0, L0, K1, L1;
+  float K0, L0, G0, G1;
 };
 
 // A finished row, published by the consumer warps for the control warp.
@@ -105,7 +106,8 @@ struct SeqRec {
   volatile int decided;        // pairs decided so far (early exit)
   volatile int stop;           // a rejection or an error: later rows are not needed
   float s;                     // sampling uniform
-  float Kt, Lt, Kd, Ld;        // normalisers of the rejected pair
+  float Kt, Lt;                // target normaliser of the rejected pair
+  float Gh, Gl;                // log2 (target / draft normaliser) of that pair, as Gh + Gl
   int tok[32];                 // drafted tokens, taken from the rows as they pass
 };
 
@@ -116,7 +118,8 @@ struct WalkReq {
   int v0, b, pos;              // first vector of the segment (-1: nothing to walk), row
   int pad;
   double t;                    // target weight left at the segment's start
-  float K0, L0, K1, L1;        // normalisers of the target (0) and draft (1) rows
+  float K0, L0;                // normaliser of the target row
+  float Gh, Gl;                // residual walks: log2 (target / draft normaliser) as Gh + Gl
 };
 
 constexpr int kRecs = 32;          // sequence records (ring)
@@ -165,7 +168,7 @@ struct Ctrl {
   WalkReq wreq[kWalkReqs];          // control warp -> walker warp
   volatile int wreq_head, wreq_tail;
   volatile int ctl_done;            // the control warp has left
-  float pairK, pairL, pairZx;       // target row of the current pair
+  float pairK, pairL, pairZx, pairS;  // target row of the current pair (pairS: its sum of 2^(z c - K))
 };
 
 constexpr int kCtrlBytes = ((static_cast<int>(sizeof(Ctrl)) + 1023) / 1024) * 1024;
@@ -393,7 +396,7 @@ struct Verifier {
       const int rc = pend % kRecs;
       if (!all && rows - C.pend_end[rc] < lag_rows && streamed - pend < kMaxPending) return true;
       int res = 0, drw = 0, b = 0, pos = 0;
-      float Kt = 0.f, Lt = 0.f, Kd = 0.f, Ld = 0.f;
+      float Kt = 0.f, Lt = 0.f, Gh = 0.f, Gl = 0.f;
       if (lane == 0) {
         const unsigned long long t0 = global_ns();
         while (true) {
@@ -405,7 +408,7 @@ struct Verifier {
           __threadfence_block();
           const SeqRec& R = C.rec[rc];
           drw = R.draw; b = R.b; pos = R.a;
-          Kt = R.Kt; Lt = R.Lt; Kd = R.Kd; Ld = R.Ld;
+          Kt = R.Kt; Lt = R.Lt; Gh = R.Gh; Gl = R.Gl;
         } else {
           atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
         }
@@ -430,7 +433,7 @@ struct Verifier {
             d.b = b; d.kb = 0; d.pos = pos; d.kind = 2;
             d.chunk = c; d.nchunks = ndraw; d.x = -1; d.rec = rc; d.seq = pend;
             d.u = 0.f; d.s = 0.f;
-            d.K0 = Kt; d.L0 = Lt; d.K1 = Kd; d.L1 = Ld;
+            d.K0 = Kt; d.L0 = Lt; d.G0 = Gh; d.G1 = Gl;
             if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(2 * bytes));
           }
           fill(dst, srcT, off, bytes, &C.full[slot], false, 0);
@@ -665,7 +668,7 @@ struct Verifier {
         __syncwarp();
         if (lane == 0) mbar_arrive(&C.empty[slot]);
         const f2 cc = pack2(c2, c2), nkt = pack2(-d.K0, -d.K0), nlt = pack2(-d.L0, -d.L0);
-        const f2 nkd = pack2(-d.K1, -d.K1), nld = pack2(-d.L1, -d.L1);
+        const f2 gh = pack2(d.G0, d.G0), gl = pack2(d.G1, d.G1);
         f2 accr[NV / 2], accp[NV / 2];
 #pragma unroll
         for (int i = 0; i < NV / 2; ++i) { accr[i] = 0ull; accp[i] = 0ull; }
@@ -676,11 +679,12 @@ struct Verifier {
           V::pairs(rd[j], zd);
 #pragma unroll
           for (int i = 0; i < NV / 2; ++i) {
-            // the same roundings as the scalar fmaf(z, c, -K) - L of the walk
-            const f2 p = exp2_2(add2(fma2(zt[i], cc, nkt), nlt));
-            float d0, d1;
-            unpack2(sub2(p, exp2_2(add2(fma2(zd[i], cc, nkd), nld))), d0, d1);
-            accr[i] = add2(accr[i], pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f)));
+            // max(0, p - q) as p (1 - 2^delta): no cancellation where p ~ q;
+            // the same roundings as the scalar resid_weight of the walk
+            f2 p;
+            float w0, w1;
+            resid_weight2(zt[i], zd[i], cc, nkt, nlt, gh, gl, p, w0, w1);
+            accr[i] = add2(accr[i], pack2(w0, w1));
             accp[i] = add2(accp[i], p);
           }
         }
@@ -892,8 +896,8 @@ struct Verifier {
   // per step, to the token where the running weight passes t.
   // RESID: weights max(0, p - q); else p.
   template <int NSTEPS, bool RESID>
-  __device__ int walk(int v0, double t, const unsigned char* rowT, const unsigned char* rowD,
-                      float Kt, float Lt, float Kd, float Ld) const {
+  __device__ __noinline__ int walk(int v0, double t, const unsigned char* rowT, const unsigned char* rowD,
+                      float Kt, float Lt, float Gh, float Gl) const {
     uint4 rt[NSTEPS], rd[RESID ? NSTEPS : 1];
 #pragma unroll
     for (int j = 0; j < NSTEPS; ++j) {
@@ -910,8 +914,9 @@ struct Verifier {
       float ls = 0.f;
 #pragma unroll
       for (int e = 0; e < NV; ++e) {
-        const float p = fast_exp2(fmaf(zt[e], P.c2, -Kt) - Lt);
-        w[e] = RESID ? fmaxf(p - fast_exp2(fmaf(zd[e], P.c2, -Kd) - Ld), 0.f) : p;
+        float p;
+        if (RESID) w[e] = resid_weight(zt[e], zd[e], P.c2, Kt, Lt, Gh, Gl, p);
+        else w[e] = fast_exp2(__fsub_rn(__fmaf_rn(zt[e], P.c2, -Kt), Lt));
         ls += w[e];
       }
       const float incl = warp_incl_scan(ls, lane);
@@ -1040,7 +1045,7 @@ struct Verifier {
           y = walk<kVecsPerLane, false>(r.v0, r.t, row_ptr(r.b, r.pos, 0), nullptr, r.K0, r.L0, 0.f, 0.f);
         else if (r.mode == 1)
           y = walk<kDrawVecsPerLane, true>(r.v0, r.t, row_ptr(r.b, r.pos, 0), row_ptr(r.b, r.pos, 1),
-                                           r.K0, r.L0, r.K1, r.L1);
+                                           r.K0, r.L0, r.Gh, r.Gl);
         else
           y = walk<kDrawVecsPerLane, false>(r.v0, r.t, row_ptr(r.b, r.pos, 0), nullptr, r.K0, r.L0, 0.f, 0.f);
       }
@@ -1116,7 +1121,7 @@ struct Verifier {
       if (lane == 0) mbar_expect_tx(&C.xrow_ready[xs], static_cast<uint32_t>(cs * sizeof(RowPart)));
       if (in) mbar_arrive_peer(peer(&C.xrow_free[xs], lane));
     }
-    const float L = log2f(Ssum);
+    const float L = static_cast<float>(log2(static_cast<double>(Ssum)));
     SeqRec& R = C.rec[d.rec];
     const size_t b = static_cast<size_t>(d.b);
     const bool diag = (rank == 0);
@@ -1152,26 +1157,34 @@ struct Verifier {
             P.ws.m_t[b * (P.k + 1) + d.pos] = M;
             P.ws.L_t[b * (P.k + 1) + d.pos] = L;
           }
-          C.pairK = K; C.pairL = L; C.pairZx = zx;
+          C.pairK = K; C.pairL = L; C.pairZx = zx; C.pairS = Ssum;
         } else if (diag) {
           P.ws.m_d[b * P.k + d.pos] = M;
           P.ws.L_d[b * P.k + d.pos] = L;
         }
         if (d.kind == 1 && !R.err) {
-          // the pair is complete: acceptance test of draft d.pos
+          // the pair is complete: acceptance test of draft d.pos.  With
+          // G = log2 of the target's over the draft's normaliser (in double,
+          // from the rows' (K, sum) pairs), log2 (p(x) / q(x)) =
+          // (z_t(x) - z_d(x)) c - G; alpha = min(1, p/q) and u < alpha are
+          // taken in double.
           const float zt = C.pairZx, zd = zx;
-          float alpha;
-          if (zt == -INFINITY) alpha = 0.f;               // p(x) = 0
-          else if (zd == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
+          const double G = (static_cast<double>(C.pairK) - static_cast<double>(K)) +
+                           log2(static_cast<double>(C.pairS) / static_cast<double>(Ssum));
+          double alpha;
+          if (zt == -INFINITY) alpha = 0.0;               // p(x) = 0
+          else if (zd == -INFINITY) alpha = 1.0;          // q(x) = 0 < p(x)
           else {
-            const float log2r = (fmaf(zt, c2, -C.pairK) - C.pairL) - (fmaf(zd, c2, -K) - L);
-            alpha = log2r >= 0.f ? 1.f : exp2f(log2r);
+            const double log2r = (static_cast<double>(zt) - static_cast<double>(zd)) * static_cast<double>(c2) - G;
+            alpha = log2r >= 0.0 ? 1.0 : exp2(log2r);
           }
-          if (diag) P.ws.alpha[b * P.k + d.pos] = alpha;
-          if (!(d.u < alpha) && R.a < 0) {
+          if (diag) P.ws.alpha[b * P.k + d.pos] = static_cast<float>(alpha);
+          if (!(static_cast<double>(d.u) < alpha) && R.a < 0) {
             // first rejection: the pair is read again for the residual draw
             R.a = d.pos;
-            R.Kt = C.pairK; R.Lt = C.pairL; R.Kd = K; R.Ld = L;
+            R.Kt = C.pairK; R.Lt = C.pairL;
+            R.Gh = static_cast<float>(G);
+            R.Gl = static_cast<float>(G - static_cast<double>(R.Gh));
           }
         } else if (last && R.a < 0 && !R.err) {
           bonus = 1;   // every draft accepted: the bonus draw
@@ -1222,7 +1235,7 @@ struct Verifier {
         WalkReq wr;
         wr.rec = d.rec; wr.mode = 0; wr.v0 = seg >= 0 ? v_lo + seg * kVecsPerWarp : -1;
         wr.b = d.b; wr.pos = d.kb; wr.pad = 0; wr.t = seg_t;
-        wr.K0 = K; wr.L0 = L; wr.K1 = 0.f; wr.L1 = 0.f;
+        wr.K0 = K; wr.L0 = L; wr.Gh = 0.f; wr.Gl = 0.f;
         push_walk(wr);       // the walker writes the outputs and frees the record
         settle = 0;
       }
@@ -1273,7 +1286,7 @@ struct Verifier {
       WalkReq wr;
       wr.rec = rc; wr.mode = resid ? 1 : 2; wr.v0 = seg >= 0 ? v_lo + seg * kDrawVecsPerWarp : -1;
       wr.b = R.b; wr.pos = R.a; wr.pad = 0; wr.t = seg_t;
-      wr.K0 = R.Kt; wr.L0 = R.Lt; wr.K1 = R.Kd; wr.L1 = R.Ld;
+      wr.K0 = R.Kt; wr.L0 = R.Lt; wr.Gh = R.Gh; wr.Gl = R.Gl;
       push_walk(wr);       // the walker writes the outputs and frees the record
     } else {
       if (rank == fin_rank) finish_sequence(rc);
@@ -1586,6 +1599,7 @@ cudaError_t query_max_clusters(int cluster, int smem_bytes, int* out) {
 }
 
 cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s) {
+  NvtxRange range("spec_verify");
   plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -1602,12 +1616,14 @@ cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaS
 
 cudaError_t launch_compact(int B, int k, const int* out_tokens, const int* out_len,
                            int* packed, int* offsets, cudaStream_t s) {
+  NvtxRange range("spec_verify_compact");
   compact_kernel<<<1, kCompactThreads, 0, s>>>(B, k, out_tokens, out_len, packed, offsets);
   return cudaGetLastError();
 }
 
 cudaError_t launch_debug(const Workspace& ws, int B, int k, int greedy, float inv_T, double* lse_t,
                          double* lse_d, double* accept_prob, double* mass, cudaStream_t s) {
+  NvtxRange range("spec_verify_debug");
   const int n = B * (k + 1);
   debug_kernel<<<(n + 255) / 256, 256, 0, s>>>(ws, B, k, greedy, inv_T, lse_t, lse_d, accept_prob, mass);
   return cudaGetLastError();

@@ -179,7 +179,8 @@ struct TreeShared {
   float csum[kTreeMaxChunks];        // chunk sums of the last weight pass (this CTA's chunks)
   double cc, PP, invPP;              // residual after the rejections so far: max(0, p - cc q) / PP
   double invSt, invSd;               // 1 / S^t, 1 / S^d of the current node
-  float wA, wB;                      // weights of the last pass: max(0, A 2^(z^t c - K^t) - B 2^(z^d c - K^d))
+  float wA, wGh, wGl;                // weights of the last pass: max(0, A 2^(z^t c - K^t) - B 2^(z^d c - K^d)),
+                                     // as A 2^(z^t c - K^t) (1 - 2^delta), delta = (z^d - z^t) c + Gh + Gl
   float wm[kTreeWarps], ws[kTreeWarps], wmd[kTreeWarps], wsd[kTreeWarps];
   int wbad[kTreeWarps], widx[kTreeWarps];
   float Kt, St, Kd, Sd;              // row statistics of the current node (whole row)
@@ -289,10 +290,14 @@ __device__ void combine_stats(float m, float K, float s, float& Kout, float& Sou
 // with A, B fixed for the pass: the bonus weights are A = 1, B = 0; the
 // residual after one more rejection A = 1 / (S^t P), B = (c + P) / (S^d P);
 // r itself (zero-residual fallback) A = 1 / (S^t P), B = c / (S^d P).
-__device__ __forceinline__ float pair_weight(float zt, float zd, float c2, float Kt, float Kd, float A, float B) {
-  const float et = fast_exp2(fmaf(zt, c2, -Kt));
-  const float ed = fast_exp2(fmaf(zd, c2, -Kd));
-  return fmaxf(fmaf(A, et, -B * ed), 0.f);
+// The difference is taken without cancellation where A e^t ~ B e^d:
+//   w = A e^t (1 - 2^delta),  delta = (z^d - z^t) c + G,
+//   G = log2(B / A) + K^t - K^d  (in double, held as Gh + Gl; B = 0 gives
+//   Gh = -inf, Gl = 0, so w = A e^t).
+__device__ __forceinline__ float pair_weight(float zt, float zd, float c2, float Kt, float A, float Gh, float Gl) {
+  const float et = fast_exp2(__fmaf_rn(zt, c2, -Kt));
+  const float delta = __fadd_rn(__fmaf_rn(__fsub_rn(zd, zt), c2, Gh), Gl);
+  return fmaxf(__fmul_rn(__fmul_rn(A, et), one_minus_exp2(delta)), 0.f);
 }
 // The bonus weight: no draft row (K^d may be -inf at a node without children).
 __device__ __forceinline__ float bonus_weight(float zt, float c2, float Kt) { return fast_exp2(fmaf(zt, c2, -Kt)); }
@@ -323,16 +328,18 @@ __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParam
                             const unsigned char* rd, int mode, int c_lo, int c_hi, int& xp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    if (mode == 0) {
-      sh.wA = 1.f;
-      sh.wB = 0.f;
-    } else {
-      sh.wA = static_cast<float>(sh.invPP * sh.invSt);
-      sh.wB = static_cast<float>((mode == 1 ? sh.cc + sh.PP : sh.cc) * sh.invPP * sh.invSd);
+    sh.wA = mode == 0 ? 1.f : static_cast<float>(sh.invPP * sh.invSt);
+    sh.wGh = -INFINITY;
+    sh.wGl = 0.f;
+    const double BA = (mode == 1 ? sh.cc + sh.PP : sh.cc) * (static_cast<double>(sh.St) / static_cast<double>(sh.Sd));
+    if (mode != 0 && BA > 0.0) {
+      const double G = log2(BA) + (static_cast<double>(sh.Kt) - static_cast<double>(sh.Kd));
+      sh.wGh = static_cast<float>(G);
+      sh.wGl = static_cast<float>(G - static_cast<double>(sh.wGh));
     }
   }
   __syncthreads();
-  const float c2 = P.c2, Kt = sh.Kt, Kd = sh.Kd, A = sh.wA, B = sh.wB;
+  const float c2 = P.c2, Kt = sh.Kt, A = sh.wA, Gh = sh.wGh, Gl = sh.wGl;
   Chunks<ELT>::each(ring, rt, rd, mode != 0, c_lo, c_hi, P.V, P.vec,
                     [&](int c, int, const float (&zt)[8], const float (&zd)[8]) {
     float part = 0.f;
@@ -341,7 +348,7 @@ __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParam
       for (int j = 0; j < 8; ++j) part += bonus_weight(zt[j], c2, Kt);
     } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) part += pair_weight(zt[j], zd[j], c2, Kt, Kd, A, B);
+      for (int j = 0; j < 8; ++j) part += pair_weight(zt[j], zd[j], c2, Kt, A, Gh, Gl);
     }
     part = warp_sum(part);
     if (lane == 0) sh.csum[c] = part;
@@ -425,7 +432,8 @@ __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt
   int lastw = -1;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    w[j] = mode == 0 ? bonus_weight(zt[j], P.c2, sh.Kt) : pair_weight(zt[j], zd[j], P.c2, sh.Kt, sh.Kd, sh.wA, sh.wB);
+    w[j] = mode == 0 ? bonus_weight(zt[j], P.c2, sh.Kt)
+                     : pair_weight(zt[j], zd[j], P.c2, sh.Kt, sh.wA, sh.wGh, sh.wGl);
     wpart += w[j];
     if (w[j] > 0.f) lastw = e0 + j;
   }
@@ -668,13 +676,20 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         const int c = sh.kids[i];
         const long long x = sh.tok[c];
         const float zt = Vec<ELT>::scalar(rt, x), zd = Vec<ELT>::scalar(rd, x);
-        const double p = static_cast<double>(fast_exp2(fmaf(zt, c2, -sh.Kt))) * sh.invSt;
-        const double q = static_cast<double>(fast_exp2(fmaf(zd, c2, -sh.Kd))) * sh.invSd;
-        const double r = fmax(p - sh.cc * q, 0.0) * sh.invPP;
-        // u < min(1, r / q) with u in [0, 1): u q < r (q = 0: accept iff r > 0)
-        const double u = static_cast<double>(sh.u[c]);
-        const bool acc = (q == 0.0) ? (r > 0.0) : (u * q < r);
-        if (P.alpha && lead) P.alpha[rb + c] = static_cast<float>((q == 0.0) ? (r > 0.0 ? 1.0 : 0.0) : fmin(1.0, r / q));
+        // r(x) / q(x) = max(0, p(x)/q(x) - c) / P, with p(x)/q(x) from its
+        // logarithm in double: (z^t - z^d) c - (K^t - K^d) - log2(S^t / S^d)
+        double rq;
+        if (zd == -INFINITY) rq = zt == -INFINITY ? 0.0 : INFINITY;    // q(x) = 0: r > 0 iff p > 0
+        else if (zt == -INFINITY) rq = 0.0;                            // p(x) = 0
+        else {
+          const double l2 = (static_cast<double>(zt) - static_cast<double>(zd)) * static_cast<double>(c2) -
+                            (static_cast<double>(sh.Kt) - static_cast<double>(sh.Kd)) -
+                            log2(static_cast<double>(sh.St) / static_cast<double>(sh.Sd));
+          rq = fmax(exp2(l2) - sh.cc, 0.0) * sh.invPP;
+        }
+        const double al = fmin(1.0, rq);
+        const bool acc = static_cast<double>(sh.u[c]) < al;
+        if (P.alpha && lead) P.alpha[rb + c] = static_cast<float>(al);
         sh.next = acc ? c : -1;
       }
       __syncthreads();
@@ -869,5 +884,6 @@ extern "C" sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtyp
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  sv::NvtxRange range("spec_verify_tree");
   return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -1,19 +1,20 @@
 """Parity of tree verification (``spec_verify_tree``, through the C ABI) with
 the fp64 oracle.
 
-The kernel computes each probability in fp32 (ex2.approx, sums over the row,
-~2e-6 relative) and each test in fp64 from those.  The first child's
-acceptance probability min(1, p(x)/q(x)) is therefore within ~1e-6 of the
-oracle's; after a rejection the residual (r - q) / S cancels, and its error
-grows to ~2e-6 max(1, p/q) / S with S the residual mass (>= ~0.02 in these
-inputs): up to ~1e-4.  The draw's CDF position is off by ~1e-6 / S (the
-normalisations of p and q do not cancel in max(0, p - q)), below 1e-5 here.
-Sequences whose oracle walk came within 1e-4 of a test threshold, or within
-1e-5 of a CDF boundary of the drawn token, are near-ties: excluded and
-counted.  A draw from a diffuse tail lands that close to a boundary whenever
-the drawn token's probability is that small, so up to a quarter of the
-sequences (plus two) may be near-ties.  Every other sequence must match the
-oracle exactly: tokens, accepted nodes and lengths.
+The kernel sums each row in fp32 (ex2.approx) and takes each test in fp64
+from those sums: p(x)/q(x) from its logarithm, (z^t - z^d) c minus the log2
+ratio of the row sums, and after h rejections r(x)/q(x) = max(0, p/q - c_h)
+/ P_h with c_h, P_h from the residual masses.  The residual weights are
+formed as A e^t (1 - 2^delta), with no cancellation where p ~ c_h q, so the
+masses carry the rows' fp32 error (~1e-7 relative) and the tests come within
+1e-5 of the oracle's.  A sequence whose oracle walk came within 1e-5 of a
+test threshold is a near-tie (excluded and counted); one whose draw came
+within 1e-5 of a CDF boundary must still match on its accepted path and draw
+a token inside the oracle's window of valid draws.  A draw from a diffuse
+tail lands that close to a boundary whenever the drawn token's probability
+is that small, so up to a quarter of the sequences (plus two) may be
+near-ties.  Every other sequence must match the oracle exactly: tokens,
+accepted nodes and lengths.
 """
 import dataclasses
 
@@ -29,7 +30,7 @@ from workloads import get_tree_workload, make_tree_inputs, get_workload, make_in
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-ACCEPT_TIE = 1e-4
+ACCEPT_TIE = 1e-5
 SAMPLE_TIE = 1e-5
 
 
@@ -51,17 +52,29 @@ def run_gpu(inp, alpha=True):
 def run_ref(inp):
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     return oracle.tree_verify(cpu["target"], cpu["draft"], cpu["parents"], cpu["tokens"], cpu["n_nodes"],
-                              cpu["uniforms"], cpu["T"])
+                              cpu["uniforms"], cpu["T"], tie_band=SAMPLE_TIE)
 
 
 def compare(g, ref, T):
+    """Exact match outside near-ties; at a sampling near-tie the accepted
+    path matches and the drawn token lies in the oracle's window.  Returns
+    the number of near-tie sequences."""
     ot, on, ol, st, al = g
-    near = (ref["accept_tie"] < ACCEPT_TIE) | (ref["sample_tie"] < SAMPLE_TIE) if T > 0 else np.zeros(len(ol), bool)
-    ok = ~near
+    B = len(ol)
+    a_near = ref["accept_tie"] < ACCEPT_TIE if T > 0 else np.zeros(B, bool)
+    s_near = (ref["sample_tie"] < SAMPLE_TIE) & ~a_near if T > 0 else np.zeros(B, bool)
+    ok = ~(a_near | s_near)
     np.testing.assert_array_equal(st, ref["status"] & 0xff)
     np.testing.assert_array_equal(ol[ok], ref["out_len"][ok])
     np.testing.assert_array_equal(ot[ok], ref["out_tokens"][ok])
     np.testing.assert_array_equal(on[ok], ref["out_nodes"][ok])
+    for b in np.nonzero(s_near)[0]:
+        n = int(ref["out_len"][b])
+        assert ol[b] == n, (b, ol[b], n)
+        np.testing.assert_array_equal(on[b], ref["out_nodes"][b])
+        np.testing.assert_array_equal(ot[b, :n - 1], ref["out_tokens"][b, :n - 1])
+        assert ref["sample_lo"][b] <= ot[b, n - 1] <= ref["sample_hi"][b], (b, ot[b, n - 1])
+    near = a_near | s_near
     if al is not None:
         ra = ref["alpha"]
         both = ok[:, None] & ~np.isnan(ra)

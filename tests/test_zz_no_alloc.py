@@ -45,6 +45,41 @@ def test_noalloc_matches_context_entry_point_twice():
         np.testing.assert_array_equal(out_t.cpu().numpy(), ref_t.cpu().numpy())
 
 
+MORE_CASES = [
+    ("ragged", dict(B=64, k=3, V=8192, T=0.0, seed=33)),          # greedy: no draft rows, no uniforms used
+    ("tiny", dict()),                                              # fp32, the small workload
+    ("tiny", dict(B=4096, k=3, V=256, seed=34)),                   # B (k + 1) = 16384: the array's capacity
+]
+
+
+def test_noalloc_greedy_fp32_and_full_capacity():
+    """Greedy and fp32 instances, and a batch that fills the array, each twice
+    in a row: equal to the context entry point (itself checked against the
+    oracle) and to the oracle, and nothing written past the batch's rows."""
+    import oracle
+    svbuild.build()
+    for name, over in MORE_CASES:
+        w = get_workload(name, **over)
+        inp = make_inputs(w, device="cuda")
+        ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+        ref_t, ref_l = ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"],
+                                  inp["uniforms"], inp["T"])
+        ref = oracle.verify(inp["target"].cpu(), inp["draft"].cpu(), inp["tokens"].cpu(), inp["draft_len"].cpu(),
+                            inp["uniforms"].cpu(), inp["T"])
+        far = (ref["accept_tie"] >= 1e-5) & (ref["sample_tie"] >= 1e-5)
+        for _ in range(2):
+            # outputs inside larger buffers: the rows after the batch must keep their sentinel
+            big_t = torch.full((w.B + 8, w.k + 1), -77, dtype=torch.int32, device="cuda")
+            big_l = torch.full((w.B + 8,), -77, dtype=torch.int32, device="cuda")
+            _noalloc_abi(inp, big_t[:w.B], big_l[:w.B])
+            got_t, got_l = big_t[:w.B].cpu().numpy(), big_l[:w.B].cpu().numpy()
+            np.testing.assert_array_equal(got_l, ref_l.cpu().numpy())
+            np.testing.assert_array_equal(got_t, ref_t.cpu().numpy())
+            np.testing.assert_array_equal(got_l[far], ref["out_len"][far])
+            np.testing.assert_array_equal(got_t[far], ref["out_tokens"][far])
+            assert bool((big_t[w.B:] == -77).all()) and bool((big_l[w.B:] == -77).all())
+
+
 def test_noalloc_rejects_sizes_beyond_the_array():
     svbuild.build()
     lib = svp.load_library()
