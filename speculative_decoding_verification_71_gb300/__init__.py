@@ -31,6 +31,7 @@ SV_OK, SV_ERR_INVALID_ARG, SV_ERR_BAD_DRAFT_LEN, SV_ERR_BAD_TOKEN = 0, 1, 2, 3
 SV_ERR_NONFINITE, SV_ERR_TIMEOUT, SV_ERR_CUDA, SV_ERR_UNSUPPORTED = 4, 5, 6, 7
 SV_F32, SV_BF16 = 0, 1
 SV_CTRL_BATCH, SV_CTRL_PER_SEQUENCE = 0, 1
+SV_KERNEL_AUTO, SV_KERNEL_CLUSTER, SV_KERNEL_PIECES = 0, 1, 2
 SV_CTRL_MAX_POINTS = 12
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
     "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_get_config", "sv_launch_shape",
-    "sv_set_wait_limit_ns",
+    "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for",
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
     "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_set_cost", "spec_ctrl_set_params", "spec_ctrl_reset",
     "spec_ctrl_observe", "spec_ctrl_choose", "spec_ctrl_alpha", "spec_ctrl_status",
@@ -109,6 +110,10 @@ def load_library(path: str | None = None):
     lib.sv_set_early_exit.argtypes = [P, c.c_int]
     lib.sv_set_cluster.restype = c.c_int
     lib.sv_set_cluster.argtypes = [P, c.c_int]
+    lib.sv_set_kernel.restype = c.c_int
+    lib.sv_set_kernel.argtypes = [P, c.c_int]
+    lib.sv_kernel_for.restype = c.c_int
+    lib.sv_kernel_for.argtypes = [P, c.c_int, c.POINTER(c.c_int)]
     lib.sv_get_config.restype = c.c_int
     lib.sv_get_config.argtypes = [P] + [c.POINTER(c.c_int)] * 6
     lib.spec_kd_loss.restype = c.c_int
@@ -316,6 +321,20 @@ class SpecVerifier:
         st = self.lib.sv_set_cluster(self._ctx, int(cluster))
         if st != SV_OK:
             self._raise(st, "sv_set_cluster")
+
+    def set_kernel(self, kernel: int):
+        """SV_KERNEL_AUTO (default), SV_KERNEL_CLUSTER or SV_KERNEL_PIECES."""
+        st = self.lib.sv_set_kernel(self._ctx, int(kernel))
+        if st != SV_OK:
+            self._raise(st, "sv_set_kernel")
+
+    def kernel_for(self, B: int) -> int:
+        """The kernel a call with batch B runs on 16-byte aligned rows."""
+        kern = ctypes.c_int()
+        st = self.lib.sv_kernel_for(self._ctx, int(B), ctypes.byref(kern))
+        if st != SV_OK:
+            self._raise(st, "sv_kernel_for")
+        return kern.value
 
     def set_early_exit(self, on: bool):
         """Skip the rows of a sequence after its first rejection once it is

@@ -30,6 +30,11 @@ struct sv_ctx {
   long long wait_limit_ns = sv::kDrainLimitNs;
   void* ws_mem = nullptr;
   sv::Workspace ws{};
+  void* pw_mem = nullptr;      // workspace of the pieces kernel (null: not available)
+  sv::PiecesWs pw{};
+  int kernel = SV_KERNEL_AUTO;
+  int pieces_ctas = 0;         // grid of the pieces kernel (one CTA per SM)
+  int np = 0, pe = 0, nr = 0, he = 0;
   long long calls = 0;
   int last_B = 0, last_k = 0, last_greedy = 0;
   float last_inv_T = 1.f;
@@ -90,6 +95,63 @@ sv_status configure(sv_ctx* ctx, int stages, int ctas_per_sm) {
 sv_status configure_auto(sv_ctx* ctx) {
   if (configure(ctx, 3, 0) == SV_OK) return SV_OK;
   return configure(ctx, 2, 0);
+}
+
+// Whether a call with batch B (rows 16-byte aligned) runs the pieces kernel.
+bool use_pieces(const sv_ctx* ctx, int B) {
+  if (ctx->kernel != SV_KERNEL_PIECES || !ctx->pw_mem || ctx->pieces_ctas <= 0) return false;
+  if (ctx->early_exit || ctx->cluster != 0) return false;
+  return B <= sv::kPiecesMaxB;
+}
+
+// The pieces kernel's workspace for (max_B, max_k) and rows of V logits:
+// one allocation, 256-byte aligned sub-arrays.  Also the launch shape.
+sv_status create_pieces(sv_ctx* ctx) {
+  sv::pieces_shape(ctx->V, ctx->elt, ctx->np, ctx->pe, ctx->nr, ctx->he);
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, ctx->device);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDeviceProperties");
+  if (sv::pieces_smem_bytes() > static_cast<int>(prop.sharedMemPerBlockOptin)) return SV_OK;
+  e = sv::prepare_pieces_kernel();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(pieces)");
+  // batches above kPiecesMaxB run the cluster kernel
+  const size_t B = static_cast<size_t>(ctx->max_B < sv::kPiecesMaxB ? ctx->max_B : sv::kPiecesMaxB);
+  const size_t k = static_cast<size_t>(ctx->max_k);
+  const size_t rows = B * (2 * k + 1);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
+  const size_t o_rowpart = take(rows * ctx->np * 16);
+  const size_t o_seqcnt = take(B * 4), o_bseg = take(B * ctx->np * 16 * 8);
+  const size_t o_rmass = take(B * ctx->nr * 16 * 4), o_pmass = take(B * ctx->nr * 16 * 4);
+  const size_t o_rcnt = take(B * 4), o_rflag = take(B * 4), o_rq = take(B * 16), o_rqn = take(B * 16);
+  // re-read pieces go round-robin to the CTAs: each receives at most
+  // ceil(B nr / ctas) of them
+  const size_t ctas = static_cast<size_t>(prop.multiProcessorCount);
+  const size_t mcap = (B * ctx->nr + ctas - 1) / ctas + 1;
+  const size_t o_mbox = take(ctas * mcap * 4), o_mtail = take(ctas * 32 * 4);
+  const size_t o_ctr = take(64 * 4), o_grp = take(33 * 4);
+  e = cudaMalloc(&ctx->pw_mem, off);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc(pieces workspace)");
+  e = cudaMemset(ctx->pw_mem, 0, off);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemset(pieces workspace)");
+  char* base = static_cast<char*>(ctx->pw_mem);
+  sv::PiecesWs& w = ctx->pw;
+  w.rowpart = reinterpret_cast<float4*>(base + o_rowpart);
+  w.seqcnt = reinterpret_cast<int*>(base + o_seqcnt);
+  w.bseg = reinterpret_cast<float2*>(base + o_bseg);
+  w.rmass = reinterpret_cast<float*>(base + o_rmass);
+  w.pmass = reinterpret_cast<float*>(base + o_pmass);
+  w.rcnt = reinterpret_cast<int*>(base + o_rcnt);
+  w.rflag = reinterpret_cast<int*>(base + o_rflag);
+  w.rq = reinterpret_cast<int4*>(base + o_rq);
+  w.rqn = reinterpret_cast<float4*>(base + o_rqn);
+  w.mbox = reinterpret_cast<int*>(base + o_mbox);
+  w.mtail = reinterpret_cast<int*>(base + o_mtail);
+  w.mcap = static_cast<int>(mcap);
+  w.ctr = reinterpret_cast<int*>(base + o_ctr);
+  w.grp = reinterpret_cast<int*>(base + o_grp);
+  ctx->pieces_ctas = prop.multiProcessorCount;   // one CTA per SM (the shared memory allows no more)
+  return SV_OK;
 }
 
 // Cluster size and grid of a call with batch B.
@@ -201,6 +263,14 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
     delete ctx;
     return s;
   }
+  s = create_pieces(ctx);
+  if (s != SV_OK) {
+    std::snprintf(g_create_msg, sizeof g_create_msg, "%s", ctx->cuda_msg);
+    cudaFree(ctx->ws_mem);
+    if (ctx->pw_mem) cudaFree(ctx->pw_mem);
+    delete ctx;
+    return s;
+  }
   *out = ctx;
   return SV_OK;
 }
@@ -208,6 +278,10 @@ sv_status sv_create(sv_ctx** out, int max_B, int max_k, int V, sv_dtype dtype) {
 sv_status sv_destroy(sv_ctx* ctx) {
   if (!ctx) return SV_OK;
   cudaError_t e = cudaFree(ctx->ws_mem);
+  if (ctx->pw_mem) {
+    const cudaError_t e2 = cudaFree(ctx->pw_mem);
+    if (e == cudaSuccess) e = e2;
+  }
   delete ctx;
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -249,6 +323,12 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   // persistent grid: every cluster that fits at once, but never more than sequences
   int ctas = 0;
   launch_shape(ctx, B, &p.cluster, &ctas);
+  if (p.bulk && use_pieces(ctx, B)) {
+    p.pieces = 1;
+    p.np = ctx->np; p.pe = ctx->pe; p.nr = ctx->nr; p.he = ctx->he;
+    p.ctas = ctx->pieces_ctas;
+    p.pw = ctx->pw;
+  }
   cudaError_t e = sv::launch_verify(p, ctas, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch verify");
   ctx->calls += 1;
@@ -360,6 +440,18 @@ sv_status sv_launch_shape(const sv_ctx* ctx, int B, int* cluster, int* grid_ctas
   launch_shape(ctx, B, &cs, &ctas);
   if (cluster) *cluster = cs;
   if (grid_ctas) *grid_ctas = ctas;
+  return SV_OK;
+}
+
+sv_status sv_set_kernel(sv_ctx* ctx, int kernel) {
+  if (!ctx || kernel < SV_KERNEL_AUTO || kernel > SV_KERNEL_PIECES) return SV_ERR_INVALID_ARG;
+  ctx->kernel = kernel;
+  return SV_OK;
+}
+
+sv_status sv_kernel_for(const sv_ctx* ctx, int B, int* kernel) {
+  if (!ctx || B < 1 || B > ctx->max_B || !kernel) return SV_ERR_INVALID_ARG;
+  *kernel = use_pieces(ctx, B) ? SV_KERNEL_PIECES : SV_KERNEL_CLUSTER;
   return SV_OK;
 }
 

@@ -134,32 +134,48 @@ __device__ __forceinline__ f2 exp2_2(f2 t) {
 }
 
 // 1 - 2^d, accurate relative to the result as d -> 0 (where 1 - ex2(d)
-// would cancel).  For d > -1/4, i.e. |y| < ln(2)/4 with y = d ln 2, the
-// Taylor series of -expm1(y) = -(y + y^2/2! + ... + y^6/6!) in Horner form
-// (truncation below 6e-9 relative); below, 1 - 2^d >= 0.16 and the
-// subtraction loses nothing.  d >= 0 gives a result <= 0 (or NaN for
-// d = +inf), which callers clamp away.  The scalar and the packed form round
-// identically, lane by lane.
-constexpr float kLn2f = 0.693147180559945309f;
+// would cancel).  For d > -1/4 the Taylor series of
+// 1 - 2^d = -(sum over n >= 1 of (d ln 2)^n / n!) up to n = 6, in Horner form
+// in d with c_n = (ln 2)^n / n! (truncation below 6e-9 relative); below -1/4,
+// 1 - 2^d >= 0.16 and the subtraction loses nothing.  d >= 0 gives a result
+// <= 0 (or NaN for d = +inf), which callers clamp away.  The scalar and the
+// packed form round identically, lane by lane.
 constexpr float kSmallDelta = -0.25f;
 __device__ __forceinline__ float one_minus_exp2(float d) {
-  const float y = __fmul_rn(d, kLn2f);
-  float s = __fmaf_rn(y, 1.f / 720.f, 1.f / 120.f);
-  s = __fmaf_rn(y, s, 1.f / 24.f);
-  s = __fmaf_rn(y, s, 1.f / 6.f);
-  s = __fmaf_rn(y, s, 0.5f);
-  s = __fmaf_rn(y, s, 1.f);
-  const float small = -__fmul_rn(y, s);
+  float s = __fmaf_rn(d, 1.5403530393381609e-4f, 1.3333558146428443e-3f);   // c6, c5
+  s = __fmaf_rn(d, s, 9.6181291076284772e-3f);                               // c4
+  s = __fmaf_rn(d, s, 5.5504108664821580e-2f);                               // c3
+  s = __fmaf_rn(d, s, 2.4022650695910071e-1f);                               // c2
+  s = __fmaf_rn(d, s, 6.9314718055994531e-1f);                               // c1 = ln 2
+  const float small = -__fmul_rn(d, s);
   const float big = __fsub_rn(1.f, fast_exp2(d));
   return d > kSmallDelta ? small : big;
 }
 __device__ __forceinline__ f2 one_minus_exp2_2(f2 d) {
-  // the series lane by lane: scalar multiply-adds take their constants as
-  // immediates, where the packed form would hold seven constant pairs in
-  // registers
+  // lane by lane: scalar multiply-adds take their constants as immediates,
+  // where the packed form would hold six constant pairs in registers
   float d0, d1;
   unpack2(d, d0, d1);
   return pack2(one_minus_exp2(d0), one_minus_exp2(d1));
+}
+
+// a + b = s + e exactly (Knuth's TwoSum, six operations, no branch).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// G = (Ka - Kb) + log2(Sa / Sb), the log2 ratio of two normalisers 2^K S,
+// as an unevaluated sum gh + gl: the difference of the K's is carried
+// exactly, so the only roundings are those of Sa / Sb and of its log2 (a
+// small number when the rows are alike).
+__device__ __forceinline__ void log2_ratio(float Ka, float Sa, float Kb, float Sb, float& gh, float& gl) {
+  float s1, e1, s2, e2;
+  two_sum(Ka, -Kb, s1, e1);
+  two_sum(s1, log2f(__fdiv_rn(Sa, Sb)), s2, e2);
+  gh = s2;
+  gl = __fadd_rn(e1, e2);
 }
 
 // Residual weight max(0, p - q) of one logit pair without cancellation:

@@ -54,6 +54,27 @@ struct Workspace {
   unsigned int* err_word;     // sticky OR of (1 << code)
 };
 
+// Workspace of the piece-streaming kernel (sv_pieces.cu), owned by the
+// context.  Rows are numbered r = b (k+1) + i for target rows and
+// B (k+1) + b k + i for draft rows.  Every counter is zero when a call
+// starts (plan_kernel clears them).
+struct PiecesWs {
+  float4* rowpart;   // [rows * np]  one piece's (M, K, S, bad) (greedy: M, arg, 0, bad)
+  int* seqcnt;       // [B]          pieces of the sequence reduced so far
+  float2* bseg;      // [B * np * 16]  the bonus row's segment (K, S), one per consumer warp and piece
+  float* rmass;      // [B * nr * 16]  residual masses of the re-read pieces of a rejected pair
+  float* pmass;      // [B * nr * 16]  target masses of the same segments (zero-residual fallback)
+  int* rcnt;         // [B]          residual pieces reduced
+  int* rflag;        // [B]          error bits seen in the residual pieces
+  int4* rq;          // [B]          the rejected pair of sequence b: (a, k_b, 0, 0)
+  float4* rqn;       // [B]          ... and (K_t, L_t, Gh, Gl) of the pair
+  int* mbox;         // [ctas * mcap] re-read pieces handed to each CTA: b * nr + j + 1 (0: not yet written)
+  int* mtail;        // [ctas * 32]  messages handed to each CTA (one 128-byte line per CTA)
+  int mcap;          //              mailbox slots per CTA
+  int* ctr;          // [64]         [32] sequences settled (its own line)
+  int* grp;          // [33]         sequences per draft length (plan_kernel)
+};
+
 struct VerifyParams {
   const void* target;   // [B, k+1, V]
   const void* draft;    // [B, k, V]
@@ -72,6 +93,12 @@ struct VerifyParams {
   int early_exit;       // 1: rows after a decided rejection are not read
   long long wait_limit_ns;
   Workspace ws;
+  // piece streaming (sv_pieces.cu) instead of the cluster kernel when set
+  int pieces;
+  int np, pe;           // pieces per row and logits per piece (pe * elt <= 64 KB, a multiple of 64)
+  int nr, he;           // re-read pieces per rejected pair and logits of each row per piece (<= 32 KB)
+  int ctas;             // grid of the piece kernel (its first ticket per CTA is its index)
+  PiecesWs pw;
 };
 
 // Launchers (sv_kernels.cu).
@@ -87,6 +114,22 @@ cudaError_t launch_init_workspace(const Workspace& ws, cudaStream_t s);
 
 // Shared-memory bytes of the verify kernel with `stages` staging slots.
 int verify_smem_bytes(int stages);
+
+// The piece-streaming kernel (sv_pieces.cu).
+constexpr int kPiecesMaxB = 2048;                         // sequences per call
+constexpr int kPiecesStages = 3;                          // 64 KB staging slots per CTA
+int pieces_smem_bytes();
+cudaError_t prepare_pieces_kernel();
+cudaError_t launch_pieces(const VerifyParams& p, cudaStream_t s);   // after plan_kernel
+// Pieces per row / logits per piece for rows of V logits of elt bytes, and
+// the same for the re-read of a pair (half slots).
+inline void pieces_shape(int V, int elt, int& np, int& pe, int& nr, int& he) {
+  const long long row = static_cast<long long>(V) * elt;
+  np = static_cast<int>((row + kChunkBytes - 1) / kChunkBytes);
+  pe = ((V + np - 1) / np + 63) / 64 * 64;
+  nr = static_cast<int>((row + kChunkBytes / 2 - 1) / (kChunkBytes / 2));
+  he = ((V + nr - 1) / nr + 63) / 64 * 64;
+}
 
 // Cluster size chosen when the caller leaves it open.  A sequence is the
 // unit of work of a cluster, so with few sequences per cluster the last ones

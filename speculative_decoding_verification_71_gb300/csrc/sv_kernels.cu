@@ -211,6 +211,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
   for (int i = tid; i < B * k; i += kPlanThreads) {
     ws.m_d[i] = NAN; ws.L_d[i] = NAN; ws.alpha[i] = NAN;
   }
+  if (P.pieces) {
+    // the piece kernel's counters start from zero
+    const PiecesWs& pw = P.pw;
+    for (int i = tid; i < B; i += kPlanThreads) {
+      pw.seqcnt[i] = 0; pw.rcnt[i] = 0; pw.rflag[i] = 0;
+    }
+    for (int i = tid; i < P.ctas * pw.mcap; i += kPlanThreads) pw.mbox[i] = 0;
+    for (int i = tid; i < P.ctas; i += kPlanThreads) pw.mtail[i * 32] = 0;
+    if (tid < 64) pw.ctr[tid] = 0;
+  }
   if (tid == 0) { base = 0; *ws.ticket = 0; }
   __syncthreads();
   // counting sort by k_b, largest first, stable in b
@@ -247,6 +257,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
       if (tid == kPlanThreads - 1) base += warp_cnt[31] + __popc(m);
       __syncthreads();
     }
+    if (P.pieces && tid == 0) P.pw.grp[L] = base;   // sequences with k_b >= L
   }
   if (tid == 0) *ws.n_seqs = base;
 }
@@ -521,8 +532,11 @@ struct Verifier {
         }
         if (P.early_exit && cs > 1 && kind == 0 && pos >= exit_lag) {
           // early exit in a cluster, decided the same way in every CTA: wait
-          // for the control warp's decision on pair pos - exit_lag; after a
-          // rejection (or an error) the rest of the sequence is not read
+          // for the control warp's decision on pair pos - exit_lag; if the
+          // first rejection is at or before that pair, the rest of the
+          // sequence is not read.  The test looks at the rejection's pair,
+          // not at whether one has been seen by now, which would depend on
+          // each CTA's timing.
           int stop = 0, seen = 0;
           if (lane == 0) {
             const unsigned long long t0 = global_ns();
@@ -530,7 +544,7 @@ struct Verifier {
               const SeqRec& R = C.rec[rc];
               if (R.seq_tag == streamed && R.decided > pos - exit_lag) {
                 __threadfence_block();
-                stop = R.stop;
+                stop = (R.a >= 0 && R.a <= pos - exit_lag) ? 1 : 0;
                 seen = 1;
                 break;
               }
@@ -896,7 +910,7 @@ struct Verifier {
   // per step, to the token where the running weight passes t.
   // RESID: weights max(0, p - q); else p.
   template <int NSTEPS, bool RESID>
-  __device__ __noinline__ int walk(int v0, double t, const unsigned char* rowT, const unsigned char* rowD,
+  __device__ int walk(int v0, double t, const unsigned char* rowT, const unsigned char* rowD,
                       float Kt, float Lt, float Gh, float Gl) const {
     uint4 rt[NSTEPS], rd[RESID ? NSTEPS : 1];
 #pragma unroll
@@ -1121,7 +1135,7 @@ struct Verifier {
       if (lane == 0) mbar_expect_tx(&C.xrow_ready[xs], static_cast<uint32_t>(cs * sizeof(RowPart)));
       if (in) mbar_arrive_peer(peer(&C.xrow_free[xs], lane));
     }
-    const float L = static_cast<float>(log2(static_cast<double>(Ssum)));
+    const float L = log2f(Ssum);
     SeqRec& R = C.rec[d.rec];
     const size_t b = static_cast<size_t>(d.b);
     const bool diag = (rank == 0);
@@ -1164,27 +1178,25 @@ struct Verifier {
         }
         if (d.kind == 1 && !R.err) {
           // the pair is complete: acceptance test of draft d.pos.  With
-          // G = log2 of the target's over the draft's normaliser (in double,
-          // from the rows' (K, sum) pairs), log2 (p(x) / q(x)) =
-          // (z_t(x) - z_d(x)) c - G; alpha = min(1, p/q) and u < alpha are
-          // taken in double.
+          // G = Gh + Gl the log2 ratio of the target's to the draft's
+          // normaliser, log2 (q(x) / p(x)) = delta = (z_d(x) - z_t(x)) c + G
+          // (the residual weights' delta) and alpha = min(1, 2^-delta)
           const float zt = C.pairZx, zd = zx;
-          const double G = (static_cast<double>(C.pairK) - static_cast<double>(K)) +
-                           log2(static_cast<double>(C.pairS) / static_cast<double>(Ssum));
-          double alpha;
-          if (zt == -INFINITY) alpha = 0.0;               // p(x) = 0
-          else if (zd == -INFINITY) alpha = 1.0;          // q(x) = 0 < p(x)
+          float Gh, Gl;
+          log2_ratio(C.pairK, C.pairS, K, Ssum, Gh, Gl);
+          float alpha;
+          if (zt == -INFINITY) alpha = 0.f;               // p(x) = 0
+          else if (zd == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
           else {
-            const double log2r = (static_cast<double>(zt) - static_cast<double>(zd)) * static_cast<double>(c2) - G;
-            alpha = log2r >= 0.0 ? 1.0 : exp2(log2r);
+            const float delta = __fadd_rn(__fmaf_rn(__fsub_rn(zd, zt), c2, Gh), Gl);
+            alpha = delta <= 0.f ? 1.f : exp2f(-delta);
           }
-          if (diag) P.ws.alpha[b * P.k + d.pos] = static_cast<float>(alpha);
-          if (!(static_cast<double>(d.u) < alpha) && R.a < 0) {
+          if (diag) P.ws.alpha[b * P.k + d.pos] = alpha;
+          if (!(d.u < alpha) && R.a < 0) {
             // first rejection: the pair is read again for the residual draw
             R.a = d.pos;
             R.Kt = C.pairK; R.Lt = C.pairL;
-            R.Gh = static_cast<float>(G);
-            R.Gl = static_cast<float>(G - static_cast<double>(R.Gh));
+            R.Gh = Gh; R.Gl = Gl;
           }
         } else if (last && R.a < 0 && !R.err) {
           bonus = 1;   // every draft accepted: the bonus draw
@@ -1603,6 +1615,7 @@ cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaS
   plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.pieces) return launch_pieces(p, s);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
   verify_config(cfg, attr, p.cluster, ctas, smem_bytes, s);

@@ -68,9 +68,55 @@ SMALL_CASES = [
 ]
 
 
+KERNELS = [svp.SV_KERNEL_PIECES, svp.SV_KERNEL_CLUSTER]
+KERNEL_IDS = ["pieces", "cluster"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("name,over", SMALL_CASES, ids=[f"{n}-{o}" for n, o in SMALL_CASES])
-def test_small_cases(name, over):
-    assert_parity(small(name, **over))
+def test_small_cases(name, over, kernel):
+    inp = small(name, **over)
+    ver = verifier_for(inp)
+    ver.set_kernel(kernel)
+    assert_parity(inp, ver)
+
+
+def test_kernel_choice():
+    """The cluster kernel is the default; the pieces kernel, when asked for,
+    runs aligned batches up to 2048 sequences unless a cluster size or early
+    exit is set."""
+    inp = small("ragged", B=8, k=3, V=4096)
+    ver = verifier_for(inp)
+    assert ver.kernel_for(8) == svp.SV_KERNEL_CLUSTER       # the default
+    ver.set_kernel(svp.SV_KERNEL_PIECES)
+    assert ver.kernel_for(8) == svp.SV_KERNEL_PIECES
+    ver.set_cluster(2)
+    assert ver.kernel_for(8) == svp.SV_KERNEL_CLUSTER
+    ver.set_cluster(0)
+    ver.set_early_exit(True)
+    assert ver.kernel_for(8) == svp.SV_KERNEL_CLUSTER
+    ver.set_early_exit(False)
+    assert ver.kernel_for(8) == svp.SV_KERNEL_PIECES
+    with pytest.raises(svp.SpecVerifyError):
+        ver.set_kernel(3)
+    big = svp.SpecVerifier(5000, 1, 64, torch.float32)
+    big.set_kernel(svp.SV_KERNEL_PIECES)
+    assert big.kernel_for(2048) == svp.SV_KERNEL_PIECES and big.kernel_for(2049) == svp.SV_KERNEL_CLUSTER
+
+
+def test_both_kernels_agree_away_from_ties():
+    """Two schedules of one rule: identical outputs wherever the oracle's
+    decision is not a near-tie (the row sums are added in another order)."""
+    inp = small("ragged", B=128, k=3, V=65536)
+    ref = run_oracle(inp)
+    outs = []
+    for kern in KERNELS:
+        ver = verifier_for(inp)
+        ver.set_kernel(kern)
+        outs.append(run_gpu(ver, inp))
+    far = (ref["accept_tie"] >= NEAR_TIE) & (ref["sample_tie"] >= NEAR_TIE)
+    np.testing.assert_array_equal(outs[0][1][far], outs[1][1][far])
+    np.testing.assert_array_equal(outs[0][0][far], outs[1][0][far])
 
 
 @pytest.mark.parametrize("stages,ctas", [(2, 1), (3, 0), (3, 1)])
@@ -337,15 +383,18 @@ def test_wait_timeout_is_reported_not_hung():
 
 # --- full-size workloads: every sequence against the oracle ---------------------
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("name", ["qwen_b32", "ragged", "ragged_dense", "long_draft", "grpo"])
-def test_full_size_workload(name):
+def test_full_size_workload(name, kernel):
     """The batch at its full size, in the launch shape the benchmark times
-    (automatic cluster, three staging slots): invariants and the oracle on
+    (the kernel it chooses, and the other one): invariants and the oracle on
     every sequence, LSE / alpha / mass of every row and draw, near-ties
     counted and reported."""
     w = get_workload(name)
     inp = make_inputs(w, device=DEV)
     ver = verifier_for(inp)
+    ver.set_kernel(kernel)
+    assert ver.kernel_for(w.B) == kernel
     ver.reset_stats()
     toks, lens = run_gpu(ver, inp)
     kb = inp["draft_len"].cpu().numpy()
@@ -355,7 +404,7 @@ def test_full_size_workload(name):
     ref = run_oracle(inp)
     res = compare(toks, lens, ref, kb)
     worst = compare_diagnostics(ver.debug(w.B, w.k), ref, kb, lens)
-    report(f"full:{name}", res, worst, cluster=ver.launch_shape(w.B)[0])
+    report(f"full:{name}:{KERNEL_IDS[KERNELS.index(kernel)]}", res, worst, cluster=ver.launch_shape(w.B)[0])
     assert res["mismatch"] == 0, res["bad"][:10]
     assert max(worst.values()) < 1.0, worst
 
