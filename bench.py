@@ -74,6 +74,9 @@ def parse():
     ap.add_argument("--tree-workloads", default="tree,tree_wide", help="tree workloads timed in the aux block")
     ap.add_argument("--ctrl-steps", type=int, default=200,
                     help="timed rounds of the draft-length controller (0 = skip)")
+    ap.add_argument("--profile-kernels", default="",
+                    help="run each named kernel's representative case twice (for ncu, one kernel per "
+                         "capture): comma list of verify, pieces, early_exit, compact, debug, kd, tree, ctrl")
     return ap.parse_args()
 
 
@@ -636,10 +639,16 @@ def our_arm(args, w):
             n = max(1, args.steps // 4)
             on = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=True)
             off = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=False)
+            # rows not read, from the kernel's own count over the timed calls
+            needed = int(np.sum(2 * on["base_inputs"]["draft_len"].cpu().numpy().astype(np.int64) + 1))
+            skipped = on["stats"]["rows_skipped"] / n
             runs.append({"workload": ew.describe() + f" draft noise {sigma}", "ms_per_step_on": on["total_ms"] / n,
                          "ms_per_step_off": off["total_ms"] / n,
                          "positions_per_s_on": on["positions"] / (on["total_ms"] / n / 1e3),
                          "speedup": off["total_ms"] / on["total_ms"], "mean_emitted": on["stats"]["mean_emitted"],
+                         "rows_needed_per_call": needed, "rows_skipped_per_call": skipped,
+                         "bytes_skipped_per_call": skipped * ew.V * ew.elt, "skipped_fraction": skipped / needed,
+                         "time_saved_fraction": 1.0 - on["total_ms"] / off["total_ms"],
                          "cluster": on["cfg"]["cluster"]})
             del on, off
         aux["early_exit"] = runs
@@ -736,11 +745,105 @@ def tree_only(args):
     print(json.dumps({"tree_verify": out}), flush=True)
 
 
+def profile_kernels(args):
+    """Each named kernel's case, run twice on cuda:0 (the first launch warms
+    up, ncu captures the second with -s/-c): the small but L2-exceeding
+    inputs the ncu summaries under profiles/ are taken on.
+
+      verify      spec_verify, cluster kernel: plan_kernel + verify_kernel on the ragged workload
+      pieces      the same batch through the pieces kernel: plan_kernel + verify_pieces_kernel
+      early_exit  long draft, B=128 (k=7, V=151936, T=0.6), early exit on: plan_kernel + verify_kernel
+      compact     compact_kernel on the ragged batch's outputs
+      debug       debug_kernel after the ragged batch
+      kd          spec_kd_loss with the gradient, 16 rollouts x 64 positions, V=151936 bf16:
+                  kd_kernel + kd_loss_kernel
+      tree        spec_verify_tree on the tree workload (B=64, 15 nodes, V=151936 bf16): tree_kernel
+      ctrl        spec_ctrl_observe + spec_ctrl_choose (B=1024 slots, max_k=7): ctrl_observe_kernel +
+                  ctrl_choose_kernel
+    """
+    import torch
+
+    import speculative_decoding_verification_71_gb300 as svp
+    from speculative_decoding_verification_71_gb300 import build as svbuild
+    from workloads import get_tree_workload, get_workload, make_inputs, make_tree_inputs
+
+    svbuild.build()
+    lib = svp.load_library()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    names = [n for n in args.profile_kernels.split(",") if n]
+    w = get_workload("ragged")
+    inp = make_inputs(w, device=device)
+    ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+    run = lambda v, i: v.verify(i["target"], i["draft"], i["tokens"], i["draft_len"], i["uniforms"], i["T"])
+    ot, ol = run(ver, inp)
+    for name in names:
+        for _ in range(2):
+            if name == "verify":
+                ot, ol = run(ver, inp)
+            elif name == "pieces":
+                pv = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+                pv.set_kernel(svp.SV_KERNEL_PIECES)
+                run(pv, inp)
+            elif name == "early_exit":
+                ew = get_workload("long_draft", B=128)
+                ei = make_inputs(ew, device=device)
+                ev = svp.SpecVerifier(ew.B, ew.k, ew.V, ew.torch_dtype)
+                ev.set_early_exit(True)
+                run(ev, ei)
+            elif name == "compact":
+                ver.compact(ot, ol)
+            elif name == "debug":
+                ver.debug(w.B, w.k)
+            elif name == "kd":
+                g = torch.Generator(device=device).manual_seed(11)
+                n_seq, t_len, V = 16, 64, 151936
+                t = torch.randn(n_seq, t_len, V, generator=g, device=device) * 3.0
+                d = (t + torch.randn(n_seq, t_len, V, generator=g, device=device) * 0.7).to(torch.bfloat16)
+                t = t.to(torch.bfloat16)
+                wts = torch.rand(n_seq, generator=g, device=device)
+                row_kl = torch.empty(n_seq, t_len, device=device)
+                loss = torch.empty(n_seq, device=device)
+                grad = torch.empty_like(t)
+                st = lib.spec_kd_loss(n_seq, t_len, V, svp.SV_BF16, t.data_ptr(), d.data_ptr(), wts.data_ptr(), 1.0,
+                                      row_kl.data_ptr(), loss.data_ptr(), grad.data_ptr(), None)
+                assert st == svp.SV_OK, st
+                del t, d, grad
+            elif name == "tree":
+                tw = get_tree_workload("tree")
+                ti = make_tree_inputs(tw, device=device)
+                svp.verify_tree(ti["target"], ti["draft"], ti["parents"], ti["tokens"], ti["n_nodes"], ti["uniforms"],
+                                ti["T"])
+                del ti
+            elif name == "ctrl":
+                B, K = 1024, 7
+                rng = np.random.default_rng(0)
+                c = svp.DraftController(B, K)
+                c.set_cost(np.array([1, 64, 256, 1024], np.int32),
+                           1.0 + np.array([0.02, 0.1, 0.3, 0.9])[:, None] * np.arange(K + 1)[None])
+                ids = torch.arange(B, dtype=torch.int32, device=device)
+                kb = torch.from_numpy(rng.integers(0, K + 1, B).astype(np.int32)).to(device)
+                on = torch.minimum(kb + 1, torch.ones_like(kb) * 3)
+                nxt = torch.empty(B, dtype=torch.int32, device=device)
+                ch = torch.empty(1, dtype=torch.int32, device=device)
+                c.observe(ids, kb, on)
+                c.choose(ids, nxt, ch)
+            else:
+                raise SystemExit(f"unknown kernel case {name}")
+            torch.cuda.synchronize()
+    st, stats = ver.stats()
+    print(json.dumps({"profile_kernels": names, "status": st}), flush=True)
+    if st != svp.SV_OK:
+        raise SystemExit(f"device error {st}")
+
+
 def main():
     args = parse()
     from workloads import get_workload
     w = get_workload(args.workload)
-    if args.kd_only:
+    if args.profile_kernels:
+        profile_kernels(args)
+    elif args.kd_only:
         kd_only(args)
     elif args.tree_only:
         tree_only(args)

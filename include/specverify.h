@@ -91,6 +91,7 @@ typedef struct {
     long long zero_residual;   /* rejections whose residual mass was exactly 0 */
     long long error_sequences; /* sequences that emitted nothing because of a device error */
     unsigned int error_bits;   /* OR of (1 << code) over device errors seen */
+    long long rows_skipped;    /* early exit: needed logit rows not read (each row once) */
 } sv_stats;
 
 /* Human-readable name of a status code (static string). */

@@ -58,6 +58,7 @@ class Stats(ctypes.Structure):
         ("drafts_accepted", ctypes.c_longlong), ("emitted", ctypes.c_longlong),
         ("spec_off", ctypes.c_longlong), ("zero_residual", ctypes.c_longlong),
         ("error_sequences", ctypes.c_longlong), ("error_bits", ctypes.c_uint),
+        ("rows_skipped", ctypes.c_longlong),
     ]
 
     def as_dict(self):

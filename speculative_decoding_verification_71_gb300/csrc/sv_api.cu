@@ -376,6 +376,7 @@ sv_status spec_verify_stats(sv_ctx* ctx, sv_stream_t stream, sv_stats* out) {
   out->zero_residual = static_cast<long long>(st[sv::kStatZeroResidual]);
   out->error_sequences = static_cast<long long>(st[sv::kStatErrorSeqs]);
   out->error_bits = word;
+  out->rows_skipped = static_cast<long long>(st[sv::kStatRowsSkipped]);
   if (out->sequences > 0) {
     out->mean_emitted = static_cast<double>(out->emitted) / static_cast<double>(out->sequences);
     out->mean_accepted = static_cast<double>(out->drafts_accepted) / static_cast<double>(out->sequences);

@@ -36,6 +36,7 @@ enum StatSlot {
   kStatSpecOff,         // k_b == 0
   kStatZeroResidual,    // residual mass exactly zero
   kStatErrorSeqs,       // sequences that emitted nothing because of an error
+  kStatRowsSkipped,     // early exit: needed rows not read
   kStatCount
 };
 

@@ -467,7 +467,6 @@ struct Verifier {
     const int k = P.k;
     const int n_seqs = __ldcg(P.ws.n_seqs);
     const uint64_t evict_first = evict_first_policy();
-    const uint64_t evict_last = evict_last_policy();
     int q = 0, tki = 0, streamed = 0, rows = 0, draws = 0, pend = 0;
     bool ok = true;
     // the next sequence's work-list entry, tokens and uniforms are fetched one
@@ -524,6 +523,7 @@ struct Verifier {
               d.chunk = 0; d.nchunks = 1; d.x = -1; d.rec = rc; d.seq = streamed;
               d.u = 0.f; d.s = s_samp;
               mbar_arrive(&C.full[slot]);
+              atomicAdd(P.ws.stats + kStatRowsSkipped, static_cast<unsigned long long>(nrows - r));
             }
             ++q;
             ++rows;
@@ -566,6 +566,8 @@ struct Verifier {
               d.chunk = 0; d.nchunks = 1; d.x = -1; d.rec = rc; d.seq = streamed;
               d.u = 0.f; d.s = s_samp;
               mbar_arrive(&C.full[slot]);
+              if (rank == 0)   // every CTA of the cluster skips the same rows: counted once
+                atomicAdd(P.ws.stats + kStatRowsSkipped, static_cast<unsigned long long>(nrows - r));
             }
             ++q;
             ++rows;
@@ -589,10 +591,10 @@ struct Verifier {
             d.u = u; d.s = s_samp;
             if (P.bulk) mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(bytes));
           }
-          // the bonus row is never read in full again: first out of L2; a
-          // pair may be read again for its draw shortly after: last out
-          fill(ring + static_cast<size_t>(slot) * kChunkBytes, src, off, bytes, &C.full[slot],
-               true, pos == kb ? evict_first : evict_last);
+          // streamed rows are marked first out of L2: keeping the pairs
+          // (whose rejected one is read again a few chunks later) measured no
+          // faster, the re-read mostly finding its lines either way
+          fill(ring + static_cast<size_t>(slot) * kChunkBytes, src, off, bytes, &C.full[slot], true, evict_first);
           if (!P.bulk) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&C.full[slot]);

@@ -189,9 +189,12 @@ def test_early_exit_keeps_the_outputs(name, over, cs):
     ver.set_cluster(cs)
     t0, l0 = run_gpu(ver, inp)
     ver.set_early_exit(True)
+    ver.reset_stats()
     t1, l1 = run_gpu(ver, inp)
     np.testing.assert_array_equal(l0, l1)
     np.testing.assert_array_equal(t0, t1)
+    st, stats = ver.stats()
+    assert st == svp.SV_OK
     ref = run_oracle(inp)
     kb = inp["draft_len"].cpu().numpy()
     res = compare(t1, l1, ref, kb)
@@ -208,6 +211,11 @@ def test_early_exit_keeps_the_outputs(name, over, cs):
         # and every row up to the rejection was
         for b in range(B):
             assert np.isfinite(lse_t[b, :l1[b]]).all()
+        # the kernel's own count of rows not read is those rows
+        lse_d = dbg["lse_d"].cpu().numpy()
+        not_read = sum(int(np.isnan(lse_t[b, :kb[b] + 1]).sum() + np.isnan(lse_d[b, :kb[b]]).sum())
+                       for b in range(B))
+        assert stats["rows_skipped"] == not_read, (stats["rows_skipped"], not_read)
 
 
 # --- exhaustive enumeration batch ----------------------------------------------
