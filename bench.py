@@ -356,6 +356,33 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
             "soak_steps": soak, "cfg": cfg, "ver": ver, "base_inputs": base, "launch": launch}
 
 
+def timeline_summary(svp, ver, inp, stream):
+    """Per-CTA timestamps of one more call on the headline batch (outside the
+    timed region): when the CTAs got to work, took their first and last
+    chunks and finished, in microseconds from the work-list kernel's start
+    (min / median / max over the CTAs)."""
+    import torch
+
+    cs, ctas = ver.launch_shape(inp["target"].shape[0])
+    buf = torch.zeros((ctas + 1) * 8, dtype=torch.int64, device=inp["target"].device)
+    ver.set_timeline(buf)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"], inp["T"],
+                       stream=stream)
+    stream.synchronize()
+    ver.set_timeline(None)
+    t = buf.cpu().numpy().reshape(ctas + 1, 8).astype(np.float64)
+    t0 = t[ctas, 0]
+    rel = lambda col: (t[:ctas, col] - t0) / 1e3
+    q = lambda x: [round(float(np.min(x)), 2), round(float(np.median(x)), 2), round(float(np.max(x)), 2)]
+    return {"note": "us from the work-list kernel's start; min, median, max over CTAs",
+            "work_list_kernel_end": round(float((t[ctas, 1] - t0) / 1e3), 2),
+            "cta_start": q(rel(7)), "work_list_ready": q(rel(0)), "first_chunk": q(rel(1)),
+            "last_chunk": q(rel(2)), "cta_end": q(rel(5)), "after_last_chunk": q(rel(5) - rel(2)),
+            "chunks_per_cta": q(t[:ctas, 6]), "cluster": cs, "ctas": ctas}
+
+
 def _graph_ms(torch, stream, fn, steps):
     """ms per call of fn, replayed `steps` times from one CUDA graph."""
     with torch.cuda.stream(stream):
@@ -609,6 +636,7 @@ def our_arm(args, w):
     peak, peak_kind = measured_peak()
 
     e2e = e2e_measure(svp, w, args, device, stream, m["ver"], m["base_inputs"])
+    timeline = timeline_summary(svp, m["ver"], m["base_inputs"], stream)
     if pg:
         from speculative_decoding_verification_71_gb300.replicas import max_over_ranks
         e2e["value"] = world * m["positions"] / (max_over_ranks(e2e["ms_per_step"]) / 1e3)
@@ -706,7 +734,7 @@ def our_arm(args, w):
         "gpu_launches": 2 * args.steps,   # per call: the work-list kernel and the verify kernel
         "acceptance": {"mean_emitted": stats["mean_emitted"], "mean_accepted": stats["mean_accepted"],
                        "accept_rate": stats["accept_rate"], "spec_off": stats["spec_off"]},
-        "cpu_baseline": cpu, "parity": parity, "aux": aux or None,
+        "cpu_baseline": cpu, "parity": parity, "timeline": timeline, "aux": aux or None,
     }
     print(json.dumps(line), flush=True)
     if pg:

@@ -222,6 +222,19 @@ typedef enum { SV_KERNEL_AUTO = 0, SV_KERNEL_CLUSTER = 1, SV_KERNEL_PIECES = 2 }
 sv_status sv_set_kernel(sv_ctx *ctx, int kernel);
 sv_status sv_kernel_for(const sv_ctx *ctx, int B, int *kernel);
 
+/* Per-CTA timeline of the cluster kernel (measurement aid, off by default).
+ * timeline: device buffer of `capacity` unsigned 64-bit words, or NULL to
+ * turn it off.  A call whose grid has G CTAs (sv_launch_shape) and for which
+ * capacity >= (G + 1) * 8 writes, per CTA g, the global timer in ns at
+ * [g*8 + 0] the end of its wait for the work list, [+1] its first chunk,
+ * [+2] its last chunk (both as consumer warp 0 takes them), [+3] its control
+ * warp done, [+4] its walker warp done, [+5] its end, [+6] the chunks it
+ * consumed, [+7] its start; and at [G*8 + 0] and [G*8 + 1] the start and end
+ * of the work-list kernel.  Calls on a smaller buffer write nothing.  The
+ * buffer stays the caller's; SV_ERR_INVALID_ARG for a negative capacity or a
+ * buffer with capacity 0. */
+sv_status sv_set_timeline(sv_ctx *ctx, unsigned long long *timeline, int capacity);
+
 /* Early exit (off by default): rows of a sequence after its first rejection
  * are not read once the rejection is decided.  The outputs are the same; the
  * diagnostics of the rows not read stay NaN.  With one CTA per sequence the

@@ -42,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
     "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_get_config", "sv_launch_shape",
-    "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for",
+    "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for", "sv_set_timeline",
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
     "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_set_cost", "spec_ctrl_set_params", "spec_ctrl_reset",
     "spec_ctrl_observe", "spec_ctrl_choose", "spec_ctrl_alpha", "spec_ctrl_status",
@@ -113,6 +113,8 @@ def load_library(path: str | None = None):
     lib.sv_set_cluster.argtypes = [P, c.c_int]
     lib.sv_set_kernel.restype = c.c_int
     lib.sv_set_kernel.argtypes = [P, c.c_int]
+    lib.sv_set_timeline.restype = c.c_int
+    lib.sv_set_timeline.argtypes = [P, P, c.c_int]
     lib.sv_kernel_for.restype = c.c_int
     lib.sv_kernel_for.argtypes = [P, c.c_int, c.POINTER(c.c_int)]
     lib.sv_get_config.restype = c.c_int
@@ -328,6 +330,15 @@ class SpecVerifier:
         st = self.lib.sv_set_kernel(self._ctx, int(kernel))
         if st != SV_OK:
             self._raise(st, "sv_set_kernel")
+
+    def set_timeline(self, buf):
+        """Per-CTA timestamps of the following calls into ``buf`` (a uint64
+        CUDA tensor of at least (grid CTAs + 1) * 8 words, or int64), or
+        None to stop.  The caller keeps ``buf`` alive while it is set."""
+        ptr = buf.data_ptr() if buf is not None else None
+        st = self.lib.sv_set_timeline(self._ctx, ptr, buf.numel() if buf is not None else 0)
+        if st != SV_OK:
+            self._raise(st, "sv_set_timeline")
 
     def kernel_for(self, B: int) -> int:
         """The kernel a call with batch B runs on 16-byte aligned rows."""

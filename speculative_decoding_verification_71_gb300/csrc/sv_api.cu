@@ -33,6 +33,8 @@ struct sv_ctx {
   void* pw_mem = nullptr;      // workspace of the pieces kernel (null: not available)
   sv::PiecesWs pw{};
   int kernel = SV_KERNEL_AUTO;
+  unsigned long long* timeline = nullptr;   // caller's buffer of per-CTA timestamps (or null)
+  int timeline_cap = 0;
   int pieces_ctas = 0;         // grid of the pieces kernel (one CTA per SM)
   int np = 0, pe = 0, nr = 0, he = 0;
   long long calls = 0;
@@ -323,12 +325,15 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   // persistent grid: every cluster that fits at once, but never more than sequences
   int ctas = 0;
   launch_shape(ctx, B, &p.cluster, &ctas);
+  p.ctas = ctas;
   if (p.bulk && use_pieces(ctx, B)) {
     p.pieces = 1;
     p.np = ctx->np; p.pe = ctx->pe; p.nr = ctx->nr; p.he = ctx->he;
     p.ctas = ctx->pieces_ctas;
     p.pw = ctx->pw;
   }
+  // the timeline covers the cluster kernel's grid (and the work-list kernel)
+  if (!p.pieces && ctx->timeline && (ctas + 1) * sv::kTimelineSlots <= ctx->timeline_cap) p.timeline = ctx->timeline;
   cudaError_t e = sv::launch_verify(p, ctas, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch verify");
   ctx->calls += 1;
@@ -441,6 +446,13 @@ sv_status sv_launch_shape(const sv_ctx* ctx, int B, int* cluster, int* grid_ctas
   launch_shape(ctx, B, &cs, &ctas);
   if (cluster) *cluster = cs;
   if (grid_ctas) *grid_ctas = ctas;
+  return SV_OK;
+}
+
+sv_status sv_set_timeline(sv_ctx* ctx, unsigned long long* timeline, int capacity) {
+  if (!ctx || capacity < 0 || (timeline && capacity == 0)) return SV_ERR_INVALID_ARG;
+  ctx->timeline = timeline;
+  ctx->timeline_cap = timeline ? capacity : 0;
   return SV_OK;
 }
 

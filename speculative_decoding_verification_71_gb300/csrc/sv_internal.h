@@ -18,7 +18,8 @@ struct NvtxRange {
 };
 
 constexpr int kConsumerWarps = 16;                      // warps that compute
-constexpr int kThreads = (kConsumerWarps + 3) * 32;     // + producer, control and walker warps
+constexpr int kWalkers = 2;                             // walker warps (walks of different sequences overlap)
+constexpr int kThreads = (kConsumerWarps + 2 + kWalkers) * 32;   // + producer, control and walker warps
 constexpr int kVecsPerLane = 8;                         // 16-byte vectors per lane and chunk
 constexpr int kVecsPerWarp = kVecsPerLane * 32;         // 256 x 16 B per warp and chunk
 constexpr int kChunkBytes = kVecsPerWarp * 16 * kConsumerWarps;  // one staging slot: 64 KB
@@ -26,6 +27,10 @@ constexpr int kMaxChunks = 16;                          // rows up to 1 MiB
 constexpr int kMaxStages = 16;                          // staging slots per CTA
 constexpr long long kDrainLimitNs = 1000000000LL;       // second wait: always 1 s
 constexpr int kMaxCluster = 8;                          // CTAs sharing one sequence (portable limit)
+// Timeline slots per CTA: 0 grid wait done, 1 first chunk, 2 last chunk,
+// 3 control warp done, 4 walker done, 5 CTA end, 6 chunks consumed,
+// 7 prologue start.
+constexpr int kTimelineSlots = 8;
 
 // Counters kept on the device (unsigned long long each).
 enum StatSlot {
@@ -94,6 +99,10 @@ struct VerifyParams {
   int early_exit;       // 1: rows after a decided rejection are not read
   long long wait_limit_ns;
   Workspace ws;
+  // optional per-CTA timestamps (global timer, ns) of the cluster kernel,
+  // kTimelineSlots per CTA and, after the last CTA's, the plan kernel's
+  // start and end: null when not asked for
+  unsigned long long* timeline;
   // piece streaming (sv_pieces.cu) instead of the cluster kernel when set
   int pieces;
   int np, pe;           // pieces per row and logits per piece (pe * elt <= 64 KB, a multiple of 64)

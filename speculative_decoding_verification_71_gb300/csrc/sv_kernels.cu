@@ -165,8 +165,8 @@ struct Ctrl {
   int pend_end[kRecs];              // producer: rows streamed when a sequence ended
   SeqRec rec[kRecs];
   double bmass[kMaxChunks * kConsumerWarps];
-  WalkReq wreq[kWalkReqs];          // control warp -> walker warp
-  volatile int wreq_head, wreq_tail;
+  WalkReq wreq[kWalkers][kWalkReqs];   // control warp -> walker warps (one ring each, taken in turn)
+  volatile int wreq_head[kWalkers], wreq_tail[kWalkers];
   volatile int ctl_done;            // the control warp has left
   float pairK, pairL, pairZx, pairS;  // target row of the current pair (pairS: its sum of 2^(z c - K))
 };
@@ -182,6 +182,7 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanCached = 8;   // k_b values a thread keeps in registers (B <= 8192)
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P) {
+  if (P.timeline && threadIdx.x == 0) P.timeline[static_cast<size_t>(P.ctas) * kTimelineSlots] = global_ns();
   grid_dependents_launch();   // the verify grid may start its prologue now
   __shared__ int warp_cnt[32];
   __shared__ int base;
@@ -259,7 +260,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
     }
     if (P.pieces && tid == 0) P.pw.grp[L] = base;   // sequences with k_b >= L
   }
-  if (tid == 0) *ws.n_seqs = base;
+  if (tid == 0) {
+    *ws.n_seqs = base;
+    if (P.timeline) P.timeline[static_cast<size_t>(P.ctas) * kTimelineSlots + 1] = global_ns();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -637,7 +641,19 @@ struct Verifier {
   // of row buffers, a re-read's weights into a pair of mass arrays, and the
   // control warp takes it from there.
 
+  // Timeline (consumer warp 0, lane 0): first and last chunk, chunks seen.
+  __device__ void stamp_chunk(bool& first, unsigned long long& n) const {
+    if (!P.timeline || warp != 0 || lane != 0) return;
+    unsigned long long* t = P.timeline + static_cast<size_t>(blockIdx.x) * kTimelineSlots;
+    const unsigned long long now = global_ns();
+    if (!first) { t[1] = now; first = true; }
+    t[2] = now;
+    t[6] = ++n;
+  }
+
   __device__ void consume() {
+    bool tl_first = false;
+    unsigned long long tl_n = 0;
     const int S = P.stages;
     const float c2 = P.c2;
     float rK = -INFINITY, rS = 0.f, rM = -INFINITY;   // running state of the current row
@@ -655,6 +671,7 @@ struct Verifier {
         }
       }
       const Desc d = C.desc[slot];
+      if (d.kind >= 0) stamp_chunk(tl_first, tl_n);
       if (d.kind < 0) {
         // tell the control warp that the work is over
         const int buf = rr % kRowBufs;
@@ -1003,45 +1020,53 @@ struct Verifier {
     __syncwarp();
   }
 
-  // Hand a walk to the walker warp (lane 0 of the control warp).  Waits,
-  // bounded, while the ring is full: the walker always makes progress.
+  // Hand a walk to the walker warps, in turn (lane 0 of the control warp):
+  // walks of sequences that finish together then overlap.  Waits, bounded,
+  // while the chosen ring is full: the walkers always make progress.
+  int wsel_ = 0;
   __device__ void push_walk(const WalkReq& r) {
     if (lane == 0) {
+      const int w = wsel_;
+      wsel_ = (wsel_ + 1) % kWalkers;
       const unsigned long long t0 = global_ns();
-      while (C.wreq_tail - C.wreq_head >= kWalkReqs) {
+      while (C.wreq_tail[w] - C.wreq_head[w] >= kWalkReqs) {
         if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
           atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
           break;
         }
         __nanosleep(64);
       }
-      const int tail = C.wreq_tail;
-      C.wreq[tail % kWalkReqs] = r;
+      const int tail = C.wreq_tail[w];
+      C.wreq[w][tail % kWalkReqs] = r;
       __threadfence_block();
-      C.wreq_tail = tail + 1;
+      C.wreq_tail[w] = tail + 1;
     }
     __syncwarp();
   }
 
-  // ======================= walker warp =======================================
-  // The only warp of the CTA that waits on logits read from global memory
+  // ======================= walker warps ======================================
+  // The only warps of the CTA that wait on logits read from global memory
   // outside the staging ring: the walk inside the drawn segment, then the
-  // sequence's outputs.  Nothing waits for it but the reuse of a record.
+  // sequence's outputs.  Nothing waits for them but the reuse of a record.
 
-  __device__ void walker() {
+  __device__ void walker(int w) {
     int head = 0;
     unsigned long long idle_since = 0;
     while (true) {
       int tail = 0, done = 0;
-      if (lane == 0) { done = C.ctl_done; tail = C.wreq_tail; }
+      if (lane == 0) { done = C.ctl_done; tail = C.wreq_tail[w]; }
       tail = __shfl_sync(0xffffffffu, tail, 0);
       done = __shfl_sync(0xffffffffu, done, 0);
       if (head == tail) {
         if (done) {
           // the control warp has left: take what it pushed before leaving
-          if (lane == 0) tail = C.wreq_tail;
+          if (lane == 0) tail = C.wreq_tail[w];
           tail = __shfl_sync(0xffffffffu, tail, 0);
-          if (head == tail) return;
+          if (head == tail) {
+            if (P.timeline && lane == 0)
+              atomicMax(P.timeline + static_cast<size_t>(blockIdx.x) * kTimelineSlots + 4, global_ns());
+            return;
+          }
         } else {
           if (!idle_since) idle_since = global_ns();
           if (static_cast<long long>(global_ns() - idle_since) > 8 * kDrainLimitNs) {
@@ -1054,7 +1079,7 @@ struct Verifier {
       }
       idle_since = 0;
       __threadfence_block();
-      const WalkReq r = C.wreq[head % kWalkReqs];
+      const WalkReq r = C.wreq[w][head % kWalkReqs];
       int y = -1;
       if (r.v0 >= 0) {
         if (r.mode == 0)
@@ -1070,7 +1095,7 @@ struct Verifier {
       finish_sequence(r.rec);
       if (lane == 0) {
         C.rec[r.rec].open = 0;
-        C.wreq_head = head + 1;
+        C.wreq_head[w] = head + 1;
       }
       __syncwarp();
       ++head;
@@ -1311,6 +1336,7 @@ struct Verifier {
 
   __device__ void control() {
     control_loop();
+    if (P.timeline && lane == 0) P.timeline[static_cast<size_t>(blockIdx.x) * kTimelineSlots + 3] = global_ns();
     __syncwarp();
     if (lane == 0) { __threadfence_block(); C.ctl_done = 1; }
   }
@@ -1464,8 +1490,7 @@ verify_kernel(const VerifyParams P) {
       C.rec[r].open = 0; C.rec[r].resolved = 0;
       C.rec[r].seq_tag = -1; C.rec[r].decided = 0; C.rec[r].stop = 0;
     }
-    C.wreq_head = 0;
-    C.wreq_tail = 0;
+    for (int w = 0; w < kWalkers; ++w) { C.wreq_head[w] = 0; C.wreq_tail[w] = 0; }
     C.ctl_done = 0;
     fence_mbar_init();
     for (int r = 0; r < 2; ++r) mbar_expect_tx(&C.tk_full[r], 4u);
@@ -1474,16 +1499,20 @@ verify_kernel(const VerifyParams P) {
       mbar_expect_tx(&C.xdraw_ready[x], static_cast<uint32_t>(cs * sizeof(DrawPart)));
     }
   }
+  unsigned long long* tl = P.timeline ? P.timeline + static_cast<size_t>(blockIdx.x) * kTimelineSlots : nullptr;
+  if (tl && tid == 0) tl[7] = global_ns();
   cluster_sync();                   // every CTA's barriers exist before anyone arrives on them
   grid_dependency_wait();           // the work list of plan_kernel is ready
+  if (tl && tid == 0) tl[0] = global_ns();
   {
     Verifier<ELT, GREEDY> v(P, C, ring, lane, warp, cs, cluster_rank());
     if (warp < kConsumerWarps) v.consume();
     else if (warp == kConsumerWarps) v.produce();
     else if (warp == kConsumerWarps + 1) v.control();
-    else v.walker();
+    else v.walker(warp - kConsumerWarps - 2);
   }
   cluster_sync();                   // nobody leaves while a peer may still reach its shared memory
+  if (tl && tid == 0) tl[5] = global_ns();
 }
 
 // ---------------------------------------------------------------------------

@@ -104,6 +104,36 @@ def test_kernel_choice():
     assert big.kernel_for(2048) == svp.SV_KERNEL_PIECES and big.kernel_for(2049) == svp.SV_KERNEL_CLUSTER
 
 
+def test_timeline_is_consistent():
+    """The per-CTA timestamps of a call: every CTA starts after the work-list
+    kernel does, takes its chunks in order and ends last; the chunks add up
+    to the streamed and re-read chunks of the batch; no timeline on a buffer
+    too small for the grid."""
+    inp = small("ragged", B=64, k=3, V=65536)
+    ver = verifier_for(inp)
+    cs, ctas = ver.launch_shape(64)
+    small_buf = torch.full((ctas * 8,), -1, dtype=torch.int64, device=DEV)
+    ver.set_timeline(small_buf)
+    run_gpu(ver, inp)
+    assert bool((small_buf == -1).all())
+    buf = torch.zeros((ctas + 1) * 8, dtype=torch.int64, device=DEV)
+    ver.set_timeline(buf)
+    toks, lens = run_gpu(ver, inp)
+    ver.set_timeline(None)
+    t = buf.cpu().numpy().reshape(ctas + 1, 8)
+    plan0, plan1 = t[ctas, 0], t[ctas, 1]
+    assert plan0 > 0 and plan1 >= plan0
+    for g in range(ctas):
+        start, ready, first, last, ctl, walk, end, n = t[g, 7], t[g, 0], t[g, 1], t[g, 2], t[g, 3], t[g, 4], t[g, 5], t[g, 6]
+        assert start >= plan0 and ready >= start and ready >= plan1
+        assert n > 0 and first >= ready and last >= first
+        assert ctl >= last and walk >= ready and end >= max(ctl, walk)
+    # every CTA of a cluster takes every chunk of its slices: per cluster the
+    # chunk count is the same in each CTA
+    n = t[:ctas, 6].reshape(-1, cs)
+    assert (n == n[:, :1]).all()
+
+
 def test_both_kernels_agree_away_from_ties():
     """Two schedules of one rule: identical outputs wherever the oracle's
     decision is not a near-tie (the row sums are added in another order)."""
