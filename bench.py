@@ -822,7 +822,11 @@ def profile_kernels(args):
             elif name == "compact":
                 ver.compact(ot, ol)
             elif name == "debug":
+                ver.set_diagnostics(True)
+                ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"], inp["T"],
+                           out_tokens=ot, out_len=ol)
                 ver.debug(w.B, w.k)
+                ver.set_diagnostics(False)
             elif name == "kd":
                 g = torch.Generator(device=device).manual_seed(11)
                 n_seq, t_len, V = 16, 64, 151936

@@ -156,15 +156,25 @@ sv_status spec_verify_compact(sv_ctx *ctx, int B, int k,
                               sv_stream_t stream);
 
 /*
+ * Diagnostics recording (off by default).  While on, spec_verify also writes
+ * the per-row values spec_verify_debug returns (one more global store per
+ * row and draw, and a reset of the arrays per call); off, those stores are
+ * skipped.  on must be 0 or 1, else SV_ERR_INVALID_ARG.
+ */
+sv_status sv_set_diagnostics(sv_ctx *ctx, int on);
+
+/*
  * Per-row diagnostics of the LAST spec_verify call on this context, for
- * parity checks (asynchronous on `stream`; device pointers; any may be NULL):
+ * parity checks (asynchronous on `stream`; device pointers; any may be NULL).
+ * SV_ERR_INVALID_ARG unless that call ran with diagnostics on
+ * (sv_set_diagnostics) and B and k match it:
  *   lse_t      [B, k+1] double  log-sum-exp of z^t_i / T for rows i <= k_b
  *   lse_d      [B, k]   double  log-sum-exp of z^d_i / T for rows i < k_b
  *   accept_prob[B, k]   double  min(1, p_i(x_i)/q_i(x_i)) for i < k_b
  *   mass       [B, k+1] double  total weight S of the draw computed at
  *                               position i (NaN where no draw was computed)
  * Entries that do not apply (padding rows, T == 0, sequences with a device
- * error) are NaN.  B and k must match the last call.
+ * error) are NaN.
  */
 sv_status spec_verify_debug(sv_ctx *ctx, int B, int k, double *lse_t, double *lse_d,
                             double *accept_prob, double *mass, sv_stream_t stream);

@@ -41,7 +41,7 @@ _lib = None
 EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
-    "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_get_config", "sv_launch_shape",
+    "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_set_diagnostics", "sv_get_config", "sv_launch_shape",
     "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for", "sv_set_timeline",
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
     "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_set_cost", "spec_ctrl_set_params", "spec_ctrl_reset",
@@ -109,6 +109,8 @@ def load_library(path: str | None = None):
     lib.sv_set_pipeline.argtypes = [P, c.c_int, c.c_int]
     lib.sv_set_early_exit.restype = c.c_int
     lib.sv_set_early_exit.argtypes = [P, c.c_int]
+    lib.sv_set_diagnostics.restype = c.c_int
+    lib.sv_set_diagnostics.argtypes = [P, c.c_int]
     lib.sv_set_cluster.restype = c.c_int
     lib.sv_set_cluster.argtypes = [P, c.c_int]
     lib.sv_set_kernel.restype = c.c_int
@@ -281,7 +283,8 @@ class SpecVerifier:
         return packed, offsets
 
     def debug(self, B, k, stream=None):
-        """Per-row diagnostics of the last call (float64 device tensors)."""
+        """Per-row diagnostics of the last call (float64 device tensors); the
+        call must have run with ``set_diagnostics(True)``."""
         dev = self.device
         lse_t = torch.empty(B, k + 1, dtype=torch.float64, device=dev)
         lse_d = torch.empty(B, max(k, 1), dtype=torch.float64, device=dev)
@@ -355,6 +358,13 @@ class SpecVerifier:
         st = self.lib.sv_set_early_exit(self._ctx, 1 if on else 0)
         if st != SV_OK:
             self._raise(st, "sv_set_early_exit")
+
+    def set_diagnostics(self, on: bool):
+        """Record the per-row diagnostics that ``debug`` returns (off by
+        default: the stores cost the verify call time)."""
+        st = self.lib.sv_set_diagnostics(self._ctx, 1 if on else 0)
+        if st != SV_OK:
+            self._raise(st, "sv_set_diagnostics")
 
     def config(self):
         vals = [ctypes.c_int() for _ in range(6)]

@@ -24,6 +24,7 @@ struct sv_ctx {
   int ctas_per_sm = 0;
   int cluster = 0;             // 0: chosen per call
   int early_exit = 0;          // 1: rows after a decided rejection are not read
+  int diagnostics = 0;         // 1: calls write the per-row diagnostics spec_verify_debug reads
   int max_clusters[4] = {0};   // clusters of 1, 2, 4, 8 CTAs that fit at once
   int num_sms = 0;
   int smem_bytes = 0;
@@ -38,7 +39,7 @@ struct sv_ctx {
   int pieces_ctas = 0;         // grid of the pieces kernel (one CTA per SM)
   int np = 0, pe = 0, nr = 0, he = 0;
   long long calls = 0;
-  int last_B = 0, last_k = 0, last_greedy = 0;
+  int last_B = 0, last_k = 0, last_greedy = 0, last_diag = 0;
   float last_inv_T = 1.f;
   char cuda_msg[256] = {0};
 };
@@ -322,6 +323,7 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   p.wait_limit_ns = ctx->wait_limit_ns;
   p.ws = ctx->ws;
   p.early_exit = ctx->early_exit;
+  p.diag = ctx->diagnostics;
   // persistent grid: every cluster that fits at once, but never more than sequences
   int ctas = 0;
   launch_shape(ctx, B, &p.cluster, &ctas);
@@ -340,6 +342,7 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   ctx->last_B = B;
   ctx->last_k = k;
   ctx->last_greedy = greedy ? 1 : 0;
+  ctx->last_diag = ctx->diagnostics;
   ctx->last_inv_T = greedy ? 0.f : 1.f / temperature;
   return SV_OK;
 }
@@ -355,7 +358,7 @@ sv_status spec_verify_compact(sv_ctx* ctx, int B, int k, const int32_t* out_toke
 
 sv_status spec_verify_debug(sv_ctx* ctx, int B, int k, double* lse_t, double* lse_d, double* accept_prob,
                             double* mass, sv_stream_t stream) {
-  if (!ctx || ctx->calls == 0) return SV_ERR_INVALID_ARG;
+  if (!ctx || ctx->calls == 0 || !ctx->last_diag) return SV_ERR_INVALID_ARG;
   if (B != ctx->last_B || k != ctx->last_k) return SV_ERR_INVALID_ARG;
   cudaError_t e = sv::launch_debug(ctx->ws, B, k, ctx->last_greedy, ctx->last_inv_T, lse_t, lse_d,
                                    accept_prob, mass, reinterpret_cast<cudaStream_t>(stream));
@@ -416,6 +419,12 @@ sv_status sv_set_pipeline(sv_ctx* ctx, int stages, int ctas_per_sm) {
 sv_status sv_set_early_exit(sv_ctx* ctx, int on) {
   if (!ctx || (on != 0 && on != 1)) return SV_ERR_INVALID_ARG;
   ctx->early_exit = on;
+  return SV_OK;
+}
+
+sv_status sv_set_diagnostics(sv_ctx* ctx, int on) {
+  if (!ctx || (on != 0 && on != 1)) return SV_ERR_INVALID_ARG;
+  ctx->diagnostics = on;
   return SV_OK;
 }
 

@@ -97,6 +97,7 @@ struct VerifyParams {
   int bulk;             // 1: rows staged with cp.async.bulk; 0: plain loads
   int cluster;          // CTAs per cluster: each takes one slice of every row (1, 2, 4 or 8)
   int early_exit;       // 1: rows after a decided rejection are not read
+  int diag;             // 1: per-row diagnostics (row maxima, log-sums, alpha, draw masses) are written
   long long wait_limit_ns;
   Workspace ws;
   // optional per-CTA timestamps (global timer, ns) of the cluster kernel,

@@ -168,7 +168,7 @@ struct Ctrl {
   WalkReq wreq[kWalkers][kWalkReqs];   // control warp -> walker warps (one ring each, taken in turn)
   volatile int wreq_head[kWalkers], wreq_tail[kWalkers];
   volatile int ctl_done;            // the control warp has left
-  float pairK, pairL, pairZx, pairS;  // target row of the current pair (pairS: its sum of 2^(z c - K))
+  float pairK, pairL, pairZx, pairS;     // target row of the current pair (pairS: its sum of 2^(z c - K))
 };
 
 constexpr int kCtrlBytes = ((static_cast<int>(sizeof(Ctrl)) + 1023) / 1024) * 1024;
@@ -206,11 +206,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
       atomicAdd(ws.stats + kStatErrorSeqs, 1ull);
     }
   }
-  for (int i = tid; i < B * (k + 1); i += kPlanThreads) {
-    ws.m_t[i] = NAN; ws.L_t[i] = NAN; ws.mass[i] = NAN;
-  }
-  for (int i = tid; i < B * k; i += kPlanThreads) {
-    ws.m_d[i] = NAN; ws.L_d[i] = NAN; ws.alpha[i] = NAN;
+  if (P.diag) {
+    for (int i = tid; i < B * (k + 1); i += kPlanThreads) {
+      ws.m_t[i] = NAN; ws.L_t[i] = NAN; ws.mass[i] = NAN;
+    }
+    for (int i = tid; i < B * k; i += kPlanThreads) {
+      ws.m_d[i] = NAN; ws.L_d[i] = NAN; ws.alpha[i] = NAN;
+    }
   }
   if (P.pieces) {
     // the piece kernel's counters start from zero
@@ -222,7 +224,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
     for (int i = tid; i < P.ctas; i += kPlanThreads) pw.mtail[i * 32] = 0;
     if (tid < 64) pw.ctr[tid] = 0;
   }
-  if (tid == 0) { base = 0; *ws.ticket = 0; }
+  // the first sequence of cluster i is entry i of the work list (no atomic
+  // needed); the shared counter hands out the rest
+  if (tid == 0) { base = 0; *ws.ticket = P.pieces ? 0 : P.ctas / max(1, P.cluster); }
   __syncthreads();
   // counting sort by k_b, largest first, stable in b
   for (int L = k; L >= 0; --L) {
@@ -287,6 +291,7 @@ struct Verifier {
   int nchunks;                  // stream chunks per slice (at least one)
   int ndraw;                    // draw chunks per slice (at least one)
   int v_lo, v_hi;               // 16-byte vectors of the row covering the slice
+  int chunks0;                  // stream chunks per row of the first (largest) slice
   int lag_rows;                 // rows between a sequence's end and its re-read (same in every CTA)
   int exit_lag;                 // early exit: pairs between a decision and the rows it can spare
 
@@ -303,7 +308,7 @@ struct Verifier {
     v_lo = slice_lo / NV;                       // slice_lo is a multiple of kSliceAlign
     v_hi = (hi * ELT + 15) / 16;
     // counted in chunks of the first (largest) slice so that every CTA agrees
-    const int chunks0 = max(1, (min(p.V, per) * ELT + kChunkBytes - 1) / kChunkBytes);
+    chunks0 = max(1, (min(p.V, per) * ELT + kChunkBytes - 1) / kChunkBytes);
     lag_rows = max(1, (kDrawLagChunks + chunks0 - 1) / chunks0);
     const int pair_chunks = (GREEDY ? 1 : 2) * chunks0;
     exit_lag = max(1, (kExitLagChunks + pair_chunks - 1) / pair_chunks);
@@ -485,7 +490,9 @@ struct Verifier {
         u_ = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(s_.x) * (k + 1) + lane) : 0.f;
       }
     };
-    int t = take_ticket(tki, ok);
+    // the first sequence of cluster i is entry i of the work list (the
+    // shared counter starts after them): no ticket to wait for
+    int t = static_cast<int>(blockIdx.x) / cs;
     int2 sq;
     int xj;
     float uj;
@@ -495,7 +502,8 @@ struct Verifier {
       const int rc = streamed % kRecs;
       // the next ticket is taken when this sequence's last row starts: late
       // enough that sequences keep going to whichever cluster frees up first
-      // (longest first), early enough to hide the fetch behind that row
+      // (longest first; taking it rows earlier measured slower), early enough
+      // to hide the fetch behind that row
       int t_next = 0x7fffffff;
       int2 sq_next = make_int2(-1, 0);
       int xj_next = -1;
@@ -1165,7 +1173,7 @@ struct Verifier {
     const float L = log2f(Ssum);
     SeqRec& R = C.rec[d.rec];
     const size_t b = static_cast<size_t>(d.b);
-    const bool diag = (rank == 0);
+    const bool diag = P.diag && rank == 0;   // one CTA of the cluster writes the diagnostics
     const bool marker = (d.kind == 3);      // the sequence was cut short after a rejection
     const bool last = (d.kind == 0 && d.pos == d.kb) || marker;
     int bonus = 0, settle = 0;
@@ -1196,12 +1204,12 @@ struct Verifier {
         if (d.kind == 0) {
           if (diag) {
             P.ws.m_t[b * (P.k + 1) + d.pos] = M;
-            P.ws.L_t[b * (P.k + 1) + d.pos] = L;
+            P.ws.L_t[b * (P.k + 1) + d.pos] = log2f(Ssum);
           }
           C.pairK = K; C.pairL = L; C.pairZx = zx; C.pairS = Ssum;
         } else if (diag) {
           P.ws.m_d[b * P.k + d.pos] = M;
-          P.ws.L_d[b * P.k + d.pos] = L;
+          P.ws.L_d[b * P.k + d.pos] = log2f(Ssum);
         }
         if (d.kind == 1 && !R.err) {
           // the pair is complete: acceptance test of draft d.pos.  With
@@ -1222,7 +1230,7 @@ struct Verifier {
           if (!(d.u < alpha) && R.a < 0) {
             // first rejection: the pair is read again for the residual draw
             R.a = d.pos;
-            R.Kt = C.pairK; R.Lt = C.pairL;
+            R.Kt = C.pairK; R.Lt = C.pairL;   // the target row's log2 S, taken only here
             R.Gh = Gh; R.Gl = Gl;
           }
         } else if (last && R.a < 0 && !R.err) {
@@ -1270,7 +1278,7 @@ struct Verifier {
         int seg;
         double seg_t;
         locate(C.bmass, nseg, t_loc, seg, seg_t);
-        if (lane == 0) P.ws.mass[b * (P.k + 1) + d.kb] = static_cast<float>(tot);
+        if (lane == 0 && P.diag) P.ws.mass[b * (P.k + 1) + d.kb] = static_cast<float>(tot);
         WalkReq wr;
         wr.rec = d.rec; wr.mode = 0; wr.v0 = seg >= 0 ? v_lo + seg * kVecsPerWarp : -1;
         wr.b = d.b; wr.pos = d.kb; wr.pad = 0; wr.t = seg_t;
@@ -1321,7 +1329,7 @@ struct Verifier {
       int seg;
       double seg_t;
       locate(resid ? C.rmass[dp] : C.pmass[dp], nseg, t_loc, seg, seg_t);
-      if (lane == 0) P.ws.mass[static_cast<size_t>(R.b) * (P.k + 1) + R.a] = static_cast<float>(tot);
+      if (lane == 0 && P.diag) P.ws.mass[static_cast<size_t>(R.b) * (P.k + 1) + R.a] = static_cast<float>(tot);
       WalkReq wr;
       wr.rec = rc; wr.mode = resid ? 1 : 2; wr.v0 = seg >= 0 ? v_lo + seg * kDrawVecsPerWarp : -1;
       wr.b = R.b; wr.pos = R.a; wr.pad = 0; wr.t = seg_t;
@@ -1641,8 +1649,10 @@ cudaError_t query_max_clusters(int cluster, int smem_bytes, int* out) {
   return cudaOccupancyMaxActiveClusters(out, reinterpret_cast<const void*>(&verify_kernel<2, false>), &cfg);
 }
 
-cudaError_t launch_verify(const VerifyParams& p, int ctas, int smem_bytes, cudaStream_t s) {
+cudaError_t launch_verify(const VerifyParams& params, int ctas, int smem_bytes, cudaStream_t s) {
   NvtxRange range("spec_verify");
+  VerifyParams p = params;
+  if (!p.pieces) p.ctas = ctas;   // the work-list kernel starts the ticket counter after every cluster's first
   plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

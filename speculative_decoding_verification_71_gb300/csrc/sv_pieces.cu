@@ -789,7 +789,8 @@ struct Pieces {
         S.row[ri] = st;
         S.bad[ri] = bad;
         // diagnostics
-        if (GREEDY) {
+        if (!P.diag) {
+        } else if (GREEDY) {
           P.ws.m_t[static_cast<size_t>(b) * k1 + ri] = st.x;
         } else if (ri & 1) {
           P.ws.m_d[static_cast<size_t>(b) * P.k + (ri >> 1)] = st.x;
@@ -814,7 +815,7 @@ struct Pieces {
         err |= kErrBadTok;
       } else if (GREEDY) {
         reject = x != __float_as_int(S.row[lane].y);
-        P.ws.alpha[static_cast<size_t>(b) * P.k + lane] = reject ? 0.f : 1.f;
+        if (P.diag) P.ws.alpha[static_cast<size_t>(b) * P.k + lane] = reject ? 0.f : 1.f;
       } else {
         const float4 T = S.row[2 * lane], D = S.row[2 * lane + 1];
         const float zt = S.zx[2 * lane], zd = S.zx[2 * lane + 1];
@@ -826,7 +827,7 @@ struct Pieces {
           const float delta = __fadd_rn(__fmaf_rn(__fsub_rn(zd, zt), c2, Gh), Gl);
           alpha = delta <= 0.f ? 1.f : exp2f(-delta);
         }
-        P.ws.alpha[static_cast<size_t>(b) * P.k + lane] = alpha;
+        if (P.diag) P.ws.alpha[static_cast<size_t>(b) * P.k + lane] = alpha;
         reject = !(u < alpha);
       }
     }
@@ -884,7 +885,7 @@ struct Pieces {
       const int v_end = min(P.V, (piece + 1) * P.pe) / NV;
       y = walk<kVecsPerLane, false>(v0, v_end, seg_t, trow(b, kb), nullptr, T.y, T.w, 0.f, 0.f);
     }
-    if (lane == 0) P.ws.mass[static_cast<size_t>(b) * k1 + kb] = static_cast<float>(tot);
+    if (lane == 0 && P.diag) P.ws.mass[static_cast<size_t>(b) * k1 + kb] = static_cast<float>(tot);
     finish_outputs(b, kb, kb, y, 0, 0);
   }
 
@@ -924,7 +925,7 @@ struct Pieces {
       else
         y = walk<kHalfVecsPerLane, false>(v0, v_end, seg_t, trow(b, a), nullptr, nrm.x, nrm.y, 0.f, 0.f);
     }
-    if (lane == 0) P.ws.mass[static_cast<size_t>(b) * k1 + a] = static_cast<float>(tot);
+    if (lane == 0 && P.diag) P.ws.mass[static_cast<size_t>(b) * k1 + a] = static_cast<float>(tot);
     finish_outputs(b, jb.pad0, a, y, (flag & 2) ? kErrTime : 0, resid ? 0 : 1);
   }
 

@@ -25,9 +25,12 @@ def _built():
     svp.load_library()
 
 
-def verifier_for(inp, **kw):
+def verifier_for(inp, diagnostics=True, **kw):
+    """A verifier sized for the batch, recording diagnostics unless asked not to."""
     w = inp["meta"]["workload"]
-    return svp.SpecVerifier(inp["meta"]["B"], w.k, w.V, w.torch_dtype, **kw)
+    ver = svp.SpecVerifier(inp["meta"]["B"], w.k, w.V, w.torch_dtype, **kw)
+    ver.set_diagnostics(diagnostics)
+    return ver
 
 
 def small(name, **over):
@@ -374,6 +377,27 @@ def test_repeated_calls_are_bitwise_identical():
         t1, l1 = run_gpu(ver, inp)
         np.testing.assert_array_equal(t0, t1)
         np.testing.assert_array_equal(l0, l1)
+
+
+@pytest.mark.parametrize("cs", [1, 2, 4])
+def test_diagnostics_switch_changes_no_output(cs):
+    """Recording diagnostics only adds stores: the outputs are bitwise the
+    same either way, and a call made without them has none to return."""
+    inp = small("ragged", B=96, k=3, V=32768)
+    ver = verifier_for(inp, diagnostics=False)
+    ver.set_cluster(cs)
+    t0, l0 = run_gpu(ver, inp)
+    with pytest.raises(svp.SpecVerifyError):
+        ver.debug(96, 3)
+    ver.set_diagnostics(True)
+    t1, l1 = run_gpu(ver, inp)
+    np.testing.assert_array_equal(t0, t1)
+    np.testing.assert_array_equal(l0, l1)
+    dbg = ver.debug(96, 3)
+    kb = inp["draft_len"].cpu().numpy()
+    lse_t = dbg["lse_t"].cpu().numpy()
+    assert all(np.isfinite(lse_t[b, :kb[b] + 1]).all() for b in range(96))
+    assert ver.lib.sv_set_diagnostics(ver.handle, 2) == svp.SV_ERR_INVALID_ARG
 
 
 def test_compaction_and_stats():
