@@ -276,18 +276,19 @@ sv_status sv_set_early_exit(sv_ctx *ctx, int on);
  * KL, NaN gradient and NaN loss for its rollout; a masked draft logit (-inf)
  * where the target has mass gives KL = +inf.  Asynchronous on `stream`; no
  * context and no allocation per call (the first call on a device allocates
- * one word).  Deterministic: every sum is taken in a fixed order.  Rows whose
- * V * sizeof(dtype) is a multiple of 16 with 16-byte aligned bases are staged
- * with bulk copies, others with plain loads.  Vocabularies up to 8 * 27 KB
- * of logits per row use two row buffers per CTA, larger ones one;
- * SV_ERR_UNSUPPORTED if a row does not fit a cluster of 8 CTAs. */
+ * one word).  Deterministic: every sum is taken in a fixed order.  One CTA
+ * per SM takes whole row pairs; with the gradient each pair is streamed twice,
+ * the second time from L2.  Rows whose V * sizeof(dtype) is a multiple of 16
+ * with 16-byte aligned bases (and gradient) are staged with bulk copies,
+ * others with plain loads.  Rows of more than 1 GiB are SV_ERR_INVALID_ARG. */
 sv_status spec_kd_loss(int n_seq, int t_len, int V, sv_dtype dtype, const void *target_logits,
                        const void *draft_logits, const float *weights, float temperature,
                        float *row_kl, float *loss, void *grad, sv_stream_t stream);
 
 /* The launch shape spec_kd_loss uses for rows of V logits of `dtype` (with or
- * without the gradient): CTAs per cluster, row buffers per CTA, and the most
- * CTAs of the persistent grid.  Any output pointer may be NULL. */
+ * without the gradient): CTAs per row (always 1), 64 KB staging slots per CTA,
+ * and the most CTAs of the persistent grid (the SM count).  Any output
+ * pointer may be NULL. */
 sv_status spec_kd_launch_shape(int V, sv_dtype dtype, int with_grad, int *cluster, int *buffers,
                                int *grid_ctas);
 

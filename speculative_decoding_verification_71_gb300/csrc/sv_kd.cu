@@ -13,16 +13,22 @@
 // S = sum_x 2^(z(x) c - K) and A = sum_x 2^(z^t(x) c - K^t) (z^t(x) - z^d(x)):
 //   KL = ln 2 * (c A / S^t - (K^t - K^d) - log2(S^t / S^d)),
 // since log2 p(x) = z^t(x) c - K^t - log2 S^t (and likewise for q).
-// Rows are independent, so a cluster of cs CTAs takes one row pair at a
-// time: each CTA stages its vocabulary slice of both rows in shared memory
-// (cp.async.bulk), computes its part of (M, S, A), sends it to every CTA of
-// the cluster (st.async, counted on their mbarriers), combines the parts in
-// rank order and, from the same shared-memory copy, writes its slice of the
-// gradient.  Each logit crosses HBM once and each gradient value once.  The
-// next row's first pass runs while the current row's parts are exchanged.
+//
+// Rows are independent: a persistent grid of one CTA per SM takes whole row
+// pairs, row b + i * grid for CTA b.  A producer warp streams each pair
+// through three 64 KB shared-memory slots with cp.async.bulk, 32 KB of the
+// target row and the same 32 KB of the draft row per slot; 16 consumer warps
+// fold every slot into running per-lane maxima and sums (two logits per
+// f32x2 instruction).  At the row's end the warps' parts are combined, in a
+// fixed order, into (M, S, A) and the KL.  For the gradient the producer
+// streams the pair a second time right behind the first: those copies find
+// the row in L2 (it was read a few microseconds before) and are marked first
+// out of it, and the gradient leaves with streaming stores.  Each logit
+// crosses HBM once and each gradient value once; no CTA waits for another.
 
 #include <cuda_runtime.h>
 
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -34,27 +40,27 @@
 namespace sv {
 namespace {
 
-constexpr int kKdWarps = 16;                         // compute warps
-constexpr int kKdThreads = (kKdWarps + 1) * 32;      // + one producer warp
-constexpr int kKdXRing = 4;                          // exchange slots (rows in flight: see below)
-constexpr int kKdMaxBuf = 6;                         // row buffers per CTA
-constexpr int kKdMaxCluster = 16;                    // 16 is a non-portable cluster size (opted into)
-constexpr int kKdBarCompute = 1;                     // named barrier of the compute warps
+constexpr int kKdWarps = 16;                          // consumer warps
+constexpr int kKdThreads = (kKdWarps + 1) * 32;       // + the producer warp
+constexpr int kKdStages = 3;                          // 64 KB staging slots
+constexpr int kKdHalf = 32 * 1024;                    // one row's part of a slot
+constexpr int kKdVecsPerWarp = kKdHalf / 16 / kKdWarps;   // 128 vectors of 16 bytes
+constexpr int kKdVecsPerLane = kKdVecsPerWarp / 32;       // 4
+constexpr int kKdBarCompute = 1;                      // named barrier of the consumer warps
 
 struct alignas(16) KdPart {
   float mt, st, a, md;         // target max, target sum, weighted difference, draft max
   float sd, pad0, pad1, pad2;  // draft sum
 };
-static_assert(sizeof(KdPart) == 32, "a part travels as two 16-byte stores");
 
 struct KdCtrl {
-  uint64_t full[kKdMaxBuf];    // both slices of a row staged (producer -> compute warps)
-  uint64_t empty[kKdMaxBuf];   // buffer released (one arrival per compute warp)
-  uint64_t xbar[kKdXRing];     // every CTA's part of a row has arrived
-  KdPart xpart[kKdXRing][kKdMaxCluster];
-  KdPart wpart[kKdWarps];      // per-warp parts of the current row
+  uint64_t full[kKdStages];    // slot filled (producer -> consumers)
+  uint64_t empty[kKdStages];   // slot released (one arrival per consumer warp)
+  KdPart wpart[2][kKdWarps];   // per-warp parts of a row (by row parity)
 };
 constexpr int kKdCtrlBytes = ((static_cast<int>(sizeof(KdCtrl)) + 1023) / 1024) * 1024;
+constexpr int kKdSmemBytes = kKdCtrlBytes + kKdStages * 2 * kKdHalf;
+static_assert(kKdSmemBytes <= 227 * 1024, "three slots must fit in one CTA");
 
 struct KdParams {
   const void* target;          // [rows, V]
@@ -65,14 +71,14 @@ struct KdParams {
   int rows, t_len, V;
   float c2;                    // log2(e) / T
   float inv_T;
-  int slice_elems;             // logits per CTA slice (multiple of 64)
-  int slot_bytes;              // bytes of one staged row slice (multiple of 128)
-  int nbuf;                    // row buffers (1 .. kKdMaxBuf)
+  int nchunks;                 // slots per row and pass: ceil(V * elt / kKdHalf)
   int bulk;                    // rows 16-byte aligned: cp.async.bulk; else plain loads
 };
 
-// A part's numbers rescaled onto the common maxima of the parts in `lane`s
-// 0..n-1 (warp-wide; every lane returns the combined part).
+// A part's numbers rescaled onto the common maxima of the parts in lanes
+// 0..n-1 (warp-wide; every lane returns the combined part).  The sums are
+// added in a fixed butterfly order, so every warp that combines the same
+// parts gets the same bits.
 __device__ __forceinline__ KdPart combine_parts(const KdPart& mine, bool in, int n_lanes_pow2, float c2) {
   const float mt = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(in ? mine.mt : -INFINITY)));
   const float md = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(in ? mine.md : -INFINITY)));
@@ -99,142 +105,205 @@ __device__ __forceinline__ KdPart combine_parts(const KdPart& mine, bool in, int
   return r;
 }
 
+// Rescale a lane's running sums onto a larger maximum vm (also the first
+// time: the sums start empty).
+__device__ __forceinline__ void raise_max(float vm, float c2, float& m, float& k, f2& s, f2& a) {
+  const float kn = __fmul_rn(vm, c2);
+  const float f = m == -INFINITY ? 0.f : fast_exp2(__fsub_rn(k, kn));
+  const f2 ff = pack2(f, f);
+  s = mul2(s, ff);
+  a = mul2(a, ff);
+  m = vm;
+  k = kn;
+}
+
+// 16 bytes to global memory, marked as read by nobody soon (st.global.cs).
+__device__ __forceinline__ void store_streaming(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 template <int ELT, bool GRAD>
-struct KdRow {
+struct KdRows {
   using V = Vec<ELT>;
   static constexpr int NV = V::N;
 
   const KdParams& P;
   KdCtrl& C;
-  unsigned char* buf;          // nbuf x (target slice, draft slice)
-  const int lane, warp, cs, rank;
-  int lo, n, bytes, nvec;      // this CTA's slice: logits [lo, lo + n), bytes, 16-byte vectors
+  unsigned char* ring;         // kKdStages slots of (target part, draft part)
+  unsigned int* failed;        // bit 0: the producer gave up; bit 1: a consumer did
+  const int lane, warp;
+  const long long row_bytes;
 
-  __device__ KdRow(const KdParams& p, KdCtrl& c, unsigned char* b, int ln, int wp, int ncta, int rk)
-      : P(p), C(c), buf(b), lane(ln), warp(wp), cs(ncta), rank(rk) {
-    lo = min(p.V, rank * p.slice_elems);
-    n = min(p.V, lo + p.slice_elems) - lo;
-    bytes = n * ELT;
-    nvec = (bytes + 15) / 16;
+  __device__ KdRows(const KdParams& p, KdCtrl& c, unsigned char* r, unsigned int* f, int ln, int wp)
+      : P(p), C(c), ring(r), failed(f), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * ELT) {}
+
+  __device__ unsigned char* slot(int s) const { return ring + static_cast<size_t>(s) * 2 * kKdHalf; }
+  __device__ int chunk_bytes(int c) const {
+    const long long left = row_bytes - static_cast<long long>(c) * kKdHalf;
+    return static_cast<int>(left < kKdHalf ? left : kKdHalf);
   }
 
-  __device__ unsigned char* tslice(int b) const { return buf + static_cast<size_t>(b) * 2 * P.slot_bytes; }
-  __device__ unsigned char* dslice(int b) const { return tslice(b) + P.slot_bytes; }
-  __device__ uint4 vec(const unsigned char* s, int v) const { return *reinterpret_cast<const uint4*>(s + static_cast<size_t>(v) * 16); }
-
-  // ---- producer warp: stage the slices of this cluster's rows --------------
-  __device__ void stage(const unsigned char* src, unsigned char* dst, int r, uint64_t* bar) const {
-    const unsigned char* row = static_cast<const unsigned char*>(src) +
-                               (static_cast<size_t>(r) * P.V + lo) * static_cast<size_t>(ELT);
-    if (P.bulk) {
-      if (lane == 0 && bytes > 0) bulk_load(dst, row, static_cast<uint32_t>(bytes), bar);
-    } else {
-      const int npad = nvec * NV;
-      for (int e = lane; e < npad; e += 32)
-        V::store_scalar(dst, e, e < n ? V::scalar(row, e) : -INFINITY);
-    }
-  }
-
-  __device__ void produce(int first, int stride, int niter, unsigned int* failed) {
-    for (int i = 0; i < niter; ++i) {
-      const int b = i % P.nbuf;
-      const uint32_t par = static_cast<uint32_t>(i / P.nbuf) & 1u;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait_bounded(&C.empty[b], par ^ 1u, kDrainLimitNs) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) { if (lane == 0) atomicOr(failed, 1u); return; }
-      const int r = first + i * stride;
-      if (lane == 0 && P.bulk) mbar_expect_tx(&C.full[b], static_cast<uint32_t>(2 * bytes));
-      stage(static_cast<const unsigned char*>(P.target), tslice(b), r, &C.full[b]);
-      stage(static_cast<const unsigned char*>(P.draft), dslice(b), r, &C.full[b]);
-      if (!P.bulk) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&C.full[b]);
+  // ---- producer warp ---------------------------------------------------------
+  // Every row pair once (and for the gradient twice, the second time right
+  // behind the first), kKdHalf bytes of each row per slot.
+  __device__ void produce() {
+    const uint64_t first_out = evict_first_policy();
+    const int passes = GRAD ? 2 : 1;
+    int q = 0;
+    for (int r = blockIdx.x; r < P.rows; r += gridDim.x) {
+      const unsigned char* rt = static_cast<const unsigned char*>(P.target) + static_cast<size_t>(r) * row_bytes;
+      const unsigned char* rd = static_cast<const unsigned char*>(P.draft) + static_cast<size_t>(r) * row_bytes;
+      for (int pass = 0; pass < passes; ++pass) {
+        // a pass read again keeps its lines in L2; the last read of a row
+        // marks them first out
+        const bool last_read = pass == passes - 1;
+        for (int c = 0; c < P.nchunks; ++c, ++q) {
+          const int s = q % kKdStages;
+          int ok = 1;
+          if (lane == 0) ok = mbar_wait_bounded(&C.empty[s], ((q / kKdStages) & 1) ^ 1, kDrainLimitNs) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            if (lane == 0) atomicOr(failed, 1u);
+            return;
+          }
+          const long long off = static_cast<long long>(c) * kKdHalf;
+          const int bytes = chunk_bytes(c);
+          unsigned char* dst = slot(s);
+          if (P.bulk) {
+            if (lane == 0) {
+              mbar_expect_tx(&C.full[s], static_cast<uint32_t>(2 * bytes));
+              if (last_read) {
+                bulk_load_hint(dst, rt + off, static_cast<uint32_t>(bytes), &C.full[s], first_out);
+                bulk_load_hint(dst + kKdHalf, rd + off, static_cast<uint32_t>(bytes), &C.full[s], first_out);
+              } else {
+                bulk_load(dst, rt + off, static_cast<uint32_t>(bytes), &C.full[s]);
+                bulk_load(dst + kKdHalf, rd + off, static_cast<uint32_t>(bytes), &C.full[s]);
+              }
+            }
+          } else {
+            // rows not 16-byte aligned: plain loads, the last vector padded with -inf
+            const long long e0 = off / ELT;
+            const int n = bytes / ELT;
+            const int npad = (n + NV - 1) / NV * NV;
+            for (int e = lane; e < npad; e += 32) {
+              V::store_scalar(dst, e, e < n ? V::scalar(rt, e0 + e) : -INFINITY);
+              V::store_scalar(dst + kKdHalf, e, e < n ? V::scalar(rd, e0 + e) : -INFINITY);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&C.full[s]);
+          }
+        }
       }
     }
   }
 
-  // ---- compute warps ---------------------------------------------------------
+  // ---- consumer warps --------------------------------------------------------
 
-  // This CTA's part of the row in buffer b, sent to every CTA of the cluster.
-  __device__ void pass1_send(int b, int xs) {
-    const unsigned char* ts = tslice(b);
-    const unsigned char* ds = dslice(b);
-    const int per_warp = (nvec + kKdWarps - 1) / kKdWarps;
-    const int v0 = warp * per_warp, v1 = min(nvec, v0 + per_warp);
-    // this lane's maxima (packed; NaN is passed over here and caught by the
-    // sums, or below when a lane holds nothing but -inf and NaN), then its
-    // sums against K = fl(M c)
-    float mt = -INFINITY, md = -INFINITY;
-    for (int v = v0 + lane; v < v1; v += 32) {
-      const uint4 tv[1] = {vec(ts, v)}, dv[1] = {vec(ds, v)};
-      mt = fmaxf(mt, V::vmax(tv));
-      md = fmaxf(md, V::vmax(dv));
+  // This lane's vectors of slot s (target, draft), -inf past the chunk; the
+  // slot is released as soon as they are in registers.  False if the wait
+  // gave up (every later wait is then skipped: the rows turn NaN).
+  __device__ bool take(int s, int q, int c, bool& dead, uint4 (&tv)[kKdVecsPerLane], uint4 (&dv)[kKdVecsPerLane]) {
+    bool ok = !dead && mbar_wait_bounded(&C.full[s], static_cast<uint32_t>(q / kKdStages) & 1u, kDrainLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && !dead) {
+      dead = true;
+      if (lane == 0) atomicOr(failed, 2u);
     }
+    const int nvec = (chunk_bytes(c) + 15) / 16;
+    const unsigned char* src = slot(s);
+#pragma unroll
+    for (int j = 0; j < kKdVecsPerLane; ++j) {
+      const int v = warp * kKdVecsPerWarp + j * 32 + lane;
+      const bool in = v < nvec;
+      tv[j] = in ? *reinterpret_cast<const uint4*>(src + static_cast<size_t>(v) * 16) : V::neg_inf();
+      dv[j] = in ? *reinterpret_cast<const uint4*>(src + kKdHalf + static_cast<size_t>(v) * 16) : V::neg_inf();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&C.empty[s]);
+    return ok;
+  }
+
+  __device__ void consume() {
     const float c2 = P.c2;
-    // (a lane whose logits are all -inf adds nothing)
-    const float kt = __fmul_rn(mt, c2), kd = __fmul_rn(md, c2);
-    const bool any_t = mt != -INFINITY, any_d = md != -INFINITY;
-    if (!any_t || !any_d) {
-      int nan_seen = 0;
-      for (int v = v0 + lane; v < v1; v += 32) {
-        float zt[NV], zd[NV];
-        V::unpack(vec(ts, v), zt);
-        V::unpack(vec(ds, v), zd);
+    const f2 cc = pack2(c2, c2);
+    int q = 0, row_i = 0;
+    bool dead = false;
+    for (int r = blockIdx.x; r < P.rows; r += gridDim.x, ++row_i) {
+      // ---- first pass: per lane, running maxima and sums against K = fl(M c)
+      float mt = -INFINITY, md = -INFINITY, kt = 0.f, kd = 0.f;
+      f2 st2 = 0ull, sd2 = 0ull, a2 = 0ull, unused = 0ull;
+      bool lost = false;
+      for (int c = 0; c < P.nchunks; ++c, ++q) {
+        uint4 tv[kKdVecsPerLane], dv[kKdVecsPerLane];
+        if (!take(q % kKdStages, q, c, dead, tv, dv)) lost = true;
+        // NaN is passed over by the maxima and kept by the sums
+        const float vt = V::vmax(tv), vd = V::vmax(dv);
+        if (vt > mt) raise_max(vt, c2, mt, kt, st2, a2);
+        if (vd > md) raise_max(vd, c2, md, kd, sd2, unused);
+        const f2 nkt = pack2(-kt, -kt), nkd = pack2(-kd, -kd);
 #pragma unroll
-        for (int e = 0; e < NV; ++e) nan_seen |= (zt[e] != zt[e]) | (zd[e] != zd[e]);
-      }
-      if (nan_seen) { mt = NAN; md = NAN; }
-    }
-    float st = 0.f, a = 0.f, sd = 0.f;
-    for (int v = v0 + lane; v < v1; v += 32) {
-      float zt[NV], zd[NV];
-      V::unpack(vec(ts, v), zt);
-      V::unpack(vec(ds, v), zd);
+        for (int j = 0; j < kKdVecsPerLane; ++j) {
+          f2 zt[NV / 2], zd[NV / 2];
+          V::pairs(tv[j], zt);
+          V::pairs(dv[j], zd);
 #pragma unroll
-      for (int e = 0; e < NV; ++e) {
-        const float et = any_t ? fast_exp2(fmaf(zt[e], c2, -kt)) : 0.f;   // NaN logits stay NaN
-        const float ed = any_d ? fast_exp2(fmaf(zd[e], c2, -kd)) : 0.f;
-        st += et;
-        sd += ed;
-        // p(x) = 0 contributes nothing, also against q(x) = 0
-        a = fmaf(et, zt[e] == -INFINITY ? 0.f : zt[e] - zd[e], a);
+          for (int i = 0; i < NV / 2; ++i) {
+            // while a lane's maximum is -inf its K is 0 and 2^(-inf) adds 0
+            const f2 et = exp2_2(fma2(zt[i], cc, nkt));
+            const f2 ed = exp2_2(fma2(zd[i], cc, nkd));
+            st2 = add2(st2, et);
+            sd2 = add2(sd2, ed);
+            // p(x) = 0 (z^t = -inf) adds nothing, also against q(x) = 0: the
+            // difference is clamped to a finite value that the zero multiplies
+            float d0, d1;
+            unpack2(sub2(zt[i], zd[i]), d0, d1);
+            a2 = fma2(et, pack2(fmaxf(d0, -FLT_MAX), fmaxf(d1, -FLT_MAX)), a2);
+          }
+        }
       }
-    }
-    KdPart mine;
-    mine.mt = mt; mine.st = st; mine.a = a; mine.md = md; mine.sd = sd;
-    mine.pad0 = mine.pad1 = mine.pad2 = 0.f;
-    const KdPart w = combine_parts(mine, true, 32, c2);
-    if (lane == 0) C.wpart[warp] = w;
-    named_barrier_sync(kKdBarCompute, kKdWarps * 32);
-    if (warp == 0) {
-      KdPart wp = C.wpart[lane < kKdWarps ? lane : 0];
-      const KdPart part = combine_parts(wp, lane < kKdWarps, kKdWarps, c2);
-      if (lane < cs) {
-        const uint32_t dst = peer(&C.xpart[xs][rank], lane);
-        const uint32_t bar = peer(&C.xbar[xs], lane);
-        st_async(dst, make_uint4(__float_as_uint(part.mt), __float_as_uint(part.st), __float_as_uint(part.a),
-                                 __float_as_uint(part.md)), bar);
-        st_async(dst + 16, make_uint4(__float_as_uint(part.sd), 0u, 0u, 0u), bar);
-      }
-      __syncwarp();
+      // ---- the row's numbers, the same in every warp
+      float x0, x1;
+      KdPart mine;
+      unpack2(st2, x0, x1); mine.st = x0 + x1;
+      unpack2(a2, x0, x1);  mine.a = x0 + x1;
+      unpack2(sd2, x0, x1); mine.sd = x0 + x1;
+      // a NaN sum is carried by the maximum (a lane whose maximum stayed
+      // -inf would otherwise drop it in the combine); so is a lost wait
+      mine.mt = (mine.st != mine.st || lost) ? NAN : mt;
+      mine.md = (mine.sd != mine.sd || lost) ? NAN : md;
+      mine.pad0 = mine.pad1 = mine.pad2 = 0.f;
+      const KdPart w = combine_parts(mine, true, 32, c2);
+      if (lane == 0) C.wpart[row_i & 1][warp] = w;
+      named_barrier_sync(kKdBarCompute, kKdWarps * 32);
+      const KdPart row = combine_parts(C.wpart[row_i & 1][lane < kKdWarps ? lane : 0], lane < kKdWarps, kKdWarps, c2);
+      const bool valid = isfinite(row.mt) && isfinite(row.md) && isfinite(row.st) && isfinite(row.sd) &&
+                         row.st > 0.f && row.sd > 0.f && !isnan(row.a);
+      if (warp == 0 && lane == 0) P.row_kl[r] = row_kl(row, valid);
+      if (GRAD) gradient(r, row, valid, q, dead);
     }
   }
 
-  // The row's numbers from every CTA's part (the same in every warp and CTA).
-  __device__ KdPart gather(int xs, int i, bool& arrived) {
-    arrived = mbar_wait_bounded(&C.xbar[xs], static_cast<uint32_t>(i / kKdXRing) & 1u, kDrainLimitNs);
-    const bool in = lane < cs;
-    KdPart pt = C.xpart[xs][in ? lane : 0];
-    int n_pow2 = 1;
-    while (n_pow2 < cs) n_pow2 <<= 1;
-    return combine_parts(pt, in, n_pow2, P.c2);
+  // KL / ln 2 = c A / S^t - (K^t - K^d) - log2(S^t / S^d), with the very
+  // K = fl(M c) and sums the exponentials were taken against.  In fp32
+  // without losing the difference: c A / S^t as hi + lo (fused multiply-add),
+  // K^t - K^d and the final difference by TwoSum; the error left is that of
+  // A / S^t's rounding and of the sums themselves.
+  __device__ float row_kl(const KdPart& row, bool valid) const {
+    if (!valid) return NAN;
+    const float kt = __fmul_rn(row.mt, P.c2), kd = __fmul_rn(row.md, P.c2);
+    const float q = __fdiv_rn(row.a, row.st);
+    const float h1 = __fmul_rn(P.c2, q);
+    if (isinf(h1)) return h1;   // q(x) = 0 where p(x) > 0: A, hence KL, is +inf
+    const float l1 = __fmaf_rn(P.c2, q, -h1);
+    float h2, l2, h3, l3;
+    two_sum(kt, -kd, h2, l2);
+    two_sum(h1, -h2, h3, l3);
+    const float rest = __fadd_rn(__fsub_rn(l1, l2), l3) - log2f(__fdiv_rn(row.st, row.sd));
+    return __fmul_rn(0.6931471805599453f, __fadd_rn(h3, rest));
   }
 
-  // Gradient of this CTA's slice of the row in buffer b.
-  __device__ void pass2(int b, int r, const KdPart& row, bool valid) {
-    const unsigned char* ts = tslice(b);
-    const unsigned char* ds = dslice(b);
+  // ---- second pass: w (q - p) / T for every logit of the row pair
+  __device__ void gradient(int r, const KdPart& row, bool valid, int& q, bool& dead) {
     const float c2 = P.c2;
     const float kt = __fmul_rn(row.mt, c2), kd = __fmul_rn(row.md, c2);
     float lt, ld;
@@ -243,78 +312,35 @@ struct KdRow {
     const float scale = P.weights[r / P.t_len] * P.inv_T;
     const float ct = valid ? -(kt + lt) : NAN;   // log2 p(x) = z c - K - log2 S, one fma
     const float cd = valid ? -(kd + ld) : NAN;   // (an invalid row writes NaN)
-    unsigned char* out = static_cast<unsigned char*>(P.grad) + (static_cast<size_t>(r) * P.V + lo) * static_cast<size_t>(ELT);
-    const int per_warp = (nvec + kKdWarps - 1) / kKdWarps;
-    const int v0 = warp * per_warp, v1 = min(nvec, v0 + per_warp);
-    for (int v = v0 + lane; v < v1; v += 32) {
-      float zt[NV], zd[NV], g[NV];
-      V::unpack(vec(ts, v), zt);
-      V::unpack(vec(ds, v), zd);
+    const f2 cc = pack2(c2, c2), ct2 = pack2(ct, ct), cd2 = pack2(cd, cd), sc2 = pack2(scale, scale);
+    unsigned char* out_row = static_cast<unsigned char*>(P.grad) + static_cast<size_t>(r) * row_bytes;
+    for (int c = 0; c < P.nchunks; ++c, ++q) {
+      uint4 tv[kKdVecsPerLane], dv[kKdVecsPerLane];
+      take(q % kKdStages, q, c, dead, tv, dv);
+      const int nvec = (chunk_bytes(c) + 15) / 16;
+      unsigned char* out = out_row + static_cast<size_t>(c) * kKdHalf;
 #pragma unroll
-      for (int e = 0; e < NV; ++e) {
-        const float p = fast_exp2(fmaf(zt[e], c2, ct));
-        const float q = fast_exp2(fmaf(zd[e], c2, cd));
-        g[e] = scale * (q - p);
-      }
-      if (P.bulk) {
-        *reinterpret_cast<uint4*>(out + static_cast<size_t>(v) * 16) = V::pack(g);
-      } else {
+      for (int j = 0; j < kKdVecsPerLane; ++j) {
+        const int v = warp * kKdVecsPerWarp + j * 32 + lane;
+        f2 zt[NV / 2], zd[NV / 2];
+        V::pairs(tv[j], zt);
+        V::pairs(dv[j], zd);
+        float g[NV];
 #pragma unroll
-        for (int e = 0; e < NV; ++e)
-          if (v * NV + e < n) V::store_rounded(out, v * NV + e, g[e]);
-      }
-    }
-  }
-
-  // Two orders of the work of a row:
-  //  * three or more buffers (loads issued well ahead): row i+1's first pass
-  //    and part go out before row i's parts are awaited, hiding the exchange;
-  //  * one or two buffers: row i is finished (exchange, KL, gradient, buffer
-  //    released) before row i+1's first pass, so that the load of row i+2 into
-  //    the released buffer has that first pass, an exchange and a gradient to
-  //    hide behind.
-  // Either way a CTA sends a row's part only after reading every part of the
-  // row two before it, and a peer's part of that row was sent after the peer
-  // read the row three before: at most four rows of parts are ever in the
-  // four exchange slots.
-  __device__ void compute(int first, int stride, int niter) {
-    if (niter <= 0) return;
-    const bool ahead = P.nbuf >= 3;
-    mbar_wait_bounded(&C.full[0], 0u, kDrainLimitNs);
-    pass1_send(0, 0);
-    for (int i = 0; i < niter; ++i) {
-      const int b = i % P.nbuf;
-      const int xs = i % kKdXRing;
-      if (ahead && i + 1 < niter) {
-        const int bn = (i + 1) % P.nbuf;
-        mbar_wait_bounded(&C.full[bn], static_cast<uint32_t>((i + 1) / P.nbuf) & 1u, kDrainLimitNs);
-        pass1_send(bn, (i + 1) % kKdXRing);
-      }
-      bool arrived = true;
-      const KdPart row = gather(xs, i, arrived);
-      if (warp == 0 && lane == 0) mbar_expect_tx(&C.xbar[xs], static_cast<uint32_t>(cs * sizeof(KdPart)));
-      const int r = first + i * stride;
-      const bool valid = arrived && isfinite(row.mt) && isfinite(row.md) && isfinite(row.st) && isfinite(row.sd) &&
-                         row.st > 0.f && row.sd > 0.f && !isnan(row.a);
-      if (rank == 0 && warp == 0 && lane == 0) {
-        // KL / ln 2 = c A / S^t - (K^t - K^d) - log2(S^t / S^d), with the very
-        // K = fl(M c) and sums the exponentials were taken against
-        double kl = NAN;
-        if (valid) {
-          const double kt = __fmul_rn(row.mt, P.c2), kd = __fmul_rn(row.md, P.c2);
-          kl = 0.69314718055994530942 *
-               (static_cast<double>(P.c2) * static_cast<double>(row.a) / static_cast<double>(row.st) -
-                (kt - kd) - log2(static_cast<double>(row.st) / static_cast<double>(row.sd)));
+        for (int i = 0; i < NV / 2; ++i) {
+          const f2 pp = exp2_2(fma2(zt[i], cc, ct2));
+          const f2 qq = exp2_2(fma2(zd[i], cc, cd2));
+          unpack2(mul2(sc2, sub2(qq, pp)), g[2 * i], g[2 * i + 1]);
         }
-        P.row_kl[r] = static_cast<float>(kl);
-      }
-      if (GRAD) pass2(b, r, row, valid);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&C.empty[b]);
-      if (!ahead && i + 1 < niter) {
-        const int bn = (i + 1) % P.nbuf;
-        mbar_wait_bounded(&C.full[bn], static_cast<uint32_t>((i + 1) / P.nbuf) & 1u, kDrainLimitNs);
-        pass1_send(bn, (i + 1) % kKdXRing);
+        if (v >= nvec) continue;
+        if (P.bulk) {
+          store_streaming(out + static_cast<size_t>(v) * 16, V::pack(g));
+        } else {
+          const int n = chunk_bytes(c) / ELT;
+#pragma unroll
+          for (int e = 0; e < NV; ++e)
+            if (v * NV + e < n) V::store_rounded(out, v * NV + e, g[e]);
+        }
       }
     }
   }
@@ -324,30 +350,19 @@ template <int ELT, bool GRAD>
 __global__ void __launch_bounds__(kKdThreads, 1) kd_kernel(const KdParams P, unsigned int* failed) {
   extern __shared__ __align__(1024) unsigned char smem[];
   KdCtrl& C = *reinterpret_cast<KdCtrl*>(smem);
-  unsigned char* buf = smem + kKdCtrlBytes;
+  unsigned char* ring = smem + kKdCtrlBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cs = cluster_ctas();
   if (tid == 0) {
-    for (int b = 0; b < kKdMaxBuf; ++b) {
-      mbar_init(&C.full[b], 1);
-      mbar_init(&C.empty[b], kKdWarps);
+    for (int s = 0; s < kKdStages; ++s) {
+      mbar_init(&C.full[s], 1);
+      mbar_init(&C.empty[s], kKdWarps);
     }
-    for (int x = 0; x < kKdXRing; ++x) mbar_init(&C.xbar[x], 1);
     fence_mbar_init();
-    for (int x = 0; x < kKdXRing; ++x) mbar_expect_tx(&C.xbar[x], static_cast<uint32_t>(cs * sizeof(KdPart)));
   }
-  cluster_sync();
-  {
-    uint32_t cid, ncl;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cid));
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(ncl));
-    const int first = static_cast<int>(cid), stride = static_cast<int>(ncl);
-    const int niter = first < P.rows ? (P.rows - first + stride - 1) / stride : 0;
-    KdRow<ELT, GRAD> k(P, C, buf, lane, warp, cs, cluster_rank());
-    if (warp == kKdWarps) k.produce(first, stride, niter, failed);
-    else k.compute(first, stride, niter);
-  }
-  cluster_sync();   // no CTA leaves while a peer may still write into its shared memory
+  __syncthreads();
+  KdRows<ELT, GRAD> k(P, C, ring, failed, lane, warp);
+  if (warp == kKdWarps) k.produce();
+  else k.consume();
 }
 
 // loss[b] = w_b * sum_t row_kl[b, t], in position order.
@@ -360,25 +375,14 @@ __global__ void kd_loss_kernel(int n_seq, int t_len, const float* row_kl, const 
 }
 
 // ---------------------------------------------------------------------------
-// Host side: the launch shape per device, cached
+// Host side
 // ---------------------------------------------------------------------------
-
-constexpr int kKdSmemLimit = 227 * 1024;
-
-struct KdShapeKey {
-  int V = 0, elt = 0, grad = 0;
-};
 
 struct KdDevice {
   bool ready = false;
   int sms = 0;
-  unsigned int* failed = nullptr;   // set by a producer that gave up (bounded wait)
-  // launch shapes already worked out (the occupancy queries cost host time)
-  static constexpr int kCached = 8;
-  KdShapeKey key[kCached];
-  int shape_cs[kCached] = {0}, shape_nbuf[kCached] = {0}, shape_slice[kCached] = {0}, shape_slot[kCached] = {0};
-  int shape_clusters[kCached] = {0}, shape_smem[kCached] = {0};
-  int next = 0;
+  unsigned int* failed = nullptr;   // set by a warp that gave up a bounded wait
+  bool smem_set[4] = {false, false, false, false};
 };
 std::mutex g_kd_mutex;
 KdDevice g_kd[64];
@@ -391,53 +395,36 @@ const void* kd_kernel_for(int elt, bool grad) {
   return grad ? kd_fn<4, true>() : kd_fn<4, false>();
 }
 
-struct KdShape {
-  int cs = 0, nbuf = 0, slice_elems = 0, slot = 0, max_clusters = 0, smem = 0;
-};
-
-// The cluster (1 .. 16 CTAs) and buffer count: as many row buffers as fit,
-// up to kKdMaxBuf, taking the fewest CTAs per row that still give three
-// buffers (rows keep arriving while earlier ones are reduced), else the
-// deepest pipeline any launchable size allows.
-bool kd_shape(int V, int elt, bool with_grad, KdShape* out) {
-  const void* fn = kd_kernel_for(elt, with_grad);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    (void)cudaGetLastError();
-  KdShape best;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kKdThreads, 1, 1);
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  for (int c = 1; c <= kKdMaxCluster; c *= 2) {
-    const int per = static_cast<int>(((static_cast<long long>(V) + c - 1) / c + 63) / 64 * 64);
-    const int sbytes = static_cast<int>(((static_cast<long long>(per) * elt) + 127) / 128 * 128);
-    int nb = static_cast<int>((kKdSmemLimit - kKdCtrlBytes) / (2LL * sbytes));
-    if (nb > kKdMaxBuf) nb = kKdMaxBuf;
-    if (nb < 1) continue;
-    if (best.cs != 0 && (best.nbuf >= 3 || nb <= best.nbuf)) continue;
-    const int sm = kKdCtrlBytes + nb * 2 * sbytes;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, sm) != cudaSuccess) {
-      (void)cudaGetLastError();
-      continue;
-    }
-    attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-    cfg.gridDim = dim3(static_cast<unsigned>(c), 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(sm);
-    int mc = 0;
-    if (cudaOccupancyMaxActiveClusters(&mc, fn, &cfg) != cudaSuccess || mc <= 0) {
-      (void)cudaGetLastError();
-      continue;
-    }
-    best.cs = c; best.nbuf = nb; best.slice_elems = per; best.slot = sbytes; best.max_clusters = mc; best.smem = sm;
+// The device's record, set up once (its properties, the failure word).
+sv_status kd_device(KdDevice** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_kd_mutex);
+  KdDevice& d = g_kd[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (!(prop.major == 10 && prop.minor == 3)) return SV_ERR_UNSUPPORTED;
+    if (cudaMalloc(&d.failed, sizeof(unsigned int)) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaMemset(d.failed, 0, sizeof(unsigned int)) != cudaSuccess) return SV_ERR_CUDA;
+    d.sms = prop.multiProcessorCount;
+    d.ready = true;
   }
-  if (best.cs == 0) return false;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, best.smem) != cudaSuccess) return false;
-  *out = best;
-  return true;
+  *out = &d;
+  return SV_OK;
+}
+
+// The kernel's shared-memory limit, raised once per instance and device.
+sv_status kd_prepare(KdDevice* d, int elt, bool grad) {
+  const int i = (elt == 2 ? 0 : 2) + (grad ? 1 : 0);
+  std::lock_guard<std::mutex> lock(g_kd_mutex);
+  if (d->smem_set[i]) return SV_OK;
+  if (cudaFuncSetAttribute(kd_kernel_for(elt, grad), cudaFuncAttributeMaxDynamicSharedMemorySize, kKdSmemBytes) !=
+      cudaSuccess)
+    return SV_ERR_CUDA;
+  d->smem_set[i] = true;
+  return SV_OK;
 }
 
 }  // namespace
@@ -454,69 +441,17 @@ extern "C" sv_status spec_kd_loss(int n_seq, int t_len, int V, sv_dtype dtype, c
   if (!target_logits || !draft_logits || !weights || !row_kl || !loss) return SV_ERR_INVALID_ARG;
   const int elt = dtype == SV_F32 ? 4 : 2;
   const long long row_bytes = static_cast<long long>(V) * elt;
+  if (row_bytes > (1LL << 30)) return SV_ERR_INVALID_ARG;
   const double c2 = 1.4426950408889634 / static_cast<double>(temperature);
   if (!(c2 < 1e30)) return SV_ERR_INVALID_ARG;
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return SV_ERR_UNSUPPORTED;
   KdDevice* D = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_kd_mutex);
-    KdDevice& d = g_kd[dev];
-    if (!d.ready) {
-      cudaDeviceProp prop;
-      if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SV_ERR_CUDA;
-      if (!(prop.major == 10 && prop.minor == 3)) return SV_ERR_UNSUPPORTED;
-      if (cudaMalloc(&d.failed, sizeof(unsigned int)) != cudaSuccess) return SV_ERR_CUDA;
-      if (cudaMemset(d.failed, 0, sizeof(unsigned int)) != cudaSuccess) return SV_ERR_CUDA;
-      d.sms = prop.multiProcessorCount;
-      d.ready = true;
-    }
-    D = &d;
-  }
-
+  sv_status st = kd_device(&D);
+  if (st != SV_OK) return st;
   const bool with_grad = grad != nullptr;
-  KdShape sh;
-  {
-    std::lock_guard<std::mutex> lock(g_kd_mutex);
-    int hit = -1;
-    for (int c = 0; c < KdDevice::kCached; ++c)
-      if (D->key[c].V == V && D->key[c].elt == elt && D->key[c].grad == (with_grad ? 1 : 0) && D->shape_cs[c] > 0)
-        hit = c;
-    if (hit >= 0) {
-      sh.cs = D->shape_cs[hit]; sh.nbuf = D->shape_nbuf[hit]; sh.slice_elems = D->shape_slice[hit];
-      sh.slot = D->shape_slot[hit]; sh.max_clusters = D->shape_clusters[hit]; sh.smem = D->shape_smem[hit];
-    } else {
-      if (!kd_shape(V, elt, with_grad, &sh)) return SV_ERR_UNSUPPORTED;
-      const int c = D->next;
-      D->next = (D->next + 1) % KdDevice::kCached;
-      D->key[c].V = V; D->key[c].elt = elt; D->key[c].grad = with_grad ? 1 : 0;
-      D->shape_cs[c] = sh.cs; D->shape_nbuf[c] = sh.nbuf; D->shape_slice[c] = sh.slice_elems;
-      D->shape_slot[c] = sh.slot; D->shape_clusters[c] = sh.max_clusters; D->shape_smem[c] = sh.smem;
-    }
-  }
-  // the kernel's shared-memory size may have been set for another shape meanwhile
-  if (cudaFuncSetAttribute(kd_kernel_for(elt, with_grad), cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem) !=
-      cudaSuccess)
-    return SV_ERR_CUDA;
-  const int cs = sh.cs, nbuf = sh.nbuf, slice_elems = sh.slice_elems, slot = sh.slot;
-  const int max_clusters = sh.max_clusters, smem = sh.smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kKdThreads, 1, 1);
-  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  const int rows = n_seq * t_len;
-  const int clusters = rows < max_clusters ? rows : max_clusters;
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
+  if ((st = kd_prepare(D, elt, with_grad)) != SV_OK) return st;
 
+  const int rows = n_seq * t_len;
   KdParams p{};
   p.target = target_logits;
   p.draft = draft_logits;
@@ -528,22 +463,23 @@ extern "C" sv_status spec_kd_loss(int n_seq, int t_len, int V, sv_dtype dtype, c
   p.V = V;
   p.c2 = static_cast<float>(c2);
   p.inv_T = 1.f / temperature;
-  p.slice_elems = slice_elems;
-  p.slot_bytes = slot;
-  p.nbuf = nbuf;
+  p.nchunks = static_cast<int>((row_bytes + kKdHalf - 1) / kKdHalf);
   auto aligned = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
   p.bulk = (row_bytes % 16 == 0) && aligned(target_logits) && aligned(draft_logits) &&
            (grad == nullptr || aligned(grad));
+  // one CTA per SM, every row to the CTA b + i * grid
+  const int ctas = rows < D->sms ? rows : D->sms;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   sv::NvtxRange range("spec_kd_loss");
-  cudaError_t e;
-  if (elt == 2)
-    e = with_grad ? cudaLaunchKernelEx(&cfg, kd_kernel<2, true>, p, D->failed)
-                  : cudaLaunchKernelEx(&cfg, kd_kernel<2, false>, p, D->failed);
-  else
-    e = with_grad ? cudaLaunchKernelEx(&cfg, kd_kernel<4, true>, p, D->failed)
-                  : cudaLaunchKernelEx(&cfg, kd_kernel<4, false>, p, D->failed);
-  if (e != cudaSuccess) return SV_ERR_CUDA;
-  kd_loss_kernel<<<(n_seq + 255) / 256, 256, 0, cfg.stream>>>(n_seq, t_len, row_kl, weights, loss);
+  if (elt == 2) {
+    if (with_grad) kd_kernel<2, true><<<ctas, kKdThreads, kKdSmemBytes, s>>>(p, D->failed);
+    else kd_kernel<2, false><<<ctas, kKdThreads, kKdSmemBytes, s>>>(p, D->failed);
+  } else {
+    if (with_grad) kd_kernel<4, true><<<ctas, kKdThreads, kKdSmemBytes, s>>>(p, D->failed);
+    else kd_kernel<4, false><<<ctas, kKdThreads, kKdSmemBytes, s>>>(p, D->failed);
+  }
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  kd_loss_kernel<<<(n_seq + 255) / 256, 256, 0, s>>>(n_seq, t_len, row_kl, weights, loss);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -551,10 +487,12 @@ extern "C" sv_status spec_kd_launch_shape(int V, sv_dtype dtype, int with_grad, 
                                           int* grid_ctas) {
   using namespace sv;
   if (V < 1 || (dtype != SV_F32 && dtype != SV_BF16)) return SV_ERR_INVALID_ARG;
-  KdShape sh;
-  if (!kd_shape(V, dtype == SV_F32 ? 4 : 2, with_grad != 0, &sh)) return SV_ERR_UNSUPPORTED;
-  if (cluster) *cluster = sh.cs;
-  if (buffers) *buffers = sh.nbuf;
-  if (grid_ctas) *grid_ctas = sh.max_clusters * sh.cs;
+  (void)with_grad;
+  KdDevice* D = nullptr;
+  const sv_status st = kd_device(&D);
+  if (st != SV_OK) return st;
+  if (cluster) *cluster = 1;
+  if (buffers) *buffers = kKdStages;
+  if (grid_ctas) *grid_ctas = D->sms;
   return SV_OK;
 }
