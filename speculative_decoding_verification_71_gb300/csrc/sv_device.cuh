@@ -153,6 +153,24 @@ __device__ __forceinline__ f2 one_minus_exp2_2(f2 d) {
   return pack2(one_minus_exp2(d0), one_minus_exp2(d1));
 }
 
+// The same with the series taken two lanes per f32x2 instruction (its six
+// coefficient pairs live in registers: for kernels with registers to spare).
+// Bit-identical to one_minus_exp2, lane by lane.
+__device__ __forceinline__ f2 one_minus_exp2_2r(f2 d) {
+  f2 s = fma2(d, pack2(1.5403530393381609e-4f, 1.5403530393381609e-4f),
+              pack2(1.3333558146428443e-3f, 1.3333558146428443e-3f));
+  s = fma2(d, s, pack2(9.6181291076284772e-3f, 9.6181291076284772e-3f));
+  s = fma2(d, s, pack2(5.5504108664821580e-2f, 5.5504108664821580e-2f));
+  s = fma2(d, s, pack2(2.4022650695910071e-1f, 2.4022650695910071e-1f));
+  s = fma2(d, s, pack2(6.9314718055994531e-1f, 6.9314718055994531e-1f));
+  float s0, s1, d0, d1;
+  unpack2(mul2(d, s), s0, s1);
+  unpack2(d, d0, d1);
+  const float r0 = d0 > kSmallDelta ? -s0 : __fsub_rn(1.f, fast_exp2(d0));
+  const float r1 = d1 > kSmallDelta ? -s1 : __fsub_rn(1.f, fast_exp2(d1));
+  return pack2(r0, r1);
+}
+
 // a + b = s + e exactly (Knuth's TwoSum, six operations, no branch).
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
@@ -267,6 +285,25 @@ template <> struct Vec<2> {
     const uint32_t w = max2(max2(m[0], m[1]), max2(m[2], m[3]));
     return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   }
+  // the same maximum, NaN if any value is NaN
+  __device__ __forceinline__ static uint32_t max2_nan(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+  }
+  template <int N>
+  __device__ __forceinline__ static float vmax_nan(const uint4 (&r)[N]) {
+    uint32_t m[4] = {r[0].x, r[0].y, r[0].z, r[0].w};
+#pragma unroll
+    for (int j = 1; j < N; ++j) {
+      m[0] = max2_nan(m[0], r[j].x); m[1] = max2_nan(m[1], r[j].y);
+      m[2] = max2_nan(m[2], r[j].z); m[3] = max2_nan(m[3], r[j].w);
+    }
+    const uint32_t w = max2_nan(max2_nan(m[0], m[1]), max2_nan(m[2], m[3]));
+    float res;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(res) : "f"(__uint_as_float(w << 16)), "f"(__uint_as_float(w & 0xffff0000u)));
+    return res;
+  }
 };
 template <> struct Vec<4> {
   static constexpr int N = 4;
@@ -300,6 +337,20 @@ template <> struct Vec<4> {
       m[2] = fmaxf(m[2], __uint_as_float(r[j].z)); m[3] = fmaxf(m[3], __uint_as_float(r[j].w));
     }
     return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+  }
+  template <int N>
+  __device__ __forceinline__ static float vmax_nan(const uint4 (&r)[N]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const float a = __uint_as_float(r[j].x), b = __uint_as_float(r[j].y);
+      const float c = __uint_as_float(r[j].z), d = __uint_as_float(r[j].w);
+      asm("max.NaN.f32 %0, %0, %1;" : "+f"(m) : "f"(a));
+      asm("max.NaN.f32 %0, %0, %1;" : "+f"(m) : "f"(b));
+      asm("max.NaN.f32 %0, %0, %1;" : "+f"(m) : "f"(c));
+      asm("max.NaN.f32 %0, %0, %1;" : "+f"(m) : "f"(d));
+    }
+    return m;
   }
 };
 

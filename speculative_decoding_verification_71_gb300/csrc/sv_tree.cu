@@ -16,18 +16,20 @@
 //   s = u[b, 0]; T == 0 accepts the first child equal to the first argmax of
 //   the node's target row and emits that argmax.
 //
-// A cluster of cs CTAs walks one sequence: each CTA streams a contiguous
-// slice of every row (through a cp.async ring in shared memory, see Chunks),
-// and the slices' sums are exchanged through distributed shared memory and
-// combined in rank order, so every CTA takes the same decisions.  cs is the
-// largest of 8, 4, 2, 1 that keeps one CTA per SM for the whole batch.  Each
-// visited node costs one pass over its
-// target row (and draft row, if it has children) for the row maximum and
-// log-sum of 2^(z c), one more pass over both rows per rejected child (the
-// residual mass, with the sums of 256-logit chunks kept for the draw), and
-// one pass for a bonus draw; the later passes find the rows in L2.  Only
-// the rows the walk visits are read.  Every reduction runs in a fixed order,
-// so the result is deterministic.
+// A cluster of cs CTAs walks one sequence: each CTA owns a contiguous slice
+// of every row (whole 256-logit chunks), and the slices' partial sums are
+// exchanged through distributed shared memory and combined in rank order, so
+// every CTA takes the same decisions.  cs is the largest of 8, 4, 2, 1 that
+// keeps one CTA per SM for the whole batch.  Within a CTA a producer warp
+// streams the slice of the rows a pass needs (the node's target row and, with
+// children, its draft row) through three 64 KB shared-memory slots with
+// cp.async.bulk, 32 KB of each row per slot, and 16 consumer warps reduce
+// each slot, two logits per f32x2 instruction.  Each visited node costs one
+// pass for the row maximum and log-sum of 2^(z c) of both rows, one more pass
+// per rejected child (the residual mass, with the sum of each warp's
+// 128-vector segment kept for the draw) and one pass for a bonus draw; the
+// later passes find the rows in L2.  Only the rows the walk visits are read.
+// Every reduction runs in a fixed order, so the result is deterministic.
 
 #include <cuda_runtime.h>
 
@@ -41,12 +43,19 @@
 namespace sv {
 namespace {
 
-constexpr int kTreeThreads = 512;
-constexpr int kTreeWarps = kTreeThreads / 32;
-constexpr int kChunkElems = 256;                 // logits per warp step: 8 per lane
-constexpr int kTreeMaxChunks = 2048;             // V <= 524288
+constexpr int kTreeWarps = 16;                          // consumer warps
+constexpr int kTreeThreads = (kTreeWarps + 1) * 32;     // + the producer warp
+constexpr int kTreeProducer = kTreeWarps;               // its warp index
+constexpr int kTreeStages = 3;                          // 64 KB staging slots
+constexpr int kTreeHalf = 32 * 1024;                    // bytes of one row per slot
+constexpr int kTreeVecsPerWarp = kTreeHalf / 16 / kTreeWarps;   // 128: one segment
+constexpr int kTreeVecsPerLane = kTreeVecsPerWarp / 32;         // 4
+constexpr int kChunkElems = 256;                        // slice boundaries: whole 256-logit chunks
+constexpr int kTreeMaxV = 524288;
+constexpr int kTreeMaxSegs = (kTreeMaxV * 4 / kTreeHalf) * kTreeWarps;   // 1024
 constexpr int kTreeMaxNodes = SV_TREE_MAX_NODES;
 constexpr int kTreeMaxCluster = 8;
+constexpr int kTreeRingBytes = kTreeStages * 2 * kTreeHalf;
 
 struct TreeParams {
   const unsigned char* target;   // [B, M, V]
@@ -61,106 +70,22 @@ struct TreeParams {
   int32_t* status;               // [B] or null
   float* alpha;                  // [B, M] or null
   int B, M, V;
-  int vec;                       // rows 16-byte aligned: vector loads
+  int vec;                       // rows 16-byte aligned: bulk copies and vector loads
   float c2;                      // log2(e) / T
   int cs;                        // CTAs per sequence (the cluster): each streams a slice of every row
 };
 
+// Sixteen bytes of logits from element e0 of a row, straight from global
+// memory (the draw's re-read): -inf past V; element loads for unaligned rows.
 template <int ELT>
-struct Rows {
-  // Eight consecutive logits from element e0 (those past V read as -inf).
-  __device__ __forceinline__ static void load8(const unsigned char* row, int e0, int V, int vec, float (&v)[8]) {
-    if (vec && e0 + 8 <= V) {
-      if (ELT == 2) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(row + static_cast<size_t>(e0) * 2));
-        Vec<2>::unpack(w, v);
-      } else {
-        const uint4 w0 = __ldg(reinterpret_cast<const uint4*>(row + static_cast<size_t>(e0) * 4));
-        const uint4 w1 = __ldg(reinterpret_cast<const uint4*>(row + static_cast<size_t>(e0) * 4 + 16));
-        v[0] = __uint_as_float(w0.x); v[1] = __uint_as_float(w0.y);
-        v[2] = __uint_as_float(w0.z); v[3] = __uint_as_float(w0.w);
-        v[4] = __uint_as_float(w1.x); v[5] = __uint_as_float(w1.y);
-        v[6] = __uint_as_float(w1.z); v[7] = __uint_as_float(w1.w);
-      }
-    } else {
+__device__ __forceinline__ uint4 load_vec(const unsigned char* row, int e0, int V, int vec) {
+  using VV = Vec<ELT>;
+  if (vec && e0 + VV::N <= V) return __ldg(reinterpret_cast<const uint4*>(row + static_cast<size_t>(e0) * ELT));
+  unsigned char buf[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        v[j] = (e0 + j < V) ? Vec<ELT>::scalar(row, e0 + j) : -INFINITY;
-    }
-  }
-};
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(smem)), "l"(gmem) : "memory");
+  for (int e = 0; e < VV::N; ++e) VV::store_scalar(buf, e, e0 + e < V ? VV::scalar(row, e0 + e) : -INFINITY);
+  return *reinterpret_cast<const uint4*>(buf);
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-
-// Calls f(c, e0, zt[8], zd[8]) for each chunk c in [c_lo, c_hi) of this
-// warp (c = c_lo + warp, c_lo + warp + W, ...), zt / zd being the lane's eight logits of the target and
-// (if `both`) draft rows from e0.  Each lane streams its own 16 (bf16) or 32
-// (fp32) bytes per row and chunk through a ring of D slots in shared memory
-// with cp.async, D chunks ahead of its use: every lane reads back only what
-// it copied itself, so no barrier is needed, and a slot is refilled only
-// after its logits were consumed.  Lanes past V or on rows that are not
-// 16-byte aligned read their logits with plain loads instead.
-template <int ELT>
-struct Chunks {
-  static constexpr int D = ELT == 2 ? 8 : 4;      // chunks in flight per warp
-  static constexpr int LB = 8 * ELT;               // bytes per lane, row and chunk
-  static constexpr int kRingBytes = kTreeWarps * D * 2 * 32 * LB;
-  __device__ __forceinline__ static unsigned char* slot(unsigned char* ring, int warp, int s, int row, int lane) {
-    return ring + ((((warp * D + s) * 2 + row) * 32 + lane) * LB);
-  }
-  template <typename F>
-  __device__ __forceinline__ static void each(unsigned char* ring, const unsigned char* rt, const unsigned char* rd,
-                                              bool both, int c_lo, int c_hi, int V, int vec, F&& f) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int mine = c_lo + warp < c_hi ? (c_hi - c_lo - warp + kTreeWarps - 1) / kTreeWarps : 0;
-    auto issue = [&](int i) {
-      const int c = c_lo + warp + i * kTreeWarps;
-      const int e0 = c * kChunkElems + lane * 8;
-      if (i < mine && vec && e0 + 8 <= V) {
-        const int sl = i % D;
-#pragma unroll
-        for (int w = 0; w < LB / 16; ++w) {
-          cp_async16(slot(ring, warp, sl, 0, lane) + 16 * w, rt + static_cast<size_t>(e0) * ELT + 16 * w);
-          if (both) cp_async16(slot(ring, warp, sl, 1, lane) + 16 * w, rd + static_cast<size_t>(e0) * ELT + 16 * w);
-        }
-      }
-      cp_async_commit();
-    };
-#pragma unroll
-    for (int i = 0; i < D; ++i) issue(i);
-    for (int i = 0; i < mine; ++i) {
-      cp_async_wait<D - 1>();                      // chunk i has landed
-      const int c = c_lo + warp + i * kTreeWarps;
-      const int e0 = c * kChunkElems + lane * 8;
-      float zt[8], zd[8];
-      if (vec && e0 + 8 <= V) {
-        const int sl = i % D;
-        unpack(slot(ring, warp, sl, 0, lane), zt);
-        if (both) unpack(slot(ring, warp, sl, 1, lane), zd);
-      } else {
-        Rows<ELT>::load8(rt, e0, V, 0, zt);
-        if (both) Rows<ELT>::load8(rd, e0, V, 0, zd);
-      }
-      f(c, e0, zt, zd);
-      issue(i + D);
-    }
-    cp_async_wait<0>();
-  }
-  __device__ __forceinline__ static void unpack(const unsigned char* p, float (&v)[8]) {
-    if (ELT == 2) {
-      Vec<2>::unpack(*reinterpret_cast<const uint4*>(p), v);
-    } else {
-      const uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
-      v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
-      v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
-    }
-  }
-};
 
 // What a CTA contributes to one exchange of its cluster (three 16-byte
 // words, read by a peer with three vector loads).
@@ -172,13 +97,17 @@ struct __align__(16) XSlot {
 
 // Per-CTA scratch for the walk.
 struct TreeShared {
+  uint64_t full[kTreeStages];        // slot filled (producer -> consumer warps)
+  uint64_t empty[kTreeStages];       // slot released (one arrival per consumer warp)
   int par[kTreeMaxNodes], tok[kTreeMaxNodes];
   float u[kTreeMaxNodes];
   int kids[kTreeMaxNodes];
   int nkids, n, cur, len, st, next, y, owner;
-  float csum[kTreeMaxChunks];        // chunk sums of the last weight pass (this CTA's chunks)
+  int pass_both;                     // the pass streams the draft row too
+  int failed;                        // a bounded wait of the streaming gave up
+  float csum[kTreeMaxSegs];          // segment sums of the last weight pass (this CTA's segments)
   double cc, PP, invPP;              // residual after the rejections so far: max(0, p - cc q) / PP
-  double invSt, invSd;               // 1 / S^t, 1 / S^d of the current node
+  double l2ratio;                    // log2(S^t / S^d) of the current node
   float wA, wGh, wGl;                // weights of the last pass: max(0, A 2^(z^t c - K^t) - B 2^(z^d c - K^d)),
                                      // as A 2^(z^t c - K^t) (1 - 2^delta), delta = (z^d - z^t) c + Gh + Gl
   float wm[kTreeWarps], ws[kTreeWarps], wmd[kTreeWarps], wsd[kTreeWarps];
@@ -220,24 +149,6 @@ __device__ __forceinline__ void exchange(TreeShared& sh, int& xp, int cs) {
   xp ^= 1;
 }
 
-// Running (max, sum 2^(z c - fl(max c))) of one lane, updated by 8 logits.
-__device__ __forceinline__ void online8(const float (&z)[8], float c2, float& m, float& K, float& s, int& bad) {
-  float vm = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) vm = fmax_nan(vm, z[j]);     // NaN survives the maximum
-  bad |= (vm != vm) || (vm == INFINITY);
-  if (vm > m) {
-    const float Kn = vm * c2;
-    s = (m == -INFINITY) ? 0.f : s * fast_exp2(K - Kn);
-    m = vm;
-    K = Kn;
-  }
-  if (m != -INFINITY) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s += fast_exp2(fmaf(z[j], c2, -K));
-  }
-}
-
 // Merge of (K, S) pairs, S = sum 2^(z c - K), K = fl(max z * c): the larger
 // K wins and the other sum is rescaled.  (-inf, 0) is the empty pair.
 __device__ __forceinline__ void merge_ks(float& K, float& S, float K2, float S2) {
@@ -255,7 +166,8 @@ __device__ __forceinline__ void merge_ks(float& K, float& S, float K2, float S2)
   }
 }
 
-// CTA-wide (K, S) of the lanes' running pairs, in warp order (thread 0).
+// CTA-wide (K, S) of the consumer lanes' running (max, K, sum) triples, in
+// warp order (thread 0).  Every thread of the CTA calls it.
 __device__ void combine_stats(float m, float K, float s, float& Kout, float& Sout, float* wm, float* ws, float c2) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float M = m;
@@ -264,7 +176,7 @@ __device__ void combine_stats(float m, float K, float s, float& Kout, float& Sou
   const float KM = M * c2;
   float v = (m == -INFINITY) ? 0.f : s * fast_exp2(K - KM);
   v = warp_sum(v);
-  if (lane == 0) {
+  if (lane == 0 && warp < kTreeWarps) {
     wm[warp] = M;
     ws[warp] = v;
   }
@@ -299,17 +211,23 @@ __device__ __forceinline__ float pair_weight(float zt, float zd, float c2, float
   const float delta = __fadd_rn(__fmaf_rn(__fsub_rn(zd, zt), c2, Gh), Gl);
   return fmaxf(__fmul_rn(__fmul_rn(A, et), one_minus_exp2(delta)), 0.f);
 }
+// The same for two logit pairs at once (bit-identical, lane by lane).
+__device__ __forceinline__ void pair_weight2(f2 zt, f2 zd, f2 cc, f2 nkt, f2 aa, f2 gh, f2 gl, float& w0, float& w1) {
+  const f2 et = exp2_2(fma2(zt, cc, nkt));
+  const f2 delta = add2(fma2(sub2(zd, zt), cc, gh), gl);
+  unpack2(mul2(mul2(aa, et), one_minus_exp2_2r(delta)), w0, w1);
+  w0 = fmaxf(w0, 0.f);
+  w1 = fmaxf(w1, 0.f);
+}
 // The bonus weight: no draft row (K^d may be -inf at a node without children).
 __device__ __forceinline__ float bonus_weight(float zt, float c2, float Kt) { return fast_exp2(fmaf(zt, c2, -Kt)); }
 
-// Fixed-order fp64 total of the chunk sums of [c_lo, c_hi): lane l adds a
-// contiguous run of chunks in order, then the lanes are scanned.
-__device__ __forceinline__ double chunk_total(const TreeShared& sh, int c_lo, int c_hi, int lane, double& excl,
-                                             int& lo, int& hi) {
-  const int n = c_hi - c_lo;
-  const int per = (n + 31) / 32;
-  lo = c_lo + min(lane * per, n);
-  hi = min(lo + per, c_hi);
+// Fixed-order fp64 total of the segment sums [0, nseg): lane l adds a
+// contiguous run of segments in order, then the lanes are scanned.
+__device__ __forceinline__ double seg_total(const TreeShared& sh, int nseg, int lane, double& excl, int& lo, int& hi) {
+  const int per = (nseg + 31) / 32;
+  lo = min(lane * per, nseg);
+  hi = min(lo + per, nseg);
   double part = 0.0;
   for (int c = lo; c < hi; ++c) part += static_cast<double>(sh.csum[c]);
   const double incl = warp_incl_scan(part, lane);
@@ -317,47 +235,194 @@ __device__ __forceinline__ double chunk_total(const TreeShared& sh, int c_lo, in
   return __shfl_sync(0xffffffffu, incl, 31);
 }
 
+// This CTA's slice of every row, streamed through the slots.  The producer
+// warp and the consumer warps run the same passes in the same order and count
+// the slots alike (q), so the slots' mbarrier phases match.  Every wait is
+// bounded; one that gives up sets sh.failed, after which no wait is made and
+// the walk ends with SV_ERR_TIMEOUT.
+template <int ELT>
+struct Slice {
+  using VV = Vec<ELT>;
+  static constexpr int NV = VV::N;
+  static constexpr int kSegElems = kTreeVecsPerWarp * NV;   // logits per segment (one warp's share of a slot)
+  static constexpr int kSlotElems = kTreeHalf / ELT;        // logits of one row per slot
+
+  TreeShared& sh;
+  unsigned char* ring;
+  const TreeParams& P;
+  int e_lo;        // first logit of the slice
+  int bytes;       // bytes of one row's slice
+  int nsl;         // slots per pass
+  int q;           // slots streamed so far
+
+  __device__ Slice(TreeShared& s, unsigned char* r, const TreeParams& p, int c_lo, int c_hi)
+      : sh(s), ring(r), P(p), q(0) {
+    e_lo = min(p.V, c_lo * kChunkElems);
+    const int e_hi = min(p.V, c_hi * kChunkElems);
+    bytes = (e_hi - e_lo) * ELT;
+    nsl = (bytes + kTreeHalf - 1) / kTreeHalf;
+  }
+
+  __device__ int nseg() const { return nsl * kTreeWarps; }
+  __device__ int slot_bytes(int k) const {
+    const int left = bytes - k * kTreeHalf;
+    return left < kTreeHalf ? left : kTreeHalf;
+  }
+  __device__ unsigned char* slot(int s) const { return ring + static_cast<size_t>(s) * 2 * kTreeHalf; }
+  __device__ bool failed() const { return *reinterpret_cast<volatile int*>(&sh.failed) != 0; }
+  __device__ void fail() { *reinterpret_cast<volatile int*>(&sh.failed) = 1; }
+  // first logit of segment g (slot g / 16, warp g % 16)
+  __device__ int seg_e0(int g) const { return e_lo + (g / kTreeWarps) * kSlotElems + (g % kTreeWarps) * kSegElems; }
+
+  // Producer warp: the pass's rows, one slot at a time.
+  __device__ void produce(const unsigned char* rt, const unsigned char* rd, bool both) {
+    const int lane = threadIdx.x & 31;
+    for (int k = 0; k < nsl; ++k, ++q) {
+      const int s = q % kTreeStages;
+      int ok = 1;
+      if (lane == 0) ok = (!failed() && mbar_wait_bounded(&sh.empty[s], ((q / kTreeStages) & 1) ^ 1, kDrainLimitNs)) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) fail();
+        continue;
+      }
+      const int nb = slot_bytes(k);
+      const size_t off = static_cast<size_t>(e_lo) * ELT + static_cast<size_t>(k) * kTreeHalf;
+      unsigned char* dst = slot(s);
+      if (P.vec) {
+        if (lane == 0) {
+          mbar_expect_tx(&sh.full[s], static_cast<uint32_t>((both ? 2 : 1) * nb));
+          bulk_load(dst, rt + off, static_cast<uint32_t>(nb), &sh.full[s]);
+          if (both) bulk_load(dst + kTreeHalf, rd + off, static_cast<uint32_t>(nb), &sh.full[s]);
+        }
+      } else {
+        // rows not 16-byte aligned: element loads, the last vector padded with -inf
+        const int e0 = e_lo + k * kSlotElems;
+        const int n = nb / ELT;
+        const int npad = (n + NV - 1) / NV * NV;
+        for (int e = lane; e < npad; e += 32) {
+          VV::store_scalar(dst, e, e < n ? VV::scalar(rt, e0 + e) : -INFINITY);
+          if (both) VV::store_scalar(dst + kTreeHalf, e, e < n ? VV::scalar(rd, e0 + e) : -INFINITY);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.full[s]);
+      }
+    }
+  }
+
+  // Consumer warps: f(k, tv, dv) for each slot k with this lane's vectors of
+  // the target (and draft) row, -inf past the slice; a slot is released as
+  // soon as its vectors are in registers.
+  template <typename F>
+  __device__ void consume(bool both, F&& f) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int k = 0; k < nsl; ++k, ++q) {
+      const int s = q % kTreeStages;
+      bool ok = !failed() && mbar_wait_bounded(&sh.full[s], static_cast<uint32_t>(q / kTreeStages) & 1u, kDrainLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) fail();
+      const int nvec = (slot_bytes(k) + 15) / 16;
+      const unsigned char* src = slot(s);
+      uint4 tv[kTreeVecsPerLane], dv[kTreeVecsPerLane];
+#pragma unroll
+      for (int j = 0; j < kTreeVecsPerLane; ++j) {
+        const int v = warp * kTreeVecsPerWarp + j * 32 + lane;
+        const bool in = v < nvec;
+        tv[j] = in ? *reinterpret_cast<const uint4*>(src + static_cast<size_t>(v) * 16) : VV::neg_inf();
+        dv[j] = (in && both) ? *reinterpret_cast<const uint4*>(src + kTreeHalf + static_cast<size_t>(v) * 16)
+                             : VV::neg_inf();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[s]);
+      f(k, tv, dv);
+    }
+  }
+
+  // One pass: the producer warp streams, the consumer warps reduce.
+  template <typename F>
+  __device__ void pass(const unsigned char* rt, const unsigned char* rd, bool both, F&& f) {
+    if ((threadIdx.x >> 5) == kTreeProducer) produce(rt, rd, both);
+    else consume(both, f);
+  }
+};
+
+// Running (max, K = fl(max c), sum 2^(z c - K)) of one lane, updated by its
+// vectors of one slot (a larger maximum rescales the sum).
+template <int ELT>
+__device__ __forceinline__ void online_vecs(const uint4 (&v)[kTreeVecsPerLane], float c2, float& m, float& K, f2& s,
+                                            int& bad) {
+  using VV = Vec<ELT>;
+  const float vm = VV::vmax_nan(v);                  // NaN survives the maximum
+  bad |= (vm != vm) || (vm == INFINITY);
+  if (vm > m) {
+    const float Kn = vm * c2;
+    const float f = (m == -INFINITY) ? 0.f : fast_exp2(K - Kn);
+    s = mul2(s, pack2(f, f));
+    m = vm;
+    K = Kn;
+  }
+  if (m != -INFINITY) {
+    const f2 cc = pack2(c2, c2), nk = pack2(-K, -K);
+#pragma unroll
+    for (int j = 0; j < kTreeVecsPerLane; ++j) {
+      f2 z[VV::N / 2];
+      VV::pairs(v[j], z);
+#pragma unroll
+      for (int i = 0; i < VV::N / 2; ++i) s = add2(s, exp2_2(fma2(z[i], cc, nk)));
+    }
+  }
+}
+
 // One pass of weights over this CTA's slice of the current node's rows:
-// chunk sums into sh.csum, then the slices' weights exchanged in the
+// segment sums into sh.csum, then the slices' weights exchanged in the
 // cluster (sh.slice, sh.base, sh.total, identical in every CTA).
 //   mode 0: bonus weights (A = 1, B = 0; the draft row is not read);
 //   mode 1: the residual after one more rejection;
 //   mode 2: the current residual r itself (zero-residual fallback).
 template <int ELT>
-__device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParams& P, const unsigned char* rt,
-                            const unsigned char* rd, int mode, int c_lo, int c_hi, int& xp) {
+__device__ void weight_pass(TreeShared& sh, Slice<ELT>& sl, const TreeParams& P, const unsigned char* rt,
+                            const unsigned char* rd, int mode, int& xp) {
+  using VV = Vec<ELT>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    sh.wA = mode == 0 ? 1.f : static_cast<float>(sh.invPP * sh.invSt);
+    sh.wA = mode == 0 ? 1.f : static_cast<float>(sh.invPP * (1.0 / static_cast<double>(sh.St)));
     sh.wGh = -INFINITY;
     sh.wGl = 0.f;
-    const double BA = (mode == 1 ? sh.cc + sh.PP : sh.cc) * (static_cast<double>(sh.St) / static_cast<double>(sh.Sd));
-    if (mode != 0 && BA > 0.0) {
-      const double G = log2(BA) + (static_cast<double>(sh.Kt) - static_cast<double>(sh.Kd));
+    const double cB = mode == 1 ? sh.cc + sh.PP : sh.cc;
+    if (mode != 0 && cB > 0.0) {
+      // log2(B / A) = log2(c_B) + log2(S^t / S^d)
+      const double G = log2(cB) + sh.l2ratio + (static_cast<double>(sh.Kt) - static_cast<double>(sh.Kd));
       sh.wGh = static_cast<float>(G);
       sh.wGl = static_cast<float>(G - static_cast<double>(sh.wGh));
     }
   }
   __syncthreads();
-  const float c2 = P.c2, Kt = sh.Kt, A = sh.wA, Gh = sh.wGh, Gl = sh.wGl;
-  Chunks<ELT>::each(ring, rt, rd, mode != 0, c_lo, c_hi, P.V, P.vec,
-                    [&](int c, int, const float (&zt)[8], const float (&zd)[8]) {
+  const float c2 = P.c2;
+  const f2 cc = pack2(c2, c2), nkt = pack2(-sh.Kt, -sh.Kt), aa = pack2(sh.wA, sh.wA);
+  const f2 gh = pack2(sh.wGh, sh.wGh), gl = pack2(sh.wGl, sh.wGl);
+  sl.pass(rt, rd, mode != 0, [&](int k, const uint4 (&tv)[kTreeVecsPerLane], const uint4 (&dv)[kTreeVecsPerLane]) {
     float part = 0.f;
-    if (mode == 0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) part += bonus_weight(zt[j], c2, Kt);
-    } else {
+    for (int j = 0; j < kTreeVecsPerLane; ++j) {
+      f2 zt[VV::N / 2], zd[VV::N / 2];
+      VV::pairs(tv[j], zt);
+      if (mode != 0) VV::pairs(dv[j], zd);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) part += pair_weight(zt[j], zd[j], c2, Kt, A, Gh, Gl);
+      for (int i = 0; i < VV::N / 2; ++i) {
+        float w0, w1;
+        if (mode == 0) unpack2(exp2_2(fma2(zt[i], cc, nkt)), w0, w1);
+        else pair_weight2(zt[i], zd[i], cc, nkt, aa, gh, gl, w0, w1);
+        part += w0;
+        part += w1;
+      }
     }
     part = warp_sum(part);
-    if (lane == 0) sh.csum[c] = part;
+    if (lane == 0) sh.csum[k * kTreeWarps + warp] = part;
   });
   __syncthreads();
   if (warp == 0) {
     double excl;
     int lo, hi;
-    const double tot = chunk_total(sh, c_lo, c_hi, lane, excl, lo, hi);
+    const double tot = seg_total(sh, sl.nseg(), lane, excl, lo, hi);
     if (lane == 0) {
       sh.mytotal = tot;
       sh.xs[xp].total = tot;
@@ -379,21 +444,26 @@ __device__ void weight_pass(TreeShared& sh, unsigned char* ring, const TreeParam
 }
 
 // Inverse CDF with the sampling uniform over the weights of the last pass,
-// for the CTA whose slice holds the point (warp 0): the chunk from the chunk
-// sums, then the logit from the chunk's recomputed weights.  `last`: the
-// point lies past every weight (rounding); take the last logit with weight.
+// for the CTA whose slice holds the point (warp 0): the segment from the
+// segment sums, then the logit from the segment's recomputed weights, in
+// index order.  `last`: the point lies past every weight (rounding); take
+// the last logit with weight.
 template <int ELT>
-__device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt, const unsigned char* rd, int mode,
-                    int c_lo, int c_hi, double t, double slice_base, bool last) {
+__device__ int draw(TreeShared& sh, const Slice<ELT>& sl, const TreeParams& P, const unsigned char* rt,
+                    const unsigned char* rd, int mode, double t, double slice_base, bool last) {
+  using VV = Vec<ELT>;
+  constexpr int NV = VV::N;
   const int lane = threadIdx.x & 31;
   const int V = P.V;
+  const int e_end = sl.e_lo + sl.bytes / ELT;   // end of this CTA's slice
+  const int nseg = sl.nseg();
   double excl;
   int lo, hi;
-  chunk_total(sh, c_lo, c_hi, lane, excl, lo, hi);
+  seg_total(sh, nseg, lane, excl, lo, hi);
   excl += slice_base;
   double part = 0.0;
   for (int c = lo; c < hi; ++c) part += static_cast<double>(sh.csum[c]);
-  int chunk = -1;
+  int seg = -1;
   double base = 0.0;
   const unsigned in = last ? 0u : __ballot_sync(0xffffffffu, part > 0.0 && excl <= t && t < excl + part);
   if (in) {
@@ -403,60 +473,69 @@ __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt
       for (int c = lo; c < hi; ++c) {
         const double nx = acc + static_cast<double>(sh.csum[c]);
         if (t < nx && sh.csum[c] > 0.f) {
-          chunk = c;
+          seg = c;
           base = acc;
           break;
         }
         acc = nx;
       }
     }
-    chunk = __shfl_sync(0xffffffffu, chunk, l);
+    seg = __shfl_sync(0xffffffffu, seg, l);
     base = __shfl_sync(0xffffffffu, base, l);
   }
-  if (chunk < 0) {
-    // past the weights: the last chunk with weight
+  if (seg < 0) {
+    // past the weights: the last segment with weight
     int lastc = -1;
     for (int c = lo; c < hi; ++c)
       if (sh.csum[c] > 0.f) lastc = c;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lastc = max(lastc, __shfl_xor_sync(0xffffffffu, lastc, o));
-    chunk = lastc;
+    seg = lastc;
     base = -1.0;
   }
-  if (chunk < 0) return -1;
-  const int e0 = chunk * kChunkElems + lane * 8;
-  float zt[8], zd[8], w[8];
-  Rows<ELT>::load8(rt, e0, V, P.vec, zt);
-  if (mode != 0) Rows<ELT>::load8(rd, e0, V, P.vec, zd);
-  float wpart = 0.f;
-  int lastw = -1;
+  if (seg < 0) return -1;
+  const int e0 = sl.seg_e0(seg);
+  int y = -1, lastw = -1;
+  double run = base;
+  for (int j = 0; j < kTreeVecsPerLane && y < 0; ++j) {
+    const int ev = e0 + (j * 32 + lane) * NV;
+    float zt[NV], zd[NV], w[NV];
+    VV::unpack(load_vec<ELT>(rt, ev, V, P.vec), zt);
+    if (mode != 0) VV::unpack(load_vec<ELT>(rd, ev, V, P.vec), zd);
+    float wl = 0.f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    w[j] = mode == 0 ? bonus_weight(zt[j], P.c2, sh.Kt)
-                     : pair_weight(zt[j], zd[j], P.c2, sh.Kt, sh.wA, sh.wGh, sh.wGl);
-    wpart += w[j];
-    if (w[j] > 0.f) lastw = e0 + j;
-  }
-  int y = -1;
-  if (base >= 0.0) {
-    const double incl = warp_incl_scan(static_cast<double>(wpart), lane);
-    const double start = base + (incl - static_cast<double>(wpart));
-    const unsigned hit = __ballot_sync(0xffffffffu, wpart > 0.f && start <= t && t < base + incl);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      if (lane == l) {
-        double acc = start;
-        for (int j = 0; j < 8; ++j) {
-          acc += static_cast<double>(w[j]);
-          if (t < acc && w[j] > 0.f) {
-            y = e0 + j;
-            break;
-          }
-        }
-        if (y < 0) y = lastw;
-      }
-      y = __shfl_sync(0xffffffffu, y, l);
+    for (int e = 0; e < NV; ++e) {
+      const bool mine = ev + e < e_end;   // logits past the slice are the next CTA's
+      w[e] = !mine ? 0.f
+                   : (mode == 0 ? bonus_weight(zt[e], P.c2, sh.Kt)
+                                : pair_weight(zt[e], zd[e], P.c2, sh.Kt, sh.wA, sh.wGh, sh.wGl));
+      wl += w[e];
+      if (w[e] > 0.f) lastw = max(lastw, ev + e);
     }
+    const double incl = warp_incl_scan(static_cast<double>(wl), lane);
+    if (base >= 0.0) {
+      const double start = run + (incl - static_cast<double>(wl));
+      const unsigned hit = __ballot_sync(0xffffffffu, wl > 0.f && start <= t && t < run + incl);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        int pick = -1;
+        if (lane == l) {
+          double acc = start;
+          int lastp = -1;
+          for (int e = 0; e < NV; ++e) {
+            if (w[e] > 0.f) lastp = ev + e;
+            acc += static_cast<double>(w[e]);
+            if (t < acc && w[e] > 0.f) {
+              pick = ev + e;
+              break;
+            }
+          }
+          if (pick < 0) pick = lastp;
+        }
+        y = __shfl_sync(0xffffffffu, pick, l);
+      }
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
   }
   if (y < 0) {
 #pragma unroll
@@ -469,7 +548,9 @@ __device__ int draw(TreeShared& sh, const TreeParams& P, const unsigned char* rt
 template <int ELT, bool GREEDY>
 __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams P) {
   __shared__ TreeShared sh;
-  extern __shared__ __align__(16) unsigned char ring[];   // Chunks<ELT>::kRingBytes
+  extern __shared__ __align__(128) unsigned char ring[];   // kTreeRingBytes
+  using VV = Vec<ELT>;
+  constexpr int NV = VV::N;
   const int cs = P.cs;
   const int rank = cluster_rank();
   const int b = blockIdx.x / cs;
@@ -483,7 +564,16 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
   const size_t rb = static_cast<size_t>(b) * M;
   const bool lead = rank == 0;        // the CTA that writes the outputs
   int xp = 0;
+  Slice<ELT> sl(sh, ring, P, c_lo, c_hi);
 
+  if (tid == 0) {
+    for (int s = 0; s < kTreeStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kTreeWarps);
+    }
+    fence_mbar_init();
+    sh.failed = 0;
+  }
   for (int j = tid; j < M; j += kTreeThreads) {
     sh.par[j] = P.parents[rb + j];
     sh.tok[j] = P.tokens[rb + j];
@@ -514,7 +604,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
   // sh.st: 0 walking, > 0 an error, -1 done.  Every decision below is taken
   // from values that are the same in every CTA of the cluster (the inputs,
   // or exchanged and combined in rank order), so the CTAs walk in lockstep
-  // and meet at every cluster barrier.
+  // and meet at every cluster barrier.  The producer warp follows the walk
+  // too, and streams during the passes.
   while (sh.st == 0) {
     const int cur = sh.cur;
     if (tid == 0) {
@@ -532,21 +623,27 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       // first argmax of the target row; both rows checked
       float best = -INFINITY, dmax = -INFINITY;
       int bi = 0x7fffffff, bad = 0;
-      Chunks<ELT>::each(ring, rt, rd, nk > 0, c_lo, c_hi, V, P.vec,
-                        [&](int, int e0, const float (&z)[8], const float (&zd)[8]) {
+      sl.pass(rt, rd, nk > 0, [&](int k, const uint4 (&tv)[kTreeVecsPerLane], const uint4 (&dv)[kTreeVecsPerLane]) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          bad |= (z[j] != z[j]) || (z[j] == INFINITY);
-          if (e0 + j < V && z[j] > best) {
-            best = z[j];
-            bi = e0 + j;
+        for (int j = 0; j < kTreeVecsPerLane; ++j) {
+          const int e0 = sl.e_lo + k * Slice<ELT>::kSlotElems + (warp * kTreeVecsPerWarp + j * 32 + lane) * NV;
+          float z[NV];
+          VV::unpack(tv[j], z);
+#pragma unroll
+          for (int e = 0; e < NV; ++e) {
+            bad |= (z[e] != z[e]) || (z[e] == INFINITY);
+            if (z[e] > best) {        // padding is -inf: only logits of the slice win
+              best = z[e];
+              bi = e0 + e;
+            }
           }
-        }
-        if (nk > 0) {
+          if (nk > 0) {
+            VV::unpack(dv[j], z);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            bad |= (zd[j] != zd[j]) || (zd[j] == INFINITY);
-            dmax = fmaxf(dmax, zd[j]);
+            for (int e = 0; e < NV; ++e) {
+              bad |= (z[e] != z[e]) || (z[e] == INFINITY);
+              dmax = fmaxf(dmax, z[e]);
+            }
           }
         }
       });
@@ -554,7 +651,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       bad = warp_or(bad);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
-      if (lane == 0) {
+      if (lane == 0 && warp < kTreeWarps) {
         sh.wm[warp] = best;
         sh.widx[warp] = bi;
         sh.wbad[warp] = bad;
@@ -591,7 +688,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
             bx = x.idx;
           }
         }
-        if (anybad || bv == -INFINITY || (nk > 0 && dm == -INFINITY)) {
+        if (sh.failed) {
+          sh.st = SV_ERR_TIMEOUT;
+        } else if (anybad || bv == -INFINITY || (nk > 0 && dm == -INFINITY)) {
           sh.st = SV_ERR_NONFINITE;
         } else {
           int next = -1;
@@ -622,15 +721,20 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     // and, for a node with children, of the draft row; then the slices'
     // pairs are merged in rank order
     {
-      float mt = -INFINITY, Kt = 0.f, st = 0.f, md = -INFINITY, Kd = 0.f, sd = 0.f;
+      float mt = -INFINITY, Kt = 0.f, md = -INFINITY, Kd = 0.f;
+      f2 st2 = 0ull, sd2 = 0ull;
       int bad = 0;
-      Chunks<ELT>::each(ring, rt, rd, nk > 0, c_lo, c_hi, V, P.vec,
-                        [&](int, int, const float (&z)[8], const float (&zd)[8]) {
-        online8(z, c2, mt, Kt, st, bad);
-        if (nk > 0) online8(zd, c2, md, Kd, sd, bad);
+      sl.pass(rt, rd, nk > 0, [&](int, const uint4 (&tv)[kTreeVecsPerLane], const uint4 (&dv)[kTreeVecsPerLane]) {
+        online_vecs<ELT>(tv, c2, mt, Kt, st2, bad);
+        if (nk > 0) online_vecs<ELT>(dv, c2, md, Kd, sd2, bad);
       });
+      float x0, x1;
+      unpack2(st2, x0, x1);
+      const float st = x0 + x1;
+      unpack2(sd2, x0, x1);
+      const float sd = x0 + x1;
       bad = warp_or(bad);
-      if (lane == 0) sh.wbad[warp] = bad;
+      if (lane == 0 && warp < kTreeWarps) sh.wbad[warp] = bad;
       combine_stats(mt, Kt, st, sh.myKt, sh.mySt, sh.wm, sh.ws, c2);
       if (nk > 0) combine_stats(md, Kd, sd, sh.myKd, sh.mySd, sh.wmd, sh.wsd, c2);
       __syncthreads();
@@ -658,9 +762,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         sh.St = S1;
         sh.Kd = K2;
         sh.Sd = S2;
-        if (anybad || !(S1 > 0.f) || (nk > 0 && !(S2 > 0.f))) sh.st = SV_ERR_NONFINITE;
-        sh.invSt = 1.0 / static_cast<double>(S1);
-        sh.invSd = nk > 0 ? 1.0 / static_cast<double>(S2) : 0.0;
+        if (sh.failed) sh.st = SV_ERR_TIMEOUT;
+        else if (anybad || !(S1 > 0.f) || (nk > 0 && !(S2 > 0.f))) sh.st = SV_ERR_NONFINITE;
+        // log2(S^t / S^d), once per node (every child's test and residual uses
+        // it); in fp32, which loses nothing against the fp32 sums S
+        sh.l2ratio = nk > 0 ? static_cast<double>(log2f(__fdiv_rn(S1, S2))) : 0.0;
         sh.cc = 0.0;
         sh.PP = 1.0;
         sh.invPP = 1.0;
@@ -675,7 +781,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       if (tid == 0) {
         const int c = sh.kids[i];
         const long long x = sh.tok[c];
-        const float zt = Vec<ELT>::scalar(rt, x), zd = Vec<ELT>::scalar(rd, x);
+        const float zt = VV::scalar(rt, x), zd = VV::scalar(rd, x);
         // r(x) / q(x) = max(0, p(x)/q(x) - c) / P, with p(x)/q(x) from its
         // logarithm in double: (z^t - z^d) c - (K^t - K^d) - log2(S^t / S^d)
         double rq;
@@ -683,8 +789,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         else if (zt == -INFINITY) rq = 0.0;                            // p(x) = 0
         else {
           const double l2 = (static_cast<double>(zt) - static_cast<double>(zd)) * static_cast<double>(c2) -
-                            (static_cast<double>(sh.Kt) - static_cast<double>(sh.Kd)) -
-                            log2(static_cast<double>(sh.St) / static_cast<double>(sh.Sd));
+                            (static_cast<double>(sh.Kt) - static_cast<double>(sh.Kd)) - sh.l2ratio;
           rq = fmax(exp2(l2) - sh.cc, 0.0) * sh.invPP;
         }
         const double al = fmin(1.0, rq);
@@ -697,12 +802,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         accepted = sh.next;
         break;
       }
-      // rejected: the residual after this rejection, its mass and chunk sums
+      // rejected: the residual after this rejection, its mass and segment sums
       last_mode = 1;
-      weight_pass<ELT>(sh, ring, P, rt, rd, 1, c_lo, c_hi, xp);
+      weight_pass<ELT>(sh, sl, P, rt, rd, 1, xp);
       if (!(sh.total > 0.0)) {
         last_mode = 2;                       // zero residual: keep r
-        weight_pass<ELT>(sh, ring, P, rt, rd, 2, c_lo, c_hi, xp);
+        weight_pass<ELT>(sh, sl, P, rt, rd, 2, xp);
       }
       if (tid == 0) {
         // S = sh.total is the mass of max(0, r - q) (or of r); the new
@@ -727,10 +832,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     }
 
     // --- the draw: the bonus weights at a node without children, else the
-    // last residual (whose chunk sums the last pass left in sh.csum).  The
+    // last residual (whose segment sums the last pass left in sh.csum).  The
     // CTA whose slice holds s * S draws; the token is then exchanged.
     const int wmode = nk == 0 ? 0 : last_mode;
-    if (nk == 0) weight_pass<ELT>(sh, ring, P, rt, rd, 0, c_lo, c_hi, xp);
+    if (nk == 0) weight_pass<ELT>(sh, sl, P, rt, rd, 0, xp);
     if (tid == 0) {
       const double t = static_cast<double>(sh.u[0]) * sh.total;
       int owner = -1, lastw = -1;
@@ -746,14 +851,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     __syncthreads();
     int y = -1;
     if (rank == sh.owner && warp == 0)
-      y = draw<ELT>(sh, P, rt, rd, wmode, c_lo, c_hi, static_cast<double>(sh.u[0]) * sh.total, sh.base[rank],
-                    sh.next == 1);
+      y = draw<ELT>(sh, sl, P, rt, rd, wmode, static_cast<double>(sh.u[0]) * sh.total, sh.base[rank], sh.next == 1);
     if (tid == 0) sh.xs[xp].y = y;
     __syncthreads();
     exchange(sh, xp, cs);
     if (tid == 0) {
       sh.y = sh.owner >= 0 ? sh.got[sh.owner].y : -1;
-      sh.st = -1;
+      sh.st = sh.failed ? SV_ERR_TIMEOUT : -1;
     }
     __syncthreads();
   }
@@ -786,7 +890,7 @@ extern "C" sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtyp
                                       const int32_t* n_nodes, const float* uniforms, float temperature,
                                       int32_t* out_tokens, int32_t* out_nodes, int32_t* out_len, int32_t* status,
                                       float* alpha, sv_stream_t stream) {
-  if (B < 0 || max_nodes < 1 || max_nodes > sv::kTreeMaxNodes || V < 1 || V > sv::kTreeMaxChunks * sv::kChunkElems)
+  if (B < 0 || max_nodes < 1 || max_nodes > sv::kTreeMaxNodes || V < 1 || V > sv::kTreeMaxV)
     return SV_ERR_INVALID_ARG;
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
   if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
@@ -820,8 +924,8 @@ extern "C" sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtyp
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   void (*kern)(const sv::TreeParams) = elt == 2 ? (greedy ? sv::tree_kernel<2, true> : sv::tree_kernel<2, false>)
                                                 : (greedy ? sv::tree_kernel<4, true> : sv::tree_kernel<4, false>);
-  const int ring = elt == 2 ? sv::Chunks<2>::kRingBytes : sv::Chunks<4>::kRingBytes;
-  // Once per device and kernel: the ring needs more than the default 48 KB
+  const int ring = sv::kTreeRingBytes;
+  // Once per device and kernel: the slots need more than the default 48 KB
   // of dynamic shared memory, and the cluster sizes that can be resident
   // with it (clusters of 1, 2, 4, 8 CTAs) are recorded.
   struct DevInfo {
