@@ -76,7 +76,7 @@ def parse():
                     help="timed rounds of the draft-length controller (0 = skip)")
     ap.add_argument("--profile-kernels", default="",
                     help="run each named kernel's representative case twice (for ncu, one kernel per "
-                         "capture): comma list of verify, pieces, early_exit, compact, debug, kd, tree, ctrl")
+                         "capture): comma list of verify, verify_dense, pieces, early_exit, compact, debug, kd, tree, ctrl")
     return ap.parse_args()
 
 
@@ -533,7 +533,7 @@ def time_kd(svp, device, stream, steps, warmup, n_seq=64, t_len=64, V=151936):
     out = {"workload": f"kd: {n_seq} rollouts x {t_len} positions, V={V} bf16, T=1",
            "kernel": "kd_kernel", "rows_per_call": rows}
     cs, nb, ctas = svp.kd_launch_shape(V, torch.bfloat16, True)
-    out["launch"] = {"cluster": cs, "row_buffers": nb, "grid_ctas": ctas}
+    out["launch"] = {"ctas_per_row": cs, "staging_slots": nb, "grid_ctas": ctas}
     for name, gp in (("with_grad", grad.data_ptr()), ("loss_only", None)):
         def call(i):
             t, d, w = sets[i % 2]
@@ -805,10 +805,16 @@ def profile_kernels(args):
     ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
     run = lambda v, i: v.verify(i["target"], i["draft"], i["tokens"], i["draft_len"], i["uniforms"], i["T"])
     ot, ol = run(ver, inp)
+    extra = {}
     for name in names:
         for _ in range(2):
             if name == "verify":
                 ot, ol = run(ver, inp)
+            elif name == "verify_dense":
+                if "dense" not in extra:
+                    dw = get_workload("ragged_dense")
+                    extra["dense"] = (svp.SpecVerifier(dw.B, dw.k, dw.V, dw.torch_dtype), make_inputs(dw, device=device))
+                run(*extra["dense"])
             elif name == "pieces":
                 pv = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
                 pv.set_kernel(svp.SV_KERNEL_PIECES)
