@@ -40,7 +40,17 @@ METRIC = "spec_verify verified positions/s and HBM GB/s (fraction of ~8 TB/s), 1
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-KERNEL_NAME = "verify_kernel"
+# the schedules of a verify call: the launches per call, the sources they are
+# compiled from, and the name of their ncu summaries under profiles/
+SCHEDULES = {
+    "cluster": {"launches": 2, "name": "verify_kernel",
+                "sources": ("sv_device.cuh", "sv_internal.h", "sv_kernels.cu"),
+                "kernels": "plan_kernel + verify_kernel (verify_kernel dominant)"},
+    "row streaming": {"launches": 5, "name": "verify_rows",
+                      "sources": ("sv_device.cuh", "sv_internal.h", "sv_pieces.cu"),
+                      "kernels": "rows_plan + rows_stats + rows_decide + rows_resid + rows_draw "
+                                 "(rows_stats_kernel dominant)"},
+}
 
 
 def parse():
@@ -76,7 +86,8 @@ def parse():
                     help="timed rounds of the draft-length controller (0 = skip)")
     ap.add_argument("--profile-kernels", default="",
                     help="run each named kernel's representative case twice (for ncu, one kernel per "
-                         "capture): comma list of verify, verify_dense, pieces, early_exit, compact, debug, kd, tree, ctrl")
+                         "capture): comma list of verify (the default schedule), verify_cluster, verify_dense, pieces, early_exit, "
+                         "compact, debug, kd, tree, ctrl")
     return ap.parse_args()
 
 
@@ -101,31 +112,28 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-VERIFY_KERNEL_SOURCES = ("sv_device.cuh", "sv_internal.h", "sv_kernels.cu")
-
-
-def kernel_source_hash():
-    """sha256 (first 16 hex digits) of the files the verify kernel is
+def kernel_source_hash(schedule="cluster"):
+    """sha256 (first 16 hex digits) of the files a schedule's kernels are
     compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_71_gb300", "csrc")
-    for f in VERIFY_KERNEL_SOURCES:
+    for f in SCHEDULES[schedule]["sources"]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per launch of the verify kernel from the committed ncu
-    summary for this workload, if that summary was taken on the current
-    kernel source (its 'source_hash' line matches); else None."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+def profiled_traffic(workload, schedule="cluster"):
+    """DRAM bytes per call of the schedule from the committed ncu summary for
+    this workload, if that summary was taken on the current sources (its
+    'source_hash' line matches); else None."""
+    path = os.path.join(ROOT, "profiles", f"{SCHEDULES[schedule]['name']}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
     m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash(schedule):
         return None
     return int(m_tr.group(1))
 
@@ -348,7 +356,11 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
     if st != svp.SV_OK:
         raise RuntimeError(f"device error {st} during the timed region: {stats}")
     cfg = ver.config()
-    cfg["cluster"], cfg["grid_ctas"] = ver.launch_shape(w.B)
+    cfg["kernel"] = kernel_name(svp, ver.kernel_for(w.B))
+    if cfg["kernel"] == "cluster":
+        cfg["cluster"], cfg["grid_ctas"] = ver.launch_shape(w.B)
+    else:
+        cfg["cluster"], cfg["grid_ctas"] = None, None
     del sets, outs
     return {"total_ms": total_ms, "kernel_ms_mean": float(np.mean(kern_ms)),
             "kernel_ms_median": float(np.median(kern_ms)), "kernel_ms_best": float(np.min(kern_ms)),
@@ -356,13 +368,19 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
             "soak_steps": soak, "cfg": cfg, "ver": ver, "base_inputs": base, "launch": launch}
 
 
+def kernel_name(svp, k):
+    return {svp.SV_KERNEL_CLUSTER: "cluster", svp.SV_KERNEL_PIECES: "row streaming"}.get(k, str(k))
+
+
 def timeline_summary(svp, ver, inp, stream):
     """Per-CTA timestamps of one more call on the headline batch (outside the
-    timed region): when the CTAs got to work, took their first and last
+    timed region), taken on the cluster kernel (the timeline is its
+    measurement aid): when the CTAs got to work, took their first and last
     chunks and finished, in microseconds from the work-list kernel's start
     (min / median / max over the CTAs)."""
     import torch
 
+    ver.set_kernel(svp.SV_KERNEL_CLUSTER)
     cs, ctas = ver.launch_shape(inp["target"].shape[0])
     buf = torch.zeros((ctas + 1) * 8, dtype=torch.int64, device=inp["target"].device)
     ver.set_timeline(buf)
@@ -372,6 +390,7 @@ def timeline_summary(svp, ver, inp, stream):
                        stream=stream)
     stream.synchronize()
     ver.set_timeline(None)
+    ver.set_kernel(svp.SV_KERNEL_AUTO)
     t = buf.cpu().numpy().reshape(ctas + 1, 8).astype(np.float64)
     t0 = t[ctas, 0]
     rel = lambda col: (t[:ctas, col] - t0) / 1e3
@@ -380,7 +399,7 @@ def timeline_summary(svp, ver, inp, stream):
             "work_list_kernel_end": round(float((t[ctas, 1] - t0) / 1e3), 2),
             "cta_start": q(rel(7)), "work_list_ready": q(rel(0)), "first_chunk": q(rel(1)),
             "last_chunk": q(rel(2)), "cta_end": q(rel(5)), "after_last_chunk": q(rel(5) - rel(2)),
-            "chunks_per_cta": q(t[:ctas, 6]), "cluster": cs, "ctas": ctas}
+            "chunks_per_cta": q(t[:ctas, 6]), "cluster": cs, "ctas": ctas, "kernel": "cluster"}
 
 
 def _graph_ms(torch, stream, fn, steps):
@@ -708,6 +727,7 @@ def our_arm(args, w):
                          f"threads; one pass in {r['seconds_1']:.1f} s on 1 thread"}
         parity = r.get("parity")
 
+    sched = m["cfg"]["kernel"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -718,20 +738,21 @@ def our_arm(args, w):
                    "l2": f"{args.rotate} rotating copies of the inputs (each larger than the 129 MB L2)",
                    "parallelism": f"replicas{world}", "launch": m["launch"], "stages": m["cfg"]["stages"],
                    "ctas_per_sm": m["cfg"]["ctas_per_sm"], "grid_ctas": m["cfg"]["grid_ctas"],
-                   "cluster": m["cfg"]["cluster"],
+                   "cluster": m["cfg"]["cluster"], "schedule": m["cfg"]["kernel"],
                    "threads": m["cfg"]["threads"], "smem_bytes": m["cfg"]["smem_bytes"]},
         "gbs": gbs_step, "frac_of_8tbs": gbs_step / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": kern_gbs, "peak": peak, "unit": "GB/s",
                      "frac": kern_gbs / peak, "peak_source": peak_kind,
-                     "traffic": profiled_traffic(w.name), "kernel": KERNEL_NAME,
-                     "traffic_source": f"dram__bytes_read.sum + dram__bytes_write.sum per launch from the "
-                                       f"committed ncu summary profiles/{KERNEL_NAME}_{w.name}.md, used only "
+                     "traffic": profiled_traffic(w.name, sched), "kernel": SCHEDULES[sched]["kernels"],
+                     "schedule": sched,
+                     "traffic_source": f"dram__bytes_read.sum + dram__bytes_write.sum per call from the "
+                                       f"committed ncu summary profiles/{SCHEDULES[sched]['name']}_{w.name}.md, used only "
                                        f"when its source hash matches this kernel (else null)",
                      "launch_ms": launch_ms, "eager_launch_ms_mean": m["kernel_ms_mean"],
                      "eager_launch_ms_median": m["kernel_ms_median"], "eager_launch_ms_best": m["kernel_ms_best"]},
         "clocks": m["clocks"], "clock_soak_steps": m["soak_steps"],
         "e2e": {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
-        "gpu_launches": 2 * args.steps,   # per call: the work-list kernel and the verify kernel
+        "gpu_launches": SCHEDULES[sched]["launches"] * args.steps,   # the schedule's launches per call
         "acceptance": {"mean_emitted": stats["mean_emitted"], "mean_accepted": stats["mean_accepted"],
                        "accept_rate": stats["accept_rate"], "spec_off": stats["spec_off"]},
         "cpu_baseline": cpu, "parity": parity, "timeline": timeline, "aux": aux or None,
@@ -810,6 +831,12 @@ def profile_kernels(args):
         for _ in range(2):
             if name == "verify":
                 ot, ol = run(ver, inp)
+            elif name == "verify_cluster":
+                if "cluster" not in extra:
+                    cv = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+                    cv.set_kernel(svp.SV_KERNEL_CLUSTER)
+                    extra["cluster"] = cv
+                run(extra["cluster"], inp)
             elif name == "verify_dense":
                 if "dense" not in extra:
                     dw = get_workload("ragged_dense")

@@ -207,24 +207,23 @@ sv_status sv_get_config(const sv_ctx *ctx, int *stages, int *ctas_per_sm, int *t
                         int *smem_bytes, int *grid_ctas, int *cluster);
 sv_status sv_launch_shape(const sv_ctx *ctx, int B, int *cluster, int *grid_ctas);
 
-/* Which kernel runs a call.  Two kernels compute the same rule:
+/* Which schedule runs a call.  Two compute the same rule with the same
+ * arithmetic:
  *   SV_KERNEL_CLUSTER  the cluster kernel described above: a sequence at a
- *                      time per cluster;
- *   SV_KERNEL_PIECES   every needed row cut into pieces of at most one 64 KB
- *                      slot, dealt round-robin to one CTA per SM in
- *                      work-list order; a sequence is decided by whichever
- *                      CTA reduces its last piece, through global counters.
- *                      It spreads every batch evenly over the SMs, but its
- *                      global round trips (a few microseconds each while the
- *                      memory is busy) make it slower than the cluster
- *                      kernel on every workload measured; it is kept as a
- *                      second schedule of the same rule.  It needs 16-byte aligned
- *                      rows (V * sizeof(dtype) a multiple of 16, aligned
- *                      bases), B <= 2048, early exit off and no fixed cluster
- *                      size; a call that does not qualify runs the cluster
- *                      kernel.
- *   SV_KERNEL_AUTO     (default) the cluster kernel, the faster of the two on
- *                      every measured workload.
+ *                      time per cluster of CTAs;
+ *   SV_KERNEL_PIECES   row streaming: every needed row is cut into 64 KB
+ *                      pieces spread evenly over one CTA per SM (no exchange
+ *                      between CTAs); then one warp per sequence takes the
+ *                      tests and the bonus draw, the rejected pairs are read
+ *                      again (spread over the SMs the same way), and one warp
+ *                      per rejected pair draws.  Five launches per call.  It
+ *                      needs 16-byte aligned rows (V * sizeof(dtype) a
+ *                      multiple of 16, aligned bases), rows of at most 1 MiB,
+ *                      B <= 2048, early exit off and no fixed cluster size;
+ *                      a call that does not qualify runs the cluster kernel.
+ *   SV_KERNEL_AUTO     (default) row streaming where it qualifies, the
+ *                      faster of the two on every measured workload; else
+ *                      the cluster kernel.
  * sv_set_kernel returns SV_ERR_INVALID_ARG for another value;
  * sv_kernel_for reports the kernel a call with batch B would run on
  * 16-byte aligned rows. */
@@ -232,7 +231,8 @@ typedef enum { SV_KERNEL_AUTO = 0, SV_KERNEL_CLUSTER = 1, SV_KERNEL_PIECES = 2 }
 sv_status sv_set_kernel(sv_ctx *ctx, int kernel);
 sv_status sv_kernel_for(const sv_ctx *ctx, int B, int *kernel);
 
-/* Per-CTA timeline of the cluster kernel (measurement aid, off by default).
+/* Per-CTA timeline of the cluster kernel (measurement aid, off by default;
+ * calls that run row streaming write nothing).
  * timeline: device buffer of `capacity` unsigned 64-bit words, or NULL to
  * turn it off.  A call whose grid has G CTAs (sv_launch_shape) and for which
  * capacity >= (G + 1) * 8 writes, per CTA g, the global timer in ns at

@@ -37,7 +37,7 @@ struct sv_ctx {
   unsigned long long* timeline = nullptr;   // caller's buffer of per-CTA timestamps (or null)
   int timeline_cap = 0;
   int pieces_ctas = 0;         // grid of the pieces kernel (one CTA per SM)
-  int np = 0, pe = 0, nr = 0, he = 0;
+  int np = 0, nr = 0;
   long long calls = 0;
   int last_B = 0, last_k = 0, last_greedy = 0, last_diag = 0;
   float last_inv_T = 1.f;
@@ -100,21 +100,23 @@ sv_status configure_auto(sv_ctx* ctx) {
   return configure(ctx, 2, 0);
 }
 
-// Whether a call with batch B (rows 16-byte aligned) runs the pieces kernel.
+// Whether a call with batch B (rows 16-byte aligned) runs row streaming (the
+// default where it qualifies, the faster schedule on every measured workload).
 bool use_pieces(const sv_ctx* ctx, int B) {
-  if (ctx->kernel != SV_KERNEL_PIECES || !ctx->pw_mem || ctx->pieces_ctas <= 0) return false;
+  if (ctx->kernel == SV_KERNEL_CLUSTER || !ctx->pw_mem || ctx->pieces_ctas <= 0) return false;
   if (ctx->early_exit || ctx->cluster != 0) return false;
   return B <= sv::kPiecesMaxB;
 }
 
-// The pieces kernel's workspace for (max_B, max_k) and rows of V logits:
-// one allocation, 256-byte aligned sub-arrays.  Also the launch shape.
+// The row-streaming schedule's workspace for (max_B, max_k) and rows of V
+// logits: one allocation, 256-byte aligned sub-arrays.  Also the launch shape.
 sv_status create_pieces(sv_ctx* ctx) {
-  sv::pieces_shape(ctx->V, ctx->elt, ctx->np, ctx->pe, ctx->nr, ctx->he);
+  sv::pieces_shape(ctx->V, ctx->elt, ctx->np, ctx->nr);
   cudaDeviceProp prop;
   cudaError_t e = cudaGetDeviceProperties(&prop, ctx->device);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGetDeviceProperties");
   if (sv::pieces_smem_bytes() > static_cast<int>(prop.sharedMemPerBlockOptin)) return SV_OK;
+  if (ctx->np > sv::kMaxChunks) return SV_OK;   // rows of at most 1 MiB, as for the cluster kernel
   e = sv::prepare_pieces_kernel();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(pieces)");
   // batches above kPiecesMaxB run the cluster kernel
@@ -123,36 +125,25 @@ sv_status create_pieces(sv_ctx* ctx) {
   const size_t rows = B * (2 * k + 1);
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
-  const size_t o_rowpart = take(rows * ctx->np * 16);
-  const size_t o_seqcnt = take(B * 4), o_bseg = take(B * ctx->np * 16 * 8);
+  const size_t o_rowoff = take((B + 1) * 4), o_rowtab = take(rows * 16);
+  const size_t o_rec = take(rows * ctx->np * 16), o_bseg = take(B * ctx->np * 16 * 8);
+  const size_t o_job = take(B * 16), o_jobn = take(B * 16), o_njobs = take(4);
   const size_t o_rmass = take(B * ctx->nr * 16 * 4), o_pmass = take(B * ctx->nr * 16 * 4);
-  const size_t o_rcnt = take(B * 4), o_rflag = take(B * 4), o_rq = take(B * 16), o_rqn = take(B * 16);
-  // re-read pieces go round-robin to the CTAs: each receives at most
-  // ceil(B nr / ctas) of them
-  const size_t ctas = static_cast<size_t>(prop.multiProcessorCount);
-  const size_t mcap = (B * ctx->nr + ctas - 1) / ctas + 1;
-  const size_t o_mbox = take(ctas * mcap * 4), o_mtail = take(ctas * 32 * 4);
-  const size_t o_ctr = take(64 * 4), o_grp = take(33 * 4);
   e = cudaMalloc(&ctx->pw_mem, off);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc(pieces workspace)");
   e = cudaMemset(ctx->pw_mem, 0, off);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemset(pieces workspace)");
   char* base = static_cast<char*>(ctx->pw_mem);
   sv::PiecesWs& w = ctx->pw;
-  w.rowpart = reinterpret_cast<float4*>(base + o_rowpart);
-  w.seqcnt = reinterpret_cast<int*>(base + o_seqcnt);
+  w.rowoff = reinterpret_cast<int*>(base + o_rowoff);
+  w.rowtab = reinterpret_cast<int4*>(base + o_rowtab);
+  w.rec = reinterpret_cast<float4*>(base + o_rec);
   w.bseg = reinterpret_cast<float2*>(base + o_bseg);
+  w.job = reinterpret_cast<int4*>(base + o_job);
+  w.jobn = reinterpret_cast<float4*>(base + o_jobn);
+  w.njobs = reinterpret_cast<int*>(base + o_njobs);
   w.rmass = reinterpret_cast<float*>(base + o_rmass);
   w.pmass = reinterpret_cast<float*>(base + o_pmass);
-  w.rcnt = reinterpret_cast<int*>(base + o_rcnt);
-  w.rflag = reinterpret_cast<int*>(base + o_rflag);
-  w.rq = reinterpret_cast<int4*>(base + o_rq);
-  w.rqn = reinterpret_cast<float4*>(base + o_rqn);
-  w.mbox = reinterpret_cast<int*>(base + o_mbox);
-  w.mtail = reinterpret_cast<int*>(base + o_mtail);
-  w.mcap = static_cast<int>(mcap);
-  w.ctr = reinterpret_cast<int*>(base + o_ctr);
-  w.grp = reinterpret_cast<int*>(base + o_grp);
   ctx->pieces_ctas = prop.multiProcessorCount;   // one CTA per SM (the shared memory allows no more)
   return SV_OK;
 }
@@ -330,7 +321,7 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   p.ctas = ctas;
   if (p.bulk && use_pieces(ctx, B)) {
     p.pieces = 1;
-    p.np = ctx->np; p.pe = ctx->pe; p.nr = ctx->nr; p.he = ctx->he;
+    p.np = ctx->np; p.nr = ctx->nr;
     p.ctas = ctx->pieces_ctas;
     p.pw = ctx->pw;
   }

@@ -60,25 +60,21 @@ struct Workspace {
   unsigned int* err_word;     // sticky OR of (1 << code)
 };
 
-// Workspace of the piece-streaming kernel (sv_pieces.cu), owned by the
-// context.  Rows are numbered r = b (k+1) + i for target rows and
-// B (k+1) + b k + i for draft rows.  Every counter is zero when a call
-// starts (plan_kernel clears them).
+// Workspace of the row-streaming schedule (sv_pieces.cu), owned by the
+// context.  Rows of the work list's sequences are numbered in work-list
+// order: rowoff[t] rows come before entry t's (target 0, draft 0, ...,
+// target k_b), rowoff[n] in all.  A piece is 64 KB of one row (np per row),
+// a re-read half-piece 32 KB of each row of a pair (nr per row).
 struct PiecesWs {
-  float4* rowpart;   // [rows * np]  one piece's (M, K, S, bad) (greedy: M, arg, 0, bad)
-  int* seqcnt;       // [B]          pieces of the sequence reduced so far
-  float2* bseg;      // [B * np * 16]  the bonus row's segment (K, S), one per consumer warp and piece
-  float* rmass;      // [B * nr * 16]  residual masses of the re-read pieces of a rejected pair
-  float* pmass;      // [B * nr * 16]  target masses of the same segments (zero-residual fallback)
-  int* rcnt;         // [B]          residual pieces reduced
-  int* rflag;        // [B]          error bits seen in the residual pieces
-  int4* rq;          // [B]          the rejected pair of sequence b: (a, k_b, 0, 0)
-  float4* rqn;       // [B]          ... and (K_t, L_t, Gh, Gl) of the pair
-  int* mbox;         // [ctas * mcap] re-read pieces handed to each CTA: b * nr + j + 1 (0: not yet written)
-  int* mtail;        // [ctas * 32]  messages handed to each CTA (one 128-byte line per CTA)
-  int mcap;          //              mailbox slots per CTA
-  int* ctr;          // [64]         [32] sequences settled (its own line)
-  int* grp;          // [33]         sequences per draft length (plan_kernel)
+  int* rowoff;       // [max_B + 1]
+  int4* rowtab;      // [rows]       each row's (b, k_b, pos | kind << 16, drafted token or -1)
+  float4* rec;       // [rows * np]   a piece's (M, S about fl(M c), token logit, flags); greedy (M, argmax, 0, flags)
+  float2* bseg;      // [max_B * np * 16]  bonus rows: each warp segment's (fl(m c), sum)
+  int4* job;         // [max_B]       a rejected pair to draw from: (entry t, b, a, k_b)
+  float4* jobn;      // [max_B]       ... its (K_t, L_t, Gh, Gl)
+  int* njobs;        // [1]
+  float* rmass;      // [max_B * nr * 16]  per job, each re-read segment's sum of max(0, p - q)
+  float* pmass;      // [max_B * nr * 16]  ... and of p (zero-residual fallback)
 };
 
 struct VerifyParams {
@@ -104,11 +100,11 @@ struct VerifyParams {
   // kTimelineSlots per CTA and, after the last CTA's, the plan kernel's
   // start and end: null when not asked for
   unsigned long long* timeline;
-  // piece streaming (sv_pieces.cu) instead of the cluster kernel when set
+  // row streaming (sv_pieces.cu) instead of the cluster kernel when set
   int pieces;
-  int np, pe;           // pieces per row and logits per piece (pe * elt <= 64 KB, a multiple of 64)
-  int nr, he;           // re-read pieces per rejected pair and logits of each row per piece (<= 32 KB)
-  int ctas;             // grid of the piece kernel (its first ticket per CTA is its index)
+  int np;               // 64 KB pieces per row
+  int nr;               // 32 KB half-pieces per row (re-reads)
+  int ctas;             // grid of the streaming kernels (one CTA per SM)
   PiecesWs pw;
 };
 
@@ -126,20 +122,16 @@ cudaError_t launch_init_workspace(const Workspace& ws, cudaStream_t s);
 // Shared-memory bytes of the verify kernel with `stages` staging slots.
 int verify_smem_bytes(int stages);
 
-// The piece-streaming kernel (sv_pieces.cu).
+// The row-streaming schedule (sv_pieces.cu).
 constexpr int kPiecesMaxB = 2048;                         // sequences per call
-constexpr int kPiecesStages = 3;                          // 64 KB staging slots per CTA
 int pieces_smem_bytes();
 cudaError_t prepare_pieces_kernel();
 cudaError_t launch_pieces(const VerifyParams& p, cudaStream_t s);   // after plan_kernel
-// Pieces per row / logits per piece for rows of V logits of elt bytes, and
-// the same for the re-read of a pair (half slots).
-inline void pieces_shape(int V, int elt, int& np, int& pe, int& nr, int& he) {
+// 64 KB pieces and 32 KB half-pieces per row of V logits of elt bytes.
+inline void pieces_shape(int V, int elt, int& np, int& nr) {
   const long long row = static_cast<long long>(V) * elt;
   np = static_cast<int>((row + kChunkBytes - 1) / kChunkBytes);
-  pe = ((V + np - 1) / np + 63) / 64 * 64;
   nr = static_cast<int>((row + kChunkBytes / 2 - 1) / (kChunkBytes / 2));
-  he = ((V + nr - 1) / nr + 63) / 64 * 64;
 }
 
 // Cluster size chosen when the caller leaves it open.  A sequence is the

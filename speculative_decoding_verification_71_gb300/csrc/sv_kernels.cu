@@ -214,19 +214,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
       ws.m_d[i] = NAN; ws.L_d[i] = NAN; ws.alpha[i] = NAN;
     }
   }
-  if (P.pieces) {
-    // the piece kernel's counters start from zero
-    const PiecesWs& pw = P.pw;
-    for (int i = tid; i < B; i += kPlanThreads) {
-      pw.seqcnt[i] = 0; pw.rcnt[i] = 0; pw.rflag[i] = 0;
-    }
-    for (int i = tid; i < P.ctas * pw.mcap; i += kPlanThreads) pw.mbox[i] = 0;
-    for (int i = tid; i < P.ctas; i += kPlanThreads) pw.mtail[i * 32] = 0;
-    if (tid < 64) pw.ctr[tid] = 0;
-  }
   // the first sequence of cluster i is entry i of the work list (no atomic
   // needed); the shared counter hands out the rest
-  if (tid == 0) { base = 0; *ws.ticket = P.pieces ? 0 : P.ctas / max(1, P.cluster); }
+  if (tid == 0) { base = 0; *ws.ticket = P.ctas / max(1, P.cluster); }
   __syncthreads();
   // counting sort by k_b, largest first, stable in b
   for (int L = k; L >= 0; --L) {
@@ -262,7 +252,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const VerifyParams P
       if (tid == kPlanThreads - 1) base += warp_cnt[31] + __popc(m);
       __syncthreads();
     }
-    if (P.pieces && tid == 0) P.pw.grp[L] = base;   // sequences with k_b >= L
   }
   if (tid == 0) {
     *ws.n_seqs = base;
@@ -1651,12 +1640,12 @@ cudaError_t query_max_clusters(int cluster, int smem_bytes, int* out) {
 
 cudaError_t launch_verify(const VerifyParams& params, int ctas, int smem_bytes, cudaStream_t s) {
   NvtxRange range("spec_verify");
+  if (params.pieces) return launch_pieces(params, s);   // its own plan, in batch order
   VerifyParams p = params;
-  if (!p.pieces) p.ctas = ctas;   // the work-list kernel starts the ticket counter after every cluster's first
+  p.ctas = ctas;   // the work-list kernel starts the ticket counter after every cluster's first
   plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (p.pieces) return launch_pieces(p, s);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
   verify_config(cfg, attr, p.cluster, ctas, smem_bytes, s);

@@ -1,46 +1,36 @@
-// Piece-streaming verification: the same rule as verify_kernel, scheduled for
-// small batches.
+// Row-streaming schedule of speculative-sampling verification
+// (SV_KERNEL_PIECES), for sm_103a.
 //
-// verify_kernel gives a whole sequence to one CTA cluster, so at a few
-// hundred sequences the last ones to finish leave most SMs idle.  Here the
-// unit of work is a piece of a row: every needed row (target rows 0..k_b,
-// draft rows 0..k_b-1 of each sequence) is cut into np pieces of at most one
-// 64 KB staging slot, and the units are dealt round-robin to persistent CTAs
-// (one per SM) in the order of plan_kernel's work list (longest sequences
-// first, each sequence's pieces together), so every CTA streams the same
-// number of bytes and none waits for a ticket.  Nothing waits for another
-// CTA on the data path: the sequence is decided by whichever CTA reduces its
-// last piece (an acq_rel counter per sequence):
-//
-//   piece     consumer warps: per warp (M, fl(M c), sum 2^(z c - K)) of its
-//             segment (greedy: maximum and first argmax), and the logit of
-//             the drafted token if it falls there;  control warps: the
-//             piece's part written out, the sequence's counter;
-//   sequence  a decider warp of the CTA completing it: every row's
-//             (M, K, S, L) from its pieces in piece order, every acceptance
-//             test alpha = min(1, p(x)/q(x)), u < alpha, the first rejection
-//             a; if every draft was accepted, the bonus token by inverse CDF
-//             over the bonus row's segment sums (kept while streaming) and a
-//             walk of one segment; else the rejected pair is read again;
-//   re-read   the pair in nr pieces (target and draft halves of one slot),
-//             handed round-robin to the CTAs' mailboxes and taken before new
-//             rows: per-segment masses of max(0, p - q) = p (1 - 2^delta);
-//             the CTA completing the last piece finds the segment holding
-//             s S and walks it.
-// A sequence's outputs are written once every row is reduced, so an invalid
-// row anywhere in 0..k_b fails it, as in verify_kernel.  Every reduction runs
-// in a fixed order, so the outputs are deterministic and equal to
-// verify_kernel's up to the summation order of the row sums.
-//
-// The rule is the standard speculative-sampling rule read into "Accelerating
-// RL Post-Training Rollouts via System-Integrated Speculative Decoding", §2
-// core mechanism: accept with min(1, p/q), stop at the first rejection,
-// resample from max(0, p - q) or draw the bonus token from the last target
-// row.
+// The same rule as verify_kernel (accept draft i with min(1, p_i/q_i) up to
+// the first rejection, then the residual max(0, p - q) or the bonus row),
+// the same arithmetic, another schedule: the rows of the batch are streamed
+// as independent 64 KB pieces spread evenly over one CTA per SM, with no
+// exchange between CTAs, and the per-sequence decisions come after.  Five
+// launches per call (each after plan_kernel's work list, each waiting for its
+// predecessor's results with programmatic dependent launch, after the first):
+//   rows_plan_kernel    in batch order: rows before each sequence (2 k_b + 1
+//                       each), the row table, invalid k_b answered;
+//   rows_stats_kernel   every needed row, piece by piece: a producer warp
+//                       streams the pieces through three shared-memory slots
+//                       with cp.async.bulk, 16 consumer warps reduce them; the
+//                       last warp to finish a piece combines the warps' parts
+//                       into its record (max, sum of 2^(z c - fl(max c)), the
+//                       drafted token's logit); bonus rows also keep each
+//                       warp segment's sum for the draw;
+//   rows_decide_kernel  one warp per sequence: the rows from their pieces, the
+//                       tests, the first rejection; the bonus draw (one
+//                       segment read again) or a job for the residual;
+//   rows_resid_kernel   every job's rejected pair read again in 32 KB
+//                       half-pieces spread over the CTAs: each warp segment's
+//                       sums of max(0, p - q) and of p;
+//   rows_draw_kernel    one warp per job: the segment holding s * S, the token.
+// Rows must be 16-byte aligned (bulk copies); other calls run the cluster
+// kernel.
 
 #include <cuda_runtime.h>
-#include <cstdint>
+
 #include <cmath>
+#include <cstdint>
 
 #include "sv_internal.h"
 #include "sv_device.cuh"
@@ -48,979 +38,881 @@
 namespace sv {
 namespace {
 
-constexpr int kCtlWarps = 2;     // control warps (alternate units), each with its decider warp
-constexpr int kPThreads = (kConsumerWarps + 1 + 2 * kCtlWarps) * 32;   // + producer
-constexpr int kWarpProducer = kConsumerWarps;
-constexpr int kWarpCtl0 = kConsumerWarps + 1;
-constexpr int kWarpDec0 = kConsumerWarps + 1 + kCtlWarps;
-constexpr int kCtrSettled = 32;  // sequences settled (a 128-byte line of its own)
-constexpr int kUBufs = 8;        // unit results in flight between consumers and control warps
-constexpr int kJobs = 64;        // decider jobs (ring)
-constexpr int kSegs = kConsumerWarps;                     // segments per piece (one per consumer warp)
-constexpr int kHalf = kChunkBytes / 2;                    // one row's half of a re-read slot
-constexpr int kHalfVecsPerWarp = kHalf / 16 / kConsumerWarps;   // 128
-constexpr int kHalfVecsPerLane = kHalfVecsPerWarp / 32;         // 4
-constexpr int kMaxResid = 2 * kMaxChunks;                 // re-read pieces of a pair (rows up to 1 MiB)
+constexpr int kRWarps = kConsumerWarps;              // consumer warps (16)
+constexpr int kRProducer = kRWarps;                  // the producer warp's index
+constexpr int kRThreads = (kRWarps + 1) * 32;
+constexpr int kRStages = 3;                          // 64 KB staging slots
+constexpr int kRHalf = kChunkBytes / 2;              // a re-read slot: 32 KB of each row of the pair
+constexpr int kRStatVecs = kChunkBytes / 16 / kRWarps / 32;   // 8 vectors per lane and piece
+constexpr int kRDrawVecs = kRHalf / 16 / kRWarps / 32;        // 4 vectors per lane and half-piece
+constexpr int kRBufs = kRStages + 1;                 // per-piece part buffers (warps run at most a ring apart)
+constexpr int kRSmallThreads = 64;                   // decide / draw kernels: 2 warps, one sequence each
 
+// flags of a part or record
+enum : int { kFBad = 1, kFHasZx = 2, kFTimeout = 4 };
 enum : int { kErrBadTok = 1 << 3, kErrNonfin = 1 << 4, kErrTime = 1 << 5 };
-enum : int { kJobSeq = 0, kJobResid = 1, kJobEnd = 2 };
-constexpr int kMaxRows = 64;     // rows of a sequence: 2 k + 1 <= 63
-constexpr int kScratch = 256;    // decider scratch: float4 piece parts, or doubles of segment weights x 2
 
-// What a staging slot holds.
-struct PDesc {
-  int b, kb, pos, kind;        // kind 0 target, 1 draft, 2 re-read of a rejected pair, -1 end
-  int piece, nbytes, r, x;     // r: row index (kinds 0/1); x: unused (-1)
-  float K0, L0, G0, G1;        // re-read: target normaliser, log2 normaliser ratio (Gh + Gl)
+struct alignas(16) WPart {     // one warp's share of a piece
+  float m, s, zx;              // max, sum of 2^(z c - fl(m c)) (greedy: argmax as int bits), token logit
+  int flags;
 };
 
-// A unit's results: the descriptor and one float4 per consumer warp.
-struct UBuf {
-  PDesc d;
-  float4 w[kConsumerWarps];
+// What a staging slot holds (written by the producer, read by the consumers).
+struct RDesc {
+  int u;                       // unit (piece or half-piece) index of this CTA's range, counted from 0
+  int rec;                     // stats: the record index (row * np + piece); re-read: the job
+  int part;                    // stats: the piece; re-read: the half-piece
+  int bytes;                   // bytes of each row in the slot
+  int b, kb, pos, kind;        // the row (stats) or the pair (re-read)
+  int x;                       // drafted token at pos (pairs' rows), else -1
+  int pad[3];
+  float4 num;                  // re-read: the pair's (K_t, L_t, Gh, Gl)
 };
 
-struct Job {
-  int kind, r, b, pos;
-  int rowkind, pad0, pad1, pad2;
+struct RCtrl {
+  uint64_t full[kRStages];     // slot filled (producer -> consumers)
+  uint64_t empty[kRStages];    // slot released (one arrival per consumer warp)
+  RDesc desc[kRStages];
+  WPart part[kRBufs][kRWarps];
+  int cnt[kRBufs];             // warps done with the piece in this buffer
 };
+constexpr int kRCtrlBytes = ((static_cast<int>(sizeof(RCtrl)) + 1023) / 1024) * 1024;
+static_assert(kRCtrlBytes + kRStages * kChunkBytes <= 227 * 1024, "three slots must fit in one CTA");
 
-struct PCtrl {
-  uint64_t full[kPiecesStages], empty[kPiecesStages];
-  uint64_t ufull[kUBufs], ufree[kUBufs];
-  PDesc desc[kPiecesStages];
-  UBuf ub[kUBufs];
-  Job jobs[kCtlWarps][kJobs];   // control warp i -> decider warp i
-  volatile int job_ready[kCtlWarps][kJobs];
-  volatile int job_head[kCtlWarps];
-  int job_tail[kCtlWarps];
-  int gstart[33], gunits[33], gcount[33];   // per draft length L: first sequence, first unit, sequences
-  int n_valid, total_units;
-  struct Dec {                  // a decider's scratch
-    union {
-      float4 part[kScratch];    // piece parts of a sequence's rows
-      double segw[2 * kScratch];  // segment weights of a draw
-    };
-    float4 row[kMaxRows];       // each row's (M, K, S, L) (greedy: M, arg, 0, 0)
-    float zx[kMaxRows];         // each pair row's logit of the drafted token
-    int bad[kMaxRows];
-  } dec[kCtlWarps];
-  int seq_b[kPiecesMaxB];       // the work list (batch index), longest first
-};
+__device__ __forceinline__ const unsigned char* row_ptr(const VerifyParams& P, int b, int pos, int kind) {
+  const size_t rb = static_cast<size_t>(P.V) * P.elt;
+  if (kind == 0) return static_cast<const unsigned char*>(P.target) + (static_cast<size_t>(b) * (P.k + 1) + pos) * rb;
+  return static_cast<const unsigned char*>(P.draft) + (static_cast<size_t>(b) * P.k + pos) * rb;
+}
 
-constexpr int kPCtrlBytes = ((static_cast<int>(sizeof(PCtrl)) + 1023) / 1024) * 1024;
-static_assert(kMaxResid * kSegs <= 2 * kScratch && kMaxChunks * kSegs <= 2 * kScratch,
-              "a draw's segment weights fit in a decider's scratch");
-static_assert(kPCtrlBytes + kPiecesStages * kChunkBytes <= 227 * 1024, "control block and ring must fit in one CTA");
+// The call's plan, in batch order (no sort: every piece is the same work):
+// rowoff[b] = rows of the sequences before b (2 k_b + 1 each, k_b + 1 for
+// T = 0; none for an invalid k_b, which is answered here), rowoff[B] = all
+// rows; each row's entry in the row table; the counters the other kernels
+// start from.  One CTA.
+__global__ void __launch_bounds__(1024) rows_plan_kernel(const VerifyParams P) {
+  grid_dependents_launch();      // the statistics kernel's prologue may start
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = P.B, k = P.k;
+  if (tid == 0) { carry = 0; *P.pw.njobs = 0; }
+  if (P.diag) {
+    for (int i = tid; i < B * (k + 1); i += 1024) { P.ws.m_t[i] = NAN; P.ws.L_t[i] = NAN; P.ws.mass[i] = NAN; }
+    for (int i = tid; i < B * k; i += 1024) { P.ws.m_d[i] = NAN; P.ws.L_d[i] = NAN; P.ws.alpha[i] = NAN; }
+  }
+  __syncthreads();
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + tid;
+    const int kb = b < B ? __ldg(P.draft_len + b) : 0;
+    const bool valid = b < B && kb >= 0 && kb <= k;
+    if (b < B && !valid) {
+      int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
+      for (int j = 0; j <= k; ++j) ot[j] = -1;
+      P.out_len[b] = 0;
+      atomicOr(P.ws.err_word, 1u << 2 /* SV_ERR_BAD_DRAFT_LEN */);
+      atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
+    }
+    const int cnt = valid ? (P.greedy ? kb + 1 : 2 * kb + 1) : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += up;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int wt = warp_tot[lane];
+      int wi = wt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += up;
+      }
+      warp_tot[lane] = wi - wt;
+    }
+    __syncthreads();
+    if (b < B) {
+      // the sequence's rows: target 0, draft 0, ..., target k_b (T = 0: the
+      // target rows alone), each with its drafted token
+      const int r0 = carry + warp_tot[warp] + incl - cnt;
+      P.pw.rowoff[b] = r0;
+      for (int ri = 0; ri < cnt; ++ri) {
+        int pos, kind;
+        if (P.greedy) { pos = ri; kind = 0; }
+        else if (ri < 2 * kb) { pos = ri >> 1; kind = ri & 1; }
+        else { pos = kb; kind = 0; }
+        const int x = pos < kb ? __ldg(P.tokens + static_cast<size_t>(b) * k + pos) : -1;
+        P.pw.rowtab[r0 + ri] = make_int4(b, kb, pos | (kind << 16), x);
+      }
+    }
+    __syncthreads();
+    if (tid == 1023) carry += warp_tot[31] + incl;
+    __syncthreads();
+  }
+  if (tid == 0) P.pw.rowoff[B] = carry;
+}
+
+// Vector v of a row (16-byte aligned rows), -inf past its end.
+template <int ELT>
+__device__ __forceinline__ uint4 row_vec(const unsigned char* row, int v, int nvec_row) {
+  return v < nvec_row ? __ldg(reinterpret_cast<const uint4*>(row) + v) : Vec<ELT>::neg_inf();
+}
+
+// The segment holding the target weight `tgt` among `nseg` masses (index
+// order, lanes taking contiguous runs); seg_t is what is left of tgt at the
+// segment's start.  Past the end (rounding) it is the last segment with
+// positive mass.  Warp-wide, in fp32: GB300's fp64 pipe is narrow, and the
+// sums' rounding (under 1e-6 of the mass) stays inside the 1e-5 band within
+// which a draw counts as a near-tie.
+__device__ void locate_seg(const float* mass, int nseg, float tgt, int lane, int& seg, float& seg_t) {
+  const int per = (nseg + 31) / 32;
+  const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
+  float gs = 0.f;
+  for (int i = g0; i < g1; ++i) gs += mass[i];
+  const float incl = warp_incl_scan(gs, lane);
+  const float excl = incl - gs;
+  const unsigned hit = __ballot_sync(0xffffffffu, gs > 0.f && tgt < incl);
+  const unsigned posg = __ballot_sync(0xffffffffu, gs > 0.f);
+  const int owner = hit ? (__ffs(hit) - 1) : (posg ? 31 - __clz(posg) : -1);
+  seg = -1;
+  seg_t = 0.f;
+  if (owner >= 0 && lane == owner) {
+    float run = excl, last_run = excl;
+    int last = -1;
+    for (int i = g0; i < g1; ++i) {
+      const float m = mass[i];
+      if (m > 0.f) { last = i; last_run = run; }
+      if (seg < 0 && m > 0.f && tgt < run + m) { seg = i; seg_t = tgt - run; }
+      run += m;
+    }
+    if (seg < 0) { seg = last; seg_t = tgt - last_run; }
+  }
+  if (owner >= 0) {
+    seg = __shfl_sync(0xffffffffu, seg, owner);
+    seg_t = __shfl_sync(0xffffffffu, seg_t, owner);
+  }
+}
+
+// Walk NSTEPS x 32 vectors from vector v0 of a row, a warp inclusive scan per
+// step, to the token where the running weight passes t.  RESID: weights
+// max(0, p - q); else p.  Warp-wide.
+template <int ELT, int NSTEPS, bool RESID>
+__device__ int walk_seg(const unsigned char* rowT, const unsigned char* rowD, int v0, int nvec_row, float t,
+                        float c2, float Kt, float Lt, float Gh, float Gl, int lane) {
+  using VV = Vec<ELT>;
+  constexpr int NV = VV::N;
+  uint4 rt[NSTEPS], rd[RESID ? NSTEPS : 1];
+#pragma unroll
+  for (int j = 0; j < NSTEPS; ++j) {
+    rt[j] = row_vec<ELT>(rowT, v0 + j * 32 + lane, nvec_row);
+    if (RESID) rd[RESID ? j : 0] = row_vec<ELT>(rowD, v0 + j * 32 + lane, nvec_row);
+  }
+  float base = 0.f;
+  int found = -1, last_positive = -1;
+#pragma unroll
+  for (int j = 0; j < NSTEPS; ++j) {
+    float w[NV], zt[NV], zd[NV];
+    VV::unpack(rt[j], zt);
+    if (RESID) VV::unpack(rd[RESID ? j : 0], zd);
+    float ls = 0.f;
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      float p;
+      if (RESID) w[e] = resid_weight(zt[e], zd[e], c2, Kt, Lt, Gh, Gl, p);
+      else w[e] = fast_exp2(__fsub_rn(__fmaf_rn(zt[e], c2, -Kt), Lt));
+      ls += w[e];
+    }
+    const float incl = warp_incl_scan(ls, lane);
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+    const float step_total = __shfl_sync(0xffffffffu, incl, 31);
+    const int x0 = (v0 + j * 32 + lane) * NV;
+    const bool mine = found < 0 && ls > 0.f && t < base + incl && !(t < base + excl);
+    const unsigned hit = __ballot_sync(0xffffffffu, mine);
+    int lp = -1;
+#pragma unroll
+    for (int e = 0; e < NV; ++e) if (w[e] > 0.f) lp = x0 + e;
+    const unsigned anyp = __ballot_sync(0xffffffffu, lp >= 0);
+    if (found < 0 && anyp) last_positive = __shfl_sync(0xffffffffu, lp, 31 - __clz(anyp));
+    if (hit) {
+      const int hl = __ffs(hit) - 1;
+      int pick = -1;
+      if (lane == hl) {
+        float c = base + excl;
+        int lastp = -1;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+          if (w[e] > 0.f) lastp = x0 + e;
+          c += w[e];
+          if (pick < 0 && w[e] > 0.f && t < c) pick = x0 + e;
+        }
+        if (pick < 0) pick = lastp;
+      }
+      found = __shfl_sync(0xffffffffu, pick, hl);
+    }
+    base += step_total;
+  }
+  return found >= 0 ? found : last_positive;
+}
+
+// Outputs and counters of a finished sequence (lane 0 writes the scalars).
+__device__ void write_outputs(const VerifyParams& P, int b, int kb, int a, int y, int err, int zero_resid,
+                              int lane) {
+  const int k = P.k;
+  const bool ok = !err && y >= 0;
+  const int acc = a < 0 ? kb : a;
+  int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
+  for (int j = lane; j <= k; j += 32) {
+    int v = -1;
+    if (ok) v = j < acc ? __ldg(P.tokens + static_cast<size_t>(b) * k + j) : (j == acc ? y : -1);
+    ot[j] = v;
+  }
+  if (lane == 0) {
+    P.out_len[b] = ok ? acc + 1 : 0;
+    if (ok) {
+      atomicAdd(P.ws.stats + kStatSequences, 1ull);
+      atomicAdd(P.ws.stats + kStatProposed, static_cast<unsigned long long>(kb));
+      atomicAdd(P.ws.stats + kStatAccepted, static_cast<unsigned long long>(acc));
+      atomicAdd(P.ws.stats + kStatEmitted, static_cast<unsigned long long>(acc + 1));
+      if (kb == 0) atomicAdd(P.ws.stats + kStatSpecOff, 1ull);
+      if (zero_resid) atomicAdd(P.ws.stats + kStatZeroResidual, 1ull);
+    } else {
+      atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
+      unsigned bits = static_cast<unsigned>(err & (kErrBadTok | kErrNonfin | kErrTime));
+      if (!bits) bits = kErrNonfin;   // no token could be drawn
+      atomicOr(P.ws.err_word, bits);
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
-// Memory-model helpers: counters and flags shared between CTAs.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-  asm volatile("st.release.gpu.global.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ float4 ld_relaxed_f4(const float4* p) {
-  float4 v;
-  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 ld_relaxed_f2(const float2* p) {
-  float2 v;
-  asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ float ld_relaxed_f(const float* p) {
-  float v;
-  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_relaxed_i(const int* p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
+// rows_stats_kernel: every needed row, 64 KB piece by piece
 // ---------------------------------------------------------------------------
 
 template <int ELT, bool GREEDY>
-struct Pieces {
+struct RowStats {
   using V = Vec<ELT>;
   static constexpr int NV = V::N;
+  static constexpr int kPieceElems = kChunkBytes / ELT;
+  static constexpr int kSegElems = kRStatVecs * 32 * NV;      // logits per warp segment
 
   const VerifyParams& P;
-  PCtrl& C;
+  RCtrl& C;
   unsigned char* ring;
   const int lane, warp;
   const long long row_bytes;
+  int u0, u1;                  // this CTA's pieces [u0, u1) of rows * np, in row order
 
-  __device__ Pieces(const VerifyParams& p, PCtrl& c, unsigned char* r, int ln, int wp)
-      : P(p), C(c), ring(r), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * ELT) {}
-
-  __device__ const unsigned char* trow(int b, int pos) const {
-    return static_cast<const unsigned char*>(P.target) +
-           (static_cast<size_t>(b) * (P.k + 1) + pos) * static_cast<size_t>(row_bytes);
-  }
-  __device__ const unsigned char* drow(int b, int pos) const {
-    return static_cast<const unsigned char*>(P.draft) +
-           (static_cast<size_t>(b) * P.k + pos) * static_cast<size_t>(row_bytes);
-  }
-  __device__ int row_index(int b, int pos, int kind) const {
-    return kind == 0 ? b * (P.k + 1) + pos : P.B * (P.k + 1) + b * P.k + pos;
+  __device__ RowStats(const VerifyParams& p, RCtrl& c, unsigned char* r, int ln, int wp)
+      : P(p), C(c), ring(r), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * p.elt) {
+    const long long units = static_cast<long long>(__ldcg(p.pw.rowoff + p.B)) * p.np;
+    u0 = static_cast<int>(units * blockIdx.x / gridDim.x);
+    u1 = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
   }
 
-  __device__ bool warp_wait(uint64_t* bar, uint32_t parity) const {
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait_bounded(bar, parity, kDrainLimitNs) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok && lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-    __syncwarp();
-    return ok != 0;
-  }
-
-  // ======================= producer ==========================================
-
-  // Stream unit t of the work list: (b, k_b, pos, kind, piece).
-  __device__ void map_unit(int t, int& b, int& kb, int& pos, int& kind, int& piece) const {
-    int L = P.k;
-    while (L > 0 && t >= C.gunits[L] + C.gcount[L] * (GREEDY ? L + 1 : 2 * L + 1) * P.np) --L;
-    const int per = (GREEDY ? L + 1 : 2 * L + 1) * P.np;
-    const int off = t - C.gunits[L];
-    const int n = C.gstart[L] + off / per;
-    const int local = off - (off / per) * per;
-    const int row = local / P.np;
-    piece = local - row * P.np;
-    b = C.seq_b[n];
-    kb = L;
-    if (GREEDY) { pos = row; kind = 0; }
-    else if (row < 2 * L) { pos = row >> 1; kind = row & 1; }
-    else { pos = L; kind = 0; }
-  }
-
-  __device__ bool acquire_slot(int q) {
-    return warp_wait(&C.empty[q % kPiecesStages], ((q / kPiecesStages) & 1) ^ 1);
-  }
-
-  // Stream unit t into slot q.
-  __device__ void issue_stream(int q, int t) {
-    int b, kb, pos, kind, piece;
-    map_unit(t, b, kb, pos, kind, piece);
-    const int slot = q % kPiecesStages;
-    const int e0 = piece * P.pe;
-    const int n = min(P.pe, P.V - e0);
-    const int nbytes = n * ELT;
-    if (lane == 0) {
-      PDesc& d = C.desc[slot];
-      d.b = b; d.kb = kb; d.pos = pos; d.kind = kind;
-      d.piece = piece; d.nbytes = nbytes; d.r = row_index(b, pos, kind); d.x = -1;
-      const unsigned char* src = (kind == 0 ? trow(b, pos) : drow(b, pos)) + static_cast<size_t>(e0) * ELT;
-      mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(nbytes));
-      bulk_load(ring + static_cast<size_t>(slot) * kChunkBytes, src, static_cast<uint32_t>(nbytes), &C.full[slot]);
-    }
-    __syncwarp();
-  }
-
-  // Re-read piece j of sequence b's rejected pair (lane 0; its message was
-  // acquired, so the pair's record is visible).
-  __device__ void issue_resid(int q, int b, int j) {
-    const int slot = q % kPiecesStages;
-    if (lane == 0) {
-      int4 ent;
-      asm volatile("ld.relaxed.gpu.global.v4.s32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(ent.x), "=r"(ent.y), "=r"(ent.z), "=r"(ent.w) : "l"(P.pw.rq + b) : "memory");
-      const float4 nrm = ld_relaxed_f4(P.pw.rqn + b);
-      const int a = ent.x;
-      const int e0 = j * P.he;
-      const int n = min(P.he, P.V - e0);
-      const int nbytes = n * ELT;
-      PDesc& d = C.desc[slot];
-      d.b = b; d.kb = ent.y; d.pos = a; d.kind = 2;
-      d.piece = j; d.nbytes = nbytes; d.r = b; d.x = -1;
-      d.K0 = nrm.x; d.L0 = nrm.y; d.G0 = nrm.z; d.G1 = nrm.w;
-      unsigned char* dst = ring + static_cast<size_t>(slot) * kChunkBytes;
-      mbar_expect_tx(&C.full[slot], static_cast<uint32_t>(2 * nbytes));
-      bulk_load(dst, trow(b, a) + static_cast<size_t>(e0) * ELT, static_cast<uint32_t>(nbytes), &C.full[slot]);
-      bulk_load(dst + kHalf, drow(b, a) + static_cast<size_t>(e0) * ELT, static_cast<uint32_t>(nbytes),
-                &C.full[slot]);
-    }
-    __syncwarp();
-  }
-
-  // The producer fills one slot at a time: with a re-read piece if one was
-  // handed to this CTA (the draws of decided sequences come first), else
-  // with its next stream unit (blockIdx.x, then every gridDim.x-th).  It
-  // reads its mailbox's count every fourth slot, using the value requested
-  // four slots earlier, so that no global load stalls it while the ring has
-  // room.
   __device__ void produce() {
-    int q = 0;
-    int t = blockIdx.x;
-    const int G = gridDim.x;
-    int mt = 0, mt_req = 0, mhead = 0;  // lane 0: mailbox count known, requested; messages taken
-    int* mtail = P.pw.mtail + blockIdx.x * 32;
-    const int* mbox = P.pw.mbox + static_cast<size_t>(blockIdx.x) * P.pw.mcap;
-    bool stream_open = true;
-    unsigned long long idle_since = 0;
-    while (true) {
-      if (!acquire_slot(q)) break;
-      int msg = 0;
-      if (lane == 0 && mhead < mt) {
-        // the slot was counted before the message was written: wait for it
-        const unsigned long long t0 = global_ns();
-        while ((msg = ld_acquire(mbox + mhead)) == 0) {
-          if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
-            atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-            msg = -1;
-            break;
-          }
-          __nanosleep(32);
-        }
-        ++mhead;
+    const uint64_t first_out = evict_first_policy();
+    int r_cur = -1;
+    int4 rt = make_int4(0, 0, 0, -1);
+    for (int u = u0, q = 0; u < u1; ++u, ++q) {
+      const int r = u / P.np, j = u - r * P.np;
+      if (r != r_cur) {   // one load per row, while the slots keep the consumers busy
+        rt = __ldcg(P.pw.rowtab + r);
+        r_cur = r;
       }
-      msg = __shfl_sync(0xffffffffu, msg, 0);
-      bool issued = false;
-      if (msg > 0) {
-        const int m = msg - 1;
-        issue_resid(q, m / P.nr, m - (m / P.nr) * P.nr);
-        issued = true;
-      } else if (stream_open && t < C.total_units) {
-        issue_stream(q, t);
-        t += G;
-        issued = true;
-      }
-      if (issued) {
-        if (lane == 0 && (q & 3) == 3) { mt = max(mt, mt_req); mt_req = ld_relaxed_i(mtail); }
-        ++q;
-        idle_since = 0;
-        continue;
-      }
-      stream_open = false;
-      // nothing for this slot yet: done once every sequence is settled
-      int settled = 0;
-      if (lane == 0) {
-        mt = max(mt, ld_relaxed_i(mtail));
-        settled = ld_relaxed_i(P.pw.ctr + kCtrSettled);
-      }
-      settled = __shfl_sync(0xffffffffu, settled, 0);
-      if (settled >= C.n_valid) break;
-      if (!idle_since) idle_since = global_ns();
-      if (static_cast<long long>(global_ns() - idle_since) > kDrainLimitNs) {
+      const int s = q % kRStages;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&C.empty[s], ((q / kRStages) & 1) ^ 1, kDrainLimitNs) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
         if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-        break;
+        return;   // the consumers time out on the slots left and flag their pieces
       }
-      __nanosleep(200);
-    }
-    // one end marker per control warp (also after an error, so that every
-    // warp stops)
-    for (int i = 0; i < kCtlWarps; ++i) {
-      if (!acquire_slot(q)) break;
       if (lane == 0) {
-        C.desc[q % kPiecesStages].kind = -1;
-        mbar_arrive(&C.full[q % kPiecesStages]);
+        const int pos = rt.z & 0xffff, kind = rt.z >> 16;
+        const long long off = static_cast<long long>(j) * kChunkBytes;
+        const int bytes = static_cast<int>(min(static_cast<long long>(kChunkBytes), row_bytes - off));
+        RDesc& d = C.desc[s];
+        d.u = u - u0; d.rec = u; d.part = j; d.bytes = bytes;
+        d.b = rt.x; d.kb = rt.y; d.pos = pos; d.kind = kind; d.x = rt.w;
+        mbar_expect_tx(&C.full[s], static_cast<uint32_t>(bytes));
+        bulk_load_hint(ring + static_cast<size_t>(s) * kChunkBytes, row_ptr(P, rt.x, pos, kind) + off,
+                       static_cast<uint32_t>(bytes), &C.full[s], first_out);
       }
       __syncwarp();
-      ++q;
     }
   }
-
-  // ======================= consumers =========================================
 
   __device__ void consume() {
     const float c2 = P.c2;
-    int q = 0, ends = 0;
-    while (true) {
-      const int slot = q % kPiecesStages;
-      const uint32_t par = static_cast<uint32_t>(q / kPiecesStages) & 1u;
-      int timed_out = 0;
-      if (!mbar_wait_bounded(&C.full[slot], par, P.wait_limit_ns)) {
-        timed_out = 1;
-        if (!mbar_wait_bounded(&C.full[slot], par, kDrainLimitNs)) {
+    for (int u = u0, q = 0; u < u1; ++u, ++q) {
+      const int s = q % kRStages;
+      int flags = 0;
+      if (!mbar_wait_bounded(&C.full[s], static_cast<uint32_t>(q / kRStages) & 1u, P.wait_limit_ns)) {
+        flags |= kFTimeout;
+        if (!mbar_wait_bounded(&C.full[s], static_cast<uint32_t>(q / kRStages) & 1u, kDrainLimitNs)) {
           if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
           return;   // the producer is gone
         }
       }
-      const PDesc d = C.desc[slot];
-      const int ubi = q % kUBufs;
-      if (!warp_wait(&C.ufree[ubi], ((q / kUBufs) & 1) ^ 1)) return;
-      UBuf& U = C.ub[ubi];
-      const unsigned char* data = ring + static_cast<size_t>(slot) * kChunkBytes;
-      if (d.kind < 0) {
-        __syncwarp();
-        if (lane == 0) {
-          if (warp == 0) U.d = d;
-          mbar_arrive(&C.empty[slot]);
-          mbar_arrive(&C.ufull[ubi]);
-        }
-        ++q;
-        // one end marker per control warp: stop after the last
-        if (++ends == kCtlWarps) return;
-        continue;
-      }
-      float4 out;
-      if (d.kind == 2) {
-        const int nvec = (d.nbytes + 15) / 16;
-        uint4 rt[kHalfVecsPerLane], rd[kHalfVecsPerLane];
+      const RDesc d = C.desc[s];
+      const unsigned char* data = ring + static_cast<size_t>(s) * kChunkBytes;
+      const int nvec = (d.bytes + 15) / 16;
+      uint4 raw[kRStatVecs];
 #pragma unroll
-        for (int j = 0; j < kHalfVecsPerLane; ++j) {
-          const int v = warp * kHalfVecsPerWarp + j * 32 + lane;
-          const bool in = v < nvec;
-          rt[j] = in ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
-          rd[j] = in ? *reinterpret_cast<const uint4*>(data + kHalf + static_cast<size_t>(v) * 16) : V::neg_inf();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&C.empty[slot]);
-        const f2 cc = pack2(c2, c2), nkt = pack2(-d.K0, -d.K0), nlt = pack2(-d.L0, -d.L0);
-        const f2 gh = pack2(d.G0, d.G0), gl = pack2(d.G1, d.G1);
-        f2 accr[NV / 2], accp[NV / 2];
-#pragma unroll
-        for (int i = 0; i < NV / 2; ++i) { accr[i] = 0ull; accp[i] = 0ull; }
-#pragma unroll
-        for (int j = 0; j < kHalfVecsPerLane; ++j) {
-          f2 zt[NV / 2], zd[NV / 2];
-          V::pairs(rt[j], zt);
-          V::pairs(rd[j], zd);
-#pragma unroll
-          for (int i = 0; i < NV / 2; ++i) {
-            f2 p;
-            float w0, w1;
-            resid_weight2(zt[i], zd[i], cc, nkt, nlt, gh, gl, p, w0, w1);
-            accr[i] = add2(accr[i], pack2(w0, w1));
-            accp[i] = add2(accp[i], p);
-          }
-        }
-        float a0, a1, sr = 0.f, sp = 0.f;
-#pragma unroll
-        for (int i = 0; i < NV / 2; ++i) {
-          unpack2(accr[i], a0, a1); sr += a0 + a1;
-          unpack2(accp[i], a0, a1); sp += a0 + a1;
-        }
-        out = make_float4(warp_sum(sr), warp_sum(sp), 0.f, __int_as_float(timed_out ? 2 : 0));
-      } else {
-        const int nvec = (d.nbytes + 15) / 16;
-        uint4 raw[kVecsPerLane];
-#pragma unroll
-        for (int j = 0; j < kVecsPerLane; ++j) {
-          const int v = warp * kVecsPerWarp + j * 32 + lane;
-          raw[j] = v < nvec ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&C.empty[slot]);
-        int bad = 0;
-        if (GREEDY) {
-          const int base = d.piece * P.pe + warp * kVecsPerWarp * NV;
-          float lm = -INFINITY;
-          int li = 0x7fffffff;
-#pragma unroll
-          for (int j = 0; j < kVecsPerLane; ++j) {
-            float z[NV];
-            V::unpack(raw[j], z);
-#pragma unroll
-            for (int e = 0; e < NV; ++e) {
-              bad |= (z[e] != z[e]) || (z[e] == INFINITY);
-              if (z[e] > lm) { lm = z[e]; li = base + (j * 32 + lane) * NV + e; }
-            }
-          }
-          warp_argmax(lm, li);
-          bad = warp_or(bad);
-          out = make_float4(lm, __int_as_float(li), 0.f, __int_as_float(bad | (timed_out ? 2 : 0)));
-        } else {
-          // the lane's (fl(m c), sum 2^(z c - K)), then the warp's
-          const float lm = V::vmax(raw);
-          float ks = -INFINITY, ls = 0.f;
-          if (lm > -INFINITY) {
-            ks = __fmul_rn(lm, c2);
-            const f2 cc = pack2(c2, c2), nk = pack2(-ks, -ks);
-            f2 acc[NV / 2];
-#pragma unroll
-            for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
-#pragma unroll
-            for (int j = 0; j < kVecsPerLane; ++j) {
-              f2 z[NV / 2];
-              V::pairs(raw[j], z);
-#pragma unroll
-              for (int i = 0; i < NV / 2; ++i) acc[i] = add2(acc[i], exp2_2(fma2(z[i], cc, nk)));
-            }
-            float a0, a1;
-#pragma unroll
-            for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); ls += a0 + a1; }
-          } else {
-            // no finite logit in this lane's part: only NaN can still hide here
-#pragma unroll
-            for (int j = 0; j < kVecsPerLane; ++j) {
-              float z[NV];
-              V::unpack(raw[j], z);
-#pragma unroll
-              for (int e = 0; e < NV; ++e) bad |= (z[e] != z[e]);
-            }
-          }
-          // NaN logits make ls NaN, +inf makes lm (and ks) +inf: both caught here
-          bad |= !(ls == ls) || lm == INFINITY;
-          const float wm = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(lm == lm ? lm : -INFINITY)));
-          const float wk = wm > -INFINITY ? __fmul_rn(wm, c2) : -INFINITY;
-          const float ws = warp_sum(ks > -INFINITY && ls == ls ? ls * fast_exp2(__fsub_rn(ks, wk)) : 0.f);
-          bad = warp_or(bad);
-          out = make_float4(wm, wk, ws, __int_as_float(bad | (timed_out ? 2 : 0)));
-        }
-      }
-      if (lane == 0) {
-        U.w[warp] = out;
-        if (warp == 0) U.d = d;
-        mbar_arrive(&C.ufull[ubi]);
+      for (int jj = 0; jj < kRStatVecs; ++jj) {
+        const int v = warp * (kRStatVecs * 32) + jj * 32 + lane;
+        raw[jj] = v < nvec ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
       }
       __syncwarp();
-      ++q;
-    }
-  }
+      if (lane == 0) mbar_arrive(&C.empty[s]);
 
-  // ======================= control warps =====================================
-
-  // Push a job for this control warp's decider (bounded wait while its ring
-  // is full).
-  __device__ void push_job(int cw, const Job& jb) {
-    if (lane == 0) {
-      const int slot = C.job_tail[cw]++;
-      const unsigned long long t0 = global_ns();
-      while (slot - C.job_head[cw] >= kJobs) {
-        if (static_cast<long long>(global_ns() - t0) > kDrainLimitNs) {
-          atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-          break;
-        }
-        __nanosleep(64);
-      }
-      C.jobs[cw][slot % kJobs] = jb;
-      __threadfence_block();
-      C.job_ready[cw][slot % kJobs] = slot + 1;
-    }
-    __syncwarp();
-  }
-
-  __device__ void control(int cw) {
-    const float c2 = P.c2;
-    for (int u = cw;; u += kCtlWarps) {
-      const int ubi = u % kUBufs;
-      if (!warp_wait(&C.ufull[ubi], static_cast<uint32_t>(u / kUBufs) & 1u)) {
-        Job jb{};
-        jb.kind = kJobEnd;
-        push_job(cw, jb);
-        return;
-      }
-      const UBuf& U = C.ub[ubi];
-      const PDesc d = U.d;
-      const float4 w = lane < kConsumerWarps ? U.w[lane] : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&C.ufree[ubi]);
-      if (d.kind < 0) {
-        Job jb{};
-        jb.kind = kJobEnd;
-        push_job(cw, jb);
-        return;
-      }
-      const bool in = lane < kConsumerWarps;
-      const int wbad = in ? __float_as_int(w.w) : 0;
-      const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(wbad)));
-      if (d.kind == 2) {
-        // a re-read piece: the per-segment masses, then the pair's counter
-        float* rm = P.pw.rmass + (static_cast<size_t>(d.b) * P.nr + d.piece) * kSegs;
-        float* pm = P.pw.pmass + (static_cast<size_t>(d.b) * P.nr + d.piece) * kSegs;
-        if (in) { rm[lane] = w.x; pm[lane] = w.y; }
-        __threadfence();       // every lane's stores before lane 0's release below
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) {
-          if (bad) atomicOr(P.pw.rflag + d.b, bad);
-          old = atom_add_acq_rel(P.pw.rcnt + d.b, 1);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == P.nr - 1) {
-          Job jb{};
-          jb.kind = kJobResid; jb.b = d.b; jb.pos = d.pos; jb.r = d.r; jb.pad0 = d.kb;
-          push_job(cw, jb);
-        }
-        continue;
-      }
-      float4 part;
+      const int seg_base = d.part * kPieceElems + warp * kSegElems;
+      WPart wp;
       if (GREEDY) {
-        const float M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(in ? w.x : -INFINITY)));
-        const int arg = __reduce_min_sync(0xffffffffu, (in && w.x == M) ? __float_as_int(w.y) : 0x7fffffff);
-        part = make_float4(M, __int_as_float(arg), 0.f, __int_as_float(bad));
-      } else {
-        const float M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(in ? w.x : -INFINITY)));
-        const float K = M > -INFINITY ? __fmul_rn(M, c2) : -INFINITY;
-        float v = (in && w.y > -INFINITY) ? w.z * fast_exp2(__fsub_rn(w.y, K)) : 0.f;
+        float lm = -INFINITY;
+        int li = 0x7fffffff, bad = 0;
 #pragma unroll
-        for (int o = kConsumerWarps / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        part = make_float4(M, K, __shfl_sync(0xffffffffu, v, 0), __int_as_float(bad));
-        if (d.kind == 0 && d.pos == d.kb && in) {
-          // bonus row: each consumer warp's segment (K, S), for the draw
-          P.pw.bseg[(static_cast<size_t>(d.b) * P.np + d.piece) * kSegs + lane] = make_float2(w.y, w.z);
-          __threadfence();     // before lane 0's release below
-        }
-      }
-      __syncwarp();
-      // the piece's part, then the sequence's counter: the last piece
-      // decides the sequence
-      int old = 0;
-      if (lane == 0) {
-        P.pw.rowpart[static_cast<size_t>(d.r) * P.np + d.piece] = part;
-        old = atom_add_acq_rel(P.pw.seqcnt + d.b, 1);
-      }
-      old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == (GREEDY ? d.kb + 1 : 2 * d.kb + 1) * P.np - 1) {
-        Job jb{};
-        jb.kind = kJobSeq; jb.b = d.b; jb.pad0 = d.kb;
-        push_job(cw, jb);
-      }
-    }
-  }
-
-  // ======================= decider warp ======================================
-
-  __device__ void finish_outputs(int b, int kb, int a, int y, int err, int zero_resid) {
-    const int k = P.k;
-    int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
-    const bool ok = !err && y >= 0;
-    for (int j = lane; j <= k; j += 32) {
-      int v = -1;
-      if (ok) v = j < a ? P.tokens[static_cast<size_t>(b) * k + j] : (j == a ? y : -1);
-      ot[j] = v;
-    }
-    if (lane == 0) {
-      P.out_len[b] = ok ? a + 1 : 0;
-      if (ok) {
-        atomicAdd(P.ws.stats + kStatSequences, 1ull);
-        atomicAdd(P.ws.stats + kStatProposed, static_cast<unsigned long long>(kb));
-        atomicAdd(P.ws.stats + kStatAccepted, static_cast<unsigned long long>(a));
-        atomicAdd(P.ws.stats + kStatEmitted, static_cast<unsigned long long>(a + 1));
-        if (kb == 0) atomicAdd(P.ws.stats + kStatSpecOff, 1ull);
-        if (zero_resid) atomicAdd(P.ws.stats + kStatZeroResidual, 1ull);
-      } else {
-        atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
-        unsigned bits = static_cast<unsigned>(err & (kErrBadTok | kErrNonfin | kErrTime));
-        if (!bits) bits = kErrNonfin;    // no token could be drawn
-        atomicOr(P.ws.err_word, bits);
-      }
-      __threadfence();
-      atomicAdd(P.pw.ctr + kCtrSettled, 1);
-    }
-    __syncwarp();
-  }
-
-  // The segment holding target weight t among n weights (index order),
-  // fp64 running sums; past the end (rounding): the last positive one.
-  // Returns the segment and what is left of t at its start.
-  __device__ int locate(const double* wts, int n, double t, double& seg_t) const {
-    const int per = (n + 31) / 32;
-    const int g0 = min(n, lane * per), g1 = min(n, g0 + per);
-    double gs = 0.0;
-    for (int i = g0; i < g1; ++i) gs += wts[i];
-    const double incl = warp_incl_scan(gs, lane);
-    const double excl = incl - gs;
-    const unsigned hit = __ballot_sync(0xffffffffu, gs > 0.0 && t < incl);
-    const unsigned posg = __ballot_sync(0xffffffffu, gs > 0.0);
-    const int owner = hit ? (__ffs(hit) - 1) : (posg ? 31 - __clz(posg) : -1);
-    int seg = -1;
-    double st = 0.0;
-    if (owner >= 0 && lane == owner) {
-      double run = excl, last_run = excl;
-      int last = -1;
-      for (int i = g0; i < g1; ++i) {
-        const double m = wts[i];
-        if (m > 0.0) { last = i; last_run = run; }
-        if (seg < 0 && m > 0.0 && t < run + m) { seg = i; st = t - run; }
-        run += m;
-      }
-      if (seg < 0) { seg = last; st = t - last_run; }
-    }
-    if (owner >= 0) {
-      seg = __shfl_sync(0xffffffffu, seg, owner);
-      st = __shfl_sync(0xffffffffu, st, owner);
-    }
-    seg_t = st;
-    return seg;
-  }
-
-  // Vector v of a row, -inf past the row.
-  __device__ uint4 load_vec(const unsigned char* row, int v, int v_end) const {
-    if (v >= v_end || v < 0) return V::neg_inf();
-    return __ldg(reinterpret_cast<const uint4*>(row) + v);
-  }
-
-  // Walk NSTEPS x 32 vectors from vector v0, none at or past v_end (the end
-  // of the piece the segment belongs to), a warp inclusive scan per step, to
-  // the token where the running weight passes t.  RESID: weights
-  // max(0, p - q); else p.  Same arithmetic as the consumers' weights.
-  template <int NSTEPS, bool RESID>
-  __device__ int walk(int v0, int v_end, double t, const unsigned char* rowT, const unsigned char* rowD,
-                                   float Kt, float Lt, float Gh, float Gl) const {
-    uint4 rt[NSTEPS], rd[RESID ? NSTEPS : 1];
-#pragma unroll
-    for (int j = 0; j < NSTEPS; ++j) {
-      rt[j] = load_vec(rowT, v0 + j * 32 + lane, v_end);
-      if (RESID) rd[RESID ? j : 0] = load_vec(rowD, v0 + j * 32 + lane, v_end);
-    }
-    double base = 0.0;
-    int found = -1, last_positive = -1;
-#pragma unroll
-    for (int j = 0; j < NSTEPS; ++j) {
-      float w[NV], zt[NV], zd[NV];
-      V::unpack(rt[j], zt);
-      if (RESID) V::unpack(rd[RESID ? j : 0], zd);
-      float ls = 0.f;
-#pragma unroll
-      for (int e = 0; e < NV; ++e) {
-        float p;
-        if (RESID) w[e] = resid_weight(zt[e], zd[e], P.c2, Kt, Lt, Gh, Gl, p);
-        else w[e] = fast_exp2(__fsub_rn(__fmaf_rn(zt[e], P.c2, -Kt), Lt));
-        ls += w[e];
-      }
-      const float incl = warp_incl_scan(ls, lane);
-      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) excl = 0.f;
-      const float step_total = __shfl_sync(0xffffffffu, incl, 31);
-      const int x0 = (v0 + j * 32 + lane) * NV;
-      const bool mine = found < 0 && ls > 0.f && t < base + static_cast<double>(incl) &&
-                        !(t < base + static_cast<double>(excl));
-      const unsigned hit = __ballot_sync(0xffffffffu, mine);
-      int lp = -1;
-#pragma unroll
-      for (int e = 0; e < NV; ++e) if (w[e] > 0.f) lp = x0 + e;
-      const unsigned anyp = __ballot_sync(0xffffffffu, lp >= 0);
-      if (found < 0 && anyp) last_positive = __shfl_sync(0xffffffffu, lp, 31 - __clz(anyp));
-      if (hit) {
-        const int hl = __ffs(hit) - 1;
-        int pick = -1;
-        if (lane == hl) {
-          double c = base + static_cast<double>(excl);
-          int lastp = -1;
+        for (int jj = 0; jj < kRStatVecs; ++jj) {
+          float z[NV];
+          V::unpack(raw[jj], z);
 #pragma unroll
           for (int e = 0; e < NV; ++e) {
-            if (w[e] > 0.f) lastp = x0 + e;
-            c += static_cast<double>(w[e]);
-            if (pick < 0 && w[e] > 0.f && t < c) pick = x0 + e;
+            bad |= (z[e] != z[e]) || (z[e] == INFINITY);
+            if (z[e] > lm) { lm = z[e]; li = seg_base + (jj * 32 + lane) * NV + e; }
           }
-          if (pick < 0) pick = lastp;
         }
-        found = __shfl_sync(0xffffffffu, pick, hl);
-      }
-      base += static_cast<double>(step_total);
-    }
-    return found >= 0 ? found : last_positive;
-  }
-
-  // Every piece of sequence b is reduced: its rows, tests, first rejection,
-  // and the bonus draw or the re-read of the rejected pair.
-  __device__ void seq_done(int b, int kb) {
-    const float c2 = P.c2;
-    const int np = P.np, k1 = P.k + 1;
-    const int nrows = GREEDY ? kb + 1 : 2 * kb + 1;
-    typename PCtrl::Dec& S = C.dec[dw];
-    fence_acq_rel_gpu();
-    // row ri of the sequence (in streaming order): target row i = ri / 2
-    // (ri even) or draft row ri / 2 (ri odd); the bonus row is ri = 2 k_b
-    // (greedy: target row ri)
-    auto row_of = [&](int ri) {
-      if (GREEDY) return row_index(b, ri, 0);
-      return row_index(b, ri >> 1, ri & 1);
-    };
-    // what the tests and the bonus draw need, requested with the parts
-    int x = -1;
-    float u = 0.f;
-    if (lane < kb) {
-      x = __ldg(P.tokens + static_cast<size_t>(b) * P.k + lane);
-      if (!GREEDY) u = __ldg(P.uniforms + static_cast<size_t>(b) * k1 + lane);
-    }
-    const float s = GREEDY ? 0.f : __ldg(P.uniforms + static_cast<size_t>(b) * k1 + P.k);
-    const int nseg = np * kSegs;
-    float2 bs[kMaxChunks * kSegs / 32];
+        warp_argmax(lm, li);
+        flags |= __reduce_or_sync(0xffffffffu, static_cast<unsigned>(bad)) ? kFBad : 0;
+        wp.m = lm; wp.s = __int_as_float(li); wp.zx = 0.f; wp.flags = flags;
+      } else {
+        // the drafted token's logit, if it lies in this warp's segment
+        float zx = 0.f;
+        int has = 0;
+        if (d.x >= 0 && d.x < P.V) {
+          const int rel = d.x - seg_base;
+          if (rel >= 0 && rel < kSegElems) {
+            const int vv = rel / NV, jj = vv >> 5, e = rel - vv * NV;
+            float zz = 0.f;
+            if ((vv & 31) == lane) {
 #pragma unroll
-    for (int i = 0; i < kMaxChunks * kSegs / 32; ++i) {
-      const int sg = lane + 32 * i;
-      bs[i] = (!GREEDY && sg < nseg) ? ld_relaxed_f2(P.pw.bseg + static_cast<size_t>(b) * nseg + sg)
-                                     : make_float2(-INFINITY, 0.f);
-    }
-    // every row's (M, K, S, L) from its pieces in piece order, rows taken
-    // kScratch / np at a time through shared memory
-    const int per = kScratch / np;
-    float zt_x = 0.f, zd_x = 0.f;    // the drafted tokens' logits (lane i: draft i)
-    for (int r0 = 0; r0 < nrows; r0 += per) {
-      const int r1 = min(nrows, r0 + per);
-      __syncwarp();
-      for (int i = lane; i < (r1 - r0) * np; i += 32)
-        S.part[i] = ld_relaxed_f4(P.pw.rowpart + static_cast<size_t>(row_of(r0 + i / np)) * np + i % np);
-      __syncwarp();
-      if (r0 == 0 && !GREEDY && lane < kb && x >= 0 && x < P.V) {
-        // requested here, used after the combines below
-        zt_x = V::scalar(trow(b, lane), x);
-        zd_x = V::scalar(drow(b, lane), x);
-      }
-      for (int ri = r0 + lane; ri < r1; ri += 32) {
-        const float4* pp = S.part + (ri - r0) * np;
+              for (int j2 = 0; j2 < kRStatVecs; ++j2) {
+                if (j2 == jj) {
+                  float z[NV];
+                  V::unpack(raw[j2], z);
+#pragma unroll
+                  for (int e2 = 0; e2 < NV; ++e2) if (e2 == e) zz = z[e2];
+                }
+              }
+            }
+            zx = __shfl_sync(0xffffffffu, zz, vv & 31);
+            has = 1;
+          }
+        }
+        const float lm = V::vmax(raw);
+        float ks = -INFINITY, ls = 0.f;
         int bad = 0;
-        float4 st;
-        if (GREEDY) {
-          float M = -INFINITY;
-          int arg = 0x7fffffff;
-          for (int j = 0; j < np; ++j) {
-            bad |= __float_as_int(pp[j].w);
-            if (pp[j].x > M) { M = pp[j].x; arg = __float_as_int(pp[j].y); }   // pieces in order: ties keep the first
-          }
-          st = make_float4(M, __int_as_float(arg), 0.f, 0.f);
-          bad = ((bad & 1) || !(M > -INFINITY) ? kErrNonfin : 0) | ((bad & 2) ? kErrTime : 0);
-        } else {
-          float M = -INFINITY;
-          for (int j = 0; j < np; ++j) { bad |= __float_as_int(pp[j].w); M = fmaxf(M, pp[j].x); }
-          const float K = M > -INFINITY ? __fmul_rn(M, c2) : -INFINITY;
-          float v = 0.f;
-          for (int j = 0; j < np; ++j) v += pp[j].y > -INFINITY ? pp[j].z * fast_exp2(__fsub_rn(pp[j].y, K)) : 0.f;
-          st = make_float4(M, K, v, log2f(v));
-          bad = ((bad & 1) || !(isfinite(M) && isfinite(v) && v > 0.f) ? kErrNonfin : 0) | ((bad & 2) ? kErrTime : 0);
-        }
-        S.row[ri] = st;
-        S.bad[ri] = bad;
-        // diagnostics
-        if (!P.diag) {
-        } else if (GREEDY) {
-          P.ws.m_t[static_cast<size_t>(b) * k1 + ri] = st.x;
-        } else if (ri & 1) {
-          P.ws.m_d[static_cast<size_t>(b) * P.k + (ri >> 1)] = st.x;
-          P.ws.L_d[static_cast<size_t>(b) * P.k + (ri >> 1)] = st.w;
-        } else {
-          P.ws.m_t[static_cast<size_t>(b) * k1 + (ri >> 1)] = st.x;
-          P.ws.L_t[static_cast<size_t>(b) * k1 + (ri >> 1)] = st.w;
-        }
-      }
-    }
-    if (!GREEDY && lane < kb) { S.zx[2 * lane] = zt_x; S.zx[2 * lane + 1] = zd_x; }
-    __syncwarp();
-    // the tests, lane i for draft i: alpha = min(1, 2^-delta) with
-    // delta = log2 (q(x) / p(x)) = (z_d(x) - z_t(x)) c + G, G the log2 ratio
-    // of the target's to the draft's normaliser
-    int err = 0;
-    for (int ri = lane; ri < nrows; ri += 32) err |= S.bad[ri];
-    bool reject = false;
-    float Gh = 0.f, Gl = 0.f;
-    if (lane < kb) {
-      if (x < 0 || x >= P.V) {
-        err |= kErrBadTok;
-      } else if (GREEDY) {
-        reject = x != __float_as_int(S.row[lane].y);
-        if (P.diag) P.ws.alpha[static_cast<size_t>(b) * P.k + lane] = reject ? 0.f : 1.f;
-      } else {
-        const float4 T = S.row[2 * lane], D = S.row[2 * lane + 1];
-        const float zt = S.zx[2 * lane], zd = S.zx[2 * lane + 1];
-        log2_ratio(T.y, T.z, D.y, D.z, Gh, Gl);
-        float alpha;
-        if (zt == -INFINITY) alpha = 0.f;               // p(x) = 0
-        else if (zd == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
-        else {
-          const float delta = __fadd_rn(__fmaf_rn(__fsub_rn(zd, zt), c2, Gh), Gl);
-          alpha = delta <= 0.f ? 1.f : exp2f(-delta);
-        }
-        if (P.diag) P.ws.alpha[static_cast<size_t>(b) * P.k + lane] = alpha;
-        reject = !(u < alpha);
-      }
-    }
-    err = warp_or(err);
-    const unsigned rej = __ballot_sync(0xffffffffu, reject);
-    const int a = rej ? __ffs(rej) - 1 : kb;
-    if (err) { finish_outputs(b, kb, a, -1, err, 0); return; }
-    if (GREEDY) {
-      finish_outputs(b, kb, a, __float_as_int(S.row[a].y), 0, 0);
-      return;
-    }
-    if (a < kb) {
-      // the rejected pair is read again in nr pieces, handed round-robin to
-      // the CTAs' mailboxes (piece j to CTA (b nr + j) mod ctas): the pair's
-      // record first, then one message per piece
-      Gh = __shfl_sync(0xffffffffu, Gh, a);
-      Gl = __shfl_sync(0xffffffffu, Gl, a);
-      if (lane == 0) {
-        const float4 T = S.row[2 * a];
-        P.pw.rq[b] = make_int4(a, kb, 0, 0);
-        P.pw.rqn[b] = make_float4(T.y, T.w, Gh, Gl);
-        __threadfence();
-      }
-      __syncwarp();
-      for (int j = lane; j < P.nr; j += 32) {
-        const int m = b * P.nr + j;
-        const int cta = m % P.ctas;
-        const int slot = atomicAdd(P.pw.mtail + cta * 32, 1);
-        st_release(P.pw.mbox + static_cast<size_t>(cta) * P.pw.mcap + slot, m + 1);
-      }
-      __syncwarp();
-      return;
-    }
-    // every draft accepted: the bonus token from p_{k_b}: the segment from
-    // the segment sums kept while streaming, then a walk of that segment
-    const float4 T = S.row[2 * kb];
-    double* seg_w = S.segw;
+        if (lm > -INFINITY) {
+          ks = __fmul_rn(lm, c2);      // fl(m c), used identically wherever rescaled
+          const f2 cc = pack2(c2, c2), nk = pack2(-ks, -ks);
+          f2 acc[NV / 2];
 #pragma unroll
-    for (int i = 0; i < kMaxChunks * kSegs / 32; ++i) {
-      const int sg = lane + 32 * i;
-      if (sg < nseg)
-        seg_w[sg] = bs[i].x == -INFINITY ? 0.0
-                    : static_cast<double>(bs[i].y) * static_cast<double>(fast_exp2(__fsub_rn(bs[i].x, T.y) - T.w));
-    }
-    __syncwarp();
-    double tot = 0.0;
-    for (int i = lane; i < nseg; i += 32) tot += seg_w[i];
-    tot = warp_sum(tot);
-    double seg_t;
-    const int seg = locate(seg_w, nseg, static_cast<double>(s) * tot, seg_t);
-    int y = -1;
-    if (seg >= 0) {
-      const int piece = seg / kSegs, sw = seg - piece * kSegs;
-      const int v0 = (piece * P.pe) / NV + sw * kVecsPerWarp;
-      const int v_end = min(P.V, (piece + 1) * P.pe) / NV;
-      y = walk<kVecsPerLane, false>(v0, v_end, seg_t, trow(b, kb), nullptr, T.y, T.w, 0.f, 0.f);
-    }
-    if (lane == 0 && P.diag) P.ws.mass[static_cast<size_t>(b) * k1 + kb] = static_cast<float>(tot);
-    finish_outputs(b, kb, kb, y, 0, 0);
-  }
-
-  // Every re-read piece of sequence b's rejected pair is reduced: the draw.
-  __device__ void resid_done(const Job& jb) {
-    const int b = jb.b, a = jb.pos;
-    const int k1 = P.k + 1;
-    fence_acq_rel_gpu();
-    double* rseg_w = C.dec[dw].segw;
-    const int nseg = P.nr * kSegs;
-    double r = 0.0;
-    for (int i = lane; i < nseg; i += 32) r += static_cast<double>(ld_relaxed_f(P.pw.rmass + static_cast<size_t>(b) * nseg + i));
-    const double rtot = warp_sum(r);
-    // exact arithmetic rules a zero residual out (a rejection implies p > q
-    // somewhere); if rounding leaves none, the draw is from p_a (counted)
-    const bool resid = rtot > 0.0;
-    const float* src = resid ? P.pw.rmass : P.pw.pmass;
-    for (int i = lane; i < nseg; i += 32) rseg_w[i] = static_cast<double>(ld_relaxed_f(src + static_cast<size_t>(b) * nseg + i));
-    __syncwarp();
-    double tot = 0.0;
-    for (int i = lane; i < nseg; i += 32) tot += rseg_w[i];
-    tot = warp_sum(tot);
-    const float s = P.uniforms[static_cast<size_t>(b) * k1 + P.k];
-    const float4 nrm = ld_relaxed_f4(P.pw.rqn + b);
-    int flag = 0;
-    if (lane == 0) flag = ld_relaxed_i(P.pw.rflag + b);
-    flag = __shfl_sync(0xffffffffu, flag, 0);
-    double seg_t;
-    const int seg = locate(rseg_w, nseg, static_cast<double>(s) * tot, seg_t);
-    int y = -1;
-    if (seg >= 0) {
-      const int piece = seg / kSegs, sw = seg - piece * kSegs;
-      const int v0 = (piece * P.he) / NV + sw * kHalfVecsPerWarp;
-      const int v_end = min(P.V, (piece + 1) * P.he) / NV;
-      if (resid)
-        y = walk<kHalfVecsPerLane, true>(v0, v_end, seg_t, trow(b, a), drow(b, a), nrm.x, nrm.y, nrm.z, nrm.w);
-      else
-        y = walk<kHalfVecsPerLane, false>(v0, v_end, seg_t, trow(b, a), nullptr, nrm.x, nrm.y, 0.f, 0.f);
-    }
-    if (lane == 0 && P.diag) P.ws.mass[static_cast<size_t>(b) * k1 + a] = static_cast<float>(tot);
-    finish_outputs(b, jb.pad0, a, y, (flag & 2) ? kErrTime : 0, resid ? 0 : 1);
-  }
-
-  int dw = 0;   // decider warp index (its job ring and scratch)
-
-  __device__ void decider(int d) {
-    dw = d;
-    int head = 0;
-    unsigned long long idle_since = 0;
-    while (true) {
-      int ready = 0;
-      if (lane == 0) ready = C.job_ready[dw][head % kJobs] == head + 1;
-      ready = __shfl_sync(0xffffffffu, ready, 0);
-      if (!ready) {
-        if (!idle_since) idle_since = global_ns();
-        if (static_cast<long long>(global_ns() - idle_since) > 8 * kDrainLimitNs) {
-          if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
-          return;
+          for (int i = 0; i < NV / 2; ++i) acc[i] = 0ull;
+#pragma unroll
+          for (int jj = 0; jj < kRStatVecs; ++jj) {
+            f2 z[NV / 2];
+            V::pairs(raw[jj], z);
+#pragma unroll
+            for (int i = 0; i < NV / 2; ++i) acc[i] = add2(acc[i], exp2_2(fma2(z[i], cc, nk)));
+          }
+          float a0, a1;
+#pragma unroll
+          for (int i = 0; i < NV / 2; ++i) { unpack2(acc[i], a0, a1); ls += a0 + a1; }
+        } else {
+          // no finite logit in this lane's part: only NaN can still hide here
+#pragma unroll
+          for (int jj = 0; jj < kRStatVecs; ++jj) {
+            float z[NV];
+            V::unpack(raw[jj], z);
+#pragma unroll
+            for (int e = 0; e < NV; ++e) bad |= (z[e] != z[e]);
+          }
         }
-        __nanosleep(64);
-        continue;
+        const float wM = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(lm)));
+        const float wK = wM > -INFINITY ? __fmul_rn(wM, c2) : -INFINITY;
+        const float wS = warp_sum(ks > -INFINITY ? ls * fast_exp2(__fsub_rn(ks, wK)) : 0.f);
+        flags |= (__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bad)) ? kFBad : 0) | (has ? kFHasZx : 0);
+        wp.m = wM; wp.s = wS; wp.zx = zx; wp.flags = flags;
+        if (d.kind == 0 && d.pos == d.kb && lane == 0)   // a bonus row: each segment's (fl(m c), sum) for its draw
+          P.pw.bseg[(static_cast<size_t>(d.b) * P.np + d.part) * kRWarps + warp] = make_float2(wK, wS);
       }
-      idle_since = 0;
-      __threadfence_block();
-      const Job jb = C.jobs[dw][head % kJobs];
-      __syncwarp();
-      if (lane == 0) C.job_head[dw] = head + 1;
-      ++head;
-      if (jb.kind == kJobEnd) {
-        return;                  // its control warp has stopped
-      } else if (jb.kind == kJobSeq) {
-        seq_done(jb.b, jb.pad0);
-      } else {
-        resid_done(jb);
+      // the last warp to finish the piece combines the warps' parts, in
+      // warp order, into the piece's record
+      const int buf = q % kRBufs;
+      int last = 0;
+      if (lane == 0) {
+        C.part[buf][warp] = wp;
+        __threadfence_block();
+        last = atomicAdd(&C.cnt[buf], 1) == kRWarps - 1 ? 1 : 0;
       }
-      __syncwarp();
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        __threadfence_block();
+        const bool in = lane < kRWarps;
+        const WPart pt = C.part[buf][in ? lane : 0];
+        const int fl = static_cast<int>(__reduce_or_sync(0xffffffffu, in ? static_cast<unsigned>(pt.flags) : 0u));
+        float4 rec;
+        if (GREEDY) {
+          float bv = in ? pt.m : -INFINITY;
+          int bi = in ? __float_as_int(pt.s) : 0x7fffffff;
+          warp_argmax(bv, bi);
+          rec = make_float4(bv, __int_as_float(bi), 0.f, __int_as_float(fl));
+        } else {
+          const float pm = in ? pt.m : -INFINITY;
+          const float M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(pm)));
+          const float K = M > -INFINITY ? __fmul_rn(M, c2) : -INFINITY;
+          const float pk = pm > -INFINITY ? __fmul_rn(pm, c2) : -INFINITY;
+          float sv = (in && pk > -INFINITY) ? pt.s * fast_exp2(__fsub_rn(pk, K)) : 0.f;
+#pragma unroll
+          for (int o = kRWarps / 2; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+          const unsigned hz = __ballot_sync(0xffffffffu, in && (pt.flags & kFHasZx));
+          const float zx = __shfl_sync(0xffffffffu, pt.zx, hz ? __ffs(hz) - 1 : 0);
+          rec = make_float4(M, __shfl_sync(0xffffffffu, sv, 0), zx, __int_as_float(fl));
+        }
+        if (lane == 0) {
+          P.pw.rec[d.rec] = rec;
+          C.cnt[buf] = 0;
+        }
+        __syncwarp();
+      }
     }
   }
 };
 
 template <int ELT, bool GREEDY>
-__global__ void __launch_bounds__(kPThreads, 1) verify_pieces_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(kRThreads, 1) rows_stats_kernel(const VerifyParams P) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  PCtrl& C = *reinterpret_cast<PCtrl*>(smem);
-  unsigned char* ring = smem + kPCtrlBytes;
+  RCtrl& C = *reinterpret_cast<RCtrl*>(smem);
+  unsigned char* ring = smem + kRCtrlBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    for (int s = 0; s < kPiecesStages; ++s) {
+    for (int s = 0; s < kRStages; ++s) {
       mbar_init(&C.full[s], 1);
-      mbar_init(&C.empty[s], kConsumerWarps);
+      mbar_init(&C.empty[s], kRWarps);
     }
-    for (int u = 0; u < kUBufs; ++u) {
-      mbar_init(&C.ufull[u], kConsumerWarps);
-      mbar_init(&C.ufree[u], 1);
-    }
-    for (int i = 0; i < kCtlWarps; ++i) { C.job_tail[i] = 0; C.job_head[i] = 0; }
+    for (int i = 0; i < kRBufs; ++i) C.cnt[i] = 0;
     fence_mbar_init();
   }
-  for (int j = tid; j < kCtlWarps * kJobs; j += kPThreads) C.job_ready[j / kJobs][j % kJobs] = 0;
-  grid_dependency_wait();             // plan_kernel: the work list, the counters
-  // the work list and its groups (draft length L, longest first)
-  const int n = __ldcg(P.ws.n_seqs);
-  for (int i = tid; i < n; i += kPThreads) C.seq_b[i] = __ldcg(&P.ws.seqs[i].x);
-  if (tid == 0) {
-    int start = 0, units = 0;
-    for (int L = P.k; L >= 0; --L) {
-      const int upto = __ldcg(P.pw.grp + L);          // sequences with k_b >= L
-      C.gstart[L] = start;
-      C.gunits[L] = units;
-      C.gcount[L] = upto - start;
-      units += (upto - start) * (GREEDY ? L + 1 : 2 * L + 1) * P.np;
-      start = upto;
+  __syncthreads();
+  grid_dependency_wait();      // the row table
+  grid_dependents_launch();
+  RowStats<ELT, GREEDY> k(P, C, ring, lane, warp);
+  if (warp == kRProducer) k.produce();
+  else k.consume();
+}
+
+// ---------------------------------------------------------------------------
+// rows_decide_kernel: one warp per work-list entry
+// ---------------------------------------------------------------------------
+
+// A row's numbers from its pieces' records (lane j holds piece j; np <= 32):
+// M the maximum, K = fl(M c), S = sum of the pieces' sums rescaled onto K (a
+// fixed butterfly), the drafted token's logit, the flags; greedy: M and the
+// first argmax.
+template <bool GREEDY>
+__device__ void merge_row(const VerifyParams& P, float4 rc, int lane, float& M, float& K, float& S, float& zx,
+                          int& flags, int& arg) {
+  const bool in = lane < P.np;
+  if (!in) rc = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  flags = static_cast<int>(__reduce_or_sync(0xffffffffu, in ? static_cast<unsigned>(__float_as_int(rc.w)) : 0u));
+  if (GREEDY) {
+    float bv = rc.x;
+    int bi = in ? __float_as_int(rc.y) : 0x7fffffff;
+    warp_argmax(bv, bi);
+    M = bv; arg = bi; K = 0.f; S = 0.f; zx = 0.f;
+    return;
+  }
+  // a NaN part is carried by the flags: the record's sum is NaN
+  const float pm = rc.x;
+  M = from_ordered_key(__reduce_max_sync(0xffffffffu, ordered_key(pm)));
+  K = M > -INFINITY ? __fmul_rn(M, P.c2) : -INFINITY;
+  const float pk = pm > -INFINITY ? __fmul_rn(pm, P.c2) : -INFINITY;
+  float sv = (in && pk > -INFINITY) ? rc.y * fast_exp2(__fsub_rn(pk, K)) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+  S = __shfl_sync(0xffffffffu, sv, 0);
+  const unsigned hz = __ballot_sync(0xffffffffu, in && (__float_as_int(rc.w) & kFHasZx));
+  zx = __shfl_sync(0xffffffffu, rc.z, hz ? __ffs(hz) - 1 : 0);
+  arg = 0;
+}
+
+template <int ELT, bool GREEDY>
+__global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const VerifyParams P) {
+  __shared__ float bmass[kRSmallThreads / 32][kMaxChunks * kRWarps];
+  grid_dependency_wait();      // the pieces' records
+  grid_dependents_launch();
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int b = blockIdx.x * (kRSmallThreads / 32) + wi;
+  if (b >= P.B) return;
+  const int r0 = __ldcg(P.pw.rowoff + b);
+  if (__ldcg(P.pw.rowoff + b + 1) == r0) return;   // an invalid k_b, answered by the plan
+  const int kb = __ldg(P.draft_len + b), k = P.k, t = b;
+  const float c2 = P.c2;
+  const bool diag = P.diag != 0;
+  const int xl = lane < kb ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
+  const float ul = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
+  const float s_samp = __shfl_sync(0xffffffffu, ul, k);
+  int a = -1, err = 0, y = -1;
+  float pK = 0.f, pS = 0.f, pzx = 0.f;                  // target row of the current pair
+  float aKt = 0.f, aLt = 0.f, aGh = 0.f, aGl = 0.f;     // the rejected pair's numbers
+  float bK = 0.f, bS = 0.f;                             // the bonus row
+  const int nrows = GREEDY ? kb + 1 : 2 * kb + 1;
+  const int np = P.np, nrec = nrows * np;
+  const float4* recs = P.pw.rec + static_cast<size_t>(r0) * np;
+  // the sequence's piece records, 32 at a time (one load per lane, all in
+  // flight together); row ri's records are lanes ri np - batch, ...
+  int batch = 0;
+  float4 held = lane < nrec ? __ldcg(recs + lane) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  for (int ri = 0; ri < nrows; ++ri) {
+    int pos, kind;
+    if (GREEDY) { pos = ri; kind = 0; }
+    else if (ri < 2 * kb) { pos = ri >> 1; kind = ri & 1; }
+    else { pos = kb; kind = 0; }
+    if (ri * np + np > batch + 32) {
+      batch = ri * np;
+      held = batch + lane < nrec ? __ldcg(recs + batch + lane) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
     }
-    C.n_valid = n;
-    C.total_units = units;
+    const int src = min(31, ri * np - batch + lane);
+    float4 rc;
+    rc.x = __shfl_sync(0xffffffffu, held.x, src);
+    rc.y = __shfl_sync(0xffffffffu, held.y, src);
+    rc.z = __shfl_sync(0xffffffffu, held.z, src);
+    rc.w = __shfl_sync(0xffffffffu, held.w, src);
+    float M, K, S, zx;
+    int fl, arg;
+    merge_row<GREEDY>(P, rc, lane, M, K, S, zx, fl, arg);
+    const int x = __shfl_sync(0xffffffffu, xl, pos < kb ? pos : 0);
+    if (fl & kFTimeout) err |= kErrTime;
+    if (pos < kb && (x < 0 || x >= P.V)) err |= kErrBadTok;
+    const size_t bt = static_cast<size_t>(b) * (k + 1) + pos, bd = static_cast<size_t>(b) * k + pos;
+    if (GREEDY) {
+      if ((fl & kFBad) || !(M > -INFINITY)) err |= kErrNonfin;
+      if (diag && lane == 0) P.ws.m_t[bt] = M;
+      if (pos < kb) {
+        const bool acc = (x == arg);
+        if (diag && lane == 0) P.ws.alpha[bd] = acc ? 1.f : 0.f;
+        if (!acc && a < 0) { a = pos; y = arg; }
+      } else if (a < 0) {
+        y = arg;
+      }
+      continue;
+    }
+    if ((fl & kFBad) || !(isfinite(M) && isfinite(S) && S > 0.f)) err |= kErrNonfin;
+    if (kind == 0) {
+      if (diag && lane == 0) { P.ws.m_t[bt] = M; P.ws.L_t[bt] = log2f(S); }
+      if (pos < kb) { pK = K; pS = S; pzx = zx; }
+      else { bK = K; bS = S; }
+    } else {
+      if (diag && lane == 0) { P.ws.m_d[bd] = M; P.ws.L_d[bd] = log2f(S); }
+      if (!err) {
+        // the acceptance test of draft pos (the cluster kernel's arithmetic):
+        // delta = (z_d(x) - z_t(x)) c + G, alpha = min(1, 2^-delta)
+        float Gh, Gl;
+        log2_ratio(pK, pS, K, S, Gh, Gl);
+        float alpha;
+        if (pzx == -INFINITY) alpha = 0.f;              // p(x) = 0
+        else if (zx == -INFINITY) alpha = 1.f;          // q(x) = 0 < p(x)
+        else {
+          const float delta = __fadd_rn(__fmaf_rn(__fsub_rn(zx, pzx), c2, Gh), Gl);
+          alpha = delta <= 0.f ? 1.f : exp2f(-delta);
+        }
+        if (diag && lane == 0) P.ws.alpha[bd] = alpha;
+        const float u = __shfl_sync(0xffffffffu, ul, pos);
+        if (!(u < alpha) && a < 0) {
+          a = pos;
+          aKt = pK; aLt = log2f(pS); aGh = Gh; aGl = Gl;
+        }
+      }
+    }
+  }
+  if (err || GREEDY) {
+    write_outputs(P, b, kb, a, err ? -1 : y, err, 0, lane);
+    return;
+  }
+  if (a >= 0) {
+    // the residual draw needs the pair read again: a job for the next kernels
+    int j = 0;
+    if (lane == 0) j = atomicAdd(P.pw.njobs, 1);
+    j = __shfl_sync(0xffffffffu, j, 0);
+    if (lane == 0) {
+      P.pw.job[j] = make_int4(t, b, a, kb);
+      P.pw.jobn[j] = make_float4(aKt, aLt, aGh, aGl);
+    }
+    return;
+  }
+  // every draft accepted: the bonus token from the bonus row's segment sums,
+  // then one segment read again
+  const float L = log2f(bS);
+  const int nseg = P.np * kRWarps;
+  float* wm = bmass[wi];
+  for (int g = lane; g < nseg; g += 32) {
+    const float2 sg = __ldcg(P.pw.bseg + static_cast<size_t>(b) * nseg + g);
+    wm[g] = sg.x == -INFINITY ? 0.f : sg.y * fast_exp2(__fsub_rn(sg.x, bK) - L);
+  }
+  __syncwarp();
+  float part = 0.f;
+  {
+    const int per = (nseg + 31) / 32;
+    const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
+    for (int g = g0; g < g1; ++g) part += wm[g];
+  }
+  const float tot = warp_sum(part);
+  int seg;
+  float seg_t;
+  locate_seg(wm, nseg, s_samp * tot, lane, seg, seg_t);
+  if (diag && lane == 0) P.ws.mass[static_cast<size_t>(b) * (k + 1) + kb] = tot;
+  const int nvec_row = static_cast<int>((static_cast<long long>(P.V) * ELT) / 16);
+  if (seg >= 0) {
+    const int v0 = (seg / kRWarps) * (kChunkBytes / 16) + (seg % kRWarps) * (kRStatVecs * 32);
+    y = walk_seg<ELT, kRStatVecs, false>(row_ptr(P, b, kb, 0), nullptr, v0, nvec_row, seg_t, c2, bK, L, 0.f, 0.f, lane);
+  }
+  write_outputs(P, b, kb, -1, y, 0, 0, lane);
+}
+
+// ---------------------------------------------------------------------------
+// rows_resid_kernel: the rejected pairs read again, 32 KB of each row per slot
+// ---------------------------------------------------------------------------
+
+template <int ELT>
+struct RowResid {
+  using V = Vec<ELT>;
+  static constexpr int NV = V::N;
+
+  const VerifyParams& P;
+  RCtrl& C;
+  unsigned char* ring;
+  const int lane, warp;
+  const long long row_bytes;
+  int u0, u1;                  // this CTA's half-pieces [u0, u1) of jobs * nr
+
+  __device__ RowResid(const VerifyParams& p, RCtrl& c, unsigned char* r, int ln, int wp)
+      : P(p), C(c), ring(r), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * p.elt) {
+    const long long units = static_cast<long long>(__ldcg(p.pw.njobs)) * p.nr;
+    u0 = static_cast<int>(units * blockIdx.x / gridDim.x);
+    u1 = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
+  }
+
+  __device__ void produce() {
+    const uint64_t first_out = evict_first_policy();
+    int j_cur = -1;
+    int4 jb = make_int4(0, 0, 0, 0);
+    float4 jn = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = u0, q = 0; u < u1; ++u, ++q) {
+      const int j = u / P.nr, h = u - j * P.nr;
+      if (j != j_cur) {
+        jb = __ldcg(P.pw.job + j);
+        jn = __ldcg(P.pw.jobn + j);
+        j_cur = j;
+      }
+      const int s = q % kRStages;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&C.empty[s], ((q / kRStages) & 1) ^ 1, kDrainLimitNs) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+        return;
+      }
+      if (lane == 0) {
+        const long long off = static_cast<long long>(h) * kRHalf;
+        const int bytes = static_cast<int>(min(static_cast<long long>(kRHalf), row_bytes - off));
+        RDesc& d = C.desc[s];
+        d.u = u - u0; d.rec = j; d.part = h; d.bytes = bytes;
+        d.b = jb.y; d.kb = jb.w; d.pos = jb.z; d.kind = 2; d.x = -1;
+        d.num = jn;
+        unsigned char* dst = ring + static_cast<size_t>(s) * kChunkBytes;
+        mbar_expect_tx(&C.full[s], static_cast<uint32_t>(2 * bytes));
+        bulk_load_hint(dst, row_ptr(P, jb.y, jb.z, 0) + off, static_cast<uint32_t>(bytes), &C.full[s], first_out);
+        bulk_load_hint(dst + kRHalf, row_ptr(P, jb.y, jb.z, 1) + off, static_cast<uint32_t>(bytes), &C.full[s],
+                       first_out);
+      }
+      __syncwarp();
+    }
+  }
+
+  // Each warp's segment sums of max(0, p - q) and of p, the residual weights
+  // of the cluster kernel (no cancellation where p ~ q).
+  __device__ void consume() {
+    const float c2 = P.c2;
+    for (int u = u0, q = 0; u < u1; ++u, ++q) {
+      const int s = q % kRStages;
+      bool timed_out = false;
+      if (!mbar_wait_bounded(&C.full[s], static_cast<uint32_t>(q / kRStages) & 1u, P.wait_limit_ns)) {
+        timed_out = true;
+        if (!mbar_wait_bounded(&C.full[s], static_cast<uint32_t>(q / kRStages) & 1u, kDrainLimitNs)) {
+          if (lane == 0) atomicOr(P.ws.err_word, 1u << 5 /* SV_ERR_TIMEOUT */);
+          return;
+        }
+      }
+      const RDesc d = C.desc[s];
+      const unsigned char* data = ring + static_cast<size_t>(s) * kChunkBytes;
+      const int nvec = (d.bytes + 15) / 16;
+      uint4 rt[kRDrawVecs], rd[kRDrawVecs];
+#pragma unroll
+      for (int jj = 0; jj < kRDrawVecs; ++jj) {
+        const int v = warp * (kRDrawVecs * 32) + jj * 32 + lane;
+        const bool in = v < nvec;
+        rt[jj] = in ? *reinterpret_cast<const uint4*>(data + static_cast<size_t>(v) * 16) : V::neg_inf();
+        rd[jj] = in ? *reinterpret_cast<const uint4*>(data + kRHalf + static_cast<size_t>(v) * 16) : V::neg_inf();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&C.empty[s]);
+      const f2 cc = pack2(c2, c2), nkt = pack2(-d.num.x, -d.num.x), nlt = pack2(-d.num.y, -d.num.y);
+      const f2 gh = pack2(d.num.z, d.num.z), gl = pack2(d.num.w, d.num.w);
+      f2 accr[NV / 2], accp[NV / 2];
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) { accr[i] = 0ull; accp[i] = 0ull; }
+#pragma unroll
+      for (int jj = 0; jj < kRDrawVecs; ++jj) {
+        f2 zt[NV / 2], zd[NV / 2];
+        V::pairs(rt[jj], zt);
+        V::pairs(rd[jj], zd);
+#pragma unroll
+        for (int i = 0; i < NV / 2; ++i) {
+          // the residual weights of resid_weight2, with the series taken two
+          // lanes per f32x2 instruction (bit-identical, lane by lane)
+          const f2 p = exp2_2(add2(fma2(zt[i], cc, nkt), nlt));
+          const f2 delta = add2(fma2(sub2(zd[i], zt[i]), cc, gh), gl);
+          float w0, w1;
+          unpack2(mul2(p, one_minus_exp2_2r(delta)), w0, w1);
+          accr[i] = add2(accr[i], pack2(fmaxf(w0, 0.f), fmaxf(w1, 0.f)));
+          accp[i] = add2(accp[i], p);
+        }
+      }
+      float a0, a1, sr = 0.f, sp = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        unpack2(accr[i], a0, a1); sr += a0 + a1;
+        unpack2(accp[i], a0, a1); sp += a0 + a1;
+      }
+      const float wr = warp_sum(sr), wp = warp_sum(sp);
+      if (lane == 0) {
+        const size_t g = (static_cast<size_t>(d.rec) * P.nr + d.part) * kRWarps + warp;
+        P.pw.rmass[g] = timed_out ? NAN : wr;
+        P.pw.pmass[g] = timed_out ? NAN : wp;
+      }
+    }
+  }
+};
+
+template <int ELT>
+__global__ void __launch_bounds__(kRThreads, 1) rows_resid_kernel(const VerifyParams P) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  RCtrl& C = *reinterpret_cast<RCtrl*>(smem);
+  unsigned char* ring = smem + kRCtrlBytes;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(&C.full[s], 1);
+      mbar_init(&C.empty[s], kRWarps);
+    }
+    fence_mbar_init();
   }
   __syncthreads();
-  {
-    Pieces<ELT, GREEDY> v(P, C, ring, lane, warp);
-    if (warp < kConsumerWarps) v.consume();
-    else if (warp == kWarpProducer) v.produce();
-    else if (warp < kWarpDec0) v.control(warp - kWarpCtl0);
-    else v.decider(warp - kWarpDec0);
+  grid_dependency_wait();      // the jobs
+  grid_dependents_launch();
+  RowResid<ELT> k(P, C, ring, lane, warp);
+  if (warp == kRProducer) k.produce();
+  else k.consume();
+}
+
+// ---------------------------------------------------------------------------
+// rows_draw_kernel: one warp per job, the residual draw
+// ---------------------------------------------------------------------------
+template <int ELT>
+__global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyParams P) {
+  grid_dependency_wait();      // the re-read masses
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * (kRSmallThreads / 32) + (threadIdx.x >> 5);
+  if (j >= __ldcg(P.pw.njobs)) return;
+  const int4 jb = __ldcg(P.pw.job + j);
+  const float4 jn = __ldcg(P.pw.jobn + j);
+  const int b = jb.y, a = jb.z, kb = jb.w, k = P.k;
+  const int nseg = P.nr * kRWarps;
+  const float* rm = P.pw.rmass + static_cast<size_t>(j) * nseg;
+  const float* pm = P.pw.pmass + static_cast<size_t>(j) * nseg;
+  const int per = (nseg + 31) / 32;
+  const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
+  float r = 0.f, pp = 0.f;
+  for (int g = g0; g < g1; ++g) {
+    r += __ldcg(rm + g);
+    pp += __ldcg(pm + g);
   }
+  const float rtot = warp_sum(r);
+  // exact arithmetic rules a zero residual out (a rejection implies p > q
+  // somewhere); if rounding leaves none, the draw is from p_a (counted)
+  const bool resid = rtot > 0.f;
+  const float tot = resid ? rtot : warp_sum(pp);
+  int err = (rtot != rtot || tot != tot) ? kErrTime : 0;   // a timed-out re-read left NaN
+  const float s = __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + k);
+  int seg;
+  float seg_t;
+  locate_seg(resid ? rm : pm, nseg, s * tot, lane, seg, seg_t);
+  if (P.diag && lane == 0) P.ws.mass[static_cast<size_t>(b) * (k + 1) + a] = tot;
+  int y = -1;
+  if (!err && seg >= 0) {
+    const int nvec_row = static_cast<int>((static_cast<long long>(P.V) * ELT) / 16);
+    const int v0 = (seg / kRWarps) * (kRHalf / 16) + (seg % kRWarps) * (kRDrawVecs * 32);
+    const unsigned char* rowT = row_ptr(P, b, a, 0);
+    if (resid)
+      y = walk_seg<ELT, kRDrawVecs, true>(rowT, row_ptr(P, b, a, 1), v0, nvec_row, seg_t, P.c2, jn.x, jn.y, jn.z,
+                                          jn.w, lane);
+    else
+      y = walk_seg<ELT, kRDrawVecs, false>(rowT, nullptr, v0, nvec_row, seg_t, P.c2, jn.x, jn.y, 0.f, 0.f, lane);
+  }
+  write_outputs(P, b, kb, a, y, err, resid ? 0 : 1, lane);
+}
+
+cudaError_t launch_dep(void (*fn)(const VerifyParams), int grid, int threads, int smem, cudaStream_t s,
+                       const VerifyParams& p) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+template <int ELT, bool GREEDY>
+cudaError_t launch_rows(const VerifyParams& p, cudaStream_t s) {
+  const int smem = kRCtrlBytes + kRStages * kChunkBytes;
+  const int small = (p.B + kRSmallThreads / 32 - 1) / (kRSmallThreads / 32);
+  // the plan in plain stream order: nothing of an earlier call may still run
+  rows_plan_kernel<<<1, 1024, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_dep(rows_stats_kernel<ELT, GREEDY>, p.ctas, kRThreads, smem, s, p);
+  if (e == cudaSuccess) e = launch_dep(rows_decide_kernel<ELT, GREEDY>, small, kRSmallThreads, 0, s, p);
+  if (!GREEDY) {
+    if (e == cudaSuccess) e = launch_dep(rows_resid_kernel<ELT>, p.ctas, kRThreads, smem, s, p);
+    if (e == cudaSuccess) e = launch_dep(rows_draw_kernel<ELT>, small, kRSmallThreads, 0, s, p);
+  }
+  return e;
 }
 
 }  // namespace
 
-int pieces_smem_bytes() { return kPCtrlBytes + kPiecesStages * kChunkBytes; }
+int pieces_smem_bytes() { return kRCtrlBytes + kRStages * kChunkBytes; }
 
 cudaError_t prepare_pieces_kernel() {
-  const void* fns[4] = {reinterpret_cast<const void*>(&verify_pieces_kernel<2, false>),
-                        reinterpret_cast<const void*>(&verify_pieces_kernel<4, false>),
-                        reinterpret_cast<const void*>(&verify_pieces_kernel<2, true>),
-                        reinterpret_cast<const void*>(&verify_pieces_kernel<4, true>)};
+  const void* fns[6] = {reinterpret_cast<const void*>(&rows_stats_kernel<2, false>),
+                        reinterpret_cast<const void*>(&rows_stats_kernel<4, false>),
+                        reinterpret_cast<const void*>(&rows_stats_kernel<2, true>),
+                        reinterpret_cast<const void*>(&rows_stats_kernel<4, true>),
+                        reinterpret_cast<const void*>(&rows_resid_kernel<2>),
+                        reinterpret_cast<const void*>(&rows_resid_kernel<4>)};
   for (const void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pieces_smem_bytes());
     if (e != cudaSuccess) return e;
@@ -1029,22 +921,9 @@ cudaError_t prepare_pieces_kernel() {
 }
 
 cudaError_t launch_pieces(const VerifyParams& p, cudaStream_t s) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.ctas), 1, 1);
-  cfg.blockDim = dim3(kPThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(pieces_smem_bytes());
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (p.greedy) {
-    if (p.elt == 2) return cudaLaunchKernelEx(&cfg, verify_pieces_kernel<2, true>, p);
-    return cudaLaunchKernelEx(&cfg, verify_pieces_kernel<4, true>, p);
-  }
-  if (p.elt == 2) return cudaLaunchKernelEx(&cfg, verify_pieces_kernel<2, false>, p);
-  return cudaLaunchKernelEx(&cfg, verify_pieces_kernel<4, false>, p);
+  NvtxRange range("spec_verify_rows");
+  if (p.greedy) return p.elt == 2 ? launch_rows<2, true>(p, s) : launch_rows<4, true>(p, s);
+  return p.elt == 2 ? launch_rows<2, false>(p, s) : launch_rows<4, false>(p, s);
 }
 
 }  // namespace sv

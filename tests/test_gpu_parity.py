@@ -85,12 +85,14 @@ def test_small_cases(name, over, kernel):
 
 
 def test_kernel_choice():
-    """The cluster kernel is the default; the pieces kernel, when asked for,
-    runs aligned batches up to 2048 sequences unless a cluster size or early
-    exit is set."""
+    """Row streaming is the default where it qualifies (aligned rows, up to
+    2048 sequences, no cluster size, no early exit); the cluster kernel runs
+    everything else, and either can be asked for."""
     inp = small("ragged", B=8, k=3, V=4096)
     ver = verifier_for(inp)
-    assert ver.kernel_for(8) == svp.SV_KERNEL_CLUSTER       # the default
+    assert ver.kernel_for(8) == svp.SV_KERNEL_PIECES        # the default
+    ver.set_kernel(svp.SV_KERNEL_CLUSTER)
+    assert ver.kernel_for(8) == svp.SV_KERNEL_CLUSTER
     ver.set_kernel(svp.SV_KERNEL_PIECES)
     assert ver.kernel_for(8) == svp.SV_KERNEL_PIECES
     ver.set_cluster(2)
@@ -100,10 +102,11 @@ def test_kernel_choice():
     assert ver.kernel_for(8) == svp.SV_KERNEL_CLUSTER
     ver.set_early_exit(False)
     assert ver.kernel_for(8) == svp.SV_KERNEL_PIECES
+    ver.set_kernel(svp.SV_KERNEL_AUTO)
+    assert ver.kernel_for(8) == svp.SV_KERNEL_PIECES
     with pytest.raises(svp.SpecVerifyError):
         ver.set_kernel(3)
     big = svp.SpecVerifier(5000, 1, 64, torch.float32)
-    big.set_kernel(svp.SV_KERNEL_PIECES)
     assert big.kernel_for(2048) == svp.SV_KERNEL_PIECES and big.kernel_for(2049) == svp.SV_KERNEL_CLUSTER
 
 
@@ -114,6 +117,7 @@ def test_timeline_is_consistent():
     too small for the grid."""
     inp = small("ragged", B=64, k=3, V=65536)
     ver = verifier_for(inp)
+    ver.set_kernel(svp.SV_KERNEL_CLUSTER)     # the timeline is the cluster kernel's
     cs, ctas = ver.launch_shape(64)
     small_buf = torch.full((ctas * 8,), -1, dtype=torch.int64, device=DEV)
     ver.set_timeline(small_buf)
@@ -156,6 +160,7 @@ def test_both_kernels_agree_away_from_ties():
 def test_every_pipeline_shape_gives_the_same_result(stages, ctas):
     inp = small("ragged", B=32, k=3, V=24576)
     ver = verifier_for(inp)
+    ver.set_kernel(svp.SV_KERNEL_CLUSTER)     # the staging ring is the cluster kernel's
     ver.set_pipeline(stages, ctas)
     cfg = ver.config()
     assert cfg["stages"] == stages and (ctas == 0 or cfg["ctas_per_sm"] == ctas)
