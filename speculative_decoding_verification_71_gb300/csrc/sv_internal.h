@@ -61,13 +61,11 @@ struct Workspace {
 };
 
 // Workspace of the row-streaming schedule (sv_pieces.cu), owned by the
-// context.  Rows of the work list's sequences are numbered in work-list
-// order: rowoff[t] rows come before entry t's (target 0, draft 0, ...,
-// target k_b), rowoff[n] in all.  A piece is 64 KB of one row (np per row),
+// context.  Rows are numbered in batch order: rowoff[b] rows come before
+// sequence b's (target 0, draft 0, ..., target k_b), rowoff[B] in all.  A piece is 64 KB of one row (np per row),
 // a re-read half-piece 32 KB of each row of a pair (nr per row).
 struct PiecesWs {
   int* rowoff;       // [max_B + 1]
-  int4* rowtab;      // [rows]       each row's (b, k_b, pos | kind << 16, drafted token or -1)
   float4* rec;       // [rows * np]   a piece's (M, S about fl(M c), token logit, flags); greedy (M, argmax, 0, flags)
   float2* bseg;      // [max_B * np * 16]  bonus rows: each warp segment's (fl(m c), sum)
   int4* job;         // [max_B]       a rejected pair to draw from: (entry t, b, a, k_b)

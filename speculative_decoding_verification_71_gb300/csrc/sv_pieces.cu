@@ -5,12 +5,12 @@
 // the first rejection, then the residual max(0, p - q) or the bonus row),
 // the same arithmetic, another schedule: the rows of the batch are streamed
 // as independent 64 KB pieces spread evenly over one CTA per SM, with no
-// exchange between CTAs, and the per-sequence decisions come after.  Five
-// launches per call (each after plan_kernel's work list, each waiting for its
-// predecessor's results with programmatic dependent launch, after the first):
-//   rows_plan_kernel    in batch order: rows before each sequence (2 k_b + 1
-//                       each), the row table, invalid k_b answered;
-//   rows_stats_kernel   every needed row, piece by piece: a producer warp
+// exchange between CTAs, and the per-sequence decisions come after.  Four
+// launches per call, each waiting for its predecessor's results with
+// programmatic dependent launch:
+//   rows_stats_kernel   the plan in every CTA (rows of the sequences before
+//                       each, in batch order: 2 k_b + 1), then every needed
+//                       row, piece by piece: a producer warp
 //                       streams the pieces through three shared-memory slots
 //                       with cp.async.bulk, 16 consumer warps reduce them; the
 //                       last warp to finish a piece combines the warps' parts
@@ -19,7 +19,8 @@
 //                       warp segment's sum for the draw;
 //   rows_decide_kernel  one warp per sequence: the rows from their pieces, the
 //                       tests, the first rejection; the bonus draw (one
-//                       segment read again) or a job for the residual;
+//                       segment read again) or a job for the residual; an
+//                       invalid k_b answered;
 //   rows_resid_kernel   every job's rejected pair read again in 32 KB
 //                       half-pieces spread over the CTAs: each warp segment's
 //                       sums of max(0, p - q) and of p;
@@ -75,6 +76,8 @@ struct RCtrl {
   RDesc desc[kRStages];
   WPart part[kRBufs][kRWarps];
   int cnt[kRBufs];             // warps done with the piece in this buffer
+  int rowoff[kPiecesMaxB + 1]; // statistics kernel: rows of the sequences before b (its own copy)
+  int warp_tot[32];
 };
 constexpr int kRCtrlBytes = ((static_cast<int>(sizeof(RCtrl)) + 1023) / 1024) * 1024;
 static_assert(kRCtrlBytes + kRStages * kChunkBytes <= 227 * 1024, "three slots must fit in one CTA");
@@ -83,75 +86,6 @@ __device__ __forceinline__ const unsigned char* row_ptr(const VerifyParams& P, i
   const size_t rb = static_cast<size_t>(P.V) * P.elt;
   if (kind == 0) return static_cast<const unsigned char*>(P.target) + (static_cast<size_t>(b) * (P.k + 1) + pos) * rb;
   return static_cast<const unsigned char*>(P.draft) + (static_cast<size_t>(b) * P.k + pos) * rb;
-}
-
-// The call's plan, in batch order (no sort: every piece is the same work):
-// rowoff[b] = rows of the sequences before b (2 k_b + 1 each, k_b + 1 for
-// T = 0; none for an invalid k_b, which is answered here), rowoff[B] = all
-// rows; each row's entry in the row table; the counters the other kernels
-// start from.  One CTA.
-__global__ void __launch_bounds__(1024) rows_plan_kernel(const VerifyParams P) {
-  grid_dependents_launch();      // the statistics kernel's prologue may start
-  __shared__ int warp_tot[32];
-  __shared__ int carry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int B = P.B, k = P.k;
-  if (tid == 0) { carry = 0; *P.pw.njobs = 0; }
-  if (P.diag) {
-    for (int i = tid; i < B * (k + 1); i += 1024) { P.ws.m_t[i] = NAN; P.ws.L_t[i] = NAN; P.ws.mass[i] = NAN; }
-    for (int i = tid; i < B * k; i += 1024) { P.ws.m_d[i] = NAN; P.ws.L_d[i] = NAN; P.ws.alpha[i] = NAN; }
-  }
-  __syncthreads();
-  for (int base = 0; base < B; base += 1024) {
-    const int b = base + tid;
-    const int kb = b < B ? __ldg(P.draft_len + b) : 0;
-    const bool valid = b < B && kb >= 0 && kb <= k;
-    if (b < B && !valid) {
-      int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
-      for (int j = 0; j <= k; ++j) ot[j] = -1;
-      P.out_len[b] = 0;
-      atomicOr(P.ws.err_word, 1u << 2 /* SV_ERR_BAD_DRAFT_LEN */);
-      atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
-    }
-    const int cnt = valid ? (P.greedy ? kb + 1 : 2 * kb + 1) : 0;
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int up = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += up;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      const int wt = warp_tot[lane];
-      int wi = wt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int up = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += up;
-      }
-      warp_tot[lane] = wi - wt;
-    }
-    __syncthreads();
-    if (b < B) {
-      // the sequence's rows: target 0, draft 0, ..., target k_b (T = 0: the
-      // target rows alone), each with its drafted token
-      const int r0 = carry + warp_tot[warp] + incl - cnt;
-      P.pw.rowoff[b] = r0;
-      for (int ri = 0; ri < cnt; ++ri) {
-        int pos, kind;
-        if (P.greedy) { pos = ri; kind = 0; }
-        else if (ri < 2 * kb) { pos = ri >> 1; kind = ri & 1; }
-        else { pos = kb; kind = 0; }
-        const int x = pos < kb ? __ldg(P.tokens + static_cast<size_t>(b) * k + pos) : -1;
-        P.pw.rowtab[r0 + ri] = make_int4(b, kb, pos | (kind << 16), x);
-      }
-    }
-    __syncthreads();
-    if (tid == 1023) carry += warp_tot[31] + incl;
-    __syncthreads();
-  }
-  if (tid == 0) P.pw.rowoff[B] = carry;
 }
 
 // Vector v of a row (16-byte aligned rows), -inf past its end.
@@ -307,20 +241,37 @@ struct RowStats {
 
   __device__ RowStats(const VerifyParams& p, RCtrl& c, unsigned char* r, int ln, int wp)
       : P(p), C(c), ring(r), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * p.elt) {
-    const long long units = static_cast<long long>(__ldcg(p.pw.rowoff + p.B)) * p.np;
+    const long long units = static_cast<long long>(c.rowoff[p.B]) * p.np;
     u0 = static_cast<int>(units * blockIdx.x / gridDim.x);
     u1 = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
   }
 
   __device__ void produce() {
     const uint64_t first_out = evict_first_policy();
-    int r_cur = -1;
-    int4 rt = make_int4(0, 0, 0, -1);
+    if (u0 >= u1) return;
+    // the sequence holding this CTA's first row (rows in batch order)
+    int lo = 0, hi = P.B;            // rowoff[lo] <= r < rowoff[hi]
+    const int r_first = u0 / P.np;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (C.rowoff[mid] <= r_first) lo = mid; else hi = mid;
+    }
+    int b = lo, kb = 0, nrows_b = 0, r_base = 0, r_cur = -1, pos = 0, kind = 0, x = -1;
     for (int u = u0, q = 0; u < u1; ++u, ++q) {
       const int r = u / P.np, j = u - r * P.np;
-      if (r != r_cur) {   // one load per row, while the slots keep the consumers busy
-        rt = __ldcg(P.pw.rowtab + r);
+      if (r != r_cur) {   // the next row: its sequence, position and drafted token
         r_cur = r;
+        while (r >= C.rowoff[b + 1]) ++b;   // (sequences with no rows are passed over)
+        if (r_base != C.rowoff[b] || nrows_b == 0) {
+          r_base = C.rowoff[b];
+          nrows_b = C.rowoff[b + 1] - r_base;
+          kb = P.greedy ? nrows_b - 1 : (nrows_b - 1) >> 1;
+        }
+        const int ri = r - r_base;
+        if (P.greedy) { pos = ri; kind = 0; }
+        else if (ri < 2 * kb) { pos = ri >> 1; kind = ri & 1; }
+        else { pos = kb; kind = 0; }
+        x = pos < kb ? __ldg(P.tokens + static_cast<size_t>(b) * P.k + pos) : -1;
       }
       const int s = q % kRStages;
       int ok = 1;
@@ -330,14 +281,13 @@ struct RowStats {
         return;   // the consumers time out on the slots left and flag their pieces
       }
       if (lane == 0) {
-        const int pos = rt.z & 0xffff, kind = rt.z >> 16;
         const long long off = static_cast<long long>(j) * kChunkBytes;
         const int bytes = static_cast<int>(min(static_cast<long long>(kChunkBytes), row_bytes - off));
         RDesc& d = C.desc[s];
         d.u = u - u0; d.rec = u; d.part = j; d.bytes = bytes;
-        d.b = rt.x; d.kb = rt.y; d.pos = pos; d.kind = kind; d.x = rt.w;
+        d.b = b; d.kb = kb; d.pos = pos; d.kind = kind; d.x = x;
         mbar_expect_tx(&C.full[s], static_cast<uint32_t>(bytes));
-        bulk_load_hint(ring + static_cast<size_t>(s) * kChunkBytes, row_ptr(P, rt.x, pos, kind) + off,
+        bulk_load_hint(ring + static_cast<size_t>(s) * kChunkBytes, row_ptr(P, b, pos, kind) + off,
                        static_cast<uint32_t>(bytes), &C.full[s], first_out);
       }
       __syncwarp();
@@ -503,9 +453,45 @@ __global__ void __launch_bounds__(kRThreads, 1) rows_stats_kernel(const VerifyPa
     for (int i = 0; i < kRBufs; ++i) C.cnt[i] = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-  grid_dependency_wait();      // the row table
+  grid_dependency_wait();      // nothing of an earlier call still reads the workspace
   grid_dependents_launch();
+  // the call's plan, in every CTA: rows of the sequences before b, in batch
+  // order (2 k_b + 1 each, k_b + 1 for T = 0; none for an invalid k_b)
+  const int B = P.B, nw = kRThreads / 32;
+  if (tid == 0) C.rowoff[0] = 0;
+  int carry = 0;
+  for (int base = 0; base < B; base += kRThreads) {
+    const int bb = base + tid;
+    const int kb = bb < B ? __ldg(P.draft_len + bb) : -1;
+    const int cnt = (bb < B && kb >= 0 && kb <= P.k) ? (GREEDY ? kb + 1 : 2 * kb + 1) : 0;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += up;
+    }
+    if (lane == 31) C.warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int wt = lane < nw ? C.warp_tot[lane] : 0;
+      int wi = wt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += up;
+      }
+      if (lane < nw) C.warp_tot[lane] = wi - wt;
+    }
+    __syncthreads();
+    if (bb < B) C.rowoff[bb + 1] = carry + C.warp_tot[warp] + incl;
+    __syncthreads();
+    carry = C.rowoff[min(B, base + kRThreads)];
+  }
+  if (blockIdx.x == 0) {
+    // the first CTA publishes the offsets for the decision kernel
+    for (int i = tid; i <= B; i += kRThreads) P.pw.rowoff[i] = C.rowoff[i];
+    if (tid == 0) *P.pw.njobs = 0;
+  }
   RowStats<ELT, GREEDY> k(P, C, ring, lane, warp);
   if (warp == kRProducer) k.produce();
   else k.consume();
@@ -554,9 +540,31 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
   const int b = blockIdx.x * (kRSmallThreads / 32) + wi;
   if (b >= P.B) return;
+  const int k = P.k, t = b;
   const int r0 = __ldcg(P.pw.rowoff + b);
-  if (__ldcg(P.pw.rowoff + b + 1) == r0) return;   // an invalid k_b, answered by the plan
-  const int kb = __ldg(P.draft_len + b), k = P.k, t = b;
+  if (P.diag) {   // every diagnostic of the sequence NaN first: only the rows read get values
+    for (int j = lane; j <= k; j += 32) {
+      const size_t i = static_cast<size_t>(b) * (k + 1) + j;
+      P.ws.m_t[i] = NAN; P.ws.L_t[i] = NAN; P.ws.mass[i] = NAN;
+    }
+    for (int j = lane; j < k; j += 32) {
+      const size_t i = static_cast<size_t>(b) * k + j;
+      P.ws.m_d[i] = NAN; P.ws.L_d[i] = NAN; P.ws.alpha[i] = NAN;
+    }
+    __syncwarp();
+  }
+  if (__ldcg(P.pw.rowoff + b + 1) == r0) {
+    // an invalid k_b: no rows were read; the sequence emits nothing
+    int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
+    for (int j = lane; j <= k; j += 32) ot[j] = -1;
+    if (lane == 0) {
+      P.out_len[b] = 0;
+      atomicOr(P.ws.err_word, 1u << 2 /* SV_ERR_BAD_DRAFT_LEN */);
+      atomicAdd(P.ws.stats + kStatErrorSeqs, 1ull);
+    }
+    return;
+  }
+  const int kb = __ldg(P.draft_len + b);
   const float c2 = P.c2;
   const bool diag = P.diag != 0;
   const int xl = lane < kb ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
@@ -890,10 +898,7 @@ template <int ELT, bool GREEDY>
 cudaError_t launch_rows(const VerifyParams& p, cudaStream_t s) {
   const int smem = kRCtrlBytes + kRStages * kChunkBytes;
   const int small = (p.B + kRSmallThreads / 32 - 1) / (kRSmallThreads / 32);
-  // the plan in plain stream order: nothing of an earlier call may still run
-  rows_plan_kernel<<<1, 1024, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) e = launch_dep(rows_stats_kernel<ELT, GREEDY>, p.ctas, kRThreads, smem, s, p);
+  cudaError_t e = launch_dep(rows_stats_kernel<ELT, GREEDY>, p.ctas, kRThreads, smem, s, p);
   if (e == cudaSuccess) e = launch_dep(rows_decide_kernel<ELT, GREEDY>, small, kRSmallThreads, 0, s, p);
   if (!GREEDY) {
     if (e == cudaSuccess) e = launch_dep(rows_resid_kernel<ELT>, p.ctas, kRThreads, smem, s, p);
