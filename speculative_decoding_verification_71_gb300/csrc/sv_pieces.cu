@@ -192,17 +192,14 @@ __device__ int walk_seg(const unsigned char* rowT, const unsigned char* rowD, in
 }
 
 // Outputs and counters of a finished sequence (lane 0 writes the scalars).
+// xl: lane j holds drafted token j (k <= 31).
 __device__ void write_outputs(const VerifyParams& P, int b, int kb, int a, int y, int err, int zero_resid,
-                              int lane) {
+                              int xl, int lane) {
   const int k = P.k;
   const bool ok = !err && y >= 0;
   const int acc = a < 0 ? kb : a;
   int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
-  for (int j = lane; j <= k; j += 32) {
-    int v = -1;
-    if (ok) v = j < acc ? __ldg(P.tokens + static_cast<size_t>(b) * k + j) : (j == acc ? y : -1);
-    ot[j] = v;
-  }
+  if (lane <= k) ot[lane] = !ok ? -1 : (lane < acc ? xl : (lane == acc ? y : -1));
   if (lane == 0) {
     P.out_len[b] = ok ? acc + 1 : 0;
     if (ok) {
@@ -541,7 +538,19 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
   const int b = blockIdx.x * (kRSmallThreads / 32) + wi;
   if (b >= P.B) return;
   const int k = P.k, t = b;
-  const int r0 = __ldcg(P.pw.rowoff + b);
+  // everything that depends on b alone, in one round trip
+  const int r0 = __ldcg(P.pw.rowoff + b), r1 = __ldcg(P.pw.rowoff + b + 1);
+  const int kb_in = __ldg(P.draft_len + b);
+  const int x_all = lane < k ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
+  const float ul = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
+  const int nseg_b = P.np * kRWarps;
+  float2 bsg[kMaxChunks * kRWarps / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxChunks * kRWarps / 32; ++i) {
+    const int g = lane + 32 * i;
+    bsg[i] = (!GREEDY && g < nseg_b) ? __ldcg(P.pw.bseg + static_cast<size_t>(b) * nseg_b + g)
+                                     : make_float2(-INFINITY, 0.f);
+  }
   if (P.diag) {   // every diagnostic of the sequence NaN first: only the rows read get values
     for (int j = lane; j <= k; j += 32) {
       const size_t i = static_cast<size_t>(b) * (k + 1) + j;
@@ -553,7 +562,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
     }
     __syncwarp();
   }
-  if (__ldcg(P.pw.rowoff + b + 1) == r0) {
+  if (r1 == r0) {
     // an invalid k_b: no rows were read; the sequence emits nothing
     int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
     for (int j = lane; j <= k; j += 32) ot[j] = -1;
@@ -564,11 +573,10 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
     }
     return;
   }
-  const int kb = __ldg(P.draft_len + b);
+  const int kb = kb_in;
   const float c2 = P.c2;
   const bool diag = P.diag != 0;
-  const int xl = lane < kb ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
-  const float ul = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
+  const int xl = lane < kb ? x_all : -1;
   const float s_samp = __shfl_sync(0xffffffffu, ul, k);
   int a = -1, err = 0, y = -1;
   float pK = 0.f, pS = 0.f, pzx = 0.f;                  // target row of the current pair
@@ -644,7 +652,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
     }
   }
   if (err || GREEDY) {
-    write_outputs(P, b, kb, a, err ? -1 : y, err, 0, lane);
+    write_outputs(P, b, kb, a, err ? -1 : y, err, 0, xl, lane);
     return;
   }
   if (a >= 0) {
@@ -663,9 +671,10 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
   const float L = log2f(bS);
   const int nseg = P.np * kRWarps;
   float* wm = bmass[wi];
-  for (int g = lane; g < nseg; g += 32) {
-    const float2 sg = __ldcg(P.pw.bseg + static_cast<size_t>(b) * nseg + g);
-    wm[g] = sg.x == -INFINITY ? 0.f : sg.y * fast_exp2(__fsub_rn(sg.x, bK) - L);
+#pragma unroll
+  for (int i = 0; i < kMaxChunks * kRWarps / 32; ++i) {
+    const int g = lane + 32 * i;
+    if (g < nseg) wm[g] = bsg[i].x == -INFINITY ? 0.f : bsg[i].y * fast_exp2(__fsub_rn(bsg[i].x, bK) - L);
   }
   __syncwarp();
   float part = 0.f;
@@ -684,7 +693,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
     const int v0 = (seg / kRWarps) * (kChunkBytes / 16) + (seg % kRWarps) * (kRStatVecs * 32);
     y = walk_seg<ELT, kRStatVecs, false>(row_ptr(P, b, kb, 0), nullptr, v0, nvec_row, seg_t, c2, bK, L, 0.f, 0.f, lane);
   }
-  write_outputs(P, b, kb, -1, y, 0, 0, lane);
+  write_outputs(P, b, kb, -1, y, 0, 0, xl, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -843,17 +852,18 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyP
   if (j >= __ldcg(P.pw.njobs)) return;
   const int4 jb = __ldcg(P.pw.job + j);
   const float4 jn = __ldcg(P.pw.jobn + j);
-  const int b = jb.y, a = jb.z, kb = jb.w, k = P.k;
   const int nseg = P.nr * kRWarps;
   const float* rm = P.pw.rmass + static_cast<size_t>(j) * nseg;
   const float* pm = P.pw.pmass + static_cast<size_t>(j) * nseg;
   const int per = (nseg + 31) / 32;
   const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
   float r = 0.f, pp = 0.f;
-  for (int g = g0; g < g1; ++g) {
+  for (int g = g0; g < g1; ++g) {   // (issued with the job's load: they depend on j alone)
     r += __ldcg(rm + g);
     pp += __ldcg(pm + g);
   }
+  const int b = jb.y, a = jb.z, kb = jb.w, k = P.k;
+  const int xl = lane < a ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
   const float rtot = warp_sum(r);
   // exact arithmetic rules a zero residual out (a rejection implies p > q
   // somewhere); if rounding leaves none, the draw is from p_a (counted)
@@ -876,7 +886,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyP
     else
       y = walk_seg<ELT, kRDrawVecs, false>(rowT, nullptr, v0, nvec_row, seg_t, P.c2, jn.x, jn.y, 0.f, 0.f, lane);
   }
-  write_outputs(P, b, kb, a, y, err, resid ? 0 : 1, lane);
+  write_outputs(P, b, kb, a, y, err, resid ? 0 : 1, xl, lane);
 }
 
 cudaError_t launch_dep(void (*fn)(const VerifyParams), int grid, int threads, int smem, cudaStream_t s,
