@@ -85,7 +85,7 @@ def parse():
                     help="timed rounds of the draft-length controller (0 = skip)")
     ap.add_argument("--profile-kernels", default="",
                     help="run each named kernel's representative case twice (for ncu, one kernel per "
-                         "capture): comma list of verify (the default schedule), verify_cluster, verify_dense, pieces, early_exit, "
+                         "capture): comma list of verify (the default schedule), verify_cluster, verify_dense, early_exit, "
                          "compact, debug, kd, tree, ctrl")
     return ap.parse_args()
 
@@ -275,8 +275,9 @@ def reference_arm(args, w):
 # our arm
 # ---------------------------------------------------------------------------
 
-def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=None, early_exit=False):
-    """Device-timed steps of one workload.  Returns a dict of measurements."""
+def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=None, early_exit=False, kernel=None):
+    """Device-timed steps of one workload (kernel: an SV_KERNEL_* value, None
+    for the automatic choice).  Returns a dict of measurements."""
     import torch
 
     from workloads import algorithmic_bytes, make_inputs
@@ -292,6 +293,8 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
         ver.set_pipeline(args.stages or 3, args.ctas_per_sm)
     ver.set_cluster(args.cluster)
     ver.set_early_exit(early_exit)
+    if kernel is not None:
+        ver.set_kernel(kernel)
     outs = [(torch.empty(w.B, w.k + 1, dtype=torch.int32, device=device),
              torch.empty(w.B, dtype=torch.int32, device=device)) for _ in range(rotate)]
 
@@ -358,8 +361,9 @@ def time_workload(svp, w, args, device, stream, rotate, steps, warmup, sampler=N
     cfg["kernel"] = kernel_name(svp, ver.kernel_for(w.B))
     if cfg["kernel"] == "cluster":
         cfg["cluster"], cfg["grid_ctas"] = ver.launch_shape(w.B)
-    else:
-        cfg["cluster"], cfg["grid_ctas"] = None, None
+    else:   # row streaming: the streaming kernels' shape (one CTA per SM, three 64 KB slots)
+        cfg["threads"], cfg["smem_bytes"], cfg["grid_ctas"] = ver.rows_shape()
+        cfg["cluster"], cfg["ctas_per_sm"], cfg["stages"] = None, 1, 3
     del sets, outs
     return {"total_ms": total_ms, "kernel_ms_mean": float(np.mean(kern_ms)),
             "kernel_ms_median": float(np.median(kern_ms)), "kernel_ms_best": float(np.min(kern_ms)),
@@ -683,20 +687,26 @@ def our_arm(args, w):
         for sigma in [float(x) for x in args.early_exit_sigmas.split(",") if x]:
             ew = get_workload(args.early_exit_workload, draft_sigma=sigma)
             n = max(1, args.steps // 4)
+            # early exit runs on the cluster kernel: compared with the same
+            # kernel without it, and with the default schedule (row streaming)
             on = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=True)
-            off = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=False)
+            off = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=False,
+                                kernel=svp.SV_KERNEL_CLUSTER)
+            dflt = time_workload(svp, ew, args, device, stream, args.rotate, n, args.warmup, early_exit=False)
             # rows not read, from the kernel's own count over the timed calls
             needed = int(np.sum(2 * on["base_inputs"]["draft_len"].cpu().numpy().astype(np.int64) + 1))
             skipped = on["stats"]["rows_skipped"] / n
             runs.append({"workload": ew.describe() + f" draft noise {sigma}", "ms_per_step_on": on["total_ms"] / n,
-                         "ms_per_step_off": off["total_ms"] / n,
+                         "ms_per_step_off": off["total_ms"] / n, "kernel_on": on["cfg"]["kernel"],
+                         "kernel_off": off["cfg"]["kernel"], "ms_per_step_default": dflt["total_ms"] / n,
+                         "kernel_default": dflt["cfg"]["kernel"],
                          "positions_per_s_on": on["positions"] / (on["total_ms"] / n / 1e3),
                          "speedup": off["total_ms"] / on["total_ms"], "mean_emitted": on["stats"]["mean_emitted"],
                          "rows_needed_per_call": needed, "rows_skipped_per_call": skipped,
                          "bytes_skipped_per_call": skipped * ew.V * ew.elt, "skipped_fraction": skipped / needed,
                          "time_saved_fraction": 1.0 - on["total_ms"] / off["total_ms"],
                          "cluster": on["cfg"]["cluster"]})
-            del on, off
+            del on, off, dflt
         aux["early_exit"] = runs
     if args.tree_steps > 0 and world == 1:
         aux["tree_verify"] = [time_tree(svp, t, device, stream, args.tree_steps)
@@ -798,16 +808,19 @@ def profile_kernels(args):
     up, ncu captures the second with -s/-c): the small but L2-exceeding
     inputs the ncu summaries under profiles/ are taken on.
 
-      verify      spec_verify, cluster kernel: plan_kernel + verify_kernel on the ragged workload
-      pieces      the same batch through the pieces kernel: plan_kernel + verify_pieces_kernel
-      early_exit  long draft, B=128 (k=7, V=151936, T=0.6), early exit on: plan_kernel + verify_kernel
-      compact     compact_kernel on the ragged batch's outputs
-      debug       debug_kernel after the ragged batch
-      kd          spec_kd_loss with the gradient, 16 rollouts x 64 positions, V=151936 bf16:
-                  kd_kernel + kd_loss_kernel
-      tree        spec_verify_tree on the tree workload (B=64, 15 nodes, V=151936 bf16): tree_kernel
-      ctrl        spec_ctrl_observe + spec_ctrl_choose (B=1024 slots, max_k=7): ctrl_observe_kernel +
-                  ctrl_choose_kernel
+      verify          spec_verify on the ragged workload, the default (row-streaming) schedule:
+                      rows_stats_kernel, rows_decide_kernel, rows_resid_kernel, rows_draw_kernel
+      verify_dense    the same with every k_b = 3
+      verify_cluster  the ragged batch through the cluster kernel: plan_kernel + verify_kernel
+      early_exit      long draft, B=128 (k=7, V=151936, T=0.6), early exit on (cluster kernel):
+                      plan_kernel + verify_kernel
+      compact         compact_kernel on the ragged batch's outputs
+      debug           debug_kernel after the ragged batch (diagnostics on)
+      kd              spec_kd_loss with the gradient, 16 rollouts x 64 positions, V=151936 bf16:
+                      kd_kernel + kd_loss_kernel
+      tree            spec_verify_tree on the tree workload (B=64, 15 nodes, V=151936 bf16): tree_kernel
+      ctrl            spec_ctrl_observe + spec_ctrl_choose (B=1024 slots, max_k=7): ctrl_observe_kernel +
+                      ctrl_choose_kernel
     """
     import torch
 
@@ -841,10 +854,6 @@ def profile_kernels(args):
                     dw = get_workload("ragged_dense")
                     extra["dense"] = (svp.SpecVerifier(dw.B, dw.k, dw.V, dw.torch_dtype), make_inputs(dw, device=device))
                 run(*extra["dense"])
-            elif name == "pieces":
-                pv = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
-                pv.set_kernel(svp.SV_KERNEL_PIECES)
-                run(pv, inp)
             elif name == "early_exit":
                 ew = get_workload("long_draft", B=128)
                 ei = make_inputs(ew, device=device)

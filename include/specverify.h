@@ -231,6 +231,14 @@ typedef enum { SV_KERNEL_AUTO = 0, SV_KERNEL_CLUSTER = 1, SV_KERNEL_PIECES = 2 }
 sv_status sv_set_kernel(sv_ctx *ctx, int kernel);
 sv_status sv_kernel_for(const sv_ctx *ctx, int B, int *kernel);
 
+/* Launch shape of row streaming's two streaming kernels (statistics and
+ * re-read): threads per CTA, dynamic shared memory per CTA and the grid (one
+ * CTA per SM); the decision and draw kernels run one warp per sequence or
+ * job.  SV_ERR_UNSUPPORTED if this context cannot run row streaming (rows
+ * over 1 MiB, or too little shared memory); SV_ERR_INVALID_ARG for a NULL
+ * context.  Any output pointer may be NULL. */
+sv_status sv_rows_shape(const sv_ctx *ctx, int *threads, int *smem_bytes, int *grid_ctas);
+
 /* Per-CTA timeline of the cluster kernel (measurement aid, off by default;
  * calls that run row streaming write nothing).
  * timeline: device buffer of `capacity` unsigned 64-bit words, or NULL to

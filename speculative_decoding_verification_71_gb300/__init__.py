@@ -42,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
     "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_set_diagnostics", "sv_get_config", "sv_launch_shape",
-    "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for", "sv_set_timeline",
+    "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for", "sv_rows_shape", "sv_set_timeline",
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
     "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_set_cost", "spec_ctrl_set_params", "spec_ctrl_reset",
     "spec_ctrl_observe", "spec_ctrl_choose", "spec_ctrl_alpha", "spec_ctrl_status",
@@ -128,6 +128,8 @@ def load_library(path: str | None = None):
                                          c.POINTER(c.c_int)]
     lib.sv_launch_shape.restype = c.c_int
     lib.sv_launch_shape.argtypes = [P, c.c_int, c.POINTER(c.c_int), c.POINTER(c.c_int)]
+    lib.sv_rows_shape.restype = c.c_int
+    lib.sv_rows_shape.argtypes = [P, c.POINTER(c.c_int), c.POINTER(c.c_int), c.POINTER(c.c_int)]
     lib.sv_set_wait_limit_ns.restype = c.c_int
     lib.sv_set_wait_limit_ns.argtypes = [P, c.c_longlong]
     lib.spec_ctrl_create.restype = c.c_int
@@ -381,6 +383,17 @@ class SpecVerifier:
         if st != SV_OK:
             self._raise(st, "sv_launch_shape")
         return cs.value, ctas.value
+
+    def rows_shape(self):
+        """(threads, shared-memory bytes, CTAs) of row streaming's streaming
+        kernels, or None if this context cannot run row streaming."""
+        vals = [ctypes.c_int() for _ in range(3)]
+        st = self.lib.sv_rows_shape(self._ctx, *[ctypes.byref(v) for v in vals])
+        if st == SV_ERR_UNSUPPORTED:
+            return None
+        if st != SV_OK:
+            self._raise(st, "sv_rows_shape")
+        return tuple(v.value for v in vals)
 
 
 def spec_verify_noalloc(target, draft, tokens, draft_len, uniforms, temperature, out_tokens, out_len,

@@ -448,6 +448,15 @@ sv_status sv_launch_shape(const sv_ctx* ctx, int B, int* cluster, int* grid_ctas
   return SV_OK;
 }
 
+sv_status sv_rows_shape(const sv_ctx* ctx, int* threads, int* smem_bytes, int* grid_ctas) {
+  if (!ctx) return SV_ERR_INVALID_ARG;
+  if (!ctx->pw_mem || ctx->pieces_ctas <= 0) return SV_ERR_UNSUPPORTED;
+  if (threads) *threads = sv::pieces_threads();
+  if (smem_bytes) *smem_bytes = sv::pieces_smem_bytes();
+  if (grid_ctas) *grid_ctas = ctx->pieces_ctas;
+  return SV_OK;
+}
+
 sv_status sv_set_timeline(sv_ctx* ctx, unsigned long long* timeline, int capacity) {
   if (!ctx || capacity < 0 || (timeline && capacity == 0)) return SV_ERR_INVALID_ARG;
   ctx->timeline = timeline;

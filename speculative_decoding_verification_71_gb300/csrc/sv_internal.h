@@ -123,6 +123,7 @@ int verify_smem_bytes(int stages);
 // The row-streaming schedule (sv_pieces.cu).
 constexpr int kPiecesMaxB = 2048;                         // sequences per call
 int pieces_smem_bytes();
+int pieces_threads();                                       // threads of the streaming kernels
 cudaError_t prepare_pieces_kernel();
 cudaError_t launch_pieces(const VerifyParams& p, cudaStream_t s);   // after plan_kernel
 // 64 KB pieces and 32 KB half-pieces per row of V logits of elt bytes.

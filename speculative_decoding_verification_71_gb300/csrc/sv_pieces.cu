@@ -920,6 +920,7 @@ cudaError_t launch_rows(const VerifyParams& p, cudaStream_t s) {
 }  // namespace
 
 int pieces_smem_bytes() { return kRCtrlBytes + kRStages * kChunkBytes; }
+int pieces_threads() { return kRThreads; }
 
 cudaError_t prepare_pieces_kernel() {
   const void* fns[6] = {reinterpret_cast<const void*>(&rows_stats_kernel<2, false>),
