@@ -125,7 +125,6 @@ sv_status create_pieces(sv_ctx* ctx) {
   const size_t rows = B * (2 * k + 1);
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
-  const size_t o_rowoff = take((B + 1) * 4);
   const size_t o_rec = take(rows * ctx->np * 16), o_bseg = take(B * ctx->np * 16 * 8);
   const size_t o_job = take(B * 16), o_jobn = take(B * 16), o_njobs = take(4);
   const size_t o_rmass = take(B * ctx->nr * 16 * 4), o_pmass = take(B * ctx->nr * 16 * 4);
@@ -135,7 +134,6 @@ sv_status create_pieces(sv_ctx* ctx) {
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemset(pieces workspace)");
   char* base = static_cast<char*>(ctx->pw_mem);
   sv::PiecesWs& w = ctx->pw;
-  w.rowoff = reinterpret_cast<int*>(base + o_rowoff);
   w.rec = reinterpret_cast<float4*>(base + o_rec);
   w.bseg = reinterpret_cast<float2*>(base + o_bseg);
   w.job = reinterpret_cast<int4*>(base + o_job);

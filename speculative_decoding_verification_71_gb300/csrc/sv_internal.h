@@ -61,14 +61,14 @@ struct Workspace {
 };
 
 // Workspace of the row-streaming schedule (sv_pieces.cu), owned by the
-// context.  Rows are numbered in batch order: rowoff[b] rows come before
-// sequence b's (target 0, draft 0, ..., target k_b), rowoff[B] in all.  A piece is 64 KB of one row (np per row),
-// a re-read half-piece 32 KB of each row of a pair (nr per row).
+// context.  A sequence's rows are target 0, draft 0, ..., target k_b; a
+// piece is 64 KB of one row (np per row), a re-read half-piece 32 KB of each
+// row of a pair (nr per row).
 struct PiecesWs {
-  int* rowoff;       // [max_B + 1]
-  float4* rec;       // [rows * np]   a piece's (M, S about fl(M c), token logit, flags); greedy (M, argmax, 0, flags)
+  float4* rec;       // [max_B * (2 max_k + 1) * np]  a piece's (M, S about fl(M c), token logit, flags), at
+                     //   ((b (2k + 1) + row of the sequence) np + piece); greedy (M, argmax, 0, flags)
   float2* bseg;      // [max_B * np * 16]  bonus rows: each warp segment's (fl(m c), sum)
-  int4* job;         // [max_B]       a rejected pair to draw from: (entry t, b, a, k_b)
+  int4* job;         // [max_B]       a rejected pair to draw from: (sampling uniform's bits, b, a, k_b)
   float4* jobn;      // [max_B]       ... its (K_t, L_t, Gh, Gl)
   int* njobs;        // [1]
   float* rmass;      // [max_B * nr * 16]  per job, each re-read segment's sum of max(0, p - q)

@@ -192,14 +192,20 @@ __device__ int walk_seg(const unsigned char* rowT, const unsigned char* rowD, in
 }
 
 // Outputs and counters of a finished sequence (lane 0 writes the scalars).
-// xl: lane j holds drafted token j (k <= 31).
+// xl: lane j holds drafted token j (k <= 31).  prefix_done: the accepted
+// prefix and the empty tail are written already (a residual draw's sequence):
+// only the drawn token remains, unless the draw failed.
 __device__ void write_outputs(const VerifyParams& P, int b, int kb, int a, int y, int err, int zero_resid,
-                              int xl, int lane) {
+                              int xl, int lane, bool prefix_done = false) {
   const int k = P.k;
   const bool ok = !err && y >= 0;
   const int acc = a < 0 ? kb : a;
   int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
-  if (lane <= k) ot[lane] = !ok ? -1 : (lane < acc ? xl : (lane == acc ? y : -1));
+  if (ok && prefix_done) {
+    if (lane == acc) ot[acc] = y;
+  } else if (lane <= k) {
+    ot[lane] = !ok ? -1 : (lane < acc ? xl : (lane == acc ? y : -1));
+  }
   if (lane == 0) {
     P.out_len[b] = ok ? acc + 1 : 0;
     if (ok) {
@@ -253,7 +259,8 @@ struct RowStats {
       const int mid = (lo + hi) >> 1;
       if (C.rowoff[mid] <= r_first) lo = mid; else hi = mid;
     }
-    int b = lo, kb = 0, nrows_b = 0, r_base = 0, r_cur = -1, pos = 0, kind = 0, x = -1;
+    int b = lo, kb = 0, nrows_b = 0, r_base = 0, r_cur = -1, pos = 0, kind = 0, x = -1, ri = 0;
+    const int stride = 2 * P.k + 1;   // record rows per sequence (the most a sequence has)
     for (int u = u0, q = 0; u < u1; ++u, ++q) {
       const int r = u / P.np, j = u - r * P.np;
       if (r != r_cur) {   // the next row: its sequence, position and drafted token
@@ -264,7 +271,7 @@ struct RowStats {
           nrows_b = C.rowoff[b + 1] - r_base;
           kb = P.greedy ? nrows_b - 1 : (nrows_b - 1) >> 1;
         }
-        const int ri = r - r_base;
+        ri = r - r_base;
         if (P.greedy) { pos = ri; kind = 0; }
         else if (ri < 2 * kb) { pos = ri >> 1; kind = ri & 1; }
         else { pos = kb; kind = 0; }
@@ -281,7 +288,7 @@ struct RowStats {
         const long long off = static_cast<long long>(j) * kChunkBytes;
         const int bytes = static_cast<int>(min(static_cast<long long>(kChunkBytes), row_bytes - off));
         RDesc& d = C.desc[s];
-        d.u = u - u0; d.rec = u; d.part = j; d.bytes = bytes;
+        d.u = u - u0; d.rec = (b * stride + ri) * P.np + j; d.part = j; d.bytes = bytes;
         d.b = b; d.kb = kb; d.pos = pos; d.kind = kind; d.x = x;
         mbar_expect_tx(&C.full[s], static_cast<uint32_t>(bytes));
         bulk_load_hint(ring + static_cast<size_t>(s) * kChunkBytes, row_ptr(P, b, pos, kind) + off,
@@ -484,11 +491,7 @@ __global__ void __launch_bounds__(kRThreads, 1) rows_stats_kernel(const VerifyPa
     __syncthreads();
     carry = C.rowoff[min(B, base + kRThreads)];
   }
-  if (blockIdx.x == 0) {
-    // the first CTA publishes the offsets for the decision kernel
-    for (int i = tid; i <= B; i += kRThreads) P.pw.rowoff[i] = C.rowoff[i];
-    if (tid == 0) *P.pw.njobs = 0;
-  }
+  if (blockIdx.x == 0 && tid == 0) *P.pw.njobs = 0;   // (the previous call is complete)
   RowStats<ELT, GREEDY> k(P, C, ring, lane, warp);
   if (warp == kRProducer) k.produce();
   else k.consume();
@@ -537,9 +540,9 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
   const int b = blockIdx.x * (kRSmallThreads / 32) + wi;
   if (b >= P.B) return;
-  const int k = P.k, t = b;
-  // everything that depends on b alone, in one round trip
-  const int r0 = __ldcg(P.pw.rowoff + b), r1 = __ldcg(P.pw.rowoff + b + 1);
+  const int k = P.k;
+  // everything that depends on b alone, in one round trip (the records sit at
+  // a fixed stride of 2k + 1 rows per sequence)
   const int kb_in = __ldg(P.draft_len + b);
   const int x_all = lane < k ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
   const float ul = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
     }
     __syncwarp();
   }
-  if (r1 == r0) {
+  if (kb_in < 0 || kb_in > k) {
     // an invalid k_b: no rows were read; the sequence emits nothing
     int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
     for (int j = lane; j <= k; j += 32) ot[j] = -1;
@@ -584,7 +587,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
   float bK = 0.f, bS = 0.f;                             // the bonus row
   const int nrows = GREEDY ? kb + 1 : 2 * kb + 1;
   const int np = P.np, nrec = nrows * np;
-  const float4* recs = P.pw.rec + static_cast<size_t>(r0) * np;
+  const float4* recs = P.pw.rec + static_cast<size_t>(b) * (2 * k + 1) * np;
   // the sequence's piece records, 32 at a time (one load per lane, all in
   // flight together); row ri's records are lanes ri np - batch, ...
   int batch = 0;
@@ -661,9 +664,12 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
     if (lane == 0) j = atomicAdd(P.pw.njobs, 1);
     j = __shfl_sync(0xffffffffu, j, 0);
     if (lane == 0) {
-      P.pw.job[j] = make_int4(t, b, a, kb);
+      P.pw.job[j] = make_int4(__float_as_int(s_samp), b, a, kb);
       P.pw.jobn[j] = make_float4(aKt, aLt, aGh, aGl);
     }
+    // the accepted prefix and the empty tail now; the draw writes token a
+    int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
+    if (lane <= k) ot[lane] = lane < a ? xl : -1;
     return;
   }
   // every draft accepted: the bonus token from the bonus row's segment sums,
@@ -863,14 +869,13 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyP
     pp += __ldcg(pm + g);
   }
   const int b = jb.y, a = jb.z, kb = jb.w, k = P.k;
-  const int xl = lane < a ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
   const float rtot = warp_sum(r);
   // exact arithmetic rules a zero residual out (a rejection implies p > q
   // somewhere); if rounding leaves none, the draw is from p_a (counted)
   const bool resid = rtot > 0.f;
   const float tot = resid ? rtot : warp_sum(pp);
   int err = (rtot != rtot || tot != tot) ? kErrTime : 0;   // a timed-out re-read left NaN
-  const float s = __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + k);
+  const float s = __int_as_float(jb.x);   // the sampling uniform, carried by the job
   int seg;
   float seg_t;
   locate_seg(resid ? rm : pm, nseg, s * tot, lane, seg, seg_t);
@@ -886,7 +891,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyP
     else
       y = walk_seg<ELT, kRDrawVecs, false>(rowT, nullptr, v0, nvec_row, seg_t, P.c2, jn.x, jn.y, 0.f, 0.f, lane);
   }
-  write_outputs(P, b, kb, a, y, err, resid ? 0 : 1, xl, lane);
+  write_outputs(P, b, kb, a, y, err, resid ? 0 : 1, -1, lane, true);
 }
 
 cudaError_t launch_dep(void (*fn)(const VerifyParams), int grid, int threads, int smem, cudaStream_t s,
