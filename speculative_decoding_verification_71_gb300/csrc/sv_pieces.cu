@@ -716,27 +716,24 @@ struct RowResid {
   unsigned char* ring;
   const int lane, warp;
   const long long row_bytes;
-  int u0, u1;                  // this CTA's half-pieces [u0, u1) of jobs * nr
+  // half-pieces are dealt round robin (this CTA's: blockIdx.x + i * grid), so
+  // that the first one's job is known before the job count arrives
 
   __device__ RowResid(const VerifyParams& p, RCtrl& c, unsigned char* r, int ln, int wp)
-      : P(p), C(c), ring(r), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * p.elt) {
-    const long long units = static_cast<long long>(__ldcg(p.pw.njobs)) * p.nr;
-    u0 = static_cast<int>(units * blockIdx.x / gridDim.x);
-    u1 = static_cast<int>(units * (blockIdx.x + 1) / gridDim.x);
-  }
+      : P(p), C(c), ring(r), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * p.elt) {}
 
   __device__ void produce() {
     const uint64_t first_out = evict_first_policy();
-    int j_cur = -1;
+    const int nr = P.nr, G = gridDim.x;
+    // the count and the first job in one round trip; each later job one
+    // half-piece ahead
+    const int units = __ldcg(P.pw.njobs) * nr;
+    int u = blockIdx.x, j = u / nr;
     int4 jb = make_int4(0, 0, 0, 0);
     float4 jn = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int u = u0, q = 0; u < u1; ++u, ++q) {
-      const int j = u / P.nr, h = u - j * P.nr;
-      if (j != j_cur) {
-        jb = __ldcg(P.pw.job + j);
-        jn = __ldcg(P.pw.jobn + j);
-        j_cur = j;
-      }
+    if (j < P.B) { jb = __ldcg(P.pw.job + j); jn = __ldcg(P.pw.jobn + j); }
+    for (int q = 0; u < units; u += G, ++q) {
+      const int h = u - j * nr;
       const int s = q % kRStages;
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(&C.empty[s], ((q / kRStages) & 1) ^ 1, kDrainLimitNs) ? 1 : 0;
@@ -748,7 +745,7 @@ struct RowResid {
         const long long off = static_cast<long long>(h) * kRHalf;
         const int bytes = static_cast<int>(min(static_cast<long long>(kRHalf), row_bytes - off));
         RDesc& d = C.desc[s];
-        d.u = u - u0; d.rec = j; d.part = h; d.bytes = bytes;
+        d.u = q; d.rec = j; d.part = h; d.bytes = bytes;
         d.b = jb.y; d.kb = jb.w; d.pos = jb.z; d.kind = 2; d.x = -1;
         d.num = jn;
         unsigned char* dst = ring + static_cast<size_t>(s) * kChunkBytes;
@@ -758,6 +755,8 @@ struct RowResid {
                        first_out);
       }
       __syncwarp();
+      j = (u + G) / nr;   // the next half-piece's job
+      if (u + G < units) { jb = __ldcg(P.pw.job + j); jn = __ldcg(P.pw.jobn + j); }
     }
   }
 
@@ -765,7 +764,8 @@ struct RowResid {
   // of the cluster kernel (no cancellation where p ~ q).
   __device__ void consume() {
     const float c2 = P.c2;
-    for (int u = u0, q = 0; u < u1; ++u, ++q) {
+    const int units = __ldcg(P.pw.njobs) * P.nr;
+    for (int u = blockIdx.x, q = 0; u < units; u += gridDim.x, ++q) {
       const int s = q % kRStages;
       bool timed_out = false;
       if (!mbar_wait_bounded(&C.full[s], static_cast<uint32_t>(q / kRStages) & 1u, P.wait_limit_ns)) {
