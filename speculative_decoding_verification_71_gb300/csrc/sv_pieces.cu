@@ -542,8 +542,12 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
   if (b >= P.B) return;
   const int k = P.k;
   // everything that depends on b alone, in one round trip (the records sit at
-  // a fixed stride of 2k + 1 rows per sequence)
+  // a fixed stride of 2k + 1 rows per sequence; the first 32 are loaded
+  // before the length is known, the unused ones ignored)
   const int kb_in = __ldg(P.draft_len + b);
+  const float4 held0 = lane < (GREEDY ? k + 1 : 2 * k + 1) * P.np
+                           ? __ldcg(P.pw.rec + static_cast<size_t>(b) * (2 * k + 1) * P.np + lane)
+                           : make_float4(-INFINITY, 0.f, 0.f, 0.f);
   const int x_all = lane < k ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
   const float ul = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
   const int nseg_b = P.np * kRWarps;
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
   // the sequence's piece records, 32 at a time (one load per lane, all in
   // flight together); row ri's records are lanes ri np - batch, ...
   int batch = 0;
-  float4 held = lane < nrec ? __ldcg(recs + lane) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  float4 held = lane < nrec ? held0 : make_float4(-INFINITY, 0.f, 0.f, 0.f);
   for (int ri = 0; ri < nrows; ++ri) {
     int pos, kind;
     if (GREEDY) { pos = ri; kind = 0; }
@@ -855,7 +859,10 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyP
   grid_dependency_wait();      // the re-read masses
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * (kRSmallThreads / 32) + (threadIdx.x >> 5);
-  if (j >= __ldcg(P.pw.njobs)) return;
+  if (j >= P.B) return;
+  // the job, its numbers and masses with the job count, in one round trip
+  // (j < B: in bounds whether or not it is a job of this call)
+  const int njobs = __ldcg(P.pw.njobs);
   const int4 jb = __ldcg(P.pw.job + j);
   const float4 jn = __ldcg(P.pw.jobn + j);
   const int nseg = P.nr * kRWarps;
@@ -868,6 +875,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyP
     r += __ldcg(rm + g);
     pp += __ldcg(pm + g);
   }
+  if (j >= njobs) return;
   const int b = jb.y, a = jb.z, kb = jb.w, k = P.k;
   const float rtot = warp_sum(r);
   // exact arithmetic rules a zero residual out (a rejection implies p > q
