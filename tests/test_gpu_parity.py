@@ -68,6 +68,8 @@ SMALL_CASES = [
     ("grpo", dict(B=32, k=3, V=8192)),                             # near-full acceptance
     ("qwen_b32", dict(B=16, k=0, V=3000)),                         # speculation off everywhere
     ("qwen_b32", dict(B=8, k=3, V=151936)),                        # full vocabulary rows
+    ("ragged", dict(B=37, k=3, V=8192)),                           # odd batch: the last warp of a block idle
+    ("ragged", dict(B=37, k=3, V=8192, T=0.0)),                    # the same, greedy
 ]
 
 
