@@ -127,6 +127,7 @@ sv_status create_pieces(sv_ctx* ctx) {
   auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
   const size_t o_rec = take(rows * ctx->np * 16), o_bseg = take(B * ctx->np * 16 * 8);
   const size_t o_job = take(B * 16), o_jobn = take(B * 16), o_njobs = take(4);
+  const size_t o_bonus = take(B * 16), o_epoch = take(4);
   const size_t o_rmass = take(B * ctx->nr * 16 * 4), o_pmass = take(B * ctx->nr * 16 * 4);
   e = cudaMalloc(&ctx->pw_mem, off);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMalloc(pieces workspace)");
@@ -139,6 +140,8 @@ sv_status create_pieces(sv_ctx* ctx) {
   w.job = reinterpret_cast<int4*>(base + o_job);
   w.jobn = reinterpret_cast<float4*>(base + o_jobn);
   w.njobs = reinterpret_cast<int*>(base + o_njobs);
+  w.bonus = reinterpret_cast<float4*>(base + o_bonus);
+  w.epoch = reinterpret_cast<int*>(base + o_epoch);
   w.rmass = reinterpret_cast<float*>(base + o_rmass);
   w.pmass = reinterpret_cast<float*>(base + o_pmass);
   ctx->pieces_ctas = prop.multiProcessorCount;   // one CTA per SM (the shared memory allows no more)

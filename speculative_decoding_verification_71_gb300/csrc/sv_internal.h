@@ -71,6 +71,8 @@ struct PiecesWs {
   int4* job;         // [max_B]       a rejected pair to draw from: (sampling uniform's bits, b, a, k_b)
   float4* jobn;      // [max_B]       ... its (K_t, L_t, Gh, Gl)
   int* njobs;        // [1]
+  float4* bonus;     // [max_B]       a fully accepted sequence's bonus row: (call number's bits, K, L, s)
+  int* epoch;        // [1]           the call number (counted by each call's statistics kernel)
   float* rmass;      // [max_B * nr * 16]  per job, each re-read segment's sum of max(0, p - q)
   float* pmass;      // [max_B * nr * 16]  ... and of p (zero-residual fallback)
 };

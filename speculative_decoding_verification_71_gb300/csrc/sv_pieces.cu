@@ -491,7 +491,10 @@ __global__ void __launch_bounds__(kRThreads, 1) rows_stats_kernel(const VerifyPa
     __syncthreads();
     carry = C.rowoff[min(B, base + kRThreads)];
   }
-  if (blockIdx.x == 0 && tid == 0) *P.pw.njobs = 0;   // (the previous call is complete)
+  if (blockIdx.x == 0 && tid == 0) {   // (the previous call is complete)
+    *P.pw.njobs = 0;
+    *P.pw.epoch += 1;
+  }
   RowStats<ELT, GREEDY> k(P, C, ring, lane, warp);
   if (warp == kRProducer) k.produce();
   else k.consume();
@@ -534,7 +537,6 @@ __device__ void merge_row(const VerifyParams& P, float4 rc, int lane, float& M, 
 
 template <int ELT, bool GREEDY>
 __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const VerifyParams P) {
-  __shared__ float bmass[kRSmallThreads / 32][kMaxChunks * kRWarps];
   grid_dependency_wait();      // the pieces' records
   grid_dependents_launch();
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
@@ -550,14 +552,6 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
                            : make_float4(-INFINITY, 0.f, 0.f, 0.f);
   const int x_all = lane < k ? __ldg(P.tokens + static_cast<size_t>(b) * k + lane) : -1;
   const float ul = (!GREEDY && lane <= k) ? __ldg(P.uniforms + static_cast<size_t>(b) * (k + 1) + lane) : 0.f;
-  const int nseg_b = P.np * kRWarps;
-  float2 bsg[kMaxChunks * kRWarps / 32];
-#pragma unroll
-  for (int i = 0; i < kMaxChunks * kRWarps / 32; ++i) {
-    const int g = lane + 32 * i;
-    bsg[i] = (!GREEDY && g < nseg_b) ? __ldcg(P.pw.bseg + static_cast<size_t>(b) * nseg_b + g)
-                                     : make_float2(-INFINITY, 0.f);
-  }
   if (P.diag) {   // every diagnostic of the sequence NaN first: only the rows read get values
     for (int j = lane; j <= k; j += 32) {
       const size_t i = static_cast<size_t>(b) * (k + 1) + j;
@@ -676,34 +670,13 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
     if (lane <= k) ot[lane] = lane < a ? xl : -1;
     return;
   }
-  // every draft accepted: the bonus token from the bonus row's segment sums,
-  // then one segment read again
-  const float L = log2f(bS);
-  const int nseg = P.np * kRWarps;
-  float* wm = bmass[wi];
-#pragma unroll
-  for (int i = 0; i < kMaxChunks * kRWarps / 32; ++i) {
-    const int g = lane + 32 * i;
-    if (g < nseg) wm[g] = bsg[i].x == -INFINITY ? 0.f : bsg[i].y * fast_exp2(__fsub_rn(bsg[i].x, bK) - L);
-  }
-  __syncwarp();
-  float part = 0.f;
-  {
-    const int per = (nseg + 31) / 32;
-    const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
-    for (int g = g0; g < g1; ++g) part += wm[g];
-  }
-  const float tot = warp_sum(part);
-  int seg;
-  float seg_t;
-  locate_seg(wm, nseg, s_samp * tot, lane, seg, seg_t);
-  if (diag && lane == 0) P.ws.mass[static_cast<size_t>(b) * (k + 1) + kb] = tot;
-  const int nvec_row = static_cast<int>((static_cast<long long>(P.V) * ELT) / 16);
-  if (seg >= 0) {
-    const int v0 = (seg / kRWarps) * (kChunkBytes / 16) + (seg % kRWarps) * (kRStatVecs * 32);
-    y = walk_seg<ELT, kRStatVecs, false>(row_ptr(P, b, kb, 0), nullptr, v0, nvec_row, seg_t, c2, bK, L, 0.f, 0.f, lane);
-  }
-  write_outputs(P, b, kb, -1, y, 0, 0, xl, lane);
+  // every draft accepted: the bonus token is drawn by the draw kernel, from
+  // the bonus row's segment sums; here the accepted prefix and the row's
+  // numbers, tagged with the call
+  int* ot = P.out_tokens + static_cast<size_t>(b) * (k + 1);
+  if (lane <= k) ot[lane] = lane < kb ? xl : -1;
+  if (lane == 0)
+    P.pw.bonus[b] = make_float4(__int_as_float(__ldcg(P.pw.epoch)), bK, log2f(bS), s_samp);
 }
 
 // ---------------------------------------------------------------------------
@@ -854,12 +827,67 @@ __global__ void __launch_bounds__(kRThreads, 1) rows_resid_kernel(const VerifyPa
 // ---------------------------------------------------------------------------
 // rows_draw_kernel: one warp per job, the residual draw
 // ---------------------------------------------------------------------------
+// The bonus draw of sequence b, if every draft of it was accepted in this
+// call (one warp; wm: kMaxChunks * kRWarps floats of shared scratch): the
+// segment holding s * S among the bonus row's segment sums, kept while it
+// streamed, then that segment read again.
+template <int ELT>
+__device__ void bonus_draw(const VerifyParams& P, int b, int lane, float* wm) {
+  const int k = P.k;
+  // the row's numbers, the call number, the length and the segment sums in one round trip
+  const float4 bo = __ldcg(P.pw.bonus + b);
+  const int ep = __ldcg(P.pw.epoch);
+  const int kb = __ldg(P.draft_len + b);
+  const int nseg = P.np * kRWarps;
+  float2 bsg[kMaxChunks * kRWarps / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxChunks * kRWarps / 32; ++i) {
+    const int g = lane + 32 * i;
+    bsg[i] = g < nseg ? __ldcg(P.pw.bseg + static_cast<size_t>(b) * nseg + g) : make_float2(-INFINITY, 0.f);
+  }
+  if (__float_as_int(bo.x) != ep) return;   // not a fully accepted sequence of this call
+  const float bK = bo.y, L = bo.z, s_samp = bo.w;
+#pragma unroll
+  for (int i = 0; i < kMaxChunks * kRWarps / 32; ++i) {
+    const int g = lane + 32 * i;
+    if (g < nseg) wm[g] = bsg[i].x == -INFINITY ? 0.f : bsg[i].y * fast_exp2(__fsub_rn(bsg[i].x, bK) - L);
+  }
+  __syncwarp();
+  float part = 0.f;
+  {
+    const int per = (nseg + 31) / 32;
+    const int g0 = min(nseg, lane * per), g1 = min(nseg, g0 + per);
+    for (int g = g0; g < g1; ++g) part += wm[g];
+  }
+  const float tot = warp_sum(part);
+  int seg;
+  float seg_t;
+  locate_seg(wm, nseg, s_samp * tot, lane, seg, seg_t);
+  if (P.diag && lane == 0) P.ws.mass[static_cast<size_t>(b) * (k + 1) + kb] = tot;
+  const int nvec_row = static_cast<int>((static_cast<long long>(P.V) * ELT) / 16);
+  int y = -1;
+  if (seg >= 0) {
+    const int v0 = (seg / kRWarps) * (kChunkBytes / 16) + (seg % kRWarps) * (kRStatVecs * 32);
+    y = walk_seg<ELT, kRStatVecs, false>(row_ptr(P, b, kb, 0), nullptr, v0, nvec_row, seg_t, P.c2, bK, L, 0.f, 0.f,
+                                        lane);
+  }
+  write_outputs(P, b, kb, -1, y, 0, 0, -1, lane, true);
+}
+
+// Warps [0, B): the residual draw of job w; warps [B, 2B): the bonus draw of
+// sequence w - B.
 template <int ELT>
 __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyParams P) {
+  __shared__ float bmass[kRSmallThreads / 32][kMaxChunks * kRWarps];
   grid_dependency_wait();      // the re-read masses
-  const int lane = threadIdx.x & 31;
-  const int j = blockIdx.x * (kRSmallThreads / 32) + (threadIdx.x >> 5);
-  if (j >= P.B) return;
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int w = blockIdx.x * (kRSmallThreads / 32) + wi;
+  if (w >= 2 * P.B) return;
+  if (w >= P.B) {
+    bonus_draw<ELT>(P, w - P.B, lane, bmass[wi]);
+    return;
+  }
+  const int j = w;
   // the job, its numbers and masses with the job count, in one round trip
   // (j < B: in bounds whether or not it is a job of this call)
   const int njobs = __ldcg(P.pw.njobs);
@@ -925,7 +953,7 @@ cudaError_t launch_rows(const VerifyParams& p, cudaStream_t s) {
   if (e == cudaSuccess) e = launch_dep(rows_decide_kernel<ELT, GREEDY>, small, kRSmallThreads, 0, s, p);
   if (!GREEDY) {
     if (e == cudaSuccess) e = launch_dep(rows_resid_kernel<ELT>, p.ctas, kRThreads, smem, s, p);
-    if (e == cudaSuccess) e = launch_dep(rows_draw_kernel<ELT>, small, kRSmallThreads, 0, s, p);
+    if (e == cudaSuccess) e = launch_dep(rows_draw_kernel<ELT>, 2 * small, kRSmallThreads, 0, s, p);
   }
   return e;
 }
