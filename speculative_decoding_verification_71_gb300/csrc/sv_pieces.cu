@@ -15,16 +15,18 @@
 //                       with cp.async.bulk, 16 consumer warps reduce them; the
 //                       last warp to finish a piece combines the warps' parts
 //                       into its record (max, sum of 2^(z c - fl(max c)), the
-//                       drafted token's logit); bonus rows also keep each
+//                       drafted token's logit), at a fixed place per
+//                       (sequence, row, piece); bonus rows also keep each
 //                       warp segment's sum for the draw;
 //   rows_decide_kernel  one warp per sequence: the rows from their pieces, the
-//                       tests, the first rejection; the bonus draw (one
-//                       segment read again) or a job for the residual; an
-//                       invalid k_b answered;
+//                       tests, the first rejection, the accepted prefix; a
+//                       job for the residual, or the bonus row's numbers for
+//                       its draw; an invalid k_b answered;
 //   rows_resid_kernel   every job's rejected pair read again in 32 KB
-//                       half-pieces spread over the CTAs: each warp segment's
-//                       sums of max(0, p - q) and of p;
-//   rows_draw_kernel    one warp per job: the segment holding s * S, the token.
+//                       half-pieces dealt round robin over the CTAs: each
+//                       warp segment's sums of max(0, p - q) and of p;
+//   rows_draw_kernel    one warp per job and one per fully accepted
+//                       sequence: the segment holding s * S, the token.
 // Rows must be 16-byte aligned (bulk copies); other calls run the cluster
 // kernel.
 
