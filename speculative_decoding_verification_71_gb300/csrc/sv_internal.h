@@ -62,7 +62,7 @@ struct Workspace {
 
 // Workspace of the row-streaming schedule (sv_pieces.cu), owned by the
 // context.  A sequence's rows are target 0, draft 0, ..., target k_b; a
-// piece is 64 KB of one row (np per row), a re-read half-piece 32 KB of each
+// piece is 64 KB of one row (np per row), a re-read half-piece 16 KB of each
 // row of a pair (nr per row).
 struct PiecesWs {
   float4* rec;       // [max_B * (2 max_k + 1) * np]  a piece's (M, S about fl(M c), token logit, flags), at
@@ -103,7 +103,7 @@ struct VerifyParams {
   // row streaming (sv_pieces.cu) instead of the cluster kernel when set
   int pieces;
   int np;               // 64 KB pieces per row
-  int nr;               // 32 KB half-pieces per row (re-reads)
+  int nr;               // 16 KB half-pieces per row (re-reads)
   int ctas;             // grid of the streaming kernels (one CTA per SM)
   PiecesWs pw;
 };
@@ -128,11 +128,12 @@ int pieces_smem_bytes();
 int pieces_threads();                                       // threads of the streaming kernels
 cudaError_t prepare_pieces_kernel();
 cudaError_t launch_pieces(const VerifyParams& p, cudaStream_t s);   // after plan_kernel
-// 64 KB pieces and 32 KB half-pieces per row of V logits of elt bytes.
+// 64 KB pieces and 16 KB re-read half-pieces per row of V logits of elt bytes.
+constexpr int kRowsHalfBytes = kChunkBytes / 4;          // a re-read slot: this much of each row of a pair
 inline void pieces_shape(int V, int elt, int& np, int& nr) {
   const long long row = static_cast<long long>(V) * elt;
   np = static_cast<int>((row + kChunkBytes - 1) / kChunkBytes);
-  nr = static_cast<int>((row + kChunkBytes / 2 - 1) / (kChunkBytes / 2));
+  nr = static_cast<int>((row + kRowsHalfBytes - 1) / kRowsHalfBytes);
 }
 
 // Cluster size chosen when the caller leaves it open.  A sequence is the

@@ -22,8 +22,8 @@
 //                       tests, the first rejection, the accepted prefix; a
 //                       job for the residual, or the bonus row's numbers for
 //                       its draw; an invalid k_b answered;
-//   rows_resid_kernel   every job's rejected pair read again in 32 KB
-//                       half-pieces dealt round robin over the CTAs: each
+//   rows_resid_kernel   every job's rejected pair read again in 16 KB
+//                       half-pieces dealt round robin over two CTAs per SM: each
 //                       warp segment's sums of max(0, p - q) and of p;
 //   rows_draw_kernel    one warp per job and one per fully accepted
 //                       sequence: the segment holding s * S, the token.
@@ -45,9 +45,10 @@ constexpr int kRWarps = kConsumerWarps;              // consumer warps (16)
 constexpr int kRProducer = kRWarps;                  // the producer warp's index
 constexpr int kRThreads = (kRWarps + 1) * 32;
 constexpr int kRStages = 3;                          // 64 KB staging slots
-constexpr int kRHalf = kChunkBytes / 2;              // a re-read slot: 32 KB of each row of the pair
+constexpr int kRHalf = kRowsHalfBytes;               // a re-read slot: 16 KB of each row of the pair
+constexpr int kQSlot = 2 * kRHalf;                   // re-read staging slot (both rows)
 constexpr int kRStatVecs = kChunkBytes / 16 / kRWarps / 32;   // 8 vectors per lane and piece
-constexpr int kRDrawVecs = kRHalf / 16 / kRWarps / 32;        // 4 vectors per lane and half-piece
+constexpr int kRDrawVecs = kRHalf / 16 / kRWarps / 32;        // 2 vectors per lane and half-piece
 constexpr int kRBufs = kRStages + 1;                 // per-piece part buffers (warps run at most a ring apart)
 constexpr int kRSmallThreads = 64;                   // decide / draw kernels: 2 warps, one sequence each
 
@@ -82,6 +83,17 @@ struct RCtrl {
   int warp_tot[32];
 };
 constexpr int kRCtrlBytes = ((static_cast<int>(sizeof(RCtrl)) + 1023) / 1024) * 1024;
+
+// The re-read kernel's control block: two CTAs share an SM (34 warps), each
+// with three 32 KB slots.
+struct QCtrl {
+  uint64_t full[kRStages];
+  uint64_t empty[kRStages];
+  RDesc desc[kRStages];
+};
+constexpr int kQCtrlBytes = ((static_cast<int>(sizeof(QCtrl)) + 1023) / 1024) * 1024;
+constexpr int kQSmem = kQCtrlBytes + kRStages * kQSlot;
+static_assert(2 * kQSmem <= 227 * 1024, "two re-read CTAs must fit in one SM");
 static_assert(kRCtrlBytes + kRStages * kChunkBytes <= 227 * 1024, "three slots must fit in one CTA");
 
 __device__ __forceinline__ const unsigned char* row_ptr(const VerifyParams& P, int b, int pos, int kind) {
@@ -682,7 +694,7 @@ __global__ void __launch_bounds__(kRSmallThreads) rows_decide_kernel(const Verif
 }
 
 // ---------------------------------------------------------------------------
-// rows_resid_kernel: the rejected pairs read again, 32 KB of each row per slot
+// rows_resid_kernel: the rejected pairs read again, 16 KB of each row per slot
 // ---------------------------------------------------------------------------
 
 template <int ELT>
@@ -691,14 +703,14 @@ struct RowResid {
   static constexpr int NV = V::N;
 
   const VerifyParams& P;
-  RCtrl& C;
+  QCtrl& C;
   unsigned char* ring;
   const int lane, warp;
   const long long row_bytes;
   // half-pieces are dealt round robin (this CTA's: blockIdx.x + i * grid), so
   // that the first one's job is known before the job count arrives
 
-  __device__ RowResid(const VerifyParams& p, RCtrl& c, unsigned char* r, int ln, int wp)
+  __device__ RowResid(const VerifyParams& p, QCtrl& c, unsigned char* r, int ln, int wp)
       : P(p), C(c), ring(r), lane(ln), warp(wp), row_bytes(static_cast<long long>(p.V) * p.elt) {}
 
   __device__ void produce() {
@@ -727,7 +739,7 @@ struct RowResid {
         d.u = q; d.rec = j; d.part = h; d.bytes = bytes;
         d.b = jb.y; d.kb = jb.w; d.pos = jb.z; d.kind = 2; d.x = -1;
         d.num = jn;
-        unsigned char* dst = ring + static_cast<size_t>(s) * kChunkBytes;
+        unsigned char* dst = ring + static_cast<size_t>(s) * kQSlot;
         mbar_expect_tx(&C.full[s], static_cast<uint32_t>(2 * bytes));
         bulk_load_hint(dst, row_ptr(P, jb.y, jb.z, 0) + off, static_cast<uint32_t>(bytes), &C.full[s], first_out);
         bulk_load_hint(dst + kRHalf, row_ptr(P, jb.y, jb.z, 1) + off, static_cast<uint32_t>(bytes), &C.full[s],
@@ -755,7 +767,7 @@ struct RowResid {
         }
       }
       const RDesc d = C.desc[s];
-      const unsigned char* data = ring + static_cast<size_t>(s) * kChunkBytes;
+      const unsigned char* data = ring + static_cast<size_t>(s) * kQSlot;
       const int nvec = (d.bytes + 15) / 16;
       uint4 rt[kRDrawVecs], rd[kRDrawVecs];
 #pragma unroll
@@ -806,10 +818,10 @@ struct RowResid {
 };
 
 template <int ELT>
-__global__ void __launch_bounds__(kRThreads, 1) rows_resid_kernel(const VerifyParams P) {
+__global__ void __launch_bounds__(kRThreads, 2) rows_resid_kernel(const VerifyParams P) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  RCtrl& C = *reinterpret_cast<RCtrl*>(smem);
-  unsigned char* ring = smem + kRCtrlBytes;
+  QCtrl& C = *reinterpret_cast<QCtrl*>(smem);
+  unsigned char* ring = smem + kQCtrlBytes;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     for (int s = 0; s < kRStages; ++s) {
@@ -954,7 +966,7 @@ cudaError_t launch_rows(const VerifyParams& p, cudaStream_t s) {
   cudaError_t e = launch_dep(rows_stats_kernel<ELT, GREEDY>, p.ctas, kRThreads, smem, s, p);
   if (e == cudaSuccess) e = launch_dep(rows_decide_kernel<ELT, GREEDY>, small, kRSmallThreads, 0, s, p);
   if (!GREEDY) {
-    if (e == cudaSuccess) e = launch_dep(rows_resid_kernel<ELT>, p.ctas, kRThreads, smem, s, p);
+    if (e == cudaSuccess) e = launch_dep(rows_resid_kernel<ELT>, 2 * p.ctas, kRThreads, kQSmem, s, p);
     if (e == cudaSuccess) e = launch_dep(rows_draw_kernel<ELT>, 2 * small, kRSmallThreads, 0, s, p);
   }
   return e;
@@ -966,14 +978,18 @@ int pieces_smem_bytes() { return kRCtrlBytes + kRStages * kChunkBytes; }
 int pieces_threads() { return kRThreads; }
 
 cudaError_t prepare_pieces_kernel() {
-  const void* fns[6] = {reinterpret_cast<const void*>(&rows_stats_kernel<2, false>),
+  const void* fns[4] = {reinterpret_cast<const void*>(&rows_stats_kernel<2, false>),
                         reinterpret_cast<const void*>(&rows_stats_kernel<4, false>),
                         reinterpret_cast<const void*>(&rows_stats_kernel<2, true>),
-                        reinterpret_cast<const void*>(&rows_stats_kernel<4, true>),
-                        reinterpret_cast<const void*>(&rows_resid_kernel<2>),
-                        reinterpret_cast<const void*>(&rows_resid_kernel<4>)};
+                        reinterpret_cast<const void*>(&rows_stats_kernel<4, true>)};
   for (const void* f : fns) {
     cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, pieces_smem_bytes());
+    if (e != cudaSuccess) return e;
+  }
+  const void* resid[2] = {reinterpret_cast<const void*>(&rows_resid_kernel<2>),
+                          reinterpret_cast<const void*>(&rows_resid_kernel<4>)};
+  for (const void* f : resid) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
