@@ -963,10 +963,15 @@ template <int ELT, bool GREEDY>
 cudaError_t launch_rows(const VerifyParams& p, cudaStream_t s) {
   const int smem = kRCtrlBytes + kRStages * kChunkBytes;
   const int small = (p.B + kRSmallThreads / 32 - 1) / (kRSmallThreads / 32);
-  cudaError_t e = launch_dep(rows_stats_kernel<ELT, GREEDY>, p.ctas, kRThreads, smem, s, p);
+  // grids no larger than the most work a batch of this shape can hold
+  const long long most_pieces = static_cast<long long>(p.B) * (GREEDY ? p.k + 1 : 2 * p.k + 1) * p.np;
+  const long long most_halves = static_cast<long long>(p.B) * p.nr;
+  const int stats_ctas = static_cast<int>(min(static_cast<long long>(p.ctas), most_pieces));
+  const int resid_ctas = static_cast<int>(min(2LL * p.ctas, most_halves));
+  cudaError_t e = launch_dep(rows_stats_kernel<ELT, GREEDY>, stats_ctas, kRThreads, smem, s, p);
   if (e == cudaSuccess) e = launch_dep(rows_decide_kernel<ELT, GREEDY>, small, kRSmallThreads, 0, s, p);
   if (!GREEDY) {
-    if (e == cudaSuccess) e = launch_dep(rows_resid_kernel<ELT>, 2 * p.ctas, kRThreads, kQSmem, s, p);
+    if (e == cudaSuccess) e = launch_dep(rows_resid_kernel<ELT>, resid_ctas, kRThreads, kQSmem, s, p);
     if (e == cudaSuccess) e = launch_dep(rows_draw_kernel<ELT>, 2 * small, kRSmallThreads, 0, s, p);
   }
   return e;
