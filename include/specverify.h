@@ -133,6 +133,12 @@ sv_status sv_destroy(sv_ctx *ctx);
  * Requires 1 <= B <= max_B, 0 <= k <= max_k.  Rows are read with 16-byte
  * bulk copies when V * sizeof(dtype) is a multiple of 16 and the logit
  * pointers are 16-byte aligned, and with plain loads otherwise.
+ * The inputs must be complete when the call is enqueued: under row
+ * streaming the call's first kernel starts reading them (not the workspace,
+ * not the outputs) while the previous kernel on the stream finishes, when
+ * that kernel allows its dependents an early start (this library's last
+ * kernel of a call does; kernels launched without programmatic dependent
+ * launch, such as PyTorch's, never do).
  * Returns SV_OK once the work is enqueued; device-side problems are reported
  * by spec_verify_stats.
  */

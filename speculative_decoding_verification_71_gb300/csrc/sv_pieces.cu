@@ -471,9 +471,12 @@ __global__ void __launch_bounds__(kRThreads, 1) rows_stats_kernel(const VerifyPa
     for (int i = 0; i < kRBufs; ++i) C.cnt[i] = 0;
     fence_mbar_init();
   }
-  grid_dependency_wait();      // nothing of an earlier call still reads the workspace
   grid_dependents_launch();
-  // the call's plan, in every CTA: rows of the sequences before b, in batch
+  // The plan and the producer's copies read only the call's inputs, so they
+  // start before the dependency wait, overlapping the previous call's last
+  // kernel (the inputs are complete when the call is enqueued); everything
+  // that writes the workspace waits first (the consumers, below).
+  // The call's plan, in every CTA: rows of the sequences before b, in batch
   // order (2 k_b + 1 each, k_b + 1 for T = 0; none for an invalid k_b)
   const int B = P.B, nw = kRThreads / 32;
   if (tid == 0) C.rowoff[0] = 0;
@@ -505,13 +508,17 @@ __global__ void __launch_bounds__(kRThreads, 1) rows_stats_kernel(const VerifyPa
     __syncthreads();
     carry = C.rowoff[min(B, base + kRThreads)];
   }
-  if (blockIdx.x == 0 && tid == 0) {   // (the previous call is complete)
-    *P.pw.njobs = 0;
-    *P.pw.epoch += 1;
-  }
   RowStats<ELT, GREEDY> k(P, C, ring, lane, warp);
-  if (warp == kRProducer) k.produce();
-  else k.consume();
+  if (warp == kRProducer) {
+    k.produce();
+  } else {
+    grid_dependency_wait();      // the previous call no longer reads the records, sums or counters
+    if (blockIdx.x == 0 && tid == 0) {
+      *P.pw.njobs = 0;
+      *P.pw.epoch += 1;
+    }
+    k.consume();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -894,6 +901,7 @@ template <int ELT>
 __global__ void __launch_bounds__(kRSmallThreads) rows_draw_kernel(const VerifyParams P) {
   __shared__ float bmass[kRSmallThreads / 32][kMaxChunks * kRWarps];
   grid_dependency_wait();      // the re-read masses
+  grid_dependents_launch();    // the next call's statistics kernel may start reading its inputs
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
   const int w = blockIdx.x * (kRSmallThreads / 32) + wi;
   if (w >= 2 * P.B) return;
