@@ -450,6 +450,36 @@ def test_wait_timeout_is_reported_not_hung():
     assert_parity(inp, ver)
 
 
+
+def test_back_to_back_calls_on_one_stream():
+    """Several calls enqueued back to back on one stream, with no host wait
+    between them (under row streaming each call's first kernel starts its
+    reads while the previous call's last kernel runs): different batches,
+    sampling and greedy, both schedules in turn, each output against the
+    oracle."""
+    cases = [small("ragged", B=48, k=3, V=20000, seed=21), small("ragged", B=40, k=4, V=12288, seed=22),
+             small("ragged", B=48, k=3, V=20000, T=0.0, seed=23), small("grpo", B=32, k=3, V=8192, seed=24),
+             small("long_draft", B=24, k=7, V=12288, seed=25)]
+    stream = torch.cuda.Stream()
+    vers = [verifier_for(inp, diagnostics=False) for inp in cases]
+    vers[3].set_kernel(svp.SV_KERNEL_CLUSTER)     # a cluster call in the middle of row-streaming ones
+    outs = []
+    for rep in range(3):
+        for inp, ver in zip(cases, vers):
+            B, k1 = inp["target"].shape[:2]
+            bt, ot = guarded(B * k1, DEV)
+            bl, ol = guarded(B, DEV)
+            ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"], inp["uniforms"], inp["T"],
+                       out_tokens=ot.view(B, k1), out_len=ol, stream=stream)
+            outs.append((inp, bt, bl, ot.view(B, k1), ol))
+    stream.synchronize()
+    refs = [run_oracle(inp) for inp in cases]
+    for i, (inp, bt, bl, ot, ol) in enumerate(outs):
+        assert_guards(bt, bl)
+        ref = refs[i % len(cases)]
+        res = compare(ot.cpu().numpy(), ol.cpu().numpy(), ref, inp["draft_len"].cpu().numpy())
+        assert res["mismatch"] == 0, (i, res["bad"][:10])
+
 # --- full-size workloads: every sequence against the oracle ---------------------
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
