@@ -390,7 +390,11 @@ sv_status spec_verify_noalloc(int B, int k, int V, sv_dtype dtype,
  * the cluster sizes that fit: make it before any stream capture.  Not
  * thread-safe on that first call.  Host-checkable errors (sizes, dtype,
  * temperature < 0 or not finite, NULL pointers) return SV_ERR_INVALID_ARG
- * and launch nothing.  V <= 524288.
+ * and launch nothing.  V <= 524288.  The inputs must be complete when the
+ * call is enqueued: a call's walks may start while the previous kernel on
+ * the stream finishes, when that kernel allows its dependents an early start
+ * (a previous tree call does); the outputs are written only after that
+ * kernel is complete, so consecutive calls may share output buffers.
  * ------------------------------------------------------------------------ */
 
 #define SV_TREE_MAX_NODES 64

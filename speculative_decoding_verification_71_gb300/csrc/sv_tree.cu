@@ -120,6 +120,10 @@ struct TreeShared {
   double slice[kTreeMaxCluster];     // weight of each CTA's slice
   XSlot xs[2];                       // exchange slots (double-buffered)
   XSlot got[kTreeMaxCluster];        // the slots of the last exchange, rank order
+  // the outputs, written to global memory only at the end (after the
+  // dependency wait: the previous call on the stream may still write them)
+  int otok[kTreeMaxNodes], onode[kTreeMaxNodes];
+  float oal[kTreeMaxNodes];
 };
 
 __device__ __forceinline__ uint4 ld_peer_v4(uint32_t a) {
@@ -574,15 +578,16 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     fence_mbar_init();
     sh.failed = 0;
   }
+  // the next kernel on the stream may start (a next call's walk reads only
+  // its inputs until it writes its outputs, after its dependency wait)
+  grid_dependents_launch();
   for (int j = tid; j < M; j += kTreeThreads) {
     sh.par[j] = P.parents[rb + j];
     sh.tok[j] = P.tokens[rb + j];
     sh.u[j] = P.uniforms[rb + j];
-    if (lead) {
-      P.out_tokens[rb + j] = -1;
-      P.out_nodes[rb + j] = -1;
-      if (P.alpha) P.alpha[rb + j] = NAN;
-    }
+    sh.otok[j] = -1;
+    sh.onode[j] = -1;
+    sh.oal[j] = NAN;
   }
   __syncthreads();
   if (tid == 0) {
@@ -697,14 +702,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
           for (int i = 0; i < nk && next < 0; ++i) {
             const int c = sh.kids[i];
             const int ok = (sh.tok[c] == bx);
-            if (P.alpha && lead) P.alpha[rb + c] = ok ? 1.f : 0.f;
+            sh.oal[c] = ok ? 1.f : 0.f;
             if (ok) next = c;
           }
           if (next >= 0) {
-            if (lead) {
-              P.out_nodes[rb + sh.len] = next;
-              P.out_tokens[rb + sh.len] = sh.tok[next];
-            }
+            sh.onode[sh.len] = next;
+            sh.otok[sh.len] = sh.tok[next];
             sh.len += 1;
             sh.cur = next;
           } else {
@@ -794,7 +797,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         }
         const double al = fmin(1.0, rq);
         const bool acc = static_cast<double>(sh.u[c]) < al;
-        if (P.alpha && lead) P.alpha[rb + c] = static_cast<float>(al);
+        sh.oal[c] = static_cast<float>(al);
         sh.next = acc ? c : -1;
       }
       __syncthreads();
@@ -820,10 +823,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     }
     if (accepted >= 0) {
       if (tid == 0) {
-        if (lead) {
-          P.out_nodes[rb + sh.len] = accepted;
-          P.out_tokens[rb + sh.len] = sh.tok[accepted];
-        }
+        sh.onode[sh.len] = accepted;
+        sh.otok[sh.len] = sh.tok[accepted];
         sh.len += 1;
         sh.cur = accepted;
       }
@@ -862,21 +863,24 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     __syncthreads();
   }
 
-  if (tid == 0 && lead) {
+  if (tid == 0) {
     const int st = sh.st < 0 ? 0 : sh.st;
-    if (st == 0) {
-      P.out_tokens[rb + sh.len] = sh.y;
-      P.out_len[b] = sh.len + 1;
-    } else {
-      P.out_len[b] = 0;
-    }
-    if (P.status) P.status[b] = st;
+    if (st == 0) sh.otok[sh.len] = sh.y;
+    sh.st = st;
   }
   __syncthreads();
-  if (sh.st > 0 && lead) {
+  if (lead) {
+    // the outputs, once the previous call on the stream has completed
+    grid_dependency_wait();
+    const int st = sh.st;
     for (int j = tid; j < M; j += kTreeThreads) {
-      P.out_tokens[rb + j] = -1;
-      P.out_nodes[rb + j] = -1;
+      P.out_tokens[rb + j] = st > 0 ? -1 : sh.otok[j];
+      P.out_nodes[rb + j] = st > 0 ? -1 : sh.onode[j];
+      if (P.alpha) P.alpha[rb + j] = sh.oal[j];
+    }
+    if (tid == 0) {
+      P.out_len[b] = st == 0 ? sh.len + 1 : 0;
+      if (P.status) P.status[b] = st;
     }
   }
   cluster_sync();                     // no CTA leaves while a peer may still read its slots
@@ -976,18 +980,22 @@ extern "C" sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtyp
   }
   if (di.fits[which][0] <= 0) return SV_ERR_UNSUPPORTED;
   p.cs = cs;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: back-to-back calls overlap (each writes
+  // its outputs after its dependency wait)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(B) * static_cast<unsigned>(cs), 1, 1);
   cfg.blockDim = dim3(sv::kTreeThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(ring);
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   sv::NvtxRange range("spec_verify_tree");
   return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -183,6 +183,34 @@ def test_root_only_and_repeated_calls():
             np.testing.assert_array_equal(x, y)
 
 
+def test_back_to_back_calls_into_the_same_outputs():
+    """Calls enqueued back to back on one stream with no host wait between
+    them, into the same output buffers (each call's walk may start while the
+    previous one runs; its outputs are written after the previous call is
+    complete): the last call's outputs are the oracle's."""
+    ws = [get_tree_workload("tree", B=24, V=20000, dtype="bf16", seed=31),
+          get_tree_workload("tree", B=24, V=20000, dtype="bf16", seed=32, draft_sigma=3.0),
+          get_tree_workload("tree", B=24, V=20000, dtype="bf16", seed=33, T=0.0)]
+    inps = [make_tree_inputs(w, device=DEV) for w in ws]
+    B, M = 24, inps[0]["target"].shape[1]
+    assert all(i["target"].shape[1] == M for i in inps)
+    stream = torch.cuda.Stream()
+    ot = torch.empty(B, M, dtype=torch.int32, device=DEV)
+    on = torch.empty(B, M, dtype=torch.int32, device=DEV)
+    ol = torch.empty(B, dtype=torch.int32, device=DEV)
+    st = torch.empty(B, dtype=torch.int32, device=DEV)
+    al = torch.empty(B, M, dtype=torch.float32, device=DEV)
+    for rep in range(4):
+        for inp in inps:
+            svp.verify_tree(inp["target"], inp["draft"], inp["parents"], inp["tokens"], inp["n_nodes"],
+                            inp["uniforms"], inp["T"], out_tokens=ot, out_nodes=on, out_len=ol, status=st, alpha=al,
+                            stream=stream)
+    stream.synchronize()
+    last = inps[-1]
+    compare((ot.cpu().numpy(), on.cpu().numpy(), ol.cpu().numpy(), st.cpu().numpy(), al.cpu().numpy()),
+            run_ref(last), last["T"])
+
+
 def test_graph_capture():
     w = get_tree_workload("tree", B=16, V=8192, dtype="bf16")
     inp = make_tree_inputs(w, device=DEV)
