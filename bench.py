@@ -83,6 +83,8 @@ def parse():
     ap.add_argument("--tree-workloads", default="tree,tree_wide", help="tree workloads timed in the aux block")
     ap.add_argument("--ctrl-steps", type=int, default=200,
                     help="timed rounds of the draft-length controller (0 = skip)")
+    ap.add_argument("--ex2-iters", type=int, default=4096,
+                    help="iterations of the exponential-rate measurement (0 = skip)")
     ap.add_argument("--profile-kernels", default="",
                     help="run each named kernel's representative case twice (for ncu, one kernel per "
                          "capture): comma list of verify (the default schedule), verify_cluster, verify_dense, early_exit, "
@@ -532,6 +534,21 @@ def time_controller(svp, w, device, stream, steps):
     return out
 
 
+def time_ex2(svp, iters, hbm_peak_gbs):
+    """The special-function unit's exponential rate (sv_measure_ex2) and the
+    streaming ceiling it sets.  The statistics pass takes one exponential per
+    streamed logit and the re-read of a rejected pair two per logit pair, so
+    both move 2 bytes (bf16) or 4 bytes (fp32) per exponential."""
+    import torch
+    clk, per_s = svp.measure_ex2(iters)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return {"per_sm_per_clock": clk, "per_second": per_s, "sms": sms, "iters": iters,
+            "implied_sm_mhz": per_s / (clk * sms) / 1e6,
+            "ceiling_bf16_gbs": 2.0 * per_s / 1e9, "ceiling_fp32_gbs": 4.0 * per_s / 1e9,
+            "ceiling_bf16_over_hbm_peak": 2.0 * per_s / 1e9 / hbm_peak_gbs,
+            "note": "one 1024-thread block per SM, 8 independent ex2.approx chains per thread"}
+
+
 def time_kd(svp, device, stream, steps, warmup, n_seq=64, t_len=64, V=151936):
     """Device-timed calls of the reward-weighted distillation loss on a batch
     of rollouts (bf16, Qwen vocabulary): with the gradient and loss alone.
@@ -715,6 +732,8 @@ def our_arm(args, w):
         aux["draft_controller"] = time_controller(svp, w, device, stream, args.ctrl_steps)
     if args.kd_steps > 0 and world == 1:
         aux["kd_loss"] = time_kd(svp, device, stream, args.kd_steps, max(3, args.warmup // 10), n_seq=args.kd_rollouts)
+    if args.ex2_iters > 0 and world == 1:
+        aux["ex2_rate"] = time_ex2(svp, args.ex2_iters, peak)
 
     if rank != 0:
         if pg:

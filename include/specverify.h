@@ -313,6 +313,19 @@ sv_status spec_kd_launch_shape(int V, sv_dtype dtype, int with_grad, int *cluste
  * default. */
 sv_status sv_set_wait_limit_ns(sv_ctx *ctx, long long ns);
 
+/* Measurement utility (no page defines it; no verify call uses it): the
+ * throughput of the special-function unit's base-2 exponential on the current
+ * device, the second bound of the verify path after HBM bandwidth (the
+ * statistics pass takes one ex2.approx per streamed logit, the re-read of a
+ * rejected pair two per logit pair).  One 1024-thread block per SM iterates
+ * `iters` times (1 <= iters <= 2^24) over 8 independent exponentials per
+ * thread.  Writes the exponentials per SM per SM clock (the median block,
+ * from its cycle counter) and per second (the whole grid, from CUDA events),
+ * either pointer may be NULL but not both.  Synchronous: it allocates and
+ * frees its own scratch and runs on the legacy default stream.  Returns
+ * SV_ERR_CUDA if a CUDA call fails. */
+sv_status sv_measure_ex2(int iters, double *per_sm_per_clock, double *per_second);
+
 /*
  * spec_verify without a context, for callers that may not allocate device
  * memory (the pages describe no such entry point; it is a property of this

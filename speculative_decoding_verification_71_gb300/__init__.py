@@ -25,6 +25,7 @@ __all__ = [
     "SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_BAD_DRAFT_LEN", "SV_ERR_BAD_TOKEN",
     "SV_ERR_NONFINITE", "SV_ERR_TIMEOUT", "SV_ERR_CUDA", "SV_ERR_UNSUPPORTED",
     "SV_F32", "SV_BF16", "EXPORTED_SYMBOLS", "DraftController", "verify_tree", "SV_CTRL_BATCH", "SV_CTRL_PER_SEQUENCE",
+    "measure_ex2",
 ]
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_BAD_DRAFT_LEN, SV_ERR_BAD_TOKEN = 0, 1, 2, 3
@@ -42,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "sv_status_string", "sv_last_cuda_error", "sv_create", "sv_destroy", "spec_verify",
     "spec_verify_compact", "spec_verify_debug", "spec_verify_stats", "spec_verify_reset_stats",
     "sv_set_pipeline", "sv_set_cluster", "sv_set_early_exit", "sv_set_diagnostics", "sv_get_config", "sv_launch_shape",
-    "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for", "sv_rows_shape", "sv_set_timeline",
+    "sv_set_wait_limit_ns", "sv_set_kernel", "sv_kernel_for", "sv_rows_shape", "sv_set_timeline", "sv_measure_ex2",
     "spec_verify_noalloc", "spec_kd_loss", "spec_kd_launch_shape",
     "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_set_cost", "spec_ctrl_set_params", "spec_ctrl_reset",
     "spec_ctrl_observe", "spec_ctrl_choose", "spec_ctrl_alpha", "spec_ctrl_status",
@@ -132,6 +133,8 @@ def load_library(path: str | None = None):
     lib.sv_rows_shape.argtypes = [P, c.POINTER(c.c_int), c.POINTER(c.c_int), c.POINTER(c.c_int)]
     lib.sv_set_wait_limit_ns.restype = c.c_int
     lib.sv_set_wait_limit_ns.argtypes = [P, c.c_longlong]
+    lib.sv_measure_ex2.restype = c.c_int
+    lib.sv_measure_ex2.argtypes = [c.c_int, c.POINTER(c.c_double), c.POINTER(c.c_double)]
     lib.spec_ctrl_create.restype = c.c_int
     lib.spec_ctrl_create.argtypes = [c.POINTER(P), c.c_int, c.c_int]
     lib.spec_ctrl_destroy.restype = c.c_int
@@ -455,6 +458,17 @@ def kd_loss(target, draft, weights, temperature=1.0, grad=True, stream=None):
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_kd_loss")
     return row_kl, loss, g
+
+
+def measure_ex2(iters=4096):
+    """(ex2 per SM per clock, ex2 per second) of the special-function unit on
+    the current device (sv_measure_ex2)."""
+    lib = load_library()
+    per_clk, per_s = ctypes.c_double(), ctypes.c_double()
+    st = lib.sv_measure_ex2(int(iters), ctypes.byref(per_clk), ctypes.byref(per_s))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "sv_measure_ex2")
+    return per_clk.value, per_s.value
 
 
 def kd_launch_shape(V, dtype=torch.bfloat16, grad=True):

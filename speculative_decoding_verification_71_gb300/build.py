@@ -16,7 +16,8 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libspecverify.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["sv_kernels.cu", "sv_pieces.cu", "sv_api.cu", "sv_noalloc.cu", "sv_kd.cu", "sv_ctrl.cu", "sv_tree.cu"]
+SOURCES = ["sv_kernels.cu", "sv_pieces.cu", "sv_api.cu", "sv_noalloc.cu", "sv_kd.cu", "sv_ctrl.cu", "sv_tree.cu",
+           "sv_micro.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "-I", INCLUDE]
 

@@ -54,6 +54,9 @@ def test_null_context_is_rejected_on_the_host(lib):
     assert lib.sv_set_cluster(P, 2) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_launch_shape(P, 4, None, None) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_rows_shape(P, None, None, None) == svp.SV_ERR_INVALID_ARG
+    d = ctypes.c_double()
+    assert lib.sv_measure_ex2(0, ctypes.byref(d), None) == svp.SV_ERR_INVALID_ARG
+    assert lib.sv_measure_ex2(16, None, None) == svp.SV_ERR_INVALID_ARG
     assert lib.sv_set_early_exit(P, 1) == svp.SV_ERR_INVALID_ARG
     # the distillation loss checks its sizes, temperature and pointers on the host
     assert lib.spec_kd_loss(0, 1, 10, 1, P, P, P, 1.0, P, P, P, P) == svp.SV_ERR_INVALID_ARG
