@@ -222,11 +222,13 @@ sv_status sv_launch_shape(const sv_ctx *ctx, int B, int *cluster, int *grid_ctas
  *                      between CTAs); then one warp per sequence takes the
  *                      tests and the bonus draw, the rejected pairs are read
  *                      again (spread over the SMs the same way), and one warp
- *                      per rejected pair draws.  Four launches per call.  It
+ *                      per rejected pair draws.  Four launches per call, per
+ *                      2048 sequences (a larger batch runs as consecutive
+ *                      calls of at most 2048 sequences on the stream).  It
  *                      needs 16-byte aligned rows (V * sizeof(dtype) a
  *                      multiple of 16, aligned bases), rows of at most 1 MiB,
- *                      B <= 2048, early exit off and no fixed cluster size;
- *                      a call that does not qualify runs the cluster kernel.
+ *                      early exit off and no fixed cluster size; a call that
+ *                      does not qualify runs the cluster kernel.
  *   SV_KERNEL_AUTO     (default) row streaming where it qualifies, the
  *                      faster of the two on every measured workload; else
  *                      the cluster kernel.

@@ -6,6 +6,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -100,12 +101,13 @@ sv_status configure_auto(sv_ctx* ctx) {
   return configure(ctx, 2, 0);
 }
 
-// Whether a call with batch B (rows 16-byte aligned) runs row streaming (the
-// default where it qualifies, the faster schedule on every measured workload).
-bool use_pieces(const sv_ctx* ctx, int B) {
+// Whether a call (rows 16-byte aligned) runs row streaming: the default
+// where it qualifies, the faster schedule on every measured workload.
+// Batches above kPiecesMaxB sequences run as consecutive row-streaming calls
+// of at most kPiecesMaxB sequences each.
+bool use_pieces(const sv_ctx* ctx) {
   if (ctx->kernel == SV_KERNEL_CLUSTER || !ctx->pw_mem || ctx->pieces_ctas <= 0) return false;
-  if (ctx->early_exit || ctx->cluster != 0) return false;
-  return B <= sv::kPiecesMaxB;
+  return !ctx->early_exit && ctx->cluster == 0;
 }
 
 // The row-streaming schedule's workspace for (max_B, max_k) and rows of V
@@ -119,7 +121,7 @@ sv_status create_pieces(sv_ctx* ctx) {
   if (ctx->np > sv::kMaxChunks) return SV_OK;   // rows of at most 1 MiB, as for the cluster kernel
   e = sv::prepare_pieces_kernel();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaFuncSetAttribute(pieces)");
-  // batches above kPiecesMaxB run the cluster kernel
+  // sized for one call of at most kPiecesMaxB sequences (larger batches run in chunks of that size)
   const size_t B = static_cast<size_t>(ctx->max_B < sv::kPiecesMaxB ? ctx->max_B : sv::kPiecesMaxB);
   const size_t k = static_cast<size_t>(ctx->max_k);
   const size_t rows = B * (2 * k + 1);
@@ -319,7 +321,7 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   int ctas = 0;
   launch_shape(ctx, B, &p.cluster, &ctas);
   p.ctas = ctas;
-  if (p.bulk && use_pieces(ctx, B)) {
+  if (p.bulk && use_pieces(ctx)) {
     p.pieces = 1;
     p.np = ctx->np; p.nr = ctx->nr;
     p.ctas = ctx->pieces_ctas;
@@ -327,7 +329,35 @@ sv_status spec_verify(sv_ctx* ctx, int B, int k, const void* target_logits, cons
   }
   // the timeline covers the cluster kernel's grid (and the work-list kernel)
   if (!p.pieces && ctx->timeline && (ctas + 1) * sv::kTimelineSlots <= ctx->timeline_cap) p.timeline = ctx->timeline;
-  cudaError_t e = sv::launch_verify(p, ctas, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaSuccess;
+  if (!p.pieces || B <= sv::kPiecesMaxB) {
+    e = sv::launch_verify(p, ctas, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
+  } else {
+    // row streaming, kPiecesMaxB sequences at a time: every per-sequence
+    // array (inputs, outputs, diagnostics) offset to the chunk's first
+    // sequence; the chunks are consecutive calls on the stream
+    const size_t rb = static_cast<size_t>(ctx->V) * ctx->elt;
+    const size_t k1 = static_cast<size_t>(k) + 1, kk = static_cast<size_t>(k);
+    for (int b0 = 0; b0 < B && e == cudaSuccess; b0 += sv::kPiecesMaxB) {
+      const size_t o = static_cast<size_t>(b0);
+      sv::VerifyParams q = p;
+      q.B = std::min(sv::kPiecesMaxB, B - b0);
+      q.target = static_cast<const char*>(p.target) + o * k1 * rb;
+      q.draft = p.draft ? static_cast<const char*>(p.draft) + o * kk * rb : nullptr;
+      q.tokens = p.tokens ? p.tokens + o * kk : nullptr;
+      q.draft_len = p.draft_len + o;
+      q.uniforms = p.uniforms ? p.uniforms + o * k1 : nullptr;
+      q.out_tokens = p.out_tokens + o * k1;
+      q.out_len = p.out_len + o;
+      q.ws.m_t = p.ws.m_t + o * k1;
+      q.ws.L_t = p.ws.L_t + o * k1;
+      q.ws.mass = p.ws.mass + o * k1;
+      q.ws.m_d = p.ws.m_d + o * kk;
+      q.ws.L_d = p.ws.L_d + o * kk;
+      q.ws.alpha = p.ws.alpha + o * kk;
+      e = sv::launch_verify(q, ctas, ctx->smem_bytes, reinterpret_cast<cudaStream_t>(stream));
+    }
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "launch verify");
   ctx->calls += 1;
   ctx->last_B = B;
@@ -473,7 +503,7 @@ sv_status sv_set_kernel(sv_ctx* ctx, int kernel) {
 
 sv_status sv_kernel_for(const sv_ctx* ctx, int B, int* kernel) {
   if (!ctx || B < 1 || B > ctx->max_B || !kernel) return SV_ERR_INVALID_ARG;
-  *kernel = use_pieces(ctx, B) ? SV_KERNEL_PIECES : SV_KERNEL_CLUSTER;
+  *kernel = use_pieces(ctx) ? SV_KERNEL_PIECES : SV_KERNEL_CLUSTER;
   return SV_OK;
 }
 

@@ -87,9 +87,9 @@ def test_small_cases(name, over, kernel):
 
 
 def test_kernel_choice():
-    """Row streaming is the default where it qualifies (aligned rows, up to
-    2048 sequences, no cluster size, no early exit); the cluster kernel runs
-    everything else, and either can be asked for."""
+    """Row streaming is the default where it qualifies (aligned rows, no
+    cluster size, no early exit; batches above 2048 sequences in chunks); the
+    cluster kernel runs everything else, and either can be asked for."""
     inp = small("ragged", B=8, k=3, V=4096)
     ver = verifier_for(inp)
     assert ver.kernel_for(8) == svp.SV_KERNEL_PIECES        # the default
@@ -109,7 +109,30 @@ def test_kernel_choice():
     with pytest.raises(svp.SpecVerifyError):
         ver.set_kernel(3)
     big = svp.SpecVerifier(5000, 1, 64, torch.float32)
-    assert big.kernel_for(2048) == svp.SV_KERNEL_PIECES and big.kernel_for(2049) == svp.SV_KERNEL_CLUSTER
+    assert big.kernel_for(2048) == svp.SV_KERNEL_PIECES and big.kernel_for(5000) == svp.SV_KERNEL_PIECES
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_batches_above_2048_run_in_row_streaming_chunks(T):
+    """A batch above 2048 sequences runs row streaming as consecutive calls of
+    at most 2048 sequences (here 2048, 2048 and 404): every sequence against
+    the oracle, and every diagnostic equal to that of the same sequences
+    verified as a call of their own (each chunk's arrays at its offset)."""
+    inp = small("ragged", B=4500, k=3, V=2048, T=T, seed=41)
+    ver = verifier_for(inp)
+    assert ver.kernel_for(4500) == svp.SV_KERNEL_PIECES
+    toks, lens, _, _ = assert_parity(inp, ver, check_diag=False)
+    whole = {n: v.cpu().numpy() for n, v in ver.debug(4500, 3).items()}
+    for b0 in range(0, 4500, 2048):
+        sl = slice(b0, min(4500, b0 + 2048))
+        part = {n: (v[sl].contiguous() if isinstance(v, torch.Tensor) and v.dim() > 0 else v) for n, v in inp.items()}
+        part["meta"] = dict(inp["meta"], B=sl.stop - sl.start)
+        one = verifier_for(part)
+        t1, l1 = run_gpu(one, part)
+        np.testing.assert_array_equal(t1, toks[sl])
+        np.testing.assert_array_equal(l1, lens[sl])
+        for n, v in one.debug(sl.stop - sl.start, 3).items():
+            np.testing.assert_array_equal(v.cpu().numpy(), whole[n][sl], err_msg=n)
 
 
 def test_timeline_is_consistent():

@@ -36,6 +36,7 @@ def test_noalloc_matches_context_entry_point_twice():
     for w in cases:   # two calls in a row on the shared array
         inp = make_inputs(w, device="cuda")
         ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+        ver.set_kernel(svp.SV_KERNEL_CLUSTER)   # the schedule this entry point runs: equal to the bit
         ref_t, ref_l = ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"],
                                   inp["uniforms"], inp["T"])
         out_t = torch.full_like(ref_t, 7)
@@ -62,6 +63,7 @@ def test_noalloc_greedy_fp32_and_full_capacity():
         w = get_workload(name, **over)
         inp = make_inputs(w, device="cuda")
         ver = svp.SpecVerifier(w.B, w.k, w.V, w.torch_dtype)
+        ver.set_kernel(svp.SV_KERNEL_CLUSTER)   # the schedule this entry point runs: equal to the bit
         ref_t, ref_l = ver.verify(inp["target"], inp["draft"], inp["tokens"], inp["draft_len"],
                                   inp["uniforms"], inp["T"])
         ref = oracle.verify(inp["target"].cpu(), inp["draft"].cpu(), inp["tokens"].cpu(), inp["draft_len"].cpu(),
