@@ -123,7 +123,7 @@ cudaError_t launch_init_workspace(const Workspace& ws, cudaStream_t s);
 int verify_smem_bytes(int stages);
 
 // The row-streaming schedule (sv_pieces.cu).
-constexpr int kPiecesMaxB = 2048;                         // sequences per call (larger batches: consecutive calls)
+constexpr int kPiecesMaxB = 2048;                         // sequences per call
 int pieces_smem_bytes();
 int pieces_threads();                                       // threads of the streaming kernels
 cudaError_t prepare_pieces_kernel();
