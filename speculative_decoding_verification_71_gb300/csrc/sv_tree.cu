@@ -22,9 +22,11 @@
 // every CTA takes the same decisions.  cs is the largest of 8, 4, 2, 1 that
 // keeps one CTA per SM for the whole batch.  Within a CTA a producer warp
 // streams the slice of the rows a pass needs (the node's target row and, with
-// children, its draft row) through three 64 KB shared-memory slots with
-// cp.async.bulk, 32 KB of each row per slot, and 16 consumer warps reduce
-// each slot, two logits per f32x2 instruction.  Each visited node costs one
+// children, its draft row) through three 32 KB shared-memory slots with
+// cp.async.bulk, 16 KB of each row per slot, and 8 consumer warps reduce
+// each slot, two logits per f32x2 instruction.  Two such CTAs fit on an SM
+// (about 103 KB of shared memory and at most 112 registers a thread), so the
+// walks of back-to-back calls share the SMs.  Each visited node costs one
 // pass for the row maximum and log-sum of 2^(z c) of both rows, one more pass
 // per rejected child (the residual mass, with the sum of each warp's
 // 128-vector segment kept for the draw) and one pass for a bonus draw; the
@@ -43,11 +45,11 @@
 namespace sv {
 namespace {
 
-constexpr int kTreeWarps = 16;                          // consumer warps
+constexpr int kTreeWarps = 8;                           // consumer warps
 constexpr int kTreeThreads = (kTreeWarps + 1) * 32;     // + the producer warp
 constexpr int kTreeProducer = kTreeWarps;               // its warp index
-constexpr int kTreeStages = 3;                          // 64 KB staging slots
-constexpr int kTreeHalf = 32 * 1024;                    // bytes of one row per slot
+constexpr int kTreeStages = 3;                          // 32 KB staging slots
+constexpr int kTreeHalf = 16 * 1024;                    // bytes of one row per slot
 constexpr int kTreeVecsPerWarp = kTreeHalf / 16 / kTreeWarps;   // 128: one segment
 constexpr int kTreeVecsPerLane = kTreeVecsPerWarp / 32;         // 4
 constexpr int kChunkElems = 256;                        // slice boundaries: whole 256-logit chunks
@@ -550,7 +552,7 @@ __device__ int draw(TreeShared& sh, const Slice<ELT>& sl, const TreeParams& P, c
 }
 
 template <int ELT, bool GREEDY>
-__global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams P) {
+__global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams P) {
   __shared__ TreeShared sh;
   extern __shared__ __align__(128) unsigned char ring[];   // kTreeRingBytes
   using VV = Vec<ELT>;
@@ -969,7 +971,8 @@ extern "C" sv_status spec_verify_tree(int B, int max_nodes, int V, sv_dtype dtyp
   }
   // CTAs per sequence: the largest cluster (up to 8) that keeps one CTA per
   // SM for the whole batch; a sequence's walk is serial, so idle SMs are
-  // better spent on slices of its rows
+  // better spent on slices of its rows.  Two CTAs of this shape fit on an
+  // SM, so the next call's walks share every SM with this call's
   int cs = 1;
   for (int l = 3; l >= 1; --l) {
     const int c = 1 << l;
