@@ -95,6 +95,7 @@ CASES = [
     ("tree", dict(B=8, V=65536, dtype="f32", draft_sigma=3.0)),  # a poor drafter: many rejections
     ("tree_wide", dict(B=24, V=5000, dtype="f32", T=0.0)),      # greedy
     ("tree", dict(B=16, V=3000, dtype="bf16", T=0.0, draft_sigma=0.1)),
+    ("tree_wide", dict(B=400, V=4096, dtype="bf16")),           # more CTAs than fit at once: in waves
 ]
 
 
