@@ -93,7 +93,7 @@ __device__ __forceinline__ uint4 load_vec(const unsigned char* row, int e0, int 
 // words, read by a peer with three vector loads).
 struct __align__(16) XSlot {
   float Kt, St, Kd, Sd;     // row statistics of its slice (greedy: Kt = best logit, St = draft maximum)
-  int bad, idx, y, pad;     // a bad logit seen; greedy argmax; the drawn token
+  int bad, idx, y, failed;  // a bad logit seen; greedy argmax; the drawn token; a bounded wait gave up
   double total, pad2;       // its slice's weight
 };
 
@@ -107,6 +107,7 @@ struct TreeShared {
   int nkids, n, cur, len, st, next, y, owner;
   int pass_both;                     // the pass streams the draft row too
   int failed;                        // a bounded wait of the streaming gave up
+  int lastq[kTreeStages];            // producer: the last slot count copied into each stage (-1: none)
   float csum[kTreeMaxSegs];          // segment sums of the last weight pass (this CTA's segments)
   double cc, PP, invPP;              // residual after the rejections so far: max(0, p - cc q) / PP
   double l2ratio;                    // log2(S^t / S^d) of the current node
@@ -140,8 +141,12 @@ __device__ __forceinline__ uint4 ld_peer_v4(uint32_t a) {
 // sh.got[r] (three 16-byte loads), so that thread 0 then merges them in rank
 // order from local shared memory.  The slots are double-buffered: a CTA
 // writes a slot again only after the next barrier, which every peer reaches
-// only after reading it.
+// only after reading it.  Each slot also carries whether a bounded wait of
+// its CTA gave up, and every CTA takes the OR: the walk ends at the same
+// step in all of them (a CTA that stopped alone would leave its peers at a
+// cluster barrier that it never reaches).
 __device__ __forceinline__ void exchange(TreeShared& sh, int& xp, int cs) {
+  if (threadIdx.x == 0) sh.xs[xp].failed = *reinterpret_cast<volatile int*>(&sh.failed);
   cluster_sync();
   const int t = threadIdx.x;
   if (t < cs) {
@@ -152,6 +157,11 @@ __device__ __forceinline__ void exchange(TreeShared& sh, int& xp, int cs) {
     dst[2] = ld_peer_v4(a + 32);
   }
   __syncthreads();
+  if (t == 0) {
+    int f = 0;
+    for (int r = 0; r < cs; ++r) f |= sh.got[r].failed;
+    if (f) *reinterpret_cast<volatile int*>(&sh.failed) = 1;
+  }
   xp ^= 1;
 }
 
@@ -245,7 +255,9 @@ __device__ __forceinline__ double seg_total(const TreeShared& sh, int nseg, int 
 // warp and the consumer warps run the same passes in the same order and count
 // the slots alike (q), so the slots' mbarrier phases match.  Every wait is
 // bounded; one that gives up sets sh.failed, after which no wait is made and
-// the walk ends with SV_ERR_TIMEOUT.
+// the walk ends with SV_ERR_TIMEOUT, in every CTA of the cluster at the same
+// step (the flag travels with each exchange); the producer drains its copies
+// before the CTA leaves.
 template <int ELT>
 struct Slice {
   using VV = Vec<ELT>;
@@ -299,6 +311,7 @@ struct Slice {
           mbar_expect_tx(&sh.full[s], static_cast<uint32_t>((both ? 2 : 1) * nb));
           bulk_load(dst, rt + off, static_cast<uint32_t>(nb), &sh.full[s]);
           if (both) bulk_load(dst + kTreeHalf, rd + off, static_cast<uint32_t>(nb), &sh.full[s]);
+          sh.lastq[s] = q;
         }
       } else {
         // rows not 16-byte aligned: element loads, the last vector padded with -inf
@@ -341,6 +354,18 @@ struct Slice {
       if (lane == 0) mbar_arrive(&sh.empty[s]);
       f(k, tv, dv);
     }
+  }
+
+  // Producer warp, before the CTA leaves: every copy it issued has landed
+  // (bounded).  On the normal path the consumers waited for each already;
+  // after a wait gave up, copies still in flight must not reach shared
+  // memory that a later CTA owns.
+  __device__ void drain() {
+    if ((threadIdx.x & 31) != 0) return;
+#pragma unroll
+    for (int s = 0; s < kTreeStages; ++s)
+      if (sh.lastq[s] >= 0)
+        mbar_wait_bounded(&sh.full[s], static_cast<uint32_t>(sh.lastq[s] / kTreeStages) & 1u, kDrainLimitNs);
   }
 
   // One pass: the producer warp streams, the consumer warps reduce.
@@ -579,6 +604,7 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
     }
     fence_mbar_init();
     sh.failed = 0;
+    for (int s = 0; s < kTreeStages; ++s) sh.lastq[s] = -1;
   }
   // the next kernel on the stream may start (a next call's walk reads only
   // its inputs until it writes its outputs, after its dependency wait)
@@ -885,6 +911,7 @@ __global__ void __launch_bounds__(kTreeThreads, 2) tree_kernel(const TreeParams 
       if (P.status) P.status[b] = st;
     }
   }
+  if (warp == kTreeProducer) sl.drain();
   cluster_sync();                     // no CTA leaves while a peer may still read its slots
 }
 
